@@ -1,0 +1,106 @@
+"""Seeded synthetic inputs for the scan: the one module both the CUDA path's
+callers (tests, benchmark) and the oracle's tests draw their inputs from.
+
+It holds none of the method's arithmetic: it only draws random numbers and
+rounds them to the storage types.
+
+Recipe (workloads shaped like the backbone stages of "VisionHOPE: Visual
+Backbones as Self-Modifying Learning Systems", App. C.1 chunk lengths
+(56, 28, 14), and a dense-prediction map; synthetic stand-ins for
+ImageNet-1K / COCO / ADE20K feature maps, which are not used):
+  x         ~ N(0, 1) drawn in fp64 with numpy default_rng(seed), rounded to
+              fp32 (round-to-nearest-even), then to bf16 (RNE) for bf16 maps.
+  memories0 ~ N(0, 1/d) for all six memories of every (route, head), fp32.
+              With x ~ N(0,1) this makes the eta/alpha logits m.x ~ N(0, 1).
+  eta_bias  +1 on the high-resolution map (eta logits ~ N(1, 1)).
+The "long-memory" variant of a workload only changes alpha_init to 0.999 so
+that the state survives all chunks of a route (with 0.9 and chunks of 56
+tokens the memories shrink by about 0.9^56 per chunk once the keys fall
+below the normalisation stabiliser).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, replace
+
+import numpy as np
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    H: int
+    W: int
+    nh: int
+    d: int
+    chunk: int = 0          # 0 = row/column aligned (Eq. (25))
+    dtype: str = "bf16"     # storage type of x
+    seed: int = 0
+    eta_bias: float = 0.0
+    alpha_init: float = 0.9
+    dirs: int = 15
+
+    @property
+    def Cc(self) -> int:
+        return self.nh * self.d
+
+    @property
+    def N(self) -> int:
+        return self.H * self.W
+
+    @property
+    def tokens(self) -> int:
+        return self.B * self.H * self.W
+
+    def long_memory(self) -> "Workload":
+        return replace(self, name=self.name + "-longmem", alpha_init=0.999)
+
+
+WORKLOADS = {
+    "tiny": Workload("tiny", 1, 8, 8, 1, 16, 0, "f32", 0),
+    "stage1": Workload("stage1", 32, 56, 56, 3, 32, 0, "bf16", 1),
+    "stage2": Workload("stage2", 32, 28, 28, 6, 32, 0, "bf16", 2),
+    "stage3": Workload("stage3", 128, 14, 14, 6, 64, 0, "bf16", 3),
+    "highres": Workload("highres", 4, 128, 160, 3, 32, 0, "bf16", 4, eta_bias=1.0),
+}
+
+
+def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
+    """Round fp32 values to bf16 (round-to-nearest-even); returns the uint16 bit patterns."""
+    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    lsb = (u >> 16) & 1
+    return ((u + 0x7FFF + lsb) >> 16).astype(np.uint16)
+
+
+def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    return (np.asarray(bits, dtype=np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+@dataclass
+class Inputs:
+    """x_store: the exact stored values (float32 array, or uint16 bf16 bits);
+    x64: the same values widened to fp64; mem0: fp32 [4][nh][4d^2+2d]."""
+    wl: Workload
+    x_store: np.ndarray
+    x64: np.ndarray
+    mem0: np.ndarray
+
+
+def make_inputs(wl: Workload, batch: int | None = None) -> Inputs:
+    """Draw the workload's inputs.  ``batch`` < wl.B draws only the first images
+    (same values as the full draw, since images are drawn in order)."""
+    rng = np.random.default_rng(wl.seed)
+    d = wl.d
+    mem0 = (rng.standard_normal((4, wl.nh, 4 * d * d + 2 * d)) / np.sqrt(d)).astype(np.float32)
+    B = wl.B if batch is None else batch
+    x = rng.standard_normal((B, wl.H, wl.W, wl.Cc)).astype(np.float32)
+    if wl.dtype == "bf16":
+        bits = f32_to_bf16_bits(x)
+        return Inputs(wl, bits, bf16_bits_to_f64(bits), mem0)
+    return Inputs(wl, x, x.astype(np.float64), mem0)
+
+
+def make_dir_scale(wl: Workload, seed: int = 1234) -> np.ndarray:
+    """Channel-wise route scales lambda_r ~ U(0.5, 1.5), fp32 [4][Cc]."""
+    rng = np.random.default_rng(seed)
+    return rng.uniform(0.5, 1.5, size=(4, wl.Cc)).astype(np.float32)
