@@ -1,0 +1,394 @@
+#!/usr/bin/env python3
+"""Benchmark of the four-direction VisionHOPE memory scan on GB300.
+
+One step = one pass of the whole scan (zero the output, then the scan
+kernel: generation, step control, readout with the fused four-route merge,
+shared-gain memory update) over one batch of synthetic feature maps already
+resident in HBM.  Default workload: the stage-1 map, B=32, 56x56, 96
+channels as 3 heads of d=32, row/column aligned chunks of 56, bf16 x.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 runs under torchrun, one process per GPU; images are independent, so
+every rank scans its own batch (weak scaling, no collective on the data
+path; one barrier and one max-reduction of the timings).  ``--impl
+reference`` times the fp64 CPU oracle on the host cores instead (rank 0
+only).  Rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "4-dir VisionHOPE scan tokens/s on 1 GB300 at 56×56×96; % of roofline"
+UNIT = "tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_SOURCES = ["visual_backbone_gb300/csrc/vh_scan_simt.cu",
+                  "visual_backbone_gb300/csrc/vh_scan_tc.cu",
+                  "visual_backbone_gb300/csrc/vh_common.cuh"]
+
+
+# ---------------------------------------------------------------- helpers
+
+def algorithmic_cost(wl, ndirs=4):
+    """Algorithmic flops and compulsory HBM bytes of one call.
+
+    Flops: 2 x (7d^2 + 20d + (4d^3 + 2d^2)/C_r) multiply-adds per (token,
+    route, head): the interaction count of "VisionHOPE", App. C.3 Eq. (56)
+    extended to six memories (generation of k, v, q; readout; the shared-gain
+    recurrence; O(d) scalars; the chunk-boundary update of four d x d and two
+    1 x d memories).  Bytes: x read once, out written once (fp32), memories0."""
+    d = wl.d
+    xb = 2 if wl.dtype == "bf16" else 4
+    flops = 0.0
+    for r in range(ndirs):
+        cr = wl.chunk if wl.chunk else (wl.W if r < 2 else wl.H)
+        macs = 7 * d * d + 20 * d + (4 * d ** 3 + 2 * d * d) / cr
+        flops += 2.0 * macs * wl.tokens * wl.nh
+    nbytes = wl.tokens * wl.Cc * (xb + 4) + 4 * wl.nh * (4 * d * d + 2 * d) * 4
+    return flops, float(nbytes)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return pk, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:12]
+
+
+def recorded_traffic(workload: str, impl: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel sources (profiles/traffic.txt: workload impl hash bytes)."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    cur = kernel_source_hash()
+    for line in open(path):
+        parts = line.split()
+        if len(parts) >= 4 and not line.startswith("#"):
+            if parts[0] == workload and parts[1] == impl and parts[2] == cur:
+                return float(parts[3])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms in the background."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index=None):
+        self.samples = []
+        self.proc = None
+        self.err = None
+        self.gpu_index = gpu_index
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+               "-lms", "200"]
+        if self.gpu_index is not None:
+            cmd += ["-i", str(self.gpu_index)]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError as e:
+            self.err = str(e)
+            return self
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            f = [s.strip() for s in line.split(",")]
+            if len(f) >= 9:
+                self.samples.append((time.time(), f))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        return self
+
+    def summary(self, t0, t1):
+        if self.err or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
+                    "note": self.err or "no nvidia-smi samples"}
+        inside = [f for (t, f) in self.samples if t0 <= t <= t1]
+        if len(inside) < 2:   # short timed region: take the samples nearest to it
+            near = sorted(self.samples, key=lambda s: min(abs(s[0] - t0), abs(s[0] - t1)))[:3]
+            inside = [f for _, f in near]
+        def num(s):
+            try:
+                return float(s)
+            except ValueError:
+                return None
+        sm = [num(f[1]) for f in inside if num(f[1]) is not None]
+        smax = [num(f[2]) for f in inside if num(f[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for f in inside for i in range(4) if f[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(inside)}
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+# --------------------------------------------------------- oracle timing
+
+def time_oracle(wl, images, nthreads):
+    import oracle
+    from visual_backbone_gb300 import synth
+    oracle.build()
+    inp = synth.make_inputs(wl, batch=images)
+    p = oracle.OracleParams(eta_bias=wl.eta_bias, alpha_init=wl.alpha_init)
+    t0 = time.perf_counter()
+    oracle.forward(inp.x64, inp.mem0, wl.H, wl.W, wl.nh, wl.d, chunk_len=wl.chunk, params=p,
+                   nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    return images * wl.N / dt, dt
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_reference(args, wl):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    images = args.ref_images
+    cores = min(cpu_cores(), images * wl.nh)
+    for _ in range(args.warmup):
+        time_oracle(wl, images, cores)
+    times = []
+    t_start = time.perf_counter()
+    for _ in range(args.steps):
+        _, dt = time_oracle(wl, images, cores)
+        times.append(dt)
+    total = sum(times)
+    value = args.steps * images * wl.N / total
+    sample = (f"{images} image(s) of the {wl.name} workload per step (all 4 routes x "
+              f"{wl.nh} heads, {images * wl.N} tokens), fp64 oracle, {cores} threads")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(wl, args),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "wall_s": time.perf_counter() - t_start,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(wl, args):
+    return {"workload": f"{wl.name}: B={wl.B} {wl.H}x{wl.W} map, Cc={wl.Cc} as {wl.nh} heads x "
+                        f"d={wl.d}, chunk={'row W / col H' if wl.chunk == 0 else wl.chunk}, "
+                        f"4 routes, {wl.dtype} x, fp32 state, alpha_init={wl.alpha_init}, "
+                        f"eta_bias={wl.eta_bias}",
+            "global_batch": wl.B * dist_env()[1], "tokens_per_step_per_gpu": wl.tokens,
+            "parallelism": f"dp{dist_env()[1]} (images split across GPUs, no collective)",
+            "l2": "256 MiB buffer written between timed steps (L2 is 129 MB)",
+            "kernel": args.kernel}
+
+
+# ------------------------------------------------------------ our arm
+
+def run_ours(args, wl):
+    import torch
+    import visual_backbone_gb300 as vh
+    from visual_backbone_gb300 import _build, synth
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0 and not os.path.exists(vh.LIB_PATH):
+        _build.build()
+    if world > 1:
+        torch.distributed.barrier()
+
+    inp = synth.make_inputs(wl)
+    if wl.dtype == "bf16":
+        x_host = torch.from_numpy(inp.x_store.view("int16")).view(torch.bfloat16)
+    else:
+        x_host = torch.from_numpy(inp.x_store)
+    x = x_host.to(dev)
+    mem0 = torch.from_numpy(inp.mem0).to(dev)
+    out = torch.empty((wl.B, wl.H, wl.W, wl.Cc), dtype=torch.float32, device=dev)
+    flush = torch.empty(64 << 20, dtype=torch.float32, device=dev)  # 256 MiB > L2
+    params = vh.ScanParams(eta_bias=wl.eta_bias, alpha_init=wl.alpha_init, impl=args.kernel)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(ev_start, ev_mid, ev_end):
+        flush.zero_()
+        ev_start.record(stream)
+        out.zero_()
+        ev_mid.record(stream)
+        vh.scan_forward(x, mem0, wl.d, chunk=wl.chunk, out=out, params=params, stream=stream,
+                        accumulate=True)
+        ev_end.record(stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            step(*evs)
+        torch.cuda.synchronize(dev)
+        events = [[torch.cuda.Event(enable_timing=True) for _ in range(3)]
+                  for _ in range(args.steps)]
+        sampler = ClockSampler(None).start() if rank == 0 else None
+        time.sleep(0.3 if sampler else 0.0)
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+        t0 = time.time()
+        for i in range(args.steps):
+            step(*events[i])
+        torch.cuda.synchronize(dev)
+        t1 = time.time()
+        if world > 1:
+            torch.distributed.barrier()
+        if sampler:
+            time.sleep(0.3)
+            sampler.stop()
+    step_ms = [e[0].elapsed_time(e[2]) for e in events]
+    kern_ms = [e[1].elapsed_time(e[2]) for e in events]
+    total_s = sum(step_ms) / 1e3
+    kern_avg_s = sum(kern_ms) / len(kern_ms) / 1e3
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([total_s, kern_avg_s], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_s, kern_avg_s = float(tt[0]), float(tt[1])
+    value = world * wl.tokens * args.steps / total_s
+
+    # end to end through the public API with host buffers (pinned), copies timed
+    x_pin = x_host.pin_memory()
+    out_pin = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+    e2e_steps = max(3, min(args.steps, 20))
+    with torch.cuda.stream(stream):
+        def e2e_step():
+            x.copy_(x_pin, non_blocking=True)
+            vh.scan_forward(x, mem0, wl.d, chunk=wl.chunk, out=out, params=params, stream=stream)
+            out_pin.copy_(out, non_blocking=True)
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ea.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        eb.record(stream)
+        torch.cuda.synchronize(dev)
+    e2e_s = ea.elapsed_time(eb) / 1e3
+    if world > 1:
+        tt = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        e2e_s = float(tt[0])
+    e2e_value = world * wl.tokens * e2e_steps / e2e_s
+
+    if rank == 0:
+        flops, nbytes = algorithmic_cost(wl)
+        peaks, src = load_peaks()
+        achieved = flops / kern_avg_s / 1e12
+        peak = float(peaks["bf16_tflops"])
+        traffic = recorded_traffic(wl.name, args.kernel)
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": traffic,
+                "peak_source": f"bf16 dense burst, {'of measured' if src == 'measured' else 'of fallback'}",
+                "flops_per_launch": flops, "kernel_ms": kern_avg_s * 1e3,
+                "hbm_compulsory_bytes": nbytes,
+                "hbm_achieved_gbs": nbytes / kern_avg_s / 1e9,
+                "hbm_frac_of_measured": nbytes / kern_avg_s / 1e9 / float(peaks["hbm_gbs"]),
+                "t_roof_ms": 1e3 * max(flops / (peak * 1e12), nbytes / (float(peaks["hbm_gbs"]) * 1e9))}
+        roof["frac_of_roofline_time"] = roof["t_roof_ms"] / (kern_avg_s * 1e3)
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32" if args.kernel == "simt" else "f32 (auto kernel)",
+            "data": "synthetic", "config": workload_config(wl, args),
+            "roofline": roof,
+            "e2e": {"value": e2e_value, "unit": UNIT,
+                    "h2d_bytes_per_step": int(x_host.numel() * x_host.element_size()),
+                    "d2h_bytes_per_step": int(out.numel() * 4), "steps": e2e_steps},
+            "gpu_launches": args.steps,
+            "clocks": sampler.summary(t0, t1) if sampler else None,
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            cores = min(cpu_cores(), args.cpu_images * wl.nh)
+            v, dt = time_oracle(wl, args.cpu_images, cores)
+            line["cpu_baseline"] = {
+                "value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                "sample": f"{args.cpu_images} of {wl.B} images of the workload (all 4 routes x "
+                          f"{wl.nh} heads), fp64, {dt:.1f} s wall"}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="stage1")
+    ap.add_argument("--variant", choices=["plain", "longmem"], default="plain")
+    ap.add_argument("--kernel", choices=["auto", "simt", "tc"], default="auto")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-images", type=int, default=16)
+    ap.add_argument("--ref-images", type=int, default=1)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    from visual_backbone_gb300 import synth
+    wl = synth.WORKLOADS[args.workload]
+    if args.variant == "longmem":
+        wl = wl.long_memory()
+    if args.gpus != dist_env()[1] and args.impl == "ours":
+        ap.error(f"--gpus {args.gpus} needs torchrun with {args.gpus} processes "
+                 f"(WORLD_SIZE={dist_env()[1]})")
+    if args.impl == "reference":
+        return run_reference(args, wl)
+    return run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

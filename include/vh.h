@@ -1,0 +1,175 @@
+/*
+ * vh.h -- C ABI of the GB300 VisionHOPE four-direction memory scan (libvh).
+ *
+ * The operation is the VisionHOPE operator F_VH of "VisionHOPE: Visual
+ * Backbones as Self-Modifying Learning Systems", Sec. 2.3 Eqs. (24)-(26):
+ * serialise a feature map along four routes, run one self-referential
+ * memory scan (SRNL, Sec. 2.1.2-2.1.3 Eqs. (9)-(16), stabilised by Def. 1
+ * Eqs. (19)-(21)) per route and head, restore the positions and sum the
+ * routes channel-wise.  The memory set is the six-memory form of "Nested
+ * Learning: The Illusion of Deep Learning Architectures", part 12,
+ * Eqs. (94)-(96): key, value, query and content memories (d x d) and the
+ * learning-rate and retention memories (1 x d).
+ *
+ * Conventions shared by every entry point:
+ *  - All tensor pointers are DEVICE pointers owned by the caller.  The
+ *    library allocates no device memory inside a call, keeps no state
+ *    between calls (apart from the thread-local error string and a cached
+ *    per-device attribute query) and never frees caller memory.
+ *  - Every call is asynchronous on params->stream (a cudaStream_t; NULL is
+ *    the legacy default stream).  Host-side argument errors are reported
+ *    before anything is enqueued.
+ *  - No C++ exception, abort or device trap crosses the ABI: every call
+ *    returns a vh_status; vh_last_error() gives a one-line reason.
+ *  - Layouts are row-major, NHWC for feature maps: x[B][H][W][Cc] with
+ *    Cc = n_heads * head_dim; head h owns channels [h*d, (h+1)*d).
+ *  - Route r: 0 = row-major forward (right), 1 = its full reversal (left),
+ *    2 = column-major forward (down: transpose, then flatten), 3 = its full
+ *    reversal (up).  The route visits pixel P_r(t) at step t:
+ *      P_0(t) = t, P_1(t) = N-1-t, P_2(t) = (t mod H)*W + t div H,
+ *      P_3(t) = P_2(N-1-t),  N = H*W.
+ */
+#ifndef VH_H_
+#define VH_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    VH_OK = 0,
+    VH_ERR_INVALID_ARG = -1,   /* bad pointer, shape, alignment, mask or parameter */
+    VH_ERR_UNSUPPORTED = -2,   /* valid but not built: head_dim not in {16,32,64}, dtype */
+    VH_ERR_CUDA = -3,          /* a CUDA runtime call or launch failed */
+    VH_ERR_WORKSPACE = -4,     /* reserved */
+    VH_ERR_NONFINITE = -5,     /* reserved for a checking helper */
+    VH_ERR_TIMEOUT = -6        /* reserved: no call here waits on another block */
+} vh_status;
+
+typedef enum { VH_DTYPE_F32 = 0, VH_DTYPE_BF16 = 1 } vh_dtype;
+
+enum { VH_DIR_RIGHT = 1, VH_DIR_LEFT = 2, VH_DIR_DOWN = 4, VH_DIR_UP = 8, VH_DIR_ALL = 15 };
+
+/* Step-control switches for ablations (VisionHOPE Sec. 3.5 "removing either
+ * control leaves the other unchanged"). */
+enum { VH_CTRL_NO_INJ_CAP = 1, VH_CTRL_NO_SPEC_CLAMP = 2 };
+
+/* Gate test hooks. */
+enum {
+    VH_GATE_GENERATED = 0,     /* eta, alpha from their memories, Eq. (15) and Eq. (53) */
+    VH_GATE_FORCED_RAW = 1,    /* raw eta = forced_eta, alpha = forced_alpha, then Def. 1 */
+    VH_GATE_FORCED_EXEC = 2    /* executed step = forced_eta, alpha = forced_alpha, no control */
+};
+
+/* Kernel selection. */
+enum {
+    VH_IMPL_AUTO = 0,          /* the fastest built kernel for the shape */
+    VH_IMPL_SIMT = 1,          /* fp32 CUDA-core kernel */
+    VH_IMPL_TC = 2             /* tensor-core (tcgen05) kernel */
+};
+
+/* Indices of the optional device counters (params->stats, 8 x uint64). */
+enum {
+    VH_STAT_TOKENS = 0,        /* token updates executed (sum over routes and heads) */
+    VH_STAT_SPEC_ACTIVE = 1,   /* spectral clamp strictly below the capped candidate */
+    VH_STAT_INJ_RATIO_GT1 = 2, /* raw step above the injection limit (eta/eta_inj > 1) */
+    VH_STAT_NONFINITE = 3,     /* non-finite readout values */
+    VH_STAT_COUNT = 8
+};
+
+typedef struct vh_params {
+    int batch;                 /* B >= 1 */
+    int channels;              /* Cc = n_heads * head_dim */
+    int head_dim;              /* d in {16, 32, 64} */
+    vh_dtype x_dtype;          /* element type of x: bf16 or f32 */
+    /* method constants ("VisionHOPE", App. C.1 and App. B.3) */
+    float gamma_eta;           /* raw-step scale, 0.025 */
+    float alpha_init;          /* initial retention in (0,1), 0.9 */
+    float eta_bias;            /* added to s^eta before softplus; 0 on the pages */
+    float eps;                 /* epsilon of Def. 1, 1e-6 */
+    float knorm_eps;           /* stabiliser of the key/query L2 norm, 1e-6 */
+    float inj_inward;          /* inward factor on eta_inj: limit * (1 - 1e-3) */
+    float spec_inward;         /* inward factor on eta_spec: limit * (1 - 1e-6) */
+    float kk_floor;            /* floor on ||k||^2 in eta_spec, 1e-20 */
+    const float *dir_scale;    /* device [4][Cc] channel-wise lambda_r of Eq. (26); NULL = 1 */
+    float *memories_out;       /* device [B][4][n_heads][4d^2+2d]: state after the last
+                                  token of each enabled route; NULL = not written; slots of
+                                  disabled routes are left untouched */
+    int gate_mode;             /* VH_GATE_* */
+    float forced_eta, forced_alpha;
+    unsigned control_flags;    /* VH_CTRL_* */
+    unsigned long long *stats; /* device [VH_STAT_COUNT] counters, accumulated (not cleared);
+                                  NULL = off */
+    int impl;                  /* VH_IMPL_* */
+    int accumulate;            /* 0: out is overwritten (the call zeroes it first);
+                                  1: the fused sum of Eq. (26) is added to out's contents */
+    void *stream;              /* cudaStream_t */
+} vh_params;
+
+/* Fill *p with the pages' constants (gamma_eta 0.025, alpha_init 0.9, eps
+ * and knorm_eps 1e-6, inward factors 1e-3 / 1e-6, kk_floor 1e-20), bf16 x,
+ * no optional outputs, default stream.  batch/channels/head_dim are zeroed
+ * and must be set by the caller. */
+void vh_params_init(vh_params *p);
+
+/*
+ * vh_scan_forward -- the VisionHOPE operator F_VH (Sec. 2.3, Eqs. (24)-(26)).
+ *
+ *   x          device, [B][H][W][Cc] of p->x_dtype, 16-byte aligned.
+ *   memories0  device fp32 [4][n_heads][4d^2+2d]: the learned initial state
+ *              of every (route, head), shared by all images (Sec. 2.3: "initialized
+ *              from learned values at the beginning of each image").  Block
+ *              order: M^k, M^v, M^q, M^m (d x d row-major, acting on column
+ *              vectors), m^eta, m^alpha (1 x d).
+ *   H, W       map size, H*W*Cc*B elements must fit in 2^31 per image row math.
+ *   dirs       nonzero mask of VH_DIR_* routes to run and sum.
+ *   chunk      0 = row/column aligned chunks (C_right = C_left = W,
+ *              C_down = C_up = H, Eq. (25)); > 0 = that fixed length on every
+ *              route, counted from each route's first token, last chunk partial.
+ *   out        device fp32 [B][H][W][Cc]: out = sum over enabled r of
+ *              lambda_r * P_r^{-1}(Y_r) (p->accumulate = 0), or out += that sum
+ *              (p->accumulate = 1).  Must not alias x.  The sum over routes
+ *              is taken with device atomics, so its fp32 rounding order is not
+ *              fixed from run to run.
+ *
+ * Per route and head, every chunk generates k, v, q, eta, alpha and the
+ * readout y_t = M^m_b q_t from its boundary state (Eqs. (15)-(16)), applies the
+ * step control of Def. 1 per token, and advances all six memories with
+ * M_t = M_{t-1} A_t + M_b B_t (App. B.4 Eq. (45)), computed through the shared
+ * gain M_end = M_b G (Prop. 2 Eq. (46)).
+ *
+ * Errors: VH_ERR_INVALID_ARG (null/misaligned pointers, sizes < 1, dirs == 0,
+ * chunk < 0, Cc != n_heads*d, alias), VH_ERR_UNSUPPORTED (head_dim or dtype),
+ * VH_ERR_CUDA (launch failure; the stream may then hold partial results).
+ */
+vh_status vh_scan_forward(const void *x, const float *memories0, const vh_params *p,
+                          int H, int W, unsigned dirs, int chunk, float *out);
+
+/*
+ * vh_debug_permute -- Z_r = P_r(Z) of Eq. (24) for one route, computed with
+ * the same device index code the scan uses.  x as in vh_scan_forward; seq
+ * device [B][N][Cc] of the same dtype, seq[b][t][:] = x[b][P_r(t)][:].
+ * Exists so the index maps can be checked bit for bit.
+ */
+vh_status vh_debug_permute(const void *x, const vh_params *p, int H, int W, int route,
+                           void *seq);
+
+/* Bytes of device workspace a vh_scan_forward call needs: always 0. */
+size_t vh_workspace_size(const vh_params *p, int H, int W, unsigned dirs, int chunk);
+
+/* Static string for a status code. */
+const char *vh_status_string(vh_status s);
+
+/* Thread-local description of the last failure on this thread ("" if none). */
+const char *vh_last_error(void);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int vh_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VH_H_ */

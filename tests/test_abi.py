@@ -1,0 +1,69 @@
+"""The C ABI on the host: the library loads, exports every declared
+function, and rejects bad arguments before touching a device (no GPU needed)."""
+import ctypes
+
+import pytest
+
+
+def test_exports_every_header_function(vhlib):
+    names = vhlib.header_functions()
+    assert {"vh_scan_forward", "vh_debug_permute", "vh_workspace_size", "vh_status_string",
+            "vh_last_error", "vh_params_init", "vh_version"} <= set(names)
+    L = vhlib.lib()
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_params_init_defaults(vhlib):
+    p = vhlib.CParams()
+    vhlib.lib().vh_params_init(ctypes.byref(p))
+    assert abs(p.gamma_eta - 0.025) < 1e-9 and abs(p.alpha_init - 0.9) < 1e-7
+    assert p.eps == pytest.approx(1e-6) and p.knorm_eps == pytest.approx(1e-6)
+    assert p.inj_inward == pytest.approx(1e-3) and p.spec_inward == pytest.approx(1e-6)
+    assert p.kk_floor == pytest.approx(1e-20)
+    assert p.x_dtype == vhlib.DTYPE_BF16 and p.accumulate == 0 and p.stats is None
+
+
+def test_status_strings_and_version(vhlib):
+    L = vhlib.lib()
+    assert L.vh_status_string(0) == b"ok"
+    assert L.vh_status_string(-1) == b"invalid argument"
+    assert L.vh_version() >= 100
+    assert L.vh_workspace_size(None, 8, 8, 15, 0) == 0
+
+
+FAKE = 0x10000  # a 16-byte aligned address that is never dereferenced
+
+
+def _call(vhlib, B=1, Cc=32, d=32, H=4, W=4, dirs=15, chunk=0, x=FAKE, mem=FAKE,
+          out=FAKE * 4096, **kw):
+    p = vhlib.make_cparams(B, Cc, d, True)
+    for k, v in kw.items():
+        setattr(p, k, v)
+    st = vhlib.lib().vh_scan_forward(x, mem, ctypes.byref(p), H, W, dirs, chunk, out)
+    return st, vhlib.lib().vh_last_error().decode()
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(dirs=0), -1), (dict(dirs=16), -1), (dict(chunk=-1), -1), (dict(H=0), -1),
+    (dict(B=0), -1), (dict(d=48, Cc=96), -2), (dict(Cc=40), -1), (dict(x=FAKE + 8), -1),
+    (dict(out=FAKE + 4), -1), (dict(x=0), -1), (dict(out=FAKE), -1),
+    (dict(gate_mode=3), -1), (dict(alpha_init=1.0), -1), (dict(impl=7), -1),
+    (dict(x_dtype=5), -2),
+])
+def test_bad_arguments_are_rejected_on_the_host(vhlib, kw, status):
+    st, msg = _call(vhlib, **kw)
+    assert st == status and msg
+
+
+def test_debug_permute_rejects_bad_route(vhlib):
+    p = vhlib.make_cparams(1, 16, 16, False)
+    assert vhlib.lib().vh_debug_permute(FAKE, ctypes.byref(p), 3, 4, 4, FAKE * 64) == -1
+
+
+def test_binding_refuses_cpu_tensors(vhlib):
+    import torch
+    x = torch.zeros(1, 4, 4, 16)
+    m = torch.zeros(4, 1, 4 * 256 + 32)
+    with pytest.raises(ValueError, match="CUDA"):
+        vhlib.scan_forward(x, m, 16)

@@ -1,0 +1,192 @@
+"""GB300-native VisionHOPE four-direction self-referential memory scan.
+
+Python binding of ``libvh.so`` (C ABI in ``include/vh.h``).  This module only
+marshals arguments: every step of the scan runs in the library's CUDA
+kernels.  There is no CPU fallback; if the library is missing or the tensors
+are not on a CUDA device, the call raises.
+
+Method: "VisionHOPE: Visual Backbones as Self-Modifying Learning Systems",
+Sec. 2.1-2.3 (the VisionHOPE operator, Eqs. (24)-(26)), with the six-memory
+set of "Nested Learning: The Illusion of Deep Learning Architectures",
+part 12, Eqs. (94)-(96).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from dataclasses import dataclass
+from typing import Optional
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libvh.so")
+HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "vh.h")
+
+DIR_RIGHT, DIR_LEFT, DIR_DOWN, DIR_UP, DIR_ALL = 1, 2, 4, 8, 15
+DTYPE_F32, DTYPE_BF16 = 0, 1
+GATE_GENERATED, GATE_FORCED_RAW, GATE_FORCED_EXEC = 0, 1, 2
+CTRL_NO_INJ_CAP, CTRL_NO_SPEC_CLAMP = 1, 2
+IMPL = {"auto": 0, "simt": 1, "tc": 2}
+STAT_TOKENS, STAT_SPEC_ACTIVE, STAT_INJ_RATIO_GT1, STAT_NONFINITE, STAT_COUNT = 0, 1, 2, 3, 8
+
+
+class VhError(RuntimeError):
+    """A libvh call returned a non-OK status."""
+
+
+class CParams(ctypes.Structure):
+    """Mirror of ``vh_params`` (include/vh.h)."""
+    _fields_ = [
+        ("batch", ctypes.c_int), ("channels", ctypes.c_int), ("head_dim", ctypes.c_int),
+        ("x_dtype", ctypes.c_int),
+        ("gamma_eta", ctypes.c_float), ("alpha_init", ctypes.c_float),
+        ("eta_bias", ctypes.c_float), ("eps", ctypes.c_float), ("knorm_eps", ctypes.c_float),
+        ("inj_inward", ctypes.c_float), ("spec_inward", ctypes.c_float),
+        ("kk_floor", ctypes.c_float),
+        ("dir_scale", ctypes.c_void_p), ("memories_out", ctypes.c_void_p),
+        ("gate_mode", ctypes.c_int), ("forced_eta", ctypes.c_float),
+        ("forced_alpha", ctypes.c_float), ("control_flags", ctypes.c_uint),
+        ("stats", ctypes.c_void_p), ("impl", ctypes.c_int), ("accumulate", ctypes.c_int),
+        ("stream", ctypes.c_void_p),
+    ]
+
+
+@dataclass
+class ScanParams:
+    """Method constants and switches of one call (defaults: the pages' values)."""
+    gamma_eta: float = 0.025
+    alpha_init: float = 0.9
+    eta_bias: float = 0.0
+    eps: float = 1e-6
+    knorm_eps: float = 1e-6
+    inj_inward: float = 1e-3
+    spec_inward: float = 1e-6
+    kk_floor: float = 1e-20
+    gate_mode: int = GATE_GENERATED
+    forced_eta: float = 0.0
+    forced_alpha: float = 0.0
+    control_flags: int = 0
+    impl: str = "auto"
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libvh.so (built by ``__graft_entry__.build()``); raise if it is missing."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libvh.so is not built ({LIB_PATH}); run __graft_entry__.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, ci, cu = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint
+        L.vh_scan_forward.restype = ci
+        L.vh_scan_forward.argtypes = [vp, vp, ctypes.POINTER(CParams), ci, ci, cu, ci, vp]
+        L.vh_debug_permute.restype = ci
+        L.vh_debug_permute.argtypes = [vp, ctypes.POINTER(CParams), ci, ci, ci, vp]
+        L.vh_workspace_size.restype = ctypes.c_size_t
+        L.vh_workspace_size.argtypes = [ctypes.POINTER(CParams), ci, ci, cu, ci]
+        L.vh_status_string.restype = ctypes.c_char_p
+        L.vh_status_string.argtypes = [ci]
+        L.vh_last_error.restype = ctypes.c_char_p
+        L.vh_last_error.argtypes = []
+        L.vh_version.restype = ci
+        L.vh_params_init.restype = None
+        L.vh_params_init.argtypes = [ctypes.POINTER(CParams)]
+        _lib = L
+    return _lib
+
+
+def header_functions() -> list[str]:
+    """Names of the functions ``include/vh.h`` declares."""
+    text = open(HEADER_PATH).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(vh_[a-z_]+)\s*\(", text)))
+
+
+def _check(status: int):
+    if status != 0:
+        L = lib()
+        raise VhError(f"{L.vh_status_string(status).decode()} ({status}): "
+                      f"{L.vh_last_error().decode()}")
+
+
+def make_cparams(batch: int, channels: int, head_dim: int, x_is_bf16: bool,
+                 params: Optional[ScanParams] = None, *, dir_scale_ptr: int = 0,
+                 memories_out_ptr: int = 0, stats_ptr: int = 0, stream_ptr: int = 0,
+                 accumulate: bool = False) -> CParams:
+    p = params or ScanParams()
+    if p.impl not in IMPL:
+        raise ValueError(f"impl must be one of {sorted(IMPL)}")
+    return CParams(batch, channels, head_dim, DTYPE_BF16 if x_is_bf16 else DTYPE_F32,
+                   p.gamma_eta, p.alpha_init, p.eta_bias, p.eps, p.knorm_eps, p.inj_inward,
+                   p.spec_inward, p.kk_floor, dir_scale_ptr or None, memories_out_ptr or None,
+                   p.gate_mode, p.forced_eta, p.forced_alpha, p.control_flags,
+                   stats_ptr or None, IMPL[p.impl], 1 if accumulate else 0,
+                   stream_ptr or None)
+
+
+def _stream_ptr(stream) -> int:
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def _require_cuda(name, t, dtypes):
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (no CPU path exists)")
+    if t.dtype not in dtypes:
+        raise ValueError(f"{name} dtype {t.dtype} not in {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def scan_forward(x, memories0, head_dim: int, dirs: int = DIR_ALL, chunk: int = 0, out=None,
+                 params: Optional[ScanParams] = None, dir_scale=None, memories_out=None,
+                 stats=None, stream=None, accumulate: bool = False):
+    """VisionHOPE operator: x [B][H][W][Cc] (bf16/fp32, CUDA) -> out [B][H][W][Cc] fp32.
+
+    memories0: fp32 [4][Cc/head_dim][4d^2+2d] initial state per (route, head).
+    Optional: dir_scale fp32 [4][Cc]; memories_out fp32 [B][4][nh][4d^2+2d];
+    stats uint64/int64 [8] (accumulated).  accumulate=True adds to ``out``
+    instead of overwriting it.  Runs on ``stream`` (default: torch's current
+    stream) asynchronously."""
+    import torch
+    _require_cuda("x", x, (torch.bfloat16, torch.float32))
+    _require_cuda("memories0", memories0, (torch.float32,))
+    B, H, W, Cc = x.shape
+    nh = Cc // head_dim
+    if memories0.numel() != 4 * nh * (4 * head_dim * head_dim + 2 * head_dim):
+        raise ValueError("memories0 must hold [4][nh][4d^2+2d] floats")
+    if out is None:
+        if accumulate:
+            raise ValueError("accumulate=True needs an out tensor")
+        out = torch.empty((B, H, W, Cc), dtype=torch.float32, device=x.device)
+    _require_cuda("out", out, (torch.float32,))
+    if dir_scale is not None:
+        _require_cuda("dir_scale", dir_scale, (torch.float32,))
+    if memories_out is not None:
+        _require_cuda("memories_out", memories_out, (torch.float32,))
+    if stats is not None:
+        _require_cuda("stats", stats, (torch.int64, torch.uint64) if hasattr(torch, "uint64") else (torch.int64,))
+    cp = make_cparams(B, Cc, head_dim, x.dtype == torch.bfloat16, params,
+                      dir_scale_ptr=dir_scale.data_ptr() if dir_scale is not None else 0,
+                      memories_out_ptr=memories_out.data_ptr() if memories_out is not None else 0,
+                      stats_ptr=stats.data_ptr() if stats is not None else 0,
+                      stream_ptr=_stream_ptr(stream), accumulate=accumulate)
+    _check(lib().vh_scan_forward(x.data_ptr(), memories0.data_ptr(), ctypes.byref(cp), H, W,
+                                 dirs, chunk, out.data_ptr()))
+    return out
+
+
+def debug_permute(x, route: int, head_dim: int, stream=None):
+    """Z_r = P_r(Z) for one route, gathered by the library's device index code."""
+    import torch
+    _require_cuda("x", x, (torch.bfloat16, torch.float32))
+    B, H, W, Cc = x.shape
+    seq = torch.empty((B, H * W, Cc), dtype=x.dtype, device=x.device)
+    cp = make_cparams(B, Cc, head_dim, x.dtype == torch.bfloat16, None,
+                      stream_ptr=_stream_ptr(stream))
+    _check(lib().vh_debug_permute(x.data_ptr(), ctypes.byref(cp), H, W, route, seq.data_ptr()))
+    return seq

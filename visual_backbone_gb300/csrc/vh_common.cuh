@@ -1,0 +1,119 @@
+// vh_common.cuh -- device helpers shared by the scan kernels of libvh.
+//
+// Method: "VisionHOPE: Visual Backbones as Self-Modifying Learning Systems"
+// (Sec. 2.1-2.3, App. B.3-B.5, App. C.1) with the six-memory set of "Nested
+// Learning: The Illusion of Deep Learning Architectures", part 12,
+// Eqs. (94)-(96).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "vh.h"
+
+namespace vh {
+
+// Everything a scan kernel needs, by value (kernel parameter space).
+struct ScanArgs {
+    const void *x;            // [B][H][W][Cc]
+    const float *mem0;        // [4][nh][4d^2+2d]
+    float *out;               // [B][H][W][Cc] fp32, zeroed before the scan kernels run
+    float *mem_out;           // [B][4][nh][4d^2+2d] or nullptr
+    const float *dir_scale;   // [4][Cc] or nullptr
+    unsigned long long *stats;
+    int B, H, W, nh, Cc;
+    int dir_list[4];          // enabled routes in ascending order
+    int ndirs;
+    int chunk;                // 0 = aligned
+    // method constants in fp32 (Def. 1, App. B.3, App. C.1)
+    float gamma_eta, alpha_logit, eta_bias, eps, knorm_eps;
+    float inj_factor;         // 1 - inj_inward
+    float spec_factor;        // 1 - spec_inward
+    float kk_floor;
+    int gate_mode;
+    float forced_eta, forced_alpha;
+    unsigned control_flags;
+};
+
+// Pixel visited at step t of route r on an H x W map (Eq. (24); the route
+// orders of the VMamba explainer: row-major, full reversal, transpose then
+// flatten, full reversal).
+__host__ __device__ __forceinline__ int route_pixel(int r, int t, int H, int W)
+{
+    const int N = H * W;
+    const int s = (r & 1) ? (N - 1 - t) : t;
+    return (r < 2) ? s : (s % H) * W + s / H;
+}
+
+// Chunk length of route r, Eq. (25) when chunk == 0.
+__host__ __device__ __forceinline__ int route_chunk(int r, int chunk, int H, int W)
+{
+    return chunk > 0 ? chunk : (r < 2 ? W : H);
+}
+
+__device__ __forceinline__ float softplus_f(float s)
+{
+    return fmaxf(s, 0.0f) + log1pf(expf(-fabsf(s)));
+}
+
+// Per-token scalars of the step-size control (Def. 1, Eqs. (19)-(20)) with
+// the App. B.3 safeguards: inward factors on both limits, ||k||^2 floored,
+// the spectral limit rounded toward zero.  kk = ||k||^2, dd = ||delta||^2.
+struct StepOut {
+    float eta_tilde;
+    bool spec_active;    // spectral limit strictly below the candidate
+    bool inj_ratio_gt1;  // raw step above the injection limit
+};
+
+__device__ __forceinline__ StepOut step_control(const ScanArgs &a, float eta, float alpha,
+                                                float kk, float dd)
+{
+    StepOut o;
+    const float r = sqrtf(dd + a.eps * a.eps) + a.eps;
+    const float eta_inj = a.inj_factor * (1.0f - alpha) / r;
+    float eta_bar;
+    if (a.control_flags & VH_CTRL_NO_INJ_CAP)
+        eta_bar = eta;
+    else if (eta_inj > 0.0f)
+        eta_bar = eta_inj * (-expm1f(-eta / eta_inj));
+    else
+        eta_bar = 0.0f;  // limit of Eq. (19) when the injection limit vanishes
+    float spec = a.spec_factor * 2.0f * alpha / fmaxf(kk, a.kk_floor);
+    spec = nextafterf(spec, 0.0f);
+    const bool clamp = !(a.control_flags & VH_CTRL_NO_SPEC_CLAMP);
+    o.spec_active = clamp && spec < eta_bar;
+    o.eta_tilde = o.spec_active ? spec : eta_bar;
+    o.inj_ratio_gt1 = eta > eta_inj;
+    return o;
+}
+
+// Raw step and retention from the scalar memory outputs, Eq. (53).
+__device__ __forceinline__ void gates(const ScanArgs &a, float s_eta, float s_alpha,
+                                      float &eta, float &alpha)
+{
+    if (a.gate_mode == VH_GATE_GENERATED) {
+        eta = a.gamma_eta * softplus_f(s_eta + a.eta_bias);
+        alpha = 1.0f / (1.0f + expf(-(s_alpha + a.alpha_logit)));
+    } else {
+        eta = a.forced_eta;
+        alpha = a.forced_alpha;
+    }
+}
+
+template <typename T> struct XElem;
+template <> struct XElem<float> {
+    static __device__ __forceinline__ float to_f(float v) { return v; }
+};
+template <> struct XElem<__nv_bfloat16> {
+    static __device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+};
+
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+}  // namespace vh

@@ -1,0 +1,322 @@
+// vh_scan_simt.cu -- fp32 CUDA-core kernel of the four-direction VisionHOPE
+// memory scan.
+//
+// One CTA owns one scan (image b, route r, head h) for its whole length and
+// keeps the six memories of that scan in shared memory.  Per chunk
+// ("VisionHOPE", Sec. 2.1.3 Eqs. (15)-(16)) it
+//   1. gathers the chunk's tokens along the route (Eq. (24)),
+//   2. generates k_raw, v, q_raw, s^eta, s^alpha from the boundary state,
+//   3. normalises k and q (App. C.1, App. B.5) and applies the step-size
+//      control of Def. 1 per token (Eqs. (19)-(20), App. B.3 safeguards),
+//   4. reads out y_t = M^m_b q_t and adds lambda_r * y_t at the token's
+//      pixel (Eq. (26)),
+//   5. advances the shared gain G_t = G_{t-1} A_t + B_t = alpha_t G_{t-1}
+//      - eta_t (G_{t-1} k_t + delta_t) k_t^T (App. B.4, Prop. 2, Eq. (46)),
+//      whose rows evolve independently,
+//   6. at the chunk end replaces every memory by M_b G (Eq. (46)).
+// Long chunks are processed in token tiles; the gain carries across tiles.
+// All arithmetic is fp32 on CUDA cores; this kernel is the simple, general
+// path (any head_dim in {16,32,64}, any chunk length) and the A/B reference
+// for the tensor-core kernel.
+#include "vh_common.cuh"
+
+namespace vh {
+
+template <int D>
+struct SimtCfg {
+    static constexpr int NT = 256;
+    static constexpr int NW = NT / 32;
+    static constexpr int R = 4 * D + 2;    // rows of the state: k, v, q, m (d each), eta, alpha
+    static constexpr int RG = 3 * D + 2;   // rows used by the generation: k, v, q, eta, alpha
+    static constexpr int SS = D + 1;       // padded row stride of the state (bank-conflict free)
+    static constexpr int T = (D == 64) ? 32 : 64;  // token tile
+    static constexpr int PS = RG + 1;      // row stride of the generation outputs
+    static constexpr int TPR = NT / D;     // threads per gain row
+    static constexpr int CPT = D / TPR;    // gain columns per thread
+    static constexpr int JB = 8;           // tokens per register block
+    static constexpr int CPL = (D + 31) / 32;  // vector components per lane
+    static constexpr int OFF_S = 0;
+    static constexpr int OFF_X = OFF_S + R * SS;
+    static constexpr int OFF_P = OFF_X + T * D;
+    static constexpr int OFF_K = OFF_P + T * PS;
+    static constexpr int OFF_DL = OFF_K + T * D;
+    static constexpr int OFF_Q = OFF_DL + T * D;
+    static constexpr int OFF_SC = OFF_Q + T * D;
+    static constexpr int OFF_PIX = OFF_SC + 2 * T;
+    static constexpr int FLOATS = OFF_PIX + T;
+    static constexpr size_t BYTES = (size_t)FLOATS * 4;
+    static_assert(T % JB == 0, "tile must hold whole register blocks");
+    static_assert(D * D <= T * PS, "gain must fit in the generation buffer it reuses");
+    static_assert(TPR * CPT == D && TPR <= 32, "gain thread map");
+};
+
+template <int D, typename XT>
+__global__ void __launch_bounds__(256) scan_simt_kernel(const ScanArgs a)
+{
+    using C = SimtCfg<D>;
+    extern __shared__ float4 smem_f4[];
+    float *sm = reinterpret_cast<float *>(smem_f4);
+    float *S = sm + C::OFF_S;
+    float *X = sm + C::OFF_X;
+    float *P = sm + C::OFF_P;
+    float *K = sm + C::OFF_K;
+    float *DL = sm + C::OFF_DL;
+    float *Q = sm + C::OFF_Q;
+    float *SC = sm + C::OFF_SC;
+    int *PIX = reinterpret_cast<int *>(sm + C::OFF_PIX);
+    __shared__ unsigned long long st_cnt[3];
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    int id = blockIdx.x;
+    const int h = id % a.nh;
+    id /= a.nh;
+    const int r = a.dir_list[id % a.ndirs];
+    const int b = id / a.ndirs;
+    const int H = a.H, W = a.W, N = H * W, Cc = a.Cc;
+    const size_t SZ = (size_t)C::R * D;
+
+    if (tid < 3) st_cnt[tid] = 0;
+    const float *m0 = a.mem0 + ((size_t)r * a.nh + h) * SZ;
+    for (int e = tid; e < C::R * D; e += C::NT) S[(e / D) * C::SS + (e % D)] = m0[e];
+
+    const int grow = tid / C::TPR;
+    const int gc0 = (tid % C::TPR) * C::CPT;
+    float G[C::CPT];
+
+    const int Cr = route_chunk(r, a.chunk, H, W);
+    const XT *xb = static_cast<const XT *>(a.x) + (size_t)b * N * Cc + (size_t)h * D;
+    float *ob = a.out + (size_t)b * N * Cc + (size_t)h * D;
+    const float *lam = a.dir_scale ? a.dir_scale + (size_t)r * Cc + (size_t)h * D : nullptr;
+    unsigned n_spec = 0, n_inj = 0, n_nf = 0;
+
+    for (int c0 = 0; c0 < N; c0 += Cr) {
+        const int L = min(Cr, N - c0);
+#pragma unroll
+        for (int c = 0; c < C::CPT; ++c) G[c] = (grow == gc0 + c) ? 1.0f : 0.0f;
+
+        for (int t0 = 0; t0 < L; t0 += C::T) {
+            const int Lt = min(C::T, L - t0);
+            __syncthreads();  // previous tile / chunk-end update finished with X, P, K, S
+            // 1. gather the tile along the route, 16-byte vectors
+            constexpr int EPV = 16 / (int)sizeof(XT);
+            constexpr int VPT = D / EPV;
+            if (tid < Lt) PIX[tid] = route_pixel(r, c0 + t0 + tid, H, W);
+            for (int e = tid; e < Lt * VPT; e += C::NT) {
+                const int j = e / VPT, v = e % VPT;
+                const int pix = route_pixel(r, c0 + t0 + j, H, W);
+                const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(xb + (size_t)pix * Cc + v * EPV));
+                const XT *el = reinterpret_cast<const XT *>(&raw);
+#pragma unroll
+                for (int u = 0; u < EPV; ++u) X[j * D + v * EPV + u] = XElem<XT>::to_f(el[u]);
+            }
+            __syncthreads();
+
+            // 2. generation from the boundary state: P[j][o] = sum_i S[o][i] x_j[i]
+            {
+                constexpr int OB = (C::RG + 31) / 32;
+                const int nJB = (Lt + C::JB - 1) / C::JB;
+                for (int item = warp; item < OB * nJB; item += C::NW) {
+                    const int o = (item % OB) * 32 + lane;
+                    const int j0 = (item / OB) * C::JB;
+                    if (o < C::RG) {
+                        float acc[C::JB];
+#pragma unroll
+                        for (int jj = 0; jj < C::JB; ++jj) acc[jj] = 0.0f;
+                        const float *srow = S + o * C::SS;
+#pragma unroll 8
+                        for (int i = 0; i < D; ++i) {
+                            const float s = srow[i];
+#pragma unroll
+                            for (int jj = 0; jj < C::JB; ++jj)
+                                acc[jj] = fmaf(s, X[(j0 + jj) * D + i], acc[jj]);
+                        }
+#pragma unroll
+                        for (int jj = 0; jj < C::JB; ++jj)
+                            if (j0 + jj < Lt) P[(j0 + jj) * C::PS + o] = acc[jj];
+                    }
+                }
+            }
+            __syncthreads();
+
+            // 3. per-token normalisation and step control, one warp per token
+            for (int j = warp; j < Lt; j += C::NW) {
+                const float *pr = P + j * C::PS;
+                float kr[C::CPL], vv[C::CPL], qr[C::CPL];
+                float kk = 0.0f, qq = 0.0f;
+#pragma unroll
+                for (int m = 0; m < C::CPL; ++m) {
+                    const int c = lane + 32 * m;
+                    const bool ok = c < D;
+                    kr[m] = ok ? pr[c] : 0.0f;
+                    vv[m] = ok ? pr[D + c] : 0.0f;
+                    qr[m] = ok ? pr[2 * D + c] : 0.0f;
+                    kk = fmaf(kr[m], kr[m], kk);
+                    qq = fmaf(qr[m], qr[m], qq);
+                }
+                kk = warp_sum(kk);
+                qq = warp_sum(qq);
+                const float nk = sqrtf(kk + a.knorm_eps), nq = sqrtf(qq + a.knorm_eps);
+                float kn2 = 0.0f, dd = 0.0f;
+#pragma unroll
+                for (int m = 0; m < C::CPL; ++m) {
+                    kr[m] = kr[m] / nk;
+                    qr[m] = qr[m] / nq;
+                    vv[m] = kr[m] - vv[m];  // delta = k - v
+                    kn2 = fmaf(kr[m], kr[m], kn2);
+                    dd = fmaf(vv[m], vv[m], dd);
+                }
+                kn2 = warp_sum(kn2);
+                dd = warp_sum(dd);
+                float eta, alpha;
+                gates(a, pr[3 * D], pr[3 * D + 1], eta, alpha);
+                float eta_t;
+                if (a.gate_mode == VH_GATE_FORCED_EXEC) {
+                    eta_t = a.forced_eta;
+                } else {
+                    const StepOut so = step_control(a, eta, alpha, kn2, dd);
+                    eta_t = so.eta_tilde;
+                    n_spec += (lane == 0 && so.spec_active);
+                    n_inj += (lane == 0 && so.inj_ratio_gt1);
+                }
+#pragma unroll
+                for (int m = 0; m < C::CPL; ++m) {
+                    const int c = lane + 32 * m;
+                    if (c < D) {
+                        K[j * D + c] = kr[m];
+                        DL[j * D + c] = vv[m];
+                        Q[j * D + c] = qr[m];
+                    }
+                }
+                if (lane == 0) {
+                    SC[2 * j] = alpha;
+                    SC[2 * j + 1] = eta_t;
+                }
+            }
+            __syncthreads();
+
+            // 4. readout y_j = M^m_b q_j and the fused restore/sum of Eq. (26)
+            {
+                const int nJB = (Lt + C::JB - 1) / C::JB;
+                for (int jb = warp; jb < nJB; jb += C::NW) {
+                    const int j0 = jb * C::JB;
+#pragma unroll
+                    for (int m = 0; m < C::CPL; ++m) {
+                        const int i = lane + 32 * m;
+                        if (i < D) {
+                            float acc[C::JB];
+#pragma unroll
+                            for (int jj = 0; jj < C::JB; ++jj) acc[jj] = 0.0f;
+                            const float *mrow = S + (3 * D + i) * C::SS;
+#pragma unroll 8
+                            for (int l = 0; l < D; ++l) {
+                                const float mv = mrow[l];
+#pragma unroll
+                                for (int jj = 0; jj < C::JB; ++jj)
+                                    acc[jj] = fmaf(mv, Q[(j0 + jj) * D + l], acc[jj]);
+                            }
+                            const float lm = lam ? lam[i] : 1.0f;
+#pragma unroll
+                            for (int jj = 0; jj < C::JB; ++jj) {
+                                if (j0 + jj < Lt) {
+                                    n_nf += !isfinite(acc[jj]);
+                                    atomicAdd(ob + (size_t)PIX[j0 + jj] * Cc + i, lm * acc[jj]);
+                                }
+                            }
+                        }
+                    }
+                }
+            }
+
+            // 5. shared gain over the tile's tokens (rows are independent)
+            for (int j = 0; j < Lt; ++j) {
+                const float *kj = K + j * D;
+                float part = 0.0f;
+#pragma unroll
+                for (int c = 0; c < C::CPT; ++c) part = fmaf(G[c], kj[gc0 + c], part);
+#pragma unroll
+                for (int o = C::TPR / 2; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+                const float s = SC[2 * j + 1] * (part + DL[j * D + grow]);
+                const float al = SC[2 * j];
+#pragma unroll
+                for (int c = 0; c < C::CPT; ++c) G[c] = fmaf(-s, kj[gc0 + c], al * G[c]);
+            }
+        }
+
+        // 6. chunk end: every memory becomes M_b G
+        float *Gs = P;
+#pragma unroll
+        for (int c = 0; c < C::CPT; ++c) Gs[grow * D + gc0 + c] = G[c];
+        __syncthreads();
+        for (int o = warp; o < C::R; o += C::NW) {
+            const float *srow = S + o * C::SS;
+            float acc[C::CPL];
+#pragma unroll
+            for (int m = 0; m < C::CPL; ++m) acc[m] = 0.0f;
+#pragma unroll 8
+            for (int l = 0; l < D; ++l) {
+                const float s = srow[l];
+#pragma unroll
+                for (int m = 0; m < C::CPL; ++m) {
+                    const int i = lane + 32 * m;
+                    if (i < D) acc[m] = fmaf(s, Gs[l * D + i], acc[m]);
+                }
+            }
+            __syncwarp();
+#pragma unroll
+            for (int m = 0; m < C::CPL; ++m) {
+                const int i = lane + 32 * m;
+                if (i < D) S[o * C::SS + i] = acc[m];
+            }
+            __syncwarp();
+        }
+    }
+    __syncthreads();
+
+    if (a.mem_out) {
+        float *mo = a.mem_out + (((size_t)b * 4 + r) * a.nh + h) * SZ;
+        for (int e = tid; e < C::R * D; e += C::NT) mo[e] = S[(e / D) * C::SS + (e % D)];
+    }
+    if (a.stats) {
+        if (n_spec) atomicAdd(&st_cnt[0], (unsigned long long)n_spec);
+        if (n_inj) atomicAdd(&st_cnt[1], (unsigned long long)n_inj);
+        if (n_nf) atomicAdd(&st_cnt[2], (unsigned long long)n_nf);
+        __syncthreads();
+        if (tid == 0) {
+            atomicAdd(a.stats + VH_STAT_TOKENS, (unsigned long long)N);
+            if (st_cnt[0]) atomicAdd(a.stats + VH_STAT_SPEC_ACTIVE, st_cnt[0]);
+            if (st_cnt[1]) atomicAdd(a.stats + VH_STAT_INJ_RATIO_GT1, st_cnt[1]);
+            if (st_cnt[2]) atomicAdd(a.stats + VH_STAT_NONFINITE, st_cnt[2]);
+        }
+    }
+}
+
+template <int D, typename XT>
+static cudaError_t launch_simt_t(const ScanArgs &a, cudaStream_t st)
+{
+    using C = SimtCfg<D>;
+    auto kern = scan_simt_kernel<D, XT>;
+    static int attr_set[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 64 && !attr_set[dev]) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::BYTES);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = 1;
+    }
+    const unsigned grid = (unsigned)(a.B * a.ndirs * a.nh);
+    kern<<<grid, C::NT, C::BYTES, st>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_scan_simt(const ScanArgs &a, int d, bool bf16, cudaStream_t st)
+{
+    switch (d) {
+    case 16: return bf16 ? launch_simt_t<16, __nv_bfloat16>(a, st) : launch_simt_t<16, float>(a, st);
+    case 32: return bf16 ? launch_simt_t<32, __nv_bfloat16>(a, st) : launch_simt_t<32, float>(a, st);
+    case 64: return bf16 ? launch_simt_t<64, __nv_bfloat16>(a, st) : launch_simt_t<64, float>(a, st);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace vh
