@@ -161,6 +161,23 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+def max_over_ranks(values, device=None):
+    """Element-wise max of per-rank timings (seconds) over the default process
+    group; identity when no group is initialised (N = 1)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def job_throughput(tokens_per_rank_step, steps, world, seconds):
+    """Whole-job units per second: all ranks' tokens over the slowest rank's time."""
+    return world * tokens_per_rank_step * steps / seconds
+
+
 # --------------------------------------------------------- oracle timing
 
 def time_oracle(wl, images, nthreads):
@@ -290,12 +307,8 @@ def run_ours(args, wl):
     kern_ms = [e[1].elapsed_time(e[2]) for e in events]
     total_s = sum(step_ms) / 1e3
     kern_avg_s = sum(kern_ms) / len(kern_ms) / 1e3
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([total_s, kern_avg_s], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_s, kern_avg_s = float(tt[0]), float(tt[1])
-    value = world * wl.tokens * args.steps / total_s
+    total_s, kern_avg_s = max_over_ranks([total_s, kern_avg_s], device=dev)
+    value = job_throughput(wl.tokens, args.steps, world, total_s)
 
     # end to end through the public API with host buffers (pinned), copies timed
     x_pin = x_host.pin_memory()
@@ -315,12 +328,8 @@ def run_ours(args, wl):
             e2e_step()
         eb.record(stream)
         torch.cuda.synchronize(dev)
-    e2e_s = ea.elapsed_time(eb) / 1e3
-    if world > 1:
-        tt = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        e2e_s = float(tt[0])
-    e2e_value = world * wl.tokens * e2e_steps / e2e_s
+    e2e_s, = max_over_ranks([ea.elapsed_time(eb) / 1e3], device=dev)
+    e2e_value = job_throughput(wl.tokens, e2e_steps, world, e2e_s)
 
     if rank == 0:
         flops, nbytes = algorithmic_cost(wl)

@@ -15,6 +15,27 @@ import numpy as np
 TOL = 2e-3
 
 
+def f32(v):
+    """A method constant as the C ABI carries it (fp32), widened back to fp64,
+    so that the oracle runs on exactly the parameter values the GPU receives
+    (with alpha_init = 0.999 the fp32 rounding of 1 - alpha_init alone moves
+    the outputs by ~2e-3)."""
+    return float(np.float32(v))
+
+
+def oracle_params_like(orc, vhp, dir_scale=None):
+    """Oracle parameters equal to a ScanParams after the fp32 round trip."""
+    p = orc.OracleParams(gamma_eta=f32(vhp.gamma_eta), alpha_init=f32(vhp.alpha_init),
+                         eta_bias=f32(vhp.eta_bias), eps=f32(vhp.eps),
+                         knorm_eps=f32(vhp.knorm_eps), inj_inward=f32(vhp.inj_inward),
+                         spec_inward=f32(vhp.spec_inward), kk_floor=f32(vhp.kk_floor),
+                         gate_mode=vhp.gate_mode, forced_eta=f32(vhp.forced_eta),
+                         forced_alpha=f32(vhp.forced_alpha), control_flags=vhp.control_flags)
+    if dir_scale is not None:
+        p.dir_scale = np.asarray(dir_scale, dtype=np.float32).astype(np.float64)
+    return p
+
+
 def parity_err(g, o):
     g = np.asarray(g, dtype=np.float64)
     o = np.asarray(o, dtype=np.float64)

@@ -9,7 +9,7 @@ import numpy as np
 import pytest
 
 from visual_backbone_gb300 import synth
-from tests._helpers import TOL, parity_err, run_gpu, to_device_x
+from tests._helpers import TOL, oracle_params_like, parity_err, run_gpu, to_device_x
 
 pytestmark = pytest.mark.gpu
 
@@ -17,14 +17,10 @@ IMPLS = ["simt", "auto"]
 
 
 def _oracle_params(orc, wl, vhp=None, dir_scale=None):
-    p = orc.OracleParams(eta_bias=wl.eta_bias, alpha_init=wl.alpha_init)
-    if vhp is not None:
-        p.gate_mode, p.forced_eta, p.forced_alpha = vhp.gate_mode, vhp.forced_eta, vhp.forced_alpha
-        p.control_flags = vhp.control_flags
-        p.eta_bias, p.alpha_init = vhp.eta_bias, vhp.alpha_init
-    if dir_scale is not None:
-        p.dir_scale = dir_scale.astype(np.float64)
-    return p
+    import visual_backbone_gb300 as vh
+    if vhp is None:
+        vhp = vh.ScanParams(eta_bias=wl.eta_bias, alpha_init=wl.alpha_init)
+    return oracle_params_like(orc, vhp, dir_scale)
 
 
 def _compare(orc, vhlib, wl, dirs=15, chunk=0, vhp=None, dir_scale=None, impl="auto",

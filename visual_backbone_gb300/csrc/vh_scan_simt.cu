@@ -122,7 +122,9 @@ __global__ void __launch_bounds__(256) scan_simt_kernel(const ScanArgs a)
                         float acc[C::JB];
 #pragma unroll
                         for (int jj = 0; jj < C::JB; ++jj) acc[jj] = 0.0f;
-                        const float *srow = S + o * C::SS;
+                        // outputs 0..3d-1 are k, v, q (state rows 0..3d-1); outputs 3d, 3d+1
+                        // are s^eta, s^alpha (state rows 4d, 4d+1, after the content memory)
+                        const float *srow = S + (o < 3 * D ? o : o + D) * C::SS;
 #pragma unroll 8
                         for (int i = 0; i < D; ++i) {
                             const float s = srow[i];
