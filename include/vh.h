@@ -76,6 +76,9 @@ enum {
     VH_STAT_SPEC_ACTIVE = 1,   /* spectral clamp strictly below the capped candidate */
     VH_STAT_INJ_RATIO_GT1 = 2, /* raw step above the injection limit (eta/eta_inj > 1) */
     VH_STAT_NONFINITE = 3,     /* non-finite readout values */
+    VH_STAT_TIMEOUT = 4,       /* CTAs whose bounded wait on an asynchronous copy or MMA
+                                  expired (the kernel then stops issuing work; results
+                                  of that call are invalid) */
     VH_STAT_COUNT = 8
 };
 

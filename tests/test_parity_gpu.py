@@ -39,7 +39,7 @@ def _compare(orc, vhlib, wl, dirs=15, chunk=0, vhp=None, dir_scale=None, impl="a
         assert np.isnan(g["mem"][:, unsel]).all(), "disabled routes' memory slots were written"
     nd = len(sel)
     assert g["stats"][0] == inp.x64.shape[0] * nd * wl.nh * wl.H * wl.W
-    assert g["stats"][3] == 0
+    assert g["stats"][3] == 0 and g["stats"][4] == 0
     return e_out, e_mem
 
 
@@ -88,6 +88,9 @@ def test_direction_subsets(orc, vhlib, impl, dirs):
 @pytest.mark.parametrize("case", [
     # B, H, W, nh, d, dtype, chunk, alpha_init, eta_bias
     (2, 5, 70, 2, 32, "bf16", 0, 0.999, 0.0),     # rows of 70: two tiles, ragged tail
+    (1, 130, 3, 1, 32, "bf16", 0, 0.999, 1.0),    # columns of 130: three tiles
+    (2, 4, 64, 2, 32, "bf16", 0, 0.9, 0.0),       # rows of exactly one tile
+    (1, 2, 65, 3, 32, "bf16", 65, 0.999, 0.0),    # explicit chunk equal to the row length
     (2, 70, 5, 1, 32, "bf16", 0, 0.99, 1.0),      # columns of 70
     (1, 9, 11, 2, 32, "f32", 7, 0.999, 0.0),      # fixed chunk, partial last chunk
     (2, 3, 40, 1, 64, "bf16", 0, 0.999, 0.0),     # d = 64, rows of 40
@@ -179,16 +182,18 @@ def test_accumulate_adds(vhlib):
 FULL = ["stage1", "stage2", "stage3", "highres"]
 
 
+@pytest.mark.parametrize("impl", IMPLS)
 @pytest.mark.parametrize("name", FULL)
 @pytest.mark.parametrize("variant", ["plain", "longmem"])
-def test_full_size_sampled(orc, vhlib, name, variant):
+def test_full_size_sampled(orc, vhlib, name, variant, impl):
     """GPU on the whole batch (as timed); oracle on the first and last image."""
     wl = synth.WORKLOADS[name]
     if variant == "longmem":
         wl = wl.long_memory()
     inp = synth.make_inputs(wl)
-    g = run_gpu(vhlib, inp, want_memories=True, want_stats=True)
+    g = run_gpu(vhlib, inp, want_memories=True, want_stats=True, impl=impl)
     assert g["stats"][0] == wl.B * 4 * wl.nh * wl.N and g["stats"][3] == 0
+    assert g["stats"][4] == 0
     p = _oracle_params(orc, wl)
     for b in (0, wl.B - 1):
         o, om = orc.forward(inp.x64[b:b + 1], inp.mem0, wl.H, wl.W, wl.nh, wl.d, params=p,
