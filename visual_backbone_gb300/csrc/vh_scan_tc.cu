@@ -42,28 +42,31 @@ namespace tc {
 constexpr int D = 32;        // head dim of this kernel
 constexpr int TT = 64;       // tokens per sub-tile (M of the generation/readout MMAs)
 constexpr int NT = 128;      // one warpgroup
-constexpr int SROWS = 144;   // operand rows of the state: k v q m (128) | eta alpha | 14 zero rows
 constexpr int ROW_B = D * 2;         // bytes of one bf16 operand row (64)
 constexpr int SBO_K32 = 8 * ROW_B;   // 8-row group stride of a K = 32 operand (512 B)
 constexpr int LBO_K32 = 128;         // K-direction core-matrix stride of a K = 32 operand
 constexpr int LBO_X = TT * 16;       // K-direction stride of the TMA-loaded x tile (1 KB)
 constexpr int SBO_X = 128;
-constexpr int KS = D + 4;            // fp32 row stride of the key / delta tiles (bank spread)
-constexpr int S_PIECE = SROWS * ROW_B;   // one bf16 piece of the state operand
+constexpr int KS = D;                // fp32 row stride of the key / delta tiles
+// One bf16 piece of the state operand: 17 row groups (rows 0..129 used).  The
+// N = 16 generation MMA of the eta/alpha rows also reads rows 130..143, which fall
+// in unused slots or in the next piece: those D columns are never read.
+constexpr int S_PIECE = 17 * SBO_K32;
 constexpr int Q_PIECE = TT * ROW_B;
 constexpr int G_PIECE = D * ROW_B;
 
 constexpr int OFF_X = 0;                          // TT x D bf16 (4 boxes of 1 KB)
-constexpr int OFF_S = OFF_X + TT * D * 2;         // 3 pieces x SROWS x D bf16
-constexpr int OFF_Q = OFF_S + 3 * S_PIECE;        // 3 pieces x TT x D bf16
-constexpr int OFF_G = OFF_Q + 3 * Q_PIECE;        // 3 pieces x D x D bf16 (B operand, n = column of G)
-constexpr int OFF_KF = OFF_G + 3 * G_PIECE;       // TT x KS fp32 keys, route order
+constexpr int OFF_S = OFF_X + TT * D * 2;         // 3 pieces of the state operand
+constexpr int OFF_Q = OFF_S + 3 * S_PIECE;        // 3 pieces x TT x D bf16 queries
+constexpr int OFF_G = OFF_Q + 3 * Q_PIECE;        // 3 pieces x D x D bf16 gain (B operand)
+constexpr int OFF_GF = OFF_G + 3 * G_PIECE;       // D x D fp32 gain rows
+constexpr int OFF_KF = OFF_GF + D * D * 4;        // TT x KS fp32 keys, route order
 constexpr int OFF_DL = OFF_KF + TT * KS * 4;      // TT x KS fp32 delta, route order
-constexpr int OFF_GF = OFF_DL + TT * KS * 4;      // D x D fp32 gain
-constexpr int OFF_SEA = OFF_GF + D * D * 4;       // 2 x D fp32 eta / alpha rows of the state
+constexpr int OFF_SEA = OFF_DL + TT * KS * 4;     // 2 x D fp32 eta / alpha rows of the state
 constexpr int OFF_SC = OFF_SEA + 2 * D * 4;       // TT x {alpha, eta_tilde/alpha, 1/alpha, 0}
 constexpr int OFF_BAR = OFF_SC + TT * 16;         // mbarriers, TMEM base, flags
 constexpr int SMEM_BYTES = OFF_BAR + 128;
+static_assert(SMEM_BYTES <= 75 * 1024, "three CTAs per SM");
 constexpr uint32_t TMEM_COLS = 128;
 constexpr int COL_GEN = 0, COL_GEN2 = 96, COL_RO = 64, COL_UPD = 32;
 
@@ -198,6 +201,18 @@ __device__ __forceinline__ void store_split8(unsigned char *dst, int stride, con
     *reinterpret_cast<uint4 *>(dst + 2 * stride) = *reinterpret_cast<const uint4 *>(c);
 }
 
+// Sum of squares of 32 values in eight independent FMA chains (scalar FMAs issue at
+// twice the rate of packed pairs on this part).
+__device__ __forceinline__ float sumsq32(const float (&v)[32])
+{
+    float a[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) a[e] = v[e] * v[e];
+#pragma unroll
+    for (int e = 8; e < 32; ++e) a[e & 7] = fmaf(v[e], v[e], a[e & 7]);
+    return ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
+}
+
 // Byte offset of row `row`, K-group g (8 elements) in a K = 32 K-major operand.
 __device__ __forceinline__ int op_off(int row, int g)
 {
@@ -251,11 +266,6 @@ __device__ __forceinline__ void red_add_v4(float *addr, float4 v)
                  : "memory");
 }
 
-__device__ __forceinline__ void mbar_arrive(uint32_t bar)
-{
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
 __global__ void __launch_bounds__(NT, 3)
     scan_tc_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tm_row,
                    const __grid_constant__ CUtensorMap tm_col)
@@ -279,7 +289,6 @@ __global__ void __launch_bounds__(NT, 3)
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + OFF_BAR);
     const uint32_t mb_x = smem_u32(&bars[0]), mb_gen = smem_u32(&bars[1]);
     const uint32_t mb_ro = smem_u32(&bars[2]), mb_upd = smem_u32(&bars[3]);
-    const uint32_t mb_g = smem_u32(&bars[4]);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + OFF_BAR + 64);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + OFF_BAR + 72);
     volatile int *role_slot = reinterpret_cast<volatile int *>(sm + OFF_BAR + 76);
@@ -300,7 +309,6 @@ __global__ void __launch_bounds__(NT, 3)
         mbar_init(mb_gen, 1);
         mbar_init(mb_ro, 1);
         mbar_init(mb_upd, 1);
-        mbar_init(mb_g, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         // The serial gain loop goes to a warp whose SM sub-partition differs between
         // co-resident CTAs: CTAs hold consecutive groups of four hardware warp slots,
@@ -342,16 +350,15 @@ __global__ void __launch_bounds__(NT, 3)
         }
 #pragma unroll
         for (int g = 0; g < 4; ++g) store_split8(sS + op_off(tid, g), S_PIECE, v + 8 * g);
-        // eta / alpha rows (fp32 copy + operand rows 128, 129) and zero rows 130..143
+        // eta / alpha rows: fp32 copy and operand rows 128, 129
         if (tid < 2 * D) Sea[tid] = m0[4 * D * D + tid];
-        if (tid < 16) {
+        if (tid < 2) {
             const int row = 128 + tid;
             float z[8];
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    z[e] = (row < 130) ? m0[4 * D * D + (row - 128) * D + 8 * g + e] : 0.0f;
+                for (int e = 0; e < 8; ++e) z[e] = m0[4 * D * D + tid * D + 8 * g + e];
                 store_split8(sS + op_off(row, g), S_PIECE, z);
             }
         }
@@ -366,10 +373,10 @@ __global__ void __launch_bounds__(NT, 3)
     const float *lam = a.dir_scale ? a.dir_scale + (size_t)r * Cc + (size_t)h * D : nullptr;
     float *ob = a.out + (size_t)b * H * W * Cc + (size_t)h * D;
     unsigned n_spec = 0, n_inj = 0, n_nf = 0;
-    uint32_t ph_x = 0, ph_gen = 0, ph_ro = 0, ph_upd = 0, ph_g = 0;
+    uint32_t ph_x = 0, ph_gen = 0, ph_ro = 0, ph_upd = 0;
 
-    // gain state of the gain warp, lane = row of G: G = gam * ghat, packed in pairs
-    float2 gh[D / 2];
+    // gain state, lane (row 8w + l/4, columns 8(l%4)..+7) of G = gam * ghat
+    float gh[8];
     float gam = 1.0f, inv_gam = 1.0f;
 
     for (int c = 0; c < nlines; ++c) {
@@ -420,28 +427,20 @@ __global__ void __launch_bounds__(NT, 3)
                 tmem_ld32(tbase + lrow + COL_GEN + 32, vv);
                 float se, sa;
                 tmem_ld2(tbase + lrow + COL_GEN2, se, sa);
-                float2 acc = make_float2(0.f, 0.f);
+                const float rk = __frsqrt_rn(sumsq32(kr) + a.knorm_eps);
 #pragma unroll
-                for (int e = 0; e < 32; e += 2)
-                    acc = __ffma2_rn(make_float2(kr[e], kr[e + 1]), make_float2(kr[e], kr[e + 1]), acc);
-                const float rk = __frsqrt_rn(acc.x + acc.y + a.knorm_eps);
-                float2 kn2 = make_float2(0.f, 0.f), dd2 = make_float2(0.f, 0.f);
-#pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    const float2 k2 = __fmul2_rn(make_float2(kr[e], kr[e + 1]), make_float2(rk, rk));
-                    const float2 d2 = __fadd2_rn(k2, make_float2(-vv[e], -vv[e + 1]));
-                    kr[e] = k2.x; kr[e + 1] = k2.y;
-                    vv[e] = d2.x; vv[e + 1] = d2.y;
-                    kn2 = __ffma2_rn(k2, k2, kn2);
-                    dd2 = __ffma2_rn(d2, d2, dd2);
+                for (int e = 0; e < 32; ++e) {
+                    kr[e] *= rk;            // k
+                    vv[e] = kr[e] - vv[e];  // delta = k - v
                 }
+                const float kn2 = sumsq32(kr), dd2 = sumsq32(vv);
                 float eta, alpha;
                 gates(a, se, sa, eta, alpha);
                 float eta_t;
                 if (a.gate_mode == VH_GATE_FORCED_EXEC) {
                     eta_t = a.forced_eta;
                 } else {
-                    const StepOut so = step_control(a, eta, alpha, kn2.x + kn2.y, dd2.x + dd2.y);
+                    const StepOut so = step_control(a, eta, alpha, kn2, dd2);
                     eta_t = so.eta_tilde;
                     n_spec += valid && so.spec_active;
                     n_inj += valid && so.inj_ratio_gt1;
@@ -460,119 +459,120 @@ __global__ void __launch_bounds__(NT, 3)
                                          keep ? __frcp_rn(alpha) : 0.0f, 0.0f);
                 }
             }
+            tc_before();
             __syncthreads();
+            tc_after();
+            // ---- shared gain over this sub-tile's tokens, in route order, on all four warps:
+            // lane l of warp w owns row 8w + l/4 of G and columns 8(l%4) .. 8(l%4)+7, so each
+            // token costs two shuffles and three shared loads per lane.  G = gam * ghat, with
+            //   ghat <- ghat - (eta/alpha) (ghat k + delta / gam) k^T,  gam <- alpha gam
+            // (a pure scaling of G_j = alpha G_{j-1} - eta (G_{j-1} k + delta) k^T), folded
+            // back whenever gam would underflow and restarted when alpha = 0.
+            {
+                const int grow = 8 * warp + (lane >> 2), gq = lane & 3;
+                if (s == 0) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) gh[e] = (8 * gq + e == grow) ? 1.0f : 0.0f;
+                    gam = 1.0f;
+                    inv_gam = 1.0f;
+                }
+                float4 ka = *reinterpret_cast<const float4 *>(Kf + 8 * gq);
+                float4 kb = *reinterpret_cast<const float4 *>(Kf + 8 * gq + 4);
+                float4 co = SC[0];
+                float dl = DLf[grow];
+                for (int j = 0; j < Lt; ++j) {
+                    const float k[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
+                    const float4 cj = co;
+                    const float dj = dl;
+                    if (j + 1 < Lt) {  // next token's operands
+                        ka = *reinterpret_cast<const float4 *>(Kf + (j + 1) * KS + 8 * gq);
+                        kb = *reinterpret_cast<const float4 *>(Kf + (j + 1) * KS + 8 * gq + 4);
+                        co = SC[j + 1];
+                        dl = DLf[(j + 1) * KS + grow];
+                    }
+                    float p0 = gh[0] * k[0], p1 = gh[1] * k[1];
+                    p0 = fmaf(gh[2], k[2], p0);
+                    p1 = fmaf(gh[3], k[3], p1);
+                    p0 = fmaf(gh[4], k[4], p0);
+                    p1 = fmaf(gh[5], k[5], p1);
+                    p0 = fmaf(gh[6], k[6], p0);
+                    p1 = fmaf(gh[7], k[7], p1);
+                    float dot = p0 + p1;
+                    dot += __shfl_xor_sync(0xffffffffu, dot, 1);
+                    dot += __shfl_xor_sync(0xffffffffu, dot, 2);
+                    if (cj.z != 0.0f) {
+                        const float sc = -cj.y * fmaf(dj, inv_gam, dot);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) gh[e] = fmaf(sc, k[e], gh[e]);
+                        gam *= cj.x;
+                        inv_gam *= cj.z;
+                        if (gam < 1e-20f) {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) gh[e] *= gam;
+                            gam = 1.0f;
+                            inv_gam = 1.0f;
+                        }
+                    } else {
+                        const float sc = -cj.y * fmaf(gam, dot, dj);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) gh[e] = sc * k[e];
+                        gam = 1.0f;
+                        inv_gam = 1.0f;
+                    }
+                }
+                if (last) {
+                    // G rows in fp32, and G as the update's B operand (row n = column of G,
+                    // K = row of G).  When the chunk retains at least half of the state the
+                    // operand is G - I: the MMA forms only the increment M_b (G - I), which the
+                    // epilogue adds to M_b in fp32, so the tensor core's accumulation error is
+                    // relative to the change.  Otherwise the state is mostly replaced and the
+                    // MMA forms M_b G directly (no cancellation).
+                    const bool use_delta = gam >= 0.5f;
+                    float gv[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) gv[e] = gam * gh[e];
+                    float4 *gd = reinterpret_cast<float4 *>(Gf + grow * D + 8 * gq);
+                    gd[0] = make_float4(gv[0], gv[1], gv[2], gv[3]);
+                    gd[1] = make_float4(gv[4], gv[5], gv[6], gv[7]);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int cc = 8 * gq + e;
+                        __nv_bfloat16 p1, p2, p3;
+                        split3(gv[e] - ((use_delta && grow == cc) ? 1.0f : 0.0f), p1, p2, p3);
+                        unsigned char *d0 = sG + op_off(cc, grow >> 3) + 2 * (grow & 7);
+                        *reinterpret_cast<__nv_bfloat16 *>(d0) = p1;
+                        *reinterpret_cast<__nv_bfloat16 *>(d0 + G_PIECE) = p2;
+                        *reinterpret_cast<__nv_bfloat16 *>(d0 + 2 * G_PIECE) = p3;
+                    }
+                    if (tid == 0) *delta_form = use_delta ? 1 : 0;
+                }
+            }
+            fence_async_smem();
+            tc_before();
+            __syncthreads();  // G ready (last sub-tile); the gain's reads of the tiles are done
+            tc_after();
+            // ---- MMA 3 (chunk end): every d x d memory <- M_b G (six split cross terms,
+            // M = 128 rows), issued at once; queries and the readout proceed meanwhile
+            if (last && issuer && !*abort_flag) {
+                mma_split6(tbase + COL_UPD, smem_u32(sS), S_PIECE, smem_u32(sG), G_PIECE,
+                           idesc_bf16(128, 32));
+                mma_commit(mb_upd);
+            }
             // queries: normalised, split and written as the readout's A operand (row = box row)
-            auto do_queries = [&]() {
+            {
                 float qr[32];
                 tmem_ld32(tbase + lrow + COL_GEN + 64, qr);
-                float2 acc = make_float2(0.f, 0.f);
-#pragma unroll
-                for (int e = 0; e < 32; e += 2)
-                    acc = __ffma2_rn(make_float2(qr[e], qr[e + 1]), make_float2(qr[e], qr[e + 1]), acc);
-                const float rq = __frsqrt_rn(acc.x + acc.y + a.knorm_eps);
+                const float rq = __frsqrt_rn(sumsq32(qr) + a.knorm_eps);
 #pragma unroll
                 for (int e = 0; e < 32; ++e) qr[e] *= rq;
                 if (lane < 16) {
 #pragma unroll
                     for (int g = 0; g < 4; ++g) store_split8(sQ + op_off(jb, g), Q_PIECE, qr + 8 * g);
                 }
-            };
-            if (warp != gw) do_queries();
-            // ---- shared gain over this sub-tile's tokens, in route order (gain warp)
-            if (warp == gw) {
-                if (s == 0) {
-#pragma unroll
-                    for (int e = 0; e < D / 2; ++e)
-                        gh[e] = make_float2(2 * e == lane ? 1.0f : 0.0f, 2 * e + 1 == lane ? 1.0f : 0.0f);
-                    gam = 1.0f;
-                    inv_gam = 1.0f;
-                }
-                for (int j = 0; j < Lt; ++j) {
-                    const float4 *kp = reinterpret_cast<const float4 *>(Kf + j * KS);
-                    float2 k2[D / 2];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const float4 f = kp[e];
-                        k2[2 * e] = make_float2(f.x, f.y);
-                        k2[2 * e + 1] = make_float2(f.z, f.w);
-                    }
-                    const float4 co = SC[j];
-                    const float dl = DLf[j * KS + lane];
-                    float2 q0 = make_float2(0.f, 0.f), q1 = q0, q2 = q0, q3 = q0;
-#pragma unroll
-                    for (int e = 0; e < D / 2; e += 4) {
-                        q0 = __ffma2_rn(gh[e], k2[e], q0);
-                        q1 = __ffma2_rn(gh[e + 1], k2[e + 1], q1);
-                        q2 = __ffma2_rn(gh[e + 2], k2[e + 2], q2);
-                        q3 = __ffma2_rn(gh[e + 3], k2[e + 3], q3);
-                    }
-                    const float2 qs = __fadd2_rn(__fadd2_rn(q0, q1), __fadd2_rn(q2, q3));
-                    const float dot = qs.x + qs.y;
-                    if (co.z != 0.0f) {
-                        // G_j = (alpha gam) (ghat - (eta/alpha) (ghat k + delta/gam) k^T)
-                        const float sc = -co.y * fmaf(dl, inv_gam, dot);
-                        const float2 sc2 = make_float2(sc, sc);
-#pragma unroll
-                        for (int e = 0; e < D / 2; ++e) gh[e] = __ffma2_rn(sc2, k2[e], gh[e]);
-                        gam *= co.x;
-                        inv_gam *= co.z;
-                        if (gam < 1e-20f) {  // fold the scale back before it underflows
-                            const float2 g2 = make_float2(gam, gam);
-#pragma unroll
-                            for (int e = 0; e < D / 2; ++e) gh[e] = __fmul2_rn(gh[e], g2);
-                            gam = 1.0f;
-                            inv_gam = 1.0f;
-                        }
-                    } else {
-                        // no retention: G_j = -eta (G_{j-1} k + delta) k^T
-                        const float sc = -co.y * fmaf(gam, dot, dl);
-                        const float2 sc2 = make_float2(sc, sc);
-#pragma unroll
-                        for (int e = 0; e < D / 2; ++e) gh[e] = __fmul2_rn(sc2, k2[e]);
-                        gam = 1.0f;
-                        inv_gam = 1.0f;
-                    }
-                }
-                if (last) {
-                    // G = gam * ghat as fp32 rows; the update's B operand takes, per lane, one
-                    // column of G (K = row index of G).  When the chunk retains at least half of
-                    // the state (gam >= 1/2) the MMA gets G - I and forms only the increment
-                    // M_b (G - I), which the epilogue adds to M_b in fp32: the tensor core's
-                    // accumulation error is then relative to the change.  Otherwise the state is
-                    // mostly replaced and the MMA forms M_b G directly (no cancellation).
-                    float4 *gd = reinterpret_cast<float4 *>(Gf + lane * D);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        gd[e] = make_float4(gam * gh[2 * e].x, gam * gh[2 * e].y,
-                                            gam * gh[2 * e + 1].x, gam * gh[2 * e + 1].y);
-                    const bool use_delta = gam >= 0.5f;
-                    __syncwarp();
-                    float col[D];
-#pragma unroll
-                    for (int l = 0; l < D; ++l)
-                        col[l] = Gf[l * D + lane] - ((use_delta && l == lane) ? 1.0f : 0.0f);
-#pragma unroll
-                    for (int g = 0; g < 4; ++g) store_split8(sG + op_off(lane, g), G_PIECE, col + 8 * g);
-                    if (lane == 0) *delta_form = use_delta ? 1 : 0;
-                    fence_async_smem();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(mb_g);  // G is ready for the update MMA
-                }
-                do_queries();
             }
-            // ---- MMA 3 (chunk end): every d x d memory <- M_b G, issued as soon as G is ready
-            if (last && issuer) {
-                if (wt.wait(mb_g, ph_g) && !*abort_flag) {
-                    tc_after();
-                    mma_split6(tbase + COL_UPD, smem_u32(sS), S_PIECE, smem_u32(sG), G_PIECE,
-                               idesc_bf16(128, 32));
-                    mma_commit(mb_upd);
-                }
-            }
-            if (last) ph_g ^= 1;
             fence_async_smem();
             tc_before();
-            __syncthreads();  // queries written (and G, eta/alpha inputs)
+            __syncthreads();  // queries written
             tc_after();
             // ---- MMA 2: readout y = q M^m_b^T (six split cross terms) into the q columns
             if (issuer && !*abort_flag) {
@@ -582,7 +582,7 @@ __global__ void __launch_bounds__(NT, 3)
             }
             if (last) {
                 // the 1 x d eta and alpha rows on CUDA cores, in fp32 (lane = column); their
-                // operand rows are not read by the update MMA
+                // operand rows are read by neither pending MMA
                 if (warp == ew) {
                     float ne = 0.0f, na = 0.0f;
 #pragma unroll 8
@@ -613,16 +613,15 @@ __global__ void __launch_bounds__(NT, 3)
                 // new state rows: thread = row (TMEM lane), re-split into the operand pieces.
                 // In the increment form M_b is recovered exactly from its three pieces (their
                 // sum rounds back to the fp32 value they were cut from) and added in fp32.
-                // The readout MMA still reads rows 96..127: those rows are rewritten only
-                // after it completes.
+                // The content rows (96..127) are read by the readout MMA: rewrite them only
+                // after it has completed.
                 float v[32];
                 tmem_ld32(tbase + lrow + COL_UPD, v);
-                const bool add_mb = *delta_form != 0;
-                const bool m_rows = tid >= 3 * D;
-                if (m_rows) {
+                if (tid >= 3 * D) {
                     wt.wait(mb_ro, ph_ro);
                     tc_after();
                 }
+                const bool add_mb = *delta_form != 0;
 #pragma unroll
                 for (int g = 0; g < 4; ++g) {
                     unsigned char *src = sS + op_off(tid, g);
