@@ -259,6 +259,11 @@ __device__ __forceinline__ void mma_split6(uint32_t dt, uint32_t a0, uint32_t a_
                 (t | ks) != 0);
 }
 
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
 __device__ __forceinline__ void red_add_v4(float *addr, float4 v)
 {
     asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr),
@@ -289,9 +294,10 @@ __global__ void __launch_bounds__(NT, 3)
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + OFF_BAR);
     const uint32_t mb_x = smem_u32(&bars[0]), mb_gen = smem_u32(&bars[1]);
     const uint32_t mb_ro = smem_u32(&bars[2]), mb_upd = smem_u32(&bars[3]);
+    const uint32_t mb_g = smem_u32(&bars[4]);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + OFF_BAR + 64);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + OFF_BAR + 72);
-    volatile int *role_slot = reinterpret_cast<volatile int *>(sm + OFF_BAR + 76);
+    volatile int *vote = reinterpret_cast<volatile int *>(sm + OFF_BAR + 96);  // 4 warp flags
     volatile int *delta_form = reinterpret_cast<volatile int *>(sm + OFF_BAR + 80);
     const Waiter wt{abort_flag, a.stats};
 
@@ -309,13 +315,8 @@ __global__ void __launch_bounds__(NT, 3)
         mbar_init(mb_gen, 1);
         mbar_init(mb_ro, 1);
         mbar_init(mb_upd, 1);
+        mbar_init(mb_g, 2);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        // The serial gain loop goes to a warp whose SM sub-partition differs between
-        // co-resident CTAs: CTAs hold consecutive groups of four hardware warp slots,
-        // so the slot group picks the role.
-        unsigned slot;
-        asm volatile("mov.u32 %0, %%warpid;" : "=r"(slot));
-        *role_slot = (int)((slot >> 2) & 3u);
     }
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -333,11 +334,11 @@ __global__ void __launch_bounds__(NT, 3)
             tma_load_4d(smem_u32(sX + q * LBO_X), tm, h * D + 8 * q, box_start(s), line_of(c), b,
                         mb_x);
     };
-    __syncthreads();  // barriers initialised, TMEM address and roles written
-    const int gw = *role_slot;          // gain warp
-    const int mw = (gw + 2) & 3;        // MMA / TMA issuing warp (lane 0)
-    const int ew = (gw + 1) & 3;        // eta / alpha row warp
-    const bool issuer = warp == mw && lane == 0;
+    __syncthreads();  // barriers initialised, TMEM address written
+    // roles: warps 0 and 1 run the gain recurrence, lane 0 of warp 2 issues the MMAs and
+    // TMA copies, warp 3 advances the eta / alpha rows
+    const int ew = 3;
+    const bool issuer = warp == 2 && lane == 0;
     if (issuer) issue_x(0, 0);
     {
         const float *m0 = a.mem0 + ((size_t)r * a.nh + h) * SZ;
@@ -373,10 +374,10 @@ __global__ void __launch_bounds__(NT, 3)
     const float *lam = a.dir_scale ? a.dir_scale + (size_t)r * Cc + (size_t)h * D : nullptr;
     float *ob = a.out + (size_t)b * H * W * Cc + (size_t)h * D;
     unsigned n_spec = 0, n_inj = 0, n_nf = 0;
-    uint32_t ph_x = 0, ph_gen = 0, ph_ro = 0, ph_upd = 0;
+    uint32_t ph_x = 0, ph_gen = 0, ph_ro = 0, ph_upd = 0, ph_g = 0;
 
-    // gain state, lane (row 8w + l/4, columns 8(l%4)..+7) of G = gam * ghat
-    float gh[8];
+    // gain state of warps 0-1: thread t owns row t/2 of G = gam * ghat, columns 16(t%2)..+15
+    float gh[16];
     float gam = 1.0f, inv_gam = 1.0f;
 
     for (int c = 0; c < nlines; ++c) {
@@ -445,6 +446,9 @@ __global__ void __launch_bounds__(NT, 3)
                     n_spec += valid && so.spec_active;
                     n_inj += valid && so.inj_ratio_gt1;
                 }
+                // tokens whose retention could underflow the scaled gain within a few steps
+                const unsigned small = __ballot_sync(0xffffffffu, valid && !(alpha >= 0.01f));
+                if (lane == 0) vote[warp] = small != 0u;
                 if (valid) {
                     float4 *kd = reinterpret_cast<float4 *>(Kf + jr * KS);
                     float4 *dd4 = reinterpret_cast<float4 *>(DLf + jr * KS);
@@ -453,69 +457,100 @@ __global__ void __launch_bounds__(NT, 3)
                         kd[e] = make_float4(kr[4 * e], kr[4 * e + 1], kr[4 * e + 2], kr[4 * e + 3]);
                         dd4[e] = make_float4(vv[4 * e], vv[4 * e + 1], vv[4 * e + 2], vv[4 * e + 3]);
                     }
-                    // coefficients of the scaled gain recurrence (alpha = 0 handled there)
-                    const bool keep = alpha > 1e-30f;
-                    SC[jr] = make_float4(alpha, keep ? eta_t / alpha : eta_t,
-                                         keep ? __frcp_rn(alpha) : 0.0f, 0.0f);
+                    // coefficients of the gain recurrence: (alpha, eta/alpha, 1/alpha, eta) for the
+                    // scaled form, (alpha, 0, 0, eta) where alpha is too small to divide by
+                    const bool keep = alpha >= 1e-6f;
+                    SC[jr] = make_float4(alpha, keep ? eta_t / alpha : 0.0f,
+                                         keep ? __frcp_rn(alpha) : 0.0f, eta_t);
                 }
             }
             tc_before();
             __syncthreads();
             tc_after();
-            // ---- shared gain over this sub-tile's tokens, in route order, on all four warps:
-            // lane l of warp w owns row 8w + l/4 of G and columns 8(l%4) .. 8(l%4)+7, so each
-            // token costs two shuffles and three shared loads per lane.  G = gam * ghat, with
-            //   ghat <- ghat - (eta/alpha) (ghat k + delta / gam) k^T,  gam <- alpha gam
-            // (a pure scaling of G_j = alpha G_{j-1} - eta (G_{j-1} k + delta) k^T), folded
-            // back whenever gam would underflow and restarted when alpha = 0.
-            {
-                const int grow = 8 * warp + (lane >> 2), gq = lane & 3;
+            // queries: normalised, split and written as the readout's A operand (row = box row)
+            auto do_queries = [&]() {
+                float qr[32];
+                tmem_ld32(tbase + lrow + COL_GEN + 64, qr);
+                const float rq = __frsqrt_rn(sumsq32(qr) + a.knorm_eps);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) qr[e] *= rq;
+                if (lane < 16) {
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) store_split8(sQ + op_off(jb, g), Q_PIECE, qr + 8 * g);
+                }
+            };
+            if (warp < 2) {
+                // ---- shared gain over this sub-tile's tokens, in route order, on warps 0-1:
+                // thread t owns row t/2 of G and columns 16(t%2)..16(t%2)+15 (one shuffle per
+                // token).  G = gam * ghat with
+                //   ghat <- ghat - (eta/alpha) (ghat k + delta / gam) k^T,  gam <- alpha gam,
+                // a pure scaling of G_j = alpha G_{j-1} - eta (G_{j-1} k + delta) k^T.  When
+                // every alpha of the sub-tile is >= 0.01 the scale is folded back every eight
+                // tokens (it cannot underflow sooner); otherwise every token is checked, and a
+                // token with alpha < 1e-6 is applied to G directly with the scale folded in.
+                const int grow = tid >> 1, gq = tid & 1;
                 if (s == 0) {
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) gh[e] = (8 * gq + e == grow) ? 1.0f : 0.0f;
+                    for (int e = 0; e < 16; ++e) gh[e] = (16 * gq + e == grow) ? 1.0f : 0.0f;
                     gam = 1.0f;
                     inv_gam = 1.0f;
                 }
-                float4 ka = *reinterpret_cast<const float4 *>(Kf + 8 * gq);
-                float4 kb = *reinterpret_cast<const float4 *>(Kf + 8 * gq + 4);
-                float4 co = SC[0];
-                float dl = DLf[grow];
-                for (int j = 0; j < Lt; ++j) {
-                    const float k[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
-                    const float4 cj = co;
-                    const float dj = dl;
-                    if (j + 1 < Lt) {  // next token's operands
-                        ka = *reinterpret_cast<const float4 *>(Kf + (j + 1) * KS + 8 * gq);
-                        kb = *reinterpret_cast<const float4 *>(Kf + (j + 1) * KS + 8 * gq + 4);
-                        co = SC[j + 1];
-                        dl = DLf[(j + 1) * KS + grow];
+                const bool careful = (vote[0] | vote[1] | vote[2] | vote[3]) != 0;
+                auto token = [&](int j, bool chk) {
+                    float k[16];
+#pragma unroll
+                    for (int e = 0; e < 16; e += 4) {
+                        const float4 f = *reinterpret_cast<const float4 *>(Kf + j * KS + 16 * gq + e);
+                        k[e] = f.x; k[e + 1] = f.y; k[e + 2] = f.z; k[e + 3] = f.w;
                     }
-                    float p0 = gh[0] * k[0], p1 = gh[1] * k[1];
-                    p0 = fmaf(gh[2], k[2], p0);
-                    p1 = fmaf(gh[3], k[3], p1);
-                    p0 = fmaf(gh[4], k[4], p0);
-                    p1 = fmaf(gh[5], k[5], p1);
-                    p0 = fmaf(gh[6], k[6], p0);
-                    p1 = fmaf(gh[7], k[7], p1);
-                    float dot = p0 + p1;
+                    const float4 cj = SC[j];
+                    const float dj = DLf[j * KS + grow];
+                    float p[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) p[e] = gh[e] * k[e];
+#pragma unroll
+                    for (int e = 4; e < 16; ++e) p[e & 3] = fmaf(gh[e], k[e], p[e & 3]);
+                    float dot = (p[0] + p[1]) + (p[2] + p[3]);
                     dot += __shfl_xor_sync(0xffffffffu, dot, 1);
-                    dot += __shfl_xor_sync(0xffffffffu, dot, 2);
-                    if (cj.z != 0.0f) {
+                    if (!chk || cj.z != 0.0f) {
                         const float sc = -cj.y * fmaf(dj, inv_gam, dot);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) gh[e] = fmaf(sc, k[e], gh[e]);
+                        for (int e = 0; e < 16; ++e) gh[e] = fmaf(sc, k[e], gh[e]);
                         gam *= cj.x;
                         inv_gam *= cj.z;
-                        if (gam < 1e-20f) {
+                        if (chk && gam < 1e-20f) {
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) gh[e] *= gam;
+                            for (int e = 0; e < 16; ++e) gh[e] *= gam;
                             gam = 1.0f;
                             inv_gam = 1.0f;
                         }
-                    } else {
-                        const float sc = -cj.y * fmaf(gam, dot, dj);
+                    } else {  // G_j = alpha G_{j-1} - eta (G_{j-1} k + delta) k^T, unscaled
+                        const float sc = -cj.w * fmaf(gam, dot, dj);
+                        const float ag = cj.x * gam;
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) gh[e] = sc * k[e];
+                        for (int e = 0; e < 16; ++e) gh[e] = fmaf(sc, k[e], ag * gh[e]);
+                        gam = 1.0f;
+                        inv_gam = 1.0f;
+                    }
+                };
+                if (careful) {
+                    for (int j = 0; j < Lt; ++j) token(j, true);
+                } else {
+                    int j = 0;
+                    for (; j + 8 <= Lt; j += 8) {
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) token(j + u, false);
+                        if (gam < 1e-20f) {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) gh[e] *= gam;
+                            gam = 1.0f;
+                            inv_gam = 1.0f;
+                        }
+                    }
+                    for (; j < Lt; ++j) token(j, false);
+                    if (gam < 1e-20f) {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) gh[e] *= gam;
                         gam = 1.0f;
                         inv_gam = 1.0f;
                     }
@@ -528,15 +563,16 @@ __global__ void __launch_bounds__(NT, 3)
                     // relative to the change.  Otherwise the state is mostly replaced and the
                     // MMA forms M_b G directly (no cancellation).
                     const bool use_delta = gam >= 0.5f;
-                    float gv[8];
+                    float gv[16];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) gv[e] = gam * gh[e];
-                    float4 *gd = reinterpret_cast<float4 *>(Gf + grow * D + 8 * gq);
-                    gd[0] = make_float4(gv[0], gv[1], gv[2], gv[3]);
-                    gd[1] = make_float4(gv[4], gv[5], gv[6], gv[7]);
+                    for (int e = 0; e < 16; ++e) gv[e] = gam * gh[e];
+                    float4 *gd = reinterpret_cast<float4 *>(Gf + grow * D + 16 * gq);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int cc = 8 * gq + e;
+                    for (int e = 0; e < 4; ++e)
+                        gd[e] = make_float4(gv[4 * e], gv[4 * e + 1], gv[4 * e + 2], gv[4 * e + 3]);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int cc = 16 * gq + e;
                         __nv_bfloat16 p1, p2, p3;
                         split3(gv[e] - ((use_delta && grow == cc) ? 1.0f : 0.0f), p1, p2, p3);
                         unsigned char *d0 = sG + op_off(cc, grow >> 3) + 2 * (grow & 7);
@@ -545,34 +581,28 @@ __global__ void __launch_bounds__(NT, 3)
                         *reinterpret_cast<__nv_bfloat16 *>(d0 + 2 * G_PIECE) = p3;
                     }
                     if (tid == 0) *delta_form = use_delta ? 1 : 0;
+                    fence_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(mb_g);  // this warp's rows of G are ready
+                }
+                do_queries();
+            } else {
+                do_queries();
+                // ---- MMA 3 (chunk end): every d x d memory <- M_b G (six split cross terms,
+                // M = 128 rows), issued as soon as both gain warps have written G
+                if (last && issuer) {
+                    if (wt.wait(mb_g, ph_g) && !*abort_flag) {
+                        tc_after();
+                        mma_split6(tbase + COL_UPD, smem_u32(sS), S_PIECE, smem_u32(sG), G_PIECE,
+                                   idesc_bf16(128, 32));
+                        mma_commit(mb_upd);
+                    }
                 }
             }
+            if (last) ph_g ^= 1;
             fence_async_smem();
             tc_before();
-            __syncthreads();  // G ready (last sub-tile); the gain's reads of the tiles are done
-            tc_after();
-            // ---- MMA 3 (chunk end): every d x d memory <- M_b G (six split cross terms,
-            // M = 128 rows), issued at once; queries and the readout proceed meanwhile
-            if (last && issuer && !*abort_flag) {
-                mma_split6(tbase + COL_UPD, smem_u32(sS), S_PIECE, smem_u32(sG), G_PIECE,
-                           idesc_bf16(128, 32));
-                mma_commit(mb_upd);
-            }
-            // queries: normalised, split and written as the readout's A operand (row = box row)
-            {
-                float qr[32];
-                tmem_ld32(tbase + lrow + COL_GEN + 64, qr);
-                const float rq = __frsqrt_rn(sumsq32(qr) + a.knorm_eps);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) qr[e] *= rq;
-                if (lane < 16) {
-#pragma unroll
-                    for (int g = 0; g < 4; ++g) store_split8(sQ + op_off(jb, g), Q_PIECE, qr + 8 * g);
-                }
-            }
-            fence_async_smem();
-            tc_before();
-            __syncthreads();  // queries written
+            __syncthreads();  // queries written (and G, on the last sub-tile)
             tc_after();
             // ---- MMA 2: readout y = q M^m_b^T (six split cross terms) into the q columns
             if (issuer && !*abort_flag) {
