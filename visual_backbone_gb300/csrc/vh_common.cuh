@@ -54,7 +54,7 @@ __host__ __device__ __forceinline__ int route_chunk(int r, int chunk, int H, int
 
 __device__ __forceinline__ float softplus_f(float s)
 {
-    return fmaxf(s, 0.0f) + log1pf(expf(-fabsf(s)));
+    return fmaxf(s, 0.0f) + log1pf(__expf(-fabsf(s)));
 }
 
 // Per-token scalars of the step-size control (Def. 1, Eqs. (19)-(20)) with
@@ -66,21 +66,24 @@ struct StepOut {
     bool inj_ratio_gt1;  // raw step above the injection limit
 };
 
+// `oma` = 1 - alpha, passed separately so it keeps its relative precision near alpha = 1.
+// Quotients use the hardware reciprocal (a few ulp): far inside the fp32 path's error.
 __device__ __forceinline__ StepOut step_control(const ScanArgs &a, float eta, float alpha,
-                                                float kk, float dd)
+                                                float oma, float kk, float dd)
 {
     StepOut o;
     const float r = sqrtf(dd + a.eps * a.eps) + a.eps;
-    const float eta_inj = a.inj_factor * (1.0f - alpha) / r;
+    const float eta_inj = __fdividef(a.inj_factor * oma, r);
     float eta_bar;
     if (a.control_flags & VH_CTRL_NO_INJ_CAP)
         eta_bar = eta;
     else if (eta_inj > 0.0f)
-        eta_bar = eta_inj * (-expm1f(-eta / eta_inj));
+        eta_bar = eta_inj * (-expm1f(-__fdividef(eta, eta_inj)));
     else
         eta_bar = 0.0f;  // limit of Eq. (19) when the injection limit vanishes
-    float spec = a.spec_factor * 2.0f * alpha / fmaxf(kk, a.kk_floor);
-    spec = nextafterf(spec, 0.0f);
+    float spec = __fdividef(a.spec_factor * 2.0f * alpha, fmaxf(kk, a.kk_floor));
+    // one step toward zero (spec >= 0): the next representable value below
+    if (spec > 0.0f) spec = __int_as_float(__float_as_int(spec) - 1);
     const bool clamp = !(a.control_flags & VH_CTRL_NO_SPEC_CLAMP);
     o.spec_active = clamp && spec < eta_bar;
     o.eta_tilde = o.spec_active ? spec : eta_bar;
@@ -89,15 +92,20 @@ __device__ __forceinline__ StepOut step_control(const ScanArgs &a, float eta, fl
 }
 
 // Raw step and retention from the scalar memory outputs, Eq. (53).
+// Also returns oma = 1 - alpha: for the sigmoid, e / (1 + e) = e alpha with
+// e = exp(-(s + logit alpha_init)), free of the cancellation in 1 - alpha.
 __device__ __forceinline__ void gates(const ScanArgs &a, float s_eta, float s_alpha,
-                                      float &eta, float &alpha)
+                                      float &eta, float &alpha, float &oma)
 {
     if (a.gate_mode == VH_GATE_GENERATED) {
         eta = a.gamma_eta * softplus_f(s_eta + a.eta_bias);
-        alpha = 1.0f / (1.0f + expf(-(s_alpha + a.alpha_logit)));
+        const float e = __expf(-(s_alpha + a.alpha_logit));
+        alpha = __frcp_rn(1.0f + e);
+        oma = alpha > 0.0f ? e * alpha : 1.0f;
     } else {
         eta = a.forced_eta;
         alpha = a.forced_alpha;
+        oma = 1.0f - a.forced_alpha;
     }
 }
 

@@ -169,13 +169,13 @@ __global__ void __launch_bounds__(256) scan_simt_kernel(const ScanArgs a)
                 }
                 kn2 = warp_sum(kn2);
                 dd = warp_sum(dd);
-                float eta, alpha;
-                gates(a, pr[3 * D], pr[3 * D + 1], eta, alpha);
+                float eta, alpha, oma;
+                gates(a, pr[3 * D], pr[3 * D + 1], eta, alpha, oma);
                 float eta_t;
                 if (a.gate_mode == VH_GATE_FORCED_EXEC) {
                     eta_t = a.forced_eta;
                 } else {
-                    const StepOut so = step_control(a, eta, alpha, kn2, dd);
+                    const StepOut so = step_control(a, eta, alpha, oma, kn2, dd);
                     eta_t = so.eta_tilde;
                     n_spec += (lane == 0 && so.spec_active);
                     n_inj += (lane == 0 && so.inj_ratio_gt1);

@@ -47,7 +47,8 @@ constexpr int SBO_K32 = 8 * ROW_B;   // 8-row group stride of a K = 32 operand (
 constexpr int LBO_K32 = 128;         // K-direction core-matrix stride of a K = 32 operand
 constexpr int LBO_X = TT * 16;       // K-direction stride of the TMA-loaded x tile (1 KB)
 constexpr int SBO_X = 128;
-constexpr int KS = D;                // fp32 row stride of the key / delta tiles
+constexpr int KS = D + 4;            // fp32 row stride of the key / delta tiles (padded so the
+                                     // per-token row stores of eight lanes hit distinct banks)
 // One bf16 piece of the state operand: 17 row groups (rows 0..129 used).  The
 // N = 16 generation MMA of the eta/alpha rows also reads rows 130..143, which fall
 // in unused slots or in the next piece: those D columns are never read.
@@ -55,20 +56,30 @@ constexpr int S_PIECE = 17 * SBO_K32;
 constexpr int Q_PIECE = TT * ROW_B;
 constexpr int G_PIECE = D * ROW_B;
 
-constexpr int OFF_X = 0;                          // TT x D bf16 (4 boxes of 1 KB)
-constexpr int OFF_S = OFF_X + TT * D * 2;         // 3 pieces of the state operand
-constexpr int OFF_Q = OFF_S + 3 * S_PIECE;        // 3 pieces x TT x D bf16 queries
+// The M = 128 generation and readout MMAs address their operand 1 KB (x) or 4 KB (each
+// query piece) below the data, so a readable region precedes both.
+constexpr int OFF_S = 0;                                      // 3 pieces of the state operand
+constexpr int OFF_X = (3 * S_PIECE + 1023) / 1024 * 1024;     // TT x D bf16 (4 boxes of 1 KB)
+constexpr int OFF_Q = OFF_X + TT * D * 2;                     // 3 pieces x TT x D bf16 queries
 constexpr int OFF_G = OFF_Q + 3 * Q_PIECE;        // 3 pieces x D x D bf16 gain (B operand)
-constexpr int OFF_GF = OFF_G + 3 * G_PIECE;       // D x D fp32 gain rows
-constexpr int OFF_KF = OFF_GF + D * D * 4;        // TT x KS fp32 keys, route order
+constexpr int GFS = D + 4;                        // fp32 row stride of the gain rows
+constexpr int OFF_GF = OFF_G + 3 * G_PIECE;       // D x GFS fp32 gain rows
+constexpr int OFF_KF = OFF_GF + D * GFS * 4;      // TT x KS fp32 keys, route order
 constexpr int OFF_DL = OFF_KF + TT * KS * 4;      // TT x KS fp32 delta, route order
 constexpr int OFF_SEA = OFF_DL + TT * KS * 4;     // 2 x D fp32 eta / alpha rows of the state
-constexpr int OFF_SC = OFF_SEA + 2 * D * 4;       // TT x {alpha, eta_tilde/alpha, 1/alpha, 0}
-constexpr int OFF_BAR = OFF_SC + TT * 16;         // mbarriers, TMEM base, flags
+constexpr int OFF_SC = OFF_SEA + 2 * D * 4;       // TT x {alpha, eta/alpha, 1/alpha, eta}
+constexpr int NB = 4;                             // tokens per block of the gain recurrence
+static_assert(NB == 4 && TT % 16 == 0, "the block solve is written out for four tokens");
+constexpr int OFF_GT = OFF_SC + TT * 16;          // per block: k_a . k_b, a < b (6 of 8 slots)
+constexpr int OFF_BAR = OFF_GT + TT / NB * 8 * 4; // mbarriers, TMEM base, flags
 constexpr int SMEM_BYTES = OFF_BAR + 128;
 static_assert(SMEM_BYTES <= 75 * 1024, "three CTAs per SM");
 constexpr uint32_t TMEM_COLS = 128;
-constexpr int COL_GEN = 0, COL_GEN2 = 96, COL_RO = 64, COL_UPD = 32;
+// TMEM columns: k_raw | v (M = 64), q_raw then the readout (M = 128), s_eta s_alpha
+// (M = 64), and the update (M = 128) over the consumed v columns.
+constexpr int COL_KV = 0, COL_Q = 64, COL_RO = 64, COL_S = 96, COL_UPD = 32;
+static_assert(OFF_X >= LBO_X && OFF_Q >= 8 * SBO_K32, "operand rows 0..63 stay in shared memory");
+static_assert(OFF_Q + 4 * Q_PIECE <= OFF_BAR, "operand rows 64..127 stay in shared memory");
 
 // ------------------------------------------------------------ PTX wrappers
 
@@ -124,6 +135,9 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t 
     return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
            ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46);
 }
+
+// The descriptor of an operand `bytes` further on (16-byte units in the address field).
+__device__ __forceinline__ uint64_t dadd(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
 
 // Instruction descriptor of kind::f16: bf16 A and B (K-major), fp32 D.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N)
@@ -245,23 +259,28 @@ struct Waiter {
 // Issue the six cross terms (a_i, b_j), i + j <= 2 (pieces counted from 0), of two
 // three-piece K = 32 operands into one accumulator: the product of the 24-bit
 // splits up to terms below 2^-24 relative.
-__device__ __forceinline__ void mma_split6(uint32_t dt, uint32_t a0, uint32_t a_stride,
-                                           uint32_t b0, uint32_t b_stride, uint32_t idesc)
+template <uint32_t A_STRIDE, uint32_t B_STRIDE>
+__device__ __forceinline__ void mma_split6(uint32_t dt, uint32_t a0, uint32_t b0, uint32_t idesc)
 {
     constexpr int pa[6] = {0, 0, 1, 0, 2, 1};
     constexpr int pb[6] = {0, 1, 0, 2, 0, 1};
+    const uint64_t da = sdesc(a0, LBO_K32, SBO_K32), db = sdesc(b0, LBO_K32, SBO_K32);
 #pragma unroll
     for (int t = 0; t < 6; ++t)
 #pragma unroll
         for (int ks = 0; ks < 2; ++ks)
-            mma(dt, sdesc(a0 + pa[t] * a_stride + ks * 2 * LBO_K32, LBO_K32, SBO_K32),
-                sdesc(b0 + pb[t] * b_stride + ks * 2 * LBO_K32, LBO_K32, SBO_K32), idesc,
-                (t | ks) != 0);
+            mma(dt, dadd(da, pa[t] * A_STRIDE + ks * 2 * LBO_K32),
+                dadd(db, pb[t] * B_STRIDE + ks * 2 * LBO_K32), idesc, (t | ks) != 0);
 }
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar)
 {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void named_sync(int id, int n)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
 __device__ __forceinline__ void red_add_v4(float *addr, float4 v)
@@ -298,6 +317,7 @@ __global__ void __launch_bounds__(NT, 3)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + OFF_BAR + 64);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + OFF_BAR + 72);
     volatile int *vote = reinterpret_cast<volatile int *>(sm + OFF_BAR + 96);  // 4 warp flags
+    volatile int *role_slot = reinterpret_cast<volatile int *>(sm + OFF_BAR + 76);
     volatile int *delta_form = reinterpret_cast<volatile int *>(sm + OFF_BAR + 80);
     const Waiter wt{abort_flag, a.stats};
 
@@ -307,6 +327,7 @@ __global__ void __launch_bounds__(NT, 3)
     float *Gf = reinterpret_cast<float *>(sm + OFF_GF);
     float *Sea = reinterpret_cast<float *>(sm + OFF_SEA);
     float4 *SC = reinterpret_cast<float4 *>(sm + OFF_SC);
+    float *GT = reinterpret_cast<float *>(sm + OFF_GT);
 
     // ---- set-up: barriers, TMEM, roles, first TMA, initial state
     if (tid == 0) {
@@ -317,6 +338,12 @@ __global__ void __launch_bounds__(NT, 3)
         mbar_init(mb_upd, 1);
         mbar_init(mb_g, 2);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        // Co-resident CTAs hold consecutive groups of four hardware warp slots, and warp w
+        // of a CTA runs on SM sub-partition w.  Alternating the gain pair between warps 0-1
+        // and 2-3 by slot group spreads the serial recurrences over the sub-partitions.
+        unsigned slot;
+        asm volatile("mov.u32 %0, %%warpid;" : "=r"(slot));
+        *role_slot = (int)((slot >> 2) & 1u);
     }
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -334,11 +361,15 @@ __global__ void __launch_bounds__(NT, 3)
             tma_load_4d(smem_u32(sX + q * LBO_X), tm, h * D + 8 * q, box_start(s), line_of(c), b,
                         mb_x);
     };
-    __syncthreads();  // barriers initialised, TMEM address written
-    // roles: warps 0 and 1 run the gain recurrence, lane 0 of warp 2 issues the MMAs and
-    // TMA copies, warp 3 advances the eta / alpha rows
-    const int ew = 3;
-    const bool issuer = warp == 2 && lane == 0;
+    __syncthreads();  // barriers initialised, TMEM address and roles written
+    // roles: warps 2gp, 2gp+1 run the gain recurrence; the other pair (first warp rw) holds
+    // the queries and readouts in TMEM lanes 32 rw..32 rw+63, issues the MMAs and TMA copies
+    // (lane 0 of warp rw) and advances the eta / alpha rows (warp rw + 1)
+    const int gp = *role_slot;
+    const int rw = 2 - 2 * gp;
+    const bool gainw = (warp >> 1) == gp;
+    const int ew = rw + 1;
+    const bool issuer = warp == rw && lane == 0;
     if (issuer) issue_x(0, 0);
     {
         const float *m0 = a.mem0 + ((size_t)r * a.nh + h) * SZ;
@@ -389,21 +420,31 @@ __global__ void __launch_bounds__(NT, 3)
             const int jb = 16 * warp + lane;   // box row (M = 64 layout: lanes 32w..32w+15)
             const int p = box_start(s) + jb;   // position along the line
             const bool valid = lane < 16 && p >= 0 && p < Lline;
-            // ---- MMA 1: generation from the boundary state (x exact in bf16: 3 passes)
+            // ---- MMA 1: generation from the boundary state (x exact in bf16: 3 passes).
+            // k_raw, v and s_eta, s_alpha use M = 64 (box row j -> lane 32(j/16) + j%16, read
+            // by all four warps); q_raw uses M = 128 with the x tile as rows 32 rw..32 rw+63
+            // (lane 32 rw + j, read by the readout warps), the other 64 A rows reading the
+            // kilobyte next to the tile into TMEM lanes nobody reads.
             if (issuer) {
                 tc_after();
                 if (wt.wait(mb_x, ph_x) && !*abort_flag) {
-                    const uint32_t xa = smem_u32(sX), s0 = smem_u32(sS);
-                    const uint32_t id96 = idesc_bf16(64, 96), id16 = idesc_bf16(64, 16);
+                    const uint32_t xa = smem_u32(sX);
+                    const uint32_t id64 = idesc_bf16(64, 64), id16 = idesc_bf16(64, 16);
+                    const uint32_t idq = idesc_bf16(128, 32);
+                    const uint64_t dx = sdesc(xa, LBO_X, SBO_X);
+                    const uint64_t dq = sdesc(xa - (rw >> 1) * LBO_X, LBO_X, SBO_X);
+                    const uint64_t ds = sdesc(smem_u32(sS), LBO_K32, SBO_K32);
 #pragma unroll
                     for (int pc = 0; pc < 3; ++pc) {
 #pragma unroll
                         for (int ks = 0; ks < 2; ++ks) {
-                            const uint64_t ad = sdesc(xa + ks * 2 * LBO_X, LBO_X, SBO_X);
-                            const uint32_t sb = s0 + pc * S_PIECE + ks * 2 * LBO_K32;
-                            mma(tbase + COL_GEN, ad, sdesc(sb, LBO_K32, SBO_K32), id96, (pc | ks) != 0);
-                            mma(tbase + COL_GEN2, ad, sdesc(sb + 16 * SBO_K32, LBO_K32, SBO_K32), id16,
-                                (pc | ks) != 0);
+                            const uint32_t acc = (pc | ks) != 0;
+                            const uint32_t ob = pc * S_PIECE + ks * 2 * LBO_K32;
+                            mma(tbase + COL_KV, dadd(dx, ks * 2 * LBO_X), dadd(ds, ob), id64, acc);
+                            mma(tbase + COL_Q, dadd(dq, ks * 2 * LBO_X), dadd(ds, ob + 8 * SBO_K32), idq,
+                                acc);
+                            mma(tbase + COL_S, dadd(dx, ks * 2 * LBO_X), dadd(ds, ob + 16 * SBO_K32), id16,
+                                acc);
                         }
                     }
                     mma_commit(mb_gen);
@@ -424,10 +465,10 @@ __global__ void __launch_bounds__(NT, 3)
                 const int tr = rev ? Lline - 1 - p : p;  // token index inside the chunk
                 const int jr = tr - t0;                  // route-ordered index inside the sub-tile
                 float kr[32], vv[32];
-                tmem_ld32(tbase + lrow + COL_GEN, kr);
-                tmem_ld32(tbase + lrow + COL_GEN + 32, vv);
+                tmem_ld32(tbase + lrow + COL_KV, kr);
+                tmem_ld32(tbase + lrow + COL_KV + 32, vv);
                 float se, sa;
-                tmem_ld2(tbase + lrow + COL_GEN2, se, sa);
+                tmem_ld2(tbase + lrow + COL_S, se, sa);
                 const float rk = __frsqrt_rn(sumsq32(kr) + a.knorm_eps);
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
@@ -435,13 +476,13 @@ __global__ void __launch_bounds__(NT, 3)
                     vv[e] = kr[e] - vv[e];  // delta = k - v
                 }
                 const float kn2 = sumsq32(kr), dd2 = sumsq32(vv);
-                float eta, alpha;
-                gates(a, se, sa, eta, alpha);
+                float eta, alpha, oma;
+                gates(a, se, sa, eta, alpha, oma);
                 float eta_t;
                 if (a.gate_mode == VH_GATE_FORCED_EXEC) {
                     eta_t = a.forced_eta;
                 } else {
-                    const StepOut so = step_control(a, eta, alpha, kn2, dd2);
+                    const StepOut so = step_control(a, eta, alpha, oma, kn2, dd2);
                     eta_t = so.eta_tilde;
                     n_spec += valid && so.spec_active;
                     n_inj += valid && so.inj_ratio_gt1;
@@ -460,35 +501,46 @@ __global__ void __launch_bounds__(NT, 3)
                     // coefficients of the gain recurrence: (alpha, eta/alpha, 1/alpha, eta) for the
                     // scaled form, (alpha, 0, 0, eta) where alpha is too small to divide by
                     const bool keep = alpha >= 1e-6f;
-                    SC[jr] = make_float4(alpha, keep ? eta_t / alpha : 0.0f,
+                    SC[jr] = make_float4(alpha, keep ? __fdividef(eta_t, alpha) : 0.0f,
                                          keep ? __frcp_rn(alpha) : 0.0f, eta_t);
+                }
+                // Gram entries k_a . k_b of each block of NB route-ordered tokens.  This
+                // warp's tokens are the 16 consecutive route rows from R0 (route order runs
+                // with the box rows forwards, against them backwards), four whole blocks:
+                // lane 6q + i takes pair i of block q.
+                __syncwarp();
+                if (lane < 24) {
+                    const int R0 = rev ? TT - 16 - 16 * warp : 16 * warp;
+                    const int q = lane / 6, pi = lane - 6 * q;
+                    const int ia = pi < 3 ? 0 : (pi < 5 ? 1 : 2);
+                    const int ib = pi < 3 ? pi + 1 : (pi < 5 ? pi - 1 : 3);
+                    const float4 *ka = reinterpret_cast<const float4 *>(Kf + (R0 + NB * q + ia) * KS);
+                    const float4 *kb = reinterpret_cast<const float4 *>(Kf + (R0 + NB * q + ib) * KS);
+                    float g4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float4 fa = ka[e], fb = kb[e];
+                        g4[0] = fmaf(fa.x, fb.x, g4[0]);
+                        g4[1] = fmaf(fa.y, fb.y, g4[1]);
+                        g4[2] = fmaf(fa.z, fb.z, g4[2]);
+                        g4[3] = fmaf(fa.w, fb.w, g4[3]);
+                    }
+                    GT[(R0 / NB + q) * 8 + pi] = (g4[0] + g4[1]) + (g4[2] + g4[3]);
                 }
             }
             tc_before();
             __syncthreads();
             tc_after();
-            // queries: normalised, split and written as the readout's A operand (row = box row)
-            auto do_queries = [&]() {
-                float qr[32];
-                tmem_ld32(tbase + lrow + COL_GEN + 64, qr);
-                const float rq = __frsqrt_rn(sumsq32(qr) + a.knorm_eps);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) qr[e] *= rq;
-                if (lane < 16) {
-#pragma unroll
-                    for (int g = 0; g < 4; ++g) store_split8(sQ + op_off(jb, g), Q_PIECE, qr + 8 * g);
-                }
-            };
-            if (warp < 2) {
-                // ---- shared gain over this sub-tile's tokens, in route order, on warps 0-1:
-                // thread t owns row t/2 of G and columns 16(t%2)..16(t%2)+15 (one shuffle per
-                // token).  G = gam * ghat with
+            if (gainw) {
+                // ---- shared gain over this sub-tile's tokens, in route order, on the gain
+                // pair: its thread t owns row t/2 of G and columns 16(t%2)..16(t%2)+15 (one
+                // shuffle per token).  G = gam * ghat with
                 //   ghat <- ghat - (eta/alpha) (ghat k + delta / gam) k^T,  gam <- alpha gam,
                 // a pure scaling of G_j = alpha G_{j-1} - eta (G_{j-1} k + delta) k^T.  When
                 // every alpha of the sub-tile is >= 0.01 the scale is folded back every eight
                 // tokens (it cannot underflow sooner); otherwise every token is checked, and a
                 // token with alpha < 1e-6 is applied to G directly with the scale folded in.
-                const int grow = tid >> 1, gq = tid & 1;
+                const int grow = (tid & 63) >> 1, gq = tid & 1;
                 if (s == 0) {
 #pragma unroll
                     for (int e = 0; e < 16; ++e) gh[e] = (16 * gq + e == grow) ? 1.0f : 0.0f;
@@ -496,128 +548,226 @@ __global__ void __launch_bounds__(NT, 3)
                     inv_gam = 1.0f;
                 }
                 const bool careful = (vote[0] | vote[1] | vote[2] | vote[3]) != 0;
-                auto token = [&](int j, bool chk) {
+                // operands of token j (key half, coefficients, delta entry); the next token's
+                // are loaded before the current one is applied, off the serial chain
+                struct Tok {
                     float k[16];
+                    float4 c;
+                    float d;
+                };
+                auto load = [&](int j, Tok &t) {
 #pragma unroll
                     for (int e = 0; e < 16; e += 4) {
                         const float4 f = *reinterpret_cast<const float4 *>(Kf + j * KS + 16 * gq + e);
-                        k[e] = f.x; k[e + 1] = f.y; k[e + 2] = f.z; k[e + 3] = f.w;
+                        t.k[e] = f.x; t.k[e + 1] = f.y; t.k[e + 2] = f.z; t.k[e + 3] = f.w;
                     }
-                    const float4 cj = SC[j];
-                    const float dj = DLf[j * KS + grow];
-                    float p[4];
+                    t.c = SC[j];
+                    t.d = DLf[j * KS + grow];
+                };
+                auto fold = [&]() {
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) p[e] = gh[e] * k[e];
+                    for (int e = 0; e < 16; ++e) gh[e] *= gam;
+                    gam = 1.0f;
+                    inv_gam = 1.0f;
+                };
+                auto apply = [&](const Tok &t, bool chk) {
+                    float p4[4];
 #pragma unroll
-                    for (int e = 4; e < 16; ++e) p[e & 3] = fmaf(gh[e], k[e], p[e & 3]);
-                    float dot = (p[0] + p[1]) + (p[2] + p[3]);
+                    for (int e = 0; e < 4; ++e) p4[e] = gh[e] * t.k[e];
+#pragma unroll
+                    for (int e = 4; e < 16; ++e) p4[e & 3] = fmaf(gh[e], t.k[e], p4[e & 3]);
+                    float dot = (p4[0] + p4[1]) + (p4[2] + p4[3]);
                     dot += __shfl_xor_sync(0xffffffffu, dot, 1);
-                    if (!chk || cj.z != 0.0f) {
-                        const float sc = -cj.y * fmaf(dj, inv_gam, dot);
+                    if (!chk || t.c.z != 0.0f) {
+                        const float sc = -t.c.y * fmaf(t.d, inv_gam, dot);
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) gh[e] = fmaf(sc, k[e], gh[e]);
-                        gam *= cj.x;
-                        inv_gam *= cj.z;
-                        if (chk && gam < 1e-20f) {
-#pragma unroll
-                            for (int e = 0; e < 16; ++e) gh[e] *= gam;
-                            gam = 1.0f;
-                            inv_gam = 1.0f;
-                        }
+                        for (int e = 0; e < 16; ++e) gh[e] = fmaf(sc, t.k[e], gh[e]);
+                        gam *= t.c.x;
+                        inv_gam *= t.c.z;
+                        if (chk && gam < 1e-20f) fold();
                     } else {  // G_j = alpha G_{j-1} - eta (G_{j-1} k + delta) k^T, unscaled
-                        const float sc = -cj.w * fmaf(gam, dot, dj);
-                        const float ag = cj.x * gam;
+                        const float sc = -t.c.w * fmaf(gam, dot, t.d);
+                        const float ag = t.c.x * gam;
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) gh[e] = fmaf(sc, k[e], ag * gh[e]);
+                        for (int e = 0; e < 16; ++e) gh[e] = fmaf(sc, t.k[e], ag * gh[e]);
                         gam = 1.0f;
                         inv_gam = 1.0f;
                     }
                 };
+                // rows Lt..TT-1 of the tiles hold stale values: a prefetch past the last token
+                // reads one and never applies it
                 if (careful) {
-                    for (int j = 0; j < Lt; ++j) token(j, true);
+                    Tok ta, tb;
+                    load(0, ta);
+                    for (int j = 0; j < Lt; j += 2) {
+                        load(min(j + 1, TT - 1), tb);
+                        apply(ta, true);
+                        if (j + 1 >= Lt) break;
+                        load(min(j + 2, TT - 1), ta);
+                        apply(tb, true);
+                    }
                 } else {
+                    // blocks of NB tokens: with a = ghat_0 . k_j for the block's starting ghat,
+                    //   ghat_{j-1} . k_j = a_j + sum_{i<j in block} sc_i (k_i . k_j),
+                    // so the NB dot products are independent, the serial part is an NB-step
+                    // scalar solve, and ghat takes one rank-NB update.
                     int j = 0;
-                    for (; j + 8 <= Lt; j += 8) {
+                    for (; j + NB <= Lt; j += NB) {
+                        float kb[NB][16];
+                        float4 cb[NB];
+                        float db[NB];
 #pragma unroll
-                        for (int u = 0; u < 8; ++u) token(j + u, false);
-                        if (gam < 1e-20f) {
+                        for (int t = 0; t < NB; ++t) {
 #pragma unroll
-                            for (int e = 0; e < 16; ++e) gh[e] *= gam;
-                            gam = 1.0f;
-                            inv_gam = 1.0f;
+                            for (int e = 0; e < 16; e += 4) {
+                                const float4 f =
+                                    *reinterpret_cast<const float4 *>(Kf + (j + t) * KS + 16 * gq + e);
+                                kb[t][e] = f.x; kb[t][e + 1] = f.y; kb[t][e + 2] = f.z; kb[t][e + 3] = f.w;
+                            }
+                            cb[t] = SC[j + t];
+                            db[t] = DLf[(j + t) * KS + grow];
                         }
-                    }
-                    for (; j < Lt; ++j) token(j, false);
-                    if (gam < 1e-20f) {
+                        const float4 g0 = *reinterpret_cast<const float4 *>(GT + (j / NB) * 8);
+                        const float2 g1 = *reinterpret_cast<const float2 *>(GT + (j / NB) * 8 + 4);
+                        float av[NB];
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) gh[e] *= gam;
-                        gam = 1.0f;
-                        inv_gam = 1.0f;
+                        for (int t = 0; t < NB; ++t) {
+                            float p0 = gh[0] * kb[t][0], p1 = gh[1] * kb[t][1];
+#pragma unroll
+                            for (int e = 2; e < 16; e += 2) {
+                                p0 = fmaf(gh[e], kb[t][e], p0);
+                                p1 = fmaf(gh[e + 1], kb[t][e + 1], p1);
+                            }
+                            av[t] = p0 + p1;
+                        }
+#pragma unroll
+                        for (int t = 0; t < NB; ++t) av[t] += __shfl_xor_sync(0xffffffffu, av[t], 1);
+                        float iv = inv_gam;
+                        const float s0 = -cb[0].y * fmaf(db[0], iv, av[0]);
+                        iv *= cb[0].z;
+                        const float s1 = -cb[1].y * (fmaf(db[1], iv, av[1]) + s0 * g0.x);
+                        iv *= cb[1].z;
+                        const float s2 = -cb[2].y * (fmaf(db[2], iv, av[2]) + fmaf(s1, g0.w, s0 * g0.y));
+                        iv *= cb[2].z;
+                        const float s3 =
+                            -cb[3].y * (fmaf(db[3], iv, av[3]) + fmaf(s2, g1.y, fmaf(s1, g1.x, s0 * g0.z)));
+                        iv *= cb[3].z;
+                        inv_gam = iv;
+                        gam *= (cb[0].x * cb[1].x) * (cb[2].x * cb[3].x);
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            gh[e] = fmaf(s3, kb[3][e],
+                                         fmaf(s2, kb[2][e], fmaf(s1, kb[1][e], fmaf(s0, kb[0][e], gh[e]))));
+                        if (gam < 1e-20f) fold();
                     }
+                    for (; j < Lt; ++j) {
+                        Tok t;
+                        load(j, t);
+                        apply(t, false);
+                    }
+                    if (gam < 1e-20f) fold();
                 }
                 if (last) {
-                    // G rows in fp32, and G as the update's B operand (row n = column of G,
-                    // K = row of G).  When the chunk retains at least half of the state the
-                    // operand is G - I: the MMA forms only the increment M_b (G - I), which the
-                    // epilogue adds to M_b in fp32, so the tensor core's accumulation error is
-                    // relative to the change.  Otherwise the state is mostly replaced and the
-                    // MMA forms M_b G directly (no cancellation).
-                    const bool use_delta = gam >= 0.5f;
-                    float gv[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) gv[e] = gam * gh[e];
-                    float4 *gd = reinterpret_cast<float4 *>(Gf + grow * D + 16 * gq);
+                    // G = gam * ghat in fp32 rows for the readout pair, which casts it as the
+                    // update's operand
+                    float4 *gd = reinterpret_cast<float4 *>(Gf + grow * GFS + 16 * gq);
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
-                        gd[e] = make_float4(gv[4 * e], gv[4 * e + 1], gv[4 * e + 2], gv[4 * e + 3]);
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const int cc = 16 * gq + e;
-                        __nv_bfloat16 p1, p2, p3;
-                        split3(gv[e] - ((use_delta && grow == cc) ? 1.0f : 0.0f), p1, p2, p3);
-                        unsigned char *d0 = sG + op_off(cc, grow >> 3) + 2 * (grow & 7);
-                        *reinterpret_cast<__nv_bfloat16 *>(d0) = p1;
-                        *reinterpret_cast<__nv_bfloat16 *>(d0 + G_PIECE) = p2;
-                        *reinterpret_cast<__nv_bfloat16 *>(d0 + 2 * G_PIECE) = p3;
-                    }
-                    if (tid == 0) *delta_form = use_delta ? 1 : 0;
-                    fence_async_smem();
+                        gd[e] = make_float4(gam * gh[4 * e], gam * gh[4 * e + 1], gam * gh[4 * e + 2],
+                                            gam * gh[4 * e + 3]);
+                    if ((tid & 63) == 0) *delta_form = gam >= 0.5f ? 1 : 0;
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(mb_g);  // this warp's rows of G are ready
+                    if (lane == 0) mbar_arrive(mb_g);  // this warp's rows of G are written
                 }
-                do_queries();
             } else {
-                do_queries();
+                // ---- the readout pair, while the gain runs: queries and the readout of this
+                // sub-tile.  Lane l of warp w holds box row j = 32(w - rw) + l (TMEM lane
+                // 32 rw + j).
+                const int jq = 32 * (warp - rw) + lane;
+                {
+                    float qr[32];
+                    tmem_ld32(tbase + lrow + COL_Q, qr);
+                    const float rq = __frsqrt_rn(sumsq32(qr) + a.knorm_eps);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) qr[e] *= rq;
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) store_split8(sQ + op_off(jq, g), Q_PIECE, qr + 8 * g);
+                }
+                fence_async_smem();
+                tc_before();
+                named_sync(1, 64);
+                tc_after();
+                // MMA 2: readout y = q M^m_b^T (six split cross terms), M = 128 with the
+                // queries as rows 32 rw..32 rw+63 (the other 64 A rows read the 4 KB next
+                // to each piece)
+                if (issuer && !*abort_flag) {
+                    mma_split6<Q_PIECE, S_PIECE>(tbase + COL_RO, smem_u32(sQ) - (rw >> 1) * 8 * SBO_K32,
+                                                 smem_u32(sS) + 12 * SBO_K32, idesc_bf16(128, 32));
+                    mma_commit(mb_ro);
+                }
+                wt.wait(mb_ro, ph_ro);
+                tc_after();
+                // readout epilogue: lambda_r y added at the token's pixel (Eq. (26))
+                float y[32];
+                tmem_ld32(tbase + lrow + COL_RO, y);
+                const int pq = box_start(s) + jq;
+                if (pq >= 0 && pq < Lline) {
+                    const int pix = rowr ? Lidx * W + pq : pq * W + Lidx;
+                    float *dst = ob + (size_t)pix * Cc;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        float4 v4 = make_float4(y[4 * e], y[4 * e + 1], y[4 * e + 2], y[4 * e + 3]);
+                        if (lam) {
+                            v4.x *= lam[4 * e]; v4.y *= lam[4 * e + 1];
+                            v4.z *= lam[4 * e + 2]; v4.w *= lam[4 * e + 3];
+                        }
+                        n_nf += !isfinite(v4.x) + !isfinite(v4.y) + !isfinite(v4.z) + !isfinite(v4.w);
+                        red_add_v4(dst + 4 * e, v4);
+                    }
+                }
                 // ---- MMA 3 (chunk end): every d x d memory <- M_b G (six split cross terms,
-                // M = 128 rows), issued as soon as both gain warps have written G
-                if (last && issuer) {
-                    if (wt.wait(mb_g, ph_g) && !*abort_flag) {
-                        tc_after();
-                        mma_split6(tbase + COL_UPD, smem_u32(sS), S_PIECE, smem_u32(sG), G_PIECE,
-                                   idesc_bf16(128, 32));
+                // M = 128 rows), issued as soon as G is cast.  G is the B operand (row n =
+                // column of G, K = row of G), three bf16 pieces.  When the chunk retains at
+                // least half of the state the operand is G - I: the MMA forms only the
+                // increment M_b (G - I), which the epilogue adds to M_b in fp32, so the tensor
+                // core's accumulation error is relative to the change.  Otherwise the state is
+                // mostly replaced and the MMA forms M_b G directly (no cancellation).
+                if (last) {
+                    wt.wait(mb_g, ph_g);
+                    const bool use_delta = *delta_form != 0;
+#pragma unroll
+                    for (int tk = jq; tk < 4 * D; tk += 64) {
+                        const int n = tk & (D - 1), g = tk / D;
+                        float v[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            v[i] = Gf[(8 * g + i) * GFS + n] - ((use_delta && 8 * g + i == n) ? 1.0f : 0.0f);
+                        store_split8(sG + op_off(n, g), G_PIECE, v);
+                    }
+                    fence_async_smem();
+                    tc_before();
+                    named_sync(1, 64);
+                    tc_after();
+                    if (issuer && !*abort_flag) {
+                        mma_split6<S_PIECE, G_PIECE>(tbase + COL_UPD, smem_u32(sS), smem_u32(sG),
+                                                     idesc_bf16(128, 32));
                         mma_commit(mb_upd);
                     }
                 }
             }
-            if (last) ph_g ^= 1;
-            fence_async_smem();
-            tc_before();
-            __syncthreads();  // queries written (and G, on the last sub-tile)
-            tc_after();
-            // ---- MMA 2: readout y = q M^m_b^T (six split cross terms) into the q columns
-            if (issuer && !*abort_flag) {
-                mma_split6(tbase + COL_RO, smem_u32(sQ), Q_PIECE, smem_u32(sS) + 12 * SBO_K32, S_PIECE,
-                           idesc_bf16(64, 32));
-                mma_commit(mb_ro);
-            }
+            ph_ro ^= 1;
             if (last) {
+                ph_g ^= 1;
+                tc_before();
+                __syncthreads();  // G and its fp32 rows written, readout complete
+                tc_after();
                 // the 1 x d eta and alpha rows on CUDA cores, in fp32 (lane = column); their
-                // operand rows are read by neither pending MMA
+                // operand rows are read by no pending MMA
                 if (warp == ew) {
                     float ne = 0.0f, na = 0.0f;
 #pragma unroll 8
                     for (int l = 0; l < D; ++l) {
-                        const float gv = Gf[l * D + lane];
+                        const float gv = Gf[l * GFS + lane];
                         ne = fmaf(Sea[l], gv, ne);
                         na = fmaf(Sea[D + l], gv, na);
                     }
@@ -643,14 +793,8 @@ __global__ void __launch_bounds__(NT, 3)
                 // new state rows: thread = row (TMEM lane), re-split into the operand pieces.
                 // In the increment form M_b is recovered exactly from its three pieces (their
                 // sum rounds back to the fp32 value they were cut from) and added in fp32.
-                // The content rows (96..127) are read by the readout MMA: rewrite them only
-                // after it has completed.
                 float v[32];
                 tmem_ld32(tbase + lrow + COL_UPD, v);
-                if (tid >= 3 * D) {
-                    wt.wait(mb_ro, ph_ro);
-                    tc_after();
-                }
                 const bool add_mb = *delta_form != 0;
 #pragma unroll
                 for (int g = 0; g < 4; ++g) {
@@ -677,28 +821,6 @@ __global__ void __launch_bounds__(NT, 3)
                         d4[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
                 }
             }
-            // ---- readout epilogue: lambda_r y added at the token's pixel (Eq. (26))
-            {
-                wt.wait(mb_ro, ph_ro);
-                tc_after();
-                float y[32];
-                tmem_ld32(tbase + lrow + COL_RO, y);
-                if (valid) {
-                    const int pix = rowr ? Lidx * W + p : p * W + Lidx;
-                    float *dst = ob + (size_t)pix * Cc;
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        float4 v4 = make_float4(y[4 * e], y[4 * e + 1], y[4 * e + 2], y[4 * e + 3]);
-                        if (lam) {
-                            v4.x *= lam[4 * e]; v4.y *= lam[4 * e + 1];
-                            v4.z *= lam[4 * e + 2]; v4.w *= lam[4 * e + 3];
-                        }
-                        n_nf += !isfinite(v4.x) + !isfinite(v4.y) + !isfinite(v4.z) + !isfinite(v4.w);
-                        red_add_v4(dst + 4 * e, v4);
-                    }
-                }
-            }
-            ph_ro ^= 1;
             fence_async_smem();
             tc_before();
             __syncthreads();  // end of sub-tile: operands rewritten, TMEM consumed
