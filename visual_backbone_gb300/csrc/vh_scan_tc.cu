@@ -49,10 +49,11 @@ constexpr int LBO_X = TT * 16;       // K-direction stride of the TMA-loaded x t
 constexpr int SBO_X = 128;
 constexpr int KS = D + 4;            // fp32 row stride of the key / delta tiles (padded so the
                                      // per-token row stores of eight lanes hit distinct banks)
-// One bf16 piece of the state operand: 17 row groups (rows 0..129 used).  The
-// N = 16 generation MMA of the eta/alpha rows also reads rows 130..143, which fall
-// in unused slots or in the next piece: those D columns are never read.
-constexpr int S_PIECE = 17 * SBO_K32;
+// One bf16 piece of the state operand, 144 rows: eta, alpha, 14 zero rows, then the k, v,
+// q and content memories (32 rows each).  The generation reads rows 0..111 as one B
+// operand, the update rows 16..143 as one A operand, the readout rows 112..143.
+constexpr int ROW_ETA = 0, ROW_MEM = 16, S_ROWS = ROW_MEM + 4 * D;
+constexpr int S_PIECE = S_ROWS / 8 * SBO_K32;
 constexpr int Q_PIECE = TT * ROW_B;
 constexpr int G_PIECE = D * ROW_B;
 
@@ -75,9 +76,11 @@ constexpr int OFF_BAR = OFF_GT + TT / NB * 8 * 4; // mbarriers, TMEM base, flags
 constexpr int SMEM_BYTES = OFF_BAR + 128;
 static_assert(SMEM_BYTES <= 75 * 1024, "three CTAs per SM");
 constexpr uint32_t TMEM_COLS = 128;
-// TMEM columns: k_raw | v (M = 64), q_raw then the readout (M = 128), s_eta s_alpha
-// (M = 64), and the update (M = 128) over the consumed v columns.
-constexpr int COL_KV = 0, COL_Q = 64, COL_RO = 64, COL_S = 96, COL_UPD = 32;
+// TMEM columns (all M = 128): the generation [s_eta s_alpha 0.. | k_raw | v | q_raw] at
+// 0..111 (COL_K, COL_V, COL_QR relative), then the readout over the consumed gate and
+// key columns and the update's three 32-column blocks over the rest.
+constexpr int COL_GEN = 0, COL_K = ROW_MEM, COL_V = ROW_MEM + D, COL_QR = ROW_MEM + 2 * D;
+constexpr int COL_RO = 0, COL_UPD = 32;
 static_assert(OFF_X >= LBO_X && OFF_Q >= 8 * SBO_K32, "operand rows 0..63 stay in shared memory");
 static_assert(OFF_Q + 4 * Q_PIECE <= OFF_BAR, "operand rows 64..127 stay in shared memory");
 
@@ -296,7 +299,6 @@ __global__ void __launch_bounds__(NT, 3)
 {
     extern __shared__ __align__(1024) unsigned char sm[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-
     int id = blockIdx.x;
     const int h = id % a.nh;
     id /= a.nh;
@@ -316,9 +318,9 @@ __global__ void __launch_bounds__(NT, 3)
     const uint32_t mb_g = smem_u32(&bars[4]);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + OFF_BAR + 64);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + OFF_BAR + 72);
-    volatile int *vote = reinterpret_cast<volatile int *>(sm + OFF_BAR + 96);  // 4 warp flags
     volatile int *role_slot = reinterpret_cast<volatile int *>(sm + OFF_BAR + 76);
     volatile int *delta_form = reinterpret_cast<volatile int *>(sm + OFF_BAR + 80);
+    volatile int *vote = reinterpret_cast<volatile int *>(sm + OFF_BAR + 96);  // 2 warp flags
     const Waiter wt{abort_flag, a.stats};
 
     unsigned char *sX = sm + OFF_X, *sS = sm + OFF_S, *sQ = sm + OFF_Q, *sG = sm + OFF_G;
@@ -362,9 +364,11 @@ __global__ void __launch_bounds__(NT, 3)
                         mb_x);
     };
     __syncthreads();  // barriers initialised, TMEM address and roles written
-    // roles: warps 2gp, 2gp+1 run the gain recurrence; the other pair (first warp rw) holds
-    // the queries and readouts in TMEM lanes 32 rw..32 rw+63, issues the MMAs and TMA copies
-    // (lane 0 of warp rw) and advances the eta / alpha rows (warp rw + 1)
+    // roles: warps 2gp, 2gp+1 run the gain recurrence.  The other pair (first warp rw) holds
+    // the tokens: every generated quantity and the readout land in its TMEM lanes
+    // 32 rw..32 rw+63, so it runs the per-token step (phase 1), the queries and the readout;
+    // lane 0 of warp rw issues the MMAs and TMA copies, warp rw + 1 advances the eta / alpha
+    // rows.
     const int gp = *role_slot;
     const int rw = 2 - 2 * gp;
     const bool gainw = (warp >> 1) == gp;
@@ -373,7 +377,7 @@ __global__ void __launch_bounds__(NT, 3)
     if (issuer) issue_x(0, 0);
     {
         const float *m0 = a.mem0 + ((size_t)r * a.nh + h) * SZ;
-        // rows 0..127 (k, v, q, m): thread = row
+        // memory rows 0..127 (k, v, q, m) -> operand rows 16..143: thread = row
         float v[32];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
@@ -381,17 +385,16 @@ __global__ void __launch_bounds__(NT, 3)
             v[4 * e] = f.x; v[4 * e + 1] = f.y; v[4 * e + 2] = f.z; v[4 * e + 3] = f.w;
         }
 #pragma unroll
-        for (int g = 0; g < 4; ++g) store_split8(sS + op_off(tid, g), S_PIECE, v + 8 * g);
-        // eta / alpha rows: fp32 copy and operand rows 128, 129
+        for (int g = 0; g < 4; ++g) store_split8(sS + op_off(ROW_MEM + tid, g), S_PIECE, v + 8 * g);
+        // eta / alpha rows: fp32 copy and operand rows 0, 1; rows 2..15 are zero
         if (tid < 2 * D) Sea[tid] = m0[4 * D * D + tid];
-        if (tid < 2) {
-            const int row = 128 + tid;
+        if (tid < ROW_MEM) {
             float z[8];
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) z[e] = m0[4 * D * D + tid * D + 8 * g + e];
-                store_split8(sS + op_off(row, g), S_PIECE, z);
+                for (int e = 0; e < 8; ++e) z[e] = tid < 2 ? m0[4 * D * D + tid * D + 8 * g + e] : 0.0f;
+                store_split8(sS + op_off(tid, g), S_PIECE, z);
             }
         }
     }
@@ -407,9 +410,13 @@ __global__ void __launch_bounds__(NT, 3)
     unsigned n_spec = 0, n_inj = 0, n_nf = 0;
     uint32_t ph_x = 0, ph_gen = 0, ph_ro = 0, ph_upd = 0, ph_g = 0;
 
-    // gain state of warps 0-1: thread t owns row t/2 of G = gam * ghat, columns 16(t%2)..+15
+    // gain state of the gain pair: its thread t owns row t/2 of G = gam * ghat, columns
+    // 16(t%2)..+15
     float gh[16];
     float gam = 1.0f, inv_gam = 1.0f;
+    // this thread's token (box row) when in the token pair: lane l of warp w holds box row
+    // 32(w - rw) + l, TMEM lane 32 rw + that row
+    const int jq = 32 * (warp - rw) + lane;
 
     for (int c = 0; c < nlines; ++c) {
         const int Lidx = line_of(c);
@@ -417,36 +424,25 @@ __global__ void __launch_bounds__(NT, 3)
             const int t0 = s * TT;
             const int Lt = min(TT, Lline - t0);
             const bool last = s == nsub - 1;
-            const int jb = 16 * warp + lane;   // box row (M = 64 layout: lanes 32w..32w+15)
-            const int p = box_start(s) + jb;   // position along the line
-            const bool valid = lane < 16 && p >= 0 && p < Lline;
-            // ---- MMA 1: generation from the boundary state (x exact in bf16: 3 passes).
-            // k_raw, v and s_eta, s_alpha use M = 64 (box row j -> lane 32(j/16) + j%16, read
-            // by all four warps); q_raw uses M = 128 with the x tile as rows 32 rw..32 rw+63
-            // (lane 32 rw + j, read by the readout warps), the other 64 A rows reading the
-            // kilobyte next to the tile into TMEM lanes nobody reads.
+            const int p = box_start(s) + jq;   // position along the line (token pair)
+            const bool valid = !gainw && p >= 0 && p < Lline;
+            // ---- MMA 1: generation from the boundary state, Eq. (15):
+            //   [s_eta s_alpha 0.. | k_raw | v | q_raw] = x (s1 + s2 + s3)^T
+            // one M = 128, N = 112 MMA per piece and K step (x is exact in bf16).  The x
+            // tile is A rows 32 rw..32 rw+63; the other 64 A rows read the kilobyte next to
+            // the tile into TMEM lanes nobody reads.
             if (issuer) {
                 tc_after();
                 if (wt.wait(mb_x, ph_x) && !*abort_flag) {
-                    const uint32_t xa = smem_u32(sX);
-                    const uint32_t id64 = idesc_bf16(64, 64), id16 = idesc_bf16(64, 16);
-                    const uint32_t idq = idesc_bf16(128, 32);
-                    const uint64_t dx = sdesc(xa, LBO_X, SBO_X);
-                    const uint64_t dq = sdesc(xa - (rw >> 1) * LBO_X, LBO_X, SBO_X);
+                    const uint64_t dq = sdesc(smem_u32(sX) - (rw >> 1) * LBO_X, LBO_X, SBO_X);
                     const uint64_t ds = sdesc(smem_u32(sS), LBO_K32, SBO_K32);
 #pragma unroll
-                    for (int pc = 0; pc < 3; ++pc) {
+                    for (int pc = 0; pc < 3; ++pc)
 #pragma unroll
-                        for (int ks = 0; ks < 2; ++ks) {
-                            const uint32_t acc = (pc | ks) != 0;
-                            const uint32_t ob = pc * S_PIECE + ks * 2 * LBO_K32;
-                            mma(tbase + COL_KV, dadd(dx, ks * 2 * LBO_X), dadd(ds, ob), id64, acc);
-                            mma(tbase + COL_Q, dadd(dq, ks * 2 * LBO_X), dadd(ds, ob + 8 * SBO_K32), idq,
-                                acc);
-                            mma(tbase + COL_S, dadd(dx, ks * 2 * LBO_X), dadd(ds, ob + 16 * SBO_K32), id16,
-                                acc);
-                        }
-                    }
+                        for (int ks = 0; ks < 2; ++ks)
+                            mma(tbase + COL_GEN, dadd(dq, ks * 2 * LBO_X),
+                                dadd(ds, pc * S_PIECE + ks * 2 * LBO_K32), idesc_bf16(128, 112),
+                                (pc | ks) != 0);
                     mma_commit(mb_gen);
                 }
             }
@@ -460,15 +456,15 @@ __global__ void __launch_bounds__(NT, 3)
                 const int nc = (s + 1 < nsub) ? c : c + 1;
                 if (nc < nlines) issue_x(nc, ns);
             }
-            // ---- keys, discrepancies, gates and step control (TMEM lane = token)
-            {
+            if (!gainw) {
+                // ---- keys, discrepancies, gates and step control (token pair, lane = token)
                 const int tr = rev ? Lline - 1 - p : p;  // token index inside the chunk
                 const int jr = tr - t0;                  // route-ordered index inside the sub-tile
                 float kr[32], vv[32];
-                tmem_ld32(tbase + lrow + COL_KV, kr);
-                tmem_ld32(tbase + lrow + COL_KV + 32, vv);
+                tmem_ld32(tbase + lrow + COL_GEN + COL_K, kr);
+                tmem_ld32(tbase + lrow + COL_GEN + COL_V, vv);
                 float se, sa;
-                tmem_ld2(tbase + lrow + COL_S, se, sa);
+                tmem_ld2(tbase + lrow + COL_GEN, se, sa);
                 const float rk = __frsqrt_rn(sumsq32(kr) + a.knorm_eps);
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
@@ -489,7 +485,7 @@ __global__ void __launch_bounds__(NT, 3)
                 }
                 // tokens whose retention could underflow the scaled gain within a few steps
                 const unsigned small = __ballot_sync(0xffffffffu, valid && !(alpha >= 0.01f));
-                if (lane == 0) vote[warp] = small != 0u;
+                if (lane == 0) vote[warp - rw] = small != 0u;
                 if (valid) {
                     float4 *kd = reinterpret_cast<float4 *>(Kf + jr * KS);
                     float4 *dd4 = reinterpret_cast<float4 *>(DLf + jr * KS);
@@ -505,13 +501,14 @@ __global__ void __launch_bounds__(NT, 3)
                                          keep ? __frcp_rn(alpha) : 0.0f, eta_t);
                 }
                 // Gram entries k_a . k_b of each block of NB route-ordered tokens.  This
-                // warp's tokens are the 16 consecutive route rows from R0 (route order runs
-                // with the box rows forwards, against them backwards), four whole blocks:
-                // lane 6q + i takes pair i of block q.
+                // warp's tokens are the 32 consecutive route rows from R0 (route order runs
+                // with the box rows forwards, against them backwards), eight whole blocks:
+                // pair i of block q goes to lane 6q + i (mod 32).
                 __syncwarp();
-                if (lane < 24) {
-                    const int R0 = rev ? TT - 16 - 16 * warp : 16 * warp;
-                    const int q = lane / 6, pi = lane - 6 * q;
+                const int R0 = rev ? TT - 32 - 32 * (warp - rw) : 32 * (warp - rw);
+#pragma unroll
+                for (int pr = lane; pr < 48; pr += 32) {
+                    const int q = pr / 6, pi = pr - 6 * q;
                     const int ia = pi < 3 ? 0 : (pi < 5 ? 1 : 2);
                     const int ib = pi < 3 ? pi + 1 : (pi < 5 ? pi - 1 : 3);
                     const float4 *ka = reinterpret_cast<const float4 *>(Kf + (R0 + NB * q + ia) * KS);
@@ -547,7 +544,7 @@ __global__ void __launch_bounds__(NT, 3)
                     gam = 1.0f;
                     inv_gam = 1.0f;
                 }
-                const bool careful = (vote[0] | vote[1] | vote[2] | vote[3]) != 0;
+                const bool careful = (vote[0] | vote[1]) != 0;
                 // operands of token j (key half, coefficients, delta entry); the next token's
                 // are loaded before the current one is applied, off the serial chain
                 struct Tok {
@@ -680,13 +677,11 @@ __global__ void __launch_bounds__(NT, 3)
                     if (lane == 0) mbar_arrive(mb_g);  // this warp's rows of G are written
                 }
             } else {
-                // ---- the readout pair, while the gain runs: queries and the readout of this
-                // sub-tile.  Lane l of warp w holds box row j = 32(w - rw) + l (TMEM lane
-                // 32 rw + j).
-                const int jq = 32 * (warp - rw) + lane;
+                // ---- the token pair, while the gain runs: queries and the readout of this
+                // sub-tile
                 {
                     float qr[32];
-                    tmem_ld32(tbase + lrow + COL_Q, qr);
+                    tmem_ld32(tbase + lrow + COL_GEN + COL_QR, qr);
                     const float rq = __frsqrt_rn(sumsq32(qr) + a.knorm_eps);
 #pragma unroll
                     for (int e = 0; e < 32; ++e) qr[e] *= rq;
@@ -697,12 +692,13 @@ __global__ void __launch_bounds__(NT, 3)
                 tc_before();
                 named_sync(1, 64);
                 tc_after();
-                // MMA 2: readout y = q M^m_b^T (six split cross terms), M = 128 with the
-                // queries as rows 32 rw..32 rw+63 (the other 64 A rows read the 4 KB next
+                // MMA 2: readout y = q M^m_b^T, Eq. (16) (six split cross terms), M = 128 with
+                // the queries as rows 32 rw..32 rw+63 (the other 64 A rows read the 4 KB next
                 // to each piece)
                 if (issuer && !*abort_flag) {
                     mma_split6<Q_PIECE, S_PIECE>(tbase + COL_RO, smem_u32(sQ) - (rw >> 1) * 8 * SBO_K32,
-                                                 smem_u32(sS) + 12 * SBO_K32, idesc_bf16(128, 32));
+                                                 smem_u32(sS) + (ROW_MEM + 3 * D) / 8 * SBO_K32,
+                                                 idesc_bf16(128, 32));
                     mma_commit(mb_ro);
                 }
                 wt.wait(mb_ro, ph_ro);
@@ -710,9 +706,8 @@ __global__ void __launch_bounds__(NT, 3)
                 // readout epilogue: lambda_r y added at the token's pixel (Eq. (26))
                 float y[32];
                 tmem_ld32(tbase + lrow + COL_RO, y);
-                const int pq = box_start(s) + jq;
-                if (pq >= 0 && pq < Lline) {
-                    const int pix = rowr ? Lidx * W + pq : pq * W + Lidx;
+                if (valid) {
+                    const int pix = rowr ? Lidx * W + p : p * W + Lidx;
                     float *dst = ob + (size_t)pix * Cc;
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
@@ -725,13 +720,16 @@ __global__ void __launch_bounds__(NT, 3)
                         red_add_v4(dst + 4 * e, v4);
                     }
                 }
-                // ---- MMA 3 (chunk end): every d x d memory <- M_b G (six split cross terms,
-                // M = 128 rows), issued as soon as G is cast.  G is the B operand (row n =
-                // column of G, K = row of G), three bf16 pieces.  When the chunk retains at
-                // least half of the state the operand is G - I: the MMA forms only the
-                // increment M_b (G - I), which the epilogue adds to M_b in fp32, so the tensor
-                // core's accumulation error is relative to the change.  Otherwise the state is
-                // mostly replaced and the MMA forms M_b G directly (no cancellation).
+                // ---- MMA 3 (chunk end): every d x d memory <- M_b G (Eq. (46)), issued as soon
+                // as G is cast.  G is the B operand (row n = column of G, K = row of G), three
+                // bf16 pieces.  When the chunk retains at least half of the state the operand
+                // is G - I: the MMA forms only the increment M_b (G - I), which the epilogue adds
+                // to M_b in fp32, so the tensor core's accumulation error is relative to the
+                // change.  Otherwise the state is mostly replaced and the MMA forms M_b G
+                // directly (no cancellation).  The six cross terms go in as three MMAs per K
+                // step, one per piece of M_b against the pieces of G stacked along N:
+                //   cols [0,32): a1 b1 + a2 b1,  [32,64): a1 b2 + a2 b2,  [64,96): a1 b3 + a3 b1,
+                // summed by the epilogue.
                 if (last) {
                     wt.wait(mb_g, ph_g);
                     const bool use_delta = *delta_form != 0;
@@ -749,8 +747,16 @@ __global__ void __launch_bounds__(NT, 3)
                     named_sync(1, 64);
                     tc_after();
                     if (issuer && !*abort_flag) {
-                        mma_split6<S_PIECE, G_PIECE>(tbase + COL_UPD, smem_u32(sS), smem_u32(sG),
-                                                     idesc_bf16(128, 32));
+                        const uint64_t da = sdesc(smem_u32(sS) + ROW_MEM / 8 * SBO_K32, LBO_K32, SBO_K32);
+                        const uint64_t db = sdesc(smem_u32(sG), LBO_K32, SBO_K32);
+#pragma unroll
+                        for (int ks = 0; ks < 2; ++ks) {
+                            const uint32_t ko = ks * 2 * LBO_K32;
+                            mma(tbase + COL_UPD, dadd(da, ko), dadd(db, ko), idesc_bf16(128, 96), ks != 0);
+                            mma(tbase + COL_UPD, dadd(da, S_PIECE + ko), dadd(db, ko), idesc_bf16(128, 64), 1);
+                            mma(tbase + COL_UPD + 2 * D, dadd(da, 2 * S_PIECE + ko), dadd(db, ko),
+                                idesc_bf16(128, 32), 1);
+                        }
                         mma_commit(mb_upd);
                     }
                 }
@@ -777,12 +783,12 @@ __global__ void __launch_bounds__(NT, 3)
                     __nv_bfloat16 p1, p2, p3;
                     const int g = lane >> 3, e = lane & 7;
                     split3(ne, p1, p2, p3);
-                    unsigned char *d0 = sS + op_off(128, g) + 2 * e;
+                    unsigned char *d0 = sS + op_off(ROW_ETA, g) + 2 * e;
                     *reinterpret_cast<__nv_bfloat16 *>(d0) = p1;
                     *reinterpret_cast<__nv_bfloat16 *>(d0 + S_PIECE) = p2;
                     *reinterpret_cast<__nv_bfloat16 *>(d0 + 2 * S_PIECE) = p3;
                     split3(na, p1, p2, p3);
-                    unsigned char *d1 = sS + op_off(129, g) + 2 * e;
+                    unsigned char *d1 = sS + op_off(ROW_ETA + 1, g) + 2 * e;
                     *reinterpret_cast<__nv_bfloat16 *>(d1) = p1;
                     *reinterpret_cast<__nv_bfloat16 *>(d1 + S_PIECE) = p2;
                     *reinterpret_cast<__nv_bfloat16 *>(d1 + 2 * S_PIECE) = p3;
@@ -790,15 +796,22 @@ __global__ void __launch_bounds__(NT, 3)
                 wt.wait(mb_upd, ph_upd);
                 ph_upd ^= 1;
                 tc_after();
-                // new state rows: thread = row (TMEM lane), re-split into the operand pieces.
-                // In the increment form M_b is recovered exactly from its three pieces (their
-                // sum rounds back to the fp32 value they were cut from) and added in fp32.
-                float v[32];
+                // new state rows: thread = memory row (TMEM lane), the three column blocks
+                // summed, re-split into the operand pieces.  In the increment form M_b is
+                // recovered exactly from its three pieces (their sum rounds back to the fp32
+                // value they were cut from) and added in fp32.
+                float v[32], w[32];
                 tmem_ld32(tbase + lrow + COL_UPD, v);
+                tmem_ld32(tbase + lrow + COL_UPD + D, w);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) v[e] += w[e];
+                tmem_ld32(tbase + lrow + COL_UPD + 2 * D, w);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) v[e] += w[e];
                 const bool add_mb = *delta_form != 0;
 #pragma unroll
                 for (int g = 0; g < 4; ++g) {
-                    unsigned char *src = sS + op_off(tid, g);
+                    unsigned char *src = sS + op_off(ROW_MEM + tid, g);
                     if (add_mb) {
                         const uint4 u1 = *reinterpret_cast<const uint4 *>(src);
                         const uint4 u2 = *reinterpret_cast<const uint4 *>(src + S_PIECE);
