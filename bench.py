@@ -180,17 +180,24 @@ def job_throughput(tokens_per_rank_step, steps, world, seconds):
 
 # --------------------------------------------------------- oracle timing
 
-def time_oracle(wl, images, nthreads):
+def time_oracle(wl, images, nthreads, min_seconds=0.0, max_passes=1000):
+    """Tokens/s of the oracle over `images` images, repeated until `min_seconds`
+    of wall time have passed; returns (tokens/s, seconds, passes)."""
     import oracle
     from visual_backbone_gb300 import synth
     oracle.build()
     inp = synth.make_inputs(wl, batch=images)
     p = oracle.OracleParams(eta_bias=wl.eta_bias, alpha_init=wl.alpha_init)
     t0 = time.perf_counter()
-    oracle.forward(inp.x64, inp.mem0, wl.H, wl.W, wl.nh, wl.d, chunk_len=wl.chunk, params=p,
-                   nthreads=nthreads)
-    dt = time.perf_counter() - t0
-    return images * wl.N / dt, dt
+    passes = 0
+    while True:
+        oracle.forward(inp.x64, inp.mem0, wl.H, wl.W, wl.nh, wl.d, chunk_len=wl.chunk, params=p,
+                       nthreads=nthreads)
+        passes += 1
+        dt = time.perf_counter() - t0
+        if dt >= min_seconds or passes >= max_passes:
+            break
+    return passes * images * wl.N / dt, dt, passes
 
 
 def cpu_cores():
@@ -211,7 +218,7 @@ def run_reference(args, wl):
     times = []
     t_start = time.perf_counter()
     for _ in range(args.steps):
-        _, dt = time_oracle(wl, images, cores)
+        _, dt, _ = time_oracle(wl, images, cores)
         times.append(dt)
     total = sum(times)
     value = args.steps * images * wl.N / total
@@ -346,11 +353,25 @@ def run_ours(args, wl):
                 "hbm_frac_of_measured": nbytes / kern_avg_s / 1e9 / float(peaks["hbm_gbs"]),
                 "t_roof_ms": 1e3 * max(flops / (peak * 1e12), nbytes / (float(peaks["hbm_gbs"]) * 1e9))}
         roof["frac_of_roofline_time"] = roof["t_roof_ms"] / (kern_avg_s * 1e3)
+        # Secondary view: the shared-gain recurrence (2 d^2 multiply-adds per token, route
+        # and head) runs on the fp32 FMA pipe, whose nominal peak is 152 SMs x 128 lanes x
+        # 2 flops x 2.07 GHz.
+        gain_flops = 4.0 * wl.d * wl.d * wl.tokens * wl.nh * 4
+        fp32_peak = 152 * 128 * 2 * 2.07e9 / 1e12
+        roof["alu_view"] = {"what": "shared-gain recurrence on the fp32 FMA pipe",
+                            "flops_per_launch": gain_flops,
+                            "achieved": gain_flops / kern_avg_s / 1e12, "peak": fp32_peak,
+                            "unit": "TFLOP/s",
+                            "frac": gain_flops / kern_avg_s / 1e12 / fp32_peak,
+                            "peak_source": "nominal (SM count x fp32 lanes x max clock)"}
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f32" if args.kernel == "simt" else "f32 (auto kernel)",
+            "dtype": "f32",
+            "numerics": ("x bf16 (exact); state, gain recurrence, gates and step control "
+                         "fp32; tensor-core products on three bf16 pieces per fp32 operand "
+                         "(24 significant bits), fp32 accumulate"),
             "data": "synthetic", "config": workload_config(wl, args),
             "roofline": roof,
             "e2e": {"value": e2e_value, "unit": UNIT,
@@ -361,11 +382,11 @@ def run_ours(args, wl):
         }
         if world == 1 and not args.no_cpu_baseline:
             cores = min(cpu_cores(), args.cpu_images * wl.nh)
-            v, dt = time_oracle(wl, args.cpu_images, cores)
+            v, dt, passes = time_oracle(wl, args.cpu_images, cores, min_seconds=args.cpu_seconds)
             line["cpu_baseline"] = {
                 "value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
-                "sample": f"{args.cpu_images} of {wl.B} images of the workload (all 4 routes x "
-                          f"{wl.nh} heads), fp64, {dt:.1f} s wall"}
+                "sample": f"{passes} pass(es) over {args.cpu_images} of {wl.B} images of the "
+                          f"workload (all 4 routes x {wl.nh} heads), fp64, {dt:.1f} s wall"}
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
@@ -383,6 +404,8 @@ def main(argv=None):
     ap.add_argument("--kernel", choices=["auto", "simt", "tc"], default="auto")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-images", type=int, default=16)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="minimum wall time of the oracle sample behind cpu_baseline")
     ap.add_argument("--ref-images", type=int, default=1)
     args = ap.parse_args(argv)
     if args.warmup < 3:
