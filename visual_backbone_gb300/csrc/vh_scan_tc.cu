@@ -206,16 +206,34 @@ __device__ __forceinline__ void split3(float v, __nv_bfloat16 &p1, __nv_bfloat16
     p3 = __float2bfloat16_rn(r1 - __bfloat162float(p2));
 }
 
+// bf16 <-> fp32 on packed pairs: element 2i in the low half, 2i + 1 in the high half of
+// a 32-bit word (the operand's memory order).  Widening is exact (a shift).
+__device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi)
+{
+    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
 // Write 8 consecutive K elements (one 16-byte core-matrix row) of each piece;
-// `dst` points at piece 1, the other pieces follow `stride` bytes apart.
+// `dst` points at piece 1, the other pieces follow `stride` bytes apart.  Same pieces
+// as split3, two elements per conversion.
 __device__ __forceinline__ void store_split8(unsigned char *dst, int stride, const float *v)
 {
-    __align__(16) __nv_bfloat16 a[8], b[8], c[8];
+    uint4 w1, w2, w3;
+    uint32_t *a = &w1.x, *b = &w2.x, *c = &w3.x;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) split3(v[e], a[e], b[e], c[e]);
-    *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(a);
-    *reinterpret_cast<uint4 *>(dst + stride) = *reinterpret_cast<const uint4 *>(b);
-    *reinterpret_cast<uint4 *>(dst + 2 * stride) = *reinterpret_cast<const uint4 *>(c);
+    for (int i = 0; i < 4; ++i) {
+        const float x0 = v[2 * i], x1 = v[2 * i + 1];
+        a[i] = pack_bf16x2_rn(x0, x1);
+        const float r0 = x0 - bf16_lo(a[i]), r1 = x1 - bf16_hi(a[i]);
+        b[i] = pack_bf16x2_rn(r0, r1);
+        c[i] = pack_bf16x2_rn(r0 - bf16_lo(b[i]), r1 - bf16_hi(b[i]));
+    }
+    *reinterpret_cast<uint4 *>(dst) = w1;
+    *reinterpret_cast<uint4 *>(dst + stride) = w2;
+    *reinterpret_cast<uint4 *>(dst + 2 * stride) = w3;
 }
 
 // Sum of squares of 32 values in eight independent FMA chains (scalar FMAs issue at
@@ -816,13 +834,12 @@ __global__ void __launch_bounds__(NT, 3)
                         const uint4 u1 = *reinterpret_cast<const uint4 *>(src);
                         const uint4 u2 = *reinterpret_cast<const uint4 *>(src + S_PIECE);
                         const uint4 u3 = *reinterpret_cast<const uint4 *>(src + 2 * S_PIECE);
-                        const __nv_bfloat16 *b1 = reinterpret_cast<const __nv_bfloat16 *>(&u1);
-                        const __nv_bfloat16 *b2 = reinterpret_cast<const __nv_bfloat16 *>(&u2);
-                        const __nv_bfloat16 *b3 = reinterpret_cast<const __nv_bfloat16 *>(&u3);
+                        const uint32_t *w1 = &u1.x, *w2 = &u2.x, *w3 = &u3.x;
 #pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            v[8 * g + e] += (__bfloat162float(b1[e]) + __bfloat162float(b2[e])) +
-                                            __bfloat162float(b3[e]);
+                        for (int i = 0; i < 4; ++i) {
+                            v[8 * g + 2 * i] += (bf16_lo(w1[i]) + bf16_lo(w2[i])) + bf16_lo(w3[i]);
+                            v[8 * g + 2 * i + 1] += (bf16_hi(w1[i]) + bf16_hi(w2[i])) + bf16_hi(w3[i]);
+                        }
                     }
                     store_split8(src, S_PIECE, v + 8 * g);
                 }
