@@ -195,6 +195,41 @@ __device__ __forceinline__ void tmem_ld2(uint32_t ta, float &a0, float &a1)
     a1 = __uint_as_float(r1);
 }
 
+// k_raw (32 columns at +COL_K), v (32 at +COL_V) and s_eta, s_alpha (2 at +0) of this
+// thread's lane, with a single wait.
+__device__ __forceinline__ void tmem_ld_kvs(uint32_t ta, float (&k)[32], float (&v)[32], float &se,
+                                            float &sa)
+{
+    uint32_t r[32], q[32], s0, s1;
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+        "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%66];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,"
+        "%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%67];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x2.b32 {%64,%65}, [%68];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+          "=r"(q[0]), "=r"(q[1]), "=r"(q[2]), "=r"(q[3]), "=r"(q[4]), "=r"(q[5]), "=r"(q[6]),
+          "=r"(q[7]), "=r"(q[8]), "=r"(q[9]), "=r"(q[10]), "=r"(q[11]), "=r"(q[12]), "=r"(q[13]),
+          "=r"(q[14]), "=r"(q[15]), "=r"(q[16]), "=r"(q[17]), "=r"(q[18]), "=r"(q[19]),
+          "=r"(q[20]), "=r"(q[21]), "=r"(q[22]), "=r"(q[23]), "=r"(q[24]), "=r"(q[25]),
+          "=r"(q[26]), "=r"(q[27]), "=r"(q[28]), "=r"(q[29]), "=r"(q[30]), "=r"(q[31]),
+          "=r"(s0), "=r"(s1)
+        : "r"(ta + COL_K), "r"(ta + COL_V), "r"(ta)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        k[i] = __uint_as_float(r[i]);
+        v[i] = __uint_as_float(q[i]);
+    }
+    se = __uint_as_float(s0);
+    sa = __uint_as_float(s1);
+}
+
 // fp32 -> three bf16 pieces p1 + p2 + p3 (24 significant bits): each piece
 // rounds what the previous ones left; the residuals are exact in fp32.
 __device__ __forceinline__ void split3(float v, __nv_bfloat16 &p1, __nv_bfloat16 &p2,
@@ -474,15 +509,16 @@ __global__ void __launch_bounds__(NT, 3)
                 const int nc = (s + 1 < nsub) ? c : c + 1;
                 if (nc < nlines) issue_x(nc, ns);
             }
+            // ---- per-token step, Eqs. (15), (19), (20), (53).  The token pair (lane = token)
+            // normalises k, forms delta = k - v and their squared norms, and publishes the
+            // token's scalars; then the gain pair (lane = route-ordered token) evaluates the
+            // gates and the step control while the token pair forms the Gram entries.
             if (!gainw) {
-                // ---- keys, discrepancies, gates and step control (token pair, lane = token)
                 const int tr = rev ? Lline - 1 - p : p;  // token index inside the chunk
                 const int jr = tr - t0;                  // route-ordered index inside the sub-tile
                 float kr[32], vv[32];
-                tmem_ld32(tbase + lrow + COL_GEN + COL_K, kr);
-                tmem_ld32(tbase + lrow + COL_GEN + COL_V, vv);
                 float se, sa;
-                tmem_ld2(tbase + lrow + COL_GEN, se, sa);
+                tmem_ld_kvs(tbase + lrow + COL_GEN, kr, vv, se, sa);
                 const float rk = __frsqrt_rn(sumsq32(kr) + a.knorm_eps);
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
@@ -490,20 +526,6 @@ __global__ void __launch_bounds__(NT, 3)
                     vv[e] = kr[e] - vv[e];  // delta = k - v
                 }
                 const float kn2 = sumsq32(kr), dd2 = sumsq32(vv);
-                float eta, alpha, oma;
-                gates(a, se, sa, eta, alpha, oma);
-                float eta_t;
-                if (a.gate_mode == VH_GATE_FORCED_EXEC) {
-                    eta_t = a.forced_eta;
-                } else {
-                    const StepOut so = step_control(a, eta, alpha, oma, kn2, dd2);
-                    eta_t = so.eta_tilde;
-                    n_spec += valid && so.spec_active;
-                    n_inj += valid && so.inj_ratio_gt1;
-                }
-                // tokens whose retention could underflow the scaled gain within a few steps
-                const unsigned small = __ballot_sync(0xffffffffu, valid && !(alpha >= 0.01f));
-                if (lane == 0) vote[warp - rw] = small != 0u;
                 if (valid) {
                     float4 *kd = reinterpret_cast<float4 *>(Kf + jr * KS);
                     float4 *dd4 = reinterpret_cast<float4 *>(DLf + jr * KS);
@@ -512,17 +534,42 @@ __global__ void __launch_bounds__(NT, 3)
                         kd[e] = make_float4(kr[4 * e], kr[4 * e + 1], kr[4 * e + 2], kr[4 * e + 3]);
                         dd4[e] = make_float4(vv[4 * e], vv[4 * e + 1], vv[4 * e + 2], vv[4 * e + 3]);
                     }
-                    // coefficients of the gain recurrence: (alpha, eta/alpha, 1/alpha, eta) for the
-                    // scaled form, (alpha, 0, 0, eta) where alpha is too small to divide by
+                    SC[jr] = make_float4(se, sa, kn2, dd2);
+                }
+            }
+            __syncthreads();
+            if (gainw) {
+                // gates and step control of route-ordered token jg; the coefficients of the
+                // gain recurrence replace the scalars: (alpha, eta/alpha, 1/alpha, eta) for the
+                // scaled form, (alpha, 0, 0, eta) where alpha is too small to divide by
+                const int jg = tid & 63;
+                const bool tv = jg < Lt;
+                float alpha = 1.0f;
+                if (tv) {
+                    const float4 sc = SC[jg];
+                    float eta, oma;
+                    gates(a, sc.x, sc.y, eta, alpha, oma);
+                    float eta_t;
+                    if (a.gate_mode == VH_GATE_FORCED_EXEC) {
+                        eta_t = a.forced_eta;
+                    } else {
+                        const StepOut so = step_control(a, eta, alpha, oma, sc.z, sc.w);
+                        eta_t = so.eta_tilde;
+                        n_spec += so.spec_active;
+                        n_inj += so.inj_ratio_gt1;
+                    }
                     const bool keep = alpha >= 1e-6f;
-                    SC[jr] = make_float4(alpha, keep ? __fdividef(eta_t, alpha) : 0.0f,
+                    SC[jg] = make_float4(alpha, keep ? __fdividef(eta_t, alpha) : 0.0f,
                                          keep ? __frcp_rn(alpha) : 0.0f, eta_t);
                 }
+                // tokens whose retention could underflow the scaled gain within a few steps
+                const unsigned small = __ballot_sync(0xffffffffu, tv && !(alpha >= 0.01f));
+                if (lane == 0) vote[warp - 2 * gp] = small != 0u;
+            } else {
                 // Gram entries k_a . k_b of each block of NB route-ordered tokens.  This
                 // warp's tokens are the 32 consecutive route rows from R0 (route order runs
                 // with the box rows forwards, against them backwards), eight whole blocks:
                 // pair i of block q goes to lane 6q + i (mod 32).
-                __syncwarp();
                 const int R0 = rev ? TT - 32 - 32 * (warp - rw) : 32 * (warp - rw);
 #pragma unroll
                 for (int pr = lane; pr < 48; pr += 32) {
