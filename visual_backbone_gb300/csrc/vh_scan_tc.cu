@@ -56,6 +56,12 @@ constexpr int ROW_ETA = 0, ROW_MEM = 16, S_ROWS = ROW_MEM + 4 * D;
 constexpr int S_PIECE = S_ROWS / 8 * SBO_K32;
 constexpr int Q_PIECE = TT * ROW_B;
 constexpr int G_PIECE = D * ROW_B;
+// The gain as the update's B operand is MN-major (N contiguous): element (n, k) of piece p
+// at (4p + n/8) * 128 + (k/8) * G_KSTR + (k%8) * 16 + (n%8) * 2, so the three pieces stack
+// along N (rows n of piece p are operand rows 32p + n) and a gain row's 16 consecutive
+// columns are two 16-byte runs.
+constexpr int G_NSTR = 128, G_KSTR = 3 * (D / 8) * G_NSTR;
+static_assert(D / 8 * G_KSTR == 3 * G_PIECE, "gain operand size");
 
 // The M = 128 generation and readout MMAs address their operand 1 KB (x) or 4 KB (each
 // query piece) below the data, so a readable region precedes both.
@@ -114,6 +120,21 @@ __device__ __forceinline__ uint32_t mbar_try(uint32_t bar, uint32_t parity)
     return ok;
 }
 
+// As mbar_try, but a thread whose phase is not complete may be suspended for up to
+// `ns` nanoseconds (or until the phase completes) instead of returning at once, so
+// waiting warps do not take issue slots from the working ones.
+__device__ __forceinline__ uint32_t mbar_try_sleep(uint32_t bar, uint32_t parity, uint32_t ns)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(bar), "r"(parity), "r"(ns)
+                 : "memory");
+    return ok;
+}
+
 __device__ __forceinline__ void fence_async_smem()
 {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -142,11 +163,12 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t 
 // The descriptor of an operand `bytes` further on (16-byte units in the address field).
 __device__ __forceinline__ uint64_t dadd(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
 
-// Instruction descriptor of kind::f16: bf16 A and B (K-major), fp32 D.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N)
+// Instruction descriptor of kind::f16: bf16 A and B, fp32 D; A K-major, B K-major or
+// (b_mn) MN-major.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn = false)
 {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
-           ((uint32_t)(M >> 4) << 24);
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn ? 1u : 0u) << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 __device__ __forceinline__ void mma(uint32_t dt, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc)
@@ -301,7 +323,7 @@ struct Waiter {
         if (mbar_try(bar, parity)) return true;
         const long long t0 = clock64();
         while (true) {
-            if (mbar_try(bar, parity)) return true;
+            if (mbar_try_sleep(bar, parity, 20000u)) return true;
             if (*abort_flag) return false;
             if (clock64() - t0 > (1ll << 32)) {  // ~2 s at the GB300 clock
                 if (atomicExch((int *)abort_flag, 1) == 0 && stats)
@@ -730,14 +752,33 @@ __global__ void __launch_bounds__(NT, 3)
                     if (gam < 1e-20f) fold();
                 }
                 if (last) {
-                    // G = gam * ghat in fp32 rows for the readout pair, which casts it as the
-                    // update's operand
+                    // G = gam * ghat: fp32 rows for the eta / alpha rows, and the update's B
+                    // operand in three bf16 pieces (MN-major: this lane's 16 columns of its
+                    // row are two 16-byte runs per piece).  When the chunk retains at least
+                    // half of the state the operand is G - I: the MMA forms only the
+                    // increment M_b (G - I), which the epilogue adds to M_b in fp32, so the
+                    // tensor core's accumulation error is relative to the change.  Otherwise
+                    // the state is mostly replaced and the MMA forms M_b G directly (no
+                    // cancellation).
+                    const bool use_delta = gam >= 0.5f;
+                    float gv[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) gv[e] = gam * gh[e];
                     float4 *gd = reinterpret_cast<float4 *>(Gf + grow * GFS + 16 * gq);
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
-                        gd[e] = make_float4(gam * gh[4 * e], gam * gh[4 * e + 1], gam * gh[4 * e + 2],
-                                            gam * gh[4 * e + 3]);
-                    if ((tid & 63) == 0) *delta_form = gam >= 0.5f ? 1 : 0;
+                        gd[e] = make_float4(gv[4 * e], gv[4 * e + 1], gv[4 * e + 2], gv[4 * e + 3]);
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        float v8[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            v8[i] = gv[8 * hh + i] - ((use_delta && 16 * gq + 8 * hh + i == grow) ? 1.0f : 0.0f);
+                        store_split8(sG + (2 * gq + hh) * G_NSTR + (grow >> 3) * G_KSTR + (grow & 7) * 16,
+                                     4 * G_NSTR, v8);
+                    }
+                    if ((tid & 63) == 0) *delta_form = use_delta ? 1 : 0;
+                    fence_async_smem();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(mb_g);  // this warp's rows of G are written
                 }
@@ -786,41 +827,24 @@ __global__ void __launch_bounds__(NT, 3)
                     }
                 }
                 // ---- MMA 3 (chunk end): every d x d memory <- M_b G (Eq. (46)), issued as soon
-                // as G is cast.  G is the B operand (row n = column of G, K = row of G), three
-                // bf16 pieces.  When the chunk retains at least half of the state the operand
-                // is G - I: the MMA forms only the increment M_b (G - I), which the epilogue adds
-                // to M_b in fp32, so the tensor core's accumulation error is relative to the
-                // change.  Otherwise the state is mostly replaced and the MMA forms M_b G
-                // directly (no cancellation).  The six cross terms go in as three MMAs per K
-                // step, one per piece of M_b against the pieces of G stacked along N:
+                // as the gain pair has written G's pieces.  The six cross terms go in as three
+                // MMAs per K step, one per piece of M_b against the pieces of G stacked along N:
                 //   cols [0,32): a1 b1 + a2 b1,  [32,64): a1 b2 + a2 b2,  [64,96): a1 b3 + a3 b1,
                 // summed by the epilogue.
-                if (last) {
-                    wt.wait(mb_g, ph_g);
-                    const bool use_delta = *delta_form != 0;
-#pragma unroll
-                    for (int tk = jq; tk < 4 * D; tk += 64) {
-                        const int n = tk & (D - 1), g = tk / D;
-                        float v[8];
-#pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            v[i] = Gf[(8 * g + i) * GFS + n] - ((use_delta && 8 * g + i == n) ? 1.0f : 0.0f);
-                        store_split8(sG + op_off(n, g), G_PIECE, v);
-                    }
-                    fence_async_smem();
-                    tc_before();
-                    named_sync(1, 64);
-                    tc_after();
-                    if (issuer && !*abort_flag) {
+                if (last && issuer) {
+                    if (wt.wait(mb_g, ph_g) && !*abort_flag) {
+                        tc_after();
                         const uint64_t da = sdesc(smem_u32(sS) + ROW_MEM / 8 * SBO_K32, LBO_K32, SBO_K32);
-                        const uint64_t db = sdesc(smem_u32(sG), LBO_K32, SBO_K32);
+                        const uint64_t db = sdesc(smem_u32(sG), G_KSTR, G_NSTR);
 #pragma unroll
                         for (int ks = 0; ks < 2; ++ks) {
-                            const uint32_t ko = ks * 2 * LBO_K32;
-                            mma(tbase + COL_UPD, dadd(da, ko), dadd(db, ko), idesc_bf16(128, 96), ks != 0);
-                            mma(tbase + COL_UPD, dadd(da, S_PIECE + ko), dadd(db, ko), idesc_bf16(128, 64), 1);
-                            mma(tbase + COL_UPD + 2 * D, dadd(da, 2 * S_PIECE + ko), dadd(db, ko),
-                                idesc_bf16(128, 32), 1);
+                            const uint32_t ka = ks * 2 * LBO_K32, kb = ks * 2 * G_KSTR;
+                            mma(tbase + COL_UPD, dadd(da, ka), dadd(db, kb), idesc_bf16(128, 96, true),
+                                ks != 0);
+                            mma(tbase + COL_UPD, dadd(da, S_PIECE + ka), dadd(db, kb),
+                                idesc_bf16(128, 64, true), 1);
+                            mma(tbase + COL_UPD + 2 * D, dadd(da, 2 * S_PIECE + ka), dadd(db, kb),
+                                idesc_bf16(128, 32, true), 1);
                         }
                         mma_commit(mb_upd);
                     }
