@@ -159,6 +159,17 @@ vh_status vh_scan_forward(const void *x, const float *memories0, const vh_params
 vh_status vh_debug_permute(const void *x, const vh_params *p, int H, int W, int route,
                            void *seq);
 
+/*
+ * vh_check -- wait for `stream` (a cudaStream_t; NULL = legacy default) and read the
+ * device counters a scan wrote into `stats` (device [VH_STAT_COUNT], as passed in
+ * vh_params.stats).  Returns VH_ERR_TIMEOUT if any CTA's bounded wait expired (the
+ * results of that call are invalid), else VH_ERR_NONFINITE if a non-finite readout
+ * value was produced, else VH_OK.  VH_ERR_INVALID_ARG for a NULL stats pointer,
+ * VH_ERR_CUDA if the synchronisation or the 64-byte copy fails.  The pages define no
+ * such step: it surfaces the kernel's own status flags.
+ */
+vh_status vh_check(const unsigned long long *stats, void *stream);
+
 /* Bytes of device workspace a vh_scan_forward call needs: always 0. */
 size_t vh_workspace_size(const vh_params *p, int H, int W, unsigned dirs, int chunk);
 

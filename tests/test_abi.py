@@ -8,7 +8,7 @@ import pytest
 def test_exports_every_header_function(vhlib):
     names = vhlib.header_functions()
     assert {"vh_scan_forward", "vh_debug_permute", "vh_workspace_size", "vh_status_string",
-            "vh_last_error", "vh_params_init", "vh_version"} <= set(names)
+            "vh_last_error", "vh_params_init", "vh_version", "vh_check"} <= set(names)
     L = vhlib.lib()
     for n in names:
         assert hasattr(L, n), n
@@ -61,9 +61,17 @@ def test_debug_permute_rejects_bad_route(vhlib):
     assert vhlib.lib().vh_debug_permute(FAKE, ctypes.byref(p), 3, 4, 4, FAKE * 64) == -1
 
 
+def test_check_rejects_null_stats(vhlib):
+    L = vhlib.lib()
+    assert L.vh_check(None, None) == -1
+    assert b"stats" in L.vh_last_error()
+
+
 def test_binding_refuses_cpu_tensors(vhlib):
     import torch
     x = torch.zeros(1, 4, 4, 16)
     m = torch.zeros(4, 1, 4 * 256 + 32)
     with pytest.raises(ValueError, match="CUDA"):
         vhlib.scan_forward(x, m, 16)
+    with pytest.raises(ValueError, match="CUDA"):
+        vhlib.check(torch.zeros(8, dtype=torch.int64))

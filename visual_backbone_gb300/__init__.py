@@ -91,6 +91,8 @@ def lib() -> ctypes.CDLL:
         L.vh_last_error.restype = ctypes.c_char_p
         L.vh_last_error.argtypes = []
         L.vh_version.restype = ci
+        L.vh_check.restype = ci
+        L.vh_check.argtypes = [vp, vp]
         L.vh_params_init.restype = None
         L.vh_params_init.argtypes = [ctypes.POINTER(CParams)]
         _lib = L
@@ -178,6 +180,14 @@ def scan_forward(x, memories0, head_dim: int, dirs: int = DIR_ALL, chunk: int = 
     _check(lib().vh_scan_forward(x.data_ptr(), memories0.data_ptr(), ctypes.byref(cp), H, W,
                                  dirs, chunk, out.data_ptr()))
     return out
+
+
+def check(stats, stream=None):
+    """Wait for `stream` and raise VhError if the counters in `stats` (the tensor passed
+    to scan_forward) report an expired wait or a non-finite readout value."""
+    import torch
+    _require_cuda("stats", stats, (torch.int64,))
+    _check(lib().vh_check(stats.data_ptr(), _stream_ptr(stream)))
 
 
 def debug_permute(x, route: int, head_dim: int, stream=None):

@@ -92,6 +92,24 @@ int vh_version(void) { return 100; }
 
 size_t vh_workspace_size(const vh_params *, int, int, unsigned, int) { return 0; }
 
+vh_status vh_check(const unsigned long long *stats, void *stream)
+{
+    g_err[0] = '\0';
+    if (!stats) return fail(VH_ERR_INVALID_ARG, "stats is NULL");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    unsigned long long h[VH_STAT_COUNT];
+    cudaError_t e = cudaMemcpyAsync(h, stats, sizeof h, cudaMemcpyDeviceToHost, st);
+    if (e != cudaSuccess) return cuda_fail(e, "reading stats");
+    e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "synchronising the stream");
+    if (h[VH_STAT_TIMEOUT])
+        return fail(VH_ERR_TIMEOUT, "%llu CTA(s) gave up a bounded wait; results are invalid",
+                    h[VH_STAT_TIMEOUT]);
+    if (h[VH_STAT_NONFINITE])
+        return fail(VH_ERR_NONFINITE, "%llu non-finite readout value(s)", h[VH_STAT_NONFINITE]);
+    return VH_OK;
+}
+
 vh_status vh_scan_forward(const void *x, const float *memories0, const vh_params *p, int H,
                           int W, unsigned dirs, int chunk, float *out)
 {
