@@ -43,6 +43,8 @@ class _Params(ctypes.Structure):
         ("dir_scale", ctypes.POINTER(ctypes.c_double)),
         ("gate_mode", ctypes.c_int), ("forced_eta", ctypes.c_double),
         ("forced_alpha", ctypes.c_double), ("control_flags", ctypes.c_uint),
+        ("w_query", ctypes.POINTER(ctypes.c_double)),
+        ("skip", ctypes.POINTER(ctypes.c_double)),
     ]
 
 
@@ -62,16 +64,22 @@ class OracleParams:
     forced_eta: float = 0.0
     forced_alpha: float = 0.0
     control_flags: int = 0
+    w_query: Optional[np.ndarray] = None     # [Cc][Cc]: VisionHOPE-exact readout query
+    skip: Optional[np.ndarray] = None        # [4][Cc]: channel-wise skip of each route
 
     def _c(self):
-        ds = None
-        keep = None
-        if self.dir_scale is not None:
-            keep = np.ascontiguousarray(self.dir_scale, dtype=np.float64)
-            ds = keep.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+        keep = []
+
+        def arr(a):
+            if a is None:
+                return None
+            a = np.ascontiguousarray(a, dtype=np.float64)
+            keep.append(a)
+            return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
         p = _Params(self.gamma_eta, self.alpha_init, self.eta_bias, self.eps, self.knorm_eps,
-                    self.inj_inward, self.spec_inward, self.kk_floor, ds, self.gate_mode,
-                    self.forced_eta, self.forced_alpha, self.control_flags)
+                    self.inj_inward, self.spec_inward, self.kk_floor, arr(self.dir_scale),
+                    self.gate_mode, self.forced_eta, self.forced_alpha, self.control_flags,
+                    arr(self.w_query), arr(self.skip))
         return p, keep
 
 
