@@ -43,7 +43,7 @@ typedef enum {
     VH_ERR_INVALID_ARG = -1,   /* bad pointer, shape, alignment, mask or parameter */
     VH_ERR_UNSUPPORTED = -2,   /* valid but not built: head_dim not in {16,32,64}, dtype */
     VH_ERR_CUDA = -3,          /* a CUDA runtime call or launch failed */
-    VH_ERR_WORKSPACE = -4,     /* reserved */
+    VH_ERR_WORKSPACE = -4,     /* workspace missing, too small or misaligned */
     VH_ERR_NONFINITE = -5,     /* reserved for a checking helper */
     VH_ERR_TIMEOUT = -6        /* reserved: no call here waits on another block */
 } vh_status;
@@ -109,6 +109,17 @@ typedef struct vh_params {
     int accumulate;            /* 0: out is overwritten (the call zeroes it first);
                                   1: the fused sum of Eq. (26) is added to out's contents */
     void *stream;              /* cudaStream_t */
+    /* VisionHOPE-exact readout ("VisionHOPE", Sec. 2.1.2 Eq. (14) and App. B.5): the query
+     * is an outer Cc x Cc projection applied once to x and reused by the four routes,
+     * L2-normalised within each head (stabiliser knorm_eps), instead of M^q_b x.  The
+     * query feeds only the readout, so the memories (memories_out) are the same as in
+     * the six-memory form; the M^q slot is carried but not read. */
+    const float *w_query;      /* device [Cc][Cc] row-major, q = W_q z; NULL = q from M^q */
+    const float *skip;         /* device [4][Cc] channel-wise skip D_r of each route:
+                                  Y_r = reads + D_r * Z_r before the fusion; NULL = none */
+    void *workspace;           /* device, >= vh_workspace_size() bytes, 16-byte aligned;
+                                  holds the normalised queries while the call runs */
+    size_t workspace_bytes;
 } vh_params;
 
 /* Fill *p with the pages' constants (gamma_eta 0.025, alpha_init 0.9, eps
@@ -143,8 +154,12 @@ void vh_params_init(vh_params *p);
  * M_t = M_{t-1} A_t + M_b B_t (App. B.4 Eq. (45)), computed through the shared
  * gain M_end = M_b G (Prop. 2 Eq. (46)).
  *
+ * With p->w_query set the readout query is the outer projection instead (see
+ * vh_params); with p->skip set, lambda_r * D_r * x is added per enabled route.
+ *
  * Errors: VH_ERR_INVALID_ARG (null/misaligned pointers, sizes < 1, dirs == 0,
- * chunk < 0, Cc != n_heads*d, alias), VH_ERR_UNSUPPORTED (head_dim or dtype),
+ * chunk < 0, Cc != n_heads*d, alias), VH_ERR_WORKSPACE (w_query without a large
+ * enough, 16-byte aligned workspace), VH_ERR_UNSUPPORTED (head_dim or dtype),
  * VH_ERR_CUDA (launch failure; the stream may then hold partial results).
  */
 vh_status vh_scan_forward(const void *x, const float *memories0, const vh_params *p,
@@ -170,7 +185,9 @@ vh_status vh_debug_permute(const void *x, const vh_params *p, int H, int W, int 
  */
 vh_status vh_check(const unsigned long long *stats, void *stream);
 
-/* Bytes of device workspace a vh_scan_forward call needs: always 0. */
+/* Bytes of device workspace a vh_scan_forward call with these parameters needs: 0 in
+ * the six-memory form, 6 * B * H * W * Cc (the normalised queries as three bf16
+ * pieces) when p->w_query is set.  NULL p gives 0. */
 size_t vh_workspace_size(const vh_params *p, int H, int W, unsigned dirs, int chunk);
 
 /* Static string for a status code. */

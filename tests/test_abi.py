@@ -61,6 +61,25 @@ def test_debug_permute_rejects_bad_route(vhlib):
     assert vhlib.lib().vh_debug_permute(FAKE, ctypes.byref(p), 3, 4, 4, FAKE * 64) == -1
 
 
+def test_workspace_is_sized_and_required(vhlib):
+    L = vhlib.lib()
+    p = vhlib.make_cparams(2, 64, 32, True)
+    assert L.vh_workspace_size(ctypes.byref(p), 5, 7, 15, 0) == 0
+    p.w_query = FAKE
+    assert L.vh_workspace_size(ctypes.byref(p), 5, 7, 15, 0) == 6 * 2 * 5 * 7 * 64
+    st, msg = _call(vhlib, B=2, Cc=64, d=32, H=5, W=7, w_query=FAKE)
+    assert st == -4 and "workspace" in msg
+    st, _ = _call(vhlib, B=2, Cc=64, d=32, H=5, W=7, w_query=FAKE, workspace=FAKE * 16,
+                  workspace_bytes=100)
+    assert st == -4
+    st, _ = _call(vhlib, B=2, Cc=64, d=32, H=5, W=7, w_query=FAKE, workspace=FAKE * 16 + 8,
+                  workspace_bytes=1 << 20)
+    assert st == -4
+    st, msg = _call(vhlib, B=2, Cc=64, d=32, H=5, W=7, w_query=FAKE, workspace=FAKE,
+                    workspace_bytes=1 << 20)
+    assert st == -1 and "alias" in msg
+
+
 def test_check_rejects_null_stats(vhlib):
     L = vhlib.lib()
     assert L.vh_check(None, None) == -1

@@ -48,6 +48,8 @@ class CParams(ctypes.Structure):
         ("forced_alpha", ctypes.c_float), ("control_flags", ctypes.c_uint),
         ("stats", ctypes.c_void_p), ("impl", ctypes.c_int), ("accumulate", ctypes.c_int),
         ("stream", ctypes.c_void_p),
+        ("w_query", ctypes.c_void_p), ("skip", ctypes.c_void_p),
+        ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
     ]
 
 
@@ -116,7 +118,8 @@ def _check(status: int):
 def make_cparams(batch: int, channels: int, head_dim: int, x_is_bf16: bool,
                  params: Optional[ScanParams] = None, *, dir_scale_ptr: int = 0,
                  memories_out_ptr: int = 0, stats_ptr: int = 0, stream_ptr: int = 0,
-                 accumulate: bool = False) -> CParams:
+                 accumulate: bool = False, w_query_ptr: int = 0, skip_ptr: int = 0,
+                 workspace_ptr: int = 0, workspace_bytes: int = 0) -> CParams:
     p = params or ScanParams()
     if p.impl not in IMPL:
         raise ValueError(f"impl must be one of {sorted(IMPL)}")
@@ -125,7 +128,8 @@ def make_cparams(batch: int, channels: int, head_dim: int, x_is_bf16: bool,
                    p.spec_inward, p.kk_floor, dir_scale_ptr or None, memories_out_ptr or None,
                    p.gate_mode, p.forced_eta, p.forced_alpha, p.control_flags,
                    stats_ptr or None, IMPL[p.impl], 1 if accumulate else 0,
-                   stream_ptr or None)
+                   stream_ptr or None, w_query_ptr or None, skip_ptr or None,
+                   workspace_ptr or None, workspace_bytes)
 
 
 def _stream_ptr(stream) -> int:
@@ -146,14 +150,18 @@ def _require_cuda(name, t, dtypes):
 
 def scan_forward(x, memories0, head_dim: int, dirs: int = DIR_ALL, chunk: int = 0, out=None,
                  params: Optional[ScanParams] = None, dir_scale=None, memories_out=None,
-                 stats=None, stream=None, accumulate: bool = False):
+                 stats=None, stream=None, accumulate: bool = False, w_query=None, skip=None,
+                 workspace=None):
     """VisionHOPE operator: x [B][H][W][Cc] (bf16/fp32, CUDA) -> out [B][H][W][Cc] fp32.
 
     memories0: fp32 [4][Cc/head_dim][4d^2+2d] initial state per (route, head).
     Optional: dir_scale fp32 [4][Cc]; memories_out fp32 [B][4][nh][4d^2+2d];
     stats uint64/int64 [8] (accumulated).  accumulate=True adds to ``out``
-    instead of overwriting it.  Runs on ``stream`` (default: torch's current
-    stream) asynchronously."""
+    instead of overwriting it.  w_query fp32 [Cc][Cc] selects the VisionHOPE-exact
+    readout (outer query projection shared by the routes) and skip fp32 [4][Cc] adds
+    the channel-wise skip; the query planes live in ``workspace`` (uint8, at least
+    vh_workspace_size bytes; allocated here when not given).  Runs on ``stream``
+    (default: torch's current stream) asynchronously."""
     import torch
     _require_cuda("x", x, (torch.bfloat16, torch.float32))
     _require_cuda("memories0", memories0, (torch.float32,))
@@ -172,11 +180,24 @@ def scan_forward(x, memories0, head_dim: int, dirs: int = DIR_ALL, chunk: int = 
         _require_cuda("memories_out", memories_out, (torch.float32,))
     if stats is not None:
         _require_cuda("stats", stats, (torch.int64, torch.uint64) if hasattr(torch, "uint64") else (torch.int64,))
+    if w_query is not None:
+        _require_cuda("w_query", w_query, (torch.float32,))
+    if skip is not None:
+        _require_cuda("skip", skip, (torch.float32,))
     cp = make_cparams(B, Cc, head_dim, x.dtype == torch.bfloat16, params,
                       dir_scale_ptr=dir_scale.data_ptr() if dir_scale is not None else 0,
                       memories_out_ptr=memories_out.data_ptr() if memories_out is not None else 0,
                       stats_ptr=stats.data_ptr() if stats is not None else 0,
-                      stream_ptr=_stream_ptr(stream), accumulate=accumulate)
+                      stream_ptr=_stream_ptr(stream), accumulate=accumulate,
+                      w_query_ptr=w_query.data_ptr() if w_query is not None else 0,
+                      skip_ptr=skip.data_ptr() if skip is not None else 0)
+    need = lib().vh_workspace_size(ctypes.byref(cp), H, W, dirs, chunk)
+    if need:
+        if workspace is None:
+            workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+        _require_cuda("workspace", workspace, (torch.uint8,))
+        cp.workspace = workspace.data_ptr()
+        cp.workspace_bytes = workspace.numel()
     _check(lib().vh_scan_forward(x.data_ptr(), memories0.data_ptr(), ctypes.byref(cp), H, W,
                                  dirs, chunk, out.data_ptr()))
     return out

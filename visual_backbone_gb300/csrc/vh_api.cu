@@ -10,6 +10,9 @@
 namespace vh {
 cudaError_t launch_scan_simt(const ScanArgs &a, int d, bool bf16, cudaStream_t st);
 cudaError_t launch_scan_tc(const ScanArgs &a, int d, bool bf16, cudaStream_t st, bool *handled);
+cudaError_t launch_qproj(const void *x, bool bf16, int d, const float *wq, const float *skip,
+                         const float *dir_scale, unsigned dirs, __nv_bfloat16 *qhat, float *out,
+                         int accumulate, long npix, int Cc, float knorm_eps, cudaStream_t st);
 }  // namespace vh
 
 namespace {
@@ -90,7 +93,11 @@ const char *vh_last_error(void) { return g_err; }
 
 int vh_version(void) { return 100; }
 
-size_t vh_workspace_size(const vh_params *, int, int, unsigned, int) { return 0; }
+size_t vh_workspace_size(const vh_params *p, int H, int W, unsigned, int)
+{
+    if (!p || !p->w_query || p->batch < 1 || H < 1 || W < 1 || p->channels < 1) return 0;
+    return (size_t)6 * p->batch * H * W * p->channels;
+}
 
 vh_status vh_check(const unsigned long long *stats, void *stream)
 {
@@ -134,6 +141,20 @@ vh_status vh_scan_forward(const void *x, const float *memories0, const vh_params
     const size_t obytes = (size_t)B * N * p->channels * 4;
     const char *xb = static_cast<const char *>(x), *oc = reinterpret_cast<const char *>(out);
     if (xb < oc + obytes && oc < xb + xbytes) return fail(VH_ERR_INVALID_ARG, "out aliases x");
+    const bool exact = p->w_query != nullptr;
+    if (exact) {
+        const size_t qbytes = (size_t)6 * B * N * p->channels;
+        const char *wb = static_cast<const char *>(p->workspace);
+        if (!wb || p->workspace_bytes < qbytes || !aligned16(wb))
+            return fail(VH_ERR_WORKSPACE, "w_query needs a 16-byte aligned workspace of %zu bytes "
+                        "(have %zu)", qbytes, p->workspace ? p->workspace_bytes : (size_t)0);
+        if ((wb < oc + obytes && oc < wb + qbytes) || (wb < xb + xbytes && xb < wb + qbytes))
+            return fail(VH_ERR_INVALID_ARG, "workspace aliases x or out");
+        if (reinterpret_cast<uintptr_t>(p->w_query) & 3u)
+            return fail(VH_ERR_INVALID_ARG, "w_query must be 4-byte aligned");
+    }
+    if (p->skip && (reinterpret_cast<uintptr_t>(p->skip) & 3u))
+        return fail(VH_ERR_INVALID_ARG, "skip must be 4-byte aligned");
 
     vh::ScanArgs a{};
     a.x = x;
@@ -159,14 +180,21 @@ vh_status vh_scan_forward(const void *x, const float *memories0, const vh_params
     a.forced_eta = p->forced_eta;
     a.forced_alpha = p->forced_alpha;
     a.control_flags = p->control_flags;
+    a.qhat = exact ? static_cast<const __nv_bfloat16 *>(p->workspace) : nullptr;
 
     cudaStream_t st = static_cast<cudaStream_t>(p->stream);
     cudaError_t e = cudaSuccess;
-    if (!p->accumulate) {
+    const bool bf16 = p->x_dtype == VH_DTYPE_BF16;
+    if (!p->accumulate && !p->skip) {
         e = cudaMemsetAsync(out, 0, obytes, st);
         if (e != cudaSuccess) return cuda_fail(e, "zeroing out");
     }
-    const bool bf16 = p->x_dtype == VH_DTYPE_BF16;
+    if (exact || p->skip) {  // outer queries and / or the skip term seeding out
+        e = vh::launch_qproj(x, bf16, d, p->w_query, p->skip, p->dir_scale, dirs,
+                             static_cast<__nv_bfloat16 *>(p->workspace), out, p->accumulate,
+                             (long)(B * N), p->channels, p->knorm_eps, st);
+        if (e != cudaSuccess) return cuda_fail(e, "query projection launch");
+    }
     bool handled = false;
     if (p->impl != VH_IMPL_SIMT) {
         e = vh::launch_scan_tc(a, d, bf16, st, &handled);

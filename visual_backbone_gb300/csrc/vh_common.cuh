@@ -34,7 +34,17 @@ struct ScanArgs {
     int gate_mode;
     float forced_eta, forced_alpha;
     unsigned control_flags;
+    // VisionHOPE-exact readout: normalised outer queries as three bf16 pieces
+    // [3][B][H][W][Cc] (piece p at qhat + p * B*H*W*Cc); nullptr = q from M^q
+    const __nv_bfloat16 *qhat;
 };
+
+// fp32 value of element e of the three-piece query planes (the pieces sum exactly).
+__device__ __forceinline__ float qhat_at(const __nv_bfloat16 *q, size_t plane, size_t e)
+{
+    return (__bfloat162float(q[e]) + __bfloat162float(q[e + plane])) +
+           __bfloat162float(q[e + 2 * plane]);
+}
 
 // Pixel visited at step t of route r on an H x W map (Eq. (24); the route
 // orders of the VMamba explainer: row-major, full reversal, transpose then

@@ -145,19 +145,24 @@ __global__ void __launch_bounds__(256) scan_simt_kernel(const ScanArgs a)
                 const float *pr = P + j * C::PS;
                 float kr[C::CPL], vv[C::CPL], qr[C::CPL];
                 float kk = 0.0f, qq = 0.0f;
+                // VisionHOPE-exact readout: the query of the token's pixel, already
+                // normalised, from the outer projection's planes
+                const size_t qo = a.qhat ? ((size_t)b * N + PIX[j]) * Cc + (size_t)h * D : 0;
+                const size_t qplane = (size_t)a.B * N * Cc;
 #pragma unroll
                 for (int m = 0; m < C::CPL; ++m) {
                     const int c = lane + 32 * m;
                     const bool ok = c < D;
                     kr[m] = ok ? pr[c] : 0.0f;
                     vv[m] = ok ? pr[D + c] : 0.0f;
-                    qr[m] = ok ? pr[2 * D + c] : 0.0f;
+                    qr[m] = ok ? (a.qhat ? qhat_at(a.qhat, qplane, qo + c) : pr[2 * D + c]) : 0.0f;
                     kk = fmaf(kr[m], kr[m], kk);
                     qq = fmaf(qr[m], qr[m], qq);
                 }
                 kk = warp_sum(kk);
                 qq = warp_sum(qq);
-                const float nk = sqrtf(kk + a.knorm_eps), nq = sqrtf(qq + a.knorm_eps);
+                const float nk = sqrtf(kk + a.knorm_eps);
+                const float nq = a.qhat ? 1.0f : sqrtf(qq + a.knorm_eps);
                 float kn2 = 0.0f, dd = 0.0f;
 #pragma unroll
                 for (int m = 0; m < C::CPL; ++m) {

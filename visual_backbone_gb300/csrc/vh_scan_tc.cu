@@ -55,6 +55,10 @@ constexpr int KS = D + 4;            // fp32 row stride of the key / delta tiles
 constexpr int ROW_ETA = 0, ROW_MEM = 16, S_ROWS = ROW_MEM + 4 * D;
 constexpr int S_PIECE = S_ROWS / 8 * SBO_K32;
 constexpr int Q_PIECE = TT * ROW_B;
+// VisionHOPE-exact readout: the outer queries' three pieces arrive by TMA, one box per
+// 8-channel group holding [piece][64 tokens][16 bytes]: K-group stride 3 KB, 8-row stride
+// 128 B, piece stride 1 KB (same 12 KB region as the in-kernel query pieces).
+constexpr int QX_LBO = 3 * TT * 16, QX_PIECE = TT * 16;
 constexpr int G_PIECE = D * ROW_B;
 // The gain as the update's B operand is MN-major (N contiguous): element (n, k) of piece p
 // at (4p + n/8) * 128 + (k/8) * G_KSTR + (k%8) * 16 + (n%8) * 2, so the three pieces stack
@@ -150,6 +154,16 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *tm,
         "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap *tm, int c0, int c1,
+                                            int c2, int c3, int c4, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(bar)
         : "memory");
 }
 
@@ -370,7 +384,9 @@ __device__ __forceinline__ void red_add_v4(float *addr, float4 v)
 
 __global__ void __launch_bounds__(NT, 3)
     scan_tc_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tm_row,
-                   const __grid_constant__ CUtensorMap tm_col)
+                   const __grid_constant__ CUtensorMap tm_col,
+                   const __grid_constant__ CUtensorMap tq_row,
+                   const __grid_constant__ CUtensorMap tq_col)
 {
     extern __shared__ __align__(1024) unsigned char sm[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -391,6 +407,8 @@ __global__ void __launch_bounds__(NT, 3)
     const uint32_t mb_x = smem_u32(&bars[0]), mb_gen = smem_u32(&bars[1]);
     const uint32_t mb_ro = smem_u32(&bars[2]), mb_upd = smem_u32(&bars[3]);
     const uint32_t mb_g = smem_u32(&bars[4]);
+    const uint32_t mb_q = smem_u32(&bars[5]);
+    const bool exact = a.qhat != nullptr;  // queries from the outer projection
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + OFF_BAR + 64);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + OFF_BAR + 72);
     volatile int *role_slot = reinterpret_cast<volatile int *>(sm + OFF_BAR + 76);
@@ -414,6 +432,7 @@ __global__ void __launch_bounds__(NT, 3)
         mbar_init(mb_ro, 1);
         mbar_init(mb_upd, 1);
         mbar_init(mb_g, 2);
+        mbar_init(mb_q, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         // Co-resident CTAs hold consecutive groups of four hardware warp slots, and warp w
         // of a CTA runs on SM sub-partition w.  Alternating the gain pair between warps 0-1
@@ -449,7 +468,18 @@ __global__ void __launch_bounds__(NT, 3)
     const bool gainw = (warp >> 1) == gp;
     const int ew = rw + 1;
     const bool issuer = warp == rw && lane == 0;
-    if (issuer) issue_x(0, 0);
+    const CUtensorMap *tq = rowr ? &tq_row : &tq_col;
+    auto issue_q = [&](int c, int s) {
+        mbar_expect_tx(mb_q, 3 * TT * D * 2);
+#pragma unroll
+        for (int q = 0; q < D / 8; ++q)
+            tma_load_5d(smem_u32(sQ + q * QX_LBO), tq, h * D + 8 * q, box_start(s), line_of(c), b, 0,
+                        mb_q);
+    };
+    if (issuer) {
+        issue_x(0, 0);
+        if (exact) issue_q(0, 0);
+    }
     {
         const float *m0 = a.mem0 + ((size_t)r * a.nh + h) * SZ;
         // memory rows 0..127 (k, v, q, m) -> operand rows 16..143: thread = row
@@ -483,7 +513,7 @@ __global__ void __launch_bounds__(NT, 3)
     const float *lam = a.dir_scale ? a.dir_scale + (size_t)r * Cc + (size_t)h * D : nullptr;
     float *ob = a.out + (size_t)b * H * W * Cc + (size_t)h * D;
     unsigned n_spec = 0, n_inj = 0, n_nf = 0;
-    uint32_t ph_x = 0, ph_gen = 0, ph_ro = 0, ph_upd = 0, ph_g = 0;
+    uint32_t ph_x = 0, ph_gen = 0, ph_ro = 0, ph_upd = 0, ph_g = 0, ph_q = 0;
 
     // gain state of the gain pair: its thread t owns row t/2 of G = gam * ghat, columns
     // 16(t%2)..+15
@@ -785,7 +815,7 @@ __global__ void __launch_bounds__(NT, 3)
             } else {
                 // ---- the token pair, while the gain runs: queries and the readout of this
                 // sub-tile
-                {
+                if (!exact) {
                     float qr[32];
                     tmem_ld32(tbase + lrow + COL_GEN + COL_QR, qr);
                     const float rq = __frsqrt_rn(sumsq32(qr) + a.knorm_eps);
@@ -793,22 +823,48 @@ __global__ void __launch_bounds__(NT, 3)
                     for (int e = 0; e < 32; ++e) qr[e] *= rq;
 #pragma unroll
                     for (int g = 0; g < 4; ++g) store_split8(sQ + op_off(jq, g), Q_PIECE, qr + 8 * g);
+                    fence_async_smem();
+                    tc_before();
+                    named_sync(1, 64);
+                    tc_after();
                 }
-                fence_async_smem();
-                tc_before();
-                named_sync(1, 64);
-                tc_after();
                 // MMA 2: readout y = q M^m_b^T, Eq. (16) (six split cross terms), M = 128 with
-                // the queries as rows 32 rw..32 rw+63 (the other 64 A rows read the 4 KB next
-                // to each piece)
-                if (issuer && !*abort_flag) {
-                    mma_split6<Q_PIECE, S_PIECE>(tbase + COL_RO, smem_u32(sQ) - (rw >> 1) * 8 * SBO_K32,
-                                                 smem_u32(sS) + (ROW_MEM + 3 * D) / 8 * SBO_K32,
-                                                 idesc_bf16(128, 32));
-                    mma_commit(mb_ro);
+                // the queries as rows 32 rw..32 rw+63 (the other 64 A rows read the region
+                // next to each piece).  The outer queries of the VisionHOPE-exact readout
+                // arrive by TMA in their own layout.
+                if (issuer) {
+                    if (!exact) {
+                        if (!*abort_flag) {
+                            mma_split6<Q_PIECE, S_PIECE>(
+                                tbase + COL_RO, smem_u32(sQ) - (rw >> 1) * 8 * SBO_K32,
+                                smem_u32(sS) + (ROW_MEM + 3 * D) / 8 * SBO_K32, idesc_bf16(128, 32));
+                            mma_commit(mb_ro);
+                        }
+                    } else if (wt.wait(mb_q, ph_q) && !*abort_flag) {
+                        constexpr int pa[6] = {0, 0, 1, 0, 2, 1};
+                        constexpr int pb[6] = {0, 1, 0, 2, 0, 1};
+                        const uint64_t da = sdesc(smem_u32(sQ) - (rw >> 1) * 8 * SBO_X, QX_LBO, SBO_X);
+                        const uint64_t db =
+                            sdesc(smem_u32(sS) + (ROW_MEM + 3 * D) / 8 * SBO_K32, LBO_K32, SBO_K32);
+#pragma unroll
+                        for (int t = 0; t < 6; ++t)
+#pragma unroll
+                            for (int ks = 0; ks < 2; ++ks)
+                                mma(tbase + COL_RO, dadd(da, pa[t] * QX_PIECE + ks * 2 * QX_LBO),
+                                    dadd(db, pb[t] * S_PIECE + ks * 2 * LBO_K32), idesc_bf16(128, 32),
+                                    (t | ks) != 0);
+                        mma_commit(mb_ro);
+                    }
                 }
+                if (exact) ph_q ^= 1;
                 wt.wait(mb_ro, ph_ro);
                 tc_after();
+                // the query tile is free again: fetch the next sub-tile's outer queries
+                if (exact && issuer && !*abort_flag) {
+                    const int ns = (s + 1 < nsub) ? s + 1 : 0;
+                    const int nc = (s + 1 < nsub) ? c : c + 1;
+                    if (nc < nlines) issue_q(nc, ns);
+                }
                 // readout epilogue: lambda_r y added at the token's pixel (Eq. (26))
                 float y[32];
                 tmem_ld32(tbase + lrow + COL_RO, y);
@@ -973,6 +1029,30 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
     return fn;
 }
 
+// 5-D view of the outer-query pieces [3][B][H][W][Cc] bf16: (channel, position along the
+// line, line, image, piece); a box is 8 channels x 64 positions x all 3 pieces.
+bool make_qmap(CUtensorMap *m, const void *q, int B, int H, int W, int Cc, bool rows)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t e = 2;
+    cuuint64_t dims[5], strides[4];
+    dims[0] = (cuuint64_t)Cc;
+    dims[1] = (cuuint64_t)(rows ? W : H);
+    dims[2] = (cuuint64_t)(rows ? H : W);
+    dims[3] = (cuuint64_t)B;
+    dims[4] = 3;
+    strides[0] = rows ? (cuuint64_t)Cc * e : (cuuint64_t)W * Cc * e;
+    strides[1] = rows ? (cuuint64_t)W * Cc * e : (cuuint64_t)Cc * e;
+    strides[2] = (cuuint64_t)H * W * Cc * e;
+    strides[3] = (cuuint64_t)B * H * W * Cc * e;
+    const cuuint32_t box[5] = {8, (cuuint32_t)TT, 1, 1, 3};
+    const cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(q), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 4-D view of x [B][H][W][Cc] bf16 with dims (channel, position along the line,
 // line, image); row routes walk W inside a row, column routes walk H inside a column.
 bool make_map(CUtensorMap *m, const void *x, int B, int H, int W, int Cc, bool rows)
@@ -1007,10 +1087,18 @@ cudaError_t launch_scan_tc(const ScanArgs &a, int d, bool bf16, cudaStream_t st,
     if (d != tc::D || !bf16 || !aligned || (a.Cc % 8) != 0 || !a16(a.mem0) ||
         (a.mem_out && !a16(a.mem_out)))
         return cudaSuccess;
-    CUtensorMap mr, mc;
+    CUtensorMap mr, mc, qr, qc;
     if (!tc::make_map(&mr, a.x, a.B, a.H, a.W, a.Cc, true) ||
         !tc::make_map(&mc, a.x, a.B, a.H, a.W, a.Cc, false))
         return cudaErrorInvalidValue;
+    if (a.qhat) {
+        if (!tc::make_qmap(&qr, a.qhat, a.B, a.H, a.W, a.Cc, true) ||
+            !tc::make_qmap(&qc, a.qhat, a.B, a.H, a.W, a.Cc, false))
+            return cudaErrorInvalidValue;
+    } else {
+        qr = mr;  // not read
+        qc = mc;
+    }
     static int attr_set[64] = {0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -1022,7 +1110,7 @@ cudaError_t launch_scan_tc(const ScanArgs &a, int d, bool bf16, cudaStream_t st,
         attr_set[dev] = 1;
     }
     const unsigned grid = (unsigned)(a.B * a.ndirs * a.nh);
-    tc::scan_tc_kernel<<<grid, tc::NT, tc::SMEM_BYTES, st>>>(a, mr, mc);
+    tc::scan_tc_kernel<<<grid, tc::NT, tc::SMEM_BYTES, st>>>(a, mr, mc, qr, qc);
     *handled = true;
     return cudaGetLastError();
 }
