@@ -180,14 +180,16 @@ def job_throughput(tokens_per_rank_step, steps, world, seconds):
 
 # --------------------------------------------------------- oracle timing
 
-def time_oracle(wl, images, nthreads, min_seconds=0.0, max_passes=1000):
+def time_oracle(wl, images, nthreads, min_seconds=0.0, max_passes=1000, w_query=None, skip=None):
     """Tokens/s of the oracle over `images` images, repeated until `min_seconds`
-    of wall time have passed; returns (tokens/s, seconds, passes)."""
+    of wall time have passed; returns (tokens/s, seconds, passes).  w_query / skip
+    (numpy) select the VisionHOPE-exact readout."""
     import oracle
     from visual_backbone_gb300 import synth
     oracle.build()
     inp = synth.make_inputs(wl, batch=images)
-    p = oracle.OracleParams(eta_bias=wl.eta_bias, alpha_init=wl.alpha_init)
+    p = oracle.OracleParams(eta_bias=wl.eta_bias, alpha_init=wl.alpha_init, w_query=w_query,
+                            skip=skip)
     t0 = time.perf_counter()
     passes = 0
     while True:
@@ -246,7 +248,7 @@ def workload_config(wl, args):
             "global_batch": wl.B * dist_env()[1], "tokens_per_step_per_gpu": wl.tokens,
             "parallelism": f"dp{dist_env()[1]} (images split across GPUs, no collective)",
             "l2": "256 MiB buffer written between timed steps (L2 is 129 MB)",
-            "kernel": args.kernel}
+            "kernel": args.kernel, "readout": args.readout}
 
 
 # ------------------------------------------------------------ our arm
@@ -278,6 +280,14 @@ def run_ours(args, wl):
     flush = torch.empty(64 << 20, dtype=torch.float32, device=dev)  # 256 MiB > L2
     params = vh.ScanParams(eta_bias=wl.eta_bias, alpha_init=wl.alpha_init, impl=args.kernel)
     stream = torch.cuda.Stream(device=dev)
+    # VisionHOPE-exact readout (outer query projection + channel-wise skip), random weights
+    extra = {}
+    if args.readout == "outer":
+        g = torch.Generator(device="cpu").manual_seed(1234)
+        extra["w_query"] = (torch.randn(wl.Cc, wl.Cc, generator=g) / wl.Cc ** 0.5).to(dev)
+        extra["skip"] = torch.randn(4, wl.Cc, generator=g).to(dev)
+        extra["workspace"] = torch.empty(6 * wl.B * wl.H * wl.W * wl.Cc, dtype=torch.uint8,
+                                         device=dev)
 
     def step(ev_start, ev_mid, ev_end):
         flush.zero_()
@@ -285,7 +295,7 @@ def run_ours(args, wl):
         out.zero_()
         ev_mid.record(stream)
         vh.scan_forward(x, mem0, wl.d, chunk=wl.chunk, out=out, params=params, stream=stream,
-                        accumulate=True)
+                        accumulate=True, **extra)
         ev_end.record(stream)
 
     with torch.cuda.stream(stream):
@@ -324,7 +334,8 @@ def run_ours(args, wl):
     with torch.cuda.stream(stream):
         def e2e_step():
             x.copy_(x_pin, non_blocking=True)
-            vh.scan_forward(x, mem0, wl.d, chunk=wl.chunk, out=out, params=params, stream=stream)
+            vh.scan_forward(x, mem0, wl.d, chunk=wl.chunk, out=out, params=params, stream=stream,
+                            **extra)
             out_pin.copy_(out, non_blocking=True)
         for _ in range(2):
             e2e_step()
@@ -377,12 +388,15 @@ def run_ours(args, wl):
             "e2e": {"value": e2e_value, "unit": UNIT,
                     "h2d_bytes_per_step": int(x_host.numel() * x_host.element_size()),
                     "d2h_bytes_per_step": int(out.numel() * 4), "steps": e2e_steps},
-            "gpu_launches": args.steps,
+            "gpu_launches": args.steps * (2 if args.readout == "outer" else 1),
             "clocks": sampler.summary(t0, t1) if sampler else None,
         }
         if world == 1 and not args.no_cpu_baseline:
             cores = min(cpu_cores(), args.cpu_images * wl.nh)
-            v, dt, passes = time_oracle(wl, args.cpu_images, cores, min_seconds=args.cpu_seconds)
+            v, dt, passes = time_oracle(
+                wl, args.cpu_images, cores, min_seconds=args.cpu_seconds,
+                w_query=extra["w_query"].double().cpu().numpy() if extra else None,
+                skip=extra["skip"].double().cpu().numpy() if extra else None)
             line["cpu_baseline"] = {
                 "value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
                 "sample": f"{passes} pass(es) over {args.cpu_images} of {wl.B} images of the "
@@ -402,6 +416,9 @@ def main(argv=None):
     ap.add_argument("--workload", default="stage1")
     ap.add_argument("--variant", choices=["plain", "longmem"], default="plain")
     ap.add_argument("--kernel", choices=["auto", "simt", "tc"], default="auto")
+    ap.add_argument("--readout", choices=["memory", "outer"], default="memory",
+                    help="memory: six-memory form (q from M^q); outer: VisionHOPE-exact "
+                         "readout with an outer query projection and channel-wise skip")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-images", type=int, default=16)
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
