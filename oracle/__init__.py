@@ -22,6 +22,11 @@ _LIB = os.path.join(_HERE, "libvh_oracle.so")
 
 NO_INJ_CAP = 1
 NO_SPEC_CLAMP = 2
+HARD_INJ = 4
+SOFT_SPEC = 8
+NO_DGD = 16
+FREEZE_KV = 32
+FREEZE_DYN = 64
 
 
 def build(force: bool = False) -> str:
