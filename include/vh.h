@@ -52,9 +52,22 @@ typedef enum { VH_DTYPE_F32 = 0, VH_DTYPE_BF16 = 1 } vh_dtype;
 
 enum { VH_DIR_RIGHT = 1, VH_DIR_LEFT = 2, VH_DIR_DOWN = 4, VH_DIR_UP = 8, VH_DIR_ALL = 15 };
 
-/* Step-control switches for ablations (VisionHOPE Sec. 3.5 "removing either
- * control leaves the other unchanged"). */
-enum { VH_CTRL_NO_INJ_CAP = 1, VH_CTRL_NO_SPEC_CLAMP = 2 };
+/* Ablation switches ("VisionHOPE" Sec. 3.5 and App. C.5):
+ *   VH_CTRL_NO_INJ_CAP     no injection control (eta_bar = eta)
+ *   VH_CTRL_NO_SPEC_CLAMP  no spectral control (eta_tilde = eta_bar)
+ *   VH_CTRL_HARD_INJ       injection clamp min(eta, eta_inj) instead of the soft cap
+ *   VH_CTRL_SOFT_SPEC      soft spectral cap eta_spec (1 - exp(-eta_bar / eta_spec))
+ *                          instead of the clamp min(eta_bar, eta_spec)
+ *   VH_CTRL_NO_DGD         no key-dependent DGD correction -eta_tilde M k k^T
+ *   VH_CTRL_FREEZE_KV      M^k, M^v fixed within the image (no adaptive K/V)
+ *   VH_CTRL_FREEZE_DYN     m^eta, m^alpha fixed within the image (no adaptive dynamics)
+ * NO_INJ_CAP takes precedence over HARD_INJ and NO_SPEC_CLAMP over SOFT_SPEC; other
+ * bits are rejected. */
+enum {
+    VH_CTRL_NO_INJ_CAP = 1, VH_CTRL_NO_SPEC_CLAMP = 2, VH_CTRL_HARD_INJ = 4,
+    VH_CTRL_SOFT_SPEC = 8, VH_CTRL_NO_DGD = 16, VH_CTRL_FREEZE_KV = 32, VH_CTRL_FREEZE_DYN = 64,
+    VH_CTRL_ALL = 127
+};
 
 /* Gate test hooks. */
 enum {

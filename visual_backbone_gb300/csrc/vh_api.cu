@@ -134,6 +134,8 @@ vh_status vh_scan_forward(const void *x, const float *memories0, const vh_params
     if (!(p->alpha_init > 0.0f && p->alpha_init < 1.0f))
         return fail(VH_ERR_INVALID_ARG, "alpha_init %g must lie in (0,1)", (double)p->alpha_init);
     if (p->impl < VH_IMPL_AUTO || p->impl > VH_IMPL_TC) return fail(VH_ERR_INVALID_ARG, "impl %d", p->impl);
+    if (p->control_flags & ~(unsigned)VH_CTRL_ALL)
+        return fail(VH_ERR_INVALID_ARG, "control_flags 0x%x has unknown bits", p->control_flags);
 
     const int d = p->head_dim, nh = p->channels / d, B = p->batch;
     const size_t N = (size_t)H * W;

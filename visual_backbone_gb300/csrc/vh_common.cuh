@@ -78,6 +78,8 @@ struct StepOut {
 
 // `oma` = 1 - alpha, passed separately so it keeps its relative precision near alpha = 1.
 // Quotients use the hardware reciprocal (a few ulp): far inside the fp32 path's error.
+// kAbl = false compiles the method as defined (every ablation switch off).
+template <bool kAbl = true>
 __device__ __forceinline__ StepOut step_control(const ScanArgs &a, float eta, float alpha,
                                                 float oma, float kk, float dd)
 {
@@ -85,8 +87,10 @@ __device__ __forceinline__ StepOut step_control(const ScanArgs &a, float eta, fl
     const float r = sqrtf(dd + a.eps * a.eps) + a.eps;
     const float eta_inj = __fdividef(a.inj_factor * oma, r);
     float eta_bar;
-    if (a.control_flags & VH_CTRL_NO_INJ_CAP)
+    if (kAbl && (a.control_flags & VH_CTRL_NO_INJ_CAP))
         eta_bar = eta;
+    else if (kAbl && (a.control_flags & VH_CTRL_HARD_INJ))
+        eta_bar = fminf(eta, eta_inj);  // injection clamp (ablation)
     else if (eta_inj > 0.0f)
         eta_bar = eta_inj * (-expm1f(-__fdividef(eta, eta_inj)));
     else
@@ -94,11 +98,23 @@ __device__ __forceinline__ StepOut step_control(const ScanArgs &a, float eta, fl
     float spec = __fdividef(a.spec_factor * 2.0f * alpha, fmaxf(kk, a.kk_floor));
     // one step toward zero (spec >= 0): the next representable value below
     if (spec > 0.0f) spec = __int_as_float(__float_as_int(spec) - 1);
-    const bool clamp = !(a.control_flags & VH_CTRL_NO_SPEC_CLAMP);
+    const bool clamp = !(kAbl && (a.control_flags & VH_CTRL_NO_SPEC_CLAMP));
     o.spec_active = clamp && spec < eta_bar;
-    o.eta_tilde = o.spec_active ? spec : eta_bar;
+    if (kAbl && clamp && (a.control_flags & VH_CTRL_SOFT_SPEC))  // soft spectral cap (ablation)
+        o.eta_tilde = spec > 0.0f ? spec * (-expm1f(-__fdividef(eta_bar, spec))) : 0.0f;
+    else
+        o.eta_tilde = o.spec_active ? spec : eta_bar;
     o.inj_ratio_gt1 = eta > eta_inj;
     return o;
+}
+
+// Row o of the (4d + 2) x d state (k, v, q, m memories, then the eta and alpha rows) is
+// held fixed within the image by an ablation switch.
+template <bool kAbl = true>
+__device__ __forceinline__ bool frozen_row(const ScanArgs &a, int o, int d)
+{
+    return kAbl && (((a.control_flags & VH_CTRL_FREEZE_KV) && o < 2 * d) ||
+                    ((a.control_flags & VH_CTRL_FREEZE_DYN) && o >= 4 * d));
 }
 
 // Raw step and retention from the scalar memory outputs, Eq. (53).

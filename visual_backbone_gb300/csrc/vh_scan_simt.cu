@@ -79,6 +79,7 @@ __global__ void __launch_bounds__(256) scan_simt_kernel(const ScanArgs a)
     const float *m0 = a.mem0 + ((size_t)r * a.nh + h) * SZ;
     for (int e = tid; e < C::R * D; e += C::NT) S[(e / D) * C::SS + (e % D)] = m0[e];
 
+    const float dgd = (a.control_flags & VH_CTRL_NO_DGD) ? 0.0f : 1.0f;
     const int grow = tid / C::TPR;
     const int gc0 = (tid % C::TPR) * C::CPT;
     float G[C::CPT];
@@ -234,7 +235,8 @@ __global__ void __launch_bounds__(256) scan_simt_kernel(const ScanArgs a)
                 }
             }
 
-            // 5. shared gain over the tile's tokens (rows are independent)
+            // 5. shared gain over the tile's tokens (rows are independent); without the
+            // DGD correction (ablation) the G k term drops: G <- alpha G - eta delta k^T
             for (int j = 0; j < Lt; ++j) {
                 const float *kj = K + j * D;
                 float part = 0.0f;
@@ -242,7 +244,7 @@ __global__ void __launch_bounds__(256) scan_simt_kernel(const ScanArgs a)
                 for (int c = 0; c < C::CPT; ++c) part = fmaf(G[c], kj[gc0 + c], part);
 #pragma unroll
                 for (int o = C::TPR / 2; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-                const float s = SC[2 * j + 1] * (part + DL[j * D + grow]);
+                const float s = SC[2 * j + 1] * (part * dgd + DL[j * D + grow]);
                 const float al = SC[2 * j];
 #pragma unroll
                 for (int c = 0; c < C::CPT; ++c) G[c] = fmaf(-s, kj[gc0 + c], al * G[c]);
@@ -255,6 +257,7 @@ __global__ void __launch_bounds__(256) scan_simt_kernel(const ScanArgs a)
         for (int c = 0; c < C::CPT; ++c) Gs[grow * D + gc0 + c] = G[c];
         __syncthreads();
         for (int o = warp; o < C::R; o += C::NW) {
+            if (frozen_row(a, o, D)) continue;  // ablation: memory fixed within the image
             const float *srow = S + o * C::SS;
             float acc[C::CPL];
 #pragma unroll

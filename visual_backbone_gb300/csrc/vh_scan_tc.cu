@@ -382,6 +382,9 @@ __device__ __forceinline__ void red_add_v4(float *addr, float4 v)
                  : "memory");
 }
 
+// kAbl: the ablation switches of the step control and the memories are compiled in
+// (false for the method as defined, so its hot loops carry no test of them).
+template <bool kAbl>
 __global__ void __launch_bounds__(NT, 3)
     scan_tc_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tm_row,
                    const __grid_constant__ CUtensorMap tm_col,
@@ -519,6 +522,9 @@ __global__ void __launch_bounds__(NT, 3)
     // 16(t%2)..+15
     float gh[16];
     float gam = 1.0f, inv_gam = 1.0f;
+    // without the DGD correction (ablation) the G k terms of the recurrence drop:
+    // G_j = alpha G_{j-1} - eta delta k^T
+    const bool no_dgd = kAbl && (a.control_flags & VH_CTRL_NO_DGD) != 0;
     // this thread's token (box row) when in the token pair: lane l of warp w holds box row
     // 32(w - rw) + l, TMEM lane 32 rw + that row
     const int jq = 32 * (warp - rw) + lane;
@@ -605,7 +611,7 @@ __global__ void __launch_bounds__(NT, 3)
                     if (a.gate_mode == VH_GATE_FORCED_EXEC) {
                         eta_t = a.forced_eta;
                     } else {
-                        const StepOut so = step_control(a, eta, alpha, oma, sc.z, sc.w);
+                        const StepOut so = step_control<kAbl>(a, eta, alpha, oma, sc.z, sc.w);
                         eta_t = so.eta_tilde;
                         n_spec += so.spec_active;
                         n_inj += so.inj_ratio_gt1;
@@ -692,6 +698,7 @@ __global__ void __launch_bounds__(NT, 3)
                     for (int e = 4; e < 16; ++e) p4[e & 3] = fmaf(gh[e], t.k[e], p4[e & 3]);
                     float dot = (p4[0] + p4[1]) + (p4[2] + p4[3]);
                     dot += __shfl_xor_sync(0xffffffffu, dot, 1);
+                    if (no_dgd) dot = 0.0f;
                     if (!chk || t.c.z != 0.0f) {
                         const float sc = -t.c.y * fmaf(t.d, inv_gam, dot);
 #pragma unroll
@@ -741,8 +748,8 @@ __global__ void __launch_bounds__(NT, 3)
                             cb[t] = SC[j + t];
                             db[t] = DLf[(j + t) * KS + grow];
                         }
-                        const float4 g0 = *reinterpret_cast<const float4 *>(GT + (j / NB) * 8);
-                        const float2 g1 = *reinterpret_cast<const float2 *>(GT + (j / NB) * 8 + 4);
+                        float4 g0 = *reinterpret_cast<const float4 *>(GT + (j / NB) * 8);
+                        float2 g1 = *reinterpret_cast<const float2 *>(GT + (j / NB) * 8 + 4);
                         float av[NB];
 #pragma unroll
                         for (int t = 0; t < NB; ++t) {
@@ -756,6 +763,12 @@ __global__ void __launch_bounds__(NT, 3)
                         }
 #pragma unroll
                         for (int t = 0; t < NB; ++t) av[t] += __shfl_xor_sync(0xffffffffu, av[t], 1);
+                        if (no_dgd) {
+#pragma unroll
+                            for (int t = 0; t < NB; ++t) av[t] = 0.0f;
+                            g0 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                            g1 = make_float2(0.0f, 0.0f);
+                        }
                         float iv = inv_gam;
                         const float s0 = -cb[0].y * fmaf(db[0], iv, av[0]);
                         iv *= cb[0].z;
@@ -914,7 +927,7 @@ __global__ void __launch_bounds__(NT, 3)
                 tc_after();
                 // the 1 x d eta and alpha rows on CUDA cores, in fp32 (lane = column); their
                 // operand rows are read by no pending MMA
-                if (warp == ew) {
+                if (warp == ew && !(kAbl && (a.control_flags & VH_CTRL_FREEZE_DYN))) {
                     float ne = 0.0f, na = 0.0f;
 #pragma unroll 8
                     for (int l = 0; l < D; ++l) {
@@ -953,7 +966,14 @@ __global__ void __launch_bounds__(NT, 3)
                 tmem_ld32(tbase + lrow + COL_UPD + 2 * D, w);
 #pragma unroll
                 for (int e = 0; e < 32; ++e) v[e] += w[e];
-                const bool add_mb = *delta_form != 0;
+                // a memory held fixed by an ablation switch keeps M_b (recovered from its
+                // pieces for memories_out) and its operand rows are not rewritten
+                const bool frz = frozen_row<kAbl>(a, tid, D);
+                if (frz) {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) v[e] = 0.0f;
+                }
+                const bool add_mb = frz || *delta_form != 0;
 #pragma unroll
                 for (int g = 0; g < 4; ++g) {
                     unsigned char *src = sS + op_off(ROW_MEM + tid, g);
@@ -968,7 +988,7 @@ __global__ void __launch_bounds__(NT, 3)
                             v[8 * g + 2 * i + 1] += (bf16_hi(w1[i]) + bf16_hi(w2[i])) + bf16_hi(w3[i]);
                         }
                     }
-                    store_split8(src, S_PIECE, v + 8 * g);
+                    if (!frz) store_split8(src, S_PIECE, v + 8 * g);
                 }
                 if (c == nlines - 1 && a.mem_out) {
                     float *mo = a.mem_out + (((size_t)b * 4 + r) * a.nh + h) * SZ;
@@ -1104,13 +1124,19 @@ cudaError_t launch_scan_tc(const ScanArgs &a, int d, bool bf16, cudaStream_t st,
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 64 && !attr_set[dev]) {
-        e = cudaFuncSetAttribute(tc::scan_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 tc::SMEM_BYTES);
+        e = cudaFuncSetAttribute(tc::scan_tc_kernel<false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, tc::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(tc::scan_tc_kernel<true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, tc::SMEM_BYTES);
         if (e != cudaSuccess) return e;
         attr_set[dev] = 1;
     }
     const unsigned grid = (unsigned)(a.B * a.ndirs * a.nh);
-    tc::scan_tc_kernel<<<grid, tc::NT, tc::SMEM_BYTES, st>>>(a, mr, mc, qr, qc);
+    if (a.control_flags)
+        tc::scan_tc_kernel<true><<<grid, tc::NT, tc::SMEM_BYTES, st>>>(a, mr, mc, qr, qc);
+    else
+        tc::scan_tc_kernel<false><<<grid, tc::NT, tc::SMEM_BYTES, st>>>(a, mr, mc, qr, qc);
     *handled = true;
     return cudaGetLastError();
 }
