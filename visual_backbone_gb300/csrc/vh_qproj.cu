@@ -161,10 +161,21 @@ cudaError_t launch_d(const void *x, const float *wq, const float *skip, const fl
 
 }  // namespace
 
+namespace tc {
+cudaError_t launch_qproj_tc(const void *x, bool bf16, int d, const float *wq, const float *skip,
+                            const float *dir_scale, unsigned dirs, __nv_bfloat16 *qhat, float *out,
+                            int accumulate, long npix, int Cc, float knorm_eps, cudaStream_t st,
+                            bool *handled);
+}
+
 cudaError_t launch_qproj(const void *x, bool bf16, int d, const float *wq, const float *skip,
                          const float *dir_scale, unsigned dirs, __nv_bfloat16 *qhat, float *out,
                          int accumulate, long npix, int Cc, float knorm_eps, cudaStream_t st)
 {
+    bool handled = false;
+    const cudaError_t e = tc::launch_qproj_tc(x, bf16, d, wq, skip, dir_scale, dirs, qhat, out,
+                                              accumulate, npix, Cc, knorm_eps, st, &handled);
+    if (e != cudaSuccess || handled) return e;
 #define VH_QP(DD)                                                                              \
     return bf16 ? launch_d<DD, __nv_bfloat16>(x, wq, skip, dir_scale, dirs, qhat, out,        \
                                                accumulate, npix, Cc, knorm_eps, st)            \
