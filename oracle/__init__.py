@@ -27,6 +27,7 @@ SOFT_SPEC = 8
 NO_DGD = 16
 FREEZE_KV = 32
 FREEZE_DYN = 64
+INTRA_READ = 128
 
 
 def build(force: bool = False) -> str:

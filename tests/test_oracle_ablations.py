@@ -140,3 +140,36 @@ def test_chunk_one_equals_token_indexed_with_switches(orc, flags):
     b, mb = orc.forward(x, mem0, 3, 4, 2, 5, params=p, want_memories=True, token_indexed_mode=True)
     np.testing.assert_allclose(a, b, rtol=1e-11, atol=1e-14)
     np.testing.assert_allclose(ma, mb, rtol=1e-11, atol=1e-14)
+
+
+def test_intra_chunk_readout_equals_boundary_readout_at_chunk_one(orc):
+    rng = np.random.default_rng(16)
+    x, mem0 = _tiny_inputs(rng, 1, 3, 4, 2, 5)
+    p0 = orc.OracleParams(eta_bias=1.0)
+    p1 = orc.OracleParams(eta_bias=1.0, control_flags=orc.INTRA_READ)
+    a = orc.forward(x, mem0, 3, 4, 2, 5, chunk_len=1, params=p0)
+    b = orc.forward(x, mem0, 3, 4, 2, 5, chunk_len=1, params=p1)
+    np.testing.assert_array_equal(a, b)
+    c = orc.forward(x, mem0, 3, 4, 2, 5, params=p0)
+    e = orc.forward(x, mem0, 3, 4, 2, 5, params=p1)
+    assert not np.allclose(c, e)   # differs once a chunk holds several tokens
+
+
+def test_intra_chunk_readout_is_boundary_state_times_gain(orc):
+    """y_t = M^m_b G_{t-1} q_t with the gain recursion built here from the tokens' own
+    (k, delta, alpha, eta_tilde) -- the shared-gain form of the working state (Prop. 2)."""
+    rng = np.random.default_rng(17)
+    d, L = 6, 10
+    S = _rand_state(rng, d)
+    xs = rng.standard_normal((L, d)) * 2.0
+    p = orc.OracleParams(eta_bias=2.0, control_flags=orc.INTRA_READ)
+    _, y, diag = orc.chunk(S, xs, p)
+    f = orc.diag_fields(d)
+    Mm = orc.split_memories(S, d)["m"]
+    G = np.eye(d)
+    for t in range(L):
+        q = diag[t, f["q"]]
+        np.testing.assert_allclose(y[t], Mm @ G @ q, rtol=1e-10, atol=1e-13)
+        k, dl = diag[t, f["k"]], diag[t, f["delta"]]
+        al, et = diag[t, f["alpha"]], diag[t, f["eta_tilde"]]
+        G = G @ (al * np.eye(d) - et * np.outer(k, k)) - et * np.outer(dl, k)
