@@ -61,12 +61,17 @@ enum { VH_DIR_RIGHT = 1, VH_DIR_LEFT = 2, VH_DIR_DOWN = 4, VH_DIR_UP = 8, VH_DIR
  *   VH_CTRL_NO_DGD         no key-dependent DGD correction -eta_tilde M k k^T
  *   VH_CTRL_FREEZE_KV      M^k, M^v fixed within the image (no adaptive K/V)
  *   VH_CTRL_FREEZE_DYN     m^eta, m^alpha fixed within the image (no adaptive dynamics)
+ *   VH_CTRL_INTRA_READ     intra-chunk readout: token t reads the working content memory
+ *                          M^m_b G_{t-1} (Prop. 2's shared gain before its own update)
+ *                          instead of the chunk's boundary state M^m_b (Eq. (16)); the two
+ *                          agree at chunk length 1.  The tensor-core kernel runs this switch
+ *                          with 9.5 KB more shared memory per CTA (two CTAs per SM).
  * NO_INJ_CAP takes precedence over HARD_INJ and NO_SPEC_CLAMP over SOFT_SPEC; other
  * bits are rejected. */
 enum {
     VH_CTRL_NO_INJ_CAP = 1, VH_CTRL_NO_SPEC_CLAMP = 2, VH_CTRL_HARD_INJ = 4,
     VH_CTRL_SOFT_SPEC = 8, VH_CTRL_NO_DGD = 16, VH_CTRL_FREEZE_KV = 32, VH_CTRL_FREEZE_DYN = 64,
-    VH_CTRL_ALL = 127
+    VH_CTRL_INTRA_READ = 128, VH_CTRL_ALL = 255
 };
 
 /* Gate test hooks. */

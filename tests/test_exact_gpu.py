@@ -20,12 +20,14 @@ def _extras(Cc, seed):
     return wq, skip, lam
 
 
-def _run(vhlib, inp, wq, skip, lam, impl, dirs=15, want_memories=True, accumulate_on=None):
+def _run(vhlib, inp, wq, skip, lam, impl, dirs=15, want_memories=True, accumulate_on=None,
+         flags=0):
     import torch
     wl = inp.wl
     x = to_device_x(inp)
     mem0 = torch.from_numpy(inp.mem0).cuda()
-    vhp = vhlib.ScanParams(eta_bias=wl.eta_bias, alpha_init=wl.alpha_init, impl=impl)
+    vhp = vhlib.ScanParams(eta_bias=wl.eta_bias, alpha_init=wl.alpha_init, impl=impl,
+                           control_flags=flags)
     mo = (torch.full((x.shape[0], 4, wl.nh, 4 * wl.d * wl.d + 2 * wl.d), float("nan"),
                      device="cuda") if want_memories else None)
     st = torch.zeros(8, dtype=torch.int64, device="cuda")
@@ -41,10 +43,10 @@ def _run(vhlib, inp, wq, skip, lam, impl, dirs=15, want_memories=True, accumulat
     return out.cpu().numpy(), (mo.cpu().numpy() if mo is not None else None), st.cpu().numpy()
 
 
-def _oracle(orc, vhlib, inp, wq, skip, lam, dirs=15):
+def _oracle(orc, vhlib, inp, wq, skip, lam, dirs=15, flags=0):
     wl = inp.wl
-    p = oracle_params_like(orc, vhlib.ScanParams(eta_bias=wl.eta_bias, alpha_init=wl.alpha_init),
-                           lam)
+    p = oracle_params_like(orc, vhlib.ScanParams(eta_bias=wl.eta_bias, alpha_init=wl.alpha_init,
+                                                 control_flags=flags), lam)
     p.w_query = None if wq is None else wq.astype(np.float64)
     p.skip = None if skip is None else skip.astype(np.float64)
     return orc.forward(inp.x64, inp.mem0, wl.H, wl.W, wl.nh, wl.d, dirs=dirs, params=p,
@@ -70,6 +72,18 @@ def test_exact_small(orc, vhlib, impl, name, wl):
     e_out, e_mem = parity_err(g, o), parity_err(gm, om)
     assert e_out < TOL and e_mem < TOL, (e_out, e_mem)
     assert st[0] == inp.x64.shape[0] * 4 * wl.nh * wl.H * wl.W
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+@pytest.mark.parametrize("name,wl", CASES[:3], ids=[c[0] for c in CASES[:3]])
+def test_exact_intra_read(orc, vhlib, impl, name, wl):
+    """The outer query read out from the working state M^m_b G_{t-1} (intra-chunk switch)."""
+    inp = synth.make_inputs(wl)
+    wq, skip, lam = _extras(wl.Cc, wl.seed)
+    g, gm, _ = _run(vhlib, inp, wq, skip, lam, impl, flags=vhlib.CTRL_INTRA_READ)
+    o, om = _oracle(orc, vhlib, inp, wq, skip, lam, flags=vhlib.CTRL_INTRA_READ)
+    e_out, e_mem = parity_err(g, o), parity_err(gm, om)
+    assert e_out < TOL and e_mem < TOL, (e_out, e_mem)
 
 
 @pytest.mark.parametrize("impl", IMPLS)

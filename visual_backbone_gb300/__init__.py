@@ -25,7 +25,8 @@ HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "vh.h")
 DIR_RIGHT, DIR_LEFT, DIR_DOWN, DIR_UP, DIR_ALL = 1, 2, 4, 8, 15
 DTYPE_F32, DTYPE_BF16 = 0, 1
 GATE_GENERATED, GATE_FORCED_RAW, GATE_FORCED_EXEC = 0, 1, 2
-CTRL_NO_INJ_CAP, CTRL_NO_SPEC_CLAMP = 1, 2
+CTRL_NO_INJ_CAP, CTRL_NO_SPEC_CLAMP, CTRL_HARD_INJ, CTRL_SOFT_SPEC = 1, 2, 4, 8
+CTRL_NO_DGD, CTRL_FREEZE_KV, CTRL_FREEZE_DYN, CTRL_INTRA_READ = 16, 32, 64, 128
 IMPL = {"auto": 0, "simt": 1, "tc": 2}
 STAT_TOKENS, STAT_SPEC_ACTIVE, STAT_INJ_RATIO_GT1, STAT_NONFINITE, STAT_COUNT = 0, 1, 2, 3, 8
 

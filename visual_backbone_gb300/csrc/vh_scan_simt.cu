@@ -80,6 +80,7 @@ __global__ void __launch_bounds__(256) scan_simt_kernel(const ScanArgs a)
     for (int e = tid; e < C::R * D; e += C::NT) S[(e / D) * C::SS + (e % D)] = m0[e];
 
     const float dgd = (a.control_flags & VH_CTRL_NO_DGD) ? 0.0f : 1.0f;
+    const bool intra = (a.control_flags & VH_CTRL_INTRA_READ) != 0;
     const int grow = tid / C::TPR;
     const int gc0 = (tid % C::TPR) * C::CPT;
     float G[C::CPT];
@@ -202,8 +203,10 @@ __global__ void __launch_bounds__(256) scan_simt_kernel(const ScanArgs a)
             }
             __syncthreads();
 
-            // 4. readout y_j = M^m_b q_j and the fused restore/sum of Eq. (26)
-            {
+            // 4. readout y_j = M^m_b q_j and the fused restore/sum of Eq. (26); with the
+            // intra-chunk readout (ablation) the query is replaced by u_j = G_{j-1} q_j,
+            // formed in the gain loop, and the readout follows it
+            auto readout = [&](const float *Qv) {
                 const int nJB = (Lt + C::JB - 1) / C::JB;
                 for (int jb = warp; jb < nJB; jb += C::NW) {
                     const int j0 = jb * C::JB;
@@ -220,7 +223,7 @@ __global__ void __launch_bounds__(256) scan_simt_kernel(const ScanArgs a)
                                 const float mv = mrow[l];
 #pragma unroll
                                 for (int jj = 0; jj < C::JB; ++jj)
-                                    acc[jj] = fmaf(mv, Q[(j0 + jj) * D + l], acc[jj]);
+                                    acc[jj] = fmaf(mv, Qv[(j0 + jj) * D + l], acc[jj]);
                             }
                             const float lm = lam ? lam[i] : 1.0f;
 #pragma unroll
@@ -233,10 +236,13 @@ __global__ void __launch_bounds__(256) scan_simt_kernel(const ScanArgs a)
                         }
                     }
                 }
-            }
+            };
+            if (!intra) readout(Q);
 
             // 5. shared gain over the tile's tokens (rows are independent); without the
-            // DGD correction (ablation) the G k term drops: G <- alpha G - eta delta k^T
+            // DGD correction (ablation) the G k term drops: G <- alpha G - eta delta k^T.
+            // The intra-chunk readout's u_j = G_{j-1} q_j goes to P (free after step 3).
+            float *U = P;
             for (int j = 0; j < Lt; ++j) {
                 const float *kj = K + j * D;
                 float part = 0.0f;
@@ -244,10 +250,24 @@ __global__ void __launch_bounds__(256) scan_simt_kernel(const ScanArgs a)
                 for (int c = 0; c < C::CPT; ++c) part = fmaf(G[c], kj[gc0 + c], part);
 #pragma unroll
                 for (int o = C::TPR / 2; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+                if (intra) {
+                    const float *qj = Q + j * D;
+                    float u = 0.0f;
+#pragma unroll
+                    for (int c = 0; c < C::CPT; ++c) u = fmaf(G[c], qj[gc0 + c], u);
+#pragma unroll
+                    for (int o = C::TPR / 2; o > 0; o >>= 1) u += __shfl_xor_sync(0xffffffffu, u, o);
+                    if (gc0 == 0) U[j * D + grow] = u;
+                }
                 const float s = SC[2 * j + 1] * (part * dgd + DL[j * D + grow]);
                 const float al = SC[2 * j];
 #pragma unroll
                 for (int c = 0; c < C::CPT; ++c) G[c] = fmaf(-s, kj[gc0 + c], al * G[c]);
+            }
+            if (intra) {
+                __syncthreads();  // U complete
+                readout(U);
+                __syncthreads();  // U read before P is reused
             }
         }
 

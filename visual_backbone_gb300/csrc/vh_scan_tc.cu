@@ -85,6 +85,12 @@ constexpr int OFF_GT = OFF_SC + TT * 16;          // per block: k_a . k_b, a < b
 constexpr int OFF_BAR = OFF_GT + TT / NB * 8 * 4; // mbarriers, TMEM base, flags
 constexpr int SMEM_BYTES = OFF_BAR + 128;
 static_assert(SMEM_BYTES <= 75 * 1024, "three CTAs per SM");
+// Intra-chunk readout (ablation), past the default layout: fp32 normalised queries in
+// route order, and per block of NB tokens the cross entries k_a . q_b, a < b (6 of 8).
+// Launched with this larger size, the kernel runs two CTAs per SM.
+constexpr int OFF_QF = (SMEM_BYTES + 15) / 16 * 16;
+constexpr int OFF_CQ = OFF_QF + TT * KS * 4;
+constexpr int SMEM_INTRA = OFF_CQ + TT / NB * 8 * 4;
 constexpr uint32_t TMEM_COLS = 128;
 // TMEM columns (all M = 128): the generation [s_eta s_alpha 0.. | k_raw | v | q_raw] at
 // 0..111 (COL_K, COL_V, COL_QR relative), then the readout over the consumed gate and
@@ -201,6 +207,12 @@ __global__ void __launch_bounds__(NT, 3)
     float *Sea = reinterpret_cast<float *>(sm + OFF_SEA);
     float4 *SC = reinterpret_cast<float4 *>(sm + OFF_SC);
     float *GT = reinterpret_cast<float *>(sm + OFF_GT);
+    // intra-chunk readout (ablation): y_t = M^m_b u_t with u_t = G_{t-1} q_t, the gain before
+    // the token's own update.  The gain pair forms u_t and leaves it in the token's row of
+    // the delta tile; the token pair then reads it out instead of q_t.
+    const bool intra = kAbl && (a.control_flags & VH_CTRL_INTRA_READ) != 0;
+    float *Qf = reinterpret_cast<float *>(sm + OFF_QF);
+    float *CQ = reinterpret_cast<float *>(sm + OFF_CQ);
 
     // ---- set-up: barriers, TMEM, roles, first TMA, initial state
     if (tid == 0) {
@@ -312,6 +324,7 @@ __global__ void __launch_bounds__(NT, 3)
             const bool last = s == nsub - 1;
             const int p = box_start(s) + jq;   // position along the line (token pair)
             const bool valid = !gainw && p >= 0 && p < Lline;
+            const int jr = (rev ? Lline - 1 - p : p) - t0;  // route-ordered index in the sub-tile
             // ---- MMA 1: generation from the boundary state, Eq. (15):
             //   [s_eta s_alpha 0.. | k_raw | v | q_raw] = x (s1 + s2 + s3)^T
             // one M = 128, N = 112 MMA per piece and K step (x is exact in bf16).  The x
@@ -347,8 +360,6 @@ __global__ void __launch_bounds__(NT, 3)
             // token's scalars; then the gain pair (lane = route-ordered token) evaluates the
             // gates and the step control while the token pair forms the Gram entries.
             if (!gainw) {
-                const int tr = rev ? Lline - 1 - p : p;  // token index inside the chunk
-                const int jr = tr - t0;                  // route-ordered index inside the sub-tile
                 float kr[32], vv[32];
                 float se, sa;
                 tmem_ld_kvs(tbase + lrow + COL_GEN, kr, vv, se, sa);
@@ -368,6 +379,38 @@ __global__ void __launch_bounds__(NT, 3)
                         dd4[e] = make_float4(vv[4 * e], vv[4 * e + 1], vv[4 * e + 2], vv[4 * e + 3]);
                     }
                     SC[jr] = make_float4(se, sa, kn2, dd2);
+                }
+                if (intra) {
+                    // the normalised query for the gain pair, route order (fp32)
+                    float qv[32];
+                    if (!exact) {
+                        tmem_ld32(tbase + lrow + COL_GEN + COL_QR, qv);
+                        const float rq = __frsqrt_rn(sumsq32(qv) + a.knorm_eps);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) qv[e] *= rq;
+                    } else {
+                        // the outer query's three pieces from its TMA tile
+                        wt.wait(mb_q, ph_q);
+#pragma unroll
+                        for (int g = 0; g < 4; ++g) {
+                            const unsigned char *src = sQ + g * QX_LBO + jq * 16;
+                            const uint4 u1 = *reinterpret_cast<const uint4 *>(src);
+                            const uint4 u2 = *reinterpret_cast<const uint4 *>(src + QX_PIECE);
+                            const uint4 u3 = *reinterpret_cast<const uint4 *>(src + 2 * QX_PIECE);
+                            const uint32_t *w1 = &u1.x, *w2 = &u2.x, *w3 = &u3.x;
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                qv[8 * g + 2 * i] = bf16_lo(w1[i]) + (bf16_lo(w2[i]) + bf16_lo(w3[i]));
+                                qv[8 * g + 2 * i + 1] = bf16_hi(w1[i]) + (bf16_hi(w2[i]) + bf16_hi(w3[i]));
+                            }
+                        }
+                    }
+                    if (valid) {
+                        float4 *qd = reinterpret_cast<float4 *>(Qf + jr * KS);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            qd[e] = make_float4(qv[4 * e], qv[4 * e + 1], qv[4 * e + 2], qv[4 * e + 3]);
+                    }
                 }
             }
             __syncthreads();
@@ -421,6 +464,20 @@ __global__ void __launch_bounds__(NT, 3)
                         g4[3] = fmaf(fa.w, fb.w, g4[3]);
                     }
                     GT[(R0 / NB + q) * 8 + pi] = (g4[0] + g4[1]) + (g4[2] + g4[3]);
+                    if (intra) {  // and k_a . q_b for the intra-chunk readout
+                        const float4 *qb = reinterpret_cast<const float4 *>(Qf + (R0 + NB * q + ib) * KS);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) g4[e] = 0.0f;
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const float4 fa = ka[e], fb = qb[e];
+                            g4[0] = fmaf(fa.x, fb.x, g4[0]);
+                            g4[1] = fmaf(fa.y, fb.y, g4[1]);
+                            g4[2] = fmaf(fa.z, fb.z, g4[2]);
+                            g4[3] = fmaf(fa.w, fb.w, g4[3]);
+                        }
+                        CQ[(R0 / NB + q) * 8 + pi] = (g4[0] + g4[1]) + (g4[2] + g4[3]);
+                    }
                 }
             }
             tc_before();
@@ -465,7 +522,26 @@ __global__ void __launch_bounds__(NT, 3)
                     gam = 1.0f;
                     inv_gam = 1.0f;
                 };
-                auto apply = [&](const Tok &t, bool chk) {
+                // intra-chunk readout: u_j = gam (ghat . q_j) before token j's update, left
+                // in the token's delta slot (read by this row's two lanes only, both done)
+                auto read_u = [&](int j) {
+                    const float4 *qp = reinterpret_cast<const float4 *>(Qf + j * KS + 16 * gq);
+                    float p0 = 0.0f, p1 = 0.0f;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float4 f = qp[e];
+                        p0 = fmaf(gh[4 * e], f.x, p0);
+                        p1 = fmaf(gh[4 * e + 1], f.y, p1);
+                        p0 = fmaf(gh[4 * e + 2], f.z, p0);
+                        p1 = fmaf(gh[4 * e + 3], f.w, p1);
+                    }
+                    float u = p0 + p1;
+                    u += __shfl_xor_sync(0xffffffffu, u, 1);
+                    __syncwarp();
+                    if (gq == 0) DLf[j * KS + grow] = gam * u;
+                };
+                auto apply = [&](const Tok &t, bool chk, int j) {
+                    if (intra) read_u(j);
                     float p4[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) p4[e] = gh[e] * t.k[e];
@@ -497,10 +573,10 @@ __global__ void __launch_bounds__(NT, 3)
                     load(0, ta);
                     for (int j = 0; j < Lt; j += 2) {
                         load(min(j + 1, TT - 1), tb);
-                        apply(ta, true);
+                        apply(ta, true, j);
                         if (j + 1 >= Lt) break;
                         load(min(j + 2, TT - 1), ta);
-                        apply(tb, true);
+                        apply(tb, true, j + 1);
                     }
                 } else {
                     // blocks of NB tokens: with a = ghat_0 . k_j for the block's starting ghat,
@@ -538,6 +614,26 @@ __global__ void __launch_bounds__(NT, 3)
                         }
 #pragma unroll
                         for (int t = 0; t < NB; ++t) av[t] += __shfl_xor_sync(0xffffffffu, av[t], 1);
+                        // intra-chunk readout: ghat_0 . q_t for the block's tokens
+                        float aq[NB];
+                        if (intra) {
+#pragma unroll
+                            for (int t = 0; t < NB; ++t) {
+                                const float4 *qp = reinterpret_cast<const float4 *>(Qf + (j + t) * KS + 16 * gq);
+                                float p0 = 0.0f, p1 = 0.0f;
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    const float4 f = qp[e];
+                                    p0 = fmaf(gh[4 * e], f.x, p0);
+                                    p1 = fmaf(gh[4 * e + 1], f.y, p1);
+                                    p0 = fmaf(gh[4 * e + 2], f.z, p0);
+                                    p1 = fmaf(gh[4 * e + 3], f.w, p1);
+                                }
+                                aq[t] = p0 + p1;
+                            }
+#pragma unroll
+                            for (int t = 0; t < NB; ++t) aq[t] += __shfl_xor_sync(0xffffffffu, aq[t], 1);
+                        }
                         if (no_dgd) {
 #pragma unroll
                             for (int t = 0; t < NB; ++t) av[t] = 0.0f;
@@ -555,6 +651,27 @@ __global__ void __launch_bounds__(NT, 3)
                             -cb[3].y * (fmaf(db[3], iv, av[3]) + fmaf(s2, g1.y, fmaf(s1, g1.x, s0 * g0.z)));
                         iv *= cb[3].z;
                         inv_gam = iv;
+                        if (intra) {
+                            // ghat_{t-1} . q_t = ghat_0 . q_t + sum_{i<t} s_i (k_i . q_t), and
+                            // gam_{t-1} = gam_0 alpha_0 .. alpha_{t-1}
+                            const float4 c0 = *reinterpret_cast<const float4 *>(CQ + (j / NB) * 8);
+                            const float2 c1 = *reinterpret_cast<const float2 *>(CQ + (j / NB) * 8 + 4);
+                            float g = gam;
+                            const float u0 = g * aq[0];
+                            g *= cb[0].x;
+                            const float u1 = g * fmaf(s0, c0.x, aq[1]);
+                            g *= cb[1].x;
+                            const float u2 = g * fmaf(s1, c0.w, fmaf(s0, c0.y, aq[2]));
+                            g *= cb[2].x;
+                            const float u3 = g * fmaf(s2, c1.y, fmaf(s1, c1.x, fmaf(s0, c0.z, aq[3])));
+                            __syncwarp();
+                            if (gq == 0) {
+                                DLf[j * KS + grow] = u0;
+                                DLf[(j + 1) * KS + grow] = u1;
+                                DLf[(j + 2) * KS + grow] = u2;
+                                DLf[(j + 3) * KS + grow] = u3;
+                            }
+                        }
                         gam *= (cb[0].x * cb[1].x) * (cb[2].x * cb[3].x);
 #pragma unroll
                         for (int e = 0; e < 16; ++e)
@@ -565,9 +682,13 @@ __global__ void __launch_bounds__(NT, 3)
                     for (; j < Lt; ++j) {
                         Tok t;
                         load(j, t);
-                        apply(t, false);
+                        apply(t, false, j);
                     }
                     if (gam < 1e-20f) fold();
+                }
+                if (intra) {
+                    __threadfence_block();
+                    named_arrive(2, NT);  // u of every token of the sub-tile written
                 }
                 if (last) {
                     // G = gam * ghat: fp32 rows for the eta / alpha rows, and the update's B
@@ -602,8 +723,20 @@ __global__ void __launch_bounds__(NT, 3)
                 }
             } else {
                 // ---- the token pair, while the gain runs: queries and the readout of this
-                // sub-tile
-                if (!exact) {
+                // sub-tile.  For the intra-chunk readout it waits for the gain pair's u_t
+                // and reads those out instead.
+                if (intra) {
+                    named_sync(2, NT);
+                    float uv[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) uv[e] = valid ? DLf[jr * KS + e] : 0.0f;
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) store_split8(sQ + op_off(jq, g), Q_PIECE, uv + 8 * g);
+                    fence_async_smem();
+                    tc_before();
+                    named_sync(1, 64);
+                    tc_after();
+                } else if (!exact) {
                     float qr[32];
                     tmem_ld32(tbase + lrow + COL_GEN + COL_QR, qr);
                     const float rq = __frsqrt_rn(sumsq32(qr) + a.knorm_eps);
@@ -621,7 +754,7 @@ __global__ void __launch_bounds__(NT, 3)
                 // next to each piece).  The outer queries of the VisionHOPE-exact readout
                 // arrive by TMA in their own layout.
                 if (issuer) {
-                    if (!exact) {
+                    if (!exact || intra) {
                         if (!*abort_flag) {
                             mma_split6<Q_PIECE, S_PIECE>(
                                 tbase + COL_RO, smem_u32(sQ) - (rw >> 1) * 8 * SBO_K32,
@@ -890,15 +1023,17 @@ cudaError_t launch_scan_tc(const ScanArgs &a, int d, bool bf16, cudaStream_t st,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, tc::SMEM_BYTES);
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(tc::scan_tc_kernel<true>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, tc::SMEM_BYTES);
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, tc::SMEM_INTRA);
         if (e != cudaSuccess) return e;
         attr_set[dev] = 1;
     }
     const unsigned grid = (unsigned)(a.B * a.ndirs * a.nh);
-    if (a.control_flags)
-        tc::scan_tc_kernel<true><<<grid, tc::NT, tc::SMEM_BYTES, st>>>(a, mr, mc, qr, qc);
-    else
+    if (a.control_flags) {
+        const int smem = (a.control_flags & VH_CTRL_INTRA_READ) ? tc::SMEM_INTRA : tc::SMEM_BYTES;
+        tc::scan_tc_kernel<true><<<grid, tc::NT, smem, st>>>(a, mr, mc, qr, qc);
+    } else {
         tc::scan_tc_kernel<false><<<grid, tc::NT, tc::SMEM_BYTES, st>>>(a, mr, mc, qr, qc);
+    }
     *handled = true;
     return cudaGetLastError();
 }

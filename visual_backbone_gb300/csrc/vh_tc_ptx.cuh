@@ -232,6 +232,12 @@ __device__ __forceinline__ void named_sync(int id, int n)
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
+// Producer side of a named barrier whose consumers wait with named_sync.
+__device__ __forceinline__ void named_arrive(int id, int n)
+{
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
 __device__ __forceinline__ void red_add_v4(float *addr, float4 v)
 {
     asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr),
