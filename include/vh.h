@@ -208,6 +208,37 @@ vh_status vh_check(const unsigned long long *stats, void *stream);
  * pieces) when p->w_query is set.  NULL p gives 0. */
 size_t vh_workspace_size(const vh_params *p, int H, int W, unsigned dirs, int chunk);
 
+/*
+ * vh_scan_backward -- outer gradients of vh_scan_forward ("VisionHOPE" Sec. 2.1.2: the
+ * recurrence is explicit and differentiable, so gradients pass through the memory
+ * trajectory; Sec. 3.4 Eq. (60) for the activation storage of training).  With
+ * L = <dout, out> + <dmem_final, memories_out> for the forward call with the same x,
+ * memories0, p, H, W, dirs and chunk, it writes
+ *   dx     device fp32 [B][H][W][Cc], 16-byte aligned: dL/dx (overwritten);
+ *   dmem0  device fp32 [4][n_heads][4d^2+2d]: dL/dmemories0 summed over the batch
+ *          (overwritten; the blocks of disabled routes are zero).
+ * dout is device fp32 [B][H][W][Cc]; dmem_final is device fp32 [B][4][n_heads][4d^2+2d]
+ * or NULL (no loss on the final memories).  None of the outputs may alias an input.
+ *
+ * The call recomputes the forward: it keeps every chunk's boundary state and, per scan,
+ * the current chunk's gain slices and token records in p->workspace, which must hold
+ * vh_backward_workspace_size() bytes, 16-byte aligned.  One CUDA-core kernel, fp32;
+ * gradients are summed over routes and images with device atomics (their rounding order
+ * is not fixed).  The branch of the step control follows the forward's choice.
+ *
+ * Errors: as vh_scan_forward; VH_ERR_UNSUPPORTED for control_flags != 0, w_query or
+ * skip (the ablation switches and the VisionHOPE-exact readout have no backward);
+ * VH_ERR_WORKSPACE for a missing, small or misaligned workspace.
+ */
+vh_status vh_scan_backward(const void *x, const float *memories0, const vh_params *p, int H,
+                           int W, unsigned dirs, int chunk, const float *dout,
+                           const float *dmem_final, float *dx, float *dmem0);
+
+/* Bytes of device workspace vh_scan_backward needs for these parameters: per scan
+ * (image, enabled route, head) the boundary states of its chunks and, for its longest
+ * chunk, d^2 + 5d + 16 floats per token.  0 for invalid arguments. */
+size_t vh_backward_workspace_size(const vh_params *p, int H, int W, unsigned dirs, int chunk);
+
 /* Static string for a status code. */
 const char *vh_status_string(vh_status s);
 

@@ -94,3 +94,52 @@ def test_binding_refuses_cpu_tensors(vhlib):
         vhlib.scan_forward(x, m, 16)
     with pytest.raises(ValueError, match="CUDA"):
         vhlib.check(torch.zeros(8, dtype=torch.int64))
+
+
+def _bwd_call(vhlib, B=1, Cc=32, d=32, H=4, W=4, dirs=15, chunk=0, ws=0, ws_bytes=0, **kw):
+    p = vhlib.make_cparams(B, Cc, d, True, workspace_ptr=ws, workspace_bytes=ws_bytes)
+    for k, v in kw.items():
+        setattr(p, k, v)
+    base = 1 << 36  # far-apart, 16-byte aligned fake device addresses, never dereferenced
+    return vhlib.lib().vh_scan_backward(base, base + (1 << 30), ctypes.byref(p), H, W, dirs,
+                                        chunk, base + (2 << 30), None, base + (3 << 30),
+                                        base + (4 << 30))
+
+
+def test_backward_workspace_size(vhlib):
+    """Per scan: the boundary states of its chunks (4d^2 + 2d floats each) plus, for the
+    longest chunk, d^2 + 5d + 16 floats per token."""
+    L = vhlib.lib()
+    p = vhlib.make_cparams(2, 64, 32, True)
+    # 3 x 5 map, all routes, aligned chunks: rows of 5 (3 chunks), columns of 3 (5 chunks)
+    per_scan = 5 * (4 * 32 * 32 + 64) + 5 * (32 * 32 + 5 * 32 + 16)
+    assert L.vh_backward_workspace_size(ctypes.byref(p), 3, 5, 15, 0) == 2 * 4 * 2 * per_scan * 4
+    # rows only: 3 chunks of 5
+    per_scan = 3 * (4 * 32 * 32 + 64) + 5 * (32 * 32 + 5 * 32 + 16)
+    assert L.vh_backward_workspace_size(ctypes.byref(p), 3, 5, 3, 0) == 2 * 2 * 2 * per_scan * 4
+    # fixed chunk 4 over 15 tokens: 4 chunks, the longest 4 tokens
+    per_scan = 4 * (4 * 32 * 32 + 64) + 4 * (32 * 32 + 5 * 32 + 16)
+    assert L.vh_backward_workspace_size(ctypes.byref(p), 3, 5, 1, 4) == 2 * 1 * 2 * per_scan * 4
+    assert L.vh_backward_workspace_size(None, 3, 5, 15, 0) == 0
+    assert L.vh_backward_workspace_size(ctypes.byref(p), 3, 5, 0, 0) == 0
+
+
+def test_backward_rejects_on_the_host(vhlib):
+    big = 1 << 40
+    assert _bwd_call(vhlib, control_flags=vhlib.CTRL_NO_DGD) == -2      # unsupported
+    assert _bwd_call(vhlib, w_query=1 << 20) == -2
+    assert _bwd_call(vhlib) == -4                                       # no workspace
+    assert _bwd_call(vhlib, ws=big + 8, ws_bytes=1 << 30) == -4         # misaligned
+    assert _bwd_call(vhlib, ws=big, ws_bytes=16) == -4                  # too small
+    assert _bwd_call(vhlib, dirs=0, ws=big, ws_bytes=1 << 30) == -1
+    assert _bwd_call(vhlib, d=24, Cc=48, ws=big, ws_bytes=1 << 30) == -2
+    # workspace overlapping dx
+    assert _bwd_call(vhlib, ws=(1 << 36) + (3 << 30), ws_bytes=1 << 30) == -1
+    assert b"overlap" in vhlib.lib().vh_last_error()
+    # dx overlapping dout
+    p = vhlib.make_cparams(1, 32, 32, True, workspace_ptr=1 << 40, workspace_bytes=1 << 30)
+    base = 1 << 36
+    assert vhlib.lib().vh_scan_backward(base, base + (1 << 30), ctypes.byref(p), 4, 4, 15, 0,
+                                        base + (2 << 30), None, base + (2 << 30),
+                                        base + (4 << 30)) == -1
+    assert b"alias" in vhlib.lib().vh_last_error()

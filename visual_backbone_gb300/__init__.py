@@ -89,6 +89,11 @@ def lib() -> ctypes.CDLL:
         L.vh_debug_permute.argtypes = [vp, ctypes.POINTER(CParams), ci, ci, ci, vp]
         L.vh_workspace_size.restype = ctypes.c_size_t
         L.vh_workspace_size.argtypes = [ctypes.POINTER(CParams), ci, ci, cu, ci]
+        L.vh_scan_backward.restype = ci
+        L.vh_scan_backward.argtypes = [vp, vp, ctypes.POINTER(CParams), ci, ci, cu, ci, vp, vp,
+                                       vp, vp]
+        L.vh_backward_workspace_size.restype = ctypes.c_size_t
+        L.vh_backward_workspace_size.argtypes = [ctypes.POINTER(CParams), ci, ci, cu, ci]
         L.vh_status_string.restype = ctypes.c_char_p
         L.vh_status_string.argtypes = [ci]
         L.vh_last_error.restype = ctypes.c_char_p
@@ -202,6 +207,58 @@ def scan_forward(x, memories0, head_dim: int, dirs: int = DIR_ALL, chunk: int = 
     _check(lib().vh_scan_forward(x.data_ptr(), memories0.data_ptr(), ctypes.byref(cp), H, W,
                                  dirs, chunk, out.data_ptr()))
     return out
+
+
+def backward_workspace_size(x, head_dim: int, dirs: int = DIR_ALL, chunk: int = 0) -> int:
+    """Bytes of workspace scan_backward needs for x's shape."""
+    import torch
+    B, H, W, Cc = x.shape
+    cp = make_cparams(B, Cc, head_dim, x.dtype == torch.bfloat16, None)
+    return int(lib().vh_backward_workspace_size(ctypes.byref(cp), H, W, dirs, chunk))
+
+
+def scan_backward(x, memories0, head_dim: int, dout, dirs: int = DIR_ALL, chunk: int = 0,
+                  params: Optional[ScanParams] = None, dir_scale=None, dmem_final=None,
+                  dx=None, dmem0=None, workspace=None, stream=None):
+    """Outer gradients of scan_forward: (dx fp32 [B][H][W][Cc], dmem0 fp32 [4][nh][4d^2+2d])
+    of <dout, out> + <dmem_final, memories_out> for the same x, memories0, params, dirs,
+    chunk and dir_scale.  dmem_final (fp32 [B][4][nh][4d^2+2d]) may be None.  The
+    workspace (uint8, at least backward_workspace_size bytes) is allocated here when not
+    given.  Runs on ``stream`` asynchronously."""
+    import torch
+    _require_cuda("x", x, (torch.bfloat16, torch.float32))
+    _require_cuda("memories0", memories0, (torch.float32,))
+    _require_cuda("dout", dout, (torch.float32,))
+    B, H, W, Cc = x.shape
+    nh = Cc // head_dim
+    if memories0.numel() != 4 * nh * (4 * head_dim * head_dim + 2 * head_dim):
+        raise ValueError("memories0 must hold [4][nh][4d^2+2d] floats")
+    if tuple(dout.shape) != (B, H, W, Cc):
+        raise ValueError("dout must have x's shape")
+    if dmem_final is not None:
+        _require_cuda("dmem_final", dmem_final, (torch.float32,))
+    if dir_scale is not None:
+        _require_cuda("dir_scale", dir_scale, (torch.float32,))
+    if dx is None:
+        dx = torch.empty((B, H, W, Cc), dtype=torch.float32, device=x.device)
+    if dmem0 is None:
+        dmem0 = torch.empty_like(memories0)
+    _require_cuda("dx", dx, (torch.float32,))
+    _require_cuda("dmem0", dmem0, (torch.float32,))
+    cp = make_cparams(B, Cc, head_dim, x.dtype == torch.bfloat16, params,
+                      dir_scale_ptr=dir_scale.data_ptr() if dir_scale is not None else 0,
+                      stream_ptr=_stream_ptr(stream))
+    need = lib().vh_backward_workspace_size(ctypes.byref(cp), H, W, dirs, chunk)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
+    _require_cuda("workspace", workspace, (torch.uint8,))
+    cp.workspace = workspace.data_ptr()
+    cp.workspace_bytes = workspace.numel()
+    _check(lib().vh_scan_backward(x.data_ptr(), memories0.data_ptr(), ctypes.byref(cp), H, W,
+                                  dirs, chunk, dout.data_ptr(),
+                                  dmem_final.data_ptr() if dmem_final is not None else None,
+                                  dx.data_ptr(), dmem0.data_ptr()))
+    return dx, dmem0
 
 
 def check(stats, stream=None):

@@ -13,6 +13,8 @@ cudaError_t launch_scan_tc(const ScanArgs &a, int d, bool bf16, cudaStream_t st,
 cudaError_t launch_qproj(const void *x, bool bf16, int d, const float *wq, const float *skip,
                          const float *dir_scale, unsigned dirs, __nv_bfloat16 *qhat, float *out,
                          int accumulate, long npix, int Cc, float knorm_eps, cudaStream_t st);
+cudaError_t launch_scan_bwd(const BwdArgs &ba, int d, bool bf16, cudaStream_t st);
+size_t bwd_floats_per_scan(int d, int nck, int lmax);
 }  // namespace vh
 
 namespace {
@@ -52,6 +54,74 @@ vh_status check_common(const vh_params *p, int H, int W)
     if (n * (double)p->channels >= 2147483647.0)
         return fail(VH_ERR_INVALID_ARG, "H*W*channels %.0f exceeds 2^31-1 per image", n * p->channels);
     return VH_OK;
+}
+
+vh_status check_scan(const vh_params *p, unsigned dirs, int chunk)
+{
+    if (dirs == 0 || (dirs & ~15u)) return fail(VH_ERR_INVALID_ARG, "dirs mask 0x%x invalid", dirs);
+    if (chunk < 0) return fail(VH_ERR_INVALID_ARG, "chunk %d < 0", chunk);
+    if (p->gate_mode < 0 || p->gate_mode > 2) return fail(VH_ERR_INVALID_ARG, "gate_mode %d", p->gate_mode);
+    if (!(p->alpha_init > 0.0f && p->alpha_init < 1.0f))
+        return fail(VH_ERR_INVALID_ARG, "alpha_init %g must lie in (0,1)", (double)p->alpha_init);
+    if (p->impl < VH_IMPL_AUTO || p->impl > VH_IMPL_TC) return fail(VH_ERR_INVALID_ARG, "impl %d", p->impl);
+    if (p->control_flags & ~(unsigned)VH_CTRL_ALL)
+        return fail(VH_ERR_INVALID_ARG, "control_flags 0x%x has unknown bits", p->control_flags);
+    return VH_OK;
+}
+
+bool overlaps(const void *a, size_t na, const void *b, size_t nb)
+{
+    const char *x = static_cast<const char *>(a), *y = static_cast<const char *>(b);
+    return a && b && x < y + nb && y < x + na;
+}
+
+vh::ScanArgs make_args(const void *x, const float *memories0, const vh_params *p, int H, int W,
+                       unsigned dirs, int chunk, float *out)
+{
+    vh::ScanArgs a{};
+    const int nh = p->channels / p->head_dim;
+    a.x = x;
+    a.mem0 = memories0;
+    a.out = out;
+    a.mem_out = p->memories_out;
+    a.dir_scale = p->dir_scale;
+    a.stats = p->stats;
+    a.B = p->batch; a.H = H; a.W = W; a.nh = nh; a.Cc = p->channels;
+    a.ndirs = 0;
+    for (int r = 0; r < 4; ++r)
+        if (dirs & (1u << r)) a.dir_list[a.ndirs++] = r;
+    a.chunk = chunk;
+    a.gamma_eta = p->gamma_eta;
+    a.alpha_logit = (float)std::log((double)p->alpha_init / (1.0 - (double)p->alpha_init));
+    a.eta_bias = p->eta_bias;
+    a.eps = p->eps;
+    a.knorm_eps = p->knorm_eps;
+    a.inj_factor = 1.0f - p->inj_inward;
+    a.spec_factor = 1.0f - p->spec_inward;
+    a.kk_floor = p->kk_floor;
+    a.gate_mode = p->gate_mode;
+    a.forced_eta = p->forced_eta;
+    a.forced_alpha = p->forced_alpha;
+    a.control_flags = p->control_flags;
+
+    return a;
+}
+
+// Routes enabled in `dirs`: chunks of the longest-chunked route's count and the longest
+// chunk, both as provisioned per scan by the backward workspace.
+void bwd_extent(int H, int W, unsigned dirs, int chunk, int *nck, int *lmax)
+{
+    const int N = H * W;
+    *nck = 0;
+    *lmax = 0;
+    for (int r = 0; r < 4; ++r) {
+        if (!(dirs & (1u << r))) continue;
+        const int Cr = vh::route_chunk(r, chunk, H, W);
+        const int L = Cr < N ? Cr : N;
+        const int n = (N + Cr - 1) / Cr;
+        if (n > *nck) *nck = n;
+        if (L > *lmax) *lmax = L;
+    }
 }
 
 }  // namespace
@@ -128,14 +198,8 @@ vh_status vh_scan_forward(const void *x, const float *memories0, const vh_params
         return fail(VH_ERR_INVALID_ARG, "x and out must be 16-byte aligned");
     if ((reinterpret_cast<uintptr_t>(memories0) & 3u) || (p->memories_out && (reinterpret_cast<uintptr_t>(p->memories_out) & 3u)))
         return fail(VH_ERR_INVALID_ARG, "memories must be 4-byte aligned");
-    if (dirs == 0 || (dirs & ~15u)) return fail(VH_ERR_INVALID_ARG, "dirs mask 0x%x invalid", dirs);
-    if (chunk < 0) return fail(VH_ERR_INVALID_ARG, "chunk %d < 0", chunk);
-    if (p->gate_mode < 0 || p->gate_mode > 2) return fail(VH_ERR_INVALID_ARG, "gate_mode %d", p->gate_mode);
-    if (!(p->alpha_init > 0.0f && p->alpha_init < 1.0f))
-        return fail(VH_ERR_INVALID_ARG, "alpha_init %g must lie in (0,1)", (double)p->alpha_init);
-    if (p->impl < VH_IMPL_AUTO || p->impl > VH_IMPL_TC) return fail(VH_ERR_INVALID_ARG, "impl %d", p->impl);
-    if (p->control_flags & ~(unsigned)VH_CTRL_ALL)
-        return fail(VH_ERR_INVALID_ARG, "control_flags 0x%x has unknown bits", p->control_flags);
+    s = check_scan(p, dirs, chunk);
+    if (s != VH_OK) return s;
 
     const int d = p->head_dim, nh = p->channels / d, B = p->batch;
     const size_t N = (size_t)H * W;
@@ -158,30 +222,7 @@ vh_status vh_scan_forward(const void *x, const float *memories0, const vh_params
     if (p->skip && (reinterpret_cast<uintptr_t>(p->skip) & 3u))
         return fail(VH_ERR_INVALID_ARG, "skip must be 4-byte aligned");
 
-    vh::ScanArgs a{};
-    a.x = x;
-    a.mem0 = memories0;
-    a.out = out;
-    a.mem_out = p->memories_out;
-    a.dir_scale = p->dir_scale;
-    a.stats = p->stats;
-    a.B = B; a.H = H; a.W = W; a.nh = nh; a.Cc = p->channels;
-    a.ndirs = 0;
-    for (int r = 0; r < 4; ++r)
-        if (dirs & (1u << r)) a.dir_list[a.ndirs++] = r;
-    a.chunk = chunk;
-    a.gamma_eta = p->gamma_eta;
-    a.alpha_logit = (float)std::log((double)p->alpha_init / (1.0 - (double)p->alpha_init));
-    a.eta_bias = p->eta_bias;
-    a.eps = p->eps;
-    a.knorm_eps = p->knorm_eps;
-    a.inj_factor = 1.0f - p->inj_inward;
-    a.spec_factor = 1.0f - p->spec_inward;
-    a.kk_floor = p->kk_floor;
-    a.gate_mode = p->gate_mode;
-    a.forced_eta = p->forced_eta;
-    a.forced_alpha = p->forced_alpha;
-    a.control_flags = p->control_flags;
+    vh::ScanArgs a = make_args(x, memories0, p, H, W, dirs, chunk, out);
     a.qhat = exact ? static_cast<const __nv_bfloat16 *>(p->workspace) : nullptr;
 
     cudaStream_t st = static_cast<cudaStream_t>(p->stream);
@@ -209,6 +250,78 @@ vh_status vh_scan_forward(const void *x, const float *memories0, const vh_params
         e = vh::launch_scan_simt(a, d, bf16, st);
         if (e != cudaSuccess) return cuda_fail(e, "scan launch");
     }
+    return VH_OK;
+}
+
+size_t vh_backward_workspace_size(const vh_params *p, int H, int W, unsigned dirs, int chunk)
+{
+    if (!p || p->batch < 1 || H < 1 || W < 1 || p->head_dim < 1 || p->channels < p->head_dim ||
+        dirs == 0 || (dirs & ~15u) || chunk < 0)
+        return 0;
+    int nck, lmax, nd = 0;
+    bwd_extent(H, W, dirs, chunk, &nck, &lmax);
+    for (int r = 0; r < 4; ++r) nd += (dirs >> r) & 1;
+    const size_t scans = (size_t)p->batch * nd * (p->channels / p->head_dim);
+    return scans * vh::bwd_floats_per_scan(p->head_dim, nck, lmax) * sizeof(float);
+}
+
+vh_status vh_scan_backward(const void *x, const float *memories0, const vh_params *p, int H,
+                           int W, unsigned dirs, int chunk, const float *dout,
+                           const float *dmem_final, float *dx, float *dmem0)
+{
+    g_err[0] = '\0';
+    vh_status s = check_common(p, H, W);
+    if (s != VH_OK) return s;
+    s = check_scan(p, dirs, chunk);
+    if (s != VH_OK) return s;
+    if (!x || !memories0 || !dout || !dx || !dmem0)
+        return fail(VH_ERR_INVALID_ARG, "x, memories0, dout, dx and dmem0 must be non-NULL");
+    if (!aligned16(x) || !aligned16(dx))
+        return fail(VH_ERR_INVALID_ARG, "x and dx must be 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(memories0) & 3u) || (reinterpret_cast<uintptr_t>(dout) & 3u) ||
+        (reinterpret_cast<uintptr_t>(dmem0) & 3u) || (reinterpret_cast<uintptr_t>(dmem_final) & 3u))
+        return fail(VH_ERR_INVALID_ARG, "memories0, dout, dmem_final and dmem0 must be 4-byte aligned");
+    if (p->control_flags || p->w_query || p->skip)
+        return fail(VH_ERR_UNSUPPORTED, "the backward covers the method as defined "
+                    "(no control_flags, w_query or skip)");
+    const int d = p->head_dim, nh = p->channels / d, B = p->batch;
+    const size_t N = (size_t)H * W;
+    const size_t xbytes = (size_t)B * N * p->channels * (p->x_dtype == VH_DTYPE_BF16 ? 2 : 4);
+    const size_t gbytes = (size_t)B * N * p->channels * 4;
+    const size_t mbytes = (size_t)4 * nh * (4 * d * d + 2 * d) * 4;
+    const size_t wbytes = vh_backward_workspace_size(p, H, W, dirs, chunk);
+    if (!p->workspace || p->workspace_bytes < wbytes || !aligned16(p->workspace))
+        return fail(VH_ERR_WORKSPACE, "the backward needs a 16-byte aligned workspace of %zu bytes "
+                    "(have %zu)", wbytes, p->workspace ? p->workspace_bytes : (size_t)0);
+    const void *ins[4] = {x, dout, memories0, dmem_final};
+    const size_t insz[4] = {xbytes, gbytes, mbytes, (size_t)B * mbytes};  // dmem_final: B blocks
+    void *outs[3] = {dx, dmem0, p->workspace};
+    const size_t outsz[3] = {gbytes, mbytes, wbytes};
+    for (int i = 0; i < 3; ++i) {
+        for (int j = 0; j < 4; ++j)
+            if (overlaps(outs[i], outsz[i], ins[j], insz[j]))
+                return fail(VH_ERR_INVALID_ARG, "an output or the workspace aliases an input");
+        for (int j = i + 1; j < 3; ++j)
+            if (overlaps(outs[i], outsz[i], outs[j], outsz[j]))
+                return fail(VH_ERR_INVALID_ARG, "outputs / workspace overlap");
+    }
+
+    vh::BwdArgs ba{};
+    ba.s = make_args(x, memories0, p, H, W, dirs, chunk, nullptr);
+    ba.s.mem_out = nullptr;
+    ba.s.stats = nullptr;
+    ba.dout = dout;
+    ba.dmem_final = dmem_final;
+    ba.dx = dx;
+    ba.dmem0 = dmem0;
+    ba.ws = static_cast<float *>(p->workspace);
+    bwd_extent(H, W, dirs, chunk, &ba.nck, &ba.lmax);
+    cudaStream_t st = static_cast<cudaStream_t>(p->stream);
+    cudaError_t e = cudaMemsetAsync(dx, 0, gbytes, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dmem0, 0, mbytes, st);
+    if (e != cudaSuccess) return cuda_fail(e, "zeroing dx / dmem0");
+    e = vh::launch_scan_bwd(ba, d, p->x_dtype == VH_DTYPE_BF16, st);
+    if (e != cudaSuccess) return cuda_fail(e, "backward scan launch");
     return VH_OK;
 }
 

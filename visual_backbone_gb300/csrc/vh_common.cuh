@@ -39,6 +39,17 @@ struct ScanArgs {
     const __nv_bfloat16 *qhat;
 };
 
+// Arguments of the backward scan kernel.
+struct BwdArgs {
+    ScanArgs s;                // forward arguments (out, mem_out, stats, qhat unused)
+    const float *dout;         // [B][H][W][Cc]
+    const float *dmem_final;   // [B][4][nh][4d^2+2d] or nullptr
+    float *dx;                 // [B][H][W][Cc], zeroed before the launch
+    float *dmem0;              // [4][nh][4d^2+2d], zeroed before the launch
+    float *ws;                 // per scan: nck boundary states, lmax gain slices and records
+    int nck, lmax;
+};
+
 // fp32 value of element e of the three-piece query planes (the pieces sum exactly).
 __device__ __forceinline__ float qhat_at(const __nv_bfloat16 *q, size_t plane, size_t e)
 {

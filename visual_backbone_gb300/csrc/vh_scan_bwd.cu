@@ -1,0 +1,616 @@
+// vh_scan_bwd.cu -- outer gradients of the four-direction VisionHOPE memory scan on
+// fp32 CUDA cores: the gradients of <dout, out> + <dmem_final, memories_final> with
+// respect to x and memories0.
+//
+// "VisionHOPE: Visual Backbones as Self-Modifying Learning Systems", Sec. 2.1.2: the
+// recurrence is explicit and differentiable, so outer gradients pass through the memory
+// trajectory without an inner solver.  Sec. 3.4 Eq. (60) budgets the activation storage
+// of training as token quantities plus one d x d gain per chunk, head and route; here
+// each chunk keeps its boundary state (the state is 4d + 2 rows of the gain's width) and
+// the gains are re-formed chunk by chunk in the reverse pass.
+//
+// One CTA owns one scan (image b, route r, head h).
+//  Pass 1 (forward): the state recurrence of the forward kernel without the readout; the
+//    boundary state S_b of every chunk goes to the workspace.
+//  Pass 2 (reverse, from the last chunk), holding dS = dL/dS_end of the chunk (dmem_final,
+//    or zero, for the last one):
+//    a. S_b is reloaded and the chunk's tokens regenerated tile by tile (Eq. (15),
+//       App. C.1 normalisation, Eq. (53) gates, Def. 1 step control); their quantities
+//       are recorded in the workspace and the shared gain (Prop. 2, Eq. (46))
+//       re-advanced, every thread keeping its slice of G_{t-1} for each token;
+//    b. the chunk end S_end = S_b G_L gives the gain adjoint P_L = S_b^T dS, and
+//       dS <- dS G_L^T;
+//    c. with z_t = G_{t-1} k_t + delta_t, G_t = alpha_t G_{t-1} - eta_t z_t k_t^T, so the
+//       adjoint runs backwards as P_{t-1} = alpha_t P_t - eta_t (P_t k_t) k_t^T and gives,
+//       with u_t = P_t k_t,
+//         dalpha_t = <P_t, G_{t-1}>,  deta_t = -z_t . u_t,  ddelta_t = -eta_t u_t,
+//         dk_t = -eta_t (G_{t-1}^T u_t + P_t^T z_t);
+//    d. per token, in parallel: the readout y = M^m_b q (Eq. (16)) with dy = lambda_r dout
+//       at the token's pixel, the executed step, the gates, delta = k - v and the two
+//       normalisations are differentiated; dx_t collects the generation memories'
+//       transposes applied to the generated quantities' adjoints, added at the pixel
+//       over the routes (Eq. (26));
+//    e. the generation and readout adjoints add their outer products with x_t and q_t to
+//       dS, which then holds dL/dS_b: the chunk-end adjoint of the previous chunk.
+//  After chunk 0, dS is the gradient of memories0, summed over the batch.
+// The branch of the step control (soft injection cap or spectral limit) follows the
+// forward's choice; the one-step rounding of the spectral limit passes the gradient of
+// the unrounded value.  The method as defined only: no ablation switch, no outer query.
+#include "vh_common.cuh"
+
+namespace vh {
+
+template <int D>
+struct BwdCfg {
+    static constexpr int NT = 256;
+    static constexpr int NW = NT / 32;
+    static constexpr int R = 4 * D + 2;     // rows of the state
+    static constexpr int SS = D + 1;        // padded row stride
+    static constexpr int T = D == 64 ? 16 : (D == 32 ? 32 : 64);  // token tile
+    static constexpr int TPR = NT / D;      // threads per gain row
+    static constexpr int CPT = D / TPR;     // gain columns per thread
+    static constexpr int RW = 32 / TPR;     // gain rows per warp
+    static constexpr int CPL = (D + 31) / 32;
+    static constexpr int PS = 3 * D + 3;    // generation outputs k_raw v q_raw s_eta s_alpha
+    static constexpr int NSC = 16;          // scalars per token
+    static constexpr int REC = 5 * D + NSC; // record: x k q delta (G_{t-1} k) scalars
+    // scalar slots
+    static constexpr int S_NK = 0, S_NQ = 1, S_SE = 2, S_AL = 4, S_OMA = 5, S_ETA = 6,
+                         S_ET = 7, S_INJ = 8, S_BAR = 9, S_SPEC = 10, S_R = 11, S_BR = 12,
+                         S_KN2 = 13, S_DD = 14, S_PIX = 15;
+    static constexpr int OFF_S = 0;
+    static constexpr int OFF_DS = OFF_S + R * SS;
+    static constexpr int OFF_GT = OFF_DS + R * SS;   // chunk-end gain (pass 1) / its transpose
+    static constexpr int OFF_X = OFF_GT + D * D;
+    static constexpr int OFF_P = OFF_X + T * D;      // generation outputs / their adjoints
+    static constexpr int OFF_K = OFF_P + T * PS;
+    static constexpr int OFF_DL = OFF_K + T * D;
+    static constexpr int OFF_Q = OFF_DL + T * D;
+    static constexpr int OFF_Z = OFF_Q + T * D;      // z = G_{t-1} k + delta
+    static constexpr int OFF_SC = OFF_Z + T * D;
+    static constexpr int OFF_KG = OFF_SC + T * NSC;  // dk from the gain
+    static constexpr int OFF_DG = OFF_KG + T * D;    // ddelta from the gain
+    static constexpr int OFF_Y = OFF_DG + T * D;     // dy
+    static constexpr int OFF_SG = OFF_Y + T * D;     // deta, dalpha from the gain
+    static constexpr int OFF_W = OFF_SG + 2 * T;     // per warp: dy | dk_raw | dv | dq_raw
+    static constexpr int OFF_PIX = OFF_W + NW * 4 * D;
+    static constexpr int FLOATS = OFF_PIX + T;
+    static constexpr size_t BYTES = (size_t)FLOATS * 4;
+    static_assert(TPR * CPT == D && TPR <= 32, "gain thread map");
+    static_assert(BYTES <= 227 * 1024, "shared memory");
+};
+
+// Column sums over the rows held by one warp, added (times `scale`) to dst[0..D): each
+// lane holds v[0..CPT) for columns gc0.. of its row.  Every level halves the value set
+// (a lane keeps one half and receives its partner's copy of it), so a lane ends with the
+// warp's sums of CPT / RW columns; when CPT < RW the last levels add duplicates, and
+// only one lane of each duplicate set writes.
+template <int D>
+__device__ __forceinline__ void col_sums_add(float (&v)[BwdCfg<D>::CPT], int lane, int gc0,
+                                             float *dst, float scale)
+{
+    using C = BwdCfg<D>;
+    int off = 0;
+    unsigned dup = 0;
+#pragma unroll
+    for (int lvl = 0; (C::TPR << lvl) < 32; ++lvl) {
+        const int o = C::TPR << lvl;
+        const int n = C::CPT >> lvl;
+        const bool up = (lane & o) != 0;
+        if (n >= 2) {
+            const int hh = n / 2;
+#pragma unroll
+            for (int i = 0; i < hh; ++i) {
+                const float send = up ? v[i] : v[hh + i];
+                const float keep = up ? v[hh + i] : v[i];
+                v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+            }
+            off += up ? hh : 0;
+        } else {
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
+            dup |= (unsigned)o;
+        }
+    }
+    constexpr int NF = (C::CPT / C::RW) > 0 ? C::CPT / C::RW : 1;
+    if ((lane & dup) == 0) {
+#pragma unroll
+        for (int i = 0; i < NF; ++i) atomicAdd(dst + gc0 + off + i, scale * v[i]);
+    }
+}
+
+template <int D, typename XT>
+__global__ void __launch_bounds__(256, D == 64 ? 1 : 2) scan_bwd_kernel(const BwdArgs ba)
+{
+    using C = BwdCfg<D>;
+    const ScanArgs &a = ba.s;
+    extern __shared__ float4 smem_f4[];
+    float *sm = reinterpret_cast<float *>(smem_f4);
+    float *S = sm + C::OFF_S, *dS = sm + C::OFF_DS, *GT = sm + C::OFF_GT;
+    float *X = sm + C::OFF_X, *P = sm + C::OFF_P, *K = sm + C::OFF_K, *DL = sm + C::OFF_DL;
+    float *Q = sm + C::OFF_Q, *Z = sm + C::OFF_Z, *SC = sm + C::OFF_SC, *KG = sm + C::OFF_KG;
+    float *DG = sm + C::OFF_DG, *Y = sm + C::OFF_Y, *SG = sm + C::OFF_SG, *Wv = sm + C::OFF_W;
+    int *PIX = reinterpret_cast<int *>(sm + C::OFF_PIX);
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    int id = blockIdx.x;
+    const int h = id % a.nh;
+    id /= a.nh;
+    const int r = a.dir_list[id % a.ndirs];
+    const int b = id / a.ndirs;
+    const int H = a.H, W = a.W, N = H * W, Cc = a.Cc;
+    const size_t SZ = (size_t)C::R * D;
+    const int Cr = route_chunk(r, a.chunk, H, W);
+    const int nchunks = (N + Cr - 1) / Cr;
+    float *ckpt = ba.ws + (size_t)blockIdx.x *
+                              ((size_t)ba.nck * SZ + (size_t)ba.lmax * (D * D + C::REC));
+    float *gsc = ckpt + (size_t)ba.nck * SZ;          // [lmax][NT][CPT]: slices of G_{t-1}
+    float *rec = gsc + (size_t)ba.lmax * D * D;       // [lmax][REC]
+    const XT *xb = static_cast<const XT *>(a.x) + (size_t)b * N * Cc + (size_t)h * D;
+    const float *lam = a.dir_scale ? a.dir_scale + (size_t)r * Cc + (size_t)h * D : nullptr;
+    const float *gob = ba.dout + (size_t)b * N * Cc + (size_t)h * D;
+    float *dxb = ba.dx + (size_t)b * N * Cc + (size_t)h * D;
+    const int grow = tid / C::TPR, gc0 = (tid % C::TPR) * C::CPT;
+
+    const float *m0 = a.mem0 + ((size_t)r * a.nh + h) * SZ;
+    for (int e = tid; e < C::R * D; e += C::NT) S[(e / D) * C::SS + (e % D)] = m0[e];
+    float G[C::CPT];
+
+    // ---- one tile of a chunk: gather, generation, per-token step and the gain; with
+    // `record` the token quantities and the gain slices go to the workspace
+    auto tile_forward = [&](int c0, int t0, int Lt, bool record) {
+        __syncthreads();  // earlier users of the tile buffers are done
+        constexpr int EPV = 16 / (int)sizeof(XT);
+        constexpr int VPT = D / EPV;
+        if (tid < Lt) PIX[tid] = route_pixel(r, c0 + t0 + tid, H, W);
+        for (int e = tid; e < Lt * VPT; e += C::NT) {
+            const int j = e / VPT, v = e % VPT;
+            const int pix = route_pixel(r, c0 + t0 + j, H, W);
+            const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(xb + (size_t)pix * Cc + v * EPV));
+            const XT *el = reinterpret_cast<const XT *>(&raw);
+#pragma unroll
+            for (int u = 0; u < EPV; ++u) X[j * D + v * EPV + u] = XElem<XT>::to_f(el[u]);
+        }
+        __syncthreads();
+        // generation from the boundary state, Eq. (15): rows 0..3d-1 (k, v, q), then the
+        // eta and alpha rows (4d, 4d + 1)
+        constexpr int NG = 3 * D + 2;
+        for (int e = tid; e < Lt * NG; e += C::NT) {
+            const int j = e / NG, o = e % NG;
+            const float *srow = S + (o < 3 * D ? o : o + D) * C::SS;
+            const float *xj = X + j * D;
+            float acc = 0.0f;
+#pragma unroll 8
+            for (int i = 0; i < D; ++i) acc = fmaf(srow[i], xj[i], acc);
+            P[j * C::PS + o] = acc;
+        }
+        __syncthreads();
+        // per-token step, one warp per token
+        for (int j = warp; j < Lt; j += C::NW) {
+            const float *pr = P + j * C::PS;
+            float kr[C::CPL], vv[C::CPL], qr[C::CPL];
+            float kk = 0.0f, qq = 0.0f;
+#pragma unroll
+            for (int m = 0; m < C::CPL; ++m) {
+                const int c = lane + 32 * m;
+                const bool ok = c < D;
+                kr[m] = ok ? pr[c] : 0.0f;
+                vv[m] = ok ? pr[D + c] : 0.0f;
+                qr[m] = ok ? pr[2 * D + c] : 0.0f;
+                kk = fmaf(kr[m], kr[m], kk);
+                qq = fmaf(qr[m], qr[m], qq);
+            }
+            kk = warp_sum(kk);
+            qq = warp_sum(qq);
+            const float nk = sqrtf(kk + a.knorm_eps), nq = sqrtf(qq + a.knorm_eps);
+            float kn2 = 0.0f, dd = 0.0f;
+#pragma unroll
+            for (int m = 0; m < C::CPL; ++m) {
+                kr[m] = kr[m] / nk;
+                qr[m] = qr[m] / nq;
+                vv[m] = kr[m] - vv[m];
+                kn2 = fmaf(kr[m], kr[m], kn2);
+                dd = fmaf(vv[m], vv[m], dd);
+            }
+            kn2 = warp_sum(kn2);
+            dd = warp_sum(dd);
+            float eta, alpha, oma;
+            gates(a, pr[3 * D], pr[3 * D + 1], eta, alpha, oma);
+            // the executed step with its intermediates (step_control of the forward kernels)
+            const float rr = sqrtf(dd + a.eps * a.eps) + a.eps;
+            const float einj = __fdividef(a.inj_factor * oma, rr);
+            const float ebar = einj > 0.0f ? einj * (-expm1f(-__fdividef(eta, einj))) : 0.0f;
+            float spec = __fdividef(a.spec_factor * 2.0f * alpha, fmaxf(kn2, a.kk_floor));
+            if (spec > 0.0f) spec = __int_as_float(__float_as_int(spec) - 1);
+            const bool sp = spec < ebar;
+            const bool forced = a.gate_mode == VH_GATE_FORCED_EXEC;
+            const float et = forced ? a.forced_eta : (sp ? spec : ebar);
+#pragma unroll
+            for (int m = 0; m < C::CPL; ++m) {
+                const int c = lane + 32 * m;
+                if (c < D) {
+                    K[j * D + c] = kr[m];
+                    DL[j * D + c] = vv[m];
+                    Q[j * D + c] = qr[m];
+                }
+            }
+            if (lane == 0) {
+                float *sc = SC + j * C::NSC;
+                sc[C::S_NK] = nk;
+                sc[C::S_NQ] = nq;
+                sc[C::S_SE] = pr[3 * D] + a.eta_bias;
+                sc[3] = pr[3 * D + 1];
+                sc[C::S_AL] = alpha;
+                sc[C::S_OMA] = oma;
+                sc[C::S_ETA] = eta;
+                sc[C::S_ET] = et;
+                sc[C::S_INJ] = einj;
+                sc[C::S_BAR] = ebar;
+                sc[C::S_SPEC] = spec;
+                sc[C::S_R] = rr;
+                sc[C::S_BR] = (!forced && sp) ? 1.0f : 0.0f;
+                sc[C::S_KN2] = kn2;
+                sc[C::S_DD] = dd;
+                sc[C::S_PIX] = __int_as_float(PIX[j]);
+            }
+        }
+        __syncthreads();
+        if (record) {
+            for (int e = tid; e < Lt * C::REC; e += C::NT) {
+                const int j = e / C::REC, f = e % C::REC;
+                float v;
+                if (f < D) v = X[j * D + f];
+                else if (f < 2 * D) v = K[j * D + f - D];
+                else if (f < 3 * D) v = Q[j * D + f - 2 * D];
+                else if (f < 4 * D) v = DL[j * D + f - 3 * D];
+                else if (f < 5 * D) continue;  // G_{t-1} k, written by the gain loop
+                else v = SC[j * C::NSC + f - 5 * D];
+                rec[(size_t)(t0 + j) * C::REC + f] = v;
+            }
+        }
+        // the shared gain over the tile's tokens: thread (grow, gc0) holds G[grow][gc0..]
+        for (int j = 0; j < Lt; ++j) {
+            const float *kj = K + j * D;
+            float part = 0.0f;
+#pragma unroll
+            for (int c = 0; c < C::CPT; ++c) part = fmaf(G[c], kj[gc0 + c], part);
+#pragma unroll
+            for (int o = C::TPR / 2; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+            if (record) {
+                float *gd = gsc + ((size_t)(t0 + j) * C::NT + tid) * C::CPT;
+                if constexpr (C::CPT % 4 == 0) {
+#pragma unroll
+                    for (int c = 0; c < C::CPT; c += 4)
+                        *reinterpret_cast<float4 *>(gd + c) = make_float4(G[c], G[c + 1], G[c + 2], G[c + 3]);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < C::CPT; ++c) gd[c] = G[c];
+                }
+                if (gc0 == 0) rec[(size_t)(t0 + j) * C::REC + 4 * D + grow] = part;
+            }
+            const float et = SC[j * C::NSC + C::S_ET], al = SC[j * C::NSC + C::S_AL];
+            const float s = et * (part + DL[j * D + grow]);
+#pragma unroll
+            for (int c = 0; c < C::CPT; ++c) G[c] = fmaf(-s, kj[gc0 + c], al * G[c]);
+        }
+    };
+
+    // ---- pass 1: forward, checkpointing each chunk's boundary state
+    for (int c = 0; c < nchunks; ++c) {
+        const int c0 = c * Cr, L = min(Cr, N - c0);
+        __syncthreads();
+        float *ck = ckpt + (size_t)c * SZ;
+        for (int e = tid; e < C::R * D; e += C::NT) ck[e] = S[(e / D) * C::SS + (e % D)];
+        if (c == nchunks - 1) break;  // the last chunk's end state is not needed
+#pragma unroll
+        for (int q = 0; q < C::CPT; ++q) G[q] = (grow == gc0 + q) ? 1.0f : 0.0f;
+        for (int t0 = 0; t0 < L; t0 += C::T) tile_forward(c0, t0, min(C::T, L - t0), false);
+        // chunk end: S <- S_b G, row by row
+        __syncthreads();
+#pragma unroll
+        for (int q = 0; q < C::CPT; ++q) GT[grow * D + gc0 + q] = G[q];
+        __syncthreads();
+        for (int o = warp; o < C::R; o += C::NW) {
+            const float *srow = S + o * C::SS;
+            float acc[C::CPL];
+#pragma unroll
+            for (int m = 0; m < C::CPL; ++m) acc[m] = 0.0f;
+#pragma unroll 8
+            for (int l = 0; l < D; ++l) {
+                const float s = srow[l];
+#pragma unroll
+                for (int m = 0; m < C::CPL; ++m) {
+                    const int i = lane + 32 * m;
+                    if (i < D) acc[m] = fmaf(s, GT[l * D + i], acc[m]);
+                }
+            }
+            __syncwarp();
+#pragma unroll
+            for (int m = 0; m < C::CPL; ++m) {
+                const int i = lane + 32 * m;
+                if (i < D) S[o * C::SS + i] = acc[m];
+            }
+            __syncwarp();
+        }
+    }
+
+    // ---- pass 2: reverse
+    __syncthreads();
+    {
+        const float *dmf = ba.dmem_final ? ba.dmem_final + (((size_t)b * 4 + r) * a.nh + h) * SZ : nullptr;
+        for (int e = tid; e < C::R * D; e += C::NT) dS[(e / D) * C::SS + (e % D)] = dmf ? dmf[e] : 0.0f;
+    }
+    for (int c = nchunks - 1; c >= 0; --c) {
+        const int c0 = c * Cr, L = min(Cr, N - c0);
+        __syncthreads();
+        const float *ck = ckpt + (size_t)c * SZ;
+        for (int e = tid; e < C::R * D; e += C::NT) S[(e / D) * C::SS + (e % D)] = ck[e];
+#pragma unroll
+        for (int q = 0; q < C::CPT; ++q) G[q] = (grow == gc0 + q) ? 1.0f : 0.0f;
+        // a. regenerate the chunk, recording
+        for (int t0 = 0; t0 < L; t0 += C::T) tile_forward(c0, t0, min(C::T, L - t0), true);
+        // b. chunk end: P_L = S_b^T dS (this thread's slice), then dS <- dS G_L^T
+        __syncthreads();
+#pragma unroll
+        for (int q = 0; q < C::CPT; ++q) GT[(gc0 + q) * D + grow] = G[q];
+        float Pg[C::CPT];
+#pragma unroll
+        for (int q = 0; q < C::CPT; ++q) Pg[q] = 0.0f;
+        for (int o = 0; o < C::R; ++o) {
+            const float sv = S[o * C::SS + grow];
+#pragma unroll
+            for (int q = 0; q < C::CPT; ++q) Pg[q] = fmaf(sv, dS[o * C::SS + gc0 + q], Pg[q]);
+        }
+        __syncthreads();
+        for (int o = warp; o < C::R; o += C::NW) {
+            const float *drow = dS + o * C::SS;
+            float acc[C::CPL];
+#pragma unroll
+            for (int m = 0; m < C::CPL; ++m) acc[m] = 0.0f;
+#pragma unroll 8
+            for (int i = 0; i < D; ++i) {
+                const float s = drow[i];
+#pragma unroll
+                for (int m = 0; m < C::CPL; ++m) {
+                    const int jj = lane + 32 * m;
+                    if (jj < D) acc[m] = fmaf(s, GT[i * D + jj], acc[m]);
+                }
+            }
+            __syncwarp();
+#pragma unroll
+            for (int m = 0; m < C::CPL; ++m) {
+                const int jj = lane + 32 * m;
+                if (jj < D) dS[o * C::SS + jj] = acc[m];
+            }
+            __syncwarp();
+        }
+        // c-e. tiles, last first
+        const int ntiles = (L + C::T - 1) / C::T;
+        for (int ti = ntiles - 1; ti >= 0; --ti) {
+            const int t0 = ti * C::T, Lt = min(C::T, L - t0);
+            __syncthreads();
+            for (int e = tid; e < Lt * D; e += C::NT) {
+                const int j = e / D, f = e % D;
+                const float *rc = rec + (size_t)(t0 + j) * C::REC;
+                X[e] = rc[f];
+                K[e] = rc[D + f];
+                Q[e] = rc[2 * D + f];
+                DL[e] = rc[3 * D + f];
+                Z[e] = rc[4 * D + f] + rc[3 * D + f];
+                KG[e] = 0.0f;
+            }
+            for (int e = tid; e < Lt * C::NSC; e += C::NT)
+                SC[e] = rec[(size_t)(t0 + e / C::NSC) * C::REC + 5 * D + e % C::NSC];
+            for (int e = tid; e < 2 * Lt; e += C::NT) SG[e] = 0.0f;
+            __syncthreads();
+            // c. gain adjoint, last token first
+            for (int j = Lt - 1; j >= 0; --j) {
+                float gp[C::CPT];
+                const float *gs = gsc + ((size_t)(t0 + j) * C::NT + tid) * C::CPT;
+                if constexpr (C::CPT % 4 == 0) {
+#pragma unroll
+                    for (int q = 0; q < C::CPT; q += 4) {
+                        const float4 f = *reinterpret_cast<const float4 *>(gs + q);
+                        gp[q] = f.x; gp[q + 1] = f.y; gp[q + 2] = f.z; gp[q + 3] = f.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int q = 0; q < C::CPT; ++q) gp[q] = gs[q];
+                }
+                const float *kj = K + j * D;
+                float u = 0.0f;
+#pragma unroll
+                for (int q = 0; q < C::CPT; ++q) u = fmaf(Pg[q], kj[gc0 + q], u);
+#pragma unroll
+                for (int o = C::TPR / 2; o > 0; o >>= 1) u += __shfl_xor_sync(0xffffffffu, u, o);
+                const float zr = Z[j * D + grow];
+                const float al = SC[j * C::NSC + C::S_AL], et = SC[j * C::NSC + C::S_ET];
+                float cp[C::CPT];
+                float sa = 0.0f;
+#pragma unroll
+                for (int q = 0; q < C::CPT; ++q) {
+                    cp[q] = fmaf(gp[q], u, Pg[q] * zr);
+                    sa = fmaf(Pg[q], gp[q], sa);
+                }
+                float se = gc0 == 0 ? -zr * u : 0.0f;
+                if (gc0 == 0) DG[j * D + grow] = -et * u;
+#pragma unroll
+                for (int q = 0; q < C::CPT; ++q) Pg[q] = fmaf(-et * u, kj[gc0 + q], al * Pg[q]);
+                col_sums_add<D>(cp, lane, gc0, KG + j * D, -et);
+                // deta (lanes < 16 keep it) and dalpha (lanes >= 16) in one reduction
+                {
+                    const bool up = (lane & 16) != 0;
+                    float v = (up ? sa : se) + __shfl_xor_sync(0xffffffffu, up ? se : sa, 16);
+#pragma unroll
+                    for (int o = 8; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+                    if (lane == 0) atomicAdd(&SG[2 * j], v);
+                    if (lane == 16) atomicAdd(&SG[2 * j + 1], v);
+                }
+            }
+            __syncthreads();
+            // d. per-token adjoints, one warp per token
+            for (int j = warp; j < Lt; j += C::NW) {
+                const float *sc = SC + j * C::NSC;
+                const int pix = __float_as_int(sc[C::S_PIX]);
+                float *wv = Wv + warp * 4 * D;  // dy | dk_raw | dv | dq_raw
+                float dy[C::CPL], kk[C::CPL], qv[C::CPL], dl[C::CPL];
+#pragma unroll
+                for (int m = 0; m < C::CPL; ++m) {
+                    const int c = lane + 32 * m;
+                    const bool ok = c < D;
+                    dy[m] = ok ? (lam ? lam[c] : 1.0f) * gob[(size_t)pix * Cc + c] : 0.0f;
+                    kk[m] = ok ? K[j * D + c] : 0.0f;
+                    qv[m] = ok ? Q[j * D + c] : 0.0f;
+                    dl[m] = ok ? DL[j * D + c] : 0.0f;
+                    if (ok) {
+                        wv[c] = dy[m];
+                        Y[j * D + c] = dy[m];
+                    }
+                }
+                __syncwarp();
+                // readout adjoint: dq = M^m_b^T dy
+                float dq[C::CPL];
+#pragma unroll
+                for (int m = 0; m < C::CPL; ++m) {
+                    const int c = lane + 32 * m;
+                    float acc = 0.0f;
+                    if (c < D) {
+#pragma unroll 8
+                        for (int i = 0; i < D; ++i) acc = fmaf(S[(3 * D + i) * C::SS + c], wv[i], acc);
+                    }
+                    dq[m] = acc;
+                }
+                // executed step and gates
+                const float det = SG[2 * j];
+                float deta = 0.0f, dalpha = SG[2 * j + 1], dkn2 = 0.0f, ddd = 0.0f;
+                if (a.gate_mode != VH_GATE_FORCED_EXEC) {
+                    if (sc[C::S_BR] != 0.0f) {  // spectral limit executed
+                        const float kn2 = sc[C::S_KN2];
+                        const float fl = fmaxf(kn2, a.kk_floor);
+                        dalpha += det * a.spec_factor * 2.0f / fl;
+                        if (kn2 > a.kk_floor) dkn2 -= det * sc[C::S_SPEC] / kn2;
+                    } else if (sc[C::S_INJ] > 0.0f) {  // soft injection cap
+                        const float einj = sc[C::S_INJ], eta = sc[C::S_ETA], rr = sc[C::S_R];
+                        const float x = eta / einj;
+                        const float ex = expf(-x);
+                        deta += det * ex;
+                        const float dinj = det * (-expm1f(-x) - x * ex);
+                        dalpha -= dinj * a.inj_factor / rr;  // eta_inj falls with alpha
+                        const float dr = -dinj * einj / rr;
+                        ddd += dr / (2.0f * sqrtf(sc[C::S_DD] + a.eps * a.eps));
+                    }
+                }
+                float dse = 0.0f, dsa = 0.0f;
+                if (a.gate_mode == VH_GATE_GENERATED) {
+                    dse = deta * a.gamma_eta / (1.0f + expf(-sc[C::S_SE]));  // softplus' = sigmoid
+                    dsa = dalpha * sc[C::S_AL] * sc[C::S_OMA];
+                }
+                // delta = k - v, the two normalisations
+                float dk[C::CPL], ddl[C::CPL];
+                float kdk = 0.0f, qdq = 0.0f;
+#pragma unroll
+                for (int m = 0; m < C::CPL; ++m) {
+                    const int c = lane + 32 * m;
+                    const bool ok = c < D;
+                    ddl[m] = ok ? fmaf(2.0f * ddd, dl[m], DG[j * D + c]) : 0.0f;
+                    dk[m] = ok ? fmaf(2.0f * dkn2, kk[m], KG[j * D + c]) + ddl[m] : 0.0f;
+                    kdk = fmaf(kk[m], dk[m], kdk);
+                    qdq = fmaf(qv[m], dq[m], qdq);
+                }
+                kdk = warp_sum(kdk);
+                qdq = warp_sum(qdq);
+                const float nk = sc[C::S_NK], nq = sc[C::S_NQ];
+                float *gv = P + j * C::PS;  // generation adjoints dk_raw | dv | dq_raw | dse dsa
+#pragma unroll
+                for (int m = 0; m < C::CPL; ++m) {
+                    const int c = lane + 32 * m;
+                    if (c < D) {
+                        const float dkr = (dk[m] - kk[m] * kdk) / nk;
+                        const float dqr = (dq[m] - qv[m] * qdq) / nq;
+                        wv[D + c] = dkr;
+                        wv[2 * D + c] = -ddl[m];
+                        wv[3 * D + c] = dqr;
+                        gv[c] = dkr;
+                        gv[D + c] = -ddl[m];
+                        gv[2 * D + c] = dqr;
+                    }
+                }
+                if (lane == 0) {
+                    gv[3 * D] = dse;
+                    gv[3 * D + 1] = dsa;
+                }
+                __syncwarp();
+                // dx_t = M^k^T dk_raw + M^v^T dv + M^q^T dq_raw + m^eta dse + m^alpha dsa
+#pragma unroll
+                for (int m = 0; m < C::CPL; ++m) {
+                    const int c = lane + 32 * m;
+                    if (c < D) {
+                        float acc = fmaf(S[(4 * D) * C::SS + c], dse, S[(4 * D + 1) * C::SS + c] * dsa);
+#pragma unroll 4
+                        for (int i = 0; i < D; ++i) {
+                            acc = fmaf(S[i * C::SS + c], wv[D + i], acc);
+                            acc = fmaf(S[(D + i) * C::SS + c], wv[2 * D + i], acc);
+                            acc = fmaf(S[(2 * D + i) * C::SS + c], wv[3 * D + i], acc);
+                        }
+                        atomicAdd(dxb + (size_t)pix * Cc + c, acc);
+                    }
+                }
+                __syncwarp();
+            }
+            __syncthreads();
+            // e. generation and readout adjoints into dL/dS_b
+            for (int e = tid; e < C::R * D; e += C::NT) {
+                const int o = e / D, jj = e % D;
+                float acc = 0.0f;
+                if (o < 3 * D) {
+                    for (int t = 0; t < Lt; ++t) acc = fmaf(P[t * C::PS + o], X[t * D + jj], acc);
+                } else if (o < 4 * D) {
+                    for (int t = 0; t < Lt; ++t) acc = fmaf(Y[t * D + o - 3 * D], Q[t * D + jj], acc);
+                } else {
+                    for (int t = 0; t < Lt; ++t) acc = fmaf(P[t * C::PS + 3 * D + (o - 4 * D)], X[t * D + jj], acc);
+                }
+                dS[o * C::SS + jj] += acc;
+            }
+        }
+    }
+    __syncthreads();
+    float *dm = ba.dmem0 + ((size_t)r * a.nh + h) * SZ;
+    for (int e = tid; e < C::R * D; e += C::NT) atomicAdd(dm + e, dS[(e / D) * C::SS + (e % D)]);
+}
+
+template <int D, typename XT>
+static cudaError_t launch_bwd_t(const BwdArgs &ba, cudaStream_t st)
+{
+    using C = BwdCfg<D>;
+    auto kern = scan_bwd_kernel<D, XT>;
+    static int attr_set[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 64 && !attr_set[dev]) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::BYTES);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = 1;
+    }
+    const unsigned grid = (unsigned)(ba.s.B * ba.s.ndirs * ba.s.nh);
+    kern<<<grid, C::NT, C::BYTES, st>>>(ba);
+    return cudaGetLastError();
+}
+
+// Floats of workspace one CTA (scan) needs: boundary states, gain slices and records.
+size_t bwd_floats_per_scan(int d, int nck, int lmax)
+{
+    const size_t sz = (size_t)(4 * d + 2) * d;
+    return (size_t)nck * sz + (size_t)lmax * ((size_t)d * d + 5 * d + 16);
+}
+
+cudaError_t launch_scan_bwd(const BwdArgs &ba, int d, bool bf16, cudaStream_t st)
+{
+    switch (d) {
+    case 16: return bf16 ? launch_bwd_t<16, __nv_bfloat16>(ba, st) : launch_bwd_t<16, float>(ba, st);
+    case 32: return bf16 ? launch_bwd_t<32, __nv_bfloat16>(ba, st) : launch_bwd_t<32, float>(ba, st);
+    case 64: return bf16 ? launch_bwd_t<64, __nv_bfloat16>(ba, st) : launch_bwd_t<64, float>(ba, st);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace vh
