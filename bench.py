@@ -31,11 +31,16 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "4-dir VisionHOPE scan tokens/s on 1 GB300 at 56×56×96; % of roofline"
+METRIC_BWD = ("4-dir VisionHOPE scan backward (dx, dmemories0) tokens/s on 1 GB300 at "
+              "56×56×96; % of roofline")
 UNIT = "tokens/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_SOURCES = ["visual_backbone_gb300/csrc/vh_scan_simt.cu",
                   "visual_backbone_gb300/csrc/vh_scan_tc.cu",
                   "visual_backbone_gb300/csrc/vh_common.cuh"]
+KERNEL_SOURCES_BWD = ["visual_backbone_gb300/csrc/vh_scan_bwd.cu",
+                      "visual_backbone_gb300/csrc/vh_common.cuh"]
+FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12   # SMs x fp32 lanes x 2 flops x max clock
 
 
 # ---------------------------------------------------------------- helpers
@@ -59,6 +64,21 @@ def algorithmic_cost(wl, ndirs=4):
     return flops, float(nbytes)
 
 
+def backward_cost(wl, ndirs=4):
+    """Algorithmic flops of one backward call: the forward quantities it consumes plus
+    their adjoints, 2 x (20d^2 + 24d + (12d^3 + 6d^2)/C_r) per (token, route, head):
+    forward 7d^2 + 20d + (4d^3 + 2d^2)/C_r; gain adjoint 5d^2 (P k, the P update,
+    <P, G>, G^T u, P^T z); readout adjoint d^2; dx 3d^2 + 2d; the outer products into the
+    state adjoint 4d^2 + 2d; at each chunk end S_b^T dS and dS G^T, 2 (4d + 2) d^2."""
+    d = wl.d
+    flops = 0.0
+    for r in range(ndirs):
+        cr = wl.chunk if wl.chunk else (wl.W if r < 2 else wl.H)
+        macs = 20 * d * d + 24 * d + (12 * d ** 3 + 6 * d * d) / cr
+        flops += 2.0 * macs * wl.tokens * wl.nh
+    return flops
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -69,21 +89,21 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash():
+def kernel_source_hash(sources=None):
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in sources or KERNEL_SOURCES:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:12]
 
 
-def recorded_traffic(workload: str, impl: str):
+def recorded_traffic(workload: str, impl: str, sources=None):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on
     the current kernel sources (profiles/traffic.txt: workload impl hash bytes)."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
         return None
-    cur = kernel_source_hash()
+    cur = kernel_source_hash(sources)
     for line in open(path):
         parts = line.split()
         if len(parts) >= 4 and not line.startswith("#"):
@@ -209,10 +229,29 @@ def cpu_cores():
         return os.cpu_count() or 1
 
 
+def time_grad_oracle(wl, images):
+    """Tokens/s of the gradient oracle (fp64 autograd of the restated forward) on the
+    first `images` images; returns (tokens/s, seconds, torch threads)."""
+    import numpy as np
+    import torch
+    from oracle import vh_grad
+    from visual_backbone_gb300 import synth
+    inp = synth.make_inputs(wl, batch=images)
+    dout = np.random.default_rng(7).standard_normal(inp.x64.shape)
+    p = __import__("oracle").OracleParams(eta_bias=wl.eta_bias, alpha_init=wl.alpha_init)
+    t0 = time.perf_counter()
+    vh_grad.backward(inp.x64, inp.mem0.astype(np.float64), dout, wl.H, wl.W, wl.nh, wl.d,
+                     chunk_len=wl.chunk, params=p)
+    dt = time.perf_counter() - t0
+    return images * wl.N / dt, dt, torch.get_num_threads()
+
+
 def run_reference(args, wl):
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
+    if args.pass_ == "backward":
+        return run_reference_backward(args, wl)
     images = args.ref_images
     cores = min(cpu_cores(), images * wl.nh)
     for _ in range(args.warmup):
@@ -240,6 +279,32 @@ def run_reference(args, wl):
     return 0
 
 
+def run_reference_backward(args, wl):
+    for _ in range(args.warmup):
+        time_grad_oracle(wl, args.ref_images)
+    times, cores = [], 1
+    t_start = time.perf_counter()
+    for _ in range(args.steps):
+        _, dt, cores = time_grad_oracle(wl, args.ref_images)
+        times.append(dt)
+    total = sum(times)
+    value = args.steps * args.ref_images * wl.N / total
+    sample = (f"{args.ref_images} image(s) of the {wl.name} workload per step, fp64 gradient "
+              f"oracle (PyTorch CPU autograd), {cores} threads")
+    line = {
+        "impl": "reference", "metric": METRIC_BWD, "value": value, "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(wl, args),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "wall_s": time.perf_counter() - t_start,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def workload_config(wl, args):
     return {"workload": f"{wl.name}: B={wl.B} {wl.H}x{wl.W} map, Cc={wl.Cc} as {wl.nh} heads x "
                         f"d={wl.d}, chunk={'row W / col H' if wl.chunk == 0 else wl.chunk}, "
@@ -248,7 +313,7 @@ def workload_config(wl, args):
             "global_batch": wl.B * dist_env()[1], "tokens_per_step_per_gpu": wl.tokens,
             "parallelism": f"dp{dist_env()[1]} (images split across GPUs, no collective)",
             "l2": "256 MiB buffer written between timed steps (L2 is 129 MB)",
-            "kernel": args.kernel, "readout": args.readout}
+            "kernel": args.kernel, "readout": args.readout, "pass": args.pass_}
 
 
 # ------------------------------------------------------------ our arm
@@ -407,6 +472,135 @@ def run_ours(args, wl):
     return 0
 
 
+def run_backward(args, wl):
+    """The backward call (vh_scan_backward): gradients of <dout, out> with respect to x and
+    memories0, on the same synthetic inputs; one kernel launch per step."""
+    import numpy as np
+    import torch
+    import visual_backbone_gb300 as vh
+    from visual_backbone_gb300 import _build, synth
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0 and not os.path.exists(vh.LIB_PATH):
+        _build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    inp = synth.make_inputs(wl)
+    if wl.dtype == "bf16":
+        x_host = torch.from_numpy(inp.x_store.view("int16")).view(torch.bfloat16)
+    else:
+        x_host = torch.from_numpy(inp.x_store)
+    dout_host = torch.from_numpy(
+        np.random.default_rng(11).standard_normal((wl.B, wl.H, wl.W, wl.Cc)).astype(np.float32))
+    x, dout = x_host.to(dev), dout_host.to(dev)
+    mem0 = torch.from_numpy(inp.mem0).to(dev)
+    dx = torch.empty((wl.B, wl.H, wl.W, wl.Cc), dtype=torch.float32, device=dev)
+    dmem0 = torch.empty_like(mem0)
+    ws = torch.empty(vh.backward_workspace_size(x, wl.d, chunk=wl.chunk), dtype=torch.uint8,
+                     device=dev)
+    flush = torch.empty(64 << 20, dtype=torch.float32, device=dev)
+    params = vh.ScanParams(eta_bias=wl.eta_bias, alpha_init=wl.alpha_init, impl=args.kernel)
+    stream = torch.cuda.Stream(device=dev)
+
+    def call():
+        vh.scan_backward(x, mem0, wl.d, dout, chunk=wl.chunk, params=params, dx=dx, dmem0=dmem0,
+                         workspace=ws, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            call()
+        torch.cuda.synchronize(dev)
+        events = [[torch.cuda.Event(enable_timing=True) for _ in range(2)]
+                  for _ in range(args.steps)]
+        sampler = ClockSampler(None).start() if rank == 0 else None
+        time.sleep(0.3 if sampler else 0.0)
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+        t0 = time.time()
+        for i in range(args.steps):
+            flush.zero_()
+            events[i][0].record(stream)
+            call()
+            events[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        t1 = time.time()
+        if world > 1:
+            torch.distributed.barrier()
+        if sampler:
+            time.sleep(0.3)
+            sampler.stop()
+    step_ms = [e[0].elapsed_time(e[1]) for e in events]
+    total_s, = max_over_ranks([sum(step_ms) / 1e3], device=dev)
+    avg_s = total_s / args.steps
+    value = job_throughput(wl.tokens, args.steps, world, total_s)
+
+    x_pin, dout_pin = x_host.pin_memory(), dout_host.pin_memory()
+    dx_pin = torch.empty(dx.shape, dtype=torch.float32).pin_memory()
+    dm_pin = torch.empty(dmem0.shape, dtype=torch.float32).pin_memory()
+    e2e_steps = max(3, min(args.steps, 10))
+    with torch.cuda.stream(stream):
+        def e2e_step():
+            x.copy_(x_pin, non_blocking=True)
+            dout.copy_(dout_pin, non_blocking=True)
+            call()
+            dx_pin.copy_(dx, non_blocking=True)
+            dm_pin.copy_(dmem0, non_blocking=True)
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ea.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        eb.record(stream)
+        torch.cuda.synchronize(dev)
+    e2e_s, = max_over_ranks([ea.elapsed_time(eb) / 1e3], device=dev)
+    e2e_value = job_throughput(wl.tokens, e2e_steps, world, e2e_s)
+
+    tc_ckpt = (wl.d == 32 and wl.dtype == "bf16" and wl.chunk == 0 and wl.Cc % 8 == 0
+               and args.kernel != "simt")
+    if rank == 0:
+        flops = backward_cost(wl)
+        achieved = flops / avg_s / 1e12
+        roof = {"bound": "alu", "achieved": achieved, "peak": FP32_PEAK_TFLOPS,
+                "unit": "TFLOP/s", "frac": achieved / FP32_PEAK_TFLOPS,
+                "traffic": recorded_traffic(wl.name, "backward", KERNEL_SOURCES_BWD),
+                "peak_source": "nominal fp32 FMA peak (152 SMs x 128 lanes x 2 x 2.07 GHz)",
+                "flops_per_launch": flops, "kernel_ms": avg_s * 1e3,
+                "workspace_bytes": int(ws.numel())}
+        line = {
+            "metric": METRIC_BWD, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * avg_s,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "numerics": "fp32 on CUDA cores (x bf16 exact); gradients summed with atomics",
+            "data": "synthetic", "config": workload_config(wl, args), "roofline": roof,
+            "e2e": {"value": e2e_value, "unit": UNIT,
+                    "h2d_bytes_per_step": int(x_host.numel() * x_host.element_size()
+                                              + dout_host.numel() * 4),
+                    "d2h_bytes_per_step": int(dx.numel() * 4 + dmem0.numel() * 4),
+                    "steps": e2e_steps},
+            # the backward kernel, after the tensor-core forward that writes the chunk
+            # boundary states where it applies (d = 32, bf16, aligned chunks)
+            "gpu_launches": args.steps * (2 if tc_ckpt else 1),
+            "clocks": sampler.summary(t0, t1) if sampler else None,
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            v, dt, cores = time_grad_oracle(wl, 1)
+            line["cpu_baseline"] = {
+                "value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                "sample": f"1 of {wl.B} images (all 4 routes x {wl.nh} heads), fp64 gradient "
+                          f"oracle, {dt:.1f} s wall"}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -419,6 +613,8 @@ def main(argv=None):
     ap.add_argument("--readout", choices=["memory", "outer"], default="memory",
                     help="memory: six-memory form (q from M^q); outer: VisionHOPE-exact "
                          "readout with an outer query projection and channel-wise skip")
+    ap.add_argument("--pass", dest="pass_", choices=["forward", "backward"], default="forward",
+                    help="forward: the scan (default); backward: its outer gradients")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-images", type=int, default=16)
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -436,6 +632,8 @@ def main(argv=None):
                  f"(WORLD_SIZE={dist_env()[1]})")
     if args.impl == "reference":
         return run_reference(args, wl)
+    if args.pass_ == "backward":
+        return run_backward(args, wl)
     return run_ours(args, wl)
 
 

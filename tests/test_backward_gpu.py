@@ -67,10 +67,14 @@ CASES = [
 ]
 
 
+@pytest.mark.parametrize("impl", ["simt", "auto"])
 @pytest.mark.parametrize("name,wl,dirs,chunk,kw,use_lam,use_dmf", CASES, ids=[c[0] for c in CASES])
-def test_backward_parity(orc, vhlib, name, wl, dirs, chunk, kw, use_lam, use_dmf):
+def test_backward_parity(orc, vhlib, name, wl, dirs, chunk, kw, use_lam, use_dmf, impl):
+    """impl "simt" runs the whole backward in its own kernel; "auto" takes the chunk
+    boundary states from the tensor-core forward where it applies (d = 32, bf16,
+    aligned chunks)."""
     inp = synth.make_inputs(wl)
-    vhp = vhlib.ScanParams(eta_bias=wl.eta_bias, alpha_init=wl.alpha_init, **kw)
+    vhp = vhlib.ScanParams(eta_bias=wl.eta_bias, alpha_init=wl.alpha_init, impl=impl, **kw)
     B = inp.x64.shape[0]
     dout = _dout(wl, B, 100 + wl.seed)
     lam = synth.make_dir_scale(wl) if use_lam else None

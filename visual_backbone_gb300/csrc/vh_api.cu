@@ -320,7 +320,19 @@ vh_status vh_scan_backward(const void *x, const float *memories0, const vh_param
     cudaError_t e = cudaMemsetAsync(dx, 0, gbytes, st);
     if (e == cudaSuccess) e = cudaMemsetAsync(dmem0, 0, mbytes, st);
     if (e != cudaSuccess) return cuda_fail(e, "zeroing dx / dmem0");
-    e = vh::launch_scan_bwd(ba, d, p->x_dtype == VH_DTYPE_BF16, st);
+    const bool bf16 = p->x_dtype == VH_DTYPE_BF16;
+    if (p->impl != VH_IMPL_SIMT) {
+        // the boundary states from the tensor-core forward (no readout), where it applies
+        vh::ScanArgs f = ba.s;
+        f.out = nullptr;
+        f.ckpt = ba.ws;
+        f.ckpt_stride = vh::bwd_floats_per_scan(d, ba.nck, ba.lmax);
+        bool handled = false;
+        e = vh::launch_scan_tc(f, d, bf16, st, &handled);
+        if (e != cudaSuccess) return cuda_fail(e, "tensor-core forward launch");
+        ba.have_ckpt = handled ? 1 : 0;
+    }
+    e = vh::launch_scan_bwd(ba, d, bf16, st);
     if (e != cudaSuccess) return cuda_fail(e, "backward scan launch");
     return VH_OK;
 }

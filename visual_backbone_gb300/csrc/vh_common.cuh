@@ -37,6 +37,10 @@ struct ScanArgs {
     // VisionHOPE-exact readout: normalised outer queries as three bf16 pieces
     // [3][B][H][W][Cc] (piece p at qhat + p * B*H*W*Cc); nullptr = q from M^q
     const __nv_bfloat16 *qhat;
+    // backward support: when set, the boundary state of every chunk of scan i is written
+    // to ckpt + i * ckpt_stride + chunk * (4d^2 + 2d) (fp32, state layout)
+    float *ckpt;
+    size_t ckpt_stride;
 };
 
 // Arguments of the backward scan kernel.
@@ -48,6 +52,7 @@ struct BwdArgs {
     float *dmem0;              // [4][nh][4d^2+2d], zeroed before the launch
     float *ws;                 // per scan: nck boundary states, lmax gain slices and records
     int nck, lmax;
+    int have_ckpt;             // the boundary states are already in ws (tensor-core forward)
 };
 
 // fp32 value of element e of the three-piece query planes (the pieces sum exactly).

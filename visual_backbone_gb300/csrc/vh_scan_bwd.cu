@@ -11,7 +11,9 @@
 //
 // One CTA owns one scan (image b, route r, head h).
 //  Pass 1 (forward): the state recurrence of the forward kernel without the readout; the
-//    boundary state S_b of every chunk goes to the workspace.
+//    boundary state S_b of every chunk goes to the workspace.  Where the tensor-core
+//    forward runs (d = 32, bf16, aligned chunks) it writes these states instead, in a
+//    launch of its own before this kernel, and pass 1 is skipped.
 //  Pass 2 (reverse, from the last chunk), holding dS = dL/dS_end of the chunk (dmem_final,
 //    or zero, for the last one):
 //    a. S_b is reloaded and the chunk's tokens regenerated tile by tile (Eq. (15),
@@ -46,7 +48,10 @@ struct BwdCfg {
     static constexpr int NW = NT / 32;
     static constexpr int R = 4 * D + 2;     // rows of the state
     static constexpr int SS = D + 1;        // padded row stride
-    static constexpr int T = D == 64 ? 16 : (D == 32 ? 32 : 64);  // token tile
+    static constexpr int T = D == 16 ? 64 : 16;   // token tile
+    static constexpr int MINB = D == 64 ? 1 : 3;  // resident CTAs per SM (one wave at stage 1)
+    static constexpr int JB = 4;                  // tokens per register block (generation)
+    static constexpr int PF = 4;                  // gain slices in flight (reverse loop)
     static constexpr int TPR = NT / D;      // threads per gain row
     static constexpr int CPT = D / TPR;     // gain columns per thread
     static constexpr int RW = 32 / TPR;     // gain rows per warp
@@ -71,8 +76,8 @@ struct BwdCfg {
     static constexpr int OFF_KG = OFF_SC + T * NSC;  // dk from the gain
     static constexpr int OFF_DG = OFF_KG + T * D;    // ddelta from the gain
     static constexpr int OFF_Y = OFF_DG + T * D;     // dy
-    static constexpr int OFF_SG = OFF_Y + T * D;     // deta, dalpha from the gain
-    static constexpr int OFF_W = OFF_SG + 2 * T;     // per warp: dy | dk_raw | dv | dq_raw
+    static constexpr int OFF_UV = OFF_Y + T * D;     // per (token, row): u = P k and <p, g>
+    static constexpr int OFF_W = OFF_UV + 2 * T * D; // per warp: dy | dk_raw | dv | dq_raw
     static constexpr int OFF_PIX = OFF_W + NW * 4 * D;
     static constexpr int FLOATS = OFF_PIX + T;
     static constexpr size_t BYTES = (size_t)FLOATS * 4;
@@ -119,7 +124,7 @@ __device__ __forceinline__ void col_sums_add(float (&v)[BwdCfg<D>::CPT], int lan
 }
 
 template <int D, typename XT>
-__global__ void __launch_bounds__(256, D == 64 ? 1 : 2) scan_bwd_kernel(const BwdArgs ba)
+__global__ void __launch_bounds__(256, BwdCfg<D>::MINB) scan_bwd_kernel(const BwdArgs ba)
 {
     using C = BwdCfg<D>;
     const ScanArgs &a = ba.s;
@@ -128,7 +133,7 @@ __global__ void __launch_bounds__(256, D == 64 ? 1 : 2) scan_bwd_kernel(const Bw
     float *S = sm + C::OFF_S, *dS = sm + C::OFF_DS, *GT = sm + C::OFF_GT;
     float *X = sm + C::OFF_X, *P = sm + C::OFF_P, *K = sm + C::OFF_K, *DL = sm + C::OFF_DL;
     float *Q = sm + C::OFF_Q, *Z = sm + C::OFF_Z, *SC = sm + C::OFF_SC, *KG = sm + C::OFF_KG;
-    float *DG = sm + C::OFF_DG, *Y = sm + C::OFF_Y, *SG = sm + C::OFF_SG, *Wv = sm + C::OFF_W;
+    float *DG = sm + C::OFF_DG, *Y = sm + C::OFF_Y, *UV = sm + C::OFF_UV, *Wv = sm + C::OFF_W;
     int *PIX = reinterpret_cast<int *>(sm + C::OFF_PIX);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -173,15 +178,30 @@ __global__ void __launch_bounds__(256, D == 64 ? 1 : 2) scan_bwd_kernel(const Bw
         __syncthreads();
         // generation from the boundary state, Eq. (15): rows 0..3d-1 (k, v, q), then the
         // eta and alpha rows (4d, 4d + 1)
-        constexpr int NG = 3 * D + 2;
-        for (int e = tid; e < Lt * NG; e += C::NT) {
-            const int j = e / NG, o = e % NG;
-            const float *srow = S + (o < 3 * D ? o : o + D) * C::SS;
-            const float *xj = X + j * D;
-            float acc = 0.0f;
+        // (lane = output row, JB tokens per item: one state load serves JB tokens)
+        {
+            constexpr int NG = 3 * D + 2;
+            constexpr int OB = (NG + 31) / 32;
+            const int nJB = (Lt + C::JB - 1) / C::JB;
+            for (int item = warp; item < OB * nJB; item += C::NW) {
+                const int o = (item % OB) * 32 + lane;
+                const int j0 = (item / OB) * C::JB;
+                if (o < NG) {
+                    const float *srow = S + (o < 3 * D ? o : o + D) * C::SS;
+                    float acc[C::JB];
+#pragma unroll
+                    for (int jj = 0; jj < C::JB; ++jj) acc[jj] = 0.0f;
 #pragma unroll 8
-            for (int i = 0; i < D; ++i) acc = fmaf(srow[i], xj[i], acc);
-            P[j * C::PS + o] = acc;
+                    for (int i = 0; i < D; ++i) {
+                        const float sv = srow[i];
+#pragma unroll
+                        for (int jj = 0; jj < C::JB; ++jj) acc[jj] = fmaf(sv, X[(j0 + jj) * D + i], acc[jj]);
+                    }
+#pragma unroll
+                    for (int jj = 0; jj < C::JB; ++jj)
+                        if (j0 + jj < Lt) P[(j0 + jj) * C::PS + o] = acc[jj];
+                }
+            }
         }
         __syncthreads();
         // per-token step, one warp per token
@@ -294,8 +314,9 @@ __global__ void __launch_bounds__(256, D == 64 ? 1 : 2) scan_bwd_kernel(const Bw
         }
     };
 
-    // ---- pass 1: forward, checkpointing each chunk's boundary state
-    for (int c = 0; c < nchunks; ++c) {
+    // ---- pass 1: forward, checkpointing each chunk's boundary state (skipped when the
+    // tensor-core forward has written them)
+    for (int c = 0; c < (ba.have_ckpt ? 0 : nchunks); ++c) {
         const int c0 = c * Cr, L = min(Cr, N - c0);
         __syncthreads();
         float *ck = ckpt + (size_t)c * SZ;
@@ -400,50 +421,67 @@ __global__ void __launch_bounds__(256, D == 64 ? 1 : 2) scan_bwd_kernel(const Bw
             }
             for (int e = tid; e < Lt * C::NSC; e += C::NT)
                 SC[e] = rec[(size_t)(t0 + e / C::NSC) * C::REC + 5 * D + e % C::NSC];
-            for (int e = tid; e < 2 * Lt; e += C::NT) SG[e] = 0.0f;
+            // dy = lambda_r dout at the tokens' pixels (Eq. (26) read backwards)
+            for (int e = tid; e < Lt * D; e += C::NT) {
+                const int j = e / D, f = e % D;
+                const int pix = route_pixel(r, c0 + t0 + j, H, W);
+                Y[e] = (lam ? lam[f] : 1.0f) * __ldg(gob + (size_t)pix * Cc + f);
+            }
             __syncthreads();
-            // c. gain adjoint, last token first
-            for (int j = Lt - 1; j >= 0; --j) {
-                float gp[C::CPT];
+            // c. gain adjoint, last token first; the slices of G_{t-1} are fetched PF
+            // tokens ahead
+            float ring[C::PF][C::CPT];
+            auto ld_slice = [&](int j, float (&g)[C::CPT]) {
                 const float *gs = gsc + ((size_t)(t0 + j) * C::NT + tid) * C::CPT;
                 if constexpr (C::CPT % 4 == 0) {
 #pragma unroll
                     for (int q = 0; q < C::CPT; q += 4) {
                         const float4 f = *reinterpret_cast<const float4 *>(gs + q);
-                        gp[q] = f.x; gp[q + 1] = f.y; gp[q + 2] = f.z; gp[q + 3] = f.w;
+                        g[q] = f.x; g[q + 1] = f.y; g[q + 2] = f.z; g[q + 3] = f.w;
                     }
                 } else {
 #pragma unroll
-                    for (int q = 0; q < C::CPT; ++q) gp[q] = gs[q];
+                    for (int q = 0; q < C::CPT; ++q) g[q] = gs[q];
                 }
-                const float *kj = K + j * D;
-                float u = 0.0f;
+            };
 #pragma unroll
-                for (int q = 0; q < C::CPT; ++q) u = fmaf(Pg[q], kj[gc0 + q], u);
+            for (int pf = 0; pf < C::PF; ++pf)
+                if (Lt - 1 - pf >= 0) ld_slice(Lt - 1 - pf, ring[pf]);
+            for (int jb = Lt - 1; jb >= 0; jb -= C::PF) {
 #pragma unroll
-                for (int o = C::TPR / 2; o > 0; o >>= 1) u += __shfl_xor_sync(0xffffffffu, u, o);
-                const float zr = Z[j * D + grow];
-                const float al = SC[j * C::NSC + C::S_AL], et = SC[j * C::NSC + C::S_ET];
-                float cp[C::CPT];
-                float sa = 0.0f;
+                for (int pf = 0; pf < C::PF; ++pf) {
+                    const int j = jb - pf;
+                    if (j < 0) break;
+                    float gp[C::CPT];
 #pragma unroll
-                for (int q = 0; q < C::CPT; ++q) {
-                    cp[q] = fmaf(gp[q], u, Pg[q] * zr);
-                    sa = fmaf(Pg[q], gp[q], sa);
-                }
-                float se = gc0 == 0 ? -zr * u : 0.0f;
-                if (gc0 == 0) DG[j * D + grow] = -et * u;
+                    for (int q = 0; q < C::CPT; ++q) gp[q] = ring[pf][q];
+                    if (j - C::PF >= 0) ld_slice(j - C::PF, ring[pf]);
+                    const float *kj = K + j * D;
+                    // u = P_t k_t and this row's share of <P_t, G_{t-1}>, reduced together
+                    float u = 0.0f, sa = 0.0f;
 #pragma unroll
-                for (int q = 0; q < C::CPT; ++q) Pg[q] = fmaf(-et * u, kj[gc0 + q], al * Pg[q]);
-                col_sums_add<D>(cp, lane, gc0, KG + j * D, -et);
-                // deta (lanes < 16 keep it) and dalpha (lanes >= 16) in one reduction
-                {
-                    const bool up = (lane & 16) != 0;
-                    float v = (up ? sa : se) + __shfl_xor_sync(0xffffffffu, up ? se : sa, 16);
+                    for (int q = 0; q < C::CPT; ++q) {
+                        u = fmaf(Pg[q], kj[gc0 + q], u);
+                        sa = fmaf(Pg[q], gp[q], sa);
+                    }
 #pragma unroll
-                    for (int o = 8; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-                    if (lane == 0) atomicAdd(&SG[2 * j], v);
-                    if (lane == 16) atomicAdd(&SG[2 * j + 1], v);
+                    for (int o = C::TPR / 2; o > 0; o >>= 1) {
+                        u += __shfl_xor_sync(0xffffffffu, u, o);
+                        sa += __shfl_xor_sync(0xffffffffu, sa, o);
+                    }
+                    const float zr = Z[j * D + grow];
+                    const float al = SC[j * C::NSC + C::S_AL], et = SC[j * C::NSC + C::S_ET];
+                    float cp[C::CPT];
+#pragma unroll
+                    for (int q = 0; q < C::CPT; ++q) cp[q] = fmaf(gp[q], u, Pg[q] * zr);
+                    if (gc0 == 0) {
+                        DG[j * D + grow] = -et * u;
+                        UV[j * D + grow] = u;
+                        UV[(C::T + j) * D + grow] = sa;
+                    }
+#pragma unroll
+                    for (int q = 0; q < C::CPT; ++q) Pg[q] = fmaf(-et * u, kj[gc0 + q], al * Pg[q]);
+                    col_sums_add<D>(cp, lane, gc0, KG + j * D, -et);
                 }
             }
             __syncthreads();
@@ -457,14 +495,11 @@ __global__ void __launch_bounds__(256, D == 64 ? 1 : 2) scan_bwd_kernel(const Bw
                 for (int m = 0; m < C::CPL; ++m) {
                     const int c = lane + 32 * m;
                     const bool ok = c < D;
-                    dy[m] = ok ? (lam ? lam[c] : 1.0f) * gob[(size_t)pix * Cc + c] : 0.0f;
+                    dy[m] = ok ? Y[j * D + c] : 0.0f;
                     kk[m] = ok ? K[j * D + c] : 0.0f;
                     qv[m] = ok ? Q[j * D + c] : 0.0f;
                     dl[m] = ok ? DL[j * D + c] : 0.0f;
-                    if (ok) {
-                        wv[c] = dy[m];
-                        Y[j * D + c] = dy[m];
-                    }
+                    if (ok) wv[c] = dy[m];
                 }
                 __syncwarp();
                 // readout adjoint: dq = M^m_b^T dy
@@ -479,9 +514,21 @@ __global__ void __launch_bounds__(256, D == 64 ? 1 : 2) scan_bwd_kernel(const Bw
                     }
                     dq[m] = acc;
                 }
+                // the gain's step and retention adjoints: deta_t = -z_t . u_t,
+                // dalpha_t = <P_t, G_{t-1}> (row shares summed)
+                float det = 0.0f, dag = 0.0f;
+#pragma unroll
+                for (int m = 0; m < C::CPL; ++m) {
+                    const int c = lane + 32 * m;
+                    if (c < D) {
+                        det = fmaf(-Z[j * D + c], UV[j * D + c], det);
+                        dag += UV[(C::T + j) * D + c];
+                    }
+                }
+                det = warp_sum(det);
+                dag = warp_sum(dag);
                 // executed step and gates
-                const float det = SG[2 * j];
-                float deta = 0.0f, dalpha = SG[2 * j + 1], dkn2 = 0.0f, ddd = 0.0f;
+                float deta = 0.0f, dalpha = dag, dkn2 = 0.0f, ddd = 0.0f;
                 if (a.gate_mode != VH_GATE_FORCED_EXEC) {
                     if (sc[C::S_BR] != 0.0f) {  // spectral limit executed
                         const float kn2 = sc[C::S_KN2];
@@ -557,18 +604,27 @@ __global__ void __launch_bounds__(256, D == 64 ? 1 : 2) scan_bwd_kernel(const Bw
                 __syncwarp();
             }
             __syncthreads();
-            // e. generation and readout adjoints into dL/dS_b
-            for (int e = tid; e < C::R * D; e += C::NT) {
-                const int o = e / D, jj = e % D;
-                float acc = 0.0f;
-                if (o < 3 * D) {
-                    for (int t = 0; t < Lt; ++t) acc = fmaf(P[t * C::PS + o], X[t * D + jj], acc);
-                } else if (o < 4 * D) {
-                    for (int t = 0; t < Lt; ++t) acc = fmaf(Y[t * D + o - 3 * D], Q[t * D + jj], acc);
-                } else {
-                    for (int t = 0; t < Lt; ++t) acc = fmaf(P[t * C::PS + 3 * D + (o - 4 * D)], X[t * D + jj], acc);
+            // e. generation and readout adjoints into dL/dS_b, four columns per item
+            for (int e = tid; e < C::R * (D / 4); e += C::NT) {
+                const int o = e / (D / 4), j4 = (e % (D / 4)) * 4;
+                float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+                const bool rd = o >= 3 * D && o < 4 * D;  // content memory: dy q^T
+                const float *vs = rd ? Y + (o - 3 * D) : P + (o < 3 * D ? o : o - D);
+                const int vstride = rd ? D : C::PS;
+                const float *us = (rd ? Q : X) + j4;
+                for (int t = 0; t < Lt; ++t) {
+                    const float g = vs[t * vstride];
+                    const float4 u = *reinterpret_cast<const float4 *>(us + t * D);
+                    a0 = fmaf(g, u.x, a0);
+                    a1 = fmaf(g, u.y, a1);
+                    a2 = fmaf(g, u.z, a2);
+                    a3 = fmaf(g, u.w, a3);
                 }
-                dS[o * C::SS + jj] += acc;
+                float *dd = dS + o * C::SS + j4;
+                dd[0] += a0;
+                dd[1] += a1;
+                dd[2] += a2;
+                dd[3] += a3;
             }
         }
     }

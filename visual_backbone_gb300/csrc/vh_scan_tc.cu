@@ -281,6 +281,13 @@ __global__ void __launch_bounds__(NT, 3)
         }
 #pragma unroll
         for (int g = 0; g < 4; ++g) store_split8(sS + op_off(ROW_MEM + tid, g), S_PIECE, v + 8 * g);
+        if (kAbl && a.ckpt) {  // boundary state of chunk 0 (backward support)
+            float4 *d4 = reinterpret_cast<float4 *>(a.ckpt + (size_t)blockIdx.x * a.ckpt_stride +
+                                                    (size_t)tid * D);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) d4[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+            if (tid < 2 * D) a.ckpt[(size_t)blockIdx.x * a.ckpt_stride + 4 * D * D + tid] = m0[4 * D * D + tid];
+        }
         // eta / alpha rows: fp32 copy and operand rows 0, 1; rows 2..15 are zero
         if (tid < 2 * D) Sea[tid] = m0[4 * D * D + tid];
         if (tid < ROW_MEM) {
@@ -301,7 +308,8 @@ __global__ void __launch_bounds__(NT, 3)
     const uint32_t lrow = ((uint32_t)(warp & 3) * 32u) << 16;  // this warp's TMEM lane quarter
 
     const float *lam = a.dir_scale ? a.dir_scale + (size_t)r * Cc + (size_t)h * D : nullptr;
-    float *ob = a.out + (size_t)b * H * W * Cc + (size_t)h * D;
+    // no out (backward support: only the boundary states are wanted): no readout adds
+    float *ob = (kAbl && !a.out) ? nullptr : a.out + (size_t)b * H * W * Cc + (size_t)h * D;
     unsigned n_spec = 0, n_inj = 0, n_nf = 0;
     uint32_t ph_x = 0, ph_gen = 0, ph_ro = 0, ph_upd = 0, ph_g = 0, ph_q = 0;
 
@@ -789,7 +797,7 @@ __global__ void __launch_bounds__(NT, 3)
                 // readout epilogue: lambda_r y added at the token's pixel (Eq. (26))
                 float y[32];
                 tmem_ld32(tbase + lrow + COL_RO, y);
-                if (valid) {
+                if (valid && (!kAbl || ob)) {
                     const int pix = rowr ? Lidx * W + p : p * W + Lidx;
                     float *dst = ob + (size_t)pix * Cc;
 #pragma unroll
@@ -846,6 +854,11 @@ __global__ void __launch_bounds__(NT, 3)
                     __syncwarp();
                     Sea[lane] = ne;
                     Sea[D + lane] = na;
+                    if (kAbl && a.ckpt && c + 1 < nlines) {  // backward support
+                        float *ck = a.ckpt + (size_t)blockIdx.x * a.ckpt_stride + (size_t)(c + 1) * SZ;
+                        ck[4 * D * D + lane] = ne;
+                        ck[4 * D * D + D + lane] = na;
+                    }
                     __nv_bfloat16 p1, p2, p3;
                     const int g = lane >> 3, e = lane & 7;
                     split3(ne, p1, p2, p3);
@@ -897,6 +910,13 @@ __global__ void __launch_bounds__(NT, 3)
                         }
                     }
                     if (!frz) store_split8(src, S_PIECE, v + 8 * g);
+                }
+                if (kAbl && a.ckpt && c + 1 < nlines) {  // boundary state of the next chunk
+                    float4 *d4 = reinterpret_cast<float4 *>(a.ckpt + (size_t)blockIdx.x * a.ckpt_stride +
+                                                            (size_t)(c + 1) * SZ + (size_t)tid * D);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        d4[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
                 }
                 if (c == nlines - 1 && a.mem_out) {
                     float *mo = a.mem_out + (((size_t)b * 4 + r) * a.nh + h) * SZ;
@@ -1028,7 +1048,7 @@ cudaError_t launch_scan_tc(const ScanArgs &a, int d, bool bf16, cudaStream_t st,
         attr_set[dev] = 1;
     }
     const unsigned grid = (unsigned)(a.B * a.ndirs * a.nh);
-    if (a.control_flags) {
+    if (a.control_flags || a.ckpt) {
         const int smem = (a.control_flags & VH_CTRL_INTRA_READ) ? tc::SMEM_INTRA : tc::SMEM_BYTES;
         tc::scan_tc_kernel<true><<<grid, tc::NT, smem, st>>>(a, mr, mc, qr, qc);
     } else {
