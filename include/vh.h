@@ -239,6 +239,56 @@ vh_status vh_scan_backward(const void *x, const float *memories0, const vh_param
  * chunk, d^2 + 5d + 16 floats per token.  0 for invalid arguments. */
 size_t vh_backward_workspace_size(const vh_params *p, int H, int W, unsigned dirs, int chunk);
 
+/*
+ * The VisionHOPE block around the operator ("VisionHOPE" Sec. 2.3 Eq. (27), App. B.5),
+ * inference, NHWC:
+ *   X0 = X + CPE(X);  U = Proj_in(LN1(X0));  Z = U + SiLU(DW(U));
+ *   Y = F_VH(Z) + DW_pos(Z);  X1 = X0 + Proj_out(Y);  out = X1 + FFN(LN2(X1)),
+ * FFN(a) = W_ff2 GELU(W_ff1 a + b_ff1) + b_ff2 (exact erf GELU).  CPE, DW and DW_pos are
+ * 3 x 3 depthwise convolutions with zero padding and a bias per channel; LN normalises
+ * the D channels of each pixel (biased variance, ln_eps) with a scale and shift per
+ * channel.  The pages fix the structure only; these forms are this library's readings.
+ * All pointers are device pointers owned by the caller.
+ */
+typedef struct {
+    int dim;                   /* D, block width (channels of x and out), multiple of 8, <= 1024 */
+    int hidden;                /* FFN width (4 D in the pages' models), multiple of 8 */
+    float ln_eps;              /* LayerNorm epsilon (1e-5 if 0) */
+    const float *cpe_w, *cpe_b;      /* [D][3][3], [D] */
+    const float *ln1_g, *ln1_b;      /* [D] */
+    const void *w_in;                /* bf16 [D_m][D], D_m = vh_params.channels */
+    const float *b_in;               /* [D_m] */
+    const float *dw_w, *dw_b;        /* [D_m][3][3], [D_m]: gated depthwise branch */
+    const float *pos_w, *pos_b;      /* [D_m][3][3], [D_m]: positional branch */
+    const void *w_out;               /* bf16 [D][D_m] */
+    const float *b_out;              /* [D] */
+    const float *ln2_g, *ln2_b;      /* [D] */
+    const void *w_ff1;               /* bf16 [hidden][D] */
+    const float *b_ff1;              /* [hidden] */
+    const void *w_ff2;               /* bf16 [D][hidden] */
+    const float *b_ff2;              /* [D] */
+} vh_block_weights;
+
+/*
+ * vh_block_forward -- one block.  x, out: device fp32 [B][H][W][D], 16-byte aligned, not
+ * aliased.  p describes the operator on the internal width: p->batch = B,
+ * p->channels = D_m, p->head_dim, p->x_dtype must be VH_DTYPE_BF16 (Z is bf16), and the
+ * operator's optional inputs as in vh_scan_forward (w_query, skip, dir_scale, stats,
+ * impl, gate and step-control constants); the operator runs all four routes with
+ * row/column-aligned chunks.  p->workspace must hold vh_block_workspace_size() bytes,
+ * 16-byte aligned: the block's intermediates, the operator's query planes and the
+ * GEMMs' scratch.  p->accumulate and p->memories_out must be 0 / NULL.
+ *
+ * The four pointwise layers run as cuBLASLt GEMMs (bf16 operands, fp32 accumulation,
+ * bias and residual in the epilogue); the library keeps one cuBLASLt handle per device,
+ * created on first use.  Errors: as vh_scan_forward, plus VH_ERR_CUDA for a GEMM failure.
+ */
+vh_status vh_block_forward(const float *x, const float *memories0, const vh_params *p,
+                           const vh_block_weights *w, int H, int W, float *out);
+
+/* Bytes of workspace vh_block_forward needs; 0 for invalid arguments. */
+size_t vh_block_workspace_size(const vh_params *p, const vh_block_weights *w, int H, int W);
+
 /* Static string for a status code. */
 const char *vh_status_string(vh_status s);
 

@@ -54,6 +54,17 @@ class CParams(ctypes.Structure):
     ]
 
 
+class CBlockWeights(ctypes.Structure):
+    """Mirror of ``vh_block_weights`` (include/vh.h)."""
+    _fields_ = [("dim", ctypes.c_int), ("hidden", ctypes.c_int), ("ln_eps", ctypes.c_float)] + [
+        (n, ctypes.c_void_p) for n in (
+            "cpe_w", "cpe_b", "ln1_g", "ln1_b", "w_in", "b_in", "dw_w", "dw_b", "pos_w", "pos_b",
+            "w_out", "b_out", "ln2_g", "ln2_b", "w_ff1", "b_ff1", "w_ff2", "b_ff2")]
+
+
+BLOCK_GEMM_WEIGHTS = ("w_in", "w_out", "w_ff1", "w_ff2")   # bf16; the rest fp32
+
+
 @dataclass
 class ScanParams:
     """Method constants and switches of one call (defaults: the pages' values)."""
@@ -94,6 +105,12 @@ def lib() -> ctypes.CDLL:
                                        vp, vp]
         L.vh_backward_workspace_size.restype = ctypes.c_size_t
         L.vh_backward_workspace_size.argtypes = [ctypes.POINTER(CParams), ci, ci, cu, ci]
+        L.vh_block_forward.restype = ci
+        L.vh_block_forward.argtypes = [vp, vp, ctypes.POINTER(CParams),
+                                       ctypes.POINTER(CBlockWeights), ci, ci, vp]
+        L.vh_block_workspace_size.restype = ctypes.c_size_t
+        L.vh_block_workspace_size.argtypes = [ctypes.POINTER(CParams),
+                                              ctypes.POINTER(CBlockWeights), ci, ci]
         L.vh_status_string.restype = ctypes.c_char_p
         L.vh_status_string.argtypes = [ci]
         L.vh_last_error.restype = ctypes.c_char_p
@@ -259,6 +276,61 @@ def scan_backward(x, memories0, head_dim: int, dout, dirs: int = DIR_ALL, chunk:
                                   dmem_final.data_ptr() if dmem_final is not None else None,
                                   dx.data_ptr(), dmem0.data_ptr()))
     return dx, dmem0
+
+
+def block_forward(x, memories0, weights: dict, head_dim: int, params: Optional[ScanParams] = None,
+                  w_query=None, skip=None, dir_scale=None, out=None, workspace=None,
+                  stats=None, stream=None, ln_eps: float = 1e-5):
+    """One VisionHOPE block (Eq. (27), App. B.5): x fp32 [B][H][W][D] (CUDA) -> out.
+
+    ``weights`` maps the fields of ``vh_block_weights`` to contiguous CUDA tensors: the
+    four GEMM weights (w_in [D_m][D], w_out [D][D_m], w_ff1 [hidden][D], w_ff2
+    [D][hidden]) bf16, the rest fp32.  The operator runs on D_m = w_in.shape[0] channels
+    as heads of ``head_dim`` with memories0, the outer query w_query [D_m][D_m], the skip
+    [4][D_m] and dir_scale [4][D_m] as in scan_forward.  The workspace (uint8, at least
+    vh_block_workspace_size bytes) is allocated here when not given."""
+    import torch
+    _require_cuda("x", x, (torch.float32,))
+    _require_cuda("memories0", memories0, (torch.float32,))
+    B, H, W, D = x.shape
+    for k in CBlockWeights._fields_[3:]:
+        name = k[0]
+        _require_cuda(name, weights[name],
+                      (torch.bfloat16,) if name in BLOCK_GEMM_WEIGHTS else (torch.float32,))
+    Dm = weights["w_in"].shape[0]
+    hidden = weights["w_ff1"].shape[0]
+    for t, name in ((w_query, "w_query"), (skip, "skip"), (dir_scale, "dir_scale")):
+        if t is not None:
+            _require_cuda(name, t, (torch.float32,))
+    if out is None:
+        out = torch.empty_like(x)
+    _require_cuda("out", out, (torch.float32,))
+    cw = CBlockWeights(D, hidden, ln_eps, *[weights[k[0]].data_ptr()
+                                            for k in CBlockWeights._fields_[3:]])
+    cp = make_cparams(B, Dm, head_dim, True, params,
+                      dir_scale_ptr=dir_scale.data_ptr() if dir_scale is not None else 0,
+                      stats_ptr=stats.data_ptr() if stats is not None else 0,
+                      stream_ptr=_stream_ptr(stream),
+                      w_query_ptr=w_query.data_ptr() if w_query is not None else 0,
+                      skip_ptr=skip.data_ptr() if skip is not None else 0)
+    need = lib().vh_block_workspace_size(ctypes.byref(cp), ctypes.byref(cw), H, W)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
+    _require_cuda("workspace", workspace, (torch.uint8,))
+    cp.workspace = workspace.data_ptr()
+    cp.workspace_bytes = workspace.numel()
+    _check(lib().vh_block_forward(x.data_ptr(), memories0.data_ptr(), ctypes.byref(cp),
+                                  ctypes.byref(cw), H, W, out.data_ptr()))
+    return out
+
+
+def block_workspace_size(x, weights: dict, head_dim: int, with_query: bool = True) -> int:
+    """Bytes of workspace block_forward needs for x's shape and these weights."""
+    B, H, W, D = x.shape
+    cp = make_cparams(B, weights["w_in"].shape[0], head_dim, True, None,
+                      w_query_ptr=1 if with_query else 0)
+    cw = CBlockWeights(D, weights["w_ff1"].shape[0], 1e-5)
+    return int(lib().vh_block_workspace_size(ctypes.byref(cp), ctypes.byref(cw), H, W))
 
 
 def check(stats, stream=None):

@@ -14,6 +14,19 @@ cudaError_t launch_qproj(const void *x, bool bf16, int d, const float *wq, const
                          const float *dir_scale, unsigned dirs, __nv_bfloat16 *qhat, float *out,
                          int accumulate, long npix, int Cc, float knorm_eps, cudaStream_t st);
 cudaError_t launch_scan_bwd(const BwdArgs &ba, int d, bool bf16, cudaStream_t st);
+cudaError_t launch_cpe_ln(const float *x, const float *cw, const float *cb, const float *g,
+                          const float *beta, float eps, float *x0, __nv_bfloat16 *a, int B, int H,
+                          int W, int D, cudaStream_t st);
+cudaError_t launch_ln(const float *x, const float *g, const float *beta, float eps,
+                      __nv_bfloat16 *a, long npix, int D, cudaStream_t st);
+cudaError_t launch_dwgate(const float *u, const float *w, const float *b, __nv_bfloat16 *z,
+                          long npix, int C, int H, int W, cudaStream_t st);
+cudaError_t launch_posdw(const float *y, const __nv_bfloat16 *z, const float *w, const float *b,
+                         __nv_bfloat16 *yb, long npix, int C, int H, int W, cudaStream_t st);
+cudaError_t launch_gelu(const float *a, __nv_bfloat16 *h, long n, cudaStream_t st);
+int block_gemm(int m, int n, int k, const __nv_bfloat16 *wt, const __nv_bfloat16 *act,
+               const float *bias, const float *res, float *out, void *ws, size_t ws_bytes,
+               cudaStream_t st);
 size_t bwd_floats_per_scan(int d, int nck, int lmax);
 }  // namespace vh
 
@@ -122,6 +135,32 @@ void bwd_extent(int H, int W, unsigned dirs, int chunk, int *nck, int *lmax)
         if (n > *nck) *nck = n;
         if (L > *lmax) *lmax = L;
     }
+}
+
+// Byte offsets of the block's intermediates in its workspace (256-byte aligned regions).
+struct BlockLayout {
+    size_t x0, a, u, z, yb, pre, h, qhat, lt, total;
+};
+
+constexpr size_t kLtWorkspace = 32u << 20;  // cuBLASLt scratch
+
+BlockLayout block_layout(const vh_params *p, const vh_block_weights *w, int H, int W)
+{
+    BlockLayout L{};
+    const size_t N = (size_t)p->batch * H * W, D = w->dim, Dm = p->channels, Hd = w->hidden;
+    size_t o = 0;
+    auto take = [&](size_t bytes) { const size_t at = o; o += (bytes + 255) & ~(size_t)255; return at; };
+    L.x0 = take(N * D * 4);
+    L.a = take(N * D * 2);
+    L.u = take(N * Dm * 4);
+    L.z = take(N * Dm * 2);
+    L.yb = take(N * Dm * 2);
+    L.pre = take(N * Hd * 4);
+    L.h = take(N * Hd * 2);
+    L.qhat = take(p->w_query ? 6 * N * Dm : 0);
+    L.lt = take(kLtWorkspace);
+    L.total = o;
+    return L;
 }
 
 }  // namespace
@@ -250,6 +289,91 @@ vh_status vh_scan_forward(const void *x, const float *memories0, const vh_params
         e = vh::launch_scan_simt(a, d, bf16, st);
         if (e != cudaSuccess) return cuda_fail(e, "scan launch");
     }
+    return VH_OK;
+}
+
+size_t vh_block_workspace_size(const vh_params *p, const vh_block_weights *w, int H, int W)
+{
+    if (!p || !w || p->batch < 1 || H < 1 || W < 1 || p->channels < 1 || w->dim < 1 ||
+        w->hidden < 1)
+        return 0;
+    return block_layout(p, w, H, W).total;
+}
+
+vh_status vh_block_forward(const float *x, const float *memories0, const vh_params *p,
+                           const vh_block_weights *w, int H, int W, float *out)
+{
+    g_err[0] = '\0';
+    vh_status s = check_common(p, H, W);
+    if (s != VH_OK) return s;
+    if (!w) return fail(VH_ERR_INVALID_ARG, "weights is NULL");
+    if (!x || !memories0 || !out) return fail(VH_ERR_INVALID_ARG, "x, memories0 and out must be non-NULL");
+    if (p->x_dtype != VH_DTYPE_BF16) return fail(VH_ERR_UNSUPPORTED, "the block runs the operator on bf16 Z");
+    if (p->accumulate || p->memories_out)
+        return fail(VH_ERR_INVALID_ARG, "accumulate and memories_out are not used by the block");
+    if (w->dim < 8 || w->dim > 1024 || w->dim % 8 || w->hidden < 8 || w->hidden % 8)
+        return fail(VH_ERR_INVALID_ARG, "dim %d (8..1024, multiple of 8) / hidden %d (multiple of 8)",
+                    w->dim, w->hidden);
+    const void *need[] = {w->cpe_w, w->cpe_b, w->ln1_g, w->ln1_b, w->w_in, w->b_in, w->dw_w, w->dw_b,
+                          w->pos_w, w->pos_b, w->w_out, w->b_out, w->ln2_g, w->ln2_b, w->w_ff1,
+                          w->b_ff1, w->w_ff2, w->b_ff2};
+    for (const void *q : need)
+        if (!q) return fail(VH_ERR_INVALID_ARG, "every weight pointer must be non-NULL");
+    const void *gw[] = {w->w_in, w->w_out, w->w_ff1, w->w_ff2};
+    for (const void *q : gw)
+        if (!aligned16(q)) return fail(VH_ERR_INVALID_ARG, "GEMM weights must be 16-byte aligned");
+    if (!aligned16(x) || !aligned16(out)) return fail(VH_ERR_INVALID_ARG, "x and out must be 16-byte aligned");
+    const BlockLayout L = block_layout(p, w, H, W);
+    if (!p->workspace || p->workspace_bytes < L.total || !aligned16(p->workspace))
+        return fail(VH_ERR_WORKSPACE, "the block needs a 16-byte aligned workspace of %zu bytes (have %zu)",
+                    L.total, p->workspace ? p->workspace_bytes : (size_t)0);
+    const int B = p->batch, D = w->dim, Dm = p->channels, Hd = w->hidden;
+    const long N = (long)B * H * W;
+    const size_t xb = (size_t)N * D * 4;
+    if (overlaps(x, xb, out, xb) || overlaps(x, xb, p->workspace, L.total) ||
+        overlaps(out, xb, p->workspace, L.total))
+        return fail(VH_ERR_INVALID_ARG, "x, out and the workspace must not overlap");
+    const float eps = w->ln_eps > 0.0f ? w->ln_eps : 1e-5f;
+    char *ws = static_cast<char *>(p->workspace);
+    float *x0 = reinterpret_cast<float *>(ws + L.x0);
+    __nv_bfloat16 *a = reinterpret_cast<__nv_bfloat16 *>(ws + L.a);
+    float *u = reinterpret_cast<float *>(ws + L.u);  // U, then Y
+    __nv_bfloat16 *z = reinterpret_cast<__nv_bfloat16 *>(ws + L.z);
+    __nv_bfloat16 *yb = reinterpret_cast<__nv_bfloat16 *>(ws + L.yb);
+    float *pre = reinterpret_cast<float *>(ws + L.pre);
+    __nv_bfloat16 *h = reinterpret_cast<__nv_bfloat16 *>(ws + L.h);
+    void *lt = ws + L.lt;
+    auto bw = [](const void *q) { return static_cast<const __nv_bfloat16 *>(q); };
+    cudaStream_t st = static_cast<cudaStream_t>(p->stream);
+    cudaError_t e;
+    int g;
+    // X0 = X + CPE(X), A = LN1(X0)
+    if ((e = vh::launch_cpe_ln(x, w->cpe_w, w->cpe_b, w->ln1_g, w->ln1_b, eps, x0, a, B, H, W, D, st)))
+        return cuda_fail(e, "CPE + LN1 launch");
+    // U = A W_in^T + b_in
+    if ((g = vh::block_gemm(Dm, (int)N, D, bw(w->w_in), a, w->b_in, nullptr, u, lt, kLtWorkspace, st)))
+        return fail(VH_ERR_CUDA, "Proj_in GEMM: cuBLASLt status %d", g);
+    // Z = U + SiLU(DW(U))
+    if ((e = vh::launch_dwgate(u, w->dw_w, w->dw_b, z, N, Dm, H, W, st)))
+        return cuda_fail(e, "gated depthwise launch");
+    // Y = F_VH(Z), into U's buffer
+    vh_params q = *p;
+    q.workspace = p->w_query ? ws + L.qhat : nullptr;
+    q.workspace_bytes = p->w_query ? 6 * (size_t)N * Dm : 0;
+    if ((s = vh_scan_forward(z, memories0, &q, H, W, VH_DIR_ALL, 0, u)) != VH_OK) return s;
+    // Y += DW_pos(Z), cast for Proj_out
+    if ((e = vh::launch_posdw(u, z, w->pos_w, w->pos_b, yb, N, Dm, H, W, st)))
+        return cuda_fail(e, "positional depthwise launch");
+    // X1 = X0 + Y W_out^T + b_out, into out
+    if ((g = vh::block_gemm(D, (int)N, Dm, bw(w->w_out), yb, w->b_out, x0, out, lt, kLtWorkspace, st)))
+        return fail(VH_ERR_CUDA, "Proj_out GEMM: cuBLASLt status %d", g);
+    // out = X1 + W_ff2 GELU(W_ff1 LN2(X1) + b_ff1) + b_ff2
+    if ((e = vh::launch_ln(out, w->ln2_g, w->ln2_b, eps, a, N, D, st))) return cuda_fail(e, "LN2 launch");
+    if ((g = vh::block_gemm(Hd, (int)N, D, bw(w->w_ff1), a, w->b_ff1, nullptr, pre, lt, kLtWorkspace, st)))
+        return fail(VH_ERR_CUDA, "FFN1 GEMM: cuBLASLt status %d", g);
+    if ((e = vh::launch_gelu(pre, h, (long)N * Hd, st))) return cuda_fail(e, "GELU launch");
+    if ((g = vh::block_gemm(D, (int)N, Hd, bw(w->w_ff2), h, w->b_ff2, out, out, lt, kLtWorkspace, st)))
+        return fail(VH_ERR_CUDA, "FFN2 GEMM: cuBLASLt status %d", g);
     return VH_OK;
 }
 
