@@ -31,6 +31,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "4-dir VisionHOPE scan tokens/s on 1 GB300 at 56×56×96; % of roofline"
+METRIC_BLOCK = ("VisionHOPE block (Eq. 27: CPE, LN, projections, gated depthwise, exact "
+                "operator, FFN) tokens/s on 1 GB300 at 56×56, D=192, D_m=96")
 METRIC_BWD = ("4-dir VisionHOPE scan backward (dx, dmemories0) tokens/s on 1 GB300 at "
               "56×56×96; % of roofline")
 UNIT = "tokens/s"
@@ -77,6 +79,21 @@ def backward_cost(wl, ndirs=4):
         macs = 20 * d * d + 24 * d + (12 * d ** 3 + 6 * d * d) / cr
         flops += 2.0 * macs * wl.tokens * wl.nh
     return flops
+
+
+def block_dims(wl):
+    """Block widths for a workload: D_m = the operator's channels, D = 2 D_m (the pages'
+    D_m = D / 2, "VisionHOPE" Sec. 3.4), FFN width 4 D."""
+    Dm = wl.Cc
+    return 2 * Dm, Dm, 8 * Dm
+
+
+def block_cost(wl):
+    """Algorithmic flops of one block call: the GEMMs (Proj_in, the outer query, Proj_out,
+    the two FFN layers) plus the operator (algorithmic_cost)."""
+    D, Dm, hidden = block_dims(wl)
+    gemm = 2.0 * wl.tokens * (D * Dm + Dm * Dm + Dm * D + 2 * D * hidden)
+    return gemm + algorithmic_cost(wl)[0], gemm
 
 
 def load_peaks():
@@ -246,12 +263,35 @@ def time_grad_oracle(wl, images):
     return images * wl.N / dt, dt, torch.get_num_threads()
 
 
+def time_block_oracle(wl, images):
+    """Tokens/s of the block oracle on the first `images` images."""
+    import numpy as np
+    import oracle
+    from oracle import vh_block as vb
+    from visual_backbone_gb300 import synth
+    oracle.build()
+    D, Dm, _ = block_dims(wl)
+    inp = synth.make_block_inputs(images, wl.H, wl.W, D, Dm, wl.d, wl.seed)
+    p = oracle.OracleParams(w_query=inp["w_query"].astype(np.float64),
+                            skip=inp["skip"].astype(np.float64),
+                            dir_scale=inp["dir_scale"].astype(np.float64))
+    cores = min(cpu_cores(), images * wl.nh)
+    t0 = time.perf_counter()
+    vb.block_forward(inp["x"].astype(np.float64), vb.weights_from(inp["weights"]),
+                     inp["mem0"].astype(np.float64), wl.H, wl.W, inp["nh"], wl.d, p,
+                     nthreads=cores)
+    dt = time.perf_counter() - t0
+    return images * wl.N / dt, dt, cores
+
+
 def run_reference(args, wl):
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
     if args.pass_ == "backward":
         return run_reference_backward(args, wl)
+    if args.pass_ == "block":
+        return run_reference_block(args, wl)
     images = args.ref_images
     cores = min(cpu_cores(), images * wl.nh)
     for _ in range(args.warmup):
@@ -305,6 +345,31 @@ def run_reference_backward(args, wl):
     return 0
 
 
+def run_reference_block(args, wl):
+    for _ in range(args.warmup):
+        time_block_oracle(wl, args.ref_images)
+    times, cores = [], 1
+    t_start = time.perf_counter()
+    for _ in range(args.steps):
+        _, dt, cores = time_block_oracle(wl, args.ref_images)
+        times.append(dt)
+    total = sum(times)
+    value = args.steps * args.ref_images * wl.N / total
+    line = {
+        "impl": "reference", "metric": METRIC_BLOCK, "value": value, "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(wl, args),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{args.ref_images} image(s) per step, fp64 block oracle "
+                                   f"(numpy + the C scan oracle), {cores} threads"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "wall_s": time.perf_counter() - t_start,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def workload_config(wl, args):
     return {"workload": f"{wl.name}: B={wl.B} {wl.H}x{wl.W} map, Cc={wl.Cc} as {wl.nh} heads x "
                         f"d={wl.d}, chunk={'row W / col H' if wl.chunk == 0 else wl.chunk}, "
@@ -313,7 +378,9 @@ def workload_config(wl, args):
             "global_batch": wl.B * dist_env()[1], "tokens_per_step_per_gpu": wl.tokens,
             "parallelism": f"dp{dist_env()[1]} (images split across GPUs, no collective)",
             "l2": "256 MiB buffer written between timed steps (L2 is 129 MB)",
-            "kernel": args.kernel, "readout": args.readout, "pass": args.pass_}
+            "kernel": args.kernel, "readout": args.readout, "pass": args.pass_,
+            **({"block": "D=%d D_m=%d hidden=%d, 3x3 depthwise, exact operator" % block_dims(wl)}
+               if args.pass_ == "block" else {})}
 
 
 # ------------------------------------------------------------ our arm
@@ -601,6 +668,124 @@ def run_backward(args, wl):
     return 0
 
 
+def run_block(args, wl):
+    """One VisionHOPE block per step (vh_block_forward) on the workload's map with
+    D = 2 D_m, synthetic weights; fp32 activations in HBM."""
+    import numpy as np
+    import torch
+    import visual_backbone_gb300 as vh
+    from visual_backbone_gb300 import _build, synth
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0 and not os.path.exists(vh.LIB_PATH):
+        _build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    D, Dm, hidden = block_dims(wl)
+    inp = synth.make_block_inputs(wl.B, wl.H, wl.W, D, Dm, wl.d, wl.seed)
+    x_host = torch.from_numpy(inp["x"])
+    x = x_host.to(dev)
+    wts = {k: (torch.from_numpy(np.ascontiguousarray(a)).to(dev).to(torch.bfloat16)
+               if k in synth.BLOCK_GEMM_WEIGHTS else torch.from_numpy(np.ascontiguousarray(a)).to(dev))
+           for k, a in inp["weights"].items()}
+    mem0 = torch.from_numpy(inp["mem0"]).to(dev)
+    wq, skip, lam = (torch.from_numpy(inp[k]).to(dev) for k in ("w_query", "skip", "dir_scale"))
+    out = torch.empty_like(x)
+    ws = torch.empty(vh.block_workspace_size(x, wts, wl.d), dtype=torch.uint8, device=dev)
+    flush = torch.empty(64 << 20, dtype=torch.float32, device=dev)
+    params = vh.ScanParams(eta_bias=wl.eta_bias, alpha_init=wl.alpha_init, impl=args.kernel)
+    stream = torch.cuda.Stream(device=dev)
+
+    def call():
+        vh.block_forward(x, mem0, wts, wl.d, params=params, w_query=wq, skip=skip,
+                         dir_scale=lam, out=out, workspace=ws, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            call()
+        torch.cuda.synchronize(dev)
+        events = [[torch.cuda.Event(enable_timing=True) for _ in range(2)]
+                  for _ in range(args.steps)]
+        sampler = ClockSampler(None).start() if rank == 0 else None
+        time.sleep(0.3 if sampler else 0.0)
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+        t0 = time.time()
+        for i in range(args.steps):
+            flush.zero_()
+            events[i][0].record(stream)
+            call()
+            events[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        t1 = time.time()
+        if world > 1:
+            torch.distributed.barrier()
+        if sampler:
+            time.sleep(0.3)
+            sampler.stop()
+    total_s, = max_over_ranks([sum(e[0].elapsed_time(e[1]) for e in events) / 1e3], device=dev)
+    avg_s = total_s / args.steps
+    value = job_throughput(wl.tokens, args.steps, world, total_s)
+    x_pin = x_host.pin_memory()
+    out_pin = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+    e2e_steps = max(3, min(args.steps, 20))
+    with torch.cuda.stream(stream):
+        def e2e_step():
+            x.copy_(x_pin, non_blocking=True)
+            call()
+            out_pin.copy_(out, non_blocking=True)
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ea.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        eb.record(stream)
+        torch.cuda.synchronize(dev)
+    e2e_s, = max_over_ranks([ea.elapsed_time(eb) / 1e3], device=dev)
+    e2e_value = job_throughput(wl.tokens, e2e_steps, world, e2e_s)
+    if rank == 0:
+        flops, gemm_flops = block_cost(wl)
+        peaks, src = load_peaks()
+        peak = float(peaks["bf16_tflops"])
+        achieved = flops / avg_s / 1e12
+        line = {
+            "metric": METRIC_BLOCK, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * avg_s,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "numerics": ("GEMMs bf16 x bf16 -> fp32 accumulate; fp32 residual stream; the "
+                         "operator as in the forward line"),
+            "data": "synthetic (random weights)", "config": workload_config(wl, args),
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
+                         "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                         "scope": "whole block call (GEMMs + operator)",
+                         "peak_source": f"bf16 dense burst, {'of measured' if src == 'measured' else 'of fallback'}",
+                         "flops_per_call": flops, "gemm_flops_per_call": gemm_flops},
+            "e2e": {"value": e2e_value, "unit": UNIT,
+                    "h2d_bytes_per_step": int(x_host.numel() * 4),
+                    "d2h_bytes_per_step": int(out.numel() * 4), "steps": e2e_steps},
+            # ours per call: CPE+LN1, gated depthwise, query projection, scan, positional
+            # depthwise, LN2, GELU (the four GEMMs are cuBLASLt's)
+            "gpu_launches": args.steps * 7,
+            "clocks": sampler.summary(t0, t1) if sampler else None,
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            v, dt, cores = time_block_oracle(wl, 1)
+            line["cpu_baseline"] = {
+                "value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                "sample": f"1 of {wl.B} images, fp64 block oracle, {dt:.1f} s wall"}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -613,8 +798,10 @@ def main(argv=None):
     ap.add_argument("--readout", choices=["memory", "outer"], default="memory",
                     help="memory: six-memory form (q from M^q); outer: VisionHOPE-exact "
                          "readout with an outer query projection and channel-wise skip")
-    ap.add_argument("--pass", dest="pass_", choices=["forward", "backward"], default="forward",
-                    help="forward: the scan (default); backward: its outer gradients")
+    ap.add_argument("--pass", dest="pass_", choices=["forward", "backward", "block"],
+                    default="forward",
+                    help="forward: the scan (default); backward: its outer gradients; "
+                         "block: the VisionHOPE block around the operator")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-images", type=int, default=16)
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -634,6 +821,8 @@ def main(argv=None):
         return run_reference(args, wl)
     if args.pass_ == "backward":
         return run_backward(args, wl)
+    if args.pass_ == "block":
+        return run_block(args, wl)
     return run_ours(args, wl)
 
 

@@ -125,26 +125,7 @@ def block_forward(x, w: BlockWeights, memories0, H: int, W: int, nh: int, d: int
     return out
 
 
-def random_weights(D: int, Dm: int, seed: int, hidden: int | None = None) -> BlockWeights:
-    """Synthetic parameters of the pages' shapes: GEMM weights ~ N(0, 1/fan_in) rounded to
-    bf16, depthwise kernels ~ N(0, 1/9) (times 0.5 for the branches), LN scale ~ 1 +
-    N(0, 0.1^2), biases ~ N(0, 0.02^2)."""
-    rng = np.random.default_rng(seed)
-    hidden = hidden or 4 * D
-
-    def lin(o, i):
-        return bf16(rng.standard_normal((o, i)) / np.sqrt(i))
-
-    def vec(n, s=0.02):
-        return rng.standard_normal(n) * s
-
-    return BlockWeights(
-        cpe_w=rng.standard_normal((D, 3, 3)) / 3.0, cpe_b=vec(D),
-        ln1_g=1.0 + vec(D, 0.1), ln1_b=vec(D),
-        w_in=lin(Dm, D), b_in=vec(Dm),
-        dw_w=rng.standard_normal((Dm, 3, 3)) / 6.0, dw_b=vec(Dm),
-        pos_w=rng.standard_normal((Dm, 3, 3)) / 6.0, pos_b=vec(Dm),
-        w_out=lin(D, Dm), b_out=vec(D),
-        ln2_g=1.0 + vec(D, 0.1), ln2_b=vec(D),
-        w_ff1=lin(hidden, D), b_ff1=vec(hidden),
-        w_ff2=lin(D, hidden), b_ff2=vec(D))
+def weights_from(arrays: dict, ln_eps: float = 1e-5) -> BlockWeights:
+    """BlockWeights (fp64) holding exactly the given arrays' values."""
+    return BlockWeights(**{k: np.asarray(v, dtype=np.float64) for k, v in arrays.items()},
+                        ln_eps=ln_eps)

@@ -39,23 +39,15 @@ pytestmark = pytest.mark.gpu
 def _make(seed, B, H, W, D, Dm, d):
     import torch
     from oracle import vh_block as vb
-    rng = np.random.default_rng(seed)
-    x = rng.standard_normal((B, H, W, D)).astype(np.float32)
-    wt = vb.random_weights(D, Dm, seed)
-    nh = Dm // d
-    mem0 = (rng.standard_normal((4, nh, 4 * d * d + 2 * d)) / np.sqrt(d)).astype(np.float32)
-    wq = (rng.standard_normal((Dm, Dm)) / np.sqrt(Dm)).astype(np.float32)
-    skip = rng.standard_normal((4, Dm)).astype(np.float32)
-    lam = rng.uniform(0.5, 1.5, (4, Dm)).astype(np.float32)
+    from visual_backbone_gb300 import synth
+    inp = synth.make_block_inputs(B, H, W, D, Dm, d, seed)
+    wt = vb.weights_from(inp["weights"])  # the oracle sees the values the GPU gets
     gpu = {}
-    for f in vb.BlockWeights.__dataclass_fields__:
-        if f == "ln_eps":
-            continue
-        a = getattr(wt, f).astype(np.float32)
-        setattr(wt, f, a.astype(np.float64))  # the oracle sees the values the GPU gets
+    for f, a in inp["weights"].items():
         t = torch.from_numpy(np.ascontiguousarray(a)).cuda()
-        gpu[f] = t.to(torch.bfloat16) if f in ("w_in", "w_out", "w_ff1", "w_ff2") else t
-    return x, wt, gpu, mem0, wq, skip, lam, nh
+        gpu[f] = t.to(torch.bfloat16) if f in synth.BLOCK_GEMM_WEIGHTS else t
+    return (inp["x"], wt, gpu, inp["mem0"], inp["w_query"], inp["skip"], inp["dir_scale"],
+            inp["nh"])
 
 
 def _gpu(vhlib, x, gpu, mem0, wq, skip, lam, d):

@@ -11,6 +11,7 @@ torch = pytest.importorskip("torch")
 scipy_signal = pytest.importorskip("scipy.signal")
 
 from oracle import vh_block as vb  # noqa: E402
+from visual_backbone_gb300 import synth  # noqa: E402
 
 
 def test_bf16_rounding_matches_torch_and_ties_to_even():
@@ -59,7 +60,7 @@ def test_gelu_and_silu():
 def _setup(orc, D, Dm, d, seed, H=5, W=6, B=1):
     rng = np.random.default_rng(seed)
     x = rng.standard_normal((B, H, W, D))
-    w = vb.random_weights(D, Dm, seed)
+    w = vb.weights_from(synth.make_block_weights(D, Dm, seed))
     nh = Dm // d
     mem0 = rng.standard_normal((4, nh, 4 * d * d + 2 * d)) / np.sqrt(d)
     p = orc.OracleParams(w_query=rng.standard_normal((Dm, Dm)) / np.sqrt(Dm),

@@ -104,3 +104,48 @@ def make_dir_scale(wl: Workload, seed: int = 1234) -> np.ndarray:
     """Channel-wise route scales lambda_r ~ U(0.5, 1.5), fp32 [4][Cc]."""
     rng = np.random.default_rng(seed)
     return rng.uniform(0.5, 1.5, size=(4, wl.Cc)).astype(np.float32)
+
+
+BLOCK_GEMM_WEIGHTS = ("w_in", "w_out", "w_ff1", "w_ff2")
+
+
+def make_block_weights(D: int, Dm: int, seed: int, hidden: int | None = None) -> dict:
+    """Synthetic parameters of one VisionHOPE block (fp32 numpy arrays; the four GEMM
+    weights hold bf16 values): GEMM weights ~ N(0, 1/fan_in), depthwise kernels
+    ~ N(0, 1/9) for CPE and N(0, 1/36) for the two branches, LN scales ~ 1 + N(0, 0.1^2),
+    biases ~ N(0, 0.02^2).  Shapes as in vh_block_weights, hidden = 4 D by default."""
+    rng = np.random.default_rng(seed)
+    hidden = hidden or 4 * D
+
+    def lin(o, i):
+        a = (rng.standard_normal((o, i)) / np.sqrt(i)).astype(np.float32)
+        return bf16_bits_to_f64(f32_to_bf16_bits(a)).astype(np.float32)
+
+    def vec(n, s=0.02):
+        return (rng.standard_normal(n) * s).astype(np.float32)
+
+    return dict(
+        cpe_w=(rng.standard_normal((D, 3, 3)) / 3.0).astype(np.float32), cpe_b=vec(D),
+        ln1_g=1.0 + vec(D, 0.1), ln1_b=vec(D),
+        w_in=lin(Dm, D), b_in=vec(Dm),
+        dw_w=(rng.standard_normal((Dm, 3, 3)) / 6.0).astype(np.float32), dw_b=vec(Dm),
+        pos_w=(rng.standard_normal((Dm, 3, 3)) / 6.0).astype(np.float32), pos_b=vec(Dm),
+        w_out=lin(D, Dm), b_out=vec(D),
+        ln2_g=1.0 + vec(D, 0.1), ln2_b=vec(D),
+        w_ff1=lin(hidden, D), b_ff1=vec(hidden),
+        w_ff2=lin(D, hidden), b_ff2=vec(D))
+
+
+def make_block_inputs(B: int, H: int, W: int, D: int, Dm: int, d: int, seed: int) -> dict:
+    """x [B][H][W][D] ~ N(0, 1) fp32, the block weights, and the operator's inputs:
+    memories0 ~ N(0, 1/d), the outer query W_q ~ N(0, 1/D_m), the skip ~ N(0, 1) and the
+    route scales lambda ~ U(0.5, 1.5) (all fp32)."""
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((B, H, W, D)).astype(np.float32)
+    nh = Dm // d
+    return dict(
+        x=x, weights=make_block_weights(D, Dm, seed),
+        mem0=(rng.standard_normal((4, nh, 4 * d * d + 2 * d)) / np.sqrt(d)).astype(np.float32),
+        w_query=(rng.standard_normal((Dm, Dm)) / np.sqrt(Dm)).astype(np.float32),
+        skip=rng.standard_normal((4, Dm)).astype(np.float32),
+        dir_scale=rng.uniform(0.5, 1.5, (4, Dm)).astype(np.float32), nh=nh)
