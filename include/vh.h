@@ -277,7 +277,8 @@ typedef struct {
  * impl, gate and step-control constants); the operator runs all four routes with
  * row/column-aligned chunks.  p->workspace must hold vh_block_workspace_size() bytes,
  * 16-byte aligned: the block's intermediates, the operator's query planes and the
- * GEMMs' scratch.  p->accumulate and p->memories_out must be 0 / NULL.
+ * GEMMs' scratch.  Activations between layers are bf16 (LN outputs, Z, Y, the FFN's
+ * hidden layer before and after GELU); the residual stream is fp32.  p->accumulate and p->memories_out must be 0 / NULL.
  *
  * The four pointwise layers run as cuBLASLt GEMMs (bf16 operands, fp32 accumulation,
  * bias and residual in the epilogue); the library keeps one cuBLASLt handle per device,

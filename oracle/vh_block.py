@@ -25,8 +25,9 @@ Readings where the pages leave a step open (kept in one place, see the module's 
   * the projections and both FFN layers have biases; GELU is the exact (erf) form.
 
 Precision points (the GPU path's, replicated here so the two compute the same function):
-the GEMM weights are bf16 values; LN1's output, Z, Y (before Proj_out), LN2's output and
-GELU's output are rounded to bf16 (round to nearest even); everything else is fp64 here.
+the GEMM weights are bf16 values; LN1's output, Z, Y (before Proj_out), LN2's output,
+FFN1's product (before its bias) and GELU's output are rounded to bf16 (round to nearest
+even); everything else is fp64 here.
 """
 from __future__ import annotations
 
@@ -118,7 +119,7 @@ def block_forward(x, w: BlockWeights, memories0, H: int, W: int, nh: int, d: int
     yb = bf16(y + dwconv3(z, w.pos_w, w.pos_b))
     x1 = x0 + yb @ w.w_out.T + w.b_out
     a2 = bf16(layer_norm(x1, w.ln2_g, w.ln2_b, w.ln_eps))
-    h = bf16(gelu(a2 @ w.w_ff1.T + w.b_ff1))
+    h = bf16(gelu(bf16(a2 @ w.w_ff1.T) + w.b_ff1))
     out = x1 + h @ w.w_ff2.T + w.b_ff2
     if return_parts:
         return out, dict(x0=x0, u=u, z=z, y=y, yb=yb, x1=x1, h=h)

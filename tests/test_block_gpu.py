@@ -2,8 +2,8 @@
 ("VisionHOPE: Visual Backbones as Self-Modifying Learning Systems", Sec. 2.3 Eq. (27),
 App. B.5), on the same seeded inputs and weights.
 
-Tolerance.  Both sides round the same five intermediates to bf16 (LN1 and LN2 outputs,
-Z, Y before Proj_out, GELU output).  An intermediate within fp32 noise of a rounding
+Tolerance.  Both sides round the same six intermediates to bf16 (LN1 and LN2 outputs,
+Z, Y before Proj_out, FFN1's product before its bias, GELU output).  An intermediate within fp32 noise of a rounding
 boundary lands one bf16 step (2^-8 of its value) apart; a step at LN2's output (|a| of
 a few units) moves every channel of that pixel through the FFN by up to a few 1e-3 of the
 output's rms.  Everywhere else the two agree to fp32 (about 1e-7 of the rms).  So the

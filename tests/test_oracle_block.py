@@ -80,7 +80,7 @@ def test_block_is_identity_without_branches(orc):
 
 def test_block_ffn_branch_matches_torch_layers(orc):
     """Operator branch off: out = X0 + FFN(LN2(X0)) with X0 = X + CPE(X), the FFN built
-    from torch.nn layers in fp64 (with the block's two bf16 rounding points)."""
+    from torch.nn layers in fp64 (with the block's three bf16 rounding points there)."""
     x, w, mem0, p, nh = _setup(orc, 8, 8, 4, 4)
     w.w_out[:] = 0; w.b_out[:] = 0
     out = vb.block_forward(x, w, mem0, 5, 6, nh, 4, p)
@@ -89,8 +89,8 @@ def test_block_ffn_branch_matches_torch_layers(orc):
     ln = torch.nn.functional.layer_norm(t, (8,), torch.from_numpy(w.ln2_g),
                                         torch.from_numpy(w.ln2_b), eps=1e-5)
     a2 = torch.from_numpy(vb.bf16(ln.numpy()))
-    h = torch.nn.functional.gelu(torch.nn.functional.linear(a2, torch.from_numpy(w.w_ff1),
-                                                            torch.from_numpy(w.b_ff1)))
+    pre = torch.nn.functional.linear(a2, torch.from_numpy(w.w_ff1))
+    h = torch.nn.functional.gelu(torch.from_numpy(vb.bf16(pre.numpy())) + torch.from_numpy(w.b_ff1))
     h = torch.from_numpy(vb.bf16(h.numpy()))
     ref = t + torch.nn.functional.linear(h, torch.from_numpy(w.w_ff2), torch.from_numpy(w.b_ff2))
     np.testing.assert_allclose(out, ref.numpy(), rtol=1e-12, atol=1e-12)

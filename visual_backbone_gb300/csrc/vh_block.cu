@@ -11,9 +11,10 @@
 //
 // The four pointwise layers are plain GEMMs on bf16 operands with fp32 accumulation
 // (cuBLASLt, bias and residual in its epilogue).  The kernels here do the rest, each one
-// pass over the activations: CPE + LN1 (one warp per pixel), the gated branch, the
-// positional branch with the cast for Proj_out, LN2, GELU.  bf16 rounding points: LN1's
-// and LN2's outputs, Z, Y before Proj_out, GELU's output.
+// pass over the activations: the three depthwise convolutions with their epilogues (CPE,
+// the gated branch, the positional branch with the cast for Proj_out), LN1 and LN2 (one
+// warp per pixel), GELU with FFN1's bias.  bf16 rounding points: LN1's and LN2's outputs,
+// Z, Y before Proj_out, FFN1's product (before its bias) and GELU's output.
 #include <cublasLt.h>
 
 #include <mutex>
@@ -23,63 +24,6 @@
 namespace vh {
 
 // ------------------------------------------------------------------ kernels
-
-// Per pixel (one warp): x0 = x + b + sum_{3x3} w x (depthwise, zero padding) and
-// a = bf16(LN(x0) * g + beta).  Channels c = lane + 32 m, m < MAXC.
-template <int MAXC>
-__global__ void __launch_bounds__(256) cpe_ln_kernel(const float *__restrict__ x,
-                                                     const float *__restrict__ cw,
-                                                     const float *__restrict__ cb,
-                                                     const float *__restrict__ g,
-                                                     const float *__restrict__ beta, float eps,
-                                                     float *__restrict__ x0,
-                                                     __nv_bfloat16 *__restrict__ a, int B, int H,
-                                                     int W, int D)
-{
-    const int lane = threadIdx.x & 31;
-    const long npix = (long)B * H * W;
-    for (long pix = (blockIdx.x * (long)blockDim.x + threadIdx.x) >> 5; pix < npix;
-         pix += ((long)gridDim.x * blockDim.x) >> 5) {
-        const int j = (int)(pix % W), i = (int)((pix / W) % H);
-        const long b = pix / ((long)H * W);
-        float v[MAXC];
-        float s = 0.0f;
-#pragma unroll
-        for (int m = 0; m < MAXC; ++m) {
-            const int c = lane + 32 * m;
-            v[m] = 0.0f;
-            if (c < D) {
-                float acc = cb[c] + x[pix * D + c];
-#pragma unroll
-                for (int di = -1; di <= 1; ++di) {
-                    const int ii = i + di;
-                    if (ii < 0 || ii >= H) continue;
-#pragma unroll
-                    for (int dj = -1; dj <= 1; ++dj) {
-                        const int jj = j + dj;
-                        if (jj < 0 || jj >= W) continue;
-                        acc = fmaf(cw[c * 9 + (di + 1) * 3 + (dj + 1)],
-                                   x[((b * H + ii) * W + jj) * D + c], acc);
-                    }
-                }
-                v[m] = acc;
-                x0[pix * D + c] = acc;
-                s += acc;
-            }
-        }
-        const float mu = warp_sum(s) / D;
-        float q = 0.0f;
-#pragma unroll
-        for (int m = 0; m < MAXC; ++m)
-            if (lane + 32 * m < D) q = fmaf(v[m] - mu, v[m] - mu, q);
-        const float rs = rsqrtf(warp_sum(q) / D + eps);
-#pragma unroll
-        for (int m = 0; m < MAXC; ++m) {
-            const int c = lane + 32 * m;
-            if (c < D) a[pix * D + c] = __float2bfloat16_rn((v[m] - mu) * rs * g[c] + beta[c]);
-        }
-    }
-}
 
 // Per pixel (one warp): a = bf16(LN(x) * g + beta).
 template <int MAXC>
@@ -113,76 +57,104 @@ __global__ void __launch_bounds__(256) ln_kernel(const float *__restrict__ x,
     }
 }
 
-// 3 x 3 depthwise cross-correlation with zero padding at element e (pixel, channel c)
-// of an NHWC tensor of type T with C channels.
-template <typename T>
-__device__ __forceinline__ float dw3(const T *__restrict__ src, const float *__restrict__ w,
-                                     long e, int c, int C, int H, int W)
+// The three 3 x 3 depthwise convolutions of the block (zero padding, bias per channel),
+// with their epilogues:
+//   kCpe:  out_f32  = src + b + dw(src)             conditional positional encoding
+//   kGate: out_bf16 = src + SiLU(b + dw(src))       gated depthwise residual branch
+//   kPos:  out_bf16 = res + b + dw(src), src bf16   positional branch, cast for Proj_out
+// One CTA per image row; the taps are staged transposed ([tap][channel]) in shared
+// memory, and a thread handles four consecutive channels of one pixel (16-byte loads).
+enum DwMode { kCpe = 0, kGate = 1, kPos = 2 };
+
+template <typename T> struct Vec4;
+template <> struct Vec4<float> {
+    static __device__ __forceinline__ float4 load(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+};
+template <> struct Vec4<__nv_bfloat16> {
+    static __device__ __forceinline__ float4 load(const __nv_bfloat16 *p)
+    {
+        const uint2 r = *reinterpret_cast<const uint2 *>(p);
+        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&r.x));
+        const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&r.y));
+        return make_float4(a.x, a.y, b.x, b.y);
+    }
+};
+
+template <int kMode, typename TIn>
+__global__ void __launch_bounds__(256) dw3_kernel(const TIn *__restrict__ src,
+                                                  const float *__restrict__ res,
+                                                  const float *__restrict__ w,
+                                                  const float *__restrict__ bias,
+                                                  void *__restrict__ out, int H, int W, int C)
 {
-    const long pix = e / C;
-    const int j = (int)(pix % W), i = (int)((pix / W) % H);
-    const long b = pix / ((long)H * W);
-    float acc = 0.0f;
+    extern __shared__ float sw[];  // [9][C] taps, then [C] bias
+    for (int e = threadIdx.x; e < 9 * C; e += blockDim.x) sw[(e % 9) * C + e / 9] = w[e];
+    for (int e = threadIdx.x; e < C; e += blockDim.x) sw[9 * C + e] = bias[e];
+    __syncthreads();
+    const int row = blockIdx.x;  // b * H + i
+    const int i = row % H;
+    const int C4 = C >> 2;
+    for (int t = threadIdx.x; t < W * C4; t += blockDim.x) {
+        const int j = t / C4, c = (t - j * C4) * 4;
+        float4 acc = *reinterpret_cast<const float4 *>(sw + 9 * C + c);
 #pragma unroll
-    for (int di = -1; di <= 1; ++di) {
-        const int ii = i + di;
-        if (ii < 0 || ii >= H) continue;
+        for (int di = -1; di <= 1; ++di) {
+            if (i + di < 0 || i + di >= H) continue;
 #pragma unroll
-        for (int dj = -1; dj <= 1; ++dj) {
-            const int jj = j + dj;
-            if (jj < 0 || jj >= W) continue;
-            acc = fmaf(w[c * 9 + (di + 1) * 3 + (dj + 1)],
-                       XElem<T>::to_f(src[((b * H + ii) * W + jj) * C + c]), acc);
+            for (int dj = -1; dj <= 1; ++dj) {
+                if (j + dj < 0 || j + dj >= W) continue;
+                const float4 v = Vec4<TIn>::load(src + ((size_t)(row + di) * W + j + dj) * C + c);
+                const float4 k = *reinterpret_cast<const float4 *>(sw + ((di + 1) * 3 + dj + 1) * C + c);
+                acc.x = fmaf(k.x, v.x, acc.x);
+                acc.y = fmaf(k.y, v.y, acc.y);
+                acc.z = fmaf(k.z, v.z, acc.z);
+                acc.w = fmaf(k.w, v.w, acc.w);
+            }
+        }
+        const size_t e = ((size_t)row * W + j) * C + c;
+        if (kMode == kCpe) {
+            const float4 x = Vec4<TIn>::load(src + e);
+            *reinterpret_cast<float4 *>(static_cast<float *>(out) + e) =
+                make_float4(x.x + acc.x, x.y + acc.y, x.z + acc.z, x.w + acc.w);
+        } else {
+            float4 r;
+            if (kMode == kGate) {
+                const float4 u = Vec4<TIn>::load(src + e);
+                r = make_float4(u.x + acc.x / (1.0f + __expf(-acc.x)),
+                                u.y + acc.y / (1.0f + __expf(-acc.y)),
+                                u.z + acc.z / (1.0f + __expf(-acc.z)),
+                                u.w + acc.w / (1.0f + __expf(-acc.w)));
+            } else {
+                const float4 y = *reinterpret_cast<const float4 *>(res + e);
+                r = make_float4(y.x + acc.x, y.y + acc.y, y.z + acc.z, y.w + acc.w);
+            }
+            __nv_bfloat162 *o = reinterpret_cast<__nv_bfloat162 *>(static_cast<__nv_bfloat16 *>(out) + e);
+            o[0] = __floats2bfloat162_rn(r.x, r.y);
+            o[1] = __floats2bfloat162_rn(r.z, r.w);
         }
     }
-    return acc;
 }
 
-// z = bf16(u + SiLU(dw(u) + b)): the gated depthwise residual branch.
-__global__ void __launch_bounds__(256) dwgate_kernel(const float *__restrict__ u,
-                                                     const float *__restrict__ w,
-                                                     const float *__restrict__ bias,
-                                                     __nv_bfloat16 *__restrict__ z, long total,
-                                                     int C, int H, int W)
+// h = bf16(GELU(h + b)) in place on the FFN's bf16 hidden layer [n][hidden],
+// GELU(a) = a (1 + erf(a / sqrt 2)) / 2; eight elements (16 bytes) per thread, 32-bit
+// indices (the launcher checks the element count).
+__global__ void __launch_bounds__(256) gelu_kernel(uint4 *__restrict__ h, const float *__restrict__ b,
+                                                   int n8, int hid8)
 {
-    for (long e = blockIdx.x * (long)blockDim.x + threadIdx.x; e < total;
-         e += (long)gridDim.x * blockDim.x) {
-        const int c = (int)(e % C);
-        const float a = dw3(u, w, e, c, C, H, W) + bias[c];
-        const float s = a / (1.0f + __expf(-a));
-        z[e] = __float2bfloat16_rn(u[e] + s);
-    }
-}
-
-// yb = bf16(y + dw(z) + b): the positional branch around the operator, cast for Proj_out.
-__global__ void __launch_bounds__(256) posdw_kernel(const float *__restrict__ y,
-                                                    const __nv_bfloat16 *__restrict__ z,
-                                                    const float *__restrict__ w,
-                                                    const float *__restrict__ bias,
-                                                    __nv_bfloat16 *__restrict__ yb, long total,
-                                                    int C, int H, int W)
-{
-    for (long e = blockIdx.x * (long)blockDim.x + threadIdx.x; e < total;
-         e += (long)gridDim.x * blockDim.x) {
-        const int c = (int)(e % C);
-        yb[e] = __float2bfloat16_rn(y[e] + dw3(z, w, e, c, C, H, W) + bias[c]);
-    }
-}
-
-// h = bf16(GELU(a)), GELU(a) = a (1 + erf(a / sqrt 2)) / 2, four elements per thread.
-__global__ void __launch_bounds__(256) gelu_kernel(const float4 *__restrict__ a,
-                                                   __nv_bfloat162 *__restrict__ h, long n4)
-{
-    for (long e = blockIdx.x * (long)blockDim.x + threadIdx.x; e < n4;
-         e += (long)gridDim.x * blockDim.x) {
-        const float4 v = a[e];
-        const float k = 0.70710678118654752f;
-        const float g0 = 0.5f * v.x * (1.0f + erff(v.x * k));
-        const float g1 = 0.5f * v.y * (1.0f + erff(v.y * k));
-        const float g2 = 0.5f * v.z * (1.0f + erff(v.z * k));
-        const float g3 = 0.5f * v.w * (1.0f + erff(v.w * k));
-        h[2 * e] = __floats2bfloat162_rn(g0, g1);
-        h[2 * e + 1] = __floats2bfloat162_rn(g2, g3);
+    const float k = 0.70710678118654752f;
+    for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < n8; e += gridDim.x * blockDim.x) {
+        uint4 r = h[e];
+        const float *bb = b + (e % hid8) * 8;
+        uint32_t *w = &r.x;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float2 v = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[q]));
+            const float a0 = v.x + bb[2 * q], a1 = v.y + bb[2 * q + 1];
+            const __nv_bfloat162 o = __floats2bfloat162_rn(0.5f * a0 * (1.0f + erff(a0 * k)),
+                                                           0.5f * a1 * (1.0f + erff(a1 * k)));
+            w[q] = *reinterpret_cast<const uint32_t *>(&o);
+        }
+        h[e] = r;
     }
 }
 
@@ -208,21 +180,22 @@ cublasStatus_t lt_handle(cublasLtHandle_t *h)
 
 }  // namespace
 
-// out[n][m] = act[n][k] . wt[m][k]^T + bias[m] (+ res[n][m]): row-major bf16 operands,
-// fp32 result, fp32 accumulation.  res may equal out.  Returns the cublasStatus_t.
+// out[n][m] = act[n][k] . wt[m][k]^T (+ bias[m]) (+ res[n][m]): row-major bf16 operands,
+// fp32 accumulation, an fp32 result (or bf16 with out_bf16, then without bias or res).
+// res may equal out.  Returns the cublasStatus_t.
 int block_gemm(int m, int n, int k, const __nv_bfloat16 *wt, const __nv_bfloat16 *act,
-               const float *bias, const float *res, float *out, void *ws, size_t ws_bytes,
-               cudaStream_t st)
+               const float *bias, const float *res, void *out, bool out_bf16, void *ws,
+               size_t ws_bytes, cudaStream_t st)
 {
     cublasLtHandle_t lt;
     cublasStatus_t s = lt_handle(&lt);
     if (s != CUBLAS_STATUS_SUCCESS) return (int)s;
     // column-major view: out^T (m x n) = wt (k x m)^T . act^T (k x n) [+ res^T]
     cublasLtMatmulDesc_t op = nullptr;
-    cublasLtMatrixLayout_t la = nullptr, lb = nullptr, lc = nullptr;
+    cublasLtMatrixLayout_t la = nullptr, lb = nullptr, lc = nullptr, ld = nullptr;
     cublasLtMatmulPreference_t pref = nullptr;
     const cublasOperation_t tA = CUBLAS_OP_T, tB = CUBLAS_OP_N;
-    const cublasLtEpilogue_t epi = CUBLASLT_EPILOGUE_BIAS;
+    const cublasLtEpilogue_t epi = bias ? CUBLASLT_EPILOGUE_BIAS : CUBLASLT_EPILOGUE_DEFAULT;
     const float alpha = 1.0f, beta = res ? 1.0f : 0.0f;
     cublasLtMatmulHeuristicResult_t hr{};
     int found = 0;
@@ -231,16 +204,18 @@ int block_gemm(int m, int n, int k, const __nv_bfloat16 *wt, const __nv_bfloat16
         if ((s = cublasLtMatmulDescSetAttribute(op, CUBLASLT_MATMUL_DESC_TRANSA, &tA, sizeof tA))) break;
         if ((s = cublasLtMatmulDescSetAttribute(op, CUBLASLT_MATMUL_DESC_TRANSB, &tB, sizeof tB))) break;
         if ((s = cublasLtMatmulDescSetAttribute(op, CUBLASLT_MATMUL_DESC_EPILOGUE, &epi, sizeof epi))) break;
-        if ((s = cublasLtMatmulDescSetAttribute(op, CUBLASLT_MATMUL_DESC_BIAS_POINTER, &bias, sizeof bias))) break;
+        if (bias && (s = cublasLtMatmulDescSetAttribute(op, CUBLASLT_MATMUL_DESC_BIAS_POINTER, &bias,
+                                                        sizeof bias))) break;
         if ((s = cublasLtMatrixLayoutCreate(&la, CUDA_R_16BF, k, m, k))) break;
         if ((s = cublasLtMatrixLayoutCreate(&lb, CUDA_R_16BF, k, n, k))) break;
-        if ((s = cublasLtMatrixLayoutCreate(&lc, CUDA_R_32F, m, n, m))) break;
+        if ((s = cublasLtMatrixLayoutCreate(&lc, out_bf16 ? CUDA_R_16BF : CUDA_R_32F, m, n, m))) break;
+        ld = lc;
         if ((s = cublasLtMatmulPreferenceCreate(&pref))) break;
         if ((s = cublasLtMatmulPreferenceSetAttribute(pref, CUBLASLT_MATMUL_PREF_MAX_WORKSPACE_BYTES,
                                                       &ws_bytes, sizeof ws_bytes))) break;
-        if ((s = cublasLtMatmulAlgoGetHeuristic(lt, op, la, lb, lc, lc, pref, 1, &hr, &found))) break;
+        if ((s = cublasLtMatmulAlgoGetHeuristic(lt, op, la, lb, lc, ld, pref, 1, &hr, &found))) break;
         if (!found) { s = CUBLAS_STATUS_NOT_SUPPORTED; break; }
-        s = cublasLtMatmul(lt, op, &alpha, wt, la, act, lb, &beta, res ? res : out, lc, out, lc,
+        s = cublasLtMatmul(lt, op, &alpha, wt, la, act, lb, &beta, res ? res : out, lc, out, ld,
                            &hr.algo, ws, ws_bytes, st);
     } while (0);
     if (pref) cublasLtMatmulPreferenceDestroy(pref);
@@ -253,6 +228,9 @@ int block_gemm(int m, int n, int k, const __nv_bfloat16 *wt, const __nv_bfloat16
 
 // ------------------------------------------------------------------ launches
 
+cudaError_t launch_ln(const float *x, const float *g, const float *beta, float eps,
+                      __nv_bfloat16 *a, long npix, int D, cudaStream_t st);
+
 namespace {
 
 unsigned grid_for(long threads)
@@ -264,17 +242,16 @@ unsigned grid_for(long threads)
 
 }  // namespace
 
+// CPE (x0 = x + dw(x) + b, fp32) then LN1 (bf16), two bandwidth-bound passes.
 cudaError_t launch_cpe_ln(const float *x, const float *cw, const float *cb, const float *g,
                           const float *beta, float eps, float *x0, __nv_bfloat16 *a, int B, int H,
                           int W, int D, cudaStream_t st)
 {
-    const long npix = (long)B * H * W;
-    const unsigned grid = grid_for(npix * 32);
-    if (D <= 256)
-        cpe_ln_kernel<8><<<grid, 256, 0, st>>>(x, cw, cb, g, beta, eps, x0, a, B, H, W, D);
-    else
-        cpe_ln_kernel<32><<<grid, 256, 0, st>>>(x, cw, cb, g, beta, eps, x0, a, B, H, W, D);
-    return cudaGetLastError();
+    const size_t sm = (size_t)10 * D * sizeof(float);
+    dw3_kernel<kCpe, float><<<B * H, 256, sm, st>>>(x, nullptr, cw, cb, x0, H, W, D);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_ln(x0, g, beta, eps, a, (long)B * H * W, D, st);
 }
 
 cudaError_t launch_ln(const float *x, const float *g, const float *beta, float eps,
@@ -291,24 +268,26 @@ cudaError_t launch_ln(const float *x, const float *g, const float *beta, float e
 cudaError_t launch_dwgate(const float *u, const float *w, const float *b, __nv_bfloat16 *z,
                           long npix, int C, int H, int W, cudaStream_t st)
 {
-    const long total = npix * C;
-    dwgate_kernel<<<grid_for(total), 256, 0, st>>>(u, w, b, z, total, C, H, W);
+    const int rows = (int)(npix / W);
+    dw3_kernel<kGate, float><<<rows, 256, (size_t)10 * C * sizeof(float), st>>>(u, nullptr, w, b, z,
+                                                                              H, W, C);
     return cudaGetLastError();
 }
 
 cudaError_t launch_posdw(const float *y, const __nv_bfloat16 *z, const float *w, const float *b,
                          __nv_bfloat16 *yb, long npix, int C, int H, int W, cudaStream_t st)
 {
-    const long total = npix * C;
-    posdw_kernel<<<grid_for(total), 256, 0, st>>>(y, z, w, b, yb, total, C, H, W);
+    const int rows = (int)(npix / W);
+    dw3_kernel<kPos, __nv_bfloat16><<<rows, 256, (size_t)10 * C * sizeof(float), st>>>(
+        z, y, w, b, yb, H, W, C);
     return cudaGetLastError();
 }
 
-cudaError_t launch_gelu(const float *a, __nv_bfloat16 *h, long n, cudaStream_t st)
+cudaError_t launch_gelu(__nv_bfloat16 *h, const float *b, long n, int hidden, cudaStream_t st)
 {
-    const long n4 = n / 4;
-    gelu_kernel<<<grid_for(n4), 256, 0, st>>>(reinterpret_cast<const float4 *>(a),
-                                              reinterpret_cast<__nv_bfloat162 *>(h), n4);
+    const long n8 = n / 8;
+    if (n8 > 0x7fe00000L) return cudaErrorInvalidValue;  // int index plus one grid stride
+    gelu_kernel<<<grid_for(n8), 256, 0, st>>>(reinterpret_cast<uint4 *>(h), b, (int)n8, hidden / 8);
     return cudaGetLastError();
 }
 
