@@ -47,7 +47,7 @@ struct BwdCfg {
     static constexpr int NT = 256;
     static constexpr int NW = NT / 32;
     static constexpr int R = 4 * D + 2;     // rows of the state
-    static constexpr int SS = D + 1;        // padded row stride
+    static constexpr int SS = D + 4;        // row stride: 16-byte rows, no two rows in a bank quad
     static constexpr int T = D == 16 ? 64 : 16;   // token tile
     static constexpr int MINB = D == 64 ? 1 : 3;  // resident CTAs per SM (one wave at stage 1)
     static constexpr int JB = 4;                  // tokens per register block (generation)
@@ -191,11 +191,17 @@ __global__ void __launch_bounds__(256, BwdCfg<D>::MINB) scan_bwd_kernel(const Bw
                     float acc[C::JB];
 #pragma unroll
                     for (int jj = 0; jj < C::JB; ++jj) acc[jj] = 0.0f;
-#pragma unroll 8
-                    for (int i = 0; i < D; ++i) {
-                        const float sv = srow[i];
+#pragma unroll 2
+                    for (int i = 0; i < D; i += 4) {
+                        const float4 sv = *reinterpret_cast<const float4 *>(srow + i);
 #pragma unroll
-                        for (int jj = 0; jj < C::JB; ++jj) acc[jj] = fmaf(sv, X[(j0 + jj) * D + i], acc[jj]);
+                        for (int jj = 0; jj < C::JB; ++jj) {
+                            const float4 xv = *reinterpret_cast<const float4 *>(X + (j0 + jj) * D + i);
+                            acc[jj] = fmaf(sv.x, xv.x, acc[jj]);
+                            acc[jj] = fmaf(sv.y, xv.y, acc[jj]);
+                            acc[jj] = fmaf(sv.z, xv.z, acc[jj]);
+                            acc[jj] = fmaf(sv.w, xv.w, acc[jj]);
+                        }
                     }
 #pragma unroll
                     for (int jj = 0; jj < C::JB; ++jj)
@@ -314,6 +320,48 @@ __global__ void __launch_bounds__(256, BwdCfg<D>::MINB) scan_bwd_kernel(const Bw
         }
     };
 
+    // Row transform M[o][:] <- sum_l M[o][l] GT[l][:] of the R rows of M (stride SS), in
+    // place, one warp per row; for d <= 32 each lane keeps its column of GT in registers.
+    auto rows_times = [&](float *M) {
+        if constexpr (D <= 32) {
+            float gcol[D];
+#pragma unroll
+            for (int l = 0; l < D; ++l) gcol[l] = lane < D ? GT[l * D + lane] : 0.0f;
+            for (int o = warp; o < C::R; o += C::NW) {
+                const float *mrow = M + o * C::SS;
+                float acc = 0.0f;
+#pragma unroll
+                for (int l = 0; l < D; l += 4) {
+                    const float4 m4 = *reinterpret_cast<const float4 *>(mrow + l);
+                    acc = fmaf(m4.x, gcol[l], acc);
+                    acc = fmaf(m4.y, gcol[l + 1], acc);
+                    acc = fmaf(m4.z, gcol[l + 2], acc);
+                    acc = fmaf(m4.w, gcol[l + 3], acc);
+                }
+                __syncwarp();
+                if (lane < D) M[o * C::SS + lane] = acc;
+                __syncwarp();
+            }
+        } else {
+            for (int o = warp; o < C::R; o += C::NW) {
+                const float *mrow = M + o * C::SS;
+                float acc[C::CPL];
+#pragma unroll
+                for (int m = 0; m < C::CPL; ++m) acc[m] = 0.0f;
+#pragma unroll 8
+                for (int l = 0; l < D; ++l) {
+                    const float s = mrow[l];
+#pragma unroll
+                    for (int m = 0; m < C::CPL; ++m) acc[m] = fmaf(s, GT[l * D + lane + 32 * m], acc[m]);
+                }
+                __syncwarp();
+#pragma unroll
+                for (int m = 0; m < C::CPL; ++m) M[o * C::SS + lane + 32 * m] = acc[m];
+                __syncwarp();
+            }
+        }
+    };
+
     // ---- pass 1: forward, checkpointing each chunk's boundary state (skipped when the
     // tensor-core forward has written them)
     for (int c = 0; c < (ba.have_ckpt ? 0 : nchunks); ++c) {
@@ -330,28 +378,7 @@ __global__ void __launch_bounds__(256, BwdCfg<D>::MINB) scan_bwd_kernel(const Bw
 #pragma unroll
         for (int q = 0; q < C::CPT; ++q) GT[grow * D + gc0 + q] = G[q];
         __syncthreads();
-        for (int o = warp; o < C::R; o += C::NW) {
-            const float *srow = S + o * C::SS;
-            float acc[C::CPL];
-#pragma unroll
-            for (int m = 0; m < C::CPL; ++m) acc[m] = 0.0f;
-#pragma unroll 8
-            for (int l = 0; l < D; ++l) {
-                const float s = srow[l];
-#pragma unroll
-                for (int m = 0; m < C::CPL; ++m) {
-                    const int i = lane + 32 * m;
-                    if (i < D) acc[m] = fmaf(s, GT[l * D + i], acc[m]);
-                }
-            }
-            __syncwarp();
-#pragma unroll
-            for (int m = 0; m < C::CPL; ++m) {
-                const int i = lane + 32 * m;
-                if (i < D) S[o * C::SS + i] = acc[m];
-            }
-            __syncwarp();
-        }
+        rows_times(S);  // GT holds G: S <- S G
     }
 
     // ---- pass 2: reverse
@@ -378,32 +405,23 @@ __global__ void __launch_bounds__(256, BwdCfg<D>::MINB) scan_bwd_kernel(const Bw
         for (int q = 0; q < C::CPT; ++q) Pg[q] = 0.0f;
         for (int o = 0; o < C::R; ++o) {
             const float sv = S[o * C::SS + grow];
+            const float *dr = dS + o * C::SS + gc0;
+            if constexpr (C::CPT % 4 == 0) {
 #pragma unroll
-            for (int q = 0; q < C::CPT; ++q) Pg[q] = fmaf(sv, dS[o * C::SS + gc0 + q], Pg[q]);
+                for (int q = 0; q < C::CPT; q += 4) {
+                    const float4 d4 = *reinterpret_cast<const float4 *>(dr + q);
+                    Pg[q] = fmaf(sv, d4.x, Pg[q]);
+                    Pg[q + 1] = fmaf(sv, d4.y, Pg[q + 1]);
+                    Pg[q + 2] = fmaf(sv, d4.z, Pg[q + 2]);
+                    Pg[q + 3] = fmaf(sv, d4.w, Pg[q + 3]);
+                }
+            } else {
+#pragma unroll
+                for (int q = 0; q < C::CPT; ++q) Pg[q] = fmaf(sv, dr[q], Pg[q]);
+            }
         }
         __syncthreads();
-        for (int o = warp; o < C::R; o += C::NW) {
-            const float *drow = dS + o * C::SS;
-            float acc[C::CPL];
-#pragma unroll
-            for (int m = 0; m < C::CPL; ++m) acc[m] = 0.0f;
-#pragma unroll 8
-            for (int i = 0; i < D; ++i) {
-                const float s = drow[i];
-#pragma unroll
-                for (int m = 0; m < C::CPL; ++m) {
-                    const int jj = lane + 32 * m;
-                    if (jj < D) acc[m] = fmaf(s, GT[i * D + jj], acc[m]);
-                }
-            }
-            __syncwarp();
-#pragma unroll
-            for (int m = 0; m < C::CPL; ++m) {
-                const int jj = lane + 32 * m;
-                if (jj < D) dS[o * C::SS + jj] = acc[m];
-            }
-            __syncwarp();
-        }
+        rows_times(dS);  // GT holds G^T: dS <- dS G^T
         // c-e. tiles, last first
         const int ntiles = (L + C::T - 1) / C::T;
         for (int ti = ntiles - 1; ti >= 0; --ti) {
@@ -509,8 +527,14 @@ __global__ void __launch_bounds__(256, BwdCfg<D>::MINB) scan_bwd_kernel(const Bw
                     const int c = lane + 32 * m;
                     float acc = 0.0f;
                     if (c < D) {
-#pragma unroll 8
-                        for (int i = 0; i < D; ++i) acc = fmaf(S[(3 * D + i) * C::SS + c], wv[i], acc);
+#pragma unroll 2
+                        for (int i = 0; i < D; i += 4) {
+                            const float4 w4 = *reinterpret_cast<const float4 *>(wv + i);
+                            acc = fmaf(S[(3 * D + i) * C::SS + c], w4.x, acc);
+                            acc = fmaf(S[(3 * D + i + 1) * C::SS + c], w4.y, acc);
+                            acc = fmaf(S[(3 * D + i + 2) * C::SS + c], w4.z, acc);
+                            acc = fmaf(S[(3 * D + i + 3) * C::SS + c], w4.w, acc);
+                        }
                     }
                     dq[m] = acc;
                 }
@@ -592,11 +616,20 @@ __global__ void __launch_bounds__(256, BwdCfg<D>::MINB) scan_bwd_kernel(const Bw
                     const int c = lane + 32 * m;
                     if (c < D) {
                         float acc = fmaf(S[(4 * D) * C::SS + c], dse, S[(4 * D + 1) * C::SS + c] * dsa);
-#pragma unroll 4
-                        for (int i = 0; i < D; ++i) {
-                            acc = fmaf(S[i * C::SS + c], wv[D + i], acc);
-                            acc = fmaf(S[(D + i) * C::SS + c], wv[2 * D + i], acc);
-                            acc = fmaf(S[(2 * D + i) * C::SS + c], wv[3 * D + i], acc);
+#pragma unroll 2
+                        for (int i = 0; i < D; i += 4) {
+                            const float4 wk = *reinterpret_cast<const float4 *>(wv + D + i);
+                            const float4 wvv = *reinterpret_cast<const float4 *>(wv + 2 * D + i);
+                            const float4 wq = *reinterpret_cast<const float4 *>(wv + 3 * D + i);
+                            const float wka[4] = {wk.x, wk.y, wk.z, wk.w};
+                            const float wva[4] = {wvv.x, wvv.y, wvv.z, wvv.w};
+                            const float wqa[4] = {wq.x, wq.y, wq.z, wq.w};
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                acc = fmaf(S[(i + u) * C::SS + c], wka[u], acc);
+                                acc = fmaf(S[(D + i + u) * C::SS + c], wva[u], acc);
+                                acc = fmaf(S[(2 * D + i + u) * C::SS + c], wqa[u], acc);
+                            }
                         }
                         atomicAdd(dxb + (size_t)pix * Cc + c, acc);
                     }
