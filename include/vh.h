@@ -290,6 +290,26 @@ vh_status vh_block_forward(const float *x, const float *memories0, const vh_para
 /* Bytes of workspace vh_block_forward needs; 0 for invalid arguments. */
 size_t vh_block_workspace_size(const vh_params *p, const vh_block_weights *w, int H, int W);
 
+/*
+ * vh_scan_forward_static -- vh_scan_forward with the outer-query readout (p->w_query set)
+ * for callers that cannot allocate device memory.  The paper has no counterpart: this is
+ * a packaging of the same computation.  Some callers can't call cudaMalloc or keep a
+ * workspace of their own -- a plug-in inside a host application that owns every device
+ * allocation, for instance -- yet the outer-query readout needs scratch for its query
+ * planes.  Here that scratch is a 16 MiB array compiled into the library (every GPU that
+ * loads the library holds it until the process exits), so B*H*W*channels may be at most
+ * 2,796,202 (6 bytes per element); larger calls return VH_ERR_WORKSPACE.  p->workspace
+ * and p->workspace_bytes are ignored; everything else is as in vh_scan_forward, whose
+ * kernels run.  The first call on a device looks up the array's device address there
+ * (make that first call before any stream capture).  Every call uses the same array and
+ * rewrites it completely before reading it, so nothing needs clearing, but two calls
+ * that overlap on the GPU (different streams, or another thread) race on it and corrupt
+ * each other's queries: serialise them.  Without w_query it returns VH_ERR_INVALID_ARG
+ * (vh_scan_forward needs no scratch then).
+ */
+vh_status vh_scan_forward_static(const void *x, const float *memories0, const vh_params *p,
+                                 int H, int W, unsigned dirs, int chunk, float *out);
+
 /* Static string for a status code. */
 const char *vh_status_string(vh_status s);
 

@@ -164,6 +164,19 @@ BlockLayout block_layout(const vh_params *p, const vh_block_weights *w, int H, i
 
 }  // namespace
 
+namespace vh {
+// Record a failure from another translation unit of the library (same thread-local text
+// as the entry points here).
+vh_status record_error(vh_status s, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return s;
+}
+}  // namespace vh
+
 extern "C" {
 
 void vh_params_init(vh_params *p)
