@@ -102,19 +102,24 @@ def test_backward_is_linear_in_dout(vhlib):
         assert parity_err(c[i], ref) < 1e-4
 
 
-@pytest.mark.parametrize("variant", ["plain", "longmem"])
-def test_backward_stage1_sampled(orc, vhlib, variant):
-    """The stage-1 batch (32 x 56 x 56, 3 heads of 32) in the launch the backward bench
-    times; dx of the first and last image against the oracle, and dmemories0 of a
+SAMPLED = [("stage1", "plain"), ("stage1", "longmem"), ("stage2", "plain"),
+           ("stage3", "plain"), ("highres", "plain")]
+
+
+@pytest.mark.parametrize("config,variant", SAMPLED, ids=[f"{c}-{v}" for c, v in SAMPLED])
+def test_backward_sampled(orc, vhlib, config, variant):
+    """A whole batch of the configuration in the launch the backward bench times; dx of
+    the first (and, for stage-1, the last) image against the oracle, and dmemories0 of a
     one-image call against the oracle on that image."""
-    wl = synth.WORKLOADS["stage1"]
+    wl = synth.WORKLOADS[config]
     if variant == "longmem":
         wl = wl.long_memory()
     inp = synth.make_inputs(wl)
     vhp = vhlib.ScanParams(eta_bias=wl.eta_bias, alpha_init=wl.alpha_init)
     dout = _dout(wl, wl.B, 300)
     gx, _ = _run(vhlib, inp, vhp, dout)
-    for b in ((0, wl.B - 1) if variant == "plain" else (0,)):
+    images = (0, wl.B - 1) if (config, variant) == ("stage1", "plain") else (0,)
+    for b in images:
         sub = copy.copy(inp)
         sub.x64 = inp.x64[b:b + 1]
         ox, om = _oracle(orc, vhlib, sub, vhp, dout[b:b + 1])
