@@ -29,7 +29,7 @@ struct SimtCfg {
     static constexpr int R = 4 * D + 2;    // rows of the state: k, v, q, m (d each), eta, alpha
     static constexpr int RG = 3 * D + 2;   // rows used by the generation: k, v, q, eta, alpha
     static constexpr int SS = D + 1;       // padded row stride of the state (bank-conflict free)
-    static constexpr int T = (D == 64) ? 32 : 64;  // token tile
+    static constexpr int T = (D == 64) ? 16 : 64;  // token tile (d = 64: two CTAs per SM)
     static constexpr int PS = RG + 1;      // row stride of the generation outputs
     static constexpr int TPR = NT / D;     // threads per gain row
     static constexpr int CPT = D / TPR;    // gain columns per thread
@@ -46,7 +46,8 @@ struct SimtCfg {
     static constexpr int FLOATS = OFF_PIX + T;
     static constexpr size_t BYTES = (size_t)FLOATS * 4;
     static_assert(T % JB == 0, "tile must hold whole register blocks");
-    static_assert(D * D <= T * PS, "gain must fit in the generation buffer it reuses");
+    static_assert(D * D <= T * PS + T * D && OFF_K == OFF_P + T * PS,
+                  "gain must fit in the generation and key buffers it reuses");
     static_assert(TPR * CPT == D && TPR <= 32, "gain thread map");
 };
 
@@ -271,7 +272,9 @@ __global__ void __launch_bounds__(256) scan_simt_kernel(const ScanArgs a)
             }
         }
 
-        // 6. chunk end: every memory becomes M_b G
+        // 6. chunk end: every memory becomes M_b G (G in the generation buffer and, for
+        // d = 64, the key buffer after it, which the gain loop reads until its last token)
+        if constexpr (D * D > C::T * C::PS) __syncthreads();
         float *Gs = P;
 #pragma unroll
         for (int c = 0; c < C::CPT; ++c) Gs[grow * D + gc0 + c] = G[c];
