@@ -37,9 +37,12 @@ METRIC_BWD = ("4-dir VisionHOPE scan backward (dx, dmemories0) tokens/s on 1 GB3
               "56×56×96; % of roofline")
 UNIT = "tokens/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-KERNEL_SOURCES = ["visual_backbone_gb300/csrc/vh_scan_simt.cu",
-                  "visual_backbone_gb300/csrc/vh_scan_tc.cu",
-                  "visual_backbone_gb300/csrc/vh_common.cuh"]
+# the sources of each kernel whose DRAM traffic profiles/traffic.txt records
+KERNEL_SOURCES_TC = ["visual_backbone_gb300/csrc/vh_scan_tc.cu",
+                     "visual_backbone_gb300/csrc/vh_tc_ptx.cuh",
+                     "visual_backbone_gb300/csrc/vh_common.cuh"]
+KERNEL_SOURCES_SIMT = ["visual_backbone_gb300/csrc/vh_scan_simt.cu",
+                       "visual_backbone_gb300/csrc/vh_common.cuh"]
 KERNEL_SOURCES_BWD = ["visual_backbone_gb300/csrc/vh_scan_bwd.cu",
                       "visual_backbone_gb300/csrc/vh_common.cuh"]
 FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12   # SMs x fp32 lanes x 2 flops x max clock
@@ -106,15 +109,22 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash(sources=None):
+def forward_sources(wl, kernel: str):
+    """Sources of the scan kernel a forward call runs: the tensor-core kernel for d = 32,
+    bf16, aligned chunks (unless the CUDA-core kernel is forced), else the CUDA-core one."""
+    tc = wl.d == 32 and wl.dtype == "bf16" and wl.chunk == 0 and wl.Cc % 8 == 0
+    return KERNEL_SOURCES_TC if tc and kernel != "simt" else KERNEL_SOURCES_SIMT
+
+
+def kernel_source_hash(sources):
     h = hashlib.sha256()
-    for rel in sources or KERNEL_SOURCES:
+    for rel in sources:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:12]
 
 
-def recorded_traffic(workload: str, impl: str, sources=None):
+def recorded_traffic(workload: str, impl: str, sources):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on
     the current kernel sources (profiles/traffic.txt: workload impl hash bytes)."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
@@ -486,7 +496,7 @@ def run_ours(args, wl):
         peaks, src = load_peaks()
         achieved = flops / kern_avg_s / 1e12
         peak = float(peaks["bf16_tflops"])
-        traffic = recorded_traffic(wl.name, args.kernel)
+        traffic = recorded_traffic(wl.name, args.kernel, forward_sources(wl, args.kernel))
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": traffic,
                 "peak_source": f"bf16 dense burst, {'of measured' if src == 'measured' else 'of fallback'}",
