@@ -64,6 +64,12 @@ CASES = [
      True),
     ("longmem", synth.Workload("b11", 1, 8, 8, 1, 32, 0, "bf16", seed=61, alpha_init=0.999),
      15, 0, {}, False, True),
+    ("one_row", synth.Workload("b13", 2, 1, 17, 1, 32, 0, "bf16", seed=63), 15, 0, {}, False,
+     False),
+    ("one_column", synth.Workload("b14", 1, 17, 1, 2, 32, 0, "bf16", seed=64), 15, 0, {}, False,
+     True),
+    ("single_pixel", synth.Workload("b15", 1, 1, 1, 1, 16, 0, "f32", seed=65), 15, 0, {}, False,
+     True),
 ]
 
 

@@ -77,6 +77,8 @@ CASES = [
     ("6x5_D32_Dm16_d16", 3, 1, 6, 5, 32, 16, 16),
     ("8x8_D128_Dm64_d16", 4, 1, 8, 8, 128, 64, 16),
     ("3x70_D64_Dm32_d32", 5, 1, 3, 70, 64, 32, 32),
+    ("1x9_D32_Dm16_d16", 6, 2, 1, 9, 32, 16, 16),     # one-row map: the depthwise edges
+    ("9x1_D64_Dm32_d32", 8, 1, 9, 1, 64, 32, 32),     # one-column map
 ]
 
 

@@ -97,6 +97,7 @@ def test_direction_subsets(orc, vhlib, impl, dirs):
     (1, 40, 3, 2, 64, "f32", 0, 0.9, 2.0),        # d = 64, columns of 40
     (1, 6, 6, 3, 16, "bf16", 4, 0.999, 0.0),      # d = 16, bf16
     (3, 1, 17, 1, 32, "bf16", 0, 0.999, 0.0),     # one-row map
+    (2, 17, 1, 2, 32, "bf16", 0, 0.999, 0.0),     # one-column map
     (1, 1, 1, 1, 16, "f32", 0, 0.9, 0.0),         # single pixel
 ])
 def test_small_shapes(orc, vhlib, impl, case):
