@@ -279,26 +279,42 @@ __global__ void __launch_bounds__(256) scan_simt_kernel(const ScanArgs a)
 #pragma unroll
         for (int c = 0; c < C::CPT; ++c) Gs[grow * D + gc0 + c] = G[c];
         __syncthreads();
-        for (int o = warp; o < C::R; o += C::NW) {
-            if (frozen_row(a, o, D)) continue;  // ablation: memory fixed within the image
-            const float *srow = S + o * C::SS;
-            float acc[C::CPL];
+        // four state rows per warp and pass: each loaded column entry of G serves four rows
+        constexpr int RB = 4;
+        for (int o0 = warp * RB; o0 < C::R; o0 += C::NW * RB) {
+            float acc[RB][C::CPL];
 #pragma unroll
-            for (int m = 0; m < C::CPL; ++m) acc[m] = 0.0f;
-#pragma unroll 8
+            for (int rr = 0; rr < RB; ++rr)
+#pragma unroll
+                for (int m = 0; m < C::CPL; ++m) acc[rr][m] = 0.0f;
+            const int nr = min(RB, C::R - o0);
+#pragma unroll 4
             for (int l = 0; l < D; ++l) {
-                const float s = srow[l];
+                float gl[C::CPL];
 #pragma unroll
                 for (int m = 0; m < C::CPL; ++m) {
                     const int i = lane + 32 * m;
-                    if (i < D) acc[m] = fmaf(s, Gs[l * D + i], acc[m]);
+                    gl[m] = i < D ? Gs[l * D + i] : 0.0f;
+                }
+#pragma unroll
+                for (int rr = 0; rr < RB; ++rr) {
+                    if (rr < nr) {
+                        const float sv = S[(o0 + rr) * C::SS + l];
+#pragma unroll
+                        for (int m = 0; m < C::CPL; ++m) acc[rr][m] = fmaf(sv, gl[m], acc[rr][m]);
+                    }
                 }
             }
             __syncwarp();
 #pragma unroll
-            for (int m = 0; m < C::CPL; ++m) {
-                const int i = lane + 32 * m;
-                if (i < D) S[o * C::SS + i] = acc[m];
+            for (int rr = 0; rr < RB; ++rr) {
+                // a memory held fixed by an ablation switch keeps its boundary value
+                if (rr >= nr || frozen_row(a, o0 + rr, D)) continue;
+#pragma unroll
+                for (int m = 0; m < C::CPL; ++m) {
+                    const int i = lane + 32 * m;
+                    if (i < D) S[(o0 + rr) * C::SS + i] = acc[rr][m];
+                }
             }
             __syncwarp();
         }
