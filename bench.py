@@ -227,6 +227,47 @@ def job_throughput(tokens_per_rank_step, steps, world, seconds):
 
 # --------------------------------------------------------- oracle timing
 
+def pipelined_e2e(dev, steps, upload, compute, download):
+    """Seconds for `steps` end-to-end steps, each with its own host->device upload, call
+    and device->host readback, double-buffered: the upload, the call and the readback run
+    on three streams, ordered by events, so the copies of one step overlap the calls of
+    its neighbours.  upload(i, slot, stream) / compute(slot, stream) /
+    download(slot, stream) enqueue the work of step i on buffer slot i % 2."""
+    import torch
+    s_up, s_run, s_down = (torch.cuda.Stream(device=dev) for _ in range(3))
+    up = [torch.cuda.Event() for _ in range(2)]
+    ran = [torch.cuda.Event() for _ in range(2)]
+    down = [torch.cuda.Event() for _ in range(2)]
+
+    def step(i):
+        k = i % 2
+        if i >= 2:
+            s_up.wait_event(ran[k])       # the call of step i - 2 has read slot k's input
+        upload(i, k, s_up)
+        up[k].record(s_up)
+        s_run.wait_event(up[k])
+        if i >= 2:
+            s_run.wait_event(down[k])     # step i - 2's result in slot k has been read back
+        compute(k, s_run)
+        ran[k].record(s_run)
+        s_down.wait_event(ran[k])
+        download(k, s_down)
+        down[k].record(s_down)
+
+    for i in range(2):                    # warm the path
+        step(i)
+    torch.cuda.synchronize(dev)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(s_up)
+    for i in range(steps):
+        step(i)
+    s_up.wait_stream(s_down)
+    t1.record(s_up)
+    torch.cuda.synchronize(dev)
+    return t0.elapsed_time(t1) / 1e3
+
+
 def time_oracle(wl, images, nthreads, min_seconds=0.0, max_passes=1000, w_query=None, skip=None):
     """Tokens/s of the oracle over `images` images, repeated until `min_seconds`
     of wall time have passed; returns (tokens/s, seconds, passes).  w_query / skip
@@ -469,26 +510,27 @@ def run_ours(args, wl):
     total_s, kern_avg_s = max_over_ranks([total_s, kern_avg_s], device=dev)
     value = job_throughput(wl.tokens, args.steps, world, total_s)
 
-    # end to end through the public API with host buffers (pinned), copies timed
+    # end to end through the public API with host buffers (pinned), copies timed: every
+    # step uploads x and reads out back, double-buffered against the neighbouring steps
     x_pin = x_host.pin_memory()
-    out_pin = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+    xs = [x, torch.empty_like(x)]
+    outs = [out, torch.empty_like(out)]
+    out_pins = [torch.empty(out.shape, dtype=torch.float32).pin_memory() for _ in range(2)]
     e2e_steps = max(3, min(args.steps, 20))
-    with torch.cuda.stream(stream):
-        def e2e_step():
-            x.copy_(x_pin, non_blocking=True)
-            vh.scan_forward(x, mem0, wl.d, chunk=wl.chunk, out=out, params=params, stream=stream,
-                            **extra)
-            out_pin.copy_(out, non_blocking=True)
-        for _ in range(2):
-            e2e_step()
-        torch.cuda.synchronize(dev)
-        ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        ea.record(stream)
-        for _ in range(e2e_steps):
-            e2e_step()
-        eb.record(stream)
-        torch.cuda.synchronize(dev)
-    e2e_s, = max_over_ranks([ea.elapsed_time(eb) / 1e3], device=dev)
+
+    def up(i, k, st):
+        with torch.cuda.stream(st):
+            xs[k].copy_(x_pin, non_blocking=True)
+
+    def run(k, st):
+        vh.scan_forward(xs[k], mem0, wl.d, chunk=wl.chunk, out=outs[k], params=params,
+                        stream=st, **extra)
+
+    def down(k, st):
+        with torch.cuda.stream(st):
+            out_pins[k].copy_(outs[k], non_blocking=True)
+
+    e2e_s, = max_over_ranks([pipelined_e2e(dev, e2e_steps, up, run, down)], device=dev)
     e2e_value = job_throughput(wl.tokens, e2e_steps, world, e2e_s)
 
     if rank == 0:
@@ -529,7 +571,8 @@ def run_ours(args, wl):
             "roofline": roof,
             "e2e": {"value": e2e_value, "unit": UNIT,
                     "h2d_bytes_per_step": int(x_host.numel() * x_host.element_size()),
-                    "d2h_bytes_per_step": int(out.numel() * 4), "steps": e2e_steps},
+                    "d2h_bytes_per_step": int(out.numel() * 4), "steps": e2e_steps,
+                    "copies": "every step, double-buffered against neighbouring steps"},
             "gpu_launches": args.steps * (2 if args.readout == "outer" else 1),
             "clocks": sampler.summary(t0, t1) if sampler else None,
         }
@@ -618,25 +661,27 @@ def run_backward(args, wl):
     value = job_throughput(wl.tokens, args.steps, world, total_s)
 
     x_pin, dout_pin = x_host.pin_memory(), dout_host.pin_memory()
-    dx_pin = torch.empty(dx.shape, dtype=torch.float32).pin_memory()
-    dm_pin = torch.empty(dmem0.shape, dtype=torch.float32).pin_memory()
+    xs, douts = [x, torch.empty_like(x)], [dout, torch.empty_like(dout)]
+    dxs, dms = [dx, torch.empty_like(dx)], [dmem0, torch.empty_like(dmem0)]
+    dx_pins = [torch.empty(dx.shape, dtype=torch.float32).pin_memory() for _ in range(2)]
+    dm_pins = [torch.empty(dmem0.shape, dtype=torch.float32).pin_memory() for _ in range(2)]
     e2e_steps = max(3, min(args.steps, 10))
-    with torch.cuda.stream(stream):
-        def e2e_step():
-            x.copy_(x_pin, non_blocking=True)
-            dout.copy_(dout_pin, non_blocking=True)
-            call()
-            dx_pin.copy_(dx, non_blocking=True)
-            dm_pin.copy_(dmem0, non_blocking=True)
-        e2e_step()
-        torch.cuda.synchronize(dev)
-        ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        ea.record(stream)
-        for _ in range(e2e_steps):
-            e2e_step()
-        eb.record(stream)
-        torch.cuda.synchronize(dev)
-    e2e_s, = max_over_ranks([ea.elapsed_time(eb) / 1e3], device=dev)
+
+    def up(i, k, st):
+        with torch.cuda.stream(st):
+            xs[k].copy_(x_pin, non_blocking=True)
+            douts[k].copy_(dout_pin, non_blocking=True)
+
+    def run(k, st):
+        vh.scan_backward(xs[k], mem0, wl.d, douts[k], chunk=wl.chunk, params=params, dx=dxs[k],
+                         dmem0=dms[k], workspace=ws, stream=st)
+
+    def down(k, st):
+        with torch.cuda.stream(st):
+            dx_pins[k].copy_(dxs[k], non_blocking=True)
+            dm_pins[k].copy_(dms[k], non_blocking=True)
+
+    e2e_s, = max_over_ranks([pipelined_e2e(dev, e2e_steps, up, run, down)], device=dev)
     e2e_value = job_throughput(wl.tokens, e2e_steps, world, e2e_s)
 
     tc_ckpt = (wl.d == 32 and wl.dtype == "bf16" and wl.chunk == 0 and wl.Cc % 8 == 0
@@ -660,7 +705,8 @@ def run_backward(args, wl):
                     "h2d_bytes_per_step": int(x_host.numel() * x_host.element_size()
                                               + dout_host.numel() * 4),
                     "d2h_bytes_per_step": int(dx.numel() * 4 + dmem0.numel() * 4),
-                    "steps": e2e_steps},
+                    "steps": e2e_steps,
+                    "copies": "every step, double-buffered against neighbouring steps"},
             # the backward kernel, after the tensor-core forward that writes the chunk
             # boundary states where it applies (d = 32, bf16, aligned chunks)
             "gpu_launches": args.steps * (2 if tc_ckpt else 1),
@@ -743,22 +789,23 @@ def run_block(args, wl):
     avg_s = total_s / args.steps
     value = job_throughput(wl.tokens, args.steps, world, total_s)
     x_pin = x_host.pin_memory()
-    out_pin = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+    xs, outs = [x, torch.empty_like(x)], [out, torch.empty_like(out)]
+    out_pins = [torch.empty(out.shape, dtype=torch.float32).pin_memory() for _ in range(2)]
     e2e_steps = max(3, min(args.steps, 20))
-    with torch.cuda.stream(stream):
-        def e2e_step():
-            x.copy_(x_pin, non_blocking=True)
-            call()
-            out_pin.copy_(out, non_blocking=True)
-        e2e_step()
-        torch.cuda.synchronize(dev)
-        ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        ea.record(stream)
-        for _ in range(e2e_steps):
-            e2e_step()
-        eb.record(stream)
-        torch.cuda.synchronize(dev)
-    e2e_s, = max_over_ranks([ea.elapsed_time(eb) / 1e3], device=dev)
+
+    def up(i, k, st):
+        with torch.cuda.stream(st):
+            xs[k].copy_(x_pin, non_blocking=True)
+
+    def run(k, st):
+        vh.block_forward(xs[k], mem0, wts, wl.d, params=params, w_query=wq, skip=skip,
+                         dir_scale=lam, out=outs[k], workspace=ws, stream=st)
+
+    def down(k, st):
+        with torch.cuda.stream(st):
+            out_pins[k].copy_(outs[k], non_blocking=True)
+
+    e2e_s, = max_over_ranks([pipelined_e2e(dev, e2e_steps, up, run, down)], device=dev)
     e2e_value = job_throughput(wl.tokens, e2e_steps, world, e2e_s)
     if rank == 0:
         flops, gemm_flops = block_cost(wl)
@@ -779,7 +826,8 @@ def run_block(args, wl):
                          "flops_per_call": flops, "gemm_flops_per_call": gemm_flops},
             "e2e": {"value": e2e_value, "unit": UNIT,
                     "h2d_bytes_per_step": int(x_host.numel() * 4),
-                    "d2h_bytes_per_step": int(out.numel() * 4), "steps": e2e_steps},
+                    "d2h_bytes_per_step": int(out.numel() * 4), "steps": e2e_steps,
+                    "copies": "every step, double-buffered against neighbouring steps"},
             # ours per call: CPE+LN1, gated depthwise, query projection, scan, positional
             # depthwise, LN2, GELU (the four GEMMs are cuBLASLt's)
             "gpu_launches": args.steps * 7,
