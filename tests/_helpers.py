@@ -1,7 +1,7 @@
 """Shared helpers of the test suite: running the CUDA path on synthetic
 inputs, and the parity metric.
 
-Parity metric (the pages fix none; spec tolerance 2e-3): for a tensor
+Parity metric (the pages fix none; the tolerance is 2e-3): for a tensor
 of oracle values o and GPU values g,
     err = max_i |g_i - o_i| / max(|o_i|, 1e-2 * rms(o), 1e-30).
 The 1e-2 * rms term keeps elements near a zero crossing from dominating; the
