@@ -430,6 +430,7 @@ def workload_config(wl, args):
             "parallelism": f"dp{dist_env()[1]} (images split across GPUs, no collective)",
             "l2": "256 MiB buffer written between timed steps (L2 is 129 MB)",
             "kernel": args.kernel, "readout": args.readout, "pass": args.pass_,
+            "memories_out": bool(getattr(args, "memories_out", False)),
             **({"block": "D=%d D_m=%d hidden=%d, 3x3 depthwise, exact operator" % block_dims(wl)}
                if args.pass_ == "block" else {})}
 
@@ -471,6 +472,11 @@ def run_ours(args, wl):
         extra["skip"] = torch.randn(4, wl.Cc, generator=g).to(dev)
         extra["workspace"] = torch.empty(6 * wl.B * wl.H * wl.W * wl.Cc, dtype=torch.uint8,
                                          device=dev)
+
+    # the second row of the measurement: the final memories written as well
+    if args.memories_out:
+        extra["memories_out"] = torch.empty((wl.B, 4, wl.nh, 4 * wl.d * wl.d + 2 * wl.d),
+                                            dtype=torch.float32, device=dev)
 
     def step(ev_start, ev_mid, ev_end):
         flush.zero_()
@@ -535,6 +541,8 @@ def run_ours(args, wl):
 
     if rank == 0:
         flops, nbytes = algorithmic_cost(wl)
+        if args.memories_out:
+            nbytes += wl.B * 4 * wl.nh * (4 * wl.d * wl.d + 2 * wl.d) * 4
         peaks, src = load_peaks()
         achieved = flops / kern_avg_s / 1e12
         peak = float(peaks["bf16_tflops"])
@@ -860,6 +868,8 @@ def main(argv=None):
                     default="forward",
                     help="forward: the scan (default); backward: its outer gradients; "
                          "block: the VisionHOPE block around the operator")
+    ap.add_argument("--memories-out", action="store_true",
+                    help="forward: also write the final memories (the measurement's second row)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-images", type=int, default=16)
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
