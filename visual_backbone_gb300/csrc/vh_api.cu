@@ -137,6 +137,15 @@ void bwd_extent(int H, int W, unsigned dirs, int chunk, int *nck, int *lmax)
     }
 }
 
+// The backward's pre-pass on the tensor-core forward also writes every token's record
+// (k, q, delta and raw scalars) where that kernel applies: head_dim 32, bf16 x, chunks
+// aligned with rows and columns.
+bool bwd_token_records(const vh_params *p, int H, int W, int chunk)
+{
+    return p->impl != VH_IMPL_SIMT && p->head_dim == 32 && p->x_dtype == VH_DTYPE_BF16 &&
+           (chunk == 0 || (chunk == W && chunk == H)) && p->channels % 8 == 0;
+}
+
 // Byte offsets of the block's intermediates in its workspace (256-byte aligned regions).
 struct BlockLayout {
     size_t x0, a, u, z, yb, h, qhat, lt, total;
@@ -397,7 +406,10 @@ size_t vh_backward_workspace_size(const vh_params *p, int H, int W, unsigned dir
     bwd_extent(H, W, dirs, chunk, &nck, &lmax);
     for (int r = 0; r < 4; ++r) nd += (dirs >> r) & 1;
     const size_t scans = (size_t)p->batch * nd * (p->channels / p->head_dim);
-    return scans * vh::bwd_floats_per_scan(p->head_dim, nck, lmax) * sizeof(float);
+    size_t floats = scans * vh::bwd_floats_per_scan(p->head_dim, nck, lmax);
+    if (bwd_token_records(p, H, W, chunk))
+        floats += scans * (size_t)H * W * vh::token_rec_floats(p->head_dim);
+    return floats * sizeof(float);
 }
 
 vh_status vh_scan_backward(const void *x, const float *memories0, const vh_params *p, int H,
@@ -457,15 +469,24 @@ vh_status vh_scan_backward(const void *x, const float *memories0, const vh_param
     if (e != cudaSuccess) return cuda_fail(e, "zeroing dx / dmem0");
     const bool bf16 = p->x_dtype == VH_DTYPE_BF16;
     if (p->impl != VH_IMPL_SIMT) {
-        // the boundary states from the tensor-core forward (no readout), where it applies
+        // the boundary states and token records from the tensor-core forward (no readout
+        // adds), where it applies; the records follow the per-scan blocks
         vh::ScanArgs f = ba.s;
         f.out = nullptr;
         f.ckpt = ba.ws;
         f.ckpt_stride = vh::bwd_floats_per_scan(d, ba.nck, ba.lmax);
+        if (bwd_token_records(p, H, W, chunk)) {
+            f.rec = ba.ws + (size_t)ba.s.B * ba.s.ndirs * ba.s.nh * f.ckpt_stride;
+            f.rec_stride = N * vh::token_rec_floats(d);
+        }
         bool handled = false;
         e = vh::launch_scan_tc(f, d, bf16, st, &handled);
         if (e != cudaSuccess) return cuda_fail(e, "tensor-core forward launch");
         ba.have_ckpt = handled ? 1 : 0;
+        if (handled) {
+            ba.s.rec = f.rec;
+            ba.s.rec_stride = f.rec_stride;
+        }
     }
     e = vh::launch_scan_bwd(ba, d, bf16, st);
     if (e != cudaSuccess) return cuda_fail(e, "backward scan launch");

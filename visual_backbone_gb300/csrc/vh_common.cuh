@@ -41,7 +41,16 @@ struct ScanArgs {
     // to ckpt + i * ckpt_stride + chunk * (4d^2 + 2d) (fp32, state layout)
     float *ckpt;
     size_t ckpt_stride;
+    // backward support: when set (with ckpt), route token t of scan i leaves its record at
+    // rec + i * rec_stride + t * (3d + 8): k, q, delta (normalised, fp32), then
+    // |k_raw|^2, s_eta, s_alpha, |k|^2, |delta|^2, |q_raw|^2 and two unused slots
+    float *rec;
+    size_t rec_stride;
 };
+
+// Floats of one token record (layout above); the scalar slots follow the three vectors.
+__host__ __device__ constexpr int token_rec_floats(int d) { return 3 * d + 8; }
+enum { TR_KK = 0, TR_SE = 1, TR_SA = 2, TR_KN2 = 3, TR_DD = 4, TR_QQ = 5 };
 
 // Arguments of the backward scan kernel.
 struct BwdArgs {
@@ -53,6 +62,7 @@ struct BwdArgs {
     float *ws;                 // per scan: nck boundary states, lmax gain slices and records
     int nck, lmax;
     int have_ckpt;             // the boundary states are already in ws (tensor-core forward)
+                               // s.rec set: so are the token records
 };
 
 // fp32 value of element e of the three-piece query planes (the pieces sum exactly).

@@ -58,7 +58,8 @@ struct BwdCfg {
     static constexpr int CPL = (D + 31) / 32;
     static constexpr int PS = 3 * D + 3;    // generation outputs k_raw v q_raw s_eta s_alpha
     static constexpr int NSC = 16;          // scalars per token
-    static constexpr int REC = 5 * D + NSC; // record: x k q delta (G_{t-1} k) scalars
+    static constexpr int TRS = token_rec_floats(D);  // token record: k q delta, raw scalars
+    static constexpr int GRS = D + NSC;              // gain record: G_{t-1} k, scalars
     // scalar slots
     static constexpr int S_NK = 0, S_NQ = 1, S_SE = 2, S_AL = 4, S_OMA = 5, S_ETA = 6,
                          S_ET = 7, S_INJ = 8, S_BAR = 9, S_SPEC = 10, S_R = 11, S_BR = 12,
@@ -123,6 +124,41 @@ __device__ __forceinline__ void col_sums_add(float (&v)[BwdCfg<D>::CPT], int lan
     }
 }
 
+// The scalars of one token (slots of BwdCfg) from its norms, raw gate inputs and squared
+// norms: gates (Eq. (53)) and the executed step with its intermediates, formed as the
+// forward kernels' step control forms them (Def. 1, App. B.3), so the branch matches.
+template <int D>
+__device__ __forceinline__ void token_scalars(const ScanArgs &a, float *sc, float nk, float nq,
+                                              float se, float sa, float kn2, float dd, int pix)
+{
+    using C = BwdCfg<D>;
+    float eta, alpha, oma;
+    gates(a, se, sa, eta, alpha, oma);
+    const float rr = sqrtf(dd + a.eps * a.eps) + a.eps;
+    const float einj = __fdividef(a.inj_factor * oma, rr);
+    const float ebar = einj > 0.0f ? einj * (-expm1f(-__fdividef(eta, einj))) : 0.0f;
+    float spec = __fdividef(a.spec_factor * 2.0f * alpha, fmaxf(kn2, a.kk_floor));
+    if (spec > 0.0f) spec = __int_as_float(__float_as_int(spec) - 1);
+    const bool sp = spec < ebar;
+    const bool forced = a.gate_mode == VH_GATE_FORCED_EXEC;
+    sc[C::S_NK] = nk;
+    sc[C::S_NQ] = nq;
+    sc[C::S_SE] = se + a.eta_bias;
+    sc[3] = sa;
+    sc[C::S_AL] = alpha;
+    sc[C::S_OMA] = oma;
+    sc[C::S_ETA] = eta;
+    sc[C::S_ET] = forced ? a.forced_eta : (sp ? spec : ebar);
+    sc[C::S_INJ] = einj;
+    sc[C::S_BAR] = ebar;
+    sc[C::S_SPEC] = spec;
+    sc[C::S_R] = rr;
+    sc[C::S_BR] = (!forced && sp) ? 1.0f : 0.0f;
+    sc[C::S_KN2] = kn2;
+    sc[C::S_DD] = dd;
+    sc[C::S_PIX] = __int_as_float(pix);
+}
+
 template <int D, typename XT>
 __global__ void __launch_bounds__(256, BwdCfg<D>::MINB) scan_bwd_kernel(const BwdArgs ba)
 {
@@ -146,10 +182,13 @@ __global__ void __launch_bounds__(256, BwdCfg<D>::MINB) scan_bwd_kernel(const Bw
     const size_t SZ = (size_t)C::R * D;
     const int Cr = route_chunk(r, a.chunk, H, W);
     const int nchunks = (N + Cr - 1) / Cr;
-    float *ckpt = ba.ws + (size_t)blockIdx.x *
-                              ((size_t)ba.nck * SZ + (size_t)ba.lmax * (D * D + C::REC));
+    float *ckpt = ba.ws + (size_t)blockIdx.x * ((size_t)ba.nck * SZ +
+                                                (size_t)ba.lmax * (D * D + C::TRS + C::GRS));
     float *gsc = ckpt + (size_t)ba.nck * SZ;          // [lmax][NT][CPT]: slices of G_{t-1}
-    float *rec = gsc + (size_t)ba.lmax * D * D;       // [lmax][REC]
+    float *trl = gsc + (size_t)ba.lmax * D * D;       // [lmax][TRS]: token records of the chunk
+    float *grec = trl + (size_t)ba.lmax * C::TRS;     // [lmax][GRS]
+    // token records of the whole scan, when the tensor-core forward wrote them
+    const float *trg = a.rec ? a.rec + (size_t)blockIdx.x * a.rec_stride : nullptr;
     const XT *xb = static_cast<const XT *>(a.x) + (size_t)b * N * Cc + (size_t)h * D;
     const float *lam = a.dir_scale ? a.dir_scale + (size_t)r * Cc + (size_t)h * D : nullptr;
     const float *gob = ba.dout + (size_t)b * N * Cc + (size_t)h * D;
@@ -160,13 +199,14 @@ __global__ void __launch_bounds__(256, BwdCfg<D>::MINB) scan_bwd_kernel(const Bw
     for (int e = tid; e < C::R * D; e += C::NT) S[(e / D) * C::SS + (e % D)] = m0[e];
     float G[C::CPT];
 
-    // ---- one tile of a chunk: gather, generation, per-token step and the gain; with
-    // `record` the token quantities and the gain slices go to the workspace
-    auto tile_forward = [&](int c0, int t0, int Lt, bool record) {
-        __syncthreads();  // earlier users of the tile buffers are done
+    // ---- a tile of a chunk, forward.  gen_tile: gather, generation and the per-token
+    // step into X, K, DL, Q, SC.  load_tile: K, DL and SC from the token records the
+    // tensor-core forward wrote.  gain_tile: with `record` the token quantities go to the
+    // chunk's records; then the shared gain over the tile's tokens, with `record` each
+    // token's slice of G_{t-1} and G_{t-1} k saved.
+    auto gather_x = [&](int c0, int t0, int Lt) {
         constexpr int EPV = 16 / (int)sizeof(XT);
         constexpr int VPT = D / EPV;
-        if (tid < Lt) PIX[tid] = route_pixel(r, c0 + t0 + tid, H, W);
         for (int e = tid; e < Lt * VPT; e += C::NT) {
             const int j = e / VPT, v = e % VPT;
             const int pix = route_pixel(r, c0 + t0 + j, H, W);
@@ -175,6 +215,11 @@ __global__ void __launch_bounds__(256, BwdCfg<D>::MINB) scan_bwd_kernel(const Bw
 #pragma unroll
             for (int u = 0; u < EPV; ++u) X[j * D + v * EPV + u] = XElem<XT>::to_f(el[u]);
         }
+    };
+    auto gen_tile = [&](int c0, int t0, int Lt) {
+        __syncthreads();  // earlier users of the tile buffers are done
+        if (tid < Lt) PIX[tid] = route_pixel(r, c0 + t0 + tid, H, W);
+        gather_x(c0, t0, Lt);
         __syncthreads();
         // generation from the boundary state, Eq. (15): rows 0..3d-1 (k, v, q), then the
         // eta and alpha rows (4d, 4d + 1)
@@ -239,17 +284,6 @@ __global__ void __launch_bounds__(256, BwdCfg<D>::MINB) scan_bwd_kernel(const Bw
             }
             kn2 = warp_sum(kn2);
             dd = warp_sum(dd);
-            float eta, alpha, oma;
-            gates(a, pr[3 * D], pr[3 * D + 1], eta, alpha, oma);
-            // the executed step with its intermediates (step_control of the forward kernels)
-            const float rr = sqrtf(dd + a.eps * a.eps) + a.eps;
-            const float einj = __fdividef(a.inj_factor * oma, rr);
-            const float ebar = einj > 0.0f ? einj * (-expm1f(-__fdividef(eta, einj))) : 0.0f;
-            float spec = __fdividef(a.spec_factor * 2.0f * alpha, fmaxf(kn2, a.kk_floor));
-            if (spec > 0.0f) spec = __int_as_float(__float_as_int(spec) - 1);
-            const bool sp = spec < ebar;
-            const bool forced = a.gate_mode == VH_GATE_FORCED_EXEC;
-            const float et = forced ? a.forced_eta : (sp ? spec : ebar);
 #pragma unroll
             for (int m = 0; m < C::CPL; ++m) {
                 const int c = lane + 32 * m;
@@ -259,41 +293,42 @@ __global__ void __launch_bounds__(256, BwdCfg<D>::MINB) scan_bwd_kernel(const Bw
                     Q[j * D + c] = qr[m];
                 }
             }
-            if (lane == 0) {
-                float *sc = SC + j * C::NSC;
-                sc[C::S_NK] = nk;
-                sc[C::S_NQ] = nq;
-                sc[C::S_SE] = pr[3 * D] + a.eta_bias;
-                sc[3] = pr[3 * D + 1];
-                sc[C::S_AL] = alpha;
-                sc[C::S_OMA] = oma;
-                sc[C::S_ETA] = eta;
-                sc[C::S_ET] = et;
-                sc[C::S_INJ] = einj;
-                sc[C::S_BAR] = ebar;
-                sc[C::S_SPEC] = spec;
-                sc[C::S_R] = rr;
-                sc[C::S_BR] = (!forced && sp) ? 1.0f : 0.0f;
-                sc[C::S_KN2] = kn2;
-                sc[C::S_DD] = dd;
-                sc[C::S_PIX] = __int_as_float(PIX[j]);
-            }
+            if (lane == 0)
+                token_scalars<D>(a, SC + j * C::NSC, nk, nq, pr[3 * D], pr[3 * D + 1], kn2, dd, PIX[j]);
         }
         __syncthreads();
-        if (record) {
-            for (int e = tid; e < Lt * C::REC; e += C::NT) {
-                const int j = e / C::REC, f = e % C::REC;
-                float v;
-                if (f < D) v = X[j * D + f];
-                else if (f < 2 * D) v = K[j * D + f - D];
-                else if (f < 3 * D) v = Q[j * D + f - 2 * D];
-                else if (f < 4 * D) v = DL[j * D + f - 3 * D];
-                else if (f < 5 * D) continue;  // G_{t-1} k, written by the gain loop
-                else v = SC[j * C::NSC + f - 5 * D];
-                rec[(size_t)(t0 + j) * C::REC + f] = v;
-            }
+    };
+    auto load_tile = [&](int c0, int t0, int Lt) {
+        __syncthreads();  // earlier users of the tile buffers are done
+        const float *tr = trg + (size_t)(c0 + t0) * C::TRS;
+        for (int e = tid; e < Lt * (D / 4); e += C::NT) {
+            const int j = e / (D / 4), f = (e % (D / 4)) * 4;
+            const float *tk = tr + (size_t)j * C::TRS;
+            *reinterpret_cast<float4 *>(K + j * D + f) = __ldg(reinterpret_cast<const float4 *>(tk + f));
+            *reinterpret_cast<float4 *>(DL + j * D + f) =
+                __ldg(reinterpret_cast<const float4 *>(tk + 2 * D + f));
         }
-        // the shared gain over the tile's tokens: thread (grow, gc0) holds G[grow][gc0..]
+        if (tid < Lt) {
+            const float *ts = tr + (size_t)tid * C::TRS + 3 * D;
+            token_scalars<D>(a, SC + tid * C::NSC, sqrtf(ts[TR_KK] + a.knorm_eps),
+                             sqrtf(ts[TR_QQ] + a.knorm_eps), ts[TR_SE], ts[TR_SA], ts[TR_KN2],
+                             ts[TR_DD], route_pixel(r, c0 + t0 + tid, H, W));
+        }
+        __syncthreads();
+    };
+    auto gain_tile = [&](int t0, int Lt, bool record) {
+        if (record) {
+            if (!trg) {
+                for (int e = tid; e < Lt * (3 * D); e += C::NT) {
+                    const int j = e / (3 * D), f = e % (3 * D);
+                    const float v = f < D ? K[j * D + f] : (f < 2 * D ? Q[j * D + f - D] : DL[j * D + f - 2 * D]);
+                    trl[(size_t)(t0 + j) * C::TRS + f] = v;
+                }
+            }
+            for (int e = tid; e < Lt * C::NSC; e += C::NT)
+                grec[(size_t)(t0 + e / C::NSC) * C::GRS + D + e % C::NSC] = SC[e];
+        }
+        // thread (grow, gc0) holds G[grow][gc0..]
         for (int j = 0; j < Lt; ++j) {
             const float *kj = K + j * D;
             float part = 0.0f;
@@ -311,7 +346,7 @@ __global__ void __launch_bounds__(256, BwdCfg<D>::MINB) scan_bwd_kernel(const Bw
 #pragma unroll
                     for (int c = 0; c < C::CPT; ++c) gd[c] = G[c];
                 }
-                if (gc0 == 0) rec[(size_t)(t0 + j) * C::REC + 4 * D + grow] = part;
+                if (gc0 == 0) grec[(size_t)(t0 + j) * C::GRS + grow] = part;
             }
             const float et = SC[j * C::NSC + C::S_ET], al = SC[j * C::NSC + C::S_AL];
             const float s = et * (part + DL[j * D + grow]);
@@ -372,7 +407,10 @@ __global__ void __launch_bounds__(256, BwdCfg<D>::MINB) scan_bwd_kernel(const Bw
         if (c == nchunks - 1) break;  // the last chunk's end state is not needed
 #pragma unroll
         for (int q = 0; q < C::CPT; ++q) G[q] = (grow == gc0 + q) ? 1.0f : 0.0f;
-        for (int t0 = 0; t0 < L; t0 += C::T) tile_forward(c0, t0, min(C::T, L - t0), false);
+        for (int t0 = 0; t0 < L; t0 += C::T) {
+            gen_tile(c0, t0, min(C::T, L - t0));
+            gain_tile(t0, min(C::T, L - t0), false);
+        }
         // chunk end: S <- S_b G, row by row
         __syncthreads();
 #pragma unroll
@@ -394,8 +432,13 @@ __global__ void __launch_bounds__(256, BwdCfg<D>::MINB) scan_bwd_kernel(const Bw
         for (int e = tid; e < C::R * D; e += C::NT) S[(e / D) * C::SS + (e % D)] = ck[e];
 #pragma unroll
         for (int q = 0; q < C::CPT; ++q) G[q] = (grow == gc0 + q) ? 1.0f : 0.0f;
-        // a. regenerate the chunk, recording
-        for (int t0 = 0; t0 < L; t0 += C::T) tile_forward(c0, t0, min(C::T, L - t0), true);
+        // a. regenerate the chunk (or read its token records), recording
+        for (int t0 = 0; t0 < L; t0 += C::T) {
+            if (trg) load_tile(c0, t0, min(C::T, L - t0));
+            else gen_tile(c0, t0, min(C::T, L - t0));
+            gain_tile(t0, min(C::T, L - t0), true);
+        }
+        const float *tr = trg ? trg + (size_t)c0 * C::TRS : trl;  // this chunk's token records
         // b. chunk end: P_L = S_b^T dS (this thread's slice), then dS <- dS G_L^T
         __syncthreads();
 #pragma unroll
@@ -427,18 +470,23 @@ __global__ void __launch_bounds__(256, BwdCfg<D>::MINB) scan_bwd_kernel(const Bw
         for (int ti = ntiles - 1; ti >= 0; --ti) {
             const int t0 = ti * C::T, Lt = min(C::T, L - t0);
             __syncthreads();
-            for (int e = tid; e < Lt * D; e += C::NT) {
-                const int j = e / D, f = e % D;
-                const float *rc = rec + (size_t)(t0 + j) * C::REC;
-                X[e] = rc[f];
-                K[e] = rc[D + f];
-                Q[e] = rc[2 * D + f];
-                DL[e] = rc[3 * D + f];
-                Z[e] = rc[4 * D + f] + rc[3 * D + f];
-                KG[e] = 0.0f;
+            gather_x(c0, t0, Lt);
+            for (int e = tid; e < Lt * (D / 4); e += C::NT) {
+                const int j = e / (D / 4), f = (e % (D / 4)) * 4;
+                const float *tk = tr + (size_t)(t0 + j) * C::TRS + f;
+                const float4 kv = *reinterpret_cast<const float4 *>(tk);
+                const float4 qv = *reinterpret_cast<const float4 *>(tk + D);
+                const float4 dv = *reinterpret_cast<const float4 *>(tk + 2 * D);
+                const float4 gv = *reinterpret_cast<const float4 *>(grec + (size_t)(t0 + j) * C::GRS + f);
+                *reinterpret_cast<float4 *>(K + j * D + f) = kv;
+                *reinterpret_cast<float4 *>(Q + j * D + f) = qv;
+                *reinterpret_cast<float4 *>(DL + j * D + f) = dv;
+                *reinterpret_cast<float4 *>(Z + j * D + f) =
+                    make_float4(gv.x + dv.x, gv.y + dv.y, gv.z + dv.z, gv.w + dv.w);
+                *reinterpret_cast<float4 *>(KG + j * D + f) = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
             }
             for (int e = tid; e < Lt * C::NSC; e += C::NT)
-                SC[e] = rec[(size_t)(t0 + e / C::NSC) * C::REC + 5 * D + e % C::NSC];
+                SC[e] = grec[(size_t)(t0 + e / C::NSC) * C::GRS + D + e % C::NSC];
             // dy = lambda_r dout at the tokens' pixels (Eq. (26) read backwards)
             for (int e = tid; e < Lt * D; e += C::NT) {
                 const int j = e / D, f = e % D;
@@ -689,7 +737,7 @@ static cudaError_t launch_bwd_t(const BwdArgs &ba, cudaStream_t st)
 size_t bwd_floats_per_scan(int d, int nck, int lmax)
 {
     const size_t sz = (size_t)(4 * d + 2) * d;
-    return (size_t)nck * sz + (size_t)lmax * ((size_t)d * d + 5 * d + 16);
+    return (size_t)nck * sz + (size_t)lmax * ((size_t)d * d + token_rec_floats(d) + d + 16);
 }
 
 cudaError_t launch_scan_bwd(const BwdArgs &ba, int d, bool bf16, cudaStream_t st)

@@ -102,6 +102,12 @@ static_assert(OFF_Q + 4 * Q_PIECE <= OFF_BAR, "operand rows 64..127 stay in shar
 
 // ------------------------------------------------- kernel-specific helpers
 
+// Record of route token t of this CTA's scan (backward support).
+__device__ __forceinline__ float *rec_at(const ScanArgs &a, int t)
+{
+    return a.rec + (size_t)blockIdx.x * a.rec_stride + (size_t)t * token_rec_floats(D);
+}
+
 // k_raw (32 columns at +COL_K), v (32 at +COL_V) and s_eta, s_alpha (2 at +0) of this
 // thread's lane, with a single wait.
 __device__ __forceinline__ void tmem_ld_kvs(uint32_t ta, float (&k)[32], float (&v)[32], float &se,
@@ -371,7 +377,8 @@ __global__ void __launch_bounds__(NT, 3)
                 float kr[32], vv[32];
                 float se, sa;
                 tmem_ld_kvs(tbase + lrow + COL_GEN, kr, vv, se, sa);
-                const float rk = __frsqrt_rn(sumsq32(kr) + a.knorm_eps);
+                const float kkr = sumsq32(kr);
+                const float rk = __frsqrt_rn(kkr + a.knorm_eps);
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
                     kr[e] *= rk;            // k
@@ -387,6 +394,16 @@ __global__ void __launch_bounds__(NT, 3)
                         dd4[e] = make_float4(vv[4 * e], vv[4 * e + 1], vv[4 * e + 2], vv[4 * e + 3]);
                     }
                     SC[jr] = make_float4(se, sa, kn2, dd2);
+                    if (kAbl && a.rec) {  // token record (backward support)
+                        float4 *rd = reinterpret_cast<float4 *>(rec_at(a, c * Lline + t0 + jr));
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            rd[e] = make_float4(kr[4 * e], kr[4 * e + 1], kr[4 * e + 2], kr[4 * e + 3]);
+                            rd[2 * D / 4 + e] = make_float4(vv[4 * e], vv[4 * e + 1], vv[4 * e + 2], vv[4 * e + 3]);
+                        }
+                        rd[3 * D / 4] = make_float4(kkr, se, sa, kn2);
+                        rd[3 * D / 4 + 1].x = dd2;
+                    }
                 }
                 if (intra) {
                     // the normalised query for the gain pair, route order (fp32)
@@ -747,9 +764,18 @@ __global__ void __launch_bounds__(NT, 3)
                 } else if (!exact) {
                     float qr[32];
                     tmem_ld32(tbase + lrow + COL_GEN + COL_QR, qr);
-                    const float rq = __frsqrt_rn(sumsq32(qr) + a.knorm_eps);
+                    const float qqr = sumsq32(qr);
+                    const float rq = __frsqrt_rn(qqr + a.knorm_eps);
 #pragma unroll
                     for (int e = 0; e < 32; ++e) qr[e] *= rq;
+                    if (kAbl && a.rec && valid) {  // the query of the token record
+                        float *rq4 = rec_at(a, c * Lline + t0 + jr);
+                        float4 *qd = reinterpret_cast<float4 *>(rq4 + D);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            qd[e] = make_float4(qr[4 * e], qr[4 * e + 1], qr[4 * e + 2], qr[4 * e + 3]);
+                        rq4[3 * D + TR_QQ] = qqr;
+                    }
 #pragma unroll
                     for (int g = 0; g < 4; ++g) store_split8(sQ + op_off(jq, g), Q_PIECE, qr + 8 * g);
                     fence_async_smem();
