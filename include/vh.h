@@ -222,9 +222,12 @@ size_t vh_workspace_size(const vh_params *p, int H, int W, unsigned dirs, int ch
  *
  * The call recomputes the forward: it keeps every chunk's boundary state and, per scan,
  * the current chunk's gain slices and token records in p->workspace, which must hold
- * vh_backward_workspace_size() bytes, 16-byte aligned.  One CUDA-core kernel, fp32;
- * gradients are summed over routes and images with device atomics (their rounding order
- * is not fixed).  The branch of the step control follows the forward's choice.
+ * vh_backward_workspace_size() bytes, 16-byte aligned.  Where the tensor-core forward
+ * applies (head_dim 32, bf16 x, chunks aligned with rows and columns, impl not SIMT) it
+ * runs first and writes the boundary states and every token's record; one CUDA-core
+ * kernel, fp32, then forms the gradients, summed over routes and images with device
+ * atomics (their rounding order is not fixed).  The branch of the step control follows
+ * the forward's choice.
  *
  * Errors: as vh_scan_forward; VH_ERR_UNSUPPORTED for control_flags != 0, w_query or
  * skip (the ablation switches and the VisionHOPE-exact readout have no backward);
@@ -236,7 +239,9 @@ vh_status vh_scan_backward(const void *x, const float *memories0, const vh_param
 
 /* Bytes of device workspace vh_scan_backward needs for these parameters: per scan
  * (image, enabled route, head) the boundary states of its chunks and, for its longest
- * chunk, d^2 + 5d + 16 floats per token.  0 for invalid arguments. */
+ * chunk, a d^2 gain slice per four tokens and 4d + 24 floats per token; where the
+ * tensor-core forward applies, also 3d + 8 floats per token of the whole scan.  0 for
+ * invalid arguments. */
 size_t vh_backward_workspace_size(const vh_params *p, int H, int W, unsigned dirs, int chunk);
 
 /*

@@ -108,25 +108,28 @@ def _bwd_call(vhlib, B=1, Cc=32, d=32, H=4, W=4, dirs=15, chunk=0, ws=0, ws_byte
 
 def test_backward_workspace_size(vhlib):
     """Per scan: the boundary states of its chunks (4d^2 + 2d floats each) plus, for the
-    longest chunk, d^2 + 4d + 24 floats per token (gain slice, token record, gain record).
-    Where the tensor-core forward runs the pre-pass (d = 32, bf16 x, aligned chunks, impl
-    not SIMT) it also writes a 3d + 8 float record for every token of every scan."""
+    longest chunk, a d^2 gain slice per four tokens and 4d + 24 floats per token (token
+    record, gain record).  Where the tensor-core forward runs the pre-pass (d = 32, bf16 x,
+    aligned chunks, impl not SIMT) it also writes a 3d + 8 float record for every token of
+    every scan."""
     L = vhlib.lib()
     p = vhlib.make_cparams(2, 64, 32, True)
-    chunk_tok = 32 * 32 + 4 * 32 + 24
+
+    def chunk_floats(lmax):
+        return (lmax + 3) // 4 * 32 * 32 + lmax * (4 * 32 + 24)
     trec = 15 * (3 * 32 + 8)
     # 3 x 5 map, all routes, aligned chunks: rows of 5 (3 chunks), columns of 3 (5 chunks)
-    per_scan = 5 * (4 * 32 * 32 + 64) + 5 * chunk_tok
+    per_scan = 5 * (4 * 32 * 32 + 64) + chunk_floats(5)
     assert L.vh_backward_workspace_size(ctypes.byref(p), 3, 5, 15, 0) == 2 * 4 * 2 * (per_scan + trec) * 4
     # rows only: 3 chunks of 5
-    per_scan = 3 * (4 * 32 * 32 + 64) + 5 * chunk_tok
+    per_scan = 3 * (4 * 32 * 32 + 64) + chunk_floats(5)
     assert L.vh_backward_workspace_size(ctypes.byref(p), 3, 5, 3, 0) == 2 * 2 * 2 * (per_scan + trec) * 4
     # fixed chunk 4 over 15 tokens: 4 chunks, the longest 4 tokens; no token records
-    per_scan = 4 * (4 * 32 * 32 + 64) + 4 * chunk_tok
+    per_scan = 4 * (4 * 32 * 32 + 64) + chunk_floats(4)
     assert L.vh_backward_workspace_size(ctypes.byref(p), 3, 5, 1, 4) == 2 * 1 * 2 * per_scan * 4
     # the CUDA-core implementation forced: no token records
     ps = vhlib.make_cparams(2, 64, 32, True, vhlib.ScanParams(impl="simt"))
-    per_scan = 3 * (4 * 32 * 32 + 64) + 5 * chunk_tok
+    per_scan = 3 * (4 * 32 * 32 + 64) + chunk_floats(5)
     assert L.vh_backward_workspace_size(ctypes.byref(ps), 3, 5, 3, 0) == 2 * 2 * 2 * per_scan * 4
     assert L.vh_backward_workspace_size(None, 3, 5, 15, 0) == 0
     assert L.vh_backward_workspace_size(ctypes.byref(p), 3, 5, 0, 0) == 0

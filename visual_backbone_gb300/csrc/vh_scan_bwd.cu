@@ -17,12 +17,14 @@
 //  Pass 2 (reverse, from the last chunk), holding dS = dL/dS_end of the chunk (dmem_final,
 //    or zero, for the last one):
 //    a. S_b is reloaded and the chunk's tokens regenerated tile by tile (Eq. (15),
-//       App. C.1 normalisation, Eq. (53) gates, Def. 1 step control); their quantities
-//       are recorded in the workspace and the shared gain (Prop. 2, Eq. (46))
-//       re-advanced, every thread keeping its slice of G_{t-1} for each token;
+//       App. C.1 normalisation, Eq. (53) gates, Def. 1 step control), or, after the
+//       tensor-core forward, read from the token records it wrote; their quantities are
+//       recorded in the workspace and the shared gain (Prop. 2, Eq. (46)) re-advanced,
+//       every thread keeping its slice of G_{t-1} for every fourth token and z_t for all;
 //    b. the chunk end S_end = S_b G_L gives the gain adjoint P_L = S_b^T dS, and
 //       dS <- dS G_L^T;
-//    c. with z_t = G_{t-1} k_t + delta_t, G_t = alpha_t G_{t-1} - eta_t z_t k_t^T, so the
+//    c. with z_t = G_{t-1} k_t + delta_t, G_t = alpha_t G_{t-1} - eta_t z_t k_t^T (which
+//       also rebuilds the slices between the stored ones, with no reduction), so the
 //       adjoint runs backwards as P_{t-1} = alpha_t P_t - eta_t (P_t k_t) k_t^T and gives,
 //       with u_t = P_t k_t,
 //         dalpha_t = <P_t, G_{t-1}>,  deta_t = -z_t . u_t,  ddelta_t = -eta_t u_t,
@@ -42,6 +44,9 @@
 
 namespace vh {
 
+// One slice of G_{t-1} is kept per this many tokens of a chunk.
+constexpr int kGainGroup = 4;
+
 template <int D>
 struct BwdCfg {
     static constexpr int NT = 256;
@@ -51,7 +56,7 @@ struct BwdCfg {
     static constexpr int T = D == 16 ? 64 : 16;   // token tile
     static constexpr int MINB = D == 64 ? 1 : 3;  // resident CTAs per SM (one wave at stage 1)
     static constexpr int JB = 4;                  // tokens per register block (generation)
-    static constexpr int PF = 4;                  // gain slices in flight (reverse loop)
+    static constexpr int GS = kGainGroup;         // tokens per stored slice of the gain
     static constexpr int TPR = NT / D;      // threads per gain row
     static constexpr int CPT = D / TPR;     // gain columns per thread
     static constexpr int RW = 32 / TPR;     // gain rows per warp
@@ -83,8 +88,24 @@ struct BwdCfg {
     static constexpr int FLOATS = OFF_PIX + T;
     static constexpr size_t BYTES = (size_t)FLOATS * 4;
     static_assert(TPR * CPT == D && TPR <= 32, "gain thread map");
+    static_assert(T % GS == 0, "tiles hold whole groups of stored gain slices");
     static_assert(BYTES <= 227 * 1024, "shared memory");
 };
+
+// Asynchronous global -> shared copies (16 or 4 bytes) and the wait for all of them.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+                 "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async4(void *dst, const void *src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+                 "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // Column sums over the rows held by one warp, added (times `scale`) to dst[0..D): each
 // lane holds v[0..CPT) for columns gc0.. of its row.  Every level halves the value set
@@ -182,10 +203,11 @@ __global__ void __launch_bounds__(256, BwdCfg<D>::MINB) scan_bwd_kernel(const Bw
     const size_t SZ = (size_t)C::R * D;
     const int Cr = route_chunk(r, a.chunk, H, W);
     const int nchunks = (N + Cr - 1) / Cr;
-    float *ckpt = ba.ws + (size_t)blockIdx.x * ((size_t)ba.nck * SZ +
-                                                (size_t)ba.lmax * (D * D + C::TRS + C::GRS));
-    float *gsc = ckpt + (size_t)ba.nck * SZ;          // [lmax][NT][CPT]: slices of G_{t-1}
-    float *trl = gsc + (size_t)ba.lmax * D * D;       // [lmax][TRS]: token records of the chunk
+    const int ngs = (ba.lmax + C::GS - 1) / C::GS;    // stored gain slices per chunk
+    float *ckpt = ba.ws + (size_t)blockIdx.x * ((size_t)ba.nck * SZ + (size_t)ngs * D * D +
+                                                (size_t)ba.lmax * (C::TRS + C::GRS));
+    float *gsc = ckpt + (size_t)ba.nck * SZ;          // [ngs][NT][CPT]: slices of G_{t-1}
+    float *trl = gsc + (size_t)ngs * D * D;           // [lmax][TRS]: token records of the chunk
     float *grec = trl + (size_t)ba.lmax * C::TRS;     // [lmax][GRS]
     // token records of the whole scan, when the tensor-core forward wrote them
     const float *trg = a.rec ? a.rec + (size_t)blockIdx.x * a.rec_stride : nullptr;
@@ -204,6 +226,20 @@ __global__ void __launch_bounds__(256, BwdCfg<D>::MINB) scan_bwd_kernel(const Bw
     // tensor-core forward wrote.  gain_tile: with `record` the token quantities go to the
     // chunk's records; then the shared gain over the tile's tokens, with `record` each
     // token's slice of G_{t-1} and G_{t-1} k saved.
+    // this thread's CPT key entries of tile token j (columns gc0..)
+    auto ld_key = [&](int j, float (&kv)[C::CPT]) {
+        const float *kj = K + j * D + gc0;
+        if constexpr (C::CPT % 4 == 0) {
+#pragma unroll
+            for (int c = 0; c < C::CPT; c += 4) {
+                const float4 f = *reinterpret_cast<const float4 *>(kj + c);
+                kv[c] = f.x; kv[c + 1] = f.y; kv[c + 2] = f.z; kv[c + 3] = f.w;
+            }
+        } else {
+#pragma unroll
+            for (int c = 0; c < C::CPT; ++c) kv[c] = kj[c];
+        }
+    };
     auto gather_x = [&](int c0, int t0, int Lt) {
         constexpr int EPV = 16 / (int)sizeof(XT);
         constexpr int VPT = D / EPV;
@@ -330,28 +366,31 @@ __global__ void __launch_bounds__(256, BwdCfg<D>::MINB) scan_bwd_kernel(const Bw
         }
         // thread (grow, gc0) holds G[grow][gc0..]
         for (int j = 0; j < Lt; ++j) {
-            const float *kj = K + j * D;
+            float kj[C::CPT];
+            ld_key(j, kj);
             float part = 0.0f;
 #pragma unroll
-            for (int c = 0; c < C::CPT; ++c) part = fmaf(G[c], kj[gc0 + c], part);
+            for (int c = 0; c < C::CPT; ++c) part = fmaf(G[c], kj[c], part);
 #pragma unroll
             for (int o = C::TPR / 2; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
             if (record) {
-                float *gd = gsc + ((size_t)(t0 + j) * C::NT + tid) * C::CPT;
-                if constexpr (C::CPT % 4 == 0) {
+                if ((j % C::GS) == 0) {  // a group's first slice of G_{t-1}
+                    float *gd = gsc + ((size_t)(t0 + j) / C::GS * C::NT + tid) * C::CPT;
+                    if constexpr (C::CPT % 4 == 0) {
 #pragma unroll
-                    for (int c = 0; c < C::CPT; c += 4)
-                        *reinterpret_cast<float4 *>(gd + c) = make_float4(G[c], G[c + 1], G[c + 2], G[c + 3]);
-                } else {
+                        for (int c = 0; c < C::CPT; c += 4)
+                            *reinterpret_cast<float4 *>(gd + c) = make_float4(G[c], G[c + 1], G[c + 2], G[c + 3]);
+                    } else {
 #pragma unroll
-                    for (int c = 0; c < C::CPT; ++c) gd[c] = G[c];
+                        for (int c = 0; c < C::CPT; ++c) gd[c] = G[c];
+                    }
                 }
                 if (gc0 == 0) grec[(size_t)(t0 + j) * C::GRS + grow] = part;
             }
             const float et = SC[j * C::NSC + C::S_ET], al = SC[j * C::NSC + C::S_AL];
             const float s = et * (part + DL[j * D + grow]);
 #pragma unroll
-            for (int c = 0; c < C::CPT; ++c) G[c] = fmaf(-s, kj[gc0 + c], al * G[c]);
+            for (int c = 0; c < C::CPT; ++c) G[c] = fmaf(-s, kj[c], al * G[c]);
         }
     };
 
@@ -428,8 +467,21 @@ __global__ void __launch_bounds__(256, BwdCfg<D>::MINB) scan_bwd_kernel(const Bw
     for (int c = nchunks - 1; c >= 0; --c) {
         const int c0 = c * Cr, L = min(Cr, N - c0);
         __syncthreads();
-        const float *ck = ckpt + (size_t)c * SZ;
-        for (int e = tid; e < C::R * D; e += C::NT) S[(e / D) * C::SS + (e % D)] = ck[e];
+        {
+            // the boundary state, every load issued before the stores
+            const float4 *ck4 = reinterpret_cast<const float4 *>(ckpt + (size_t)c * SZ);
+            constexpr int NS4 = (C::R * D / 4 + C::NT - 1) / C::NT;
+            float4 v[NS4];
+#pragma unroll
+            for (int i = 0; i < NS4; ++i)
+                if (tid + i * C::NT < C::R * D / 4) v[i] = ck4[tid + i * C::NT];
+#pragma unroll
+            for (int i = 0; i < NS4; ++i) {
+                const int e = tid + i * C::NT;
+                if (e < C::R * D / 4)
+                    *reinterpret_cast<float4 *>(S + (e / (D / 4)) * C::SS + (e % (D / 4)) * 4) = v[i];
+            }
+        }
 #pragma unroll
         for (int q = 0; q < C::CPT; ++q) G[q] = (grow == gc0 + q) ? 1.0f : 0.0f;
         // a. regenerate the chunk (or read its token records), recording
@@ -470,35 +522,59 @@ __global__ void __launch_bounds__(256, BwdCfg<D>::MINB) scan_bwd_kernel(const Bw
         for (int ti = ntiles - 1; ti >= 0; --ti) {
             const int t0 = ti * C::T, Lt = min(C::T, L - t0);
             __syncthreads();
-            gather_x(c0, t0, Lt);
-            for (int e = tid; e < Lt * (D / 4); e += C::NT) {
-                const int j = e / (D / 4), f = (e % (D / 4)) * 4;
-                const float *tk = tr + (size_t)(t0 + j) * C::TRS + f;
-                const float4 kv = *reinterpret_cast<const float4 *>(tk);
-                const float4 qv = *reinterpret_cast<const float4 *>(tk + D);
-                const float4 dv = *reinterpret_cast<const float4 *>(tk + 2 * D);
-                const float4 gv = *reinterpret_cast<const float4 *>(grec + (size_t)(t0 + j) * C::GRS + f);
-                *reinterpret_cast<float4 *>(K + j * D + f) = kv;
-                *reinterpret_cast<float4 *>(Q + j * D + f) = qv;
-                *reinterpret_cast<float4 *>(DL + j * D + f) = dv;
-                *reinterpret_cast<float4 *>(Z + j * D + f) =
-                    make_float4(gv.x + dv.x, gv.y + dv.y, gv.z + dv.z, gv.w + dv.w);
-                *reinterpret_cast<float4 *>(KG + j * D + f) = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-            }
-            for (int e = tid; e < Lt * C::NSC; e += C::NT)
-                SC[e] = grec[(size_t)(t0 + e / C::NSC) * C::GRS + D + e % C::NSC];
-            // dy = lambda_r dout at the tokens' pixels (Eq. (26) read backwards)
-            for (int e = tid; e < Lt * D; e += C::NT) {
-                const int j = e / D, f = e % D;
-                const int pix = route_pixel(r, c0 + t0 + j, H, W);
-                Y[e] = (lam ? lam[f] : 1.0f) * __ldg(gob + (size_t)pix * Cc + f);
+            // staging by asynchronous copies, all in flight together: the token records
+            // (k, q, delta), G_{t-1} k into Z and the scalars from the gain records, x at the
+            // tokens' pixels (fp32 straight into X; bf16 through the P buffer, which is free
+            // until the per-token adjoints) and dout at the pixels into Y
+            {
+                constexpr int EPV = 16 / (int)sizeof(XT), VPT = D / EPV;
+                unsigned char *xraw = sizeof(XT) == 4 ? reinterpret_cast<unsigned char *>(X)
+                                                      : reinterpret_cast<unsigned char *>(P);
+                for (int e = tid; e < Lt * (D / 4); e += C::NT) {
+                    const int j = e / (D / 4), f = (e % (D / 4)) * 4;
+                    const float *tk = tr + (size_t)(t0 + j) * C::TRS + f;
+                    cp_async16(K + j * D + f, tk);
+                    cp_async16(Q + j * D + f, tk + D);
+                    cp_async16(DL + j * D + f, tk + 2 * D);
+                    cp_async16(Z + j * D + f, grec + (size_t)(t0 + j) * C::GRS + f);
+                }
+                for (int e = tid; e < Lt * (C::NSC / 4); e += C::NT)
+                    cp_async16(SC + 4 * e, grec + (size_t)(t0 + e / (C::NSC / 4)) * C::GRS + D + (e % (C::NSC / 4)) * 4);
+                for (int e = tid; e < Lt * VPT; e += C::NT) {
+                    const int pix = route_pixel(r, c0 + t0 + e / VPT, H, W);
+                    cp_async16(xraw + (size_t)e * 16, xb + (size_t)pix * Cc + (e % VPT) * EPV);
+                }
+                for (int e = tid; e < Lt * D; e += C::NT) {
+                    const int pix = route_pixel(r, c0 + t0 + e / D, H, W);
+                    cp_async4(Y + e, gob + (size_t)pix * Cc + e % D);
+                }
+                cp_async_wait_all();
+                __syncthreads();
+                // z = G_{t-1} k + delta; the dk share of the gain starts at zero; x to fp32
+                for (int e = tid; e < Lt * (D / 4); e += C::NT) {
+                    float4 *z4 = reinterpret_cast<float4 *>(Z) + e;
+                    const float4 d4 = reinterpret_cast<const float4 *>(DL)[e];
+                    const float4 g4 = *z4;
+                    *z4 = make_float4(g4.x + d4.x, g4.y + d4.y, g4.z + d4.z, g4.w + d4.w);
+                    reinterpret_cast<float4 *>(KG)[e] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                }
+                if constexpr (sizeof(XT) != 4) {
+                    for (int e = tid; e < Lt * VPT; e += C::NT) {
+                        const uint4 raw = *reinterpret_cast<const uint4 *>(xraw + (size_t)e * 16);
+                        const XT *el = reinterpret_cast<const XT *>(&raw);
+                        float *xd = X + e * EPV;
+#pragma unroll
+                        for (int u = 0; u < EPV; ++u) xd[u] = XElem<XT>::to_f(el[u]);
+                    }
+                }
             }
             __syncthreads();
-            // c. gain adjoint, last token first; the slices of G_{t-1} are fetched PF
-            // tokens ahead
-            float ring[C::PF][C::CPT];
+            // c. gain adjoint, last token first, by groups of GS tokens.  A group's first
+            // slice of G_{t-1} is in the workspace (fetched one group ahead); the others
+            // follow forward from it, G_t = alpha_t G_{t-1} - eta_t z_t k_t^T with the
+            // recorded z_t, exactly as the recompute formed them.
             auto ld_slice = [&](int j, float (&g)[C::CPT]) {
-                const float *gs = gsc + ((size_t)(t0 + j) * C::NT + tid) * C::CPT;
+                const float *gs = gsc + ((size_t)(t0 + j) / C::GS * C::NT + tid) * C::CPT;
                 if constexpr (C::CPT % 4 == 0) {
 #pragma unroll
                     for (int q = 0; q < C::CPT; q += 4) {
@@ -510,25 +586,37 @@ __global__ void __launch_bounds__(256, BwdCfg<D>::MINB) scan_bwd_kernel(const Bw
                     for (int q = 0; q < C::CPT; ++q) g[q] = gs[q];
                 }
             };
+            float nxt[C::CPT];
+            const int ngrp = (Lt + C::GS - 1) / C::GS;
+            ld_slice((ngrp - 1) * C::GS, nxt);
+            for (int gi = ngrp - 1; gi >= 0; --gi) {
+                const int m0 = gi * C::GS;
+                float ring[C::GS][C::CPT];
 #pragma unroll
-            for (int pf = 0; pf < C::PF; ++pf)
-                if (Lt - 1 - pf >= 0) ld_slice(Lt - 1 - pf, ring[pf]);
-            for (int jb = Lt - 1; jb >= 0; jb -= C::PF) {
+                for (int q = 0; q < C::CPT; ++q) ring[0][q] = nxt[q];
+                if (gi > 0) ld_slice(m0 - C::GS, nxt);
 #pragma unroll
-                for (int pf = 0; pf < C::PF; ++pf) {
-                    const int j = jb - pf;
-                    if (j < 0) break;
-                    float gp[C::CPT];
+                for (int i = 1; i < C::GS; ++i) {
+                    const int jp = min(m0 + i - 1, Lt - 1);  // past the tile's end: unused
+                    float kp[C::CPT];
+                    ld_key(jp, kp);
+                    const float sp = SC[jp * C::NSC + C::S_ET] * Z[jp * D + grow];
+                    const float ap = SC[jp * C::NSC + C::S_AL];
 #pragma unroll
-                    for (int q = 0; q < C::CPT; ++q) gp[q] = ring[pf][q];
-                    if (j - C::PF >= 0) ld_slice(j - C::PF, ring[pf]);
-                    const float *kj = K + j * D;
+                    for (int q = 0; q < C::CPT; ++q) ring[i][q] = fmaf(-sp, kp[q], ap * ring[i - 1][q]);
+                }
+#pragma unroll
+                for (int i = C::GS - 1; i >= 0; --i) {
+                    const int j = m0 + i;
+                    if (j >= Lt) continue;
+                    float kj[C::CPT];
+                    ld_key(j, kj);
                     // u = P_t k_t and this row's share of <P_t, G_{t-1}>, reduced together
                     float u = 0.0f, sa = 0.0f;
 #pragma unroll
                     for (int q = 0; q < C::CPT; ++q) {
-                        u = fmaf(Pg[q], kj[gc0 + q], u);
-                        sa = fmaf(Pg[q], gp[q], sa);
+                        u = fmaf(Pg[q], kj[q], u);
+                        sa = fmaf(Pg[q], ring[i][q], sa);
                     }
 #pragma unroll
                     for (int o = C::TPR / 2; o > 0; o >>= 1) {
@@ -539,14 +627,14 @@ __global__ void __launch_bounds__(256, BwdCfg<D>::MINB) scan_bwd_kernel(const Bw
                     const float al = SC[j * C::NSC + C::S_AL], et = SC[j * C::NSC + C::S_ET];
                     float cp[C::CPT];
 #pragma unroll
-                    for (int q = 0; q < C::CPT; ++q) cp[q] = fmaf(gp[q], u, Pg[q] * zr);
+                    for (int q = 0; q < C::CPT; ++q) cp[q] = fmaf(ring[i][q], u, Pg[q] * zr);
                     if (gc0 == 0) {
                         DG[j * D + grow] = -et * u;
                         UV[j * D + grow] = u;
                         UV[(C::T + j) * D + grow] = sa;
                     }
 #pragma unroll
-                    for (int q = 0; q < C::CPT; ++q) Pg[q] = fmaf(-et * u, kj[gc0 + q], al * Pg[q]);
+                    for (int q = 0; q < C::CPT; ++q) Pg[q] = fmaf(-et * u, kj[q], al * Pg[q]);
                     col_sums_add<D>(cp, lane, gc0, KG + j * D, -et);
                 }
             }
@@ -561,7 +649,7 @@ __global__ void __launch_bounds__(256, BwdCfg<D>::MINB) scan_bwd_kernel(const Bw
                 for (int m = 0; m < C::CPL; ++m) {
                     const int c = lane + 32 * m;
                     const bool ok = c < D;
-                    dy[m] = ok ? Y[j * D + c] : 0.0f;
+                    dy[m] = ok ? (lam ? lam[c] : 1.0f) * Y[j * D + c] : 0.0f;  // dy = lambda_r dout
                     kk[m] = ok ? K[j * D + c] : 0.0f;
                     qv[m] = ok ? Q[j * D + c] : 0.0f;
                     dl[m] = ok ? DL[j * D + c] : 0.0f;
@@ -701,6 +789,13 @@ __global__ void __launch_bounds__(256, BwdCfg<D>::MINB) scan_bwd_kernel(const Bw
                     a2 = fmaf(g, u.z, a2);
                     a3 = fmaf(g, u.w, a3);
                 }
+                if (rd && lam) {  // Y holds dout: dy = lambda_r dout
+                    const float l = lam[o - 3 * D];
+                    a0 *= l;
+                    a1 *= l;
+                    a2 *= l;
+                    a3 *= l;
+                }
                 float *dd = dS + o * C::SS + j4;
                 dd[0] += a0;
                 dd[1] += a1;
@@ -737,7 +832,8 @@ static cudaError_t launch_bwd_t(const BwdArgs &ba, cudaStream_t st)
 size_t bwd_floats_per_scan(int d, int nck, int lmax)
 {
     const size_t sz = (size_t)(4 * d + 2) * d;
-    return (size_t)nck * sz + (size_t)lmax * ((size_t)d * d + token_rec_floats(d) + d + 16);
+    return (size_t)nck * sz + (size_t)(lmax + kGainGroup - 1) / kGainGroup * d * d +
+           (size_t)lmax * (token_rec_floats(d) + d + 16);
 }
 
 cudaError_t launch_scan_bwd(const BwdArgs &ba, int d, bool bf16, cudaStream_t st)
