@@ -61,7 +61,8 @@ struct BwdCfg {
     static constexpr int CPT = D / TPR;     // gain columns per thread
     static constexpr int RW = 32 / TPR;     // gain rows per warp
     static constexpr int CPL = (D + 31) / 32;
-    static constexpr int PS = 3 * D + 3;    // generation outputs k_raw v q_raw s_eta s_alpha
+    static constexpr int PS = 3 * D + 4;    // generation outputs k_raw v q_raw s_eta s_alpha
+                                            // (16-byte rows)
     static constexpr int NSC = 16;          // scalars per token
     static constexpr int TRS = token_rec_floats(D);  // token record: k q delta, raw scalars
     static constexpr int GRS = D + NSC;              // gain record: G_{t-1} k, scalars
@@ -83,8 +84,7 @@ struct BwdCfg {
     static constexpr int OFF_DG = OFF_KG + T * D;    // ddelta from the gain
     static constexpr int OFF_Y = OFF_DG + T * D;     // dy
     static constexpr int OFF_UV = OFF_Y + T * D;     // per (token, row): u = P k and <p, g>
-    static constexpr int OFF_W = OFF_UV + 2 * T * D; // per warp: dy | dk_raw | dv | dq_raw
-    static constexpr int OFF_PIX = OFF_W + NW * 4 * D;
+    static constexpr int OFF_PIX = OFF_UV + 2 * T * D;
     static constexpr int FLOATS = OFF_PIX + T;
     static constexpr size_t BYTES = (size_t)FLOATS * 4;
     static_assert(TPR * CPT == D && TPR <= 32, "gain thread map");
@@ -190,7 +190,7 @@ __global__ void __launch_bounds__(256, BwdCfg<D>::MINB) scan_bwd_kernel(const Bw
     float *S = sm + C::OFF_S, *dS = sm + C::OFF_DS, *GT = sm + C::OFF_GT;
     float *X = sm + C::OFF_X, *P = sm + C::OFF_P, *K = sm + C::OFF_K, *DL = sm + C::OFF_DL;
     float *Q = sm + C::OFF_Q, *Z = sm + C::OFF_Z, *SC = sm + C::OFF_SC, *KG = sm + C::OFF_KG;
-    float *DG = sm + C::OFF_DG, *Y = sm + C::OFF_Y, *UV = sm + C::OFF_UV, *Wv = sm + C::OFF_W;
+    float *DG = sm + C::OFF_DG, *Y = sm + C::OFF_Y, *UV = sm + C::OFF_UV;
     int *PIX = reinterpret_cast<int *>(sm + C::OFF_PIX);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -558,6 +558,8 @@ __global__ void __launch_bounds__(256, BwdCfg<D>::MINB) scan_bwd_kernel(const Bw
                     *z4 = make_float4(g4.x + d4.x, g4.y + d4.y, g4.z + d4.z, g4.w + d4.w);
                     reinterpret_cast<float4 *>(KG)[e] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
                 }
+                if (lam)  // dy = lambda_r dout
+                    for (int e = tid; e < Lt * D; e += C::NT) Y[e] *= lam[e % D];
                 if constexpr (sizeof(XT) != 4) {
                     for (int e = tid; e < Lt * VPT; e += C::NT) {
                         const uint4 raw = *reinterpret_cast<const uint4 *>(xraw + (size_t)e * 16);
@@ -639,135 +641,157 @@ __global__ void __launch_bounds__(256, BwdCfg<D>::MINB) scan_bwd_kernel(const Bw
                 }
             }
             __syncthreads();
-            // d. per-token adjoints, one warp per token
-            for (int j = warp; j < Lt; j += C::NW) {
-                const float *sc = SC + j * C::NSC;
-                const int pix = __float_as_int(sc[C::S_PIX]);
-                float *wv = Wv + warp * 4 * D;  // dy | dk_raw | dv | dq_raw
-                float dy[C::CPL], kk[C::CPL], qv[C::CPL], dl[C::CPL];
-#pragma unroll
-                for (int m = 0; m < C::CPL; ++m) {
-                    const int c = lane + 32 * m;
-                    const bool ok = c < D;
-                    dy[m] = ok ? (lam ? lam[c] : 1.0f) * Y[j * D + c] : 0.0f;  // dy = lambda_r dout
-                    kk[m] = ok ? K[j * D + c] : 0.0f;
-                    qv[m] = ok ? Q[j * D + c] : 0.0f;
-                    dl[m] = ok ? DL[j * D + c] : 0.0f;
-                    if (ok) wv[c] = dy[m];
-                }
-                __syncwarp();
+            // d. per-token adjoints; a warp takes two tokens at a time (j and j + NW) so
+            // that every load of the state serves both
+            for (int j0 = warp; j0 < Lt; j0 += 2 * C::NW) {
+                const bool two = j0 + C::NW < Lt;
+                const int jt[2] = {j0, two ? j0 + C::NW : j0};
                 // readout adjoint: dq = M^m_b^T dy
-                float dq[C::CPL];
+                float dq[2][C::CPL];
 #pragma unroll
                 for (int m = 0; m < C::CPL; ++m) {
                     const int c = lane + 32 * m;
-                    float acc = 0.0f;
+                    float a0 = 0.0f, a1 = 0.0f, b0 = 0.0f, b1 = 0.0f;
                     if (c < D) {
-#pragma unroll 2
+#pragma unroll 4
                         for (int i = 0; i < D; i += 4) {
-                            const float4 w4 = *reinterpret_cast<const float4 *>(wv + i);
-                            acc = fmaf(S[(3 * D + i) * C::SS + c], w4.x, acc);
-                            acc = fmaf(S[(3 * D + i + 1) * C::SS + c], w4.y, acc);
-                            acc = fmaf(S[(3 * D + i + 2) * C::SS + c], w4.z, acc);
-                            acc = fmaf(S[(3 * D + i + 3) * C::SS + c], w4.w, acc);
+                            const float4 ya = *reinterpret_cast<const float4 *>(Y + jt[0] * D + i);
+                            const float4 yb = *reinterpret_cast<const float4 *>(Y + jt[1] * D + i);
+                            const float *sm0 = S + (3 * D + i) * C::SS + c;
+                            const float s0 = sm0[0], s1 = sm0[C::SS], s2 = sm0[2 * C::SS], s3 = sm0[3 * C::SS];
+                            a0 = fmaf(s0, ya.x, a0);
+                            a1 = fmaf(s1, ya.y, a1);
+                            a0 = fmaf(s2, ya.z, a0);
+                            a1 = fmaf(s3, ya.w, a1);
+                            b0 = fmaf(s0, yb.x, b0);
+                            b1 = fmaf(s1, yb.y, b1);
+                            b0 = fmaf(s2, yb.z, b0);
+                            b1 = fmaf(s3, yb.w, b1);
                         }
                     }
-                    dq[m] = acc;
+                    dq[0][m] = a0 + a1;
+                    dq[1][m] = b0 + b1;
                 }
-                // the gain's step and retention adjoints: deta_t = -z_t . u_t,
-                // dalpha_t = <P_t, G_{t-1}> (row shares summed)
-                float det = 0.0f, dag = 0.0f;
+                int pixt[2];
 #pragma unroll
-                for (int m = 0; m < C::CPL; ++m) {
-                    const int c = lane + 32 * m;
-                    if (c < D) {
-                        det = fmaf(-Z[j * D + c], UV[j * D + c], det);
-                        dag += UV[(C::T + j) * D + c];
-                    }
-                }
-                det = warp_sum(det);
-                dag = warp_sum(dag);
-                // executed step and gates
-                float deta = 0.0f, dalpha = dag, dkn2 = 0.0f, ddd = 0.0f;
-                if (a.gate_mode != VH_GATE_FORCED_EXEC) {
-                    if (sc[C::S_BR] != 0.0f) {  // spectral limit executed
-                        const float kn2 = sc[C::S_KN2];
-                        const float fl = fmaxf(kn2, a.kk_floor);
-                        dalpha += det * a.spec_factor * 2.0f / fl;
-                        if (kn2 > a.kk_floor) dkn2 -= det * sc[C::S_SPEC] / kn2;
-                    } else if (sc[C::S_INJ] > 0.0f) {  // soft injection cap
-                        const float einj = sc[C::S_INJ], eta = sc[C::S_ETA], rr = sc[C::S_R];
-                        const float x = eta / einj;
-                        const float ex = expf(-x);
-                        deta += det * ex;
-                        const float dinj = det * (-expm1f(-x) - x * ex);
-                        dalpha -= dinj * a.inj_factor / rr;  // eta_inj falls with alpha
-                        const float dr = -dinj * einj / rr;
-                        ddd += dr / (2.0f * sqrtf(sc[C::S_DD] + a.eps * a.eps));
-                    }
-                }
-                float dse = 0.0f, dsa = 0.0f;
-                if (a.gate_mode == VH_GATE_GENERATED) {
-                    dse = deta * a.gamma_eta / (1.0f + expf(-sc[C::S_SE]));  // softplus' = sigmoid
-                    dsa = dalpha * sc[C::S_AL] * sc[C::S_OMA];
-                }
-                // delta = k - v, the two normalisations
-                float dk[C::CPL], ddl[C::CPL];
-                float kdk = 0.0f, qdq = 0.0f;
+                for (int u = 0; u < 2; ++u) {
+                    const int j = jt[u];
+                    const float *sc = SC + j * C::NSC;
+                    pixt[u] = __float_as_int(sc[C::S_PIX]);
+                    float kk[C::CPL], qv[C::CPL], dl[C::CPL];
 #pragma unroll
-                for (int m = 0; m < C::CPL; ++m) {
-                    const int c = lane + 32 * m;
-                    const bool ok = c < D;
-                    ddl[m] = ok ? fmaf(2.0f * ddd, dl[m], DG[j * D + c]) : 0.0f;
-                    dk[m] = ok ? fmaf(2.0f * dkn2, kk[m], KG[j * D + c]) + ddl[m] : 0.0f;
-                    kdk = fmaf(kk[m], dk[m], kdk);
-                    qdq = fmaf(qv[m], dq[m], qdq);
-                }
-                kdk = warp_sum(kdk);
-                qdq = warp_sum(qdq);
-                const float nk = sc[C::S_NK], nq = sc[C::S_NQ];
-                float *gv = P + j * C::PS;  // generation adjoints dk_raw | dv | dq_raw | dse dsa
-#pragma unroll
-                for (int m = 0; m < C::CPL; ++m) {
-                    const int c = lane + 32 * m;
-                    if (c < D) {
-                        const float dkr = (dk[m] - kk[m] * kdk) / nk;
-                        const float dqr = (dq[m] - qv[m] * qdq) / nq;
-                        wv[D + c] = dkr;
-                        wv[2 * D + c] = -ddl[m];
-                        wv[3 * D + c] = dqr;
-                        gv[c] = dkr;
-                        gv[D + c] = -ddl[m];
-                        gv[2 * D + c] = dqr;
+                    for (int m = 0; m < C::CPL; ++m) {
+                        const int c = lane + 32 * m;
+                        const bool ok = c < D;
+                        kk[m] = ok ? K[j * D + c] : 0.0f;
+                        qv[m] = ok ? Q[j * D + c] : 0.0f;
+                        dl[m] = ok ? DL[j * D + c] : 0.0f;
                     }
-                }
-                if (lane == 0) {
-                    gv[3 * D] = dse;
-                    gv[3 * D + 1] = dsa;
+                    // the gain's step and retention adjoints: deta_t = -z_t . u_t,
+                    // dalpha_t = <P_t, G_{t-1}> (row shares summed)
+                    float det = 0.0f, dag = 0.0f;
+#pragma unroll
+                    for (int m = 0; m < C::CPL; ++m) {
+                        const int c = lane + 32 * m;
+                        if (c < D) {
+                            det = fmaf(-Z[j * D + c], UV[j * D + c], det);
+                            dag += UV[(C::T + j) * D + c];
+                        }
+                    }
+                    det = warp_sum(det);
+                    dag = warp_sum(dag);
+                    // executed step and gates
+                    float deta = 0.0f, dalpha = dag, dkn2 = 0.0f, ddd = 0.0f;
+                    if (a.gate_mode != VH_GATE_FORCED_EXEC) {
+                        if (sc[C::S_BR] != 0.0f) {  // spectral limit executed
+                            const float kn2 = sc[C::S_KN2];
+                            const float fl = fmaxf(kn2, a.kk_floor);
+                            dalpha += det * a.spec_factor * 2.0f / fl;
+                            if (kn2 > a.kk_floor) dkn2 -= det * sc[C::S_SPEC] / kn2;
+                        } else if (sc[C::S_INJ] > 0.0f) {  // soft injection cap
+                            const float einj = sc[C::S_INJ], eta = sc[C::S_ETA], rr = sc[C::S_R];
+                            const float x = eta / einj;
+                            const float ex = expf(-x);
+                            deta += det * ex;
+                            const float dinj = det * (-expm1f(-x) - x * ex);
+                            dalpha -= dinj * a.inj_factor / rr;  // eta_inj falls with alpha
+                            const float dr = -dinj * einj / rr;
+                            ddd += dr / (2.0f * sqrtf(sc[C::S_DD] + a.eps * a.eps));
+                        }
+                    }
+                    float dse = 0.0f, dsa = 0.0f;
+                    if (a.gate_mode == VH_GATE_GENERATED) {
+                        dse = deta * a.gamma_eta / (1.0f + expf(-sc[C::S_SE]));  // softplus' = sigmoid
+                        dsa = dalpha * sc[C::S_AL] * sc[C::S_OMA];
+                    }
+                    // delta = k - v, the two normalisations
+                    float dk[C::CPL], ddl[C::CPL];
+                    float kdk = 0.0f, qdq = 0.0f;
+#pragma unroll
+                    for (int m = 0; m < C::CPL; ++m) {
+                        const int c = lane + 32 * m;
+                        const bool ok = c < D;
+                        ddl[m] = ok ? fmaf(2.0f * ddd, dl[m], DG[j * D + c]) : 0.0f;
+                        dk[m] = ok ? fmaf(2.0f * dkn2, kk[m], KG[j * D + c]) + ddl[m] : 0.0f;
+                        kdk = fmaf(kk[m], dk[m], kdk);
+                        qdq = fmaf(qv[m], dq[u][m], qdq);
+                    }
+                    kdk = warp_sum(kdk);
+                    qdq = warp_sum(qdq);
+                    const float nk = sc[C::S_NK], nq = sc[C::S_NQ];
+                    float *gv = P + j * C::PS;  // generation adjoints dk_raw | dv | dq_raw | dse dsa
+                    if (u == 0 || two) {
+#pragma unroll
+                        for (int m = 0; m < C::CPL; ++m) {
+                            const int c = lane + 32 * m;
+                            if (c < D) {
+                                gv[c] = (dk[m] - kk[m] * kdk) / nk;
+                                gv[D + c] = -ddl[m];
+                                gv[2 * D + c] = (dq[u][m] - qv[m] * qdq) / nq;
+                            }
+                        }
+                        if (lane == 0) {
+                            gv[3 * D] = dse;
+                            gv[3 * D + 1] = dsa;
+                        }
+                    }
                 }
                 __syncwarp();
                 // dx_t = M^k^T dk_raw + M^v^T dv + M^q^T dq_raw + m^eta dse + m^alpha dsa
+                const float *ga = P + jt[0] * C::PS, *gb = P + jt[1] * C::PS;
 #pragma unroll
                 for (int m = 0; m < C::CPL; ++m) {
                     const int c = lane + 32 * m;
                     if (c < D) {
-                        float acc = fmaf(S[(4 * D) * C::SS + c], dse, S[(4 * D + 1) * C::SS + c] * dsa);
+                        const float se = S[(4 * D) * C::SS + c], sl = S[(4 * D + 1) * C::SS + c];
+                        float a0 = fmaf(se, ga[3 * D], sl * ga[3 * D + 1]), a1 = 0.0f, a2 = 0.0f;
+                        float b0 = fmaf(se, gb[3 * D], sl * gb[3 * D + 1]), b1 = 0.0f, b2 = 0.0f;
 #pragma unroll 2
                         for (int i = 0; i < D; i += 4) {
-                            const float4 wk = *reinterpret_cast<const float4 *>(wv + D + i);
-                            const float4 wvv = *reinterpret_cast<const float4 *>(wv + 2 * D + i);
-                            const float4 wq = *reinterpret_cast<const float4 *>(wv + 3 * D + i);
-                            const float wka[4] = {wk.x, wk.y, wk.z, wk.w};
-                            const float wva[4] = {wvv.x, wvv.y, wvv.z, wvv.w};
-                            const float wqa[4] = {wq.x, wq.y, wq.z, wq.w};
+                            const float4 ka = *reinterpret_cast<const float4 *>(ga + i);
+                            const float4 va = *reinterpret_cast<const float4 *>(ga + D + i);
+                            const float4 qa = *reinterpret_cast<const float4 *>(ga + 2 * D + i);
+                            const float4 kb = *reinterpret_cast<const float4 *>(gb + i);
+                            const float4 vb = *reinterpret_cast<const float4 *>(gb + D + i);
+                            const float4 qb = *reinterpret_cast<const float4 *>(gb + 2 * D + i);
+                            const float kaa[4] = {ka.x, ka.y, ka.z, ka.w}, vaa[4] = {va.x, va.y, va.z, va.w};
+                            const float qaa[4] = {qa.x, qa.y, qa.z, qa.w}, kba[4] = {kb.x, kb.y, kb.z, kb.w};
+                            const float vba[4] = {vb.x, vb.y, vb.z, vb.w}, qba[4] = {qb.x, qb.y, qb.z, qb.w};
 #pragma unroll
-                            for (int u = 0; u < 4; ++u) {
-                                acc = fmaf(S[(i + u) * C::SS + c], wka[u], acc);
-                                acc = fmaf(S[(D + i + u) * C::SS + c], wva[u], acc);
-                                acc = fmaf(S[(2 * D + i + u) * C::SS + c], wqa[u], acc);
+                            for (int w = 0; w < 4; ++w) {
+                                const float sk = S[(i + w) * C::SS + c];
+                                const float sv = S[(D + i + w) * C::SS + c];
+                                const float sq = S[(2 * D + i + w) * C::SS + c];
+                                a0 = fmaf(sk, kaa[w], a0);
+                                a1 = fmaf(sv, vaa[w], a1);
+                                a2 = fmaf(sq, qaa[w], a2);
+                                b0 = fmaf(sk, kba[w], b0);
+                                b1 = fmaf(sv, vba[w], b1);
+                                b2 = fmaf(sq, qba[w], b2);
                             }
                         }
-                        atomicAdd(dxb + (size_t)pix * Cc + c, acc);
+                        atomicAdd(dxb + (size_t)pixt[0] * Cc + c, (a0 + a1) + a2);
+                        if (two) atomicAdd(dxb + (size_t)pixt[1] * Cc + c, (b0 + b1) + b2);
                     }
                 }
                 __syncwarp();
@@ -788,13 +812,6 @@ __global__ void __launch_bounds__(256, BwdCfg<D>::MINB) scan_bwd_kernel(const Bw
                     a1 = fmaf(g, u.y, a1);
                     a2 = fmaf(g, u.z, a2);
                     a3 = fmaf(g, u.w, a3);
-                }
-                if (rd && lam) {  // Y holds dout: dy = lambda_r dout
-                    const float l = lam[o - 3 * D];
-                    a0 *= l;
-                    a1 *= l;
-                    a2 *= l;
-                    a3 *= l;
                 }
                 float *dd = dS + o * C::SS + j4;
                 dd[0] += a0;
