@@ -340,9 +340,8 @@ __global__ void __launch_bounds__(256, BwdCfg<D>::MINB) scan_bwd_kernel(const Bw
         for (int e = tid; e < Lt * (D / 4); e += C::NT) {
             const int j = e / (D / 4), f = (e % (D / 4)) * 4;
             const float *tk = tr + (size_t)j * C::TRS;
-            *reinterpret_cast<float4 *>(K + j * D + f) = __ldg(reinterpret_cast<const float4 *>(tk + f));
-            *reinterpret_cast<float4 *>(DL + j * D + f) =
-                __ldg(reinterpret_cast<const float4 *>(tk + 2 * D + f));
+            cp_async16(K + j * D + f, tk + f);
+            cp_async16(DL + j * D + f, tk + 2 * D + f);
         }
         if (tid < Lt) {
             const float *ts = tr + (size_t)tid * C::TRS + 3 * D;
@@ -350,6 +349,7 @@ __global__ void __launch_bounds__(256, BwdCfg<D>::MINB) scan_bwd_kernel(const Bw
                              sqrtf(ts[TR_QQ] + a.knorm_eps), ts[TR_SE], ts[TR_SA], ts[TR_KN2],
                              ts[TR_DD], route_pixel(r, c0 + t0 + tid, H, W));
         }
+        cp_async_wait_all();
         __syncthreads();
     };
     auto gain_tile = [&](int t0, int Lt, bool record) {
