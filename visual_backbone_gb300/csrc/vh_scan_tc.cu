@@ -394,13 +394,9 @@ __global__ void __launch_bounds__(NT, 3)
                         dd4[e] = make_float4(vv[4 * e], vv[4 * e + 1], vv[4 * e + 2], vv[4 * e + 3]);
                     }
                     SC[jr] = make_float4(se, sa, kn2, dd2);
-                    if (kAbl && a.rec) {  // token record (backward support)
+                    if (kAbl && a.rec) {  // token record scalars (backward support); the
+                                          // vectors follow while the gain runs
                         float4 *rd = reinterpret_cast<float4 *>(rec_at(a, c * Lline + t0 + jr));
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            rd[e] = make_float4(kr[4 * e], kr[4 * e + 1], kr[4 * e + 2], kr[4 * e + 3]);
-                            rd[2 * D / 4 + e] = make_float4(vv[4 * e], vv[4 * e + 1], vv[4 * e + 2], vv[4 * e + 3]);
-                        }
                         rd[3 * D / 4] = make_float4(kkr, se, sa, kn2);
                         rd[3 * D / 4 + 1].x = dd2;
                     }
@@ -768,12 +764,18 @@ __global__ void __launch_bounds__(NT, 3)
                     const float rq = __frsqrt_rn(qqr + a.knorm_eps);
 #pragma unroll
                     for (int e = 0; e < 32; ++e) qr[e] *= rq;
-                    if (kAbl && a.rec && valid) {  // the query of the token record
+                    if (kAbl && a.rec && valid) {  // the token record's vectors: k and delta
+                                                   // from their tiles (read-only here), q
                         float *rq4 = rec_at(a, c * Lline + t0 + jr);
-                        float4 *qd = reinterpret_cast<float4 *>(rq4 + D);
+                        float4 *rd = reinterpret_cast<float4 *>(rq4);
+                        const float4 *ks = reinterpret_cast<const float4 *>(Kf + jr * KS);
+                        const float4 *ds = reinterpret_cast<const float4 *>(DLf + jr * KS);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            qd[e] = make_float4(qr[4 * e], qr[4 * e + 1], qr[4 * e + 2], qr[4 * e + 3]);
+                        for (int e = 0; e < 8; ++e) {
+                            rd[e] = ks[e];
+                            rd[D / 4 + e] = make_float4(qr[4 * e], qr[4 * e + 1], qr[4 * e + 2], qr[4 * e + 3]);
+                            rd[2 * D / 4 + e] = ds[e];
+                        }
                         rq4[3 * D + TR_QQ] = qqr;
                     }
 #pragma unroll
