@@ -297,9 +297,10 @@ def cpu_cores():
         return os.cpu_count() or 1
 
 
-def time_grad_oracle(wl, images):
+def time_grad_oracle(wl, images, min_seconds=0.0, max_passes=1000):
     """Tokens/s of the gradient oracle (fp64 autograd of the restated forward) on the
-    first `images` images; returns (tokens/s, seconds, torch threads)."""
+    first `images` images, repeated until `min_seconds` of wall time have passed;
+    returns (tokens/s, seconds, torch threads, passes)."""
     import numpy as np
     import torch
     from oracle import vh_grad
@@ -307,15 +308,22 @@ def time_grad_oracle(wl, images):
     inp = synth.make_inputs(wl, batch=images)
     dout = np.random.default_rng(7).standard_normal(inp.x64.shape)
     p = __import__("oracle").OracleParams(eta_bias=wl.eta_bias, alpha_init=wl.alpha_init)
+    m64 = inp.mem0.astype(np.float64)
     t0 = time.perf_counter()
-    vh_grad.backward(inp.x64, inp.mem0.astype(np.float64), dout, wl.H, wl.W, wl.nh, wl.d,
-                     chunk_len=wl.chunk, params=p)
-    dt = time.perf_counter() - t0
-    return images * wl.N / dt, dt, torch.get_num_threads()
+    passes = 0
+    while True:
+        vh_grad.backward(inp.x64, m64, dout, wl.H, wl.W, wl.nh, wl.d, chunk_len=wl.chunk, params=p)
+        passes += 1
+        dt = time.perf_counter() - t0
+        if dt >= min_seconds or passes >= max_passes:
+            break
+    return passes * images * wl.N / dt, dt, torch.get_num_threads(), passes
 
 
-def time_block_oracle(wl, images):
-    """Tokens/s of the block oracle on the first `images` images."""
+def time_block_oracle(wl, images, min_seconds=0.0, max_passes=1000):
+    """Tokens/s of the block oracle on the first `images` images, repeated until
+    `min_seconds` of wall time have passed; returns (tokens/s, seconds, threads,
+    passes)."""
     import numpy as np
     import oracle
     from oracle import vh_block as vb
@@ -327,12 +335,17 @@ def time_block_oracle(wl, images):
                             skip=inp["skip"].astype(np.float64),
                             dir_scale=inp["dir_scale"].astype(np.float64))
     cores = min(cpu_cores(), images * wl.nh)
+    x64, w64 = inp["x"].astype(np.float64), vb.weights_from(inp["weights"])
+    m64 = inp["mem0"].astype(np.float64)
     t0 = time.perf_counter()
-    vb.block_forward(inp["x"].astype(np.float64), vb.weights_from(inp["weights"]),
-                     inp["mem0"].astype(np.float64), wl.H, wl.W, inp["nh"], wl.d, p,
-                     nthreads=cores)
-    dt = time.perf_counter() - t0
-    return images * wl.N / dt, dt, cores
+    passes = 0
+    while True:
+        vb.block_forward(x64, w64, m64, wl.H, wl.W, inp["nh"], wl.d, p, nthreads=cores)
+        passes += 1
+        dt = time.perf_counter() - t0
+        if dt >= min_seconds or passes >= max_passes:
+            break
+    return passes * images * wl.N / dt, dt, cores, passes
 
 
 def run_reference(args, wl):
@@ -343,7 +356,8 @@ def run_reference(args, wl):
         return run_reference_backward(args, wl)
     if args.pass_ == "block":
         return run_reference_block(args, wl)
-    images = args.ref_images
+    # forward: enough images per step that every host core has an (image, head) scan job
+    images = args.ref_images or min(wl.B, -(-cpu_cores() // wl.nh))
     cores = min(cpu_cores(), images * wl.nh)
     for _ in range(args.warmup):
         time_oracle(wl, images, cores)
@@ -371,12 +385,13 @@ def run_reference(args, wl):
 
 
 def run_reference_backward(args, wl):
+    args.ref_images = args.ref_images or 1
     for _ in range(args.warmup):
         time_grad_oracle(wl, args.ref_images)
     times, cores = [], 1
     t_start = time.perf_counter()
     for _ in range(args.steps):
-        _, dt, cores = time_grad_oracle(wl, args.ref_images)
+        _, dt, cores, _ = time_grad_oracle(wl, args.ref_images)
         times.append(dt)
     total = sum(times)
     value = args.steps * args.ref_images * wl.N / total
@@ -397,12 +412,13 @@ def run_reference_backward(args, wl):
 
 
 def run_reference_block(args, wl):
+    args.ref_images = args.ref_images or 1
     for _ in range(args.warmup):
         time_block_oracle(wl, args.ref_images)
     times, cores = [], 1
     t_start = time.perf_counter()
     for _ in range(args.steps):
-        _, dt, cores = time_block_oracle(wl, args.ref_images)
+        _, dt, cores, _ = time_block_oracle(wl, args.ref_images)
         times.append(dt)
     total = sum(times)
     value = args.steps * args.ref_images * wl.N / total
@@ -721,11 +737,11 @@ def run_backward(args, wl):
             "clocks": sampler.summary(t0, t1) if sampler else None,
         }
         if world == 1 and not args.no_cpu_baseline:
-            v, dt, cores = time_grad_oracle(wl, 1)
+            v, dt, cores, passes = time_grad_oracle(wl, 1, min_seconds=10.0)
             line["cpu_baseline"] = {
                 "value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
-                "sample": f"1 of {wl.B} images (all 4 routes x {wl.nh} heads), fp64 gradient "
-                          f"oracle, {dt:.1f} s wall"}
+                "sample": f"{passes} pass(es) over 1 of {wl.B} images (all 4 routes x {wl.nh} "
+                          f"heads), fp64 gradient oracle, {dt:.1f} s wall"}
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
@@ -842,10 +858,13 @@ def run_block(args, wl):
             "clocks": sampler.summary(t0, t1) if sampler else None,
         }
         if world == 1 and not args.no_cpu_baseline:
-            v, dt, cores = time_block_oracle(wl, 1)
+            # enough images that every host core has an (image, head) scan job
+            imgs = min(wl.B, -(-cpu_cores() // wl.nh))
+            v, dt, cores, passes = time_block_oracle(wl, imgs, min_seconds=10.0)
             line["cpu_baseline"] = {
                 "value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
-                "sample": f"1 of {wl.B} images, fp64 block oracle, {dt:.1f} s wall"}
+                "sample": f"{passes} pass(es) over {imgs} of {wl.B} images, fp64 block oracle, "
+                          f"{dt:.1f} s wall"}
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
@@ -874,7 +893,9 @@ def main(argv=None):
     ap.add_argument("--cpu-images", type=int, default=16)
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="minimum wall time of the oracle sample behind cpu_baseline")
-    ap.add_argument("--ref-images", type=int, default=1)
+    ap.add_argument("--ref-images", type=int, default=0,
+                    help="images per step of the reference arm (0: forward, enough for every "
+                         "host core; backward and block, one)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
