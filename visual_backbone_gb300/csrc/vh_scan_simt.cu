@@ -44,6 +44,10 @@ struct SimtCfg {
     static constexpr int OFF_SC = OFF_Q + T * D;
     static constexpr int OFF_PIX = OFF_SC + 2 * T;
     static constexpr int FLOATS = OFF_PIX + T;
+    // the chunk-end copy of G starts at the first 16-byte boundary of the generation buffer
+    // and may run on into the key buffer (d = 64), never into the delta buffer
+    static constexpr int GS_PAD = (4 - OFF_P % 4) % 4;
+    static_assert(OFF_P + GS_PAD + D * D <= OFF_DL, "chunk-end G copy");
     static constexpr size_t BYTES = (size_t)FLOATS * 4;
     static_assert(T % JB == 0, "tile must hold whole register blocks");
     static_assert(D * D <= T * PS + T * D && OFF_K == OFF_P + T * PS,
@@ -275,13 +279,45 @@ __global__ void __launch_bounds__(256) scan_simt_kernel(const ScanArgs a)
         // 6. chunk end: every memory becomes M_b G (G in the generation buffer and, for
         // d = 64, the key buffer after it, which the gain loop reads until its last token)
         if constexpr (D * D > C::T * C::PS) __syncthreads();
-        float *Gs = P;
+        float *Gs = P + C::GS_PAD;
 #pragma unroll
         for (int c = 0; c < C::CPT; ++c) Gs[grow * D + gc0 + c] = G[c];
         __syncthreads();
+        int row_first = 0;  // state rows left to the four-row passes below
+        if constexpr (D == 64) {
+            // the four d x d memories in 8 x 8 register tiles: warp w owns rows 32w..32w+31,
+            // lane = (row group lane / 8) x (column group lane % 8), so every loaded entry of
+            // G serves eight rows and every state entry eight columns
+            const int r0 = warp * 32 + (lane >> 3) * 8, c0 = (lane & 7) * 8;
+            float acc[8][8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int m = 0; m < 8; ++m) acc[i][m] = 0.0f;
+#pragma unroll 2
+            for (int l = 0; l < D; ++l) {
+                const float4 g0 = *reinterpret_cast<const float4 *>(Gs + l * D + c0);
+                const float4 g1 = *reinterpret_cast<const float4 *>(Gs + l * D + c0 + 4);
+                const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float sv = S[(r0 + i) * C::SS + l];
+#pragma unroll
+                    for (int m = 0; m < 8; ++m) acc[i][m] = fmaf(sv, gv[m], acc[i][m]);
+                }
+            }
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if (frozen_row(a, r0 + i, D)) continue;
+#pragma unroll
+                for (int m = 0; m < 8; ++m) S[(r0 + i) * C::SS + c0 + m] = acc[i][m];
+            }
+            row_first = 4 * D;
+        }
         // four state rows per warp and pass: each loaded column entry of G serves four rows
         constexpr int RB = 4;
-        for (int o0 = warp * RB; o0 < C::R; o0 += C::NW * RB) {
+        for (int o0 = row_first + warp * RB; o0 < C::R; o0 += C::NW * RB) {
             float acc[RB][C::CPL];
 #pragma unroll
             for (int rr = 0; rr < RB; ++rr)
