@@ -28,7 +28,10 @@ struct SimtCfg {
     static constexpr int NW = NT / 32;
     static constexpr int R = 4 * D + 2;    // rows of the state: k, v, q, m (d each), eta, alpha
     static constexpr int RG = 3 * D + 2;   // rows used by the generation: k, v, q, eta, alpha
-    static constexpr int SS = D + 1;       // padded row stride of the state (bank-conflict free)
+    // padded row stride of the state: d + 1 keeps column walks over lane-distinct rows
+    // conflict-free; at d = 64 the rows are 16-byte aligned instead (d + 4), so every phase
+    // reads along a row with 16-byte vectors
+    static constexpr int SS = (D == 64) ? D + 4 : D + 1;
     static constexpr int T = (D == 64) ? 16 : 64;  // token tile (d = 64: two CTAs per SM)
     static constexpr int PS = RG + 1;      // row stride of the generation outputs
     static constexpr int TPR = NT / D;     // threads per gain row
@@ -48,6 +51,8 @@ struct SimtCfg {
     // and may run on into the key buffer (d = 64), never into the delta buffer
     static constexpr int GS_PAD = (4 - OFF_P % 4) % 4;
     static_assert(OFF_P + GS_PAD + D * D <= OFF_DL, "chunk-end G copy");
+    static_assert(D != 64 || (SS % 4 == 0 && OFF_X % 4 == 0 && OFF_P % 4 == 0 && OFF_Q % 4 == 0),
+                  "16-byte rows at d = 64");
     static constexpr size_t BYTES = (size_t)FLOATS * 4;
     static_assert(T % JB == 0, "tile must hold whole register blocks");
     static_assert(D * D <= T * PS + T * D && OFF_K == OFF_P + T * PS,
@@ -56,7 +61,7 @@ struct SimtCfg {
 };
 
 template <int D, typename XT>
-__global__ void __launch_bounds__(256) scan_simt_kernel(const ScanArgs a)
+__device__ __forceinline__ void scan_simt_body(const ScanArgs &a)
 {
     using C = SimtCfg<D>;
     extern __shared__ float4 smem_f4[];
@@ -119,7 +124,29 @@ __global__ void __launch_bounds__(256) scan_simt_kernel(const ScanArgs a)
             __syncthreads();
 
             // 2. generation from the boundary state: P[j][o] = sum_i S[o][i] x_j[i]
-            {
+            if constexpr (D == 64) {
+                // thread = output o (the k, v, q rows and the two gate rows) for every token
+                // of the tile: the 16-token tile would leave most warps idle as blocks of JB
+                const int o = tid;
+                if (o < C::RG) {
+                    float acc[C::T];
+#pragma unroll
+                    for (int jj = 0; jj < C::T; ++jj) acc[jj] = 0.0f;
+                    const float *srow = S + (o < 3 * D ? o : o + D) * C::SS;
+#pragma unroll 1
+                    for (int i = 0; i < D; i += 4) {
+                        const float4 sv = *reinterpret_cast<const float4 *>(srow + i);
+#pragma unroll
+                        for (int jj = 0; jj < C::T; ++jj) {
+                            const float4 xv = *reinterpret_cast<const float4 *>(X + jj * D + i);
+                            acc[jj] = fmaf(sv.w, xv.w, fmaf(sv.z, xv.z, fmaf(sv.y, xv.y, fmaf(sv.x, xv.x, acc[jj]))));
+                        }
+                    }
+#pragma unroll
+                    for (int jj = 0; jj < C::T; ++jj)
+                        if (jj < Lt) P[jj * C::PS + o] = acc[jj];
+                }
+            } else {
                 constexpr int OB = (C::RG + 31) / 32;
                 const int nJB = (Lt + C::JB - 1) / C::JB;
                 for (int item = warp; item < OB * nJB; item += C::NW) {
@@ -147,18 +174,33 @@ __global__ void __launch_bounds__(256) scan_simt_kernel(const ScanArgs a)
             }
             __syncthreads();
 
-            // 3. per-token normalisation and step control, one warp per token
-            for (int j = warp; j < Lt; j += C::NW) {
+            // 3. per-token normalisation and step control, one warp per token (half a warp
+            // at d = 64, so the 16-token tile takes one pass)
+            constexpr int LPT = (D == 64) ? 16 : 32;  // lanes per token
+            constexpr int TPW = 32 / LPT;             // tokens per warp and pass
+            const int sub = lane / LPT, sl = lane % LPT;
+            const unsigned smask = (LPT == 32) ? 0xffffffffu : (0xffffu << (16 * sub));
+            auto tsum = [&](float v) {
+                if constexpr (LPT == 32) {
+                    return warp_sum(v);
+                } else {
+#pragma unroll
+                    for (int o = LPT / 2; o > 0; o >>= 1) v += __shfl_xor_sync(smask, v, o);
+                    return v;
+                }
+            };
+            constexpr int CPT3 = (D + LPT - 1) / LPT;  // components per lane
+            for (int j = warp * TPW + sub; j < Lt; j += C::NW * TPW) {
                 const float *pr = P + j * C::PS;
-                float kr[C::CPL], vv[C::CPL], qr[C::CPL];
+                float kr[CPT3], vv[CPT3], qr[CPT3];
                 float kk = 0.0f, qq = 0.0f;
                 // VisionHOPE-exact readout: the query of the token's pixel, already
                 // normalised, from the outer projection's planes
                 const size_t qo = a.qhat ? ((size_t)b * N + PIX[j]) * Cc + (size_t)h * D : 0;
                 const size_t qplane = (size_t)a.B * N * Cc;
 #pragma unroll
-                for (int m = 0; m < C::CPL; ++m) {
-                    const int c = lane + 32 * m;
+                for (int m = 0; m < CPT3; ++m) {
+                    const int c = sl + LPT * m;
                     const bool ok = c < D;
                     kr[m] = ok ? pr[c] : 0.0f;
                     vv[m] = ok ? pr[D + c] : 0.0f;
@@ -166,21 +208,21 @@ __global__ void __launch_bounds__(256) scan_simt_kernel(const ScanArgs a)
                     kk = fmaf(kr[m], kr[m], kk);
                     qq = fmaf(qr[m], qr[m], qq);
                 }
-                kk = warp_sum(kk);
-                qq = warp_sum(qq);
+                kk = tsum(kk);
+                qq = tsum(qq);
                 const float nk = sqrtf(kk + a.knorm_eps);
                 const float nq = a.qhat ? 1.0f : sqrtf(qq + a.knorm_eps);
                 float kn2 = 0.0f, dd = 0.0f;
 #pragma unroll
-                for (int m = 0; m < C::CPL; ++m) {
+                for (int m = 0; m < CPT3; ++m) {
                     kr[m] = kr[m] / nk;
                     qr[m] = qr[m] / nq;
                     vv[m] = kr[m] - vv[m];  // delta = k - v
                     kn2 = fmaf(kr[m], kr[m], kn2);
                     dd = fmaf(vv[m], vv[m], dd);
                 }
-                kn2 = warp_sum(kn2);
-                dd = warp_sum(dd);
+                kn2 = tsum(kn2);
+                dd = tsum(dd);
                 float eta, alpha, oma;
                 gates(a, pr[3 * D], pr[3 * D + 1], eta, alpha, oma);
                 float eta_t;
@@ -189,19 +231,19 @@ __global__ void __launch_bounds__(256) scan_simt_kernel(const ScanArgs a)
                 } else {
                     const StepOut so = step_control(a, eta, alpha, oma, kn2, dd);
                     eta_t = so.eta_tilde;
-                    n_spec += (lane == 0 && so.spec_active);
-                    n_inj += (lane == 0 && so.inj_ratio_gt1);
+                    n_spec += (sl == 0 && so.spec_active);
+                    n_inj += (sl == 0 && so.inj_ratio_gt1);
                 }
 #pragma unroll
-                for (int m = 0; m < C::CPL; ++m) {
-                    const int c = lane + 32 * m;
+                for (int m = 0; m < CPT3; ++m) {
+                    const int c = sl + LPT * m;
                     if (c < D) {
                         K[j * D + c] = kr[m];
                         DL[j * D + c] = vv[m];
                         Q[j * D + c] = qr[m];
                     }
                 }
-                if (lane == 0) {
+                if (sl == 0) {
                     SC[2 * j] = alpha;
                     SC[2 * j + 1] = eta_t;
                 }
@@ -212,6 +254,34 @@ __global__ void __launch_bounds__(256) scan_simt_kernel(const ScanArgs a)
             // intra-chunk readout (ablation) the query is replaced by u_j = G_{j-1} q_j,
             // formed in the gain loop, and the readout follows it
             auto readout = [&](const float *Qv) {
+                if constexpr (D == 64) {
+                    // every warp: thread = output channel i, tokens tg, tg + TG, ...
+                    constexpr int TG = C::NT / D, JT = C::T / TG;
+                    const int i = tid % D, tg = tid / D;
+                    float acc[JT];
+#pragma unroll
+                    for (int jj = 0; jj < JT; ++jj) acc[jj] = 0.0f;
+                    const float *mrow = S + (3 * D + i) * C::SS;
+#pragma unroll 2
+                    for (int l = 0; l < D; l += 4) {
+                        const float4 mv = *reinterpret_cast<const float4 *>(mrow + l);
+#pragma unroll
+                        for (int jj = 0; jj < JT; ++jj) {
+                            const float4 qv = *reinterpret_cast<const float4 *>(Qv + (tg + TG * jj) * D + l);
+                            acc[jj] = fmaf(mv.w, qv.w, fmaf(mv.z, qv.z, fmaf(mv.y, qv.y, fmaf(mv.x, qv.x, acc[jj]))));
+                        }
+                    }
+                    const float lm = lam ? lam[i] : 1.0f;
+#pragma unroll
+                    for (int jj = 0; jj < JT; ++jj) {
+                        const int j = tg + TG * jj;
+                        if (j < Lt) {
+                            n_nf += !isfinite(acc[jj]);
+                            atomicAdd(ob + (size_t)PIX[j] * Cc + i, lm * acc[jj]);
+                        }
+                    }
+                    return;
+                }
                 const int nJB = (Lt + C::JB - 1) / C::JB;
                 for (int jb = warp; jb < nJB; jb += C::NW) {
                     const int j0 = jb * C::JB;
@@ -251,8 +321,15 @@ __global__ void __launch_bounds__(256) scan_simt_kernel(const ScanArgs a)
             for (int j = 0; j < Lt; ++j) {
                 const float *kj = K + j * D;
                 float part = 0.0f;
+                if constexpr (C::CPT >= 8) {  // four partial sums: a short dependent chain
+                    float p4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-                for (int c = 0; c < C::CPT; ++c) part = fmaf(G[c], kj[gc0 + c], part);
+                    for (int c = 0; c < C::CPT; ++c) p4[c & 3] = fmaf(G[c], kj[gc0 + c], p4[c & 3]);
+                    part = (p4[0] + p4[1]) + (p4[2] + p4[3]);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < C::CPT; ++c) part = fmaf(G[c], kj[gc0 + c], part);
+                }
 #pragma unroll
                 for (int o = C::TPR / 2; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
                 if (intra) {
@@ -286,32 +363,39 @@ __global__ void __launch_bounds__(256) scan_simt_kernel(const ScanArgs a)
         int row_first = 0;  // state rows left to the four-row passes below
         if constexpr (D == 64) {
             // the four d x d memories in 8 x 8 register tiles: warp w owns rows 32w..32w+31,
-            // lane = (row group lane / 8) x (column group lane % 8), so every loaded entry of
-            // G serves eight rows and every state entry eight columns
-            const int r0 = warp * 32 + (lane >> 3) * 8, c0 = (lane & 7) * 8;
+            // lane = (row group lane / 8) x (column group lane % 8); the row group takes the
+            // rows 4 apart (so the four groups' vector state reads hit distinct banks).  Every
+            // loaded entry of G serves eight rows and every state entry eight columns.
+            const int r0 = warp * 32 + (lane >> 3), c0 = (lane & 7) * 8;
             float acc[8][8];
 #pragma unroll
             for (int i = 0; i < 8; ++i)
 #pragma unroll
                 for (int m = 0; m < 8; ++m) acc[i][m] = 0.0f;
-#pragma unroll 2
-            for (int l = 0; l < D; ++l) {
-                const float4 g0 = *reinterpret_cast<const float4 *>(Gs + l * D + c0);
-                const float4 g1 = *reinterpret_cast<const float4 *>(Gs + l * D + c0 + 4);
-                const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+#pragma unroll 1
+            for (int l = 0; l < D; l += 2) {
+                float2 s2[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float sv = S[(r0 + i) * C::SS + l];
+                for (int i = 0; i < 8; ++i) s2[i] = *reinterpret_cast<const float2 *>(S + (r0 + 4 * i) * C::SS + l);
 #pragma unroll
-                    for (int m = 0; m < 8; ++m) acc[i][m] = fmaf(sv, gv[m], acc[i][m]);
+                for (int u = 0; u < 2; ++u) {
+                    const float4 g0 = *reinterpret_cast<const float4 *>(Gs + (l + u) * D + c0);
+                    const float4 g1 = *reinterpret_cast<const float4 *>(Gs + (l + u) * D + c0 + 4);
+                    const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const float sv = u == 0 ? s2[i].x : s2[i].y;
+#pragma unroll
+                        for (int m = 0; m < 8; ++m) acc[i][m] = fmaf(sv, gv[m], acc[i][m]);
+                    }
                 }
             }
             __syncwarp();
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                if (frozen_row(a, r0 + i, D)) continue;
+                if (frozen_row(a, r0 + 4 * i, D)) continue;
 #pragma unroll
-                for (int m = 0; m < 8; ++m) S[(r0 + i) * C::SS + c0 + m] = acc[i][m];
+                for (int m = 0; m < 8; ++m) S[(r0 + 4 * i) * C::SS + c0 + m] = acc[i][m];
             }
             row_first = 4 * D;
         }
@@ -376,10 +460,27 @@ __global__ void __launch_bounds__(256) scan_simt_kernel(const ScanArgs a)
 }
 
 template <int D, typename XT>
+__global__ void __launch_bounds__(256) scan_simt_kernel(const ScanArgs a)
+{
+    scan_simt_body<D, XT>(a);
+}
+
+// d = 64: two CTAs per SM (their shared memory fits twice), registers capped to match
+template <typename XT>
+__global__ void __launch_bounds__(256, 2) scan_simt_kernel_d64(const ScanArgs a)
+{
+    scan_simt_body<64, XT>(a);
+}
+
+template <int D, typename XT>
 static cudaError_t launch_simt_t(const ScanArgs &a, cudaStream_t st)
 {
     using C = SimtCfg<D>;
-    auto kern = scan_simt_kernel<D, XT>;
+    void (*kern)(const ScanArgs);
+    if constexpr (D == 64)
+        kern = scan_simt_kernel_d64<XT>;
+    else
+        kern = scan_simt_kernel<D, XT>;
     static int attr_set[64] = {0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
