@@ -125,26 +125,48 @@ __device__ __forceinline__ void scan_simt_body(const ScanArgs &a)
 
             // 2. generation from the boundary state: P[j][o] = sum_i S[o][i] x_j[i]
             if constexpr (D == 64) {
-                // thread = output o (the k, v, q rows and the two gate rows) for every token
-                // of the tile: the 16-token tile would leave most warps idle as blocks of JB
-                const int o = tid;
-                if (o < C::RG) {
-                    float acc[C::T];
+                // register tiles of 4 tokens x 4 outputs: thread (tg, og) takes tokens
+                // 4 tg..4 tg+3 and outputs og + 49 k (k, v, q rows and the two gate rows),
+                // so one 16-byte load of x serves four outputs and one of the state four
+                // tokens; consecutive og read rows 16 bytes apart in the bank space
+                constexpr int OG = (C::RG + 3) / 4;  // 49 output groups
+                static_assert(4 * 4 == C::T && 4 * OG >= C::RG && 4 * OG <= C::NT, "tiles");
+                if (tid < 4 * OG) {
+                    const int tg = tid / OG, og = tid % OG;
+                    int srow[4];  // state row offsets
 #pragma unroll
-                    for (int jj = 0; jj < C::T; ++jj) acc[jj] = 0.0f;
-                    const float *srow = S + (o < 3 * D ? o : o + D) * C::SS;
+                    for (int k = 0; k < 4; ++k) {
+                        const int o = min(og + OG * k, C::RG - 1);  // a padding output reads a real row
+                        srow[k] = (o < 3 * D ? o : o + D) * C::SS;
+                    }
+                    float acc[4][4];
+#pragma unroll
+                    for (int t = 0; t < 4; ++t)
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) acc[t][k] = 0.0f;
 #pragma unroll 1
                     for (int i = 0; i < D; i += 4) {
-                        const float4 sv = *reinterpret_cast<const float4 *>(srow + i);
+                        float4 sv[4], xv[4];
 #pragma unroll
-                        for (int jj = 0; jj < C::T; ++jj) {
-                            const float4 xv = *reinterpret_cast<const float4 *>(X + jj * D + i);
-                            acc[jj] = fmaf(sv.w, xv.w, fmaf(sv.z, xv.z, fmaf(sv.y, xv.y, fmaf(sv.x, xv.x, acc[jj]))));
-                        }
+                        for (int k = 0; k < 4; ++k) sv[k] = *reinterpret_cast<const float4 *>(S + srow[k] + i);
+#pragma unroll
+                        for (int t = 0; t < 4; ++t)
+                            xv[t] = *reinterpret_cast<const float4 *>(X + (4 * tg + t) * D + i);
+#pragma unroll
+                        for (int t = 0; t < 4; ++t)
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)
+                                acc[t][k] = fmaf(sv[k].w, xv[t].w,
+                                                 fmaf(sv[k].z, xv[t].z,
+                                                      fmaf(sv[k].y, xv[t].y, fmaf(sv[k].x, xv[t].x, acc[t][k]))));
                     }
 #pragma unroll
-                    for (int jj = 0; jj < C::T; ++jj)
-                        if (jj < Lt) P[jj * C::PS + o] = acc[jj];
+                    for (int t = 0; t < 4; ++t)
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const int o = og + OG * k, j = 4 * tg + t;
+                            if (o < C::RG && j < Lt) P[j * C::PS + o] = acc[t][k];
+                        }
                 }
             } else {
                 constexpr int OB = (C::RG + 31) / 32;
@@ -318,7 +340,43 @@ __device__ __forceinline__ void scan_simt_body(const ScanArgs &a)
             // DGD correction (ablation) the G k term drops: G <- alpha G - eta delta k^T.
             // The intra-chunk readout's u_j = G_{j-1} q_j goes to P (free after step 3).
             float *U = P;
-            for (int j = 0; j < Lt; ++j) {
+            if constexpr (C::CPT >= 8) {
+                // d = 64: the next token's key slice, delta entry and scalars are loaded
+                // while the current token is applied
+                if (!intra) {
+                    float kc[C::CPT], kn[C::CPT];
+                    auto ldk = [&](int j, float (&kv)[C::CPT]) {
+#pragma unroll
+                        for (int c = 0; c < C::CPT; c += 4) {
+                            const float4 f = *reinterpret_cast<const float4 *>(K + j * D + gc0 + c);
+                            kv[c] = f.x; kv[c + 1] = f.y; kv[c + 2] = f.z; kv[c + 3] = f.w;
+                        }
+                    };
+                    ldk(0, kc);
+                    float dlc = DL[grow];
+                    float2 scc = *reinterpret_cast<const float2 *>(SC);
+                    for (int j = 0; j < Lt; ++j) {
+                        const int jn = min(j + 1, Lt - 1);
+                        ldk(jn, kn);
+                        const float dln = DL[jn * D + grow];
+                        const float2 scn = *reinterpret_cast<const float2 *>(SC + 2 * jn);
+                        float p4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+                        for (int c = 0; c < C::CPT; ++c) p4[c & 3] = fmaf(G[c], kc[c], p4[c & 3]);
+                        float part = (p4[0] + p4[1]) + (p4[2] + p4[3]);
+#pragma unroll
+                        for (int o = C::TPR / 2; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+                        const float sg = scc.y * (part * dgd + dlc);
+#pragma unroll
+                        for (int c = 0; c < C::CPT; ++c) G[c] = fmaf(-sg, kc[c], scc.x * G[c]);
+#pragma unroll
+                        for (int c = 0; c < C::CPT; ++c) kc[c] = kn[c];
+                        dlc = dln;
+                        scc = scn;
+                    }
+                }
+            }
+            for (int j = 0; j < Lt && !(C::CPT >= 8 && !intra); ++j) {
                 const float *kj = K + j * D;
                 float part = 0.0f;
                 if constexpr (C::CPT >= 8) {  // four partial sums: a short dependent chain
