@@ -93,6 +93,12 @@ __device__ __forceinline__ void scan_simt_body(const ScanArgs &a)
     const bool intra = (a.control_flags & VH_CTRL_INTRA_READ) != 0;
     const int grow = tid / C::TPR;
     const int gc0 = (tid % C::TPR) * C::CPT;
+    // column of this thread's c-th gain entry: a contiguous slice, or at d = 64 four
+    // 4-column groups 4 TPR apart, so a row's lanes read their 16-byte key pieces from
+    // distinct banks
+    auto gcol = [&](int c) {
+        return C::CPT >= 8 ? 4 * (tid % C::TPR) + 4 * C::TPR * (c >> 2) + (c & 3) : gc0 + c;
+    };
     float G[C::CPT];
 
     const int Cr = route_chunk(r, a.chunk, H, W);
@@ -104,7 +110,7 @@ __device__ __forceinline__ void scan_simt_body(const ScanArgs &a)
     for (int c0 = 0; c0 < N; c0 += Cr) {
         const int L = min(Cr, N - c0);
 #pragma unroll
-        for (int c = 0; c < C::CPT; ++c) G[c] = (grow == gc0 + c) ? 1.0f : 0.0f;
+        for (int c = 0; c < C::CPT; ++c) G[c] = (grow == gcol(c)) ? 1.0f : 0.0f;
 
         for (int t0 = 0; t0 < L; t0 += C::T) {
             const int Lt = min(C::T, L - t0);
@@ -348,7 +354,7 @@ __device__ __forceinline__ void scan_simt_body(const ScanArgs &a)
                     auto ldk = [&](int j, float (&kv)[C::CPT]) {
 #pragma unroll
                         for (int c = 0; c < C::CPT; c += 4) {
-                            const float4 f = *reinterpret_cast<const float4 *>(K + j * D + gc0 + c);
+                            const float4 f = *reinterpret_cast<const float4 *>(K + j * D + gcol(c));
                             kv[c] = f.x; kv[c + 1] = f.y; kv[c + 2] = f.z; kv[c + 3] = f.w;
                         }
                     };
@@ -382,11 +388,11 @@ __device__ __forceinline__ void scan_simt_body(const ScanArgs &a)
                 if constexpr (C::CPT >= 8) {  // four partial sums: a short dependent chain
                     float p4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-                    for (int c = 0; c < C::CPT; ++c) p4[c & 3] = fmaf(G[c], kj[gc0 + c], p4[c & 3]);
+                    for (int c = 0; c < C::CPT; ++c) p4[c & 3] = fmaf(G[c], kj[gcol(c)], p4[c & 3]);
                     part = (p4[0] + p4[1]) + (p4[2] + p4[3]);
                 } else {
 #pragma unroll
-                    for (int c = 0; c < C::CPT; ++c) part = fmaf(G[c], kj[gc0 + c], part);
+                    for (int c = 0; c < C::CPT; ++c) part = fmaf(G[c], kj[gcol(c)], part);
                 }
 #pragma unroll
                 for (int o = C::TPR / 2; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
@@ -394,7 +400,7 @@ __device__ __forceinline__ void scan_simt_body(const ScanArgs &a)
                     const float *qj = Q + j * D;
                     float u = 0.0f;
 #pragma unroll
-                    for (int c = 0; c < C::CPT; ++c) u = fmaf(G[c], qj[gc0 + c], u);
+                    for (int c = 0; c < C::CPT; ++c) u = fmaf(G[c], qj[gcol(c)], u);
 #pragma unroll
                     for (int o = C::TPR / 2; o > 0; o >>= 1) u += __shfl_xor_sync(0xffffffffu, u, o);
                     if (gc0 == 0) U[j * D + grow] = u;
@@ -402,7 +408,7 @@ __device__ __forceinline__ void scan_simt_body(const ScanArgs &a)
                 const float s = SC[2 * j + 1] * (part * dgd + DL[j * D + grow]);
                 const float al = SC[2 * j];
 #pragma unroll
-                for (int c = 0; c < C::CPT; ++c) G[c] = fmaf(-s, kj[gc0 + c], al * G[c]);
+                for (int c = 0; c < C::CPT; ++c) G[c] = fmaf(-s, kj[gcol(c)], al * G[c]);
             }
             if (intra) {
                 __syncthreads();  // U complete
@@ -416,15 +422,16 @@ __device__ __forceinline__ void scan_simt_body(const ScanArgs &a)
         if constexpr (D * D > C::T * C::PS) __syncthreads();
         float *Gs = P + C::GS_PAD;
 #pragma unroll
-        for (int c = 0; c < C::CPT; ++c) Gs[grow * D + gc0 + c] = G[c];
+        for (int c = 0; c < C::CPT; ++c) Gs[grow * D + gcol(c)] = G[c];
         __syncthreads();
         int row_first = 0;  // state rows left to the four-row passes below
         if constexpr (D == 64) {
             // the four d x d memories in 8 x 8 register tiles: warp w owns rows 32w..32w+31,
             // lane = (row group lane / 8) x (column group lane % 8); the row group takes the
-            // rows 4 apart (so the four groups' vector state reads hit distinct banks).  Every
-            // loaded entry of G serves eight rows and every state entry eight columns.
-            const int r0 = warp * 32 + (lane >> 3), c0 = (lane & 7) * 8;
+            // rows 4 apart and the column group columns 4 cg..4 cg+3 and 32 + 4 cg..+3, so
+            // the vector reads of the state and of G hit distinct banks.  Every loaded entry
+            // of G serves eight rows and every state entry eight columns.
+            const int r0 = warp * 32 + (lane >> 3), c0 = (lane & 7) * 4;
             float acc[8][8];
 #pragma unroll
             for (int i = 0; i < 8; ++i)
@@ -438,7 +445,7 @@ __device__ __forceinline__ void scan_simt_body(const ScanArgs &a)
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
                     const float4 g0 = *reinterpret_cast<const float4 *>(Gs + (l + u) * D + c0);
-                    const float4 g1 = *reinterpret_cast<const float4 *>(Gs + (l + u) * D + c0 + 4);
+                    const float4 g1 = *reinterpret_cast<const float4 *>(Gs + (l + u) * D + 32 + c0);
                     const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
@@ -453,7 +460,7 @@ __device__ __forceinline__ void scan_simt_body(const ScanArgs &a)
             for (int i = 0; i < 8; ++i) {
                 if (frozen_row(a, r0 + 4 * i, D)) continue;
 #pragma unroll
-                for (int m = 0; m < 8; ++m) S[(r0 + 4 * i) * C::SS + c0 + m] = acc[i][m];
+                for (int m = 0; m < 8; ++m) S[(r0 + 4 * i) * C::SS + (m < 4 ? c0 + m : 28 + c0 + m)] = acc[i][m];
             }
             row_first = 4 * D;
         }
