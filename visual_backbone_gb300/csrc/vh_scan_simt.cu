@@ -462,7 +462,18 @@ __device__ __forceinline__ void scan_simt_body(const ScanArgs &a)
 #pragma unroll
                 for (int m = 0; m < 8; ++m) S[(r0 + 4 * i) * C::SS + (m < 4 ? c0 + m : 28 + c0 + m)] = acc[i][m];
             }
-            row_first = 4 * D;
+            // the eta and alpha rows on warps 0-3, one output each (row 4d + tid / d, column
+            // tid % d); every read of the two rows precedes every write (named barrier 1
+            // spans those four warps)
+            if (tid < 2 * D) {
+                const int row = 4 * D + tid / D, col = tid % D;
+                float ea = 0.0f;
+#pragma unroll 8
+                for (int l = 0; l < D; ++l) ea = fmaf(S[row * C::SS + l], Gs[l * D + col], ea);
+                asm volatile("bar.sync 1, %0;" ::"n"(2 * D) : "memory");
+                if (!frozen_row(a, row, D)) S[row * C::SS + col] = ea;
+            }
+            row_first = C::R;
         }
         // four state rows per warp and pass: each loaded column entry of G serves four rows
         constexpr int RB = 4;
