@@ -19,6 +19,9 @@ SHAPES = [
     ("tiny", synth.WORKLOADS["tiny"]),
     ("6x6x2x32", synth.Workload("a1", 2, 6, 6, 2, 32, 0, "bf16", seed=41, alpha_init=0.999)),
     ("5x70x2x32", synth.Workload("a2", 1, 5, 70, 2, 32, 0, "bf16", seed=42, eta_bias=3.0)),
+    # d = 64: the CUDA-core kernel's register-tiled update and its eta / alpha rows, three
+    # 16-token tiles per row
+    ("3x40x1x64", synth.Workload("a5", 1, 3, 40, 1, 64, 0, "bf16", seed=48, alpha_init=0.999)),
 ]
 
 
@@ -33,14 +36,13 @@ def test_ablation_parity(orc, vhlib, impl, flag, name, wl):
 
 
 @pytest.mark.parametrize("impl", IMPLS)
-def test_frozen_memories_unchanged_on_gpu(vhlib, impl):
-    import torch
+@pytest.mark.parametrize("H,W,nh,d", [(6, 6, 2, 32), (3, 40, 1, 64)])
+def test_frozen_memories_unchanged_on_gpu(vhlib, impl, H, W, nh, d):
     from tests._helpers import run_gpu
-    wl = synth.Workload("a3", 1, 6, 6, 2, 32, 0, "bf16", seed=43, alpha_init=0.999)
+    wl = synth.Workload("a3", 1, H, W, nh, d, 0, "bf16", seed=43, alpha_init=0.999)
     inp = synth.make_inputs(wl)
     vhp = vhlib.ScanParams(alpha_init=wl.alpha_init, impl=impl, control_flags=32 | 64)
     g = run_gpu(vhlib, inp, params=vhp, want_memories=True)
-    d = wl.d
     mo = g["mem"][0]
     m0 = inp.mem0
     for r in range(4):
