@@ -22,6 +22,23 @@
 
 namespace vh {
 
+// Packed fp32 pairs for fma.rn.f32x2: lane 0 in the low word.
+__device__ __forceinline__ unsigned long long pack_f32x2(float lo, float hi)
+{
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void unpack_f32x2(unsigned long long v, float &lo, float &hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+// d = a * b + d on both lanes, each an fp32 fma rounded to nearest
+__device__ __forceinline__ void fma_f32x2(unsigned long long &d, unsigned long long a, unsigned long long b)
+{
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
+}
+
 template <int D>
 struct SimtCfg {
     static constexpr int NT = 256;
@@ -433,11 +450,13 @@ __device__ __forceinline__ void scan_simt_body(const ScanArgs &a)
             // the vector reads of the state and of G hit distinct banks.  Every loaded entry
             // of G serves eight rows and every state entry eight columns.
             const int r0 = warp * 32 + (lane >> 3), c0 = (lane & 7) * 4;
-            float acc[8][8];
+            // pairs of adjacent columns accumulate in packed fp32x2 FMAs (each half an fp32
+            // fma rounded to nearest, as fmaf), half the FMA issue slots of scalar FMAs
+            unsigned long long acc2[8][4];
 #pragma unroll
             for (int i = 0; i < 8; ++i)
 #pragma unroll
-                for (int m = 0; m < 8; ++m) acc[i][m] = 0.0f;
+                for (int m = 0; m < 4; ++m) acc2[i][m] = 0ull;
 #pragma unroll 1
             for (int l = 0; l < D; l += 2) {
                 float2 s2[8];
@@ -447,15 +466,22 @@ __device__ __forceinline__ void scan_simt_body(const ScanArgs &a)
                 for (int u = 0; u < 2; ++u) {
                     const float4 g0 = *reinterpret_cast<const float4 *>(Gs + (l + u) * D + c0);
                     const float4 g1 = *reinterpret_cast<const float4 *>(Gs + (l + u) * D + 32 + c0);
-                    const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+                    const unsigned long long gp[4] = {pack_f32x2(g0.x, g0.y), pack_f32x2(g0.z, g0.w),
+                                                      pack_f32x2(g1.x, g1.y), pack_f32x2(g1.z, g1.w)};
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         const float sv = u == 0 ? s2[i].x : s2[i].y;
+                        const unsigned long long sp = pack_f32x2(sv, sv);
 #pragma unroll
-                        for (int m = 0; m < 8; ++m) acc[i][m] = fmaf(sv, gv[m], acc[i][m]);
+                        for (int m = 0; m < 4; ++m) fma_f32x2(acc2[i][m], sp, gp[m]);
                     }
                 }
             }
+            float acc[8][8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int m = 0; m < 4; ++m) unpack_f32x2(acc2[i][m], acc[i][2 * m], acc[i][2 * m + 1]);
             __syncwarp();
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
