@@ -610,6 +610,14 @@ def run_ours(args, wl):
                 "value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
                 "sample": f"{passes} pass(es) over {args.cpu_images} of {wl.B} images of the "
                           f"workload (all 4 routes x {wl.nh} heads), fp64, {dt:.1f} s wall"}
+            # the same oracle on one host thread (one image, about 3 s)
+            v1, dt1, passes1 = time_oracle(
+                wl, 1, 1, min_seconds=3.0,
+                w_query=extra["w_query"].double().cpu().numpy() if extra else None,
+                skip=extra["skip"].double().cpu().numpy() if extra else None)
+            line["cpu_baseline"]["single_thread"] = {
+                "value": v1, "unit": UNIT, "cores": 1,
+                "sample": f"{passes1} pass(es) over 1 image, fp64, {dt1:.1f} s wall"}
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
