@@ -15,9 +15,12 @@
 //      whose rows evolve independently,
 //   6. at the chunk end replaces every memory by M_b G (Eq. (46)).
 // Long chunks are processed in token tiles; the gain carries across tiles.
-// All arithmetic is fp32 on CUDA cores; this kernel is the simple, general
-// path (any head_dim in {16,32,64}, any chunk length) and the A/B reference
-// for the tensor-core kernel.
+// All arithmetic is fp32 on CUDA cores; this kernel is the general path (any
+// head_dim in {16,32,64}, any chunk length) and the A/B reference for the
+// tensor-core kernel.  At d = 64, where it is the only kernel, the phases are
+// shaped for its 16-token tile: register-tiled generation and chunk-end update
+// over 16-byte state rows, every warp in the readout, half a warp per token in
+// the step control.
 #include "vh_common.cuh"
 
 namespace vh {
