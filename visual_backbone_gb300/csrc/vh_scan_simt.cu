@@ -258,13 +258,15 @@ __device__ __forceinline__ void scan_simt_body(const ScanArgs &a)
                 }
                 kk = tsum(kk);
                 qq = tsum(qq);
-                const float nk = sqrtf(kk + a.knorm_eps);
-                const float nq = a.qhat ? 1.0f : sqrtf(qq + a.knorm_eps);
+                // stabilised norms as correctly rounded reciprocal square roots (one
+                // multiply per component instead of a division)
+                const float rk = __frsqrt_rn(kk + a.knorm_eps);
+                const float rq = a.qhat ? 1.0f : __frsqrt_rn(qq + a.knorm_eps);
                 float kn2 = 0.0f, dd = 0.0f;
 #pragma unroll
                 for (int m = 0; m < CPT3; ++m) {
-                    kr[m] = kr[m] / nk;
-                    qr[m] = qr[m] / nq;
+                    kr[m] *= rk;
+                    qr[m] *= rq;
                     vv[m] = kr[m] - vv[m];  // delta = k - v
                     kn2 = fmaf(kr[m], kr[m], kn2);
                     dd = fmaf(vv[m], vv[m], dd);
