@@ -85,7 +85,14 @@ enum {
 enum {
     VH_IMPL_AUTO = 0,          /* the fastest built kernel for the shape */
     VH_IMPL_SIMT = 1,          /* fp32 CUDA-core kernel */
-    VH_IMPL_TC = 2             /* tensor-core (tcgen05) kernel */
+    VH_IMPL_TC = 2,            /* tensor-core (tcgen05) kernel, its faster gain form */
+    VH_IMPL_TC_WY = 3,         /* tensor-core kernel, shared gain in WY form ("VisionHOPE",
+                                  App. B.4 Prop. 2, Eqs. (46), (49) unrolled: the keys' Gram
+                                  matrix and the gain assembly on the tensor core, the
+                                  chunk's triangular system on CUDA cores); the method as
+                                  defined with H, W <= 64 only, else VH_ERR_UNSUPPORTED */
+    VH_IMPL_TC_RECUR = 4       /* tensor-core kernel, shared gain as the blocked per-token
+                                  recurrence of Eq. (46) */
 };
 
 /* Indices of the optional device counters (params->stats, 8 x uint64). */

@@ -9,7 +9,8 @@
 
 namespace vh {
 cudaError_t launch_scan_simt(const ScanArgs &a, int d, bool bf16, cudaStream_t st);
-cudaError_t launch_scan_tc(const ScanArgs &a, int d, bool bf16, cudaStream_t st, bool *handled);
+cudaError_t launch_scan_tc(const ScanArgs &a, int d, bool bf16, cudaStream_t st, bool *handled,
+                           int gain);
 cudaError_t launch_qproj(const void *x, bool bf16, int d, const float *wq, const float *skip,
                          const float *dir_scale, unsigned dirs, __nv_bfloat16 *qhat, float *out,
                          int accumulate, long npix, int Cc, float knorm_eps, cudaStream_t st);
@@ -76,7 +77,7 @@ vh_status check_scan(const vh_params *p, unsigned dirs, int chunk)
     if (p->gate_mode < 0 || p->gate_mode > 2) return fail(VH_ERR_INVALID_ARG, "gate_mode %d", p->gate_mode);
     if (!(p->alpha_init > 0.0f && p->alpha_init < 1.0f))
         return fail(VH_ERR_INVALID_ARG, "alpha_init %g must lie in (0,1)", (double)p->alpha_init);
-    if (p->impl < VH_IMPL_AUTO || p->impl > VH_IMPL_TC) return fail(VH_ERR_INVALID_ARG, "impl %d", p->impl);
+    if (p->impl < VH_IMPL_AUTO || p->impl > VH_IMPL_TC_RECUR) return fail(VH_ERR_INVALID_ARG, "impl %d", p->impl);
     if (p->control_flags & ~(unsigned)VH_CTRL_ALL)
         return fail(VH_ERR_INVALID_ARG, "control_flags 0x%x has unknown bits", p->control_flags);
     return VH_OK;
@@ -300,9 +301,12 @@ vh_status vh_scan_forward(const void *x, const float *memories0, const vh_params
     }
     bool handled = false;
     if (p->impl != VH_IMPL_SIMT) {
-        e = vh::launch_scan_tc(a, d, bf16, st, &handled);
+        e = vh::launch_scan_tc(a, d, bf16, st, &handled, p->impl);
+        if (e == cudaErrorNotSupported)
+            return fail(VH_ERR_UNSUPPORTED, "the WY gain needs the method as defined (no control_flags, "
+                        "no w_query) and H, W <= 64");
         if (e != cudaSuccess) return cuda_fail(e, "tensor-core scan launch");
-        if (!handled && p->impl == VH_IMPL_TC)
+        if (!handled && p->impl != VH_IMPL_AUTO)
             return fail(VH_ERR_UNSUPPORTED, "no tensor-core kernel for d=%d dtype=%d chunk=%d",
                         d, (int)p->x_dtype, chunk);
     }
@@ -480,7 +484,7 @@ vh_status vh_scan_backward(const void *x, const float *memories0, const vh_param
             f.rec_stride = N * vh::token_rec_floats(d);
         }
         bool handled = false;
-        e = vh::launch_scan_tc(f, d, bf16, st, &handled);
+        e = vh::launch_scan_tc(f, d, bf16, st, &handled, VH_IMPL_TC_RECUR);
         if (e != cudaSuccess) return cuda_fail(e, "tensor-core forward launch");
         ba.have_ckpt = handled ? 1 : 0;
         if (handled) {

@@ -91,12 +91,54 @@ static_assert(SMEM_BYTES <= 75 * 1024, "three CTAs per SM");
 constexpr int OFF_QF = (SMEM_BYTES + 15) / 16 * 16;
 constexpr int OFF_CQ = OFF_QF + TT * KS * 4;
 constexpr int SMEM_INTRA = OFF_CQ + TT / NB * 8 * 4;
+// WY form of the shared gain (chunks of at most one sub-tile, the method as defined):
+// the keys' Gram matrix on the tensor core, the chunk's triangular system solved on one
+// warp, and G assembled on the tensor core from the solution.  The update then reads G's
+// pieces K-major (row n = column of G), pieces G_PIECE apart.
+//  * key pieces: the keys of the sub-tile in three bf16 pieces, element (token j, column b,
+//    piece p) at (j/8) KP_GSTR + (4p + b/8) 128 + (j%8) 16 + (b%8) 2.  Read K-major (rows j,
+//    K = b; piece p at +512 B) by the Gram MMA and MN-major (N = 32p + b stacks the pieces,
+//    K = j) by the assembly MMA.
+//  * W' pieces: the assembly's B operand, rows = gain rows a, K = tokens (64, zero past the
+//    chunk), element (a, j) at (a/8) WP_SBO + (j/8) 128 + (a%8) 16 + (j%8) 2, pieces WP_PIECE
+//    apart (so N = 32p + a stacks them).
+//  * packed coefficients: row i holds c(i, j) for j = j0(i) .. Lp - 1, j0(i) = 4 floor((i+1)/4)
+//    (16-byte aligned rows; entries j <= i are zero).
+constexpr int KP_GSTR = 3 * (D / 8) * 128;
+constexpr int KP_BYTES = TT / 8 * KP_GSTR;
+constexpr int WP_SBO = (TT / 8) * 128;
+constexpr int WP_PIECE = D / 8 * WP_SBO;
+// The recurrence layout above; the WY layout moves the key and delta tiles behind the key
+// pieces, which overlay the gain operand and rows (those are written only after the
+// assembly has read the keys).  The coefficients overlay the key tile once the shifted
+// deltas are formed, and W' overlays both tiles once the solve has read them.
+template <bool kWY> struct Lay {
+    static constexpr int KF = OFF_KF, DL = OFF_DL, SEA = OFF_SEA, SC = OFF_SC, BAR = OFF_BAR;
+    static constexpr int BYTES = SMEM_BYTES;
+};
+template <> struct Lay<true> {
+    static constexpr int KP = OFF_G;
+    static constexpr int KF = KP + KP_BYTES, DL = KF + TT * KS * 4, SEA = DL + TT * KS * 4;
+    static constexpr int SC = SEA + 2 * D * 4, BAR = SC + TT * 16, BYTES = BAR + 128;
+    static constexpr int CP = KF, WP = KF;
+};
+static_assert(Lay<true>::BYTES <= 75 * 1024, "three CTAs per SM");
+static_assert(OFF_GF + D * GFS * 4 <= Lay<true>::KF, "gain rows inside the key pieces");
+static_assert(Lay<true>::WP + 3 * WP_PIECE <= Lay<true>::SEA, "W' inside the key and delta tiles");
+static_assert(Lay<true>::KP - 8 * KP_GSTR >= 0 && Lay<true>::KP + 16 * KP_GSTR <= Lay<true>::BYTES,
+              "Gram operand rows 0..127 stay in shared memory");
+static_assert(Lay<true>::KP - 1024 >= 0 && Lay<true>::KP + KP_BYTES + 2048 <= Lay<true>::BYTES,
+              "assembly operand rows 0..127 (key columns, MN-major) stay in shared memory");
+static_assert((TT * TT / 2 + 2 * TT) * 4 <= TT * KS * 4, "packed coefficients inside the key tile");
 constexpr uint32_t TMEM_COLS = 128;
 // TMEM columns (all M = 128): the generation [s_eta s_alpha 0.. | k_raw | v | q_raw] at
 // 0..111 (COL_K, COL_V, COL_QR relative), then the readout over the consumed gate and
 // key columns and the update's three 32-column blocks over the rest.
 constexpr int COL_GEN = 0, COL_K = ROW_MEM, COL_V = ROW_MEM + D, COL_QR = ROW_MEM + 2 * D;
 constexpr int COL_RO = 0, COL_UPD = 32;
+// WY form: the Gram matrix over the consumed generation columns, the readout beside it,
+// the assembly's three column blocks over both once they are read.
+constexpr int COL_GRAM = 0, COL_RO_WY = 64, COL_ASM = 0;
 static_assert(OFF_X >= LBO_X && OFF_Q >= 8 * SBO_K32, "operand rows 0..63 stay in shared memory");
 static_assert(OFF_Q + 4 * Q_PIECE <= OFF_BAR, "operand rows 64..127 stay in shared memory");
 
@@ -169,9 +211,74 @@ __device__ __forceinline__ void mma_split6(uint32_t dt, uint32_t a0, uint32_t b0
 }
 
 
+// ---------------------------------------------------------------- WY form
+
+// Start of row i of the packed coefficients (16-byte aligned), and its offset for a
+// system of size lp: sum over earlier rows of lp - j0(r).
+__host__ __device__ constexpr int wy_j0(int i) { return 4 * ((i + 1) / 4); }
+__host__ __device__ constexpr int wy_off(int lp, int i)
+{
+    // sum_{m=1..i} floor(m/4) = 2 q (q - 1) + q (s + 1) for i = 4q + s
+    return i * lp - 4 * (2 * (i / 4) * (i / 4 - 1) + (i / 4) * (i % 4 + 1));
+}
+
+// The chunk's triangular system for gain row a (lane = a), with the shared gain written as
+//   G = gamma_L I + sum_j sigma_j w_j k_j^T,   w_j = -eta_j z_j,
+//   z_j = G_{j-1} k_j + delta_j = r_j + sum_{i<j} c(i, j) w_i,
+//   r_j = gamma_{j-1} k_j + delta_j,  c(i, j) = (prod_{i<s<j} alpha_s) k_i . k_j,
+// gamma_j = prod_{s<=j} alpha_s and sigma_j = prod_{s>j} alpha_s ("VisionHOPE", App. B.4
+// Prop. 2, Eqs. (46), (49): the recurrence unrolled; every factor is a product of
+// retentions, so nothing is divided).  Right-looking: w_i is final once the earlier tokens
+// have been added to its accumulator; each then adds c(i, j) w_i to every later token.
+// The accumulators live in registers (lp of them); the coefficients are read as 16-byte
+// broadcasts.  Then W' = sigma_j w_j goes out as the assembly's A operand, three bf16 pieces.
+template <int LP>
+__device__ __forceinline__ void wy_solve(const float *__restrict__ dl, const float *__restrict__ cpk,
+                                         const float *__restrict__ eta, const float *__restrict__ sig,
+                                         unsigned char *wp, int a)
+{
+    float acc[LP];
+#pragma unroll
+    for (int j = 0; j < LP; ++j) acc[j] = dl[j * KS + a];
+    float4 e4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+    for (int i = 0; i < LP; ++i) {
+        if ((i & 3) == 0) e4 = *reinterpret_cast<const float4 *>(eta + i);
+        const float ei = (i & 3) == 0 ? e4.x : (i & 3) == 1 ? e4.y : (i & 3) == 2 ? e4.z : e4.w;
+        const float w = -ei * acc[i];
+        acc[i] = w;
+        const int j0 = wy_j0(i), o = wy_off(LP, i);
+#pragma unroll
+        for (int j4 = j0; j4 < LP; j4 += 4) {
+            const float4 cv = *reinterpret_cast<const float4 *>(cpk + o + (j4 - j0));
+            if (j4 + 0 > i) acc[j4 + 0] = fmaf(cv.x, w, acc[j4 + 0]);
+            if (j4 + 1 > i) acc[j4 + 1] = fmaf(cv.y, w, acc[j4 + 1]);
+            if (j4 + 2 > i) acc[j4 + 2] = fmaf(cv.z, w, acc[j4 + 2]);
+            if (j4 + 3 > i) acc[j4 + 3] = fmaf(cv.w, w, acc[j4 + 3]);
+        }
+    }
+#pragma unroll
+    for (int g = 0; g < TT / 8; ++g) {
+        float v8[8];
+        if (8 * g < LP) {
+            const float4 s0 = *reinterpret_cast<const float4 *>(sig + 8 * g);
+            const float4 s1 = *reinterpret_cast<const float4 *>(sig + 8 * g + 4);
+            const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v8[u] = (8 * g + u < LP) ? sv[u] * acc[(8 * g + u) % LP] : 0.0f;
+        } else {
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v8[u] = 0.0f;
+        }
+        store_split8(wp + (a >> 3) * WP_SBO + g * 128 + (a & 7) * 16, WP_PIECE, v8);
+    }
+}
+
 // kAbl: the ablation switches of the step control and the memories are compiled in
 // (false for the method as defined, so its hot loops carry no test of them).
-template <bool kAbl>
+// kWY: the shared gain in WY form (chunks of one sub-tile, the method as defined: kAbl
+// false, no outer queries); otherwise the blocked recurrence.
+template <bool kAbl, bool kWY>
 __global__ void __launch_bounds__(NT, 3)
     scan_tc_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tm_row,
                    const __grid_constant__ CUtensorMap tm_col,
@@ -179,6 +286,7 @@ __global__ void __launch_bounds__(NT, 3)
                    const __grid_constant__ CUtensorMap tq_col)
 {
     extern __shared__ __align__(1024) unsigned char sm[];
+    using LY = Lay<kWY>;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     int id = blockIdx.x;
     const int h = id % a.nh;
@@ -193,25 +301,26 @@ __global__ void __launch_bounds__(NT, 3)
     const CUtensorMap *tm = rowr ? &tm_row : &tm_col;
     const size_t SZ = (size_t)4 * D * D + 2 * D;
 
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + OFF_BAR);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + LY::BAR);
     const uint32_t mb_x = smem_u32(&bars[0]), mb_gen = smem_u32(&bars[1]);
     const uint32_t mb_ro = smem_u32(&bars[2]), mb_upd = smem_u32(&bars[3]);
     const uint32_t mb_g = smem_u32(&bars[4]);
     const uint32_t mb_q = smem_u32(&bars[5]);
+    const uint32_t mb_gram = smem_u32(&bars[6]), mb_asm = smem_u32(&bars[7]);
     const bool exact = a.qhat != nullptr;  // queries from the outer projection
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + OFF_BAR + 64);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + OFF_BAR + 72);
-    volatile int *role_slot = reinterpret_cast<volatile int *>(sm + OFF_BAR + 76);
-    volatile int *delta_form = reinterpret_cast<volatile int *>(sm + OFF_BAR + 80);
-    volatile int *vote = reinterpret_cast<volatile int *>(sm + OFF_BAR + 96);  // 2 warp flags
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + LY::BAR + 64);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + LY::BAR + 72);
+    volatile int *role_slot = reinterpret_cast<volatile int *>(sm + LY::BAR + 76);
+    volatile int *delta_form = reinterpret_cast<volatile int *>(sm + LY::BAR + 80);
+    volatile int *vote = reinterpret_cast<volatile int *>(sm + LY::BAR + 96);  // 2 warp flags
     const Waiter wt{abort_flag, a.stats};
 
     unsigned char *sX = sm + OFF_X, *sS = sm + OFF_S, *sQ = sm + OFF_Q, *sG = sm + OFF_G;
-    float *Kf = reinterpret_cast<float *>(sm + OFF_KF);
-    float *DLf = reinterpret_cast<float *>(sm + OFF_DL);
+    float *Kf = reinterpret_cast<float *>(sm + LY::KF);
+    float *DLf = reinterpret_cast<float *>(sm + LY::DL);
     float *Gf = reinterpret_cast<float *>(sm + OFF_GF);
-    float *Sea = reinterpret_cast<float *>(sm + OFF_SEA);
-    float4 *SC = reinterpret_cast<float4 *>(sm + OFF_SC);
+    float *Sea = reinterpret_cast<float *>(sm + LY::SEA);
+    float4 *SC = reinterpret_cast<float4 *>(sm + LY::SC);
     float *GT = reinterpret_cast<float *>(sm + OFF_GT);
     // intra-chunk readout (ablation): y_t = M^m_b u_t with u_t = G_{t-1} q_t, the gain before
     // the token's own update.  The gain pair forms u_t and leaves it in the token's row of
@@ -229,6 +338,8 @@ __global__ void __launch_bounds__(NT, 3)
         mbar_init(mb_upd, 1);
         mbar_init(mb_g, 2);
         mbar_init(mb_q, 1);
+        mbar_init(mb_gram, 1);
+        mbar_init(mb_asm, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         // Co-resident CTAs hold consecutive groups of four hardware warp slots, and warp w
         // of a CTA runs on SM sub-partition w.  Alternating the gain pair between warps 0-1
@@ -317,7 +428,7 @@ __global__ void __launch_bounds__(NT, 3)
     // no out (backward support: only the boundary states are wanted): no readout adds
     float *ob = (kAbl && !a.out) ? nullptr : a.out + (size_t)b * H * W * Cc + (size_t)h * D;
     unsigned n_spec = 0, n_inj = 0, n_nf = 0;
-    uint32_t ph_x = 0, ph_gen = 0, ph_ro = 0, ph_upd = 0, ph_g = 0, ph_q = 0;
+    uint32_t ph_x = 0, ph_gen = 0, ph_ro = 0, ph_upd = 0, ph_g = 0, ph_q = 0, ph_gram = 0, ph_asm = 0;
 
     // gain state of the gain pair: its thread t owns row t/2 of G = gam * ghat, columns
     // 16(t%2)..+15
@@ -369,6 +480,296 @@ __global__ void __launch_bounds__(NT, 3)
                 const int nc = (s + 1 < nsub) ? c : c + 1;
                 if (nc < nlines) issue_x(nc, ns);
             }
+            if constexpr (kWY) {
+            // ================= WY form of the shared gain (one sub-tile per chunk) =========
+            float *cpk = reinterpret_cast<float *>(sm + Lay<true>::CP);
+            unsigned char *sKP = sm + Lay<true>::KP, *sWP = sm + Lay<true>::WP;
+            float *ALP = reinterpret_cast<float *>(SC), *ETA = ALP + TT, *GPRE = ETA + TT, *SIG = GPRE + TT;
+            float *gam_slot = reinterpret_cast<float *>(sm + LY::BAR + 84);
+            float *scan_tot = reinterpret_cast<float *>(sm + LY::BAR + 88);
+            // size of the triangular system: the chunk length where a solve is built for it,
+            // else the next of 32 and 64 (tokens past the chunk contribute zero)
+            const int Lp = Lt == 56 ? 56 : Lt == 28 ? 28 : Lt <= 32 ? 32 : 64;
+            // ---- A. per token (token pair, lane = token): stabilised norms (App. C.1,
+            // App. B.5), delta = k - v, the raw scalars, the fp32 key and delta rows and the
+            // keys' operand pieces (rows past the chunk's last token are zero)
+            if (!gainw) {
+                float kr[32], vv[32];
+                float se, sa;
+                tmem_ld_kvs(tbase + lrow + COL_GEN, kr, vv, se, sa);
+                const float kkr = sumsq32(kr);
+                const float rk = __frsqrt_rn(kkr + a.knorm_eps);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    kr[e] *= rk;
+                    vv[e] = kr[e] - vv[e];
+                }
+                const float kn2 = sumsq32(kr), dd2 = sumsq32(vv);
+                if (valid) {
+                    float4 *kd = reinterpret_cast<float4 *>(Kf + jr * KS);
+                    float4 *dd4 = reinterpret_cast<float4 *>(DLf + jr * KS);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        kd[e] = make_float4(kr[4 * e], kr[4 * e + 1], kr[4 * e + 2], kr[4 * e + 3]);
+                        dd4[e] = make_float4(vv[4 * e], vv[4 * e + 1], vv[4 * e + 2], vv[4 * e + 3]);
+                    }
+                    SC[jr] = make_float4(se, sa, kn2, dd2);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) kr[e] = 0.0f;
+                }
+#pragma unroll
+                for (int g = 0; g < 4; ++g)
+                    store_split8(sKP + (jr >> 3) * KP_GSTR + g * 128 + (jr & 7) * 16, 512, kr + 8 * g);
+            }
+            fence_async_smem();
+            tc_before();
+            __syncthreads();
+            tc_after();
+            // ---- B. the Gram matrix k_i . k_j on the tensor core (six split cross terms,
+            // rows i in the token pair's lanes, columns j); the gates and step control of each
+            // token with the retention products (gain pair); the queries and the readout MMA
+            // (token pair)
+            if (issuer && !*abort_flag) {
+                constexpr int pa[6] = {0, 0, 1, 0, 2, 1};
+                constexpr int pb[6] = {0, 1, 0, 2, 0, 1};
+                const uint64_t da = sdesc(smem_u32(sKP) - (rw >> 1) * 8 * KP_GSTR, 128, KP_GSTR);
+                const uint64_t db = sdesc(smem_u32(sKP), 128, KP_GSTR);
+#pragma unroll
+                for (int t = 0; t < 6; ++t)
+#pragma unroll
+                    for (int ks = 0; ks < 2; ++ks)
+                        mma(tbase + COL_GRAM, dadd(da, pa[t] * 512 + ks * 256), dadd(db, pb[t] * 512 + ks * 256),
+                            idesc_bf16(128, 64), (t | ks) != 0);
+                mma_commit(mb_gram);
+            }
+            if (gainw) {
+                const int jg = tid & 63;  // route-ordered token
+                const bool tv = jg < Lt;
+                float alpha = 1.0f, eta_t = 0.0f;
+                if (tv) {
+                    const float4 sc = SC[jg];
+                    float eta, oma;
+                    gates(a, sc.x, sc.y, eta, alpha, oma);
+                    if (a.gate_mode == VH_GATE_FORCED_EXEC) {
+                        eta_t = a.forced_eta;
+                    } else {
+                        const StepOut so = step_control<kAbl>(a, eta, alpha, oma, sc.z, sc.w);
+                        eta_t = so.eta_tilde;
+                        n_spec += so.spec_active;
+                        n_inj += so.inj_ratio_gt1;
+                    }
+                }
+                // inclusive prefix and suffix products of the retentions over the sub-tile
+                // (tokens past the chunk retain 1), each warp holding 32 tokens
+                const int gl = jg & 31;
+                const bool hi = jg >= 32;
+                float pre = alpha, suf = alpha;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const float t1 = __shfl_up_sync(0xffffffffu, pre, o);
+                    const float t2 = __shfl_down_sync(0xffffffffu, suf, o);
+                    if (gl >= o) pre *= t1;
+                    if (gl + o < 32) suf *= t2;
+                }
+                if (!hi && gl == 31) scan_tot[0] = pre;  // tokens 0..31
+                if (hi && gl == 0) scan_tot[1] = suf;    // tokens 32..63
+                named_sync(3, 64);                       // both halves written; SC read
+                if (hi) pre *= scan_tot[0]; else suf *= scan_tot[1];
+                float gpre = __shfl_up_sync(0xffffffffu, pre, 1);    // gamma_{j-1}
+                float sig = __shfl_down_sync(0xffffffffu, suf, 1);   // sigma_j
+                if (gl == 0) gpre = hi ? scan_tot[0] : 1.0f;
+                if (gl == 31) sig = hi ? 1.0f : scan_tot[1];
+                ALP[jg] = alpha;
+                ETA[jg] = eta_t;
+                GPRE[jg] = gpre;
+                SIG[jg] = sig;
+                if (jg == Lt - 1) *gam_slot = pre;  // gamma_L
+                // r_j = gamma_{j-1} k_j + delta_j in place of delta_j (zero past the chunk)
+                float4 *dr = reinterpret_cast<float4 *>(DLf + jg * KS);
+                const float4 *kk = reinterpret_cast<const float4 *>(Kf + jg * KS);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float4 dv = dr[e], kv = kk[e];
+                    dr[e] = tv ? make_float4(fmaf(gpre, kv.x, dv.x), fmaf(gpre, kv.y, dv.y),
+                                             fmaf(gpre, kv.z, dv.z), fmaf(gpre, kv.w, dv.w))
+                               : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                }
+            } else {
+                // queries: q = normalize(M^q_b x), split into the readout's A operand
+                float qr[32];
+                tmem_ld32(tbase + lrow + COL_GEN + COL_QR, qr);
+                const float rq = __frsqrt_rn(sumsq32(qr) + a.knorm_eps);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) qr[e] *= rq;
+#pragma unroll
+                for (int g = 0; g < 4; ++g) store_split8(sQ + op_off(jq, g), Q_PIECE, qr + 8 * g);
+                fence_async_smem();
+                tc_before();
+                named_sync(1, 64);
+                tc_after();
+                // MMA 2: readout y = q M^m_b^T, Eq. (16), beside the Gram columns
+                if (issuer && !*abort_flag) {
+                    mma_split6<Q_PIECE, S_PIECE>(tbase + COL_RO_WY, smem_u32(sQ) - (rw >> 1) * 8 * SBO_K32,
+                                                 smem_u32(sS) + (ROW_MEM + 3 * D) / 8 * SBO_K32,
+                                                 idesc_bf16(128, 32));
+                    mma_commit(mb_ro);
+                }
+            }
+            tc_before();
+            __syncthreads();
+            tc_after();
+            // ---- C. the solve's coefficients: row i = jq of the packed matrix from Gram row i
+            // (this thread's TMEM lane), c(i, j) = (prod_{i<s<j} alpha_s) k_i . k_j for j > i
+            if (!gainw) {
+                wt.wait(mb_gram, ph_gram);
+                tc_after();
+                float gr[64];
+                {
+                    float g0[32], g1[32];
+                    tmem_ld32(tbase + lrow + COL_GRAM, g0);
+                    tmem_ld32(tbase + lrow + COL_GRAM + 32, g1);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        gr[e] = g0[e];
+                        gr[32 + e] = g1[e];
+                    }
+                }
+                const int i = jq;
+                if (i < Lp - 1) {
+                    const int j0 = wy_j0(i);
+                    float *row = cpk + wy_off(Lp, i) - j0;  // row[j] = c(i, j), j >= j0
+                    const bool live = i < Lt;
+                    float rat = 1.0f;
+#pragma unroll
+                    for (int j4 = 0; j4 < TT; j4 += 4) {
+                        if (j4 < Lp) {
+                            const float4 al = *reinterpret_cast<const float4 *>(ALP + j4);
+                            const float av[4] = {al.x, al.y, al.z, al.w};
+                            float cv[4];
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                const int j = j4 + u;
+                                cv[u] = (live && j > i && j < Lt) ? rat * gr[j] : 0.0f;
+                                if (j > i) rat *= av[u];
+                            }
+                            if (j4 >= j0)
+                                *reinterpret_cast<float4 *>(row + j4) = make_float4(cv[0], cv[1], cv[2], cv[3]);
+                        }
+                    }
+                }
+            }
+            ph_gram ^= 1;
+            tc_before();
+            __syncthreads();
+            tc_after();
+            // ---- D. the solve on one warp of the gain pair (lane = gain row) while the token
+            // pair adds the readout to out
+            const int gw0 = 2 * gp;
+            if (warp == gw0) {
+                if (Lp == 56)
+                    wy_solve<56>(DLf, cpk, ETA, SIG, sWP, lane);
+                else if (Lp == 28)
+                    wy_solve<28>(DLf, cpk, ETA, SIG, sWP, lane);
+                else if (Lp == 32)
+                    wy_solve<32>(DLf, cpk, ETA, SIG, sWP, lane);
+                else
+                    wy_solve<64>(DLf, cpk, ETA, SIG, sWP, lane);
+                fence_async_smem();
+            } else if (!gainw) {
+                wt.wait(mb_ro, ph_ro);
+                tc_after();
+                float y[32];
+                tmem_ld32(tbase + lrow + COL_RO_WY, y);
+                if (valid) {
+                    const int pix = rowr ? Lidx * W + p : p * W + Lidx;
+                    float *dst = ob + (size_t)pix * Cc;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        float4 v4 = make_float4(y[4 * e], y[4 * e + 1], y[4 * e + 2], y[4 * e + 3]);
+                        if (lam) {
+                            v4.x *= lam[4 * e]; v4.y *= lam[4 * e + 1];
+                            v4.z *= lam[4 * e + 2]; v4.w *= lam[4 * e + 3];
+                        }
+                        n_nf += !isfinite(v4.x) + !isfinite(v4.y) + !isfinite(v4.z) + !isfinite(v4.w);
+                        red_add_v4(dst + 4 * e, v4);
+                    }
+                }
+            }
+            tc_before();
+            __syncthreads();
+            tc_after();
+            // ---- E. G = gamma_L I + W' K^T on the tensor core, formed transposed:
+            // G^T = gamma_L I + K W'^T with the key pieces as the MN-major A operand (rows =
+            // columns b of G, landing in the solving warp's lanes) and W' as B with its three
+            // pieces stacked along N.  Per K step (16 tokens) one MMA per key piece against
+            // N = 96, 64, 32: the six cross terms in three column blocks.
+            if (issuer && !*abort_flag) {
+                const uint64_t dk = sdesc(smem_u32(sKP) - 1024 * gp, KP_GSTR, 128);
+                const uint64_t dw = sdesc(smem_u32(sWP), 128, WP_SBO);
+#pragma unroll
+                for (int ks = 0; ks < TT / 16; ++ks)
+#pragma unroll
+                    for (int pc = 0; pc < 3; ++pc)
+                        mma(tbase + COL_ASM, dadd(dk, pc * 512 + ks * 2 * KP_GSTR), dadd(dw, ks * 256),
+                            idesc_bf16(128, 96 - 32 * pc, false, true), (ks | pc) != 0);
+                mma_commit(mb_asm);
+            }
+            if (warp == gw0) {
+                // column b = lane of G: the three blocks summed, gamma_L on the diagonal; fp32
+                // rows for the eta / alpha rows and the update's B operand (K-major: row n = b,
+                // K = the rows of G; pieces stacked along N) in three bf16 pieces, as G - I when
+                // the chunk retains at least half of the state (as in the recurrence form)
+                wt.wait(mb_asm, ph_asm);
+                tc_after();
+                float v[32], w2[32];
+                tmem_ld32(tbase + lrow + COL_ASM, v);
+                tmem_ld32(tbase + lrow + COL_ASM + D, w2);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) v[e] += w2[e];
+                tmem_ld32(tbase + lrow + COL_ASM + 2 * D, w2);
+                const float gL = *gam_slot;
+                const bool use_delta = gL >= 0.5f;
+#pragma unroll
+                for (int e = 0; e < 32; ++e) v[e] = (v[e] + w2[e]) + (e == lane ? gL : 0.0f);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) Gf[e * GFS + lane] = v[e];
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    float v8[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        v8[u] = v[8 * g + u] - ((use_delta && 8 * g + u == lane) ? 1.0f : 0.0f);
+                    store_split8(sG + (lane >> 3) * SBO_K32 + g * LBO_K32 + (lane & 7) * 16, G_PIECE, v8);
+                }
+                if (lane == 0) *delta_form = use_delta ? 1 : 0;
+                fence_async_smem();
+                tc_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(mb_g);
+            } else if (warp == gw0 + 1) {
+                if (lane == 0) mbar_arrive(mb_g);
+            }
+            ph_asm ^= 1;
+            // ---- MMA 3 (chunk end): every d x d memory <- M_b G, as in the recurrence form
+            // but with G's pieces K-major
+            if (issuer) {
+                if (wt.wait(mb_g, ph_g) && !*abort_flag) {
+                    tc_after();
+                    const uint64_t da = sdesc(smem_u32(sS) + ROW_MEM / 8 * SBO_K32, LBO_K32, SBO_K32);
+                    const uint64_t db = sdesc(smem_u32(sG), LBO_K32, SBO_K32);
+#pragma unroll
+                    for (int ks = 0; ks < 2; ++ks) {
+                        const uint32_t ka = ks * 2 * LBO_K32;
+                        mma(tbase + COL_UPD, dadd(da, ka), dadd(db, ka), idesc_bf16(128, 96), ks != 0);
+                        mma(tbase + COL_UPD, dadd(da, S_PIECE + ka), dadd(db, ka), idesc_bf16(128, 64), 1);
+                        mma(tbase + COL_UPD + 2 * D, dadd(da, 2 * S_PIECE + ka), dadd(db, ka),
+                            idesc_bf16(128, 32), 1);
+                    }
+                    mma_commit(mb_upd);
+                }
+            }
+            } else {
             // ---- per-token step, Eqs. (15), (19), (20), (53).  The token pair (lane = token)
             // normalises k, forms delta = k - v and their squared norms, and publishes the
             // token's scalars; then the gain pair (lane = route-ordered token) evaluates the
@@ -863,6 +1264,7 @@ __global__ void __launch_bounds__(NT, 3)
                     }
                 }
             }
+            }  // recurrence form
             ph_ro ^= 1;
             if (last) {
                 ph_g ^= 1;
@@ -1041,8 +1443,12 @@ bool make_map(CUtensorMap *m, const void *x, int B, int H, int W, int Cc, bool r
 }  // namespace tc
 
 // Tensor-core path: head_dim 32, bf16 x, row/column-aligned chunks.  Sets
-// *handled = false (and returns success) for any other shape.
-cudaError_t launch_scan_tc(const ScanArgs &a, int d, bool bf16, cudaStream_t st, bool *handled)
+// *handled = false (and returns success) for any other shape.  gain: VH_IMPL_TC_WY selects
+// the WY form of the shared gain (the method as defined, no outer queries, every chunk
+// within one 64-token sub-tile; a request the shape does not admit returns
+// cudaErrorNotSupported); anything else takes the blocked recurrence, the faster form.
+cudaError_t launch_scan_tc(const ScanArgs &a, int d, bool bf16, cudaStream_t st, bool *handled,
+                           int gain)
 {
     *handled = false;
     const bool aligned = a.chunk == 0 || (a.chunk == a.W && a.chunk == a.H);
@@ -1050,6 +1456,10 @@ cudaError_t launch_scan_tc(const ScanArgs &a, int d, bool bf16, cudaStream_t st,
     if (d != tc::D || !bf16 || !aligned || (a.Cc % 8) != 0 || !a16(a.mem0) ||
         (a.mem_out && !a16(a.mem_out)))
         return cudaSuccess;
+    const bool abl = a.control_flags || a.ckpt;
+    const bool wy_ok = !abl && !a.qhat && a.H <= tc::TT && a.W <= tc::TT;
+    if (gain == VH_IMPL_TC_WY && !wy_ok) return cudaErrorNotSupported;
+    const bool wy = wy_ok && gain == VH_IMPL_TC_WY;
     CUtensorMap mr, mc, qr, qc;
     if (!tc::make_map(&mr, a.x, a.B, a.H, a.W, a.Cc, true) ||
         !tc::make_map(&mc, a.x, a.B, a.H, a.W, a.Cc, false))
@@ -1067,20 +1477,25 @@ cudaError_t launch_scan_tc(const ScanArgs &a, int d, bool bf16, cudaStream_t st,
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 64 && !attr_set[dev]) {
-        e = cudaFuncSetAttribute(tc::scan_tc_kernel<false>,
+        e = cudaFuncSetAttribute(tc::scan_tc_kernel<false, false>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, tc::SMEM_BYTES);
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(tc::scan_tc_kernel<true>,
+        e = cudaFuncSetAttribute(tc::scan_tc_kernel<true, false>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, tc::SMEM_INTRA);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(tc::scan_tc_kernel<false, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, tc::Lay<true>::BYTES);
         if (e != cudaSuccess) return e;
         attr_set[dev] = 1;
     }
     const unsigned grid = (unsigned)(a.B * a.ndirs * a.nh);
-    if (a.control_flags || a.ckpt) {
+    if (abl) {
         const int smem = (a.control_flags & VH_CTRL_INTRA_READ) ? tc::SMEM_INTRA : tc::SMEM_BYTES;
-        tc::scan_tc_kernel<true><<<grid, tc::NT, smem, st>>>(a, mr, mc, qr, qc);
+        tc::scan_tc_kernel<true, false><<<grid, tc::NT, smem, st>>>(a, mr, mc, qr, qc);
+    } else if (wy) {
+        tc::scan_tc_kernel<false, true><<<grid, tc::NT, tc::Lay<true>::BYTES, st>>>(a, mr, mc, qr, qc);
     } else {
-        tc::scan_tc_kernel<false><<<grid, tc::NT, tc::SMEM_BYTES, st>>>(a, mr, mc, qr, qc);
+        tc::scan_tc_kernel<false, false><<<grid, tc::NT, tc::SMEM_BYTES, st>>>(a, mr, mc, qr, qc);
     }
     *handled = true;
     return cudaGetLastError();

@@ -92,11 +92,11 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t 
 // The descriptor of an operand `bytes` further on (16-byte units in the address field).
 __device__ __forceinline__ uint64_t dadd(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
 
-// Instruction descriptor of kind::f16: bf16 A and B, fp32 D; A K-major, B K-major or
-// (b_mn) MN-major.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn = false)
+// Instruction descriptor of kind::f16: bf16 A and B, fp32 D; each operand K-major or
+// (a_mn, b_mn) MN-major.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn = false, bool a_mn = false)
 {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn ? 1u : 0u) << 16) |
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
