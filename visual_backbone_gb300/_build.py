@@ -15,8 +15,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libvh.so")
-SOURCES = ["vh_api.cu", "vh_scan_simt.cu", "vh_scan_tc.cu", "vh_scan_bwd.cu", "vh_qproj.cu",
-           "vh_qproj_tc.cu", "vh_block.cu", "vh_noalloc.cu"]
+SOURCES = ["vh_api.cu", "vh_scan_simt.cu", "vh_scan_tc.cu", "vh_scan_tc64.cu", "vh_scan_bwd.cu",
+           "vh_qproj.cu", "vh_qproj_tc.cu", "vh_block.cu", "vh_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC = os.environ.get("NVCC", "nvcc")
 

@@ -11,6 +11,7 @@ namespace vh {
 cudaError_t launch_scan_simt(const ScanArgs &a, int d, bool bf16, cudaStream_t st);
 cudaError_t launch_scan_tc(const ScanArgs &a, int d, bool bf16, cudaStream_t st, bool *handled,
                            int gain);
+cudaError_t launch_scan_tc64(const ScanArgs &a, int d, bool bf16, cudaStream_t st, bool *handled);
 cudaError_t launch_qproj(const void *x, bool bf16, int d, const float *wq, const float *skip,
                          const float *dir_scale, unsigned dirs, __nv_bfloat16 *qhat, float *out,
                          int accumulate, long npix, int Cc, float knorm_eps, cudaStream_t st);
@@ -301,7 +302,10 @@ vh_status vh_scan_forward(const void *x, const float *memories0, const vh_params
     }
     bool handled = false;
     if (p->impl != VH_IMPL_SIMT) {
-        e = vh::launch_scan_tc(a, d, bf16, st, &handled, p->impl);
+        if (d == 64 && p->impl != VH_IMPL_TC_WY)
+            e = vh::launch_scan_tc64(a, d, bf16, st, &handled);
+        else
+            e = vh::launch_scan_tc(a, d, bf16, st, &handled, p->impl);
         if (e == cudaErrorNotSupported)
             return fail(VH_ERR_UNSUPPORTED, "the WY gain needs the method as defined (no control_flags, "
                         "no w_query) and H, W <= 64");
