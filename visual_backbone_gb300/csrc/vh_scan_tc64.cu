@@ -69,8 +69,19 @@ constexpr int OFF_DL = OFF_KF + TT * KS * 4;
 constexpr int OFF_SEA = OFF_DL + TT * KS * 4;
 constexpr int OFF_SC = OFF_SEA + 2 * D * 4;
 constexpr int OFF_GT = OFF_SC + TT * 16;
-constexpr int OFF_BAR = OFF_GT + TT / NB * 8 * 4;
+// WY form (chunks of at most one sub-tile): the keys' operand pieces (MN-major A of the
+// gain assembly: element (column b, token j, piece p) at (j/8) KP_KSTR + (8p + b/8) 128 +
+// (j%8) 16 + (b%8) 2), the solution's pieces W' (K-major B: row n = 64p + a, K = token,
+// element at (n/8) WP_SBO + (j/8) 128 + (n%8) 16 + (j%8) 2) and the Gram entries (fp32).
+constexpr int KP_KSTR = 3 * (D / 8) * 128;
+constexpr int OFF_KP = OFF_GT + TT / NB * 8 * 4;
+constexpr int WP_SBO = TT / 8 * 128;
+constexpr int OFF_WP = OFF_KP + TT / 8 * KP_KSTR;
+constexpr int GRS = TT + 4;
+constexpr int OFF_GR = OFF_WP + 3 * D / 8 * WP_SBO;
+constexpr int OFF_BAR = OFF_GR + TT * GRS * 4;
 constexpr int SMEM_BYTES = OFF_BAR + 128;
+static_assert(OFF_KP + TT / 8 * KP_KSTR + 2048 <= SMEM_BYTES, "assembly operand rows stay in shared memory");
 static_assert(SMEM_BYTES <= 227 * 1024, "one CTA per SM");
 static_assert(OFF_X % 1024 == 0, "x tile aligned");
 // the M = 128 operands read past their data: rows 32..127 of the x tile and the queries
@@ -108,6 +119,53 @@ __device__ __forceinline__ float sumsq64(const float (&v)[64])
     return ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
 }
 
+// The chunk's triangular system for gain row a (lane = a), as in the d = 32 kernel's WY
+// form ("VisionHOPE", App. B.4 Prop. 2, Eqs. (46), (49) unrolled):
+//   G = gamma_L I + sum_j sigma_j w_j k_j^T,  w_j = -eta_j (r_j + sum_{i<j} c(i, j) w_i),
+//   r_j = gamma_{j-1} k_j + delta_j,  c(i, j) = (prod_{i<s<j} alpha_s) k_i . k_j,
+// every factor a product of retentions.  With at most 32 tokens the coefficients are
+// formed on the fly from the Gram entries (a running product along each row).  Then
+// W' = sigma_j w_j goes out as the assembly's B operand (row a of each piece, K = token,
+// zero past LP).
+template <int LP>
+__device__ __forceinline__ void wy64_solve(const float *__restrict__ dl, const float *__restrict__ gr,
+                                           const float *__restrict__ alp, const float *__restrict__ eta,
+                                           const float *__restrict__ sig, unsigned char *wp, int a)
+{
+    float acc[LP];
+#pragma unroll
+    for (int j = 0; j < LP; ++j) acc[j] = dl[j * KS + a];
+#pragma unroll
+    for (int i = 0; i < LP; ++i) {
+        const float w = -eta[i] * acc[i];
+        acc[i] = w;
+        float rat = 1.0f;
+#pragma unroll
+        for (int j4 = (i + 1) & ~3; j4 < LP; j4 += 4) {
+            const float4 g4 = *reinterpret_cast<const float4 *>(gr + i * GRS + j4);
+            const float4 a4 = *reinterpret_cast<const float4 *>(alp + j4);
+            const float gv[4] = {g4.x, g4.y, g4.z, g4.w}, av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                if (j4 + u > i) {
+                    acc[j4 + u] = fmaf(rat * gv[u], w, acc[j4 + u]);
+                    rat *= av[u];
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int g = 0; g < TT / 8; ++g) {
+        float v8[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v8[u] = (8 * g + u < LP) ? sig[8 * g + u] * acc[(8 * g + u) % LP] : 0.0f;
+        store_split8(wp + (a >> 3) * WP_SBO + g * 128 + (a & 7) * 16, 8 * WP_SBO, v8);
+    }
+}
+
+// kWY: the shared gain in WY form (every chunk within one sub-tile); otherwise the blocked
+// recurrence on all 256 threads.
+template <bool kWY>
 __global__ void __launch_bounds__(NT, 1)
     scan_tc64_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tm_row,
                      const __grid_constant__ CUtensorMap tm_col)
@@ -169,7 +227,7 @@ __global__ void __launch_bounds__(NT, 1)
             tma_load_4d(smem_u32(sX + q * LBO_X), tm, h * D + 8 * q, box_start(s), line_of(c), b, mb_x);
     };
     __syncthreads();  // barriers initialised, TMEM address written
-    const bool issuer = tid == 0;
+    const bool issuer = warp == 3 && lane == 0;  // MMA and TMA issue; no token work
     if (issuer) issue_x(0, 0);
     {
         const float *m0 = a.mem0 + ((size_t)r * a.nh + h) * SZ;
@@ -213,7 +271,80 @@ __global__ void __launch_bounds__(NT, 1)
     // the token of this thread's TMEM lane (warps 0 and 4: box row = lane)
     const bool tokw = (warp & 3) == 0;
 
-    for (int c = 0; c < nlines; ++c) {
+    // the 1 x d eta and alpha rows advanced by G on CUDA cores, in fp32 (one warp, lane =
+    // column pair): eta <- eta G, alpha <- alpha G, with their operand rows re-split
+    auto eta_alpha_rows = [&]() {
+                    float ne0 = 0.0f, na0 = 0.0f, ne1 = 0.0f, na1 = 0.0f;
+#pragma unroll 8
+                    for (int l = 0; l < D; ++l) {
+                        const float g0 = Gf[l * GFS + lane], g1 = Gf[l * GFS + 32 + lane];
+                        ne0 = fmaf(Sea[l], g0, ne0);
+                        na0 = fmaf(Sea[D + l], g0, na0);
+                        ne1 = fmaf(Sea[l], g1, ne1);
+                        na1 = fmaf(Sea[D + l], g1, na1);
+                    }
+                    __syncwarp();
+                    Sea[lane] = ne0;
+                    Sea[32 + lane] = ne1;
+                    Sea[D + lane] = na0;
+                    Sea[D + 32 + lane] = na1;
+                    const float vals[4] = {ne0, ne1, na0, na1};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int row = k >> 1, col = lane + 32 * (k & 1);
+                        __nv_bfloat16 p1, p2, p3;
+                        split3(vals[k], p1, p2, p3);
+                        unsigned char *d0 = sS + op64(ROW_MEM * 0 + row, col >> 3) + 2 * (col & 7);
+                        *reinterpret_cast<__nv_bfloat16 *>(d0) = p1;
+                        *reinterpret_cast<__nv_bfloat16 *>(d0 + S_PIECE) = p2;
+                        *reinterpret_cast<__nv_bfloat16 *>(d0 + 2 * S_PIECE) = p3;
+                    }
+                    };
+    // new state rows after the update MMA: thread = memory row (TMEM lane of its tile), the
+    // three column blocks summed, re-split into the operand pieces; in the increment form M_b
+    // is recovered exactly from its three pieces and added in fp32
+    int c = 0;
+    auto resplit = [&]() {
+                const int tl = warp >> 2;
+                const int mrow = ROW_MEM + 128 * tl + 32 * (warp & 3) + lane;
+                float v[64];
+                {
+                    float w2[64];
+                    tmem_ld64(tbase + lrow + COL_UPD + UPD_TILE * tl, v);
+                    tmem_ld64(tbase + lrow + COL_UPD + UPD_TILE * tl + D, w2);
+#pragma unroll
+                    for (int e = 0; e < 64; ++e) v[e] += w2[e];
+                    tmem_ld64(tbase + lrow + COL_UPD + UPD_TILE * tl + 2 * D, w2);
+#pragma unroll
+                    for (int e = 0; e < 64; ++e) v[e] += w2[e];
+                }
+                const bool add_mb = *delta_form != 0;
+#pragma unroll
+                for (int g = 0; g < 8; ++g) {
+                    unsigned char *src = sS + op64(mrow, g);
+                    if (add_mb) {
+                        const uint4 u1 = *reinterpret_cast<const uint4 *>(src);
+                        const uint4 u2 = *reinterpret_cast<const uint4 *>(src + S_PIECE);
+                        const uint4 u3 = *reinterpret_cast<const uint4 *>(src + 2 * S_PIECE);
+                        const uint32_t *w1 = &u1.x, *x2 = &u2.x, *x3 = &u3.x;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            v[8 * g + 2 * i] += (bf16_lo(w1[i]) + bf16_lo(x2[i])) + bf16_lo(x3[i]);
+                            v[8 * g + 2 * i + 1] += (bf16_hi(w1[i]) + bf16_hi(x2[i])) + bf16_hi(x3[i]);
+                        }
+                    }
+                    store_split8(src, S_PIECE, v + 8 * g);
+                }
+                if (c == nlines - 1 && a.mem_out) {
+                    float *mo = a.mem_out + (((size_t)b * 4 + r) * a.nh + h) * SZ;
+                    float4 *d4 = reinterpret_cast<float4 *>(mo + (size_t)(mrow - ROW_MEM) * D);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        d4[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+                }
+                };
+
+    for (c = 0; c < nlines; ++c) {
         const int Lidx = line_of(c);
         for (int s = 0; s < nsub; ++s) {
             const int t0 = s * TT;
@@ -247,6 +378,258 @@ __global__ void __launch_bounds__(NT, 1)
                 const int nc = (s + 1 < nsub) ? c : c + 1;
                 if (nc < nlines) issue_x(nc, ns);
             }
+            if constexpr (kWY) {
+            // ================= WY form of the shared gain (one sub-tile per chunk) =========
+            float *ALP = reinterpret_cast<float *>(SC), *ETA = ALP + TT, *GPRE = ETA + TT, *SIG = GPRE + TT;
+            float *GR = reinterpret_cast<float *>(sm + OFF_GR);
+            unsigned char *sKP = sm + OFF_KP, *sWP = sm + OFF_WP;
+            float *gam_slot = reinterpret_cast<float *>(sm + OFF_BAR + 84);
+            const int Lp = Lt <= 16 ? 16 : 32;  // size of the triangular system (tokens past Lt are zero)
+            // ---- per-token step.  Warp 0 (lane = token): norms, delta, gates and step control,
+            // the retention products along the route, the shifted deltas r_j, the fp32 keys
+            // (for the Gram warps) and the keys' operand pieces.  Warp 4: the queries, handed
+            // to the issuer for the readout MMA.  Warps 1, 2, 5, 6: the Gram entries once the
+            // keys are written.
+            if (warp == 0) {
+                float kr[64], vv[64];
+                tmem_ld64(tbase + lrow + COL_K, kr);
+                tmem_ld64(tbase + lrow + COL_V, vv);
+                float se, sa;
+                tmem_ld2(tbase + lrow + COL_GEN, se, sa);
+                const float kkr = sumsq64(kr);
+                const float rk = __frsqrt_rn(kkr + a.knorm_eps);
+#pragma unroll
+                for (int e = 0; e < 64; ++e) {
+                    kr[e] *= rk;            // k
+                    vv[e] = kr[e] - vv[e];  // delta = k - v
+                }
+                const float kn2 = sumsq64(kr), dd2 = sumsq64(vv);
+                if (!valid) {
+#pragma unroll
+                    for (int e = 0; e < 64; ++e) kr[e] = 0.0f;
+                }
+                {
+                    float4 *kd = reinterpret_cast<float4 *>(Kf + jr * KS);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) kd[e] = make_float4(kr[4 * e], kr[4 * e + 1], kr[4 * e + 2], kr[4 * e + 3]);
+                }
+                __threadfence_block();
+                named_arrive(1, 5 * 32);  // keys written: the Gram warps may start
+                float alpha = 1.0f, eta_t = 0.0f;
+                if (valid) {
+                    float eta, oma;
+                    gates(a, se, sa, eta, alpha, oma);
+                    if (a.gate_mode == VH_GATE_FORCED_EXEC) {
+                        eta_t = a.forced_eta;
+                    } else {
+                        const StepOut so = step_control<false>(a, eta, alpha, oma, kn2, dd2);
+                        eta_t = so.eta_tilde;
+                        n_spec += so.spec_active;
+                        n_inj += so.inj_ratio_gt1;
+                    }
+                }
+                ALP[jr] = alpha;
+                ETA[jr] = eta_t;
+                __syncwarp();
+                // prefix and suffix products of the retentions in route order (lane = route index)
+                float pre = ALP[lane], suf = pre;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const float t1 = __shfl_up_sync(0xffffffffu, pre, o);
+                    const float t2 = __shfl_down_sync(0xffffffffu, suf, o);
+                    if (lane >= o) pre *= t1;
+                    if (lane + o < 32) suf *= t2;
+                }
+                float gp = __shfl_up_sync(0xffffffffu, pre, 1), sg = __shfl_down_sync(0xffffffffu, suf, 1);
+                if (lane == 0) gp = 1.0f;
+                if (lane == 31) sg = 1.0f;
+                GPRE[lane] = gp;
+                SIG[lane] = sg;
+                if (lane == Lt - 1) *gam_slot = pre;  // gamma_L
+                __syncwarp();
+                // r_j = gamma_{j-1} k_j + delta_j (zero past the chunk)
+                const float gj = GPRE[jr];
+                float4 *dr = reinterpret_cast<float4 *>(DLf + jr * KS);
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    dr[e] = valid ? make_float4(fmaf(gj, kr[4 * e], vv[4 * e]), fmaf(gj, kr[4 * e + 1], vv[4 * e + 1]),
+                                                fmaf(gj, kr[4 * e + 2], vv[4 * e + 2]), fmaf(gj, kr[4 * e + 3], vv[4 * e + 3]))
+                                  : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            } else if (warp == 4) {
+                float qr[64];
+                tmem_ld64(tbase + lrow + COL_QR, qr);
+                const float rq = __frsqrt_rn(sumsq64(qr) + a.knorm_eps);
+#pragma unroll
+                for (int e = 0; e < 64; ++e) qr[e] *= rq;
+#pragma unroll
+                for (int g = 0; g < 8; ++g) store_split8(sQ + op64(lane, g), Q_PIECE, qr + 8 * g);
+                fence_async_smem();
+                tc_before();
+                named_arrive(2, 64);  // queries written: the issuer may start the readout
+            } else if (warp == 3) {
+                named_sync(2, 64);
+                tc_after();
+                // MMA 2: readout y = q M^m_b^T, Eq. (16), six split cross terms
+                if (issuer && !*abort_flag) {
+                    constexpr int pa[6] = {0, 0, 1, 0, 2, 1};
+                    constexpr int pb[6] = {0, 1, 0, 2, 0, 1};
+                    const uint64_t da = sdesc(smem_u32(sQ), LBO, SBO);
+                    const uint64_t db = sdesc(smem_u32(sS) + (ROW_MEM + 3 * D) / 8 * SBO, LBO, SBO);
+#pragma unroll
+                    for (int t = 0; t < 6; ++t)
+#pragma unroll
+                        for (int ks = 0; ks < D / 16; ++ks)
+                            mma(tbase + COL_RO, dadd(da, pa[t] * Q_PIECE + ks * 2 * LBO),
+                                dadd(db, pb[t] * S_PIECE + ks * 2 * LBO), idesc_bf16(128, D), (t | ks) != 0);
+                    mma_commit(mb_ro);
+                }
+            } else if (warp == 1 || warp == 2 || warp == 5 || warp == 6) {
+                // the keys' operand pieces (MN-major: 8 consecutive columns b per 16-byte run;
+                // zero rows past the chunk) and the Gram entries k_i . k_j, i < j < Lp (zero past
+                // the chunk), route order
+                named_sync(1, 5 * 32);
+                const int gt = (warp == 1 ? 0 : warp == 2 ? 1 : warp == 5 ? 2 : 3) * 32 + lane;
+#pragma unroll
+                for (int u = 0; u < TT * (D / 8) / 128; ++u) {
+                    const int item = gt + 128 * u, j = item >> 3, g = item & 7;
+                    const float4 f0 = *reinterpret_cast<const float4 *>(Kf + j * KS + 8 * g);
+                    const float4 f1 = *reinterpret_cast<const float4 *>(Kf + j * KS + 8 * g + 4);
+                    const float v8[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
+                    store_split8(sKP + (j >> 3) * KP_KSTR + g * 128 + (j & 7) * 16, 1024, v8);
+                }
+                const int npair = Lp * (Lp - 1) / 2;
+                for (int pr = gt; pr < npair; pr += 128) {
+                    // pair index -> (i, j), i < j: row i holds Lp - 1 - i pairs
+                    int i = 0, rem = pr;
+                    while (rem >= Lp - 1 - i) { rem -= Lp - 1 - i; ++i; }
+                    const int j = i + 1 + rem;
+                    float g = 0.0f;
+                    if (j < Lt) {
+                        const float4 *ka = reinterpret_cast<const float4 *>(Kf + i * KS);
+                        const float4 *kb = reinterpret_cast<const float4 *>(Kf + j * KS);
+                        float g4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const float4 fa = ka[e], fb = kb[e];
+                            g4[0] = fmaf(fa.x, fb.x, g4[0]);
+                            g4[1] = fmaf(fa.y, fb.y, g4[1]);
+                            g4[2] = fmaf(fa.z, fb.z, g4[2]);
+                            g4[3] = fmaf(fa.w, fb.w, g4[3]);
+                        }
+                        g = (g4[0] + g4[1]) + (g4[2] + g4[3]);
+                    }
+                    GR[i * GRS + j] = g;
+                }
+            }
+            fence_async_smem();
+            tc_before();
+            __syncthreads();
+            tc_after();
+            // ---- the solve (warps 0, 1: lane = gain row) while warp 4 adds the readout to out
+            if (warp < 2) {
+                if (Lp == 16)
+                    wy64_solve<16>(DLf, GR, ALP, ETA, SIG, sWP, 32 * warp + lane);
+                else
+                    wy64_solve<32>(DLf, GR, ALP, ETA, SIG, sWP, 32 * warp + lane);
+                fence_async_smem();
+            } else if (warp == 4) {
+                wt.wait(mb_ro, ph_ro);
+                tc_after();
+                float y[32], y2[32];
+                tmem_ld32(tbase + lrow + COL_RO, y);
+                tmem_ld32(tbase + lrow + COL_RO + 32, y2);
+                if (valid) {
+                    const int pix = rowr ? Lidx * W + p : p * W + Lidx;
+                    float *dst = ob + (size_t)pix * Cc;
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const float *yy = e < 8 ? y : y2;
+                        const int k = 4 * (e & 7);
+                        float4 v4 = make_float4(yy[k], yy[k + 1], yy[k + 2], yy[k + 3]);
+                        if (lam) {
+                            v4.x *= lam[4 * e]; v4.y *= lam[4 * e + 1];
+                            v4.z *= lam[4 * e + 2]; v4.w *= lam[4 * e + 3];
+                        }
+                        n_nf += !isfinite(v4.x) + !isfinite(v4.y) + !isfinite(v4.z) + !isfinite(v4.w);
+                        red_add_v4(dst + 4 * e, v4);
+                    }
+                }
+            }
+            ph_ro ^= 1;
+            tc_before();
+            __syncthreads();
+            tc_after();
+            // ---- G^T = gamma_L I + K W'^T on the tensor core: the keys' pieces as the MN-major A
+            // operand (rows = columns b of G), W' as B with its pieces stacked along N
+            // (192, 128, 64): the six cross terms in three column blocks of 64
+            if (issuer && !*abort_flag) {
+                const uint64_t dk = sdesc(smem_u32(sKP), KP_KSTR, 128);
+                const uint64_t dw = sdesc(smem_u32(sWP), 128, WP_SBO);
+                for (int ks = 0; ks < Lp / 16; ++ks)
+#pragma unroll
+                    for (int pc = 0; pc < 3; ++pc)
+                        mma(tbase + COL_UPD, dadd(dk, pc * 1024 + ks * 2 * KP_KSTR), dadd(dw, ks * 256),
+                            idesc_bf16(128, 3 * D - D * pc, false, true), (ks | pc) != 0);
+                mma_commit(mb_upd);
+            }
+            if ((warp & 3) < 2) {
+                // column b = this lane's TMEM row of G; warps 0, 1 hold rows a = 0..31 of their
+                // columns, warps 4, 5 rows 32..63: fp32 rows for the eta / alpha rows and the
+                // update's B operand (K-major: row n = b, K = a; G - I when the chunk retains at
+                // least half of the state)
+                wt.wait(mb_upd, ph_upd);
+                tc_after();
+                const int bcol = 32 * (warp & 3) + lane, half = warp >> 2;
+                float v[32], w2[32];
+                tmem_ld32(tbase + lrow + COL_UPD + 32 * half, v);
+                tmem_ld32(tbase + lrow + COL_UPD + D + 32 * half, w2);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) v[e] += w2[e];
+                tmem_ld32(tbase + lrow + COL_UPD + 2 * D + 32 * half, w2);
+                const float gL = *gam_slot;
+                const bool use_delta = gL >= 0.5f;
+#pragma unroll
+                for (int e = 0; e < 32; ++e) v[e] = (v[e] + w2[e]) + (32 * half + e == bcol ? gL : 0.0f);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) Gf[(32 * half + e) * GFS + bcol] = v[e];
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    float v8[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        v8[u] = v[8 * g + u] - ((use_delta && 32 * half + 8 * g + u == bcol) ? 1.0f : 0.0f);
+                    store_split8(sG + (bcol >> 3) * SBO + (4 * half + g) * LBO + (bcol & 7) * 16, 8 * SBO, v8);
+                }
+                if (warp == 0 && lane == 0) *delta_form = use_delta ? 1 : 0;
+                fence_async_smem();
+            }
+            ph_upd ^= 1;
+            tc_before();
+            __syncthreads();  // G and its fp32 rows written
+            tc_after();
+            // ---- MMA 3 (chunk end): every d x d memory <- M_b G, with G's pieces K-major
+            if (issuer && !*abort_flag) {
+                const uint64_t db = sdesc(smem_u32(sG), LBO, SBO);
+#pragma unroll
+                for (int tl = 0; tl < 2; ++tl) {
+                    const uint64_t da = sdesc(smem_u32(sS) + (ROW_MEM / 8 + 16 * tl) * SBO, LBO, SBO);
+#pragma unroll
+                    for (int ks = 0; ks < D / 16; ++ks) {
+                        const uint32_t ka = ks * 2 * LBO;
+#pragma unroll
+                        for (int pc = 0; pc < 3; ++pc)
+                            mma(tbase + COL_UPD + UPD_TILE * tl, dadd(da, pc * S_PIECE + ka), dadd(db, ka),
+                                idesc_bf16(128, 3 * D - D * pc), (ks | pc) != 0);
+                    }
+                }
+                mma_commit(mb_upd);
+            }
+            if (warp == 2) eta_alpha_rows();
+            wt.wait(mb_upd, ph_upd);
+            ph_upd ^= 1;
+            tc_after();
+            resplit();
+            } else {
             // ---- per-token step (lane = token).  Warp 0: stabilised norm of k, delta = k - v,
             // the token's fp32 rows and raw scalars.  Warp 4: the query, normalised and split
             // into the readout's A operand (row = box row).
@@ -539,77 +922,13 @@ __global__ void __launch_bounds__(NT, 1)
             if (last) {
                 // the 1 x d eta and alpha rows on CUDA cores, in fp32 (lane = column pair);
                 // their operand rows are read by no pending MMA
-                if (warp == 1) {
-                    float ne0 = 0.0f, na0 = 0.0f, ne1 = 0.0f, na1 = 0.0f;
-#pragma unroll 8
-                    for (int l = 0; l < D; ++l) {
-                        const float g0 = Gf[l * GFS + lane], g1 = Gf[l * GFS + 32 + lane];
-                        ne0 = fmaf(Sea[l], g0, ne0);
-                        na0 = fmaf(Sea[D + l], g0, na0);
-                        ne1 = fmaf(Sea[l], g1, ne1);
-                        na1 = fmaf(Sea[D + l], g1, na1);
-                    }
-                    __syncwarp();
-                    Sea[lane] = ne0;
-                    Sea[32 + lane] = ne1;
-                    Sea[D + lane] = na0;
-                    Sea[D + 32 + lane] = na1;
-                    const float vals[4] = {ne0, ne1, na0, na1};
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int row = k >> 1, col = lane + 32 * (k & 1);
-                        __nv_bfloat16 p1, p2, p3;
-                        split3(vals[k], p1, p2, p3);
-                        unsigned char *d0 = sS + op64(ROW_MEM * 0 + row, col >> 3) + 2 * (col & 7);
-                        *reinterpret_cast<__nv_bfloat16 *>(d0) = p1;
-                        *reinterpret_cast<__nv_bfloat16 *>(d0 + S_PIECE) = p2;
-                        *reinterpret_cast<__nv_bfloat16 *>(d0 + 2 * S_PIECE) = p3;
-                    }
-                }
+                if (warp == 1) eta_alpha_rows();
                 wt.wait(mb_upd, ph_upd);
                 ph_upd ^= 1;
                 tc_after();
-                // new state rows: thread = memory row (TMEM lane of its tile), the three column
-                // blocks summed, re-split into the operand pieces; in the increment form M_b is
-                // recovered exactly from its three pieces and added in fp32
-                const int tl = warp >> 2;
-                const int mrow = ROW_MEM + 128 * tl + 32 * (warp & 3) + lane;
-                float v[64];
-                {
-                    float w2[64];
-                    tmem_ld64(tbase + lrow + COL_UPD + UPD_TILE * tl, v);
-                    tmem_ld64(tbase + lrow + COL_UPD + UPD_TILE * tl + D, w2);
-#pragma unroll
-                    for (int e = 0; e < 64; ++e) v[e] += w2[e];
-                    tmem_ld64(tbase + lrow + COL_UPD + UPD_TILE * tl + 2 * D, w2);
-#pragma unroll
-                    for (int e = 0; e < 64; ++e) v[e] += w2[e];
-                }
-                const bool add_mb = *delta_form != 0;
-#pragma unroll
-                for (int g = 0; g < 8; ++g) {
-                    unsigned char *src = sS + op64(mrow, g);
-                    if (add_mb) {
-                        const uint4 u1 = *reinterpret_cast<const uint4 *>(src);
-                        const uint4 u2 = *reinterpret_cast<const uint4 *>(src + S_PIECE);
-                        const uint4 u3 = *reinterpret_cast<const uint4 *>(src + 2 * S_PIECE);
-                        const uint32_t *w1 = &u1.x, *x2 = &u2.x, *x3 = &u3.x;
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            v[8 * g + 2 * i] += (bf16_lo(w1[i]) + bf16_lo(x2[i])) + bf16_lo(x3[i]);
-                            v[8 * g + 2 * i + 1] += (bf16_hi(w1[i]) + bf16_hi(x2[i])) + bf16_hi(x3[i]);
-                        }
-                    }
-                    store_split8(src, S_PIECE, v + 8 * g);
-                }
-                if (c == nlines - 1 && a.mem_out) {
-                    float *mo = a.mem_out + (((size_t)b * 4 + r) * a.nh + h) * SZ;
-                    float4 *d4 = reinterpret_cast<float4 *>(mo + (size_t)(mrow - ROW_MEM) * D);
-#pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        d4[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
-                }
+                resplit();
             }
+            }  // recurrence form
             fence_async_smem();
             tc_before();
             __syncthreads();  // end of sub-tile: operands rewritten, TMEM consumed
@@ -690,13 +1009,20 @@ cudaError_t launch_scan_tc64(const ScanArgs &a, int d, bool bf16, cudaStream_t s
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 64 && !attr_set[dev]) {
-        e = cudaFuncSetAttribute(tc64::scan_tc64_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(tc64::scan_tc64_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 tc64::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(tc64::scan_tc64_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  tc64::SMEM_BYTES);
         if (e != cudaSuccess) return e;
         attr_set[dev] = 1;
     }
     const unsigned grid = (unsigned)(a.B * a.ndirs * a.nh);
-    tc64::scan_tc64_kernel<<<grid, tc64::NT, tc64::SMEM_BYTES, st>>>(a, mr, mc);
+    // the WY form where every chunk fits one sub-tile (both orientations), else the recurrence
+    if (a.H <= tc64::TT && a.W <= tc64::TT)
+        tc64::scan_tc64_kernel<true><<<grid, tc64::NT, tc64::SMEM_BYTES, st>>>(a, mr, mc);
+    else
+        tc64::scan_tc64_kernel<false><<<grid, tc64::NT, tc64::SMEM_BYTES, st>>>(a, mr, mc);
     *handled = true;
     return cudaGetLastError();
 }
