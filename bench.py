@@ -41,6 +41,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 KERNEL_SOURCES_TC = ["visual_backbone_gb300/csrc/vh_scan_tc.cu",
                      "visual_backbone_gb300/csrc/vh_tc_ptx.cuh",
                      "visual_backbone_gb300/csrc/vh_common.cuh"]
+KERNEL_SOURCES_TC64 = ["visual_backbone_gb300/csrc/vh_scan_tc64.cu",
+                       "visual_backbone_gb300/csrc/vh_tc_ptx.cuh",
+                       "visual_backbone_gb300/csrc/vh_common.cuh"]
 KERNEL_SOURCES_SIMT = ["visual_backbone_gb300/csrc/vh_scan_simt.cu",
                        "visual_backbone_gb300/csrc/vh_common.cuh"]
 KERNEL_SOURCES_BWD = ["visual_backbone_gb300/csrc/vh_scan_bwd.cu",
@@ -116,10 +119,15 @@ def load_peaks():
 
 
 def forward_sources(wl, kernel: str):
-    """Sources of the scan kernel a forward call runs: the tensor-core kernel for d = 32,
-    bf16, aligned chunks (unless the CUDA-core kernel is forced), else the CUDA-core one."""
-    tc = wl.d == 32 and wl.dtype == "bf16" and wl.chunk == 0 and wl.Cc % 8 == 0
-    return KERNEL_SOURCES_TC if tc and kernel != "simt" else KERNEL_SOURCES_SIMT
+    """Sources of the scan kernel a forward call runs: a tensor-core kernel for d = 32 or
+    64, bf16, aligned chunks (unless the CUDA-core kernel is forced), else the CUDA-core one."""
+    aligned = wl.chunk == 0 or (wl.chunk == wl.W and wl.chunk == wl.H)
+    tc = wl.dtype == "bf16" and aligned and wl.Cc % 8 == 0 and kernel != "simt"
+    if tc and wl.d == 32:
+        return KERNEL_SOURCES_TC
+    if tc and wl.d == 64:
+        return KERNEL_SOURCES_TC64
+    return KERNEL_SOURCES_SIMT
 
 
 def kernel_source_hash(sources):
@@ -449,7 +457,9 @@ def workload_config(wl, args):
                         f"4 routes, {wl.dtype} x, fp32 state, alpha_init={wl.alpha_init}, "
                         f"eta_bias={wl.eta_bias}",
             "global_batch": wl.B * dist_env()[1], "tokens_per_step_per_gpu": wl.tokens,
-            "parallelism": f"dp{dist_env()[1]} (images split across GPUs, no collective)",
+            "parallelism": f"dp{dist_env()[1]}: weak scaling, rank r scans images "
+                           f"[r*{wl.B}, (r+1)*{wl.B}) of a synthetic batch of "
+                           f"{dist_env()[1] * wl.B} (vh.shard_images), no collective",
             "l2": "256 MiB buffer written between timed steps (L2 is 129 MB)",
             "kernel": args.kernel, "readout": args.readout, "pass": args.pass_,
             "memories_out": bool(getattr(args, "memories_out", False)),
@@ -475,7 +485,8 @@ def run_ours(args, wl):
     if world > 1:
         torch.distributed.barrier()
 
-    inp = synth.make_inputs(wl)
+    mine = vh.shard_images(wl.B * world, world, rank)  # this rank's images of the job
+    inp = synth.make_inputs(wl, batch=len(mine), first_image=mine.start)
     if wl.dtype == "bf16":
         x_host = torch.from_numpy(inp.x_store.view("int16")).view(torch.bfloat16)
     else:
@@ -648,13 +659,14 @@ def run_backward(args, wl):
         _build.build()
     if world > 1:
         torch.distributed.barrier()
-    inp = synth.make_inputs(wl)
+    mine = vh.shard_images(wl.B * world, world, rank)  # this rank's images of the job
+    inp = synth.make_inputs(wl, batch=len(mine), first_image=mine.start)
     if wl.dtype == "bf16":
         x_host = torch.from_numpy(inp.x_store.view("int16")).view(torch.bfloat16)
     else:
         x_host = torch.from_numpy(inp.x_store)
     dout_host = torch.from_numpy(
-        np.random.default_rng(11).standard_normal((wl.B, wl.H, wl.W, wl.Cc)).astype(np.float32))
+        np.random.default_rng(11 + rank).standard_normal((wl.B, wl.H, wl.W, wl.Cc)).astype(np.float32))
     x, dout = x_host.to(dev), dout_host.to(dev)
     mem0 = torch.from_numpy(inp.mem0).to(dev)
     dx = torch.empty((wl.B, wl.H, wl.W, wl.Cc), dtype=torch.float32, device=dev)
@@ -781,7 +793,8 @@ def run_block(args, wl):
     if world > 1:
         torch.distributed.barrier()
     D, Dm, hidden = block_dims(wl)
-    inp = synth.make_block_inputs(wl.B, wl.H, wl.W, D, Dm, wl.d, wl.seed)
+    mine = vh.shard_images(wl.B * world, world, rank)  # this rank's images of the job
+    inp = synth.make_block_inputs(len(mine), wl.H, wl.W, D, Dm, wl.d, wl.seed, first_image=mine.start)
     x_host = torch.from_numpy(inp["x"])
     x = x_host.to(dev)
     wts = {k: (torch.from_numpy(np.ascontiguousarray(a)).to(dev).to(torch.bfloat16)
@@ -893,7 +906,14 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="stage1")
     ap.add_argument("--variant", choices=["plain", "longmem"], default="plain")
-    ap.add_argument("--kernel", choices=["auto", "simt", "tc"], default="auto")
+    ap.add_argument("--kernel", choices=["auto", "simt", "tc", "tc_wy", "tc_recur"], default="auto",
+                    help="scan kernel: auto / tc (tensor core, its faster gain form), tc_wy or "
+                         "tc_recur (tensor core with the WY or the blocked-recurrence gain, the "
+                         "A/B pair at d = 32), simt (fp32 CUDA cores)")
+    ap.add_argument("--chunk", type=int, default=-1,
+                    help="chunk length for every route (the chunk-length ablation); default: "
+                         "the workload's (rows / columns); a length that is not the row or "
+                         "column length runs on the CUDA-core kernel")
     ap.add_argument("--readout", choices=["memory", "outer"], default="memory",
                     help="memory: six-memory form (q from M^q); outer: VisionHOPE-exact "
                          "readout with an outer query projection and channel-wise skip")
@@ -917,6 +937,9 @@ def main(argv=None):
     wl = synth.WORKLOADS[args.workload]
     if args.variant == "longmem":
         wl = wl.long_memory()
+    if args.chunk >= 0:
+        import dataclasses
+        wl = dataclasses.replace(wl, chunk=args.chunk)
     if args.gpus != dist_env()[1] and args.impl == "ours":
         ap.error(f"--gpus {args.gpus} needs torchrun with {args.gpus} processes "
                  f"(WORLD_SIZE={dist_env()[1]})")

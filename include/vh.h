@@ -145,6 +145,15 @@ typedef struct vh_params {
     void *workspace;           /* device, >= vh_workspace_size() bytes, 16-byte aligned;
                                   holds the normalised queries while the call runs */
     size_t workspace_bytes;
+    /* Bounded waits.  Every wait of the tensor-core kernels on an asynchronous copy or MMA
+     * gives up after a limit: the CTA then records VH_STAT_TIMEOUT (when stats are given),
+     * issues no further copy or MMA and runs to its end; vh_check reports VH_ERR_TIMEOUT
+     * and the call's results are invalid.  The context stays usable. */
+    long long wait_limit;      /* clock cycles before a wait gives up; 0 = 2^32 (about 2 s) */
+    int withhold_first_copy;   /* test hook, head_dim 32 tensor-core kernel only (else
+                                  VH_ERR_INVALID_ARG): the kernel never issues its first
+                                  input copy, so its first wait can only end by giving up,
+                                  with nothing asynchronous issued before or after */
 } vh_params;
 
 /* Fill *p with the pages' constants (gamma_eta 0.025, alpha_init 0.9, eps
@@ -313,7 +322,10 @@ size_t vh_block_workspace_size(const vh_params *p, const vh_block_weights *w, in
  * 2,796,202 (6 bytes per element); larger calls return VH_ERR_WORKSPACE.  p->workspace
  * and p->workspace_bytes are ignored; everything else is as in vh_scan_forward, whose
  * kernels run.  The first call on a device looks up the array's device address there
- * (make that first call before any stream capture).  Every call uses the same array and
+ * (make that first call before any stream capture) and keeps it for the life of the
+ * process: cudaDeviceReset, or anything else that destroys and recreates the device's
+ * primary context, can move the array, so do not call this entry point again on a device
+ * after resetting it in the same process.  Every call uses the same array and
  * rewrites it completely before reading it, so nothing needs clearing, but two calls
  * that overlap on the GPU (different streams, or another thread) race on it and corrupt
  * each other's queries: serialise them.  Without w_query it returns VH_ERR_INVALID_ARG

@@ -49,7 +49,10 @@ def _call(vhlib, B=1, Cc=32, d=32, H=4, W=4, dirs=15, chunk=0, x=FAKE, mem=FAKE,
     (dict(B=0), -1), (dict(d=48, Cc=96), -2), (dict(Cc=40), -1), (dict(x=FAKE + 8), -1),
     (dict(out=FAKE + 4), -1), (dict(x=0), -1), (dict(out=FAKE), -1),
     (dict(gate_mode=3), -1), (dict(alpha_init=1.0), -1), (dict(impl=7), -1),
-    (dict(x_dtype=5), -2),
+    (dict(x_dtype=5), -2), (dict(wait_limit=-5), -1),
+    # the withheld-copy hook belongs to the head_dim 32 tensor-core kernel only
+    (dict(withhold_first_copy=1, d=16), -1), (dict(withhold_first_copy=1, impl=1), -1),
+    (dict(withhold_first_copy=1, chunk=3), -1), (dict(withhold_first_copy=1, x_dtype=0), -1),
 ])
 def test_bad_arguments_are_rejected_on_the_host(vhlib, kw, status):
     st, msg = _call(vhlib, **kw)

@@ -1,6 +1,8 @@
 """vh_check on a GB300: the device status counters reach the caller.  Non-finite
-values are made from the input (a NaN pixel); an expired wait is represented by
-writing its counter, never by stalling the device."""
+values are made from the input (a NaN pixel).  An expired wait is made without stalling
+or faulting the device: a small wait limit with the test hook that never issues the
+kernel's first input copy, so the first wait can only give up and the kernel then issues
+no copy or MMA at all before it ends; the context stays usable afterwards."""
 import numpy as np
 import pytest
 
@@ -48,3 +50,27 @@ def test_check_reports_timeout_counter(vhlib):
     st[3] = 7
     with pytest.raises(vhlib.VhError, match="timeout"):
         vhlib.check(st)
+
+
+def test_expired_wait_reports_timeout_and_leaves_context_usable(vhlib, orc):
+    import torch
+    from tests._helpers import TOL, oracle_params_like, parity_err
+    wl = synth.Workload("t", 1, 8, 8, 1, 32, 0, "bf16", seed=5, alpha_init=0.999)
+    inp = synth.make_inputs(wl)
+    x = torch.from_numpy(inp.x_store.view(np.int16)).view(torch.bfloat16).cuda()
+    m = torch.from_numpy(inp.mem0).cuda()
+    for impl in ("tc_recur", "tc_wy"):
+        st = torch.zeros(8, dtype=torch.int64, device="cuda")
+        p = vhlib.ScanParams(alpha_init=wl.alpha_init, impl=impl, wait_limit=20000,
+                             withhold_first_copy=True)
+        vhlib.scan_forward(x, m, 32, stats=st, params=p)
+        with pytest.raises(vhlib.VhError, match="timeout"):
+            vhlib.check(st)
+        assert int(st[4].item()) == 4   # every CTA (4 routes x 1 head) gave up once
+        # the same context runs a normal call correctly afterwards
+        st = torch.zeros(8, dtype=torch.int64, device="cuda")
+        q = vhlib.ScanParams(alpha_init=wl.alpha_init, impl=impl)
+        out = vhlib.scan_forward(x, m, 32, stats=st, params=q)
+        vhlib.check(st)
+        o = orc.forward(inp.x64, inp.mem0, wl.H, wl.W, wl.nh, wl.d, params=oracle_params_like(orc, q))
+        assert parity_err(out.cpu().numpy(), o) < TOL

@@ -5,7 +5,8 @@ the caller passes only inputs and outputs.
 
 Checked through the C ABI against vh_scan_forward with a caller-allocated workspace, on
 two calls in a row with different shapes (the second call reuses the array the first
-one filled), and on the size limit.  This file is collected last on purpose."""
+one filled), on a call that fills the array almost to its limit, on a call that adds to
+out (accumulate), and on the size limit.  This file is collected last on purpose."""
 import ctypes
 
 import numpy as np
@@ -67,3 +68,42 @@ def test_static_scratch_rejects_what_does_not_fit(vhlib):
     assert b"static scratch" in vhlib.lib().vh_last_error()
     cp.w_query = None
     assert f(base, base, ctypes.byref(cp), H, W, 15, 0, base) == -1
+
+
+def _call_both(vhlib, f, wl, accumulate=False):
+    """The static entry and vh_scan_forward (caller workspace) on the same inputs; out
+    starts from the same values on both sides (NaN unless accumulating)."""
+    import torch
+    x, mem0, wq, skip, lam = _inputs(wl)
+    B, H, W, Cc = x.shape
+    if accumulate:
+        base = torch.randn(B, H, W, Cc, device="cuda")
+        out, ref = base.clone(), base.clone()
+    else:
+        out = torch.full((B, H, W, Cc), float("nan"), device="cuda")
+        ref = None
+    cp = vhlib.make_cparams(B, Cc, wl.d, wl.dtype == "bf16", None, accumulate=accumulate,
+                            dir_scale_ptr=lam.data_ptr(), stream_ptr=vhlib._stream_ptr(None),
+                            w_query_ptr=wq.data_ptr(), skip_ptr=skip.data_ptr())
+    st = f(x.data_ptr(), mem0.data_ptr(), ctypes.byref(cp), H, W, 15, 0, out.data_ptr())
+    assert st == 0, vhlib.lib().vh_last_error().decode()
+    ref = vhlib.scan_forward(x, mem0, wl.d, w_query=wq, skip=skip, dir_scale=lam, out=ref,
+                             accumulate=accumulate)
+    torch.cuda.synchronize()
+    return out.cpu().numpy(), ref.cpu().numpy()
+
+
+def test_static_scratch_near_its_limit(vhlib):
+    """Nine stage-1 images, 97 % of the array: the whole scratch is usable."""
+    f = _entry(vhlib)
+    wl = synth.Workload("near", 9, 56, 56, 3, 32, 0, "bf16", seed=73, alpha_init=0.999)
+    assert 0.95 * STATIC_LIMIT < wl.B * wl.N * wl.Cc <= STATIC_LIMIT
+    got, ref = _call_both(vhlib, f, wl)
+    assert parity_err(got, ref) < TOL
+
+
+def test_static_scratch_accumulates(vhlib):
+    f = _entry(vhlib)
+    wl = synth.Workload("acc", 2, 10, 12, 2, 32, 0, "bf16", seed=74, alpha_init=0.999)
+    got, ref = _call_both(vhlib, f, wl, accumulate=True)
+    assert parity_err(got, ref) < TOL

@@ -51,6 +51,7 @@ class CParams(ctypes.Structure):
         ("stream", ctypes.c_void_p),
         ("w_query", ctypes.c_void_p), ("skip", ctypes.c_void_p),
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+        ("wait_limit", ctypes.c_longlong), ("withhold_first_copy", ctypes.c_int),
     ]
 
 
@@ -81,6 +82,8 @@ class ScanParams:
     forced_alpha: float = 0.0
     control_flags: int = 0
     impl: str = "auto"
+    wait_limit: int = 0               # cycles before a bounded wait gives up; 0 = 2^32
+    withhold_first_copy: bool = False  # test hook: the first input copy is never issued
 
 
 _lib = None
@@ -131,6 +134,18 @@ def header_functions() -> list[str]:
     return sorted(set(re.findall(r"\b(vh_[a-z_]+)\s*\(", text)))
 
 
+def shard_images(global_batch: int, world: int, rank: int) -> range:
+    """Images of a batch held by one rank when the batch is sharded across ``world``
+    ranks: contiguous blocks, the first ``global_batch % world`` ranks one image larger.
+    Images are independent (every route of every image starts from memories0), so the
+    shards need no exchange; the union over ranks is the batch, each image once."""
+    if world < 1 or not 0 <= rank < world or global_batch < 0:
+        raise ValueError(f"shard_images({global_batch}, {world}, {rank})")
+    base, extra = divmod(global_batch, world)
+    start = rank * base + min(rank, extra)
+    return range(start, start + base + (1 if rank < extra else 0))
+
+
 def _check(status: int):
     if status != 0:
         L = lib()
@@ -152,7 +167,8 @@ def make_cparams(batch: int, channels: int, head_dim: int, x_is_bf16: bool,
                    p.gate_mode, p.forced_eta, p.forced_alpha, p.control_flags,
                    stats_ptr or None, IMPL[p.impl], 1 if accumulate else 0,
                    stream_ptr or None, w_query_ptr or None, skip_ptr or None,
-                   workspace_ptr or None, workspace_bytes)
+                   workspace_ptr or None, workspace_bytes, int(p.wait_limit),
+                   1 if p.withhold_first_copy else 0)
 
 
 def _stream_ptr(stream) -> int:

@@ -118,6 +118,8 @@ vh::ScanArgs make_args(const void *x, const float *memories0, const vh_params *p
     a.forced_eta = p->forced_eta;
     a.forced_alpha = p->forced_alpha;
     a.control_flags = p->control_flags;
+    a.wait_limit = p->wait_limit;
+    a.withhold_first_copy = p->withhold_first_copy;
 
     return a;
 }
@@ -283,6 +285,12 @@ vh_status vh_scan_forward(const void *x, const float *memories0, const vh_params
     }
     if (p->skip && (reinterpret_cast<uintptr_t>(p->skip) & 3u))
         return fail(VH_ERR_INVALID_ARG, "skip must be 4-byte aligned");
+    if (p->wait_limit < 0) return fail(VH_ERR_INVALID_ARG, "wait_limit %lld < 0", p->wait_limit);
+    if (p->withhold_first_copy &&
+        (p->head_dim != 32 || p->x_dtype != VH_DTYPE_BF16 || p->impl == VH_IMPL_SIMT ||
+         !(chunk == 0 || (chunk == W && chunk == H)) || p->channels % 8))
+        return fail(VH_ERR_INVALID_ARG, "withhold_first_copy is a hook of the head_dim 32 "
+                    "tensor-core kernel (bf16 x, row/column chunks)");
 
     vh::ScanArgs a = make_args(x, memories0, p, H, W, dirs, chunk, out);
     a.qhat = exact ? static_cast<const __nv_bfloat16 *>(p->workspace) : nullptr;

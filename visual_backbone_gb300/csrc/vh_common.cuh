@@ -46,6 +46,10 @@ struct ScanArgs {
     // |k_raw|^2, s_eta, s_alpha, |k|^2, |delta|^2, |q_raw|^2 and two unused slots
     float *rec;
     size_t rec_stride;
+    // bounded waits: cycles before a wait gives up (0 = 2^32); test hook that never issues
+    // the first input copy (head_dim 32 tensor-core kernel)
+    long long wait_limit;
+    int withhold_first_copy;
 };
 
 // Floats of one token record (layout above); the scalar slots follow the three vectors.

@@ -26,7 +26,9 @@ static __device__ __align__(256) unsigned char g_qscratch[kStaticScratchBytes];
 std::mutex g_mu;
 void *g_scratch_ptr[64] = {};
 
-// The array's device address on the current device, looked up on the first call there.
+// The array's device address on the current device, looked up on the first call there and
+// kept for the process (a device reset that recreates the primary context can move the
+// array; the header tells callers not to use this entry point after one).
 cudaError_t scratch_address(void **ptr)
 {
     int dev = 0;

@@ -313,7 +313,7 @@ __global__ void __launch_bounds__(NT, 3)
     volatile int *role_slot = reinterpret_cast<volatile int *>(sm + LY::BAR + 76);
     volatile int *delta_form = reinterpret_cast<volatile int *>(sm + LY::BAR + 80);
     volatile int *vote = reinterpret_cast<volatile int *>(sm + LY::BAR + 96);  // 2 warp flags
-    const Waiter wt{abort_flag, a.stats};
+    const Waiter wt{abort_flag, a.stats, a.wait_limit > 0 ? a.wait_limit : (1ll << 32)};
 
     unsigned char *sX = sm + OFF_X, *sS = sm + OFF_S, *sQ = sm + OFF_Q, *sG = sm + OFF_G;
     float *Kf = reinterpret_cast<float *>(sm + LY::KF);
@@ -383,7 +383,9 @@ __global__ void __launch_bounds__(NT, 3)
             tma_load_5d(smem_u32(sQ + q * QX_LBO), tq, h * D + 8 * q, box_start(s), line_of(c), b, 0,
                         mb_q);
     };
-    if (issuer) {
+    // (test hook: with the first copies withheld the first wait can only give up, and the
+    // kernel then issues no asynchronous work at all)
+    if (issuer && !a.withhold_first_copy) {
         issue_x(0, 0);
         if (exact) issue_q(0, 0);
     }

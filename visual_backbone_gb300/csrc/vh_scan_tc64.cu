@@ -192,7 +192,7 @@ __global__ void __launch_bounds__(NT, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + OFF_BAR + 72);
     volatile int *delta_form = reinterpret_cast<volatile int *>(sm + OFF_BAR + 80);
     volatile int *vote = reinterpret_cast<volatile int *>(sm + OFF_BAR + 96);
-    const Waiter wt{abort_flag, a.stats};
+    const Waiter wt{abort_flag, a.stats, a.wait_limit > 0 ? a.wait_limit : (1ll << 32)};
 
     unsigned char *sX = sm + OFF_X, *sS = sm + OFF_S, *sQ = sm + OFF_Q, *sG = sm + OFF_G;
     float *Kf = reinterpret_cast<float *>(sm + OFF_KF);

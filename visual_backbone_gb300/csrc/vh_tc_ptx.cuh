@@ -204,16 +204,19 @@ __device__ __forceinline__ float sumsq32(const float (&v)[32])
 struct Waiter {
     volatile int *abort_flag;
     unsigned long long *stats;
-    // Bounded wait for `parity` on an mbarrier; true when it completed.
+    long long limit = 1ll << 32;  // clock cycles (~2 s at the GB300 clock)
+    // Bounded wait for `parity` on an mbarrier; true when it completed.  On expiry the CTA
+    // is flagged to abort: every later wait returns false at once and the kernels issue no
+    // further copy or MMA.
     __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity) const
     {
         if (*abort_flag) return false;
         if (mbar_try(bar, parity)) return true;
         const long long t0 = clock64();
         while (true) {
-            if (mbar_try_sleep(bar, parity, 20000u)) return true;
+            if (mbar_try_sleep(bar, parity, limit < 20000 ? (uint32_t)limit : 20000u)) return true;
             if (*abort_flag) return false;
-            if (clock64() - t0 > (1ll << 32)) {  // ~2 s at the GB300 clock
+            if (clock64() - t0 > limit) {
                 if (atomicExch((int *)abort_flag, 1) == 0 && stats)
                     atomicAdd(stats + VH_STAT_TIMEOUT, 1ull);
                 return false;

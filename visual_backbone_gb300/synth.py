@@ -86,13 +86,17 @@ class Inputs:
     mem0: np.ndarray
 
 
-def make_inputs(wl: Workload, batch: int | None = None) -> Inputs:
-    """Draw the workload's inputs.  ``batch`` < wl.B draws only the first images
-    (same values as the full draw, since images are drawn in order)."""
+def make_inputs(wl: Workload, batch: int | None = None, first_image: int = 0) -> Inputs:
+    """Draw the workload's inputs.  Images are drawn in order from one stream after
+    memories0, so ``batch`` images starting at ``first_image`` are exactly those images of
+    any longer draw: a rank holding images [s, s + n) of a batch sharded across ranks draws
+    them with first_image = s, batch = n (the images before s are drawn and discarded)."""
     rng = np.random.default_rng(wl.seed)
     d = wl.d
     mem0 = (rng.standard_normal((4, wl.nh, 4 * d * d + 2 * d)) / np.sqrt(d)).astype(np.float32)
     B = wl.B if batch is None else batch
+    for _ in range(first_image):
+        rng.standard_normal((wl.H, wl.W, wl.Cc))
     x = rng.standard_normal((B, wl.H, wl.W, wl.Cc)).astype(np.float32)
     if wl.dtype == "bf16":
         bits = f32_to_bf16_bits(x)
@@ -136,16 +140,21 @@ def make_block_weights(D: int, Dm: int, seed: int, hidden: int | None = None) ->
         w_ff2=lin(D, hidden), b_ff2=vec(D))
 
 
-def make_block_inputs(B: int, H: int, W: int, D: int, Dm: int, d: int, seed: int) -> dict:
+def make_block_inputs(B: int, H: int, W: int, D: int, Dm: int, d: int, seed: int,
+                      first_image: int = 0) -> dict:
     """x [B][H][W][D] ~ N(0, 1) fp32, the block weights, and the operator's inputs:
     memories0 ~ N(0, 1/d), the outer query W_q ~ N(0, 1/D_m), the skip ~ N(0, 1) and the
-    route scales lambda ~ U(0.5, 1.5) (all fp32)."""
+    route scales lambda ~ U(0.5, 1.5) (all fp32).  The parameters are drawn first and the
+    images after them in order, so ``first_image`` selects a rank's images of a sharded
+    batch while every rank draws the same parameters."""
     rng = np.random.default_rng(seed)
-    x = rng.standard_normal((B, H, W, D)).astype(np.float32)
     nh = Dm // d
-    return dict(
-        x=x, weights=make_block_weights(D, Dm, seed),
-        mem0=(rng.standard_normal((4, nh, 4 * d * d + 2 * d)) / np.sqrt(d)).astype(np.float32),
-        w_query=(rng.standard_normal((Dm, Dm)) / np.sqrt(Dm)).astype(np.float32),
-        skip=rng.standard_normal((4, Dm)).astype(np.float32),
-        dir_scale=rng.uniform(0.5, 1.5, (4, Dm)).astype(np.float32), nh=nh)
+    mem0 = (rng.standard_normal((4, nh, 4 * d * d + 2 * d)) / np.sqrt(d)).astype(np.float32)
+    w_query = (rng.standard_normal((Dm, Dm)) / np.sqrt(Dm)).astype(np.float32)
+    skip = rng.standard_normal((4, Dm)).astype(np.float32)
+    dir_scale = rng.uniform(0.5, 1.5, (4, Dm)).astype(np.float32)
+    for _ in range(first_image):
+        rng.standard_normal((H, W, D))
+    x = rng.standard_normal((B, H, W, D)).astype(np.float32)
+    return dict(x=x, weights=make_block_weights(D, Dm, seed), mem0=mem0, w_query=w_query,
+                skip=skip, dir_scale=dir_scale, nh=nh)
