@@ -297,13 +297,14 @@ typedef struct {
  * operator's optional inputs as in vh_scan_forward (w_query, skip, dir_scale, stats,
  * impl, gate and step-control constants); the operator runs all four routes with
  * row/column-aligned chunks.  p->workspace must hold vh_block_workspace_size() bytes,
- * 16-byte aligned: the block's intermediates, the operator's query planes and the
- * GEMMs' scratch.  Activations between layers are bf16 (LN outputs, Z, Y, the FFN's
- * hidden layer before and after GELU); the residual stream is fp32.  p->accumulate and p->memories_out must be 0 / NULL.
+ * 16-byte aligned: the block's intermediates and the operator's query planes.
+ * Activations between layers are bf16 (LN outputs, Z, Y, the FFN's hidden layer before
+ * and after GELU); the residual stream is fp32.  p->accumulate and p->memories_out must
+ * be 0 / NULL.
  *
- * The four pointwise layers run as cuBLASLt GEMMs (bf16 operands, fp32 accumulation,
- * bias and residual in the epilogue); the library keeps one cuBLASLt handle per device,
- * created on first use.  Errors: as vh_scan_forward, plus VH_ERR_CUDA for a GEMM failure.
+ * The four pointwise layers run as the library's own tcgen05 GEMMs (bf16 operands, fp32
+ * accumulation in TMEM) with the bias, the residual and (FFN1) the GELU in their
+ * epilogues.  Errors: as vh_scan_forward, plus VH_ERR_CUDA for a GEMM launch failure.
  */
 vh_status vh_block_forward(const float *x, const float *memories0, const vh_params *p,
                            const vh_block_weights *w, int H, int W, float *out);

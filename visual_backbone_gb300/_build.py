@@ -16,7 +16,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libvh.so")
 SOURCES = ["vh_api.cu", "vh_scan_simt.cu", "vh_scan_tc.cu", "vh_scan_tc64.cu", "vh_scan_bwd.cu",
-           "vh_qproj.cu", "vh_qproj_tc.cu", "vh_block.cu", "vh_noalloc.cu"]
+           "vh_qproj.cu", "vh_qproj_tc.cu", "vh_block.cu", "vh_gemm_tc.cu", "vh_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC = os.environ.get("NVCC", "nvcc")
 
@@ -59,7 +59,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False) -> 
     if errors:
         raise RuntimeError("nvcc failed:\n" + "\n".join(errors))
     tmp = LIB + f".tmp{os.getpid()}"
-    subprocess.check_call([NVCC, *ARCH, "-shared", "-o", tmp, *objs, "-lcublasLt"])
+    subprocess.check_call([NVCC, *ARCH, "-shared", "-o", tmp, *objs])
     os.replace(tmp, LIB)
     return LIB
 

@@ -26,9 +26,9 @@ cudaError_t launch_dwgate(const float *u, const float *w, const float *b, __nv_b
 cudaError_t launch_posdw(const float *y, const __nv_bfloat16 *z, const float *w, const float *b,
                          __nv_bfloat16 *yb, long npix, int C, int H, int W, cudaStream_t st);
 cudaError_t launch_gelu(__nv_bfloat16 *h, const float *b, long n, int hidden, cudaStream_t st);
-int block_gemm(int m, int n, int k, const __nv_bfloat16 *wt, const __nv_bfloat16 *act,
-               const float *bias, const float *res, void *out, bool out_bf16, void *ws,
-               size_t ws_bytes, cudaStream_t st);
+cudaError_t launch_gemm_tc(int M, int N, int K, const __nv_bfloat16 *w, const __nv_bfloat16 *act,
+                           const float *bias, const float *res, void *out, int epi,
+                           cudaStream_t st);
 size_t bwd_floats_per_scan(int d, int nck, int lmax);
 }  // namespace vh
 
@@ -152,10 +152,8 @@ bool bwd_token_records(const vh_params *p, int H, int W, int chunk)
 
 // Byte offsets of the block's intermediates in its workspace (256-byte aligned regions).
 struct BlockLayout {
-    size_t x0, a, u, z, yb, h, qhat, lt, total;
+    size_t x0, a, u, z, yb, h, qhat, total;
 };
-
-constexpr size_t kLtWorkspace = 32u << 20;  // cuBLASLt scratch
 
 BlockLayout block_layout(const vh_params *p, const vh_block_weights *w, int H, int W)
 {
@@ -170,7 +168,6 @@ BlockLayout block_layout(const vh_params *p, const vh_block_weights *w, int H, i
     L.yb = take(N * Dm * 2);
     L.h = take(N * Hd * 2);
     L.qhat = take(p->w_query ? 6 * N * Dm : 0);
-    L.lt = take(kLtWorkspace);
     L.total = o;
     return L;
 }
@@ -378,17 +375,15 @@ vh_status vh_block_forward(const float *x, const float *memories0, const vh_para
     __nv_bfloat16 *z = reinterpret_cast<__nv_bfloat16 *>(ws + L.z);
     __nv_bfloat16 *yb = reinterpret_cast<__nv_bfloat16 *>(ws + L.yb);
     __nv_bfloat16 *h = reinterpret_cast<__nv_bfloat16 *>(ws + L.h);
-    void *lt = ws + L.lt;
     auto bw = [](const void *q) { return static_cast<const __nv_bfloat16 *>(q); };
     cudaStream_t st = static_cast<cudaStream_t>(p->stream);
     cudaError_t e;
-    int g;
     // X0 = X + CPE(X), A = LN1(X0)
     if ((e = vh::launch_cpe_ln(x, w->cpe_w, w->cpe_b, w->ln1_g, w->ln1_b, eps, x0, a, B, H, W, D, st)))
         return cuda_fail(e, "CPE + LN1 launch");
     // U = A W_in^T + b_in
-    if ((g = vh::block_gemm(Dm, (int)N, D, bw(w->w_in), a, w->b_in, nullptr, u, false, lt, kLtWorkspace, st)))
-        return fail(VH_ERR_CUDA, "Proj_in GEMM: cuBLASLt status %d", g);
+    if ((e = vh::launch_gemm_tc((int)N, Dm, D, bw(w->w_in), a, w->b_in, nullptr, u, 0, st)))
+        return cuda_fail(e, "Proj_in GEMM launch");
     // Z = U + SiLU(DW(U))
     if ((e = vh::launch_dwgate(u, w->dw_w, w->dw_b, z, N, Dm, H, W, st)))
         return cuda_fail(e, "gated depthwise launch");
@@ -401,15 +396,15 @@ vh_status vh_block_forward(const float *x, const float *memories0, const vh_para
     if ((e = vh::launch_posdw(u, z, w->pos_w, w->pos_b, yb, N, Dm, H, W, st)))
         return cuda_fail(e, "positional depthwise launch");
     // X1 = X0 + Y W_out^T + b_out, into out
-    if ((g = vh::block_gemm(D, (int)N, Dm, bw(w->w_out), yb, w->b_out, x0, out, false, lt, kLtWorkspace, st)))
-        return fail(VH_ERR_CUDA, "Proj_out GEMM: cuBLASLt status %d", g);
+    if ((e = vh::launch_gemm_tc((int)N, D, Dm, bw(w->w_out), yb, w->b_out, x0, out, 0, st)))
+        return cuda_fail(e, "Proj_out GEMM launch");
     // out = X1 + W_ff2 GELU(W_ff1 LN2(X1) + b_ff1) + b_ff2
     if ((e = vh::launch_ln(out, w->ln2_g, w->ln2_b, eps, a, N, D, st))) return cuda_fail(e, "LN2 launch");
-    if ((g = vh::block_gemm(Hd, (int)N, D, bw(w->w_ff1), a, nullptr, nullptr, h, true, lt, kLtWorkspace, st)))
-        return fail(VH_ERR_CUDA, "FFN1 GEMM: cuBLASLt status %d", g);
-    if ((e = vh::launch_gelu(h, w->b_ff1, (long)N * Hd, Hd, st))) return cuda_fail(e, "GELU launch");
-    if ((g = vh::block_gemm(D, (int)N, Hd, bw(w->w_ff2), h, w->b_ff2, out, out, false, lt, kLtWorkspace, st)))
-        return fail(VH_ERR_CUDA, "FFN2 GEMM: cuBLASLt status %d", g);
+    // H = bf16(GELU(bf16(LN2(X1) W_ff1^T) + b_ff1)), the GELU in the GEMM's epilogue
+    if ((e = vh::launch_gemm_tc((int)N, Hd, D, bw(w->w_ff1), a, w->b_ff1, nullptr, h, 1, st)))
+        return cuda_fail(e, "FFN1 GEMM launch");
+    if ((e = vh::launch_gemm_tc((int)N, D, Hd, bw(w->w_ff2), h, w->b_ff2, out, out, 0, st)))
+        return cuda_fail(e, "FFN2 GEMM launch");
     return VH_OK;
 }
 

@@ -15,7 +15,6 @@
 // the gated branch, the positional branch with the cast for Proj_out), LN1 and LN2 (one
 // warp per pixel), GELU with FFN1's bias.  bf16 rounding points: LN1's and LN2's outputs,
 // Z, Y before Proj_out, FFN1's product (before its bias) and GELU's output.
-#include <cublasLt.h>
 
 #include <mutex>
 
@@ -156,74 +155,6 @@ __global__ void __launch_bounds__(256) gelu_kernel(uint4 *__restrict__ h, const 
         }
         h[e] = r;
     }
-}
-
-// ------------------------------------------------------------------ GEMMs (cuBLASLt)
-
-namespace {
-
-std::mutex g_lt_mu;
-cublasLtHandle_t g_lt[64] = {};
-
-cublasStatus_t lt_handle(cublasLtHandle_t *h)
-{
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return CUBLAS_STATUS_NOT_INITIALIZED;
-    std::lock_guard<std::mutex> lk(g_lt_mu);
-    if (!g_lt[dev]) {
-        const cublasStatus_t s = cublasLtCreate(&g_lt[dev]);
-        if (s != CUBLAS_STATUS_SUCCESS) return s;
-    }
-    *h = g_lt[dev];
-    return CUBLAS_STATUS_SUCCESS;
-}
-
-}  // namespace
-
-// out[n][m] = act[n][k] . wt[m][k]^T (+ bias[m]) (+ res[n][m]): row-major bf16 operands,
-// fp32 accumulation, an fp32 result (or bf16 with out_bf16, then without bias or res).
-// res may equal out.  Returns the cublasStatus_t.
-int block_gemm(int m, int n, int k, const __nv_bfloat16 *wt, const __nv_bfloat16 *act,
-               const float *bias, const float *res, void *out, bool out_bf16, void *ws,
-               size_t ws_bytes, cudaStream_t st)
-{
-    cublasLtHandle_t lt;
-    cublasStatus_t s = lt_handle(&lt);
-    if (s != CUBLAS_STATUS_SUCCESS) return (int)s;
-    // column-major view: out^T (m x n) = wt (k x m)^T . act^T (k x n) [+ res^T]
-    cublasLtMatmulDesc_t op = nullptr;
-    cublasLtMatrixLayout_t la = nullptr, lb = nullptr, lc = nullptr, ld = nullptr;
-    cublasLtMatmulPreference_t pref = nullptr;
-    const cublasOperation_t tA = CUBLAS_OP_T, tB = CUBLAS_OP_N;
-    const cublasLtEpilogue_t epi = bias ? CUBLASLT_EPILOGUE_BIAS : CUBLASLT_EPILOGUE_DEFAULT;
-    const float alpha = 1.0f, beta = res ? 1.0f : 0.0f;
-    cublasLtMatmulHeuristicResult_t hr{};
-    int found = 0;
-    do {
-        if ((s = cublasLtMatmulDescCreate(&op, CUBLAS_COMPUTE_32F, CUDA_R_32F))) break;
-        if ((s = cublasLtMatmulDescSetAttribute(op, CUBLASLT_MATMUL_DESC_TRANSA, &tA, sizeof tA))) break;
-        if ((s = cublasLtMatmulDescSetAttribute(op, CUBLASLT_MATMUL_DESC_TRANSB, &tB, sizeof tB))) break;
-        if ((s = cublasLtMatmulDescSetAttribute(op, CUBLASLT_MATMUL_DESC_EPILOGUE, &epi, sizeof epi))) break;
-        if (bias && (s = cublasLtMatmulDescSetAttribute(op, CUBLASLT_MATMUL_DESC_BIAS_POINTER, &bias,
-                                                        sizeof bias))) break;
-        if ((s = cublasLtMatrixLayoutCreate(&la, CUDA_R_16BF, k, m, k))) break;
-        if ((s = cublasLtMatrixLayoutCreate(&lb, CUDA_R_16BF, k, n, k))) break;
-        if ((s = cublasLtMatrixLayoutCreate(&lc, out_bf16 ? CUDA_R_16BF : CUDA_R_32F, m, n, m))) break;
-        ld = lc;
-        if ((s = cublasLtMatmulPreferenceCreate(&pref))) break;
-        if ((s = cublasLtMatmulPreferenceSetAttribute(pref, CUBLASLT_MATMUL_PREF_MAX_WORKSPACE_BYTES,
-                                                      &ws_bytes, sizeof ws_bytes))) break;
-        if ((s = cublasLtMatmulAlgoGetHeuristic(lt, op, la, lb, lc, ld, pref, 1, &hr, &found))) break;
-        if (!found) { s = CUBLAS_STATUS_NOT_SUPPORTED; break; }
-        s = cublasLtMatmul(lt, op, &alpha, wt, la, act, lb, &beta, res ? res : out, lc, out, ld,
-                           &hr.algo, ws, ws_bytes, st);
-    } while (0);
-    if (pref) cublasLtMatmulPreferenceDestroy(pref);
-    if (lc) cublasLtMatrixLayoutDestroy(lc);
-    if (lb) cublasLtMatrixLayoutDestroy(lb);
-    if (la) cublasLtMatrixLayoutDestroy(la);
-    if (op) cublasLtMatmulDescDestroy(op);
-    return (int)s;
 }
 
 // ------------------------------------------------------------------ launches

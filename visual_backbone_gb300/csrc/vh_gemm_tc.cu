@@ -1,0 +1,317 @@
+// vh_gemm_tc.cu -- the pointwise layers of the VisionHOPE block ("VisionHOPE: Visual
+// Backbones as Self-Modifying Learning Systems", Sec. 2.3 Eq. (27), App. B.5: Proj_in,
+// Proj_out and the two FFN layers) as tcgen05 GEMMs with fused epilogues:
+//   out[m][n] = act[m][:] . w[n][:]  (+ bias[n])  (+ res[m][n])        fp32 out, or
+//   out[m][n] = bf16(GELU(bf16(act[m][:] . w[n][:]) + bias[n]))        bf16 out (FFN1 + GELU)
+// act [M][K] and w [N][K] are row-major bf16 (both K-major operands), fp32 accumulation in
+// TMEM.  GELU is the exact erf form; the bf16 rounding of the product before its bias is
+// the block's rounding point.
+//
+// Persistent CTAs (one per SM, 448 threads): warp 0 issues the TMA copies of a three-stage
+// ring (per stage 64 K-elements of a 128-row activation tile and of the BN-row weight tile,
+// each one box of whole 128-byte rows in the 128-byte swizzled K-major layout), warp 1 (one
+// lane) issues the MMAs (M = 128, N = BN <= 256, K = 16) into one of two TMEM accumulators,
+// and warps 2..13 (thread = tile row, three warps per row quarter taking every third
+// 32-column chunk) run the epilogue of one tile while the next one accumulates.  The
+// epilogue turns each 32 x 32 chunk around in a padded shared tile, so its global loads
+// and stores run along rows.  Tiles are ordered with the N tiles of one M tile adjacent, so an
+// activation tile is read from HBM once and from L2 for its other N tiles.  Every mbarrier
+// wait is bounded.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "vh_tc_ptx.cuh"
+
+namespace vh {
+namespace gemm {
+
+using namespace vh::tc;
+
+constexpr int BM = 128, BK = 64, STAGES = 3;
+constexpr int EPI_WARPS = 12;  // warps 2..13: three per TMEM lane quarter, every third 32-column chunk
+constexpr int NT = 32 * (2 + EPI_WARPS);
+constexpr int MAX_BN = 256;
+constexpr int A_STAGE = BM * BK * 2;                 // 16 KB
+constexpr int B_STAGE = MAX_BN * BK * 2;             // 32 KB
+constexpr int OFF_A = 0;
+constexpr int OFF_B = OFF_A + STAGES * A_STAGE;
+constexpr int STG_WORDS = 32 * 33;                  // per epilogue warp: a 32 x 32 chunk, padded
+constexpr int OFF_STG = OFF_B + STAGES * B_STAGE;
+constexpr int OFF_BAR = OFF_STG + EPI_WARPS * STG_WORDS * 4;
+constexpr int SMEM_BYTES = OFF_BAR + 256;
+static_assert(SMEM_BYTES <= 227 * 1024, "one CTA per SM");
+static_assert(A_STAGE % 1024 == 0 && B_STAGE % 1024 == 0 && OFF_B % 1024 == 0, "swizzled tiles 1 KB aligned");
+
+enum { EPI_F32 = 0, EPI_GELU_BF16 = 1 };
+
+struct GemmArgs {
+    const float *bias;  // [N] or nullptr
+    const float *res;   // [M][N] fp32 or nullptr (may equal out)
+    void *out;          // [M][N] fp32 (EPI_F32) or bf16 (EPI_GELU_BF16)
+    int M, N, K;
+    int BN, ntn, nkb;   // N tile, N tiles, K blocks of BK
+    int epi;
+    unsigned long long *stats;  // timeout counter (or nullptr)
+};
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *tm, int c0, int c1, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major operand in the 128-byte swizzled layout:
+// rows of 64 bf16 (128 bytes) with their 16-byte chunks permuted by row % 8 (the layout
+// the TMA writes with 128-byte swizzle), 8-row groups 1 KB apart, the tile 1 KB aligned.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t addr)
+{
+    return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+__device__ __forceinline__ float gelu_erf(float a)
+{
+    return 0.5f * a * (1.0f + erff(a * 0.70710678118654752f));
+}
+
+__global__ void __launch_bounds__(NT, 1)
+    gemm_tc_kernel(const GemmArgs g, const __grid_constant__ CUtensorMap tm_a,
+                   const __grid_constant__ CUtensorMap tm_b)
+{
+    extern __shared__ __align__(1024) unsigned char sm[];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + OFF_BAR);
+    // bars[0..3] full, [4..7] empty, [8..9] tmem full, [10..11] tmem empty
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + OFF_BAR + 128);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + OFF_BAR + 136);
+    const Waiter wt{abort_flag, g.stats};
+    const int BN = g.BN;
+    const uint32_t tcols = BN <= 64 ? 128 : (BN <= 128 ? 256 : 512);  // two accumulators
+
+    if (tid == 0) {
+        *abort_flag = 0;
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(smem_u32(&bars[s]), 1);
+            mbar_init(smem_u32(&bars[4 + s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&bars[8 + b]), 1);
+            mbar_init(smem_u32(&bars[10 + b]), EPI_WARPS);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)), "r"(tcols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_before();
+    __syncthreads();
+    tc_after();
+    const uint32_t tbase = *tmem_slot;
+    const int ntiles = ((g.M + BM - 1) / BM) * g.ntn;
+    const uint32_t a_bytes = BM * BK * 2, b_bytes = (uint32_t)BN * BK * 2;
+
+    if (warp == 0) {
+        // ---- TMA producer (one lane)
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+                const int tm = t / g.ntn, tn = t % g.ntn;
+                for (int kb = 0; kb < g.nkb; ++kb) {
+                    if (!wt.wait(smem_u32(&bars[4 + s]), ph ^ 1)) break;  // stage free
+                    const uint32_t full = smem_u32(&bars[s]);
+                    mbar_expect_tx(full, a_bytes + b_bytes);
+                    const uint32_t sa = smem_u32(sm + OFF_A + s * A_STAGE);
+                    const uint32_t sb = smem_u32(sm + OFF_B + s * B_STAGE);
+                    tma_load_2d(sa, &tm_a, kb * BK, tm * BM, full);
+                    tma_load_2d(sb, &tm_b, kb * BK, tn * BN, full);
+                    if (++s == STAGES) { s = 0; ph ^= 1; }
+                }
+                if (*abort_flag) break;
+            }
+        }
+    } else if (warp == 1) {
+        // ---- MMA issuer (one lane)
+        if (lane == 0) {
+            int s = 0, acc = 0;
+            uint32_t ph = 0, aph[2] = {0, 0};
+            const uint32_t idesc = idesc_bf16(BM, BN);
+            for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+                if (!wt.wait(smem_u32(&bars[10 + acc]), aph[acc] ^ 1)) break;  // accumulator free
+                aph[acc] ^= 1;
+                tc_after();
+                const uint32_t dt = tbase + (uint32_t)(acc * BN);
+                for (int kb = 0; kb < g.nkb; ++kb) {
+                    if (!wt.wait(smem_u32(&bars[s]), ph)) break;  // stage landed
+                    tc_after();
+                    const uint64_t da = sdesc_sw128(smem_u32(sm + OFF_A + s * A_STAGE));
+                    const uint64_t db = sdesc_sw128(smem_u32(sm + OFF_B + s * B_STAGE));
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k)  // K step of 16 elements: 32 bytes into each row
+                        mma(dt, dadd(da, 32 * k), dadd(db, 32 * k), idesc, (kb | k) != 0);
+                    mma_commit(smem_u32(&bars[4 + s]));  // the stage is free once these complete
+                    if (++s == STAGES) { s = 0; ph ^= 1; }
+                }
+                if (*abort_flag) break;
+                mma_commit(smem_u32(&bars[8 + acc]));  // the tile's accumulator is complete
+                acc ^= 1;
+            }
+        }
+    } else {
+        // ---- epilogue: thread = tile row (TMEM lane), 32 columns per TMEM load; the three
+        // warps of a lane quarter take every third chunk
+        const int q = warp & 3;  // TMEM lane quarter of this warp
+        const int part = (warp - 2) >> 2;  // which third of the chunks
+        const uint32_t lrow = ((uint32_t)q * 32u) << 16;
+        float *stg = reinterpret_cast<float *>(sm + OFF_STG) + (warp - 2) * STG_WORDS;
+        int acc = 0;
+        uint32_t fph[2] = {0, 0};
+        for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+            const int tm = t / g.ntn, tn = t % g.ntn;
+            const bool ok = wt.wait(smem_u32(&bars[8 + acc]), fph[acc]);
+            fph[acc] ^= 1;
+            tc_after();
+            const int mbase = tm * BM + 32 * q;  // first of this warp's 32 rows
+            for (int cb = 32 * part; ok && cb < BN; cb += 32 * (EPI_WARPS / 4)) {
+                float v[32];
+                tmem_ld32(tbase + lrow + (uint32_t)(acc * BN + cb), v);
+                const int n0 = tn * BN + cb;
+                if (n0 >= g.N) continue;
+                // the chunk (row per lane) goes through the warp's staging tile so that the
+                // global accesses run along rows: lane = column (fp32) or 32-bit word (bf16)
+                if (g.epi == EPI_F32) {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) stg[lane * 33 + e] = v[e];
+                    __syncwarp();
+                    const int n = n0 + lane;
+                    const float bn = (g.bias && n < g.N) ? __ldg(g.bias + n) : 0.0f;
+                    float *out = reinterpret_cast<float *>(g.out);
+                    // the residual rows first, all in flight together (they may be out itself)
+                    float rv[32];
+#pragma unroll
+                    for (int rr = 0; rr < 32; ++rr) {
+                        const int m = mbase + rr;
+                        rv[rr] = (g.res && m < g.M && n < g.N) ? g.res[(size_t)m * g.N + n] : 0.0f;
+                    }
+#pragma unroll
+                    for (int rr = 0; rr < 32; ++rr) {
+                        const int m = mbase + rr;
+                        if (m < g.M && n < g.N)
+                            out[(size_t)m * g.N + n] = (stg[rr * 33 + lane] + bn) + rv[rr];
+                    }
+                    __syncwarp();
+                } else {
+                    uint32_t *stw = reinterpret_cast<uint32_t *>(stg);
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        const float b0 = (n0 + e < g.N) ? __ldg(g.bias + n0 + e) : 0.0f;
+                        const float b1 = (n0 + e + 1 < g.N) ? __ldg(g.bias + n0 + e + 1) : 0.0f;
+                        // the product rounded to bf16, then the bias and GELU, rounded again
+                        const float p0 = __bfloat162float(__float2bfloat16_rn(v[e])) + b0;
+                        const float p1 = __bfloat162float(__float2bfloat16_rn(v[e + 1])) + b1;
+                        stw[lane * 17 + e / 2] = pack_bf16x2_rn(gelu_erf(p0), gelu_erf(p1));
+                    }
+                    __syncwarp();
+                    // two rows of 16 words per pass
+                    const int wd = lane & 15, n = n0 + 2 * wd;
+                    __nv_bfloat16 *out = reinterpret_cast<__nv_bfloat16 *>(g.out);
+#pragma unroll 4
+                    for (int rr = lane >> 4; rr < 32; rr += 2) {
+                        const int m = mbase + rr;
+                        if (m < g.M && n < g.N) {
+                            const uint32_t val = stw[rr * 17 + wd];
+                            const size_t idx = (size_t)m * g.N + n;
+                            if (n + 1 < g.N)
+                                *reinterpret_cast<uint32_t *>(out + idx) = val;
+                            else
+                                *reinterpret_cast<uint16_t *>(out + idx) = (uint16_t)(val & 0xffffu);
+                        }
+                    }
+                    __syncwarp();
+                }
+            }
+            tc_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bars[10 + acc]));  // accumulator free again
+            acc ^= 1;
+            if (!ok) break;
+        }
+    }
+    tc_before();
+    __syncthreads();
+    tc_after();
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "r"(tcols)
+                     : "memory");
+}
+
+// 2-D view of a row-major bf16 matrix [rows][K]: dims (K, rows), a box of 64 elements (128
+// bytes) x box_rows rows written with 128-byte swizzle.  Out-of-range elements read as zero.
+bool make_gemm_map(CUtensorMap *m, const void *p, int rows, int K, int box_rows)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+    const cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(p), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace gemm
+
+// out = act . w^T with the epilogue `epi` (0: + bias + res, fp32 out; 1: bf16 GELU of the
+// bf16-rounded product plus bias).  act [M][K], w [N][K] bf16 row-major; K a multiple of 8
+// (16-byte rows), 16-byte aligned pointers.  Returns a CUDA error code.
+cudaError_t launch_gemm_tc(int M, int N, int K, const __nv_bfloat16 *w, const __nv_bfloat16 *act,
+                           const float *bias, const float *res, void *out, int epi,
+                           cudaStream_t st)
+{
+    if (M < 1 || N < 1 || K < 8 || (K & 7) || (epi == gemm::EPI_GELU_BF16 && !bias))
+        return cudaErrorInvalidValue;
+    gemm::GemmArgs g{};
+    g.bias = bias;
+    g.res = res;
+    g.out = out;
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    // whole 32-column TMEM loads; for wide outputs an N tile whose chunks split evenly over
+    // the three epilogue warps of a lane quarter
+    g.BN = N <= gemm::MAX_BN ? (N + 31) / 32 * 32 : (N % 192 == 0 ? 192 : gemm::MAX_BN);
+    g.ntn = (N + g.BN - 1) / g.BN;
+    g.nkb = (K + gemm::BK - 1) / gemm::BK;
+    g.epi = epi;
+    g.stats = nullptr;
+    CUtensorMap ma, mb;
+    if (!gemm::make_gemm_map(&ma, act, M, K, gemm::BM) || !gemm::make_gemm_map(&mb, w, N, K, g.BN))
+        return cudaErrorInvalidValue;
+    static int attr_set[64] = {0};
+    static int nsm[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+        e = cudaFuncSetAttribute(gemm::gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 gemm::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        e = cudaDeviceGetAttribute(&nsm[dev], cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = 1;
+    }
+    const int ntiles = ((M + gemm::BM - 1) / gemm::BM) * g.ntn;
+    const unsigned grid = (unsigned)(ntiles < nsm[dev] ? ntiles : nsm[dev]);
+    gemm::gemm_tc_kernel<<<grid, gemm::NT, gemm::SMEM_BYTES, st>>>(g, ma, mb);
+    return cudaGetLastError();
+}
+
+}  // namespace vh
