@@ -79,6 +79,8 @@ CASES = [
     ("3x70_D64_Dm32_d32", 5, 1, 3, 70, 64, 32, 32),
     ("1x9_D32_Dm16_d16", 6, 2, 1, 9, 32, 16, 16),     # one-row map: the depthwise edges
     ("9x1_D64_Dm32_d32", 8, 1, 9, 1, 64, 32, 32),     # one-column map
+    ("4x5_D256_Dm64_d32", 9, 1, 4, 5, 256, 64, 32),   # FFN wider than the fused kernel takes
+    ("6x7_D192_Dm96_d32", 10, 2, 6, 7, 192, 96, 32),  # the stage-1 widths, fused FFN
 ]
 
 

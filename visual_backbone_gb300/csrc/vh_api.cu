@@ -25,7 +25,6 @@ cudaError_t launch_dwgate(const float *u, const float *w, const float *b, __nv_b
                           long npix, int C, int H, int W, cudaStream_t st);
 cudaError_t launch_posdw(const float *y, const __nv_bfloat16 *z, const float *w, const float *b,
                          __nv_bfloat16 *yb, long npix, int C, int H, int W, cudaStream_t st);
-cudaError_t launch_gelu(__nv_bfloat16 *h, const float *b, long n, int hidden, cudaStream_t st);
 cudaError_t launch_gemm_tc(int M, int N, int K, const __nv_bfloat16 *w, const __nv_bfloat16 *act,
                            const float *bias, const float *res, void *out, int epi,
                            cudaStream_t st);
@@ -400,7 +399,8 @@ vh_status vh_block_forward(const float *x, const float *memories0, const vh_para
         return cuda_fail(e, "Proj_out GEMM launch");
     // out = X1 + W_ff2 GELU(W_ff1 LN2(X1) + b_ff1) + b_ff2
     if ((e = vh::launch_ln(out, w->ln2_g, w->ln2_b, eps, a, N, D, st))) return cuda_fail(e, "LN2 launch");
-    // H = bf16(GELU(bf16(LN2(X1) W_ff1^T) + b_ff1)), the GELU in the GEMM's epilogue
+    // H = bf16(GELU(bf16(LN2(X1) W_ff1^T) + b_ff1)) (GELU in the GEMM's epilogue), then
+    // out = X1 + H W_ff2^T + b_ff2
     if ((e = vh::launch_gemm_tc((int)N, Hd, D, bw(w->w_ff1), a, w->b_ff1, nullptr, h, 1, st)))
         return cuda_fail(e, "FFN1 GEMM launch");
     if ((e = vh::launch_gemm_tc((int)N, D, Hd, bw(w->w_ff2), h, w->b_ff2, out, out, 0, st)))

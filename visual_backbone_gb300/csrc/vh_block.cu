@@ -9,14 +9,12 @@
 //   X1  = X0 + Proj_out(Y)               D_m -> D
 //   out = X1 + W2 GELU(W1 LN2(X1) + b1) + b2
 //
-// The four pointwise layers are plain GEMMs on bf16 operands with fp32 accumulation
-// (cuBLASLt, bias and residual in its epilogue).  The kernels here do the rest, each one
-// pass over the activations: the three depthwise convolutions with their epilogues (CPE,
-// the gated branch, the positional branch with the cast for Proj_out), LN1 and LN2 (one
-// warp per pixel), GELU with FFN1's bias.  bf16 rounding points: LN1's and LN2's outputs,
-// Z, Y before Proj_out, FFN1's product (before its bias) and GELU's output.
-
-#include <mutex>
+// The four pointwise layers are GEMMs on bf16 operands with fp32 accumulation
+// (vh_gemm_tc.cu: bias, residual and FFN1's GELU in their epilogues).  The kernels here do
+// the rest, each one pass over the activations: the three depthwise convolutions with
+// their epilogues (CPE, the gated branch, the positional branch with the cast for
+// Proj_out) and LN1 and LN2 (one warp per pixel).  bf16 rounding points: LN1's and LN2's
+// outputs, Z, Y before Proj_out, FFN1's product (before its bias) and GELU's output.
 
 #include "vh_common.cuh"
 
@@ -134,29 +132,6 @@ __global__ void __launch_bounds__(256) dw3_kernel(const TIn *__restrict__ src,
     }
 }
 
-// h = bf16(GELU(h + b)) in place on the FFN's bf16 hidden layer [n][hidden],
-// GELU(a) = a (1 + erf(a / sqrt 2)) / 2; eight elements (16 bytes) per thread, 32-bit
-// indices (the launcher checks the element count).
-__global__ void __launch_bounds__(256) gelu_kernel(uint4 *__restrict__ h, const float *__restrict__ b,
-                                                   int n8, int hid8)
-{
-    const float k = 0.70710678118654752f;
-    for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < n8; e += gridDim.x * blockDim.x) {
-        uint4 r = h[e];
-        const float *bb = b + (e % hid8) * 8;
-        uint32_t *w = &r.x;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const float2 v = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[q]));
-            const float a0 = v.x + bb[2 * q], a1 = v.y + bb[2 * q + 1];
-            const __nv_bfloat162 o = __floats2bfloat162_rn(0.5f * a0 * (1.0f + erff(a0 * k)),
-                                                           0.5f * a1 * (1.0f + erff(a1 * k)));
-            w[q] = *reinterpret_cast<const uint32_t *>(&o);
-        }
-        h[e] = r;
-    }
-}
-
 // ------------------------------------------------------------------ launches
 
 cudaError_t launch_ln(const float *x, const float *g, const float *beta, float eps,
@@ -214,12 +189,5 @@ cudaError_t launch_posdw(const float *y, const __nv_bfloat16 *z, const float *w,
     return cudaGetLastError();
 }
 
-cudaError_t launch_gelu(__nv_bfloat16 *h, const float *b, long n, int hidden, cudaStream_t st)
-{
-    const long n8 = n / 8;
-    if (n8 > 0x7fe00000L) return cudaErrorInvalidValue;  // int index plus one grid stride
-    gelu_kernel<<<grid_for(n8), 256, 0, st>>>(reinterpret_cast<uint4 *>(h), b, (int)n8, hidden / 8);
-    return cudaGetLastError();
-}
 
 }  // namespace vh

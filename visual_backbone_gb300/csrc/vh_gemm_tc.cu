@@ -140,11 +140,11 @@ __global__ void __launch_bounds__(NT, 1)
         // ---- MMA issuer (one lane)
         if (lane == 0) {
             int s = 0, acc = 0;
-            uint32_t ph = 0, aph[2] = {0, 0};
+            uint32_t ph = 0, aph = 0;  // bit b: phase of accumulator b (no indexed arrays: registers)
             const uint32_t idesc = idesc_bf16(BM, BN);
             for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
-                if (!wt.wait(smem_u32(&bars[10 + acc]), aph[acc] ^ 1)) break;  // accumulator free
-                aph[acc] ^= 1;
+                if (!wt.wait(smem_u32(&bars[10 + acc]), ((aph >> acc) & 1u) ^ 1u)) break;  // accumulator free
+                aph ^= 1u << acc;
                 tc_after();
                 const uint32_t dt = tbase + (uint32_t)(acc * BN);
                 for (int kb = 0; kb < g.nkb; ++kb) {
@@ -171,11 +171,11 @@ __global__ void __launch_bounds__(NT, 1)
         const uint32_t lrow = ((uint32_t)q * 32u) << 16;
         float *stg = reinterpret_cast<float *>(sm + OFF_STG) + (warp - 2) * STG_WORDS;
         int acc = 0;
-        uint32_t fph[2] = {0, 0};
+        uint32_t fph = 0;  // bit b: phase of accumulator b
         for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
             const int tm = t / g.ntn, tn = t % g.ntn;
-            const bool ok = wt.wait(smem_u32(&bars[8 + acc]), fph[acc]);
-            fph[acc] ^= 1;
+            const bool ok = wt.wait(smem_u32(&bars[8 + acc]), (fph >> acc) & 1u);
+            fph ^= 1u << acc;
             tc_after();
             const int mbase = tm * BM + 32 * q;  // first of this warp's 32 rows
             for (int cb = 32 * part; ok && cb < BN; cb += 32 * (EPI_WARPS / 4)) {
@@ -315,3 +315,4 @@ cudaError_t launch_gemm_tc(int M, int N, int K, const __nv_bfloat16 *w, const __
 }
 
 }  // namespace vh
+
