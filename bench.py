@@ -20,6 +20,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -311,6 +312,14 @@ def cpu_cores():
         return os.cpu_count() or 1
 
 
+def oracle_images(wl, cores=None):
+    """Images in one oracle sample: the fewest (at most the batch) whose (image, head)
+    scan jobs fill every host core equally, lcm(cores, heads) / heads.  The reference arm
+    and cpu_baseline both use it, so they time the same sample and report one rate."""
+    cores = cores or cpu_cores()
+    return max(1, min(wl.B, math.lcm(cores, wl.nh) // wl.nh))
+
+
 def time_grad_oracle(wl, images, min_seconds=0.0, max_passes=1000):
     """Tokens/s of the gradient oracle (fp64 autograd of the restated forward) on the
     first `images` images, repeated until `min_seconds` of wall time have passed;
@@ -370,8 +379,8 @@ def run_reference(args, wl):
         return run_reference_backward(args, wl)
     if args.pass_ == "block":
         return run_reference_block(args, wl)
-    # forward: enough images per step that every host core has an (image, head) scan job
-    images = args.ref_images or min(wl.B, -(-cpu_cores() // wl.nh))
+    # forward: the oracle sample of cpu_baseline, one pass per step
+    images = args.ref_images or oracle_images(wl)
     cores = min(cpu_cores(), images * wl.nh)
     for _ in range(args.warmup):
         time_oracle(wl, images, cores)
@@ -426,7 +435,7 @@ def run_reference_backward(args, wl):
 
 
 def run_reference_block(args, wl):
-    args.ref_images = args.ref_images or 1
+    args.ref_images = args.ref_images or oracle_images(wl)
     for _ in range(args.warmup):
         time_block_oracle(wl, args.ref_images)
     times, cores = [], 1
@@ -618,14 +627,15 @@ def run_ours(args, wl):
             "clocks": sampler.summary(t0, t1) if sampler else None,
         }
         if world == 1 and not args.no_cpu_baseline:
-            cores = min(cpu_cores(), args.cpu_images * wl.nh)
+            cpu_images = args.cpu_images or oracle_images(wl)
+            cores = min(cpu_cores(), cpu_images * wl.nh)
             v, dt, passes = time_oracle(
-                wl, args.cpu_images, cores, min_seconds=args.cpu_seconds,
+                wl, cpu_images, cores, min_seconds=args.cpu_seconds,
                 w_query=extra["w_query"].double().cpu().numpy() if extra else None,
                 skip=extra["skip"].double().cpu().numpy() if extra else None)
             line["cpu_baseline"] = {
                 "value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
-                "sample": f"{passes} pass(es) over {args.cpu_images} of {wl.B} images of the "
+                "sample": f"{passes} pass(es) over {cpu_images} of {wl.B} images of the "
                           f"workload (all 4 routes x {wl.nh} heads), fp64, {dt:.1f} s wall"}
             # the same oracle on one host thread (one image, about 3 s)
             v1, dt1, passes1 = time_oracle(
@@ -879,14 +889,13 @@ def run_block(args, wl):
                     "h2d_bytes_per_step": int(x_host.numel() * 4),
                     "d2h_bytes_per_step": int(out.numel() * 4), "steps": e2e_steps,
                     "copies": "every step, double-buffered against neighbouring steps"},
-            # ours per call: CPE+LN1, gated depthwise, query projection, scan, positional
-            # depthwise, LN2, GELU (the four GEMMs are cuBLASLt's)
-            "gpu_launches": args.steps * 7,
+            # ours per call: CPE, LN1, Proj_in, gated depthwise, query projection, scan,
+            # positional depthwise, Proj_out, LN2, FFN1 (+GELU), FFN2
+            "gpu_launches": args.steps * 11,
             "clocks": sampler.summary(t0, t1) if sampler else None,
         }
         if world == 1 and not args.no_cpu_baseline:
-            # enough images that every host core has an (image, head) scan job
-            imgs = min(wl.B, -(-cpu_cores() // wl.nh))
+            imgs = oracle_images(wl)
             v, dt, cores, passes = time_block_oracle(wl, imgs, min_seconds=10.0)
             line["cpu_baseline"] = {
                 "value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
@@ -924,12 +933,14 @@ def main(argv=None):
     ap.add_argument("--memories-out", action="store_true",
                     help="forward: also write the final memories (the measurement's second row)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-images", type=int, default=16)
+    ap.add_argument("--cpu-images", type=int, default=0,
+                    help="images in the oracle sample behind cpu_baseline (0: the fewest that "
+                         "fill every host core equally, as the reference arm)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="minimum wall time of the oracle sample behind cpu_baseline")
     ap.add_argument("--ref-images", type=int, default=0,
-                    help="images per step of the reference arm (0: forward, enough for every "
-                         "host core; backward and block, one)")
+                    help="images per step of the reference arm (0: forward and block, the "
+                         "cpu_baseline sample; backward, one)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

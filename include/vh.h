@@ -85,12 +85,15 @@ enum {
 enum {
     VH_IMPL_AUTO = 0,          /* the fastest built kernel for the shape */
     VH_IMPL_SIMT = 1,          /* fp32 CUDA-core kernel */
-    VH_IMPL_TC = 2,            /* tensor-core (tcgen05) kernel, its faster gain form */
+    VH_IMPL_TC = 2,            /* tensor-core (tcgen05) kernel, its faster gain form: the
+                                  recurrence at head_dim 32, WY at head_dim 64 where every
+                                  chunk fits one 32-token sub-tile */
     VH_IMPL_TC_WY = 3,         /* tensor-core kernel, shared gain in WY form ("VisionHOPE",
-                                  App. B.4 Prop. 2, Eqs. (46), (49) unrolled: the keys' Gram
-                                  matrix and the gain assembly on the tensor core, the
-                                  chunk's triangular system on CUDA cores); the method as
-                                  defined with H, W <= 64 only, else VH_ERR_UNSUPPORTED */
+                                  App. B.4 Prop. 2, Eqs. (46), (49) unrolled: the chunk's
+                                  triangular system on CUDA cores, the gain assembly
+                                  G = gamma_L I + W' K^T on the tensor core); the method as
+                                  defined only, with H, W <= 64 at head_dim 32 and H, W <= 32
+                                  at head_dim 64, else VH_ERR_UNSUPPORTED */
     VH_IMPL_TC_RECUR = 4       /* tensor-core kernel, shared gain as the blocked per-token
                                   recurrence of Eq. (46) */
 };
@@ -207,6 +210,16 @@ vh_status vh_scan_forward(const void *x, const float *memories0, const vh_params
  */
 vh_status vh_debug_permute(const void *x, const vh_params *p, int H, int W, int route,
                            void *seq);
+
+/*
+ * vh_debug_gelu -- out[i] = bf16(GELU(a[i])) with the exact GELU a Phi(a) ("VisionHOPE",
+ * Sec. 2.3 Eq. (27): the block's FFN; the form the block's FFN1 epilogue applies to its
+ * bias-added product), computed by the same device function.  a: device fp32 [n];
+ * out: device bf16 [n]; stream: cudaStream_t (NULL = legacy default).  n = 0 is a no-op.
+ * Errors: VH_ERR_INVALID_ARG (n < 0, NULL pointers with n > 0), VH_ERR_CUDA.
+ * Exists so the activation can be checked element by element.
+ */
+vh_status vh_debug_gelu(const float *a, void *out, long long n, void *stream);
 
 /*
  * vh_check -- wait for `stream` (a cudaStream_t; NULL = legacy default) and read the

@@ -95,12 +95,14 @@ def silu(a):
     return a / (1.0 + np.exp(-a))
 
 
-_erf = np.vectorize(math.erf, otypes=[np.float64])
+_erfc = np.vectorize(math.erfc, otypes=[np.float64])
 
 
 def gelu(a):
-    """Exact GELU, a Phi(a) = a (1 + erf(a / sqrt 2)) / 2."""
-    return 0.5 * a * (1.0 + _erf(a / math.sqrt(2.0)))
+    """Exact GELU, a Phi(a) = a (1 + erf(a / sqrt 2)) / 2, written as a erfc(-a / sqrt 2) / 2
+    (the same function; the erfc form keeps full precision in the lower tail, where
+    1 + erf cancels)."""
+    return 0.5 * a * _erfc(-a / math.sqrt(2.0))
 
 
 def block_forward(x, w: BlockWeights, memories0, H: int, W: int, nh: int, d: int,

@@ -157,3 +157,11 @@ def test_backward_rejects_on_the_host(vhlib):
                                         base + (2 << 30), None, base + (2 << 30),
                                         base + (4 << 30)) == -1
     assert b"alias" in vhlib.lib().vh_last_error()
+
+
+def test_debug_gelu_rejects_bad_args(vhlib):
+    L = vhlib.lib()
+    assert L.vh_debug_gelu(FAKE, FAKE, -1, None) == -1
+    assert L.vh_debug_gelu(None, FAKE, 8, None) == -1
+    assert L.vh_debug_gelu(FAKE, None, 8, None) == -1
+    assert L.vh_debug_gelu(None, None, 0, None) == 0   # nothing to do, nothing launched

@@ -74,3 +74,29 @@ def test_expired_wait_reports_timeout_and_leaves_context_usable(vhlib, orc):
         vhlib.check(st)
         o = orc.forward(inp.x64, inp.mem0, wl.H, wl.W, wl.nh, wl.d, params=oracle_params_like(orc, q))
         assert parity_err(out.cpu().numpy(), o) < TOL
+
+
+@pytest.mark.parametrize("d,impl", [(32, "tc_recur"), (32, "tc_wy"), (64, "tc_wy"), (64, "tc_recur")])
+def test_wait_expiring_mid_scan_drains(vhlib, orc, d, impl):
+    """A one-cycle wait limit makes the first wait that is not already complete give up
+    while the CTA's own MMAs (and possibly a copy) are in flight.  The CTA lets them land
+    before it frees TMEM and exits: the call reports VH_ERR_TIMEOUT, and the context then
+    runs a normal call correctly."""
+    import torch
+    from tests._helpers import TOL, oracle_params_like, parity_err
+    wl = synth.Workload("t", 2, 8, 12, 2, d, 0, "bf16", seed=6, alpha_init=0.999)
+    inp = synth.make_inputs(wl)
+    x = torch.from_numpy(inp.x_store.view(np.int16)).view(torch.bfloat16).cuda()
+    m = torch.from_numpy(inp.mem0).cuda()
+    st = torch.zeros(8, dtype=torch.int64, device="cuda")
+    p = vhlib.ScanParams(alpha_init=wl.alpha_init, impl=impl, wait_limit=1)
+    vhlib.scan_forward(x, m, d, stats=st, params=p)
+    with pytest.raises(vhlib.VhError, match="timeout"):
+        vhlib.check(st)
+    assert 1 <= int(st[4].item()) <= wl.B * 4 * wl.nh   # at most once per CTA
+    st = torch.zeros(8, dtype=torch.int64, device="cuda")
+    q = vhlib.ScanParams(alpha_init=wl.alpha_init, impl=impl)
+    out = vhlib.scan_forward(x, m, d, stats=st, params=q)
+    vhlib.check(st)
+    o = orc.forward(inp.x64, inp.mem0, wl.H, wl.W, wl.nh, wl.d, params=oracle_params_like(orc, q))
+    assert parity_err(out.cpu().numpy(), o) < TOL

@@ -55,6 +55,12 @@ def test_gelu_and_silu():
                                rtol=1e-14, atol=1e-15)
     np.testing.assert_allclose(vb.silu(a), torch.nn.functional.silu(torch.from_numpy(a)).numpy(),
                                rtol=1e-14, atol=1e-15)
+    # the lower tail in relative terms: Phi(-x) = phi(x) / x (1 - 1/x^2 + 3/x^4 - 15/x^6 +
+    # 105/x^8 - ...), the asymptotic series of Mills' ratio (error below the first omitted term)
+    for x in (10.0, 20.0):
+        s = sum(c / x ** (2 * k) for k, c in enumerate([1, -1, 3, -15, 105, -945]))
+        phi = math.exp(-x * x / 2) / math.sqrt(2 * math.pi) / x * s
+        np.testing.assert_allclose(vb.gelu(np.array(-x)), -x * phi, rtol=1e-7)
 
 
 def _setup(orc, D, Dm, d, seed, H=5, W=6, B=1):

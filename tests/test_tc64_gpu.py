@@ -16,12 +16,12 @@ from tests._helpers import TOL, oracle_params_like, parity_err, run_gpu
 pytestmark = pytest.mark.gpu
 
 
-def _compare(orc, vhlib, wl, dirs=15, vhp=None, dir_scale=None):
+def _compare(orc, vhlib, wl, dirs=15, vhp=None, dir_scale=None, impl="tc"):
     inp = synth.make_inputs(wl)
     if vhp is None:
         vhp = vhlib.ScanParams(eta_bias=wl.eta_bias, alpha_init=wl.alpha_init)
     g = run_gpu(vhlib, inp, params=vhp, dirs=dirs, dir_scale=dir_scale, want_memories=True,
-                want_stats=True, impl="tc")
+                want_stats=True, impl=impl)
     p = oracle_params_like(orc, vhp, dir_scale)
     o, om = orc.forward(inp.x64, inp.mem0, wl.H, wl.W, wl.nh, wl.d, dirs=dirs, params=p,
                         want_memories=True, nthreads=8)
@@ -86,3 +86,29 @@ def test_tc64_dir_scale(orc, vhlib):
     ds = synth.make_dir_scale(wl)
     e_out, e_mem = _compare(orc, vhlib, wl, dir_scale=ds)
     assert e_out < TOL and e_mem < TOL, (e_out, e_mem)
+
+
+@pytest.mark.parametrize("impl", ["tc_recur", "tc_wy"])
+@pytest.mark.parametrize("case", [
+    (2, 14, 14, 2, 0.999, 0.0),    # the stage-3 chunk
+    (1, 9, 32, 1, 0.9, 1.0),       # rows of a full sub-tile, the pages' retention
+])
+def test_tc64_gain_forms(orc, vhlib, impl, case):
+    """Either gain form forced on chunks that fit one sub-tile (where the default is WY)."""
+    B, H, W, nh, ainit, eb = case
+    wl = synth.Workload("t64f", B, H, W, nh, 64, 0, "bf16", seed=H * 7 + W, eta_bias=eb,
+                        alpha_init=ainit)
+    e_out, e_mem = _compare(orc, vhlib, wl, impl=impl)
+    assert e_out < TOL and e_mem < TOL, (e_out, e_mem)
+
+
+def test_tc64_wy_rejects_long_chunks(vhlib):
+    """WY at head_dim 64 needs every chunk within one 32-token sub-tile."""
+    import torch
+    from tests._helpers import to_device_x
+    wl = synth.Workload("t64x", 1, 4, 40, 1, 64, 0, "bf16", seed=44)
+    inp = synth.make_inputs(wl)
+    x = to_device_x(inp)
+    m = torch.from_numpy(inp.mem0).cuda()
+    with pytest.raises(vhlib.VhError, match="unsupported"):
+        vhlib.scan_forward(x, m, 64, params=vhlib.ScanParams(impl="tc_wy"))

@@ -101,6 +101,8 @@ def lib() -> ctypes.CDLL:
         L.vh_scan_forward.argtypes = [vp, vp, ctypes.POINTER(CParams), ci, ci, cu, ci, vp]
         L.vh_debug_permute.restype = ci
         L.vh_debug_permute.argtypes = [vp, ctypes.POINTER(CParams), ci, ci, ci, vp]
+        L.vh_debug_gelu.restype = ci
+        L.vh_debug_gelu.argtypes = [vp, vp, ctypes.c_longlong, vp]
         L.vh_workspace_size.restype = ctypes.c_size_t
         L.vh_workspace_size.argtypes = [ctypes.POINTER(CParams), ci, ci, cu, ci]
         L.vh_scan_backward.restype = ci
@@ -355,6 +357,16 @@ def check(stats, stream=None):
     import torch
     _require_cuda("stats", stats, (torch.int64,))
     _check(lib().vh_check(stats.data_ptr(), _stream_ptr(stream)))
+
+
+def debug_gelu(a, stream=None):
+    """bf16(GELU(a)) elementwise with the exact GELU the block's FFN1 epilogue applies."""
+    import torch
+    _require_cuda("a", a, (torch.float32,))
+    a = a.contiguous()
+    out = torch.empty(a.shape, dtype=torch.bfloat16, device=a.device)
+    _check(lib().vh_debug_gelu(a.data_ptr(), out.data_ptr(), a.numel(), _stream_ptr(stream)))
+    return out
 
 
 def debug_permute(x, route: int, head_dim: int, stream=None):

@@ -11,7 +11,9 @@ namespace vh {
 cudaError_t launch_scan_simt(const ScanArgs &a, int d, bool bf16, cudaStream_t st);
 cudaError_t launch_scan_tc(const ScanArgs &a, int d, bool bf16, cudaStream_t st, bool *handled,
                            int gain);
-cudaError_t launch_scan_tc64(const ScanArgs &a, int d, bool bf16, cudaStream_t st, bool *handled);
+cudaError_t launch_gelu_debug(const float *a, __nv_bfloat16 *out, long long n, cudaStream_t st);
+cudaError_t launch_scan_tc64(const ScanArgs &a, int d, bool bf16, cudaStream_t st, bool *handled,
+                             int gain);
 cudaError_t launch_qproj(const void *x, bool bf16, int d, const float *wq, const float *skip,
                          const float *dir_scale, unsigned dirs, __nv_bfloat16 *qhat, float *out,
                          int accumulate, long npix, int Cc, float knorm_eps, cudaStream_t st);
@@ -306,13 +308,13 @@ vh_status vh_scan_forward(const void *x, const float *memories0, const vh_params
     }
     bool handled = false;
     if (p->impl != VH_IMPL_SIMT) {
-        if (d == 64 && p->impl != VH_IMPL_TC_WY)
-            e = vh::launch_scan_tc64(a, d, bf16, st, &handled);
+        if (d == 64)
+            e = vh::launch_scan_tc64(a, d, bf16, st, &handled, p->impl);
         else
             e = vh::launch_scan_tc(a, d, bf16, st, &handled, p->impl);
         if (e == cudaErrorNotSupported)
             return fail(VH_ERR_UNSUPPORTED, "the WY gain needs the method as defined (no control_flags, "
-                        "no w_query) and H, W <= 64");
+                        "no w_query) and H, W <= 64 (head_dim 32) or <= 32 (head_dim 64)");
         if (e != cudaSuccess) return cuda_fail(e, "tensor-core scan launch");
         if (!handled && p->impl != VH_IMPL_AUTO)
             return fail(VH_ERR_UNSUPPORTED, "no tensor-core kernel for d=%d dtype=%d chunk=%d",
@@ -523,6 +525,17 @@ __global__ void permute_kernel(const XT *__restrict__ x, XT *__restrict__ seq, i
 }
 
 }  // namespace
+
+extern "C" vh_status vh_debug_gelu(const float *a, void *out, long long n, void *stream)
+{
+    g_err[0] = '\0';
+    if (n < 0) return fail(VH_ERR_INVALID_ARG, "n %lld", n);
+    if (n > 0 && (!a || !out)) return fail(VH_ERR_INVALID_ARG, "a and out must be non-NULL");
+    cudaError_t e = vh::launch_gelu_debug(a, static_cast<__nv_bfloat16 *>(out), n,
+                                          static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "gelu launch");
+    return VH_OK;
+}
 
 extern "C" vh_status vh_debug_permute(const void *x, const vh_params *p, int H, int W, int route,
                                       void *seq)

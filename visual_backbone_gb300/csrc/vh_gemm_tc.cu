@@ -72,9 +72,54 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t addr)
            ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
-__device__ __forceinline__ float gelu_erf(float a)
+__device__ __forceinline__ float rcp_approx(float x)
 {
-    return 0.5f * a * (1.0f + erff(a * 0.70710678118654752f));
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
+__device__ __forceinline__ float ex2_approx(float x)
+{
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
+// Exact GELU, a Phi(a) with Phi the standard normal CDF.  With z = |a| / sqrt(2),
+//   Phi(a) = e(z) for a < 0 and 1 - e(z) for a >= 0,   e(z) = erfc(z) / 2 = exp(-z^2) t S(t),
+//   t = 1 / (1 + z / 2),
+// the substitution of the Chebyshev erfc fit in Numerical Recipes (2nd ed., Sec. 6.2).  S
+// is our own degree-8 polynomial in t, fitted (fp32 coefficients) by least squares weighted
+// for relative error at Chebyshev nodes of t in [1/6, 1], i.e. z in [0, 10]: the relative
+// error of e is below 7e-8 in exact arithmetic.  e is accurate in relative terms on both
+// tails, so a Phi(a) keeps its precision for negative a, where 1 + erf(a / sqrt 2) would
+// cancel.  exp(-z^2) = 2^(a^2 K) with K = -log2(e) / 2; the roundings of a^2 and of a^2 K
+// are carried into a first-order correction, so they do not reach the result.  Beyond
+// |a| = 13 the tail underflows: Phi is 0 or 1 there (GELU(a) = -0 or a).
+__device__ __forceinline__ float gelu_exact(float a)
+{
+    const float ax = fminf(fabsf(a), 13.5f);
+    const float t = rcp_approx(fmaf(ax, 0.353553391f, 1.0f));  // 1 / (1 + |a| / (2 sqrt 2))
+    float S = -0.0300543532f;
+    S = fmaf(S, t, 0.144723058f);
+    S = fmaf(S, t, -0.248414785f);
+    S = fmaf(S, t, 0.144257575f);
+    S = fmaf(S, t, -0.0166995097f);
+    S = fmaf(S, t, 0.102680214f);
+    S = fmaf(S, t, 0.121239692f);
+    S = fmaf(S, t, 0.141226918f);
+    S = fmaf(S, t, 0.141041175f);
+    constexpr float K = -0.721347520f;           // -log2(e) / 2, rounded
+    constexpr float K_LO = -9.62981495e-09f;      // -log2(e) / 2 - K
+    const float a2 = ax * ax;
+    const float a2_lo = fmaf(ax, ax, -a2);        // a^2 = a2 + a2_lo exactly
+    const float yh = a2 * K;
+    const float yl = fmaf(a2, K, -yh) + fmaf(a2_lo, K, a2 * K_LO);
+    const float p = ex2_approx(yh);
+    const float ex = fmaf(p, yl * 0.693147181f, p);  // 2^(yh + yl), to first order in yl
+    const float e = t * S * ex;
+    return a * (a < 0.0f ? e : 1.0f - e);
 }
 
 __global__ void __launch_bounds__(NT, 1)
@@ -124,7 +169,7 @@ __global__ void __launch_bounds__(NT, 1)
             for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
                 const int tm = t / g.ntn, tn = t % g.ntn;
                 for (int kb = 0; kb < g.nkb; ++kb) {
-                    if (!wt.wait(smem_u32(&bars[4 + s]), ph ^ 1)) break;  // stage free
+                    if (!wt.wait_inline(smem_u32(&bars[4 + s]), ph ^ 1)) break;  // stage free
                     const uint32_t full = smem_u32(&bars[s]);
                     mbar_expect_tx(full, a_bytes + b_bytes);
                     const uint32_t sa = smem_u32(sm + OFF_A + s * A_STAGE);
@@ -143,12 +188,12 @@ __global__ void __launch_bounds__(NT, 1)
             uint32_t ph = 0, aph = 0;  // bit b: phase of accumulator b (no indexed arrays: registers)
             const uint32_t idesc = idesc_bf16(BM, BN);
             for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
-                if (!wt.wait(smem_u32(&bars[10 + acc]), ((aph >> acc) & 1u) ^ 1u)) break;  // accumulator free
+                if (!wt.wait_inline(smem_u32(&bars[10 + acc]), ((aph >> acc) & 1u) ^ 1u)) break;  // accumulator free
                 aph ^= 1u << acc;
                 tc_after();
                 const uint32_t dt = tbase + (uint32_t)(acc * BN);
                 for (int kb = 0; kb < g.nkb; ++kb) {
-                    if (!wt.wait(smem_u32(&bars[s]), ph)) break;  // stage landed
+                    if (!wt.wait_inline(smem_u32(&bars[s]), ph)) break;  // stage landed
                     tc_after();
                     const uint64_t da = sdesc_sw128(smem_u32(sm + OFF_A + s * A_STAGE));
                     const uint64_t db = sdesc_sw128(smem_u32(sm + OFF_B + s * B_STAGE));
@@ -174,7 +219,7 @@ __global__ void __launch_bounds__(NT, 1)
         uint32_t fph = 0;  // bit b: phase of accumulator b
         for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
             const int tm = t / g.ntn, tn = t % g.ntn;
-            const bool ok = wt.wait(smem_u32(&bars[8 + acc]), (fph >> acc) & 1u);
+            const bool ok = wt.wait_inline(smem_u32(&bars[8 + acc]), (fph >> acc) & 1u);
             fph ^= 1u << acc;
             tc_after();
             const int mbase = tm * BM + 32 * q;  // first of this warp's 32 rows
@@ -215,7 +260,7 @@ __global__ void __launch_bounds__(NT, 1)
                         // the product rounded to bf16, then the bias and GELU, rounded again
                         const float p0 = __bfloat162float(__float2bfloat16_rn(v[e])) + b0;
                         const float p1 = __bfloat162float(__float2bfloat16_rn(v[e + 1])) + b1;
-                        stw[lane * 17 + e / 2] = pack_bf16x2_rn(gelu_erf(p0), gelu_erf(p1));
+                        stw[lane * 17 + e / 2] = pack_bf16x2_rn(gelu_exact(p0), gelu_exact(p1));
                     }
                     __syncwarp();
                     // two rows of 16 words per pass
@@ -266,7 +311,23 @@ bool make_gemm_map(CUtensorMap *m, const void *p, int rows, int K, int box_rows)
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The epilogue's GELU alone: out[i] = bf16(GELU(a[i])).
+__global__ void gelu_debug_kernel(const float *__restrict__ a, __nv_bfloat16 *__restrict__ out, long long n)
+{
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+         i += (long long)gridDim.x * blockDim.x)
+        out[i] = __float2bfloat16_rn(gelu_exact(a[i]));
+}
+
 }  // namespace gemm
+
+cudaError_t launch_gelu_debug(const float *a, __nv_bfloat16 *out, long long n, cudaStream_t st)
+{
+    if (n <= 0) return cudaSuccess;
+    const long long blocks = (n + 255) / 256;
+    gemm::gelu_debug_kernel<<<(unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, st>>>(a, out, n);
+    return cudaGetLastError();
+}
 
 // out = act . w^T with the epilogue `epi` (0: + bias + res, fp32 out; 1: bf16 GELU of the
 // bf16-rounded product plus bias).  act [M][K], w [N][K] bf16 row-major; K a multiple of 8

@@ -307,6 +307,7 @@ __global__ void __launch_bounds__(NT, 3)
     const uint32_t mb_g = smem_u32(&bars[4]);
     const uint32_t mb_q = smem_u32(&bars[5]);
     const uint32_t mb_gram = smem_u32(&bars[6]), mb_asm = smem_u32(&bars[7]);
+    const uint32_t mb_drain = smem_u32(sm + LY::BAR + 112);  // end of a CTA that gave up
     const bool exact = a.qhat != nullptr;  // queries from the outer projection
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + LY::BAR + 64);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + LY::BAR + 72);
@@ -340,6 +341,7 @@ __global__ void __launch_bounds__(NT, 3)
         mbar_init(mb_q, 1);
         mbar_init(mb_gram, 1);
         mbar_init(mb_asm, 1);
+        mbar_init(mb_drain, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         // Co-resident CTAs hold consecutive groups of four hardware warp slots, and warp w
         // of a CTA runs on SM sub-partition w.  Alternating the gain pair between warps 0-1
@@ -357,7 +359,17 @@ __global__ void __launch_bounds__(NT, 3)
     }
     auto line_of = [&](int c) { return rev ? nlines - 1 - c : c; };
     auto box_start = [&](int s) { return rev ? Lline - (s + 1) * TT : s * TT; };
+    // copies issued and completions observed per TMA barrier (issuing thread); at most one
+    // copy per barrier is in flight, so after an abort the drain waits for completion
+    // number n_iss - 1 where n_obs < n_iss
+    uint32_t nx_iss = 0, nx_obs = 0, nq_iss = 0, nq_obs = 0;
+    auto wait_copy = [&](uint32_t bar, uint32_t ph, uint32_t &n_obs) {
+        const bool got = wt.wait(bar, ph);
+        n_obs += got;
+        return got;
+    };
     auto issue_x = [&](int c, int s) {
+        ++nx_iss;
         mbar_expect_tx(mb_x, TT * D * 2);
 #pragma unroll
         for (int q = 0; q < D / 8; ++q)
@@ -377,6 +389,7 @@ __global__ void __launch_bounds__(NT, 3)
     const bool issuer = warp == rw && lane == 0;
     const CUtensorMap *tq = rowr ? &tq_row : &tq_col;
     auto issue_q = [&](int c, int s) {
+        ++nq_iss;
         mbar_expect_tx(mb_q, 3 * TT * D * 2);
 #pragma unroll
         for (int q = 0; q < D / 8; ++q)
@@ -459,7 +472,7 @@ __global__ void __launch_bounds__(NT, 3)
             // the tile into TMEM lanes nobody reads.
             if (issuer) {
                 tc_after();
-                if (wt.wait(mb_x, ph_x) && !*abort_flag) {
+                if (wait_copy(mb_x, ph_x, nx_obs) && !*abort_flag) {
                     const uint64_t dq = sdesc(smem_u32(sX) - (rw >> 1) * LBO_X, LBO_X, SBO_X);
                     const uint64_t ds = sdesc(smem_u32(sS), LBO_K32, SBO_K32);
 #pragma unroll
@@ -814,7 +827,7 @@ __global__ void __launch_bounds__(NT, 3)
                         for (int e = 0; e < 32; ++e) qv[e] *= rq;
                     } else {
                         // the outer query's three pieces from its TMA tile
-                        wt.wait(mb_q, ph_q);
+                        wait_copy(mb_q, ph_q, nq_obs);  // (the drain reads the issuer's count)
 #pragma unroll
                         for (int g = 0; g < 4; ++g) {
                             const unsigned char *src = sQ + g * QX_LBO + jq * 16;
@@ -1200,7 +1213,7 @@ __global__ void __launch_bounds__(NT, 3)
                                 smem_u32(sS) + (ROW_MEM + 3 * D) / 8 * SBO_K32, idesc_bf16(128, 32));
                             mma_commit(mb_ro);
                         }
-                    } else if (wt.wait(mb_q, ph_q) && !*abort_flag) {
+                    } else if (wait_copy(mb_q, ph_q, nq_obs) && !*abort_flag) {
                         constexpr int pa[6] = {0, 0, 1, 0, 2, 1};
                         constexpr int pb[6] = {0, 1, 0, 2, 0, 1};
                         const uint64_t da = sdesc(smem_u32(sQ) - (rw >> 1) * 8 * SBO_X, QX_LBO, SBO_X);
@@ -1383,6 +1396,15 @@ __global__ void __launch_bounds__(NT, 3)
             if (cn) atomicAdd(st + VH_STAT_NONFINITE, (unsigned long long)cn);
         }
         if (tid == 0) atomicAdd(st + VH_STAT_TOKENS, (unsigned long long)H * W);
+    }
+    // A CTA that gave up lets its own asynchronous work land (bounded) before TMEM is freed
+    // and its shared memory released: every MMA it issued (one more commit tracks them all)
+    // and the copy in flight on each TMA barrier.
+    if (issuer && *abort_flag) {
+        mma_commit(mb_drain);
+        drain_wait(mb_drain, 0);
+        if (nx_obs < nx_iss) drain_wait(mb_x, (nx_iss - 1) & 1);
+        if (nq_obs < nq_iss) drain_wait(mb_q, (nq_iss - 1) & 1);
     }
     tc_before();
     __syncthreads();

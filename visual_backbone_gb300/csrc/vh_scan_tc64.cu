@@ -19,9 +19,18 @@
 //          beside the Gram entries of four-token blocks (warps 2 and 3).
 //   MMA 2  readout, Eq. (16): y = q M^m_b^T, six split cross terms, N = 64, issued before
 //          the gain and added to out (lambda_r y at the token's pixel, Eq. (26)) after it.
-//   SIMT   shared gain G_t = alpha_t G_{t-1} - eta_t (G_{t-1} k_t + delta_t) k_t^T
-//          (Prop. 2, Eq. (46)) on all 256 threads: four lanes per row of G, sixteen
-//          columns each, in the scaled form G = gamma Ghat and blocks of four tokens.
+//   GAIN   the shared gain of Prop. 2, Eq. (46), in one of two forms:
+//          - recurrence (chunks longer than a sub-tile): G_t = alpha_t G_{t-1} -
+//            eta_t (G_{t-1} k_t + delta_t) k_t^T on all 256 threads, four lanes per row of
+//            G, sixteen columns each, in the scaled form G = gamma Ghat, blocks of four
+//            tokens;
+//          - WY (every chunk within one sub-tile, the stage-3 shape): Eq. (46) unrolled
+//            over the chunk gives G = gamma_L I + sum_j sigma_j w_j k_j^T with
+//            w_j = -eta_j (r_j + sum_{i<j} c(i,j) w_i), r_j = gamma_{j-1} k_j + delta_j and
+//            c(i,j) = (prod_{i<s<j} alpha_s) k_i.k_j, retention products only; the Gram
+//            entries and this triangular system run on CUDA cores (warps 0 and 1, one
+//            row of G per thread), and G = gamma_L I + W' K^T is one tensor-core
+//            assembly (three to six MMAs, keys as the MN-major A operand).
 //   MMA 3  at the chunk end every memory <- M_b G: the k, v memories and the q, m memories
 //          as two M = 128 tiles; per K step one MMA per piece of M_b against G's pieces
 //          stacked along N (192, 128, 64 columns), the six cross terms in three column
@@ -188,6 +197,7 @@ __global__ void __launch_bounds__(NT, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + OFF_BAR);
     const uint32_t mb_x = smem_u32(&bars[0]), mb_gen = smem_u32(&bars[1]);
     const uint32_t mb_ro = smem_u32(&bars[2]), mb_upd = smem_u32(&bars[3]);
+    const uint32_t mb_drain = smem_u32(sm + OFF_BAR + 112);  // end of a CTA that gave up
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + OFF_BAR + 64);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + OFF_BAR + 72);
     volatile int *delta_form = reinterpret_cast<volatile int *>(sm + OFF_BAR + 80);
@@ -209,6 +219,7 @@ __global__ void __launch_bounds__(NT, 1)
         mbar_init(mb_gen, 1);
         mbar_init(mb_ro, 1);
         mbar_init(mb_upd, 1);
+        mbar_init(mb_drain, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 0) {
@@ -220,7 +231,11 @@ __global__ void __launch_bounds__(NT, 1)
     }
     auto line_of = [&](int c) { return rev ? nlines - 1 - c : c; };
     auto box_start = [&](int s) { return rev ? Lline - (s + 1) * TT : s * TT; };
+    // x copies issued and completions observed (issuing thread); at most one copy is in
+    // flight, so after an abort the drain waits for completion number nx_iss - 1
+    uint32_t nx_iss = 0, nx_obs = 0;
     auto issue_x = [&](int c, int s) {
+        ++nx_iss;
         mbar_expect_tx(mb_x, TT * D * 2);
 #pragma unroll
         for (int q = 0; q < D / 8; ++q)
@@ -356,7 +371,9 @@ __global__ void __launch_bounds__(NT, 1)
             // ---- MMA 1: generation from the boundary state, Eq. (15)
             if (issuer) {
                 tc_after();
-                if (wt.wait(mb_x, ph_x) && !*abort_flag) {
+                const bool got_x = wt.wait(mb_x, ph_x);
+                nx_obs += got_x;
+                if (got_x && !*abort_flag) {
                     const uint64_t dx = sdesc(smem_u32(sX), LBO_X, SBO_X);
                     const uint64_t ds = sdesc(smem_u32(sS), LBO, SBO);
 #pragma unroll
@@ -956,6 +973,14 @@ __global__ void __launch_bounds__(NT, 1)
         }
         if (tid == 0) atomicAdd(st + VH_STAT_TOKENS, (unsigned long long)H * W);
     }
+    // A CTA that gave up lets its own asynchronous work land (bounded) before TMEM is freed
+    // and its shared memory released: every MMA it issued (one more commit tracks them all)
+    // and the x copy in flight.
+    if (issuer && *abort_flag) {
+        mma_commit(mb_drain);
+        drain_wait(mb_drain, 0);
+        if (nx_obs < nx_iss) drain_wait(mb_x, (nx_iss - 1) & 1);
+    }
     tc_before();
     __syncthreads();
     tc_after();
@@ -991,8 +1016,11 @@ bool make_map64(CUtensorMap *m, const void *x, int B, int H, int W, int Cc, bool
 
 // Tensor-core path for head_dim 64: bf16 x, row/column-aligned chunks, the method as
 // defined (no control flags, no outer queries, no backward records).  Sets *handled =
-// false (and returns success) for any other call.
-cudaError_t launch_scan_tc64(const ScanArgs &a, int d, bool bf16, cudaStream_t st, bool *handled)
+// false (and returns success) for any other call.  `gain` (VH_IMPL_*) picks the gain form:
+// VH_IMPL_TC_WY the WY form (cudaErrorNotSupported unless every chunk fits one sub-tile),
+// VH_IMPL_TC_RECUR the blocked recurrence, otherwise WY where it applies.
+cudaError_t launch_scan_tc64(const ScanArgs &a, int d, bool bf16, cudaStream_t st, bool *handled,
+                             int gain)
 {
     *handled = false;
     const bool aligned = a.chunk == 0 || (a.chunk == a.W && a.chunk == a.H);
@@ -1019,7 +1047,9 @@ cudaError_t launch_scan_tc64(const ScanArgs &a, int d, bool bf16, cudaStream_t s
     }
     const unsigned grid = (unsigned)(a.B * a.ndirs * a.nh);
     // the WY form where every chunk fits one sub-tile (both orientations), else the recurrence
-    if (a.H <= tc64::TT && a.W <= tc64::TT)
+    const bool wy_ok = a.H <= tc64::TT && a.W <= tc64::TT;
+    if (gain == VH_IMPL_TC_WY && !wy_ok) return cudaErrorNotSupported;
+    if (wy_ok && gain != VH_IMPL_TC_RECUR)
         tc64::scan_tc64_kernel<true><<<grid, tc64::NT, tc64::SMEM_BYTES, st>>>(a, mr, mc);
     else
         tc64::scan_tc64_kernel<false><<<grid, tc64::NT, tc64::SMEM_BYTES, st>>>(a, mr, mc);

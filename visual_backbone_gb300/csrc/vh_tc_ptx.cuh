@@ -39,6 +39,19 @@ __device__ __forceinline__ uint32_t mbar_try(uint32_t bar, uint32_t parity)
     return ok;
 }
 
+// Non-blocking test of the phase with `parity`.
+__device__ __forceinline__ uint32_t mbar_test(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(bar), "r"(parity)
+                 : "memory");
+    return ok;
+}
+
 // As mbar_try, but a thread whose phase is not complete may be suspended for up to
 // `ns` nanoseconds (or until the phase completes) instead of returning at once, so
 // waiting warps do not take issue slots from the working ones.
@@ -201,6 +214,26 @@ __device__ __forceinline__ float sumsq32(const float (&v)[32])
 }
 
 
+// Out-of-line part of a bounded wait (below): the phase was not complete at the first
+// test.  Kept out of line so the many wait sites of a kernel stay small.
+static __device__ __noinline__ bool wait_slow(volatile int *abort_flag, unsigned long long *stats,
+                                       long long limit, uint32_t bar, uint32_t parity)
+{
+    const long long t0 = clock64();
+    while (true) {
+        // short limits poll without suspending, so the limit alone decides (a suspended
+        // try_wait may outlast it and return with the phase complete)
+        if (limit < 20000 ? mbar_test(bar, parity) : mbar_try_sleep(bar, parity, 20000u))
+            return true;
+        if (*abort_flag) return false;
+        if (clock64() - t0 > limit) {
+            if (atomicExch((int *)abort_flag, 1) == 0 && stats)
+                atomicAdd(stats + VH_STAT_TIMEOUT, 1ull);
+            return false;
+        }
+    }
+}
+
 struct Waiter {
     volatile int *abort_flag;
     unsigned long long *stats;
@@ -211,10 +244,19 @@ struct Waiter {
     __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity) const
     {
         if (*abort_flag) return false;
-        if (mbar_try(bar, parity)) return true;
+        if (limit >= 20000 && mbar_try(bar, parity)) return true;
+        return wait_slow(abort_flag, stats, limit, bar, parity);
+    }
+    // The same wait with the polling loop inline, for kernels with few wait sites whose
+    // waits often miss the first test (a call there costs more than the code it saves).
+    __device__ __forceinline__ bool wait_inline(uint32_t bar, uint32_t parity) const
+    {
+        if (*abort_flag) return false;
+        if (limit >= 20000 && mbar_try(bar, parity)) return true;
         const long long t0 = clock64();
         while (true) {
-            if (mbar_try_sleep(bar, parity, limit < 20000 ? (uint32_t)limit : 20000u)) return true;
+            if (limit < 20000 ? mbar_test(bar, parity) : mbar_try_sleep(bar, parity, 20000u))
+                return true;
             if (*abort_flag) return false;
             if (clock64() - t0 > limit) {
                 if (atomicExch((int *)abort_flag, 1) == 0 && stats)
@@ -224,6 +266,18 @@ struct Waiter {
         }
     }
 };
+
+// Bounded wait that ignores the abort flag: a CTA that gave up uses it to let its own
+// copies and MMAs in flight land before it frees TMEM and exits.  Its limit is the default
+// one (2^32 cycles, about 2 s) whatever the wait limit of the call, since work still in
+// flight at exit is what it prevents.  False on expiry.
+__device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity)
+{
+    const long long t0 = clock64();
+    while (!mbar_try_sleep(bar, parity, 20000u))
+        if (clock64() - t0 > (1ll << 32)) return false;
+    return true;
+}
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar)
 {
