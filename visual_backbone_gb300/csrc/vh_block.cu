@@ -22,34 +22,48 @@ namespace vh {
 
 // ------------------------------------------------------------------ kernels
 
-// Per pixel (one warp): a = bf16(LN(x) * g + beta).
-template <int MAXC>
+// Per pixel (one warp): a = bf16(LN(x) * g + beta).  A lane holds channel pairs 2 lane +
+// 64 m (8-byte loads, bf16x2 stores); the scale and shift of its channels stay in
+// registers across the pixels it visits.  D even, x 8-byte aligned rows.
+template <int MAXP>
 __global__ void __launch_bounds__(256) ln_kernel(const float *__restrict__ x,
                                                  const float *__restrict__ g,
                                                  const float *__restrict__ beta, float eps,
                                                  __nv_bfloat16 *__restrict__ a, long npix, int D)
 {
     const int lane = threadIdx.x & 31;
+    float2 gv[MAXP], bv[MAXP];
+#pragma unroll
+    for (int m = 0; m < MAXP; ++m) {
+        const int c = 2 * lane + 64 * m;
+        gv[m] = c < D ? make_float2(g[c], g[c + 1]) : make_float2(0.0f, 0.0f);
+        bv[m] = c < D ? make_float2(beta[c], beta[c + 1]) : make_float2(0.0f, 0.0f);
+    }
     for (long pix = (blockIdx.x * (long)blockDim.x + threadIdx.x) >> 5; pix < npix;
          pix += ((long)gridDim.x * blockDim.x) >> 5) {
-        float v[MAXC];
+        float2 v[MAXP];
         float s = 0.0f;
 #pragma unroll
-        for (int m = 0; m < MAXC; ++m) {
-            const int c = lane + 32 * m;
-            v[m] = c < D ? x[pix * D + c] : 0.0f;
-            s += v[m];
+        for (int m = 0; m < MAXP; ++m) {
+            const int c = 2 * lane + 64 * m;
+            v[m] = c < D ? *reinterpret_cast<const float2 *>(x + pix * D + c) : make_float2(0.0f, 0.0f);
+            s += v[m].x + v[m].y;
         }
         const float mu = warp_sum(s) / D;
         float q = 0.0f;
 #pragma unroll
-        for (int m = 0; m < MAXC; ++m)
-            if (lane + 32 * m < D) q = fmaf(v[m] - mu, v[m] - mu, q);
+        for (int m = 0; m < MAXP; ++m)
+            if (2 * lane + 64 * m < D) {
+                q = fmaf(v[m].x - mu, v[m].x - mu, q);
+                q = fmaf(v[m].y - mu, v[m].y - mu, q);
+            }
         const float rs = rsqrtf(warp_sum(q) / D + eps);
 #pragma unroll
-        for (int m = 0; m < MAXC; ++m) {
-            const int c = lane + 32 * m;
-            if (c < D) a[pix * D + c] = __float2bfloat16_rn((v[m] - mu) * rs * g[c] + beta[c]);
+        for (int m = 0; m < MAXP; ++m) {
+            const int c = 2 * lane + 64 * m;
+            if (c < D)
+                *reinterpret_cast<__nv_bfloat162 *>(a + pix * D + c) = __floats2bfloat162_rn(
+                    (v[m].x - mu) * rs * gv[m].x + bv[m].x, (v[m].y - mu) * rs * gv[m].y + bv[m].y);
         }
     }
 }
@@ -59,8 +73,11 @@ __global__ void __launch_bounds__(256) ln_kernel(const float *__restrict__ x,
 //   kCpe:  out_f32  = src + b + dw(src)             conditional positional encoding
 //   kGate: out_bf16 = src + SiLU(b + dw(src))       gated depthwise residual branch
 //   kPos:  out_bf16 = res + b + dw(src), src bf16   positional branch, cast for Proj_out
-// One CTA per image row; the taps are staged transposed ([tap][channel]) in shared
-// memory, and a thread handles four consecutive channels of one pixel (16-byte loads).
+// One CTA per image row.  A thread takes four consecutive channels (16-byte loads) of NP
+// neighbouring pixels: each tap loaded from shared memory serves all of them, and they
+// share the columns of their 3 x 3 windows (3 (NP + 2) 16-byte loads for NP outputs
+// instead of 9 NP).  The taps are summed in the order (di, dj) = (-1, -1), (-1, 0), ... (1, 1),
+// starting from the bias; taps outside the map are skipped.
 enum DwMode { kCpe = 0, kGate = 1, kPos = 2 };
 
 template <typename T> struct Vec4;
@@ -77,7 +94,39 @@ template <> struct Vec4<__nv_bfloat16> {
     }
 };
 
+__device__ __forceinline__ void fma4(float4 &acc, const float4 k, const float4 v)
+{
+    acc.x = fmaf(k.x, v.x, acc.x);
+    acc.y = fmaf(k.y, v.y, acc.y);
+    acc.z = fmaf(k.z, v.z, acc.z);
+    acc.w = fmaf(k.w, v.w, acc.w);
+}
+
 template <int kMode, typename TIn>
+__device__ __forceinline__ void dw3_store(const TIn *__restrict__ src, const float *__restrict__ res,
+                                          void *__restrict__ out, size_t e, float4 acc)
+{
+    if (kMode == kCpe) {
+        const float4 x = Vec4<TIn>::load(src + e);
+        *reinterpret_cast<float4 *>(static_cast<float *>(out) + e) =
+            make_float4(x.x + acc.x, x.y + acc.y, x.z + acc.z, x.w + acc.w);
+    } else {
+        float4 r;
+        if (kMode == kGate) {
+            const float4 u = Vec4<TIn>::load(src + e);
+            r = make_float4(u.x + acc.x / (1.0f + __expf(-acc.x)), u.y + acc.y / (1.0f + __expf(-acc.y)),
+                            u.z + acc.z / (1.0f + __expf(-acc.z)), u.w + acc.w / (1.0f + __expf(-acc.w)));
+        } else {
+            const float4 y = *reinterpret_cast<const float4 *>(res + e);
+            r = make_float4(y.x + acc.x, y.y + acc.y, y.z + acc.z, y.w + acc.w);
+        }
+        __nv_bfloat162 *o = reinterpret_cast<__nv_bfloat162 *>(static_cast<__nv_bfloat16 *>(out) + e);
+        o[0] = __floats2bfloat162_rn(r.x, r.y);
+        o[1] = __floats2bfloat162_rn(r.z, r.w);
+    }
+}
+
+template <int kMode, typename TIn, int NP>
 __global__ void __launch_bounds__(256) dw3_kernel(const TIn *__restrict__ src,
                                                   const float *__restrict__ res,
                                                   const float *__restrict__ w,
@@ -90,46 +139,52 @@ __global__ void __launch_bounds__(256) dw3_kernel(const TIn *__restrict__ src,
     __syncthreads();
     const int row = blockIdx.x;  // b * H + i
     const int i = row % H;
-    const int C4 = C >> 2;
-    for (int t = threadIdx.x; t < W * C4; t += blockDim.x) {
-        const int j = t / C4, c = (t - j * C4) * 4;
-        float4 acc = *reinterpret_cast<const float4 *>(sw + 9 * C + c);
+    const int C4 = C >> 2, Wp = (W + NP - 1) / NP;
+    for (int t = threadIdx.x; t < Wp * C4; t += blockDim.x) {
+        const int j = NP * (t / C4), c = (t - (t / C4) * C4) * 4;
+        float4 acc[NP];
+        acc[0] = *reinterpret_cast<const float4 *>(sw + 9 * C + c);
+#pragma unroll
+        for (int q = 1; q < NP; ++q) acc[q] = acc[0];
 #pragma unroll
         for (int di = -1; di <= 1; ++di) {
             if (i + di < 0 || i + di >= H) continue;
+            const TIn *p = src + ((size_t)(row + di) * W + j) * C + c;
+            // columns j-1 .. j+NP of this row (those outside the map are not read)
+            float4 v[NP + 2];
+#pragma unroll
+            for (int q = 0; q < NP + 2; ++q) {
+                const int jj = j - 1 + q;
+                v[q] = (jj >= 0 && jj < W) ? Vec4<TIn>::load(p + (q - 1) * C)
+                                           : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            }
 #pragma unroll
             for (int dj = -1; dj <= 1; ++dj) {
-                if (j + dj < 0 || j + dj >= W) continue;
-                const float4 v = Vec4<TIn>::load(src + ((size_t)(row + di) * W + j + dj) * C + c);
                 const float4 k = *reinterpret_cast<const float4 *>(sw + ((di + 1) * 3 + dj + 1) * C + c);
-                acc.x = fmaf(k.x, v.x, acc.x);
-                acc.y = fmaf(k.y, v.y, acc.y);
-                acc.z = fmaf(k.z, v.z, acc.z);
-                acc.w = fmaf(k.w, v.w, acc.w);
+#pragma unroll
+                for (int q = 0; q < NP; ++q)
+                    if (j + q + dj >= 0 && j + q + dj < W) fma4(acc[q], k, v[q + dj + 1]);
             }
         }
         const size_t e = ((size_t)row * W + j) * C + c;
-        if (kMode == kCpe) {
-            const float4 x = Vec4<TIn>::load(src + e);
-            *reinterpret_cast<float4 *>(static_cast<float *>(out) + e) =
-                make_float4(x.x + acc.x, x.y + acc.y, x.z + acc.z, x.w + acc.w);
-        } else {
-            float4 r;
-            if (kMode == kGate) {
-                const float4 u = Vec4<TIn>::load(src + e);
-                r = make_float4(u.x + acc.x / (1.0f + __expf(-acc.x)),
-                                u.y + acc.y / (1.0f + __expf(-acc.y)),
-                                u.z + acc.z / (1.0f + __expf(-acc.z)),
-                                u.w + acc.w / (1.0f + __expf(-acc.w)));
-            } else {
-                const float4 y = *reinterpret_cast<const float4 *>(res + e);
-                r = make_float4(y.x + acc.x, y.y + acc.y, y.z + acc.z, y.w + acc.w);
-            }
-            __nv_bfloat162 *o = reinterpret_cast<__nv_bfloat162 *>(static_cast<__nv_bfloat16 *>(out) + e);
-            o[0] = __floats2bfloat162_rn(r.x, r.y);
-            o[1] = __floats2bfloat162_rn(r.z, r.w);
-        }
+#pragma unroll
+        for (int q = 0; q < NP; ++q)
+            if (j + q < W) dw3_store<kMode, TIn>(src, res, out, e + (size_t)q * C, acc[q]);
     }
+}
+
+template <int kMode, typename TIn>
+cudaError_t launch_dw3(const TIn *src, const float *res, const float *w, const float *b, void *out,
+                       int rows, int H, int W, int C, cudaStream_t st)
+{
+    // four pixels a thread when that still leaves every thread two or more of them (CPE at
+    // 192 channels), else two
+    const size_t sm = (size_t)10 * C * sizeof(float);
+    if ((C >> 2) * ((W + 3) / 4) >= 2 * 256)
+        dw3_kernel<kMode, TIn, 4><<<rows, 256, sm, st>>>(src, res, w, b, out, H, W, C);
+    else
+        dw3_kernel<kMode, TIn, 2><<<rows, 256, sm, st>>>(src, res, w, b, out, H, W, C);
+    return cudaGetLastError();
 }
 
 // ------------------------------------------------------------------ launches
@@ -153,9 +208,7 @@ cudaError_t launch_cpe_ln(const float *x, const float *cw, const float *cb, cons
                           const float *beta, float eps, float *x0, __nv_bfloat16 *a, int B, int H,
                           int W, int D, cudaStream_t st)
 {
-    const size_t sm = (size_t)10 * D * sizeof(float);
-    dw3_kernel<kCpe, float><<<B * H, 256, sm, st>>>(x, nullptr, cw, cb, x0, H, W, D);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_dw3<kCpe, float>(x, nullptr, cw, cb, x0, B * H, H, W, D, st);
     if (e != cudaSuccess) return e;
     return launch_ln(x0, g, beta, eps, a, (long)B * H * W, D, st);
 }
@@ -165,28 +218,22 @@ cudaError_t launch_ln(const float *x, const float *g, const float *beta, float e
 {
     const unsigned grid = grid_for(npix * 32);
     if (D <= 256)
-        ln_kernel<8><<<grid, 256, 0, st>>>(x, g, beta, eps, a, npix, D);
+        ln_kernel<4><<<grid, 256, 0, st>>>(x, g, beta, eps, a, npix, D);
     else
-        ln_kernel<32><<<grid, 256, 0, st>>>(x, g, beta, eps, a, npix, D);
+        ln_kernel<16><<<grid, 256, 0, st>>>(x, g, beta, eps, a, npix, D);
     return cudaGetLastError();
 }
 
 cudaError_t launch_dwgate(const float *u, const float *w, const float *b, __nv_bfloat16 *z,
                           long npix, int C, int H, int W, cudaStream_t st)
 {
-    const int rows = (int)(npix / W);
-    dw3_kernel<kGate, float><<<rows, 256, (size_t)10 * C * sizeof(float), st>>>(u, nullptr, w, b, z,
-                                                                              H, W, C);
-    return cudaGetLastError();
+    return launch_dw3<kGate, float>(u, nullptr, w, b, z, (int)(npix / W), H, W, C, st);
 }
 
 cudaError_t launch_posdw(const float *y, const __nv_bfloat16 *z, const float *w, const float *b,
                          __nv_bfloat16 *yb, long npix, int C, int H, int W, cudaStream_t st)
 {
-    const int rows = (int)(npix / W);
-    dw3_kernel<kPos, __nv_bfloat16><<<rows, 256, (size_t)10 * C * sizeof(float), st>>>(
-        z, y, w, b, yb, H, W, C);
-    return cudaGetLastError();
+    return launch_dw3<kPos, __nv_bfloat16>(z, y, w, b, yb, (int)(npix / W), H, W, C, st);
 }
 
 
