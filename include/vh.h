@@ -44,8 +44,11 @@ typedef enum {
     VH_ERR_UNSUPPORTED = -2,   /* valid but not built: head_dim not in {16,32,64}, dtype */
     VH_ERR_CUDA = -3,          /* a CUDA runtime call or launch failed */
     VH_ERR_WORKSPACE = -4,     /* workspace missing, too small or misaligned */
-    VH_ERR_NONFINITE = -5,     /* reserved for a checking helper */
-    VH_ERR_TIMEOUT = -6        /* reserved: no call here waits on another block */
+    VH_ERR_NONFINITE = -5,     /* vh_check: a readout value was not finite */
+    VH_ERR_TIMEOUT = -6,       /* vh_check: a bounded wait on an asynchronous copy or MMA
+                                  expired; that call's results are invalid */
+    VH_ERR_BOUNDS = -7         /* vh_check: an index check of a VH_DEBUG_BOUNDS build failed
+                                  (the access was skipped; results are invalid) */
 } vh_status;
 
 typedef enum { VH_DTYPE_F32 = 0, VH_DTYPE_BF16 = 1 } vh_dtype;
@@ -107,6 +110,12 @@ enum {
     VH_STAT_TIMEOUT = 4,       /* CTAs whose bounded wait on an asynchronous copy or MMA
                                   expired (the kernel then stops issuing work; results
                                   of that call are invalid) */
+    VH_STAT_BOUNDS = 5,        /* index checks that failed; counted only by a library built
+                                  with VH_DEBUG_BOUNDS (libvh_dbg.so), where every global
+                                  access of the scan kernels computed from an index (and the
+                                  shared-memory rows addressed by token position) is checked
+                                  against its array before it is made, and skipped if out
+                                  of range */
     VH_STAT_COUNT = 8
 };
 
@@ -225,12 +234,17 @@ vh_status vh_debug_gelu(const float *a, void *out, long long n, void *stream);
  * vh_check -- wait for `stream` (a cudaStream_t; NULL = legacy default) and read the
  * device counters a scan wrote into `stats` (device [VH_STAT_COUNT], as passed in
  * vh_params.stats).  Returns VH_ERR_TIMEOUT if any CTA's bounded wait expired (the
- * results of that call are invalid), else VH_ERR_NONFINITE if a non-finite readout
- * value was produced, else VH_OK.  VH_ERR_INVALID_ARG for a NULL stats pointer,
+ * results of that call are invalid), else VH_ERR_BOUNDS if an index check of a
+ * VH_DEBUG_BOUNDS build failed, else VH_ERR_NONFINITE if a non-finite readout value was
+ * produced, else VH_OK.  VH_ERR_INVALID_ARG for a NULL stats pointer,
  * VH_ERR_CUDA if the synchronisation or the 64-byte copy fails.  The pages define no
  * such step: it surfaces the kernel's own status flags.
  */
 vh_status vh_check(const unsigned long long *stats, void *stream);
+
+/* 1 in a library built with VH_DEBUG_BOUNDS (libvh_dbg.so: checked indices, counted in
+ * stats[VH_STAT_BOUNDS]), else 0. */
+int vh_debug_bounds_build(void);
 
 /* Bytes of device workspace a vh_scan_forward call with these parameters needs: 0 in
  * the six-memory form, 6 * B * H * W * Cc (the normalised queries as three bf16
@@ -256,7 +270,9 @@ size_t vh_workspace_size(const vh_params *p, int H, int W, unsigned dirs, int ch
  * runs first and writes the boundary states and every token's record; one CUDA-core
  * kernel, fp32, then forms the gradients, summed over routes and images with device
  * atomics (their rounding order is not fixed).  The branch of the step control follows
- * the forward's choice.
+ * the forward's choice.  p->stats, when set, receives the tensor-core pre-pass's counters
+ * (as a forward call's), expired waits and, in a VH_DEBUG_BOUNDS build, failed index
+ * checks of both kernels; read them with vh_check.
  *
  * Errors: as vh_scan_forward; VH_ERR_UNSUPPORTED for control_flags != 0, w_query or
  * skip (the ablation switches and the VisionHOPE-exact readout have no backward);

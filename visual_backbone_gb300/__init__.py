@@ -20,6 +20,10 @@ from typing import Optional
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libvh.so")
+# VH_DEBUG_BOUNDS=1 in the environment loads the checked-index build instead
+# (``_build.build(debug=True)``); its failed checks show up as VH_ERR_BOUNDS in check()
+if os.environ.get("VH_DEBUG_BOUNDS") == "1":
+    LIB_PATH = os.path.join(_HERE, "libvh_dbg.so")
 HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "vh.h")
 
 DIR_RIGHT, DIR_LEFT, DIR_DOWN, DIR_UP, DIR_ALL = 1, 2, 4, 8, 15
@@ -28,7 +32,8 @@ GATE_GENERATED, GATE_FORCED_RAW, GATE_FORCED_EXEC = 0, 1, 2
 CTRL_NO_INJ_CAP, CTRL_NO_SPEC_CLAMP, CTRL_HARD_INJ, CTRL_SOFT_SPEC = 1, 2, 4, 8
 CTRL_NO_DGD, CTRL_FREEZE_KV, CTRL_FREEZE_DYN, CTRL_INTRA_READ = 16, 32, 64, 128
 IMPL = {"auto": 0, "simt": 1, "tc": 2, "tc_wy": 3, "tc_recur": 4}
-STAT_TOKENS, STAT_SPEC_ACTIVE, STAT_INJ_RATIO_GT1, STAT_NONFINITE, STAT_COUNT = 0, 1, 2, 3, 8
+STAT_TOKENS, STAT_SPEC_ACTIVE, STAT_INJ_RATIO_GT1, STAT_NONFINITE = 0, 1, 2, 3
+STAT_TIMEOUT, STAT_BOUNDS, STAT_COUNT = 4, 5, 8
 
 
 class VhError(RuntimeError):
@@ -94,7 +99,8 @@ def lib() -> ctypes.CDLL:
     global _lib
     if _lib is None:
         if not os.path.exists(LIB_PATH):
-            raise RuntimeError(f"libvh.so is not built ({LIB_PATH}); run __graft_entry__.build()")
+            raise RuntimeError(f"{os.path.basename(LIB_PATH)} is not built ({LIB_PATH}); run "
+                               "__graft_entry__.build()")
         L = ctypes.CDLL(LIB_PATH)
         vp, ci, cu = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint
         L.vh_scan_forward.restype = ci
@@ -254,7 +260,7 @@ def backward_workspace_size(x, head_dim: int, dirs: int = DIR_ALL, chunk: int = 
 
 def scan_backward(x, memories0, head_dim: int, dout, dirs: int = DIR_ALL, chunk: int = 0,
                   params: Optional[ScanParams] = None, dir_scale=None, dmem_final=None,
-                  dx=None, dmem0=None, workspace=None, stream=None):
+                  dx=None, dmem0=None, workspace=None, stream=None, stats=None):
     """Outer gradients of scan_forward: (dx fp32 [B][H][W][Cc], dmem0 fp32 [4][nh][4d^2+2d])
     of <dout, out> + <dmem_final, memories_out> for the same x, memories0, params, dirs,
     chunk and dir_scale.  dmem_final (fp32 [B][4][nh][4d^2+2d]) may be None.  The
@@ -280,8 +286,11 @@ def scan_backward(x, memories0, head_dim: int, dout, dirs: int = DIR_ALL, chunk:
         dmem0 = torch.empty_like(memories0)
     _require_cuda("dx", dx, (torch.float32,))
     _require_cuda("dmem0", dmem0, (torch.float32,))
+    if stats is not None:
+        _require_cuda("stats", stats, (torch.int64,))
     cp = make_cparams(B, Cc, head_dim, x.dtype == torch.bfloat16, params,
                       dir_scale_ptr=dir_scale.data_ptr() if dir_scale is not None else 0,
+                      stats_ptr=stats.data_ptr() if stats is not None else 0,
                       stream_ptr=_stream_ptr(stream))
     need = lib().vh_backward_workspace_size(ctypes.byref(cp), H, W, dirs, chunk)
     if workspace is None:

@@ -217,6 +217,7 @@ const char *vh_status_string(vh_status s)
     case VH_ERR_WORKSPACE: return "workspace error";
     case VH_ERR_NONFINITE: return "non-finite value";
     case VH_ERR_TIMEOUT: return "timeout";
+    case VH_ERR_BOUNDS: return "index out of bounds";
     }
     return "unknown status";
 }
@@ -224,6 +225,15 @@ const char *vh_status_string(vh_status s)
 const char *vh_last_error(void) { return g_err; }
 
 int vh_version(void) { return 100; }
+
+int vh_debug_bounds_build(void)
+{
+#ifdef VH_DEBUG_BOUNDS
+    return 1;
+#else
+    return 0;
+#endif
+}
 
 size_t vh_workspace_size(const vh_params *p, int H, int W, unsigned, int)
 {
@@ -244,6 +254,8 @@ vh_status vh_check(const unsigned long long *stats, void *stream)
     if (h[VH_STAT_TIMEOUT])
         return fail(VH_ERR_TIMEOUT, "%llu CTA(s) gave up a bounded wait; results are invalid",
                     h[VH_STAT_TIMEOUT]);
+    if (h[VH_STAT_BOUNDS])
+        return fail(VH_ERR_BOUNDS, "%llu index check(s) failed; results are invalid", h[VH_STAT_BOUNDS]);
     if (h[VH_STAT_NONFINITE])
         return fail(VH_ERR_NONFINITE, "%llu non-finite readout value(s)", h[VH_STAT_NONFINITE]);
     return VH_OK;
@@ -468,8 +480,8 @@ vh_status vh_scan_backward(const void *x, const float *memories0, const vh_param
 
     vh::BwdArgs ba{};
     ba.s = make_args(x, memories0, p, H, W, dirs, chunk, nullptr);
-    ba.s.mem_out = nullptr;
-    ba.s.stats = nullptr;
+    ba.s.mem_out = nullptr;  // (p->stats stays: the pre-pass counts as a forward call, and
+                             // both kernels count expired waits and failed index checks)
     ba.dout = dout;
     ba.dmem_final = dmem_final;
     ba.dx = dx;

@@ -52,6 +52,32 @@ struct ScanArgs {
     int withhold_first_copy;
 };
 
+// Checked index of a VH_DEBUG_BOUNDS build: elements [i, i + n) of an array of `total`
+// elements.  A failed check is counted in stats[VH_STAT_BOUNDS] (when stats are given) and
+// the caller skips the access.  In other builds the check compiles to `true`.
+#ifdef VH_DEBUG_BOUNDS
+__device__ __forceinline__ bool vh_in_bounds(unsigned long long *stats, size_t i, size_t n,
+                                             size_t total)
+{
+    const bool ok = i <= total && n <= total - i;  // a negative index wraps to a huge i
+    if (!ok && stats) atomicAdd(stats + VH_STAT_BOUNDS, 1ull);
+    return ok;
+}
+#define VH_IN(stats, i, n, total) ::vh::vh_in_bounds((stats), (size_t)(i), (size_t)(n), (size_t)(total))
+#else
+#define VH_IN(stats, i, n, total) true
+#endif
+
+// Element counts of the arrays a scan reads and writes (for the checked indices).
+__host__ __device__ __forceinline__ size_t map_elems(const ScanArgs &a)
+{
+    return (size_t)a.B * a.H * a.W * a.Cc;
+}
+__host__ __device__ __forceinline__ size_t state_elems(const ScanArgs &a, int d)
+{
+    return (size_t)4 * d * d + 2 * d;
+}
+
 // Floats of one token record (layout above); the scalar slots follow the three vectors.
 __host__ __device__ constexpr int token_rec_floats(int d) { return 3 * d + 8; }
 enum { TR_KK = 0, TR_SE = 1, TR_SA = 2, TR_KN2 = 3, TR_DD = 4, TR_QQ = 5 };

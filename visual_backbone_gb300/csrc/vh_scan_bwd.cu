@@ -246,7 +246,9 @@ __global__ void __launch_bounds__(256, BwdCfg<D>::MINB) scan_bwd_kernel(const Bw
         for (int e = tid; e < Lt * VPT; e += C::NT) {
             const int j = e / VPT, v = e % VPT;
             const int pix = route_pixel(r, c0 + t0 + j, H, W);
-            const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(xb + (size_t)pix * Cc + v * EPV));
+            const uint4 raw = VH_IN(a.stats, ((size_t)b * N + pix) * Cc + (size_t)h * D + v * EPV, EPV, map_elems(a))
+                                  ? __ldg(reinterpret_cast<const uint4 *>(xb + (size_t)pix * Cc + v * EPV))
+                                  : make_uint4(0u, 0u, 0u, 0u);
             const XT *el = reinterpret_cast<const XT *>(&raw);
 #pragma unroll
             for (int u = 0; u < EPV; ++u) X[j * D + v * EPV + u] = XElem<XT>::to_f(el[u]);
@@ -542,11 +544,14 @@ __global__ void __launch_bounds__(256, BwdCfg<D>::MINB) scan_bwd_kernel(const Bw
                     cp_async16(SC + 4 * e, grec + (size_t)(t0 + e / (C::NSC / 4)) * C::GRS + D + (e % (C::NSC / 4)) * 4);
                 for (int e = tid; e < Lt * VPT; e += C::NT) {
                     const int pix = route_pixel(r, c0 + t0 + e / VPT, H, W);
-                    cp_async16(xraw + (size_t)e * 16, xb + (size_t)pix * Cc + (e % VPT) * EPV);
+                    if (VH_IN(a.stats, ((size_t)b * N + pix) * Cc + (size_t)h * D + (e % VPT) * EPV, EPV,
+                              map_elems(a)))
+                        cp_async16(xraw + (size_t)e * 16, xb + (size_t)pix * Cc + (e % VPT) * EPV);
                 }
                 for (int e = tid; e < Lt * D; e += C::NT) {
                     const int pix = route_pixel(r, c0 + t0 + e / D, H, W);
-                    cp_async4(Y + e, gob + (size_t)pix * Cc + e % D);
+                    if (VH_IN(a.stats, ((size_t)b * N + pix) * Cc + (size_t)h * D + e % D, 1, map_elems(a)))
+                        cp_async4(Y + e, gob + (size_t)pix * Cc + e % D);
                 }
                 cp_async_wait_all();
                 __syncthreads();
@@ -790,8 +795,11 @@ __global__ void __launch_bounds__(256, BwdCfg<D>::MINB) scan_bwd_kernel(const Bw
                                 b2 = fmaf(sq, qba[w], b2);
                             }
                         }
-                        atomicAdd(dxb + (size_t)pixt[0] * Cc + c, (a0 + a1) + a2);
-                        if (two) atomicAdd(dxb + (size_t)pixt[1] * Cc + c, (b0 + b1) + b2);
+                        if (VH_IN(a.stats, ((size_t)b * N + pixt[0]) * Cc + (size_t)h * D + c, 1, map_elems(a)))
+                            atomicAdd(dxb + (size_t)pixt[0] * Cc + c, (a0 + a1) + a2);
+                        if (two &&
+                            VH_IN(a.stats, ((size_t)b * N + pixt[1]) * Cc + (size_t)h * D + c, 1, map_elems(a)))
+                            atomicAdd(dxb + (size_t)pixt[1] * Cc + c, (b0 + b1) + b2);
                     }
                 }
                 __syncwarp();
@@ -823,7 +831,8 @@ __global__ void __launch_bounds__(256, BwdCfg<D>::MINB) scan_bwd_kernel(const Bw
     }
     __syncthreads();
     float *dm = ba.dmem0 + ((size_t)r * a.nh + h) * SZ;
-    for (int e = tid; e < C::R * D; e += C::NT) atomicAdd(dm + e, dS[(e / D) * C::SS + (e % D)]);
+    if (VH_IN(a.stats, ((size_t)r * a.nh + h) * SZ, SZ, (size_t)4 * a.nh * SZ))
+        for (int e = tid; e < C::R * D; e += C::NT) atomicAdd(dm + e, dS[(e / D) * C::SS + (e % D)]);
 }
 
 template <int D, typename XT>

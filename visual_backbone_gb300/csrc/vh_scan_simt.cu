@@ -106,7 +106,10 @@ __device__ __forceinline__ void scan_simt_body(const ScanArgs &a)
     const size_t SZ = (size_t)C::R * D;
 
     if (tid < 3) st_cnt[tid] = 0;
-    const float *m0 = a.mem0 + ((size_t)r * a.nh + h) * SZ;
+    // checked indices (VH_DEBUG_BOUNDS builds; `true` otherwise): this scan's slices of
+    // memories0 and memories_out; every pixel index of the gather, the queries and the adds
+    const size_t mem_base = ((size_t)r * a.nh + h) * SZ;
+    const float *m0 = a.mem0 + (VH_IN(a.stats, mem_base, SZ, (size_t)4 * a.nh * SZ) ? mem_base : 0);
     for (int e = tid; e < C::R * D; e += C::NT) S[(e / D) * C::SS + (e % D)] = m0[e];
 
     const float dgd = (a.control_flags & VH_CTRL_NO_DGD) ? 0.0f : 1.0f;
@@ -142,7 +145,10 @@ __device__ __forceinline__ void scan_simt_body(const ScanArgs &a)
             for (int e = tid; e < Lt * VPT; e += C::NT) {
                 const int j = e / VPT, v = e % VPT;
                 const int pix = route_pixel(r, c0 + t0 + j, H, W);
-                const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(xb + (size_t)pix * Cc + v * EPV));
+                const bool in = VH_IN(a.stats, ((size_t)b * N + pix) * Cc + (size_t)h * D + v * EPV, EPV,
+                                      map_elems(a));
+                const uint4 raw = in ? __ldg(reinterpret_cast<const uint4 *>(xb + (size_t)pix * Cc + v * EPV))
+                                     : make_uint4(0u, 0u, 0u, 0u);
                 const XT *el = reinterpret_cast<const XT *>(&raw);
 #pragma unroll
                 for (int u = 0; u < EPV; ++u) X[j * D + v * EPV + u] = XElem<XT>::to_f(el[u]);
@@ -244,8 +250,11 @@ __device__ __forceinline__ void scan_simt_body(const ScanArgs &a)
                 float kk = 0.0f, qq = 0.0f;
                 // VisionHOPE-exact readout: the query of the token's pixel, already
                 // normalised, from the outer projection's planes
-                const size_t qo = a.qhat ? ((size_t)b * N + PIX[j]) * Cc + (size_t)h * D : 0;
                 const size_t qplane = (size_t)a.B * N * Cc;
+                const size_t qo = (a.qhat && VH_IN(a.stats, ((size_t)b * N + PIX[j]) * Cc + (size_t)h * D, D,
+                                                   qplane))
+                                      ? ((size_t)b * N + PIX[j]) * Cc + (size_t)h * D
+                                      : 0;
 #pragma unroll
                 for (int m = 0; m < CPT3; ++m) {
                     const int c = sl + LPT * m;
@@ -325,7 +334,8 @@ __device__ __forceinline__ void scan_simt_body(const ScanArgs &a)
 #pragma unroll
                     for (int jj = 0; jj < JT; ++jj) {
                         const int j = tg + TG * jj;
-                        if (j < Lt) {
+                        if (j < Lt && VH_IN(a.stats, ((size_t)b * N + PIX[j]) * Cc + (size_t)h * D + i, 1,
+                                            map_elems(a))) {
                             n_nf += !isfinite(acc[jj]);
                             atomicAdd(ob + (size_t)PIX[j] * Cc + i, lm * acc[jj]);
                         }
@@ -352,7 +362,9 @@ __device__ __forceinline__ void scan_simt_body(const ScanArgs &a)
                                 const float lm = lam ? lam[i] : 1.0f;
 #pragma unroll
                                 for (int jj = 0; jj < C::JB; ++jj) {
-                                    if (j0 + jj < Lt) {
+                                    if (j0 + jj < Lt &&
+                                        VH_IN(a.stats, ((size_t)b * N + PIX[j0 + jj]) * Cc + (size_t)h * D + i, 1,
+                                              map_elems(a))) {
                                         n_nf += !isfinite(acc[jj]);
                                         atomicAdd(ob + (size_t)PIX[j0 + jj] * Cc + i, lm * acc[jj]);
                                     }
@@ -549,7 +561,8 @@ __device__ __forceinline__ void scan_simt_body(const ScanArgs &a)
     }
     __syncthreads();
 
-    if (a.mem_out) {
+    if (a.mem_out &&
+        VH_IN(a.stats, (((size_t)b * 4 + r) * a.nh + h) * SZ, SZ, (size_t)a.B * 4 * a.nh * SZ)) {
         float *mo = a.mem_out + (((size_t)b * 4 + r) * a.nh + h) * SZ;
         for (int e = tid; e < C::R * D; e += C::NT) mo[e] = S[(e / D) * C::SS + (e % D)];
     }

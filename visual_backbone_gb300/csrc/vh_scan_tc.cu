@@ -402,8 +402,19 @@ __global__ void __launch_bounds__(NT, 3)
         issue_x(0, 0);
         if (exact) issue_q(0, 0);
     }
+    // checked indices (VH_DEBUG_BOUNDS builds; `true` otherwise): this scan's slices of
+    // memories0, memories_out and the backward records, checked once for their whole extent
+    const size_t mem_base = ((size_t)r * a.nh + h) * SZ;
+    const bool mo_ok = !a.mem_out ||
+                       VH_IN(a.stats, (((size_t)b * 4 + r) * a.nh + h) * SZ, SZ, (size_t)a.B * 4 * a.nh * SZ);
+    const bool ck_ok = !(kAbl && a.ckpt) ||
+                       VH_IN(a.stats, (size_t)blockIdx.x * a.ckpt_stride, (size_t)nlines * SZ,
+                             (size_t)gridDim.x * a.ckpt_stride);
+    const bool rec_ok = !(kAbl && a.rec) ||
+                        VH_IN(a.stats, (size_t)blockIdx.x * a.rec_stride,
+                              (size_t)H * W * token_rec_floats(D), (size_t)gridDim.x * a.rec_stride);
     {
-        const float *m0 = a.mem0 + ((size_t)r * a.nh + h) * SZ;
+        const float *m0 = a.mem0 + (VH_IN(a.stats, mem_base, SZ, (size_t)4 * a.nh * SZ) ? mem_base : 0);
         // memory rows 0..127 (k, v, q, m) -> operand rows 16..143: thread = row
         float v[32];
 #pragma unroll
@@ -413,7 +424,7 @@ __global__ void __launch_bounds__(NT, 3)
         }
 #pragma unroll
         for (int g = 0; g < 4; ++g) store_split8(sS + op_off(ROW_MEM + tid, g), S_PIECE, v + 8 * g);
-        if (kAbl && a.ckpt) {  // boundary state of chunk 0 (backward support)
+        if (kAbl && a.ckpt && ck_ok) {  // boundary state of chunk 0 (backward support)
             float4 *d4 = reinterpret_cast<float4 *>(a.ckpt + (size_t)blockIdx.x * a.ckpt_stride +
                                                     (size_t)tid * D);
 #pragma unroll
@@ -463,8 +474,8 @@ __global__ void __launch_bounds__(NT, 3)
             const int Lt = min(TT, Lline - t0);
             const bool last = s == nsub - 1;
             const int p = box_start(s) + jq;   // position along the line (token pair)
-            const bool valid = !gainw && p >= 0 && p < Lline;
             const int jr = (rev ? Lline - 1 - p : p) - t0;  // route-ordered index in the sub-tile
+            const bool valid = !gainw && p >= 0 && p < Lline && VH_IN(a.stats, jr, 1, TT);
             // ---- MMA 1: generation from the boundary state, Eq. (15):
             //   [s_eta s_alpha 0.. | k_raw | v | q_raw] = x (s1 + s2 + s3)^T
             // one M = 128, N = 112 MMA per piece and K step (x is exact in bf16).  The x
@@ -696,8 +707,8 @@ __global__ void __launch_bounds__(NT, 3)
                 tc_after();
                 float y[32];
                 tmem_ld32(tbase + lrow + COL_RO_WY, y);
-                if (valid) {
-                    const int pix = rowr ? Lidx * W + p : p * W + Lidx;
+                const int pix = rowr ? Lidx * W + p : p * W + Lidx;
+                if (valid && VH_IN(a.stats, ((size_t)b * H * W + pix) * Cc + (size_t)h * D, D, map_elems(a))) {
                     float *dst = ob + (size_t)pix * Cc;
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
@@ -810,7 +821,7 @@ __global__ void __launch_bounds__(NT, 3)
                         dd4[e] = make_float4(vv[4 * e], vv[4 * e + 1], vv[4 * e + 2], vv[4 * e + 3]);
                     }
                     SC[jr] = make_float4(se, sa, kn2, dd2);
-                    if (kAbl && a.rec) {  // token record scalars (backward support); the
+                    if (kAbl && a.rec && rec_ok) {  // token record scalars (backward support); the
                                           // vectors follow while the gain runs
                         float4 *rd = reinterpret_cast<float4 *>(rec_at(a, c * Lline + t0 + jr));
                         rd[3 * D / 4] = make_float4(kkr, se, sa, kn2);
@@ -1180,7 +1191,7 @@ __global__ void __launch_bounds__(NT, 3)
                     const float rq = __frsqrt_rn(qqr + a.knorm_eps);
 #pragma unroll
                     for (int e = 0; e < 32; ++e) qr[e] *= rq;
-                    if (kAbl && a.rec && valid) {  // the token record's vectors: k and delta
+                    if (kAbl && a.rec && rec_ok && valid) {  // the token record's vectors: k and delta
                                                    // from their tiles (read-only here), q
                         float *rq4 = rec_at(a, c * Lline + t0 + jr);
                         float4 *rd = reinterpret_cast<float4 *>(rq4);
@@ -1241,8 +1252,9 @@ __global__ void __launch_bounds__(NT, 3)
                 // readout epilogue: lambda_r y added at the token's pixel (Eq. (26))
                 float y[32];
                 tmem_ld32(tbase + lrow + COL_RO, y);
-                if (valid && (!kAbl || ob)) {
-                    const int pix = rowr ? Lidx * W + p : p * W + Lidx;
+                const int pix = rowr ? Lidx * W + p : p * W + Lidx;
+                if (valid && (!kAbl || ob) &&
+                    VH_IN(a.stats, ((size_t)b * H * W + pix) * Cc + (size_t)h * D, D, map_elems(a))) {
                     float *dst = ob + (size_t)pix * Cc;
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
@@ -1299,7 +1311,7 @@ __global__ void __launch_bounds__(NT, 3)
                     __syncwarp();
                     Sea[lane] = ne;
                     Sea[D + lane] = na;
-                    if (kAbl && a.ckpt && c + 1 < nlines) {  // backward support
+                    if (kAbl && a.ckpt && ck_ok && c + 1 < nlines) {  // backward support
                         float *ck = a.ckpt + (size_t)blockIdx.x * a.ckpt_stride + (size_t)(c + 1) * SZ;
                         ck[4 * D * D + lane] = ne;
                         ck[4 * D * D + D + lane] = na;
@@ -1356,14 +1368,14 @@ __global__ void __launch_bounds__(NT, 3)
                     }
                     if (!frz) store_split8(src, S_PIECE, v + 8 * g);
                 }
-                if (kAbl && a.ckpt && c + 1 < nlines) {  // boundary state of the next chunk
+                if (kAbl && a.ckpt && ck_ok && c + 1 < nlines) {  // boundary state of the next chunk
                     float4 *d4 = reinterpret_cast<float4 *>(a.ckpt + (size_t)blockIdx.x * a.ckpt_stride +
                                                             (size_t)(c + 1) * SZ + (size_t)tid * D);
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
                         d4[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
                 }
-                if (c == nlines - 1 && a.mem_out) {
+                if (c == nlines - 1 && a.mem_out && mo_ok) {
                     float *mo = a.mem_out + (((size_t)b * 4 + r) * a.nh + h) * SZ;
                     float4 *d4 = reinterpret_cast<float4 *>(mo + (size_t)tid * D);
 #pragma unroll
@@ -1377,7 +1389,7 @@ __global__ void __launch_bounds__(NT, 3)
         }
     }
 
-    if (a.mem_out && tid < 2 * D) {
+    if (a.mem_out && mo_ok && tid < 2 * D) {
         float *mo = a.mem_out + (((size_t)b * 4 + r) * a.nh + h) * SZ;
         mo[4 * D * D + tid] = Sea[tid];
     }

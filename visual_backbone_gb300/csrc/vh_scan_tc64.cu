@@ -244,8 +244,13 @@ __global__ void __launch_bounds__(NT, 1)
     __syncthreads();  // barriers initialised, TMEM address written
     const bool issuer = warp == 3 && lane == 0;  // MMA and TMA issue; no token work
     if (issuer) issue_x(0, 0);
+    // checked indices (VH_DEBUG_BOUNDS builds; `true` otherwise): this scan's slices of
+    // memories0 and memories_out, checked once for their whole extent
+    const size_t mem_base = ((size_t)r * a.nh + h) * SZ;
+    const bool mo_ok = !a.mem_out ||
+                       VH_IN(a.stats, (((size_t)b * 4 + r) * a.nh + h) * SZ, SZ, (size_t)a.B * 4 * a.nh * SZ);
     {
-        const float *m0 = a.mem0 + ((size_t)r * a.nh + h) * SZ;
+        const float *m0 = a.mem0 + (VH_IN(a.stats, mem_base, SZ, (size_t)4 * a.nh * SZ) ? mem_base : 0);
         // memory rows 0..255 (k, v, q, m) -> operand rows 16..271: thread = row
         float v[64];
 #pragma unroll
@@ -350,7 +355,7 @@ __global__ void __launch_bounds__(NT, 1)
                     }
                     store_split8(src, S_PIECE, v + 8 * g);
                 }
-                if (c == nlines - 1 && a.mem_out) {
+                if (c == nlines - 1 && a.mem_out && mo_ok) {
                     float *mo = a.mem_out + (((size_t)b * 4 + r) * a.nh + h) * SZ;
                     float4 *d4 = reinterpret_cast<float4 *>(mo + (size_t)(mrow - ROW_MEM) * D);
 #pragma unroll
@@ -366,8 +371,9 @@ __global__ void __launch_bounds__(NT, 1)
             const int Lt = min(TT, Lline - t0);
             const bool last = s == nsub - 1;
             const int p = box_start(s) + lane;  // position along the line (token warps)
-            const bool valid = tokw && p >= 0 && p < Lline;
             const int jr = (rev ? Lline - 1 - p : p) - t0;  // route-ordered index in the sub-tile
+            const bool jr_in = !tokw || VH_IN(a.stats, jr, 1, TT);  // (token warps' row index)
+            const bool valid = tokw && p >= 0 && p < Lline && jr_in;
             // ---- MMA 1: generation from the boundary state, Eq. (15)
             if (issuer) {
                 tc_after();
@@ -425,7 +431,7 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
                     for (int e = 0; e < 64; ++e) kr[e] = 0.0f;
                 }
-                {
+                if (jr_in) {
                     float4 *kd = reinterpret_cast<float4 *>(Kf + jr * KS);
 #pragma unroll
                     for (int e = 0; e < 16; ++e) kd[e] = make_float4(kr[4 * e], kr[4 * e + 1], kr[4 * e + 2], kr[4 * e + 3]);
@@ -445,8 +451,10 @@ __global__ void __launch_bounds__(NT, 1)
                         n_inj += so.inj_ratio_gt1;
                     }
                 }
-                ALP[jr] = alpha;
-                ETA[jr] = eta_t;
+                if (jr_in) {
+                    ALP[jr] = alpha;
+                    ETA[jr] = eta_t;
+                }
                 __syncwarp();
                 // prefix and suffix products of the retentions in route order (lane = route index)
                 float pre = ALP[lane], suf = pre;
@@ -465,11 +473,11 @@ __global__ void __launch_bounds__(NT, 1)
                 if (lane == Lt - 1) *gam_slot = pre;  // gamma_L
                 __syncwarp();
                 // r_j = gamma_{j-1} k_j + delta_j (zero past the chunk)
-                const float gj = GPRE[jr];
-                float4 *dr = reinterpret_cast<float4 *>(DLf + jr * KS);
+                const float gj = jr_in ? GPRE[jr] : 0.0f;
+                float4 *dr = reinterpret_cast<float4 *>(DLf + (jr_in ? jr : 0) * KS);
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
-                    dr[e] = valid ? make_float4(fmaf(gj, kr[4 * e], vv[4 * e]), fmaf(gj, kr[4 * e + 1], vv[4 * e + 1]),
+                    if (jr_in) dr[e] = valid ? make_float4(fmaf(gj, kr[4 * e], vv[4 * e]), fmaf(gj, kr[4 * e + 1], vv[4 * e + 1]),
                                                 fmaf(gj, kr[4 * e + 2], vv[4 * e + 2]), fmaf(gj, kr[4 * e + 3], vv[4 * e + 3]))
                                   : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
             } else if (warp == 4) {
@@ -555,8 +563,8 @@ __global__ void __launch_bounds__(NT, 1)
                 float y[32], y2[32];
                 tmem_ld32(tbase + lrow + COL_RO, y);
                 tmem_ld32(tbase + lrow + COL_RO + 32, y2);
-                if (valid) {
-                    const int pix = rowr ? Lidx * W + p : p * W + Lidx;
+                const int pix = rowr ? Lidx * W + p : p * W + Lidx;
+                if (valid && VH_IN(a.stats, ((size_t)b * H * W + pix) * Cc + (size_t)h * D, D, map_elems(a))) {
                     float *dst = ob + (size_t)pix * Cc;
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
@@ -919,8 +927,9 @@ __global__ void __launch_bounds__(NT, 1)
                 const int half = warp >> 2;
                 float y[32];
                 tmem_ld32(tbase + lrow + COL_RO + 32 * half, y);
-                if (valid) {
-                    const int pix = rowr ? Lidx * W + p : p * W + Lidx;
+                const int pix = rowr ? Lidx * W + p : p * W + Lidx;
+                if (valid && VH_IN(a.stats, ((size_t)b * H * W + pix) * Cc + (size_t)h * D + 32 * half, 32,
+                                   map_elems(a))) {
                     float *dst = ob + (size_t)pix * Cc + 32 * half;
                     const float *lm = lam ? lam + 32 * half : nullptr;
 #pragma unroll
@@ -953,7 +962,7 @@ __global__ void __launch_bounds__(NT, 1)
         }
     }
 
-    if (a.mem_out && tid < 2 * D) {
+    if (a.mem_out && mo_ok && tid < 2 * D) {
         float *mo = a.mem_out + (((size_t)b * 4 + r) * a.nh + h) * SZ;
         mo[4 * D * D + tid] = Sea[tid];
     }
