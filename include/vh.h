@@ -317,6 +317,16 @@ typedef struct {
     const float *b_ff1;              /* [hidden] */
     const void *w_ff2;               /* bf16 [D][hidden] */
     const float *b_ff2;              /* [D] */
+    int f32_intermediates;           /* test mode (0 = off): 1 keeps every intermediate in
+                                        fp32 -- the LN outputs, Z, Y and the FFN's hidden
+                                        layer are never rounded to bf16.  The GEMMs then take
+                                        each fp32 activation as its three bf16 pieces
+                                        (24 significant bits) against the bf16 weights
+                                        repeated three times along K, and the operator runs
+                                        on fp32 Z (CUDA-core scan).  Slower, and a larger
+                                        workspace; it exists so the block can be compared
+                                        element by element with an oracle that rounds
+                                        nothing. */
 } vh_block_weights;
 
 /*
@@ -328,8 +338,8 @@ typedef struct {
  * row/column-aligned chunks.  p->workspace must hold vh_block_workspace_size() bytes,
  * 16-byte aligned: the block's intermediates and the operator's query planes.
  * Activations between layers are bf16 (LN outputs, Z, Y, the FFN's hidden layer before
- * and after GELU); the residual stream is fp32.  p->accumulate and p->memories_out must
- * be 0 / NULL.
+ * and after GELU; fp32 throughout with w->f32_intermediates); the residual stream is
+ * fp32.  p->accumulate and p->memories_out must be 0 / NULL.
  *
  * The four pointwise layers run as the library's own tcgen05 GEMMs (bf16 operands, fp32
  * accumulation in TMEM) with the bias, the residual and (FFN1) the GELU in their

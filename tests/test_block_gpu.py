@@ -50,24 +50,26 @@ def _make(seed, B, H, W, D, Dm, d):
             inp["nh"])
 
 
-def _gpu(vhlib, x, gpu, mem0, wq, skip, lam, d):
+def _gpu(vhlib, x, gpu, mem0, wq, skip, lam, d, f32=False):
     import torch
     st = torch.zeros(8, dtype=torch.int64, device="cuda")
     out = vhlib.block_forward(torch.from_numpy(x).cuda(), torch.from_numpy(mem0).cuda(), gpu, d,
                               w_query=torch.from_numpy(wq).cuda(),
                               skip=torch.from_numpy(skip).cuda(),
-                              dir_scale=torch.from_numpy(lam).cuda(), stats=st)
+                              dir_scale=torch.from_numpy(lam).cuda(), stats=st,
+                              f32_intermediates=f32)
     torch.cuda.synchronize()
     vhlib.check(st)
     return out.cpu().numpy()
 
 
-def _oracle(orc, x, wt, mem0, wq, skip, lam, H, W, nh, d):
+def _oracle(orc, x, wt, mem0, wq, skip, lam, H, W, nh, d, round_bf16=True):
     from oracle import vh_block as vb
     p = orc.OracleParams(alpha_init=float(np.float32(0.9)), gamma_eta=float(np.float32(0.025)),
                          w_query=wq.astype(np.float64), skip=skip.astype(np.float64),
                          dir_scale=lam.astype(np.float64))
-    return vb.block_forward(x.astype(np.float64), wt, mem0.astype(np.float64), H, W, nh, d, p)
+    return vb.block_forward(x.astype(np.float64), wt, mem0.astype(np.float64), H, W, nh, d, p,
+                            round_bf16=round_bf16)
 
 
 CASES = [
@@ -79,8 +81,8 @@ CASES = [
     ("3x70_D64_Dm32_d32", 5, 1, 3, 70, 64, 32, 32),
     ("1x9_D32_Dm16_d16", 6, 2, 1, 9, 32, 16, 16),     # one-row map: the depthwise edges
     ("9x1_D64_Dm32_d32", 8, 1, 9, 1, 64, 32, 32),     # one-column map
-    ("4x5_D256_Dm64_d32", 9, 1, 4, 5, 256, 64, 32),   # FFN wider than the fused kernel takes
-    ("6x7_D192_Dm96_d32", 10, 2, 6, 7, 192, 96, 32),  # the stage-1 widths, fused FFN
+    ("4x5_D256_Dm64_d32", 9, 1, 4, 5, 256, 64, 32),   # N tiles of 192 / 256 (hidden 1024)
+    ("6x7_D192_Dm96_d32", 10, 2, 6, 7, 192, 96, 32),  # the stage-1 widths
 ]
 
 
@@ -113,3 +115,43 @@ def test_block_rejects_on_the_host(vhlib):
         gpu[k] = torch.zeros((16, 12), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(vhlib.VhError, match="dim 12"):
         vhlib.block_forward(x, torch.zeros(4 * 16 * 16 + 32, device="cuda"), gpu, 16)
+
+
+# ---------------------------------------------------------- fp32-intermediate test mode
+#
+# With w->f32_intermediates the library rounds no intermediate to bf16: the GEMMs take each
+# fp32 activation as three bf16 pieces against the weights tripled along K, GELU acts on
+# the unrounded product, and the operator scans fp32 Z.  The oracle drops its rounding
+# points as well, so no bf16 boundary can split the two, and every element is held to the
+# scan's tolerance: max |g - o| / max(|o|, 1e-2 rms(o)) < 2e-3.
+
+@pytest.mark.parametrize("name,seed,B,H,W,D,Dm,d", CASES, ids=[c[0] for c in CASES])
+def test_block_f32_intermediates_elementwise(orc, vhlib, name, seed, B, H, W, D, Dm, d):
+    from tests._helpers import TOL, parity_err
+    x, wt, gpu, mem0, wq, skip, lam, nh = _make(seed, B, H, W, D, Dm, d)
+    g = _gpu(vhlib, x, gpu, mem0, wq, skip, lam, d, f32=True)
+    o = _oracle(orc, x, wt, mem0, wq, skip, lam, H, W, nh, d, round_bf16=False)
+    err = parity_err(g, o)
+    assert err < TOL, (name, err)
+
+
+def test_block_f32_intermediates_stage1_sampled(orc, vhlib):
+    """The stage-1 widths and map in the test mode; the first and last image."""
+    from tests._helpers import TOL, parity_err
+    B, H, W, D, Dm, d = 4, 56, 56, 192, 96, 32
+    x, wt, gpu, mem0, wq, skip, lam, nh = _make(11, B, H, W, D, Dm, d)
+    g = _gpu(vhlib, x, gpu, mem0, wq, skip, lam, d, f32=True)
+    for b in (0, B - 1):
+        o = _oracle(orc, x[b:b + 1], wt, mem0, wq, skip, lam, H, W, nh, d, round_bf16=False)
+        err = parity_err(g[b:b + 1], o)
+        assert err < TOL, (b, err)
+
+
+def test_block_modes_differ_only_by_rounding(orc, vhlib):
+    """The two modes on the same inputs: apart by bf16 rounding (about 2^-8 of a value at
+    most), so a mode that dropped or misplaced a term would stand out."""
+    x, wt, gpu, mem0, wq, skip, lam, nh = _make(12, 1, 6, 7, 64, 32, 32)
+    g16 = _gpu(vhlib, x, gpu, mem0, wq, skip, lam, 32)
+    g32 = _gpu(vhlib, x, gpu, mem0, wq, skip, lam, 32, f32=True)
+    rel = np.abs(g16 - g32).max() / np.sqrt(np.mean(g32.astype(np.float64) ** 2))
+    assert 0 < rel < 0.1, rel

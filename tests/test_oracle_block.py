@@ -131,3 +131,24 @@ def test_gated_branch_and_positional_branch_enter_as_stated(orc):
     # the operator sees Z exactly
     y = orc.forward(a["z"], mem0, 5, 6, nh, 4, params=p)
     np.testing.assert_allclose(a["y"], y, rtol=0, atol=0)
+
+
+def test_f32_mode_is_the_unrounded_block(orc):
+    """round_bf16=False (the library's fp32-intermediate test mode) is the block with no
+    rounding point: it differs from the rounded block, and its residual stream and FFN
+    branch equal the layers written out in fp64 without rounding."""
+    D, Dm, d = 32, 16, 16
+    H, W = 5, 6
+    x, w, mem0, p, nh = _setup(orc, D, Dm, d, seed=21)
+    a = vb.block_forward(x, w, mem0, H, W, nh, d, p, round_bf16=False)
+    b = vb.block_forward(x, w, mem0, H, W, nh, d, p, round_bf16=True)
+    assert np.abs(a - b).max() > 0
+    # the unrounded block against its parts written out without any rounding
+    out, parts = vb.block_forward(x, w, mem0, H, W, nh, d, p, return_parts=True, round_bf16=False)
+    x0 = x + vb.dwconv3(x, w.cpe_w, w.cpe_b)
+    np.testing.assert_allclose(parts["x0"], x0, rtol=0, atol=0)
+    u = vb.layer_norm(x0, w.ln1_g, w.ln1_b, w.ln_eps) @ w.w_in.T + w.b_in
+    np.testing.assert_allclose(parts["u"], u, rtol=1e-13, atol=1e-13)
+    x1 = parts["x1"]
+    ref = x1 + vb.gelu(vb.layer_norm(x1, w.ln2_g, w.ln2_b, w.ln_eps) @ w.w_ff1.T + w.b_ff1) @ w.w_ff2.T + w.b_ff2
+    np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-12)

@@ -60,12 +60,15 @@ class CParams(ctypes.Structure):
     ]
 
 
+BLOCK_WEIGHT_NAMES = ("cpe_w", "cpe_b", "ln1_g", "ln1_b", "w_in", "b_in", "dw_w", "dw_b", "pos_w",
+                      "pos_b", "w_out", "b_out", "ln2_g", "ln2_b", "w_ff1", "b_ff1", "w_ff2", "b_ff2")
+
+
 class CBlockWeights(ctypes.Structure):
     """Mirror of ``vh_block_weights`` (include/vh.h)."""
-    _fields_ = [("dim", ctypes.c_int), ("hidden", ctypes.c_int), ("ln_eps", ctypes.c_float)] + [
-        (n, ctypes.c_void_p) for n in (
-            "cpe_w", "cpe_b", "ln1_g", "ln1_b", "w_in", "b_in", "dw_w", "dw_b", "pos_w", "pos_b",
-            "w_out", "b_out", "ln2_g", "ln2_b", "w_ff1", "b_ff1", "w_ff2", "b_ff2")]
+    _fields_ = ([("dim", ctypes.c_int), ("hidden", ctypes.c_int), ("ln_eps", ctypes.c_float)] +
+                [(n, ctypes.c_void_p) for n in BLOCK_WEIGHT_NAMES] +
+                [("f32_intermediates", ctypes.c_int)])
 
 
 BLOCK_GEMM_WEIGHTS = ("w_in", "w_out", "w_ff1", "w_ff2")   # bf16; the rest fp32
@@ -307,7 +310,7 @@ def scan_backward(x, memories0, head_dim: int, dout, dirs: int = DIR_ALL, chunk:
 
 def block_forward(x, memories0, weights: dict, head_dim: int, params: Optional[ScanParams] = None,
                   w_query=None, skip=None, dir_scale=None, out=None, workspace=None,
-                  stats=None, stream=None, ln_eps: float = 1e-5):
+                  stats=None, stream=None, ln_eps: float = 1e-5, f32_intermediates: bool = False):
     """One VisionHOPE block (Eq. (27), App. B.5): x fp32 [B][H][W][D] (CUDA) -> out.
 
     ``weights`` maps the fields of ``vh_block_weights`` to contiguous CUDA tensors: the
@@ -315,13 +318,13 @@ def block_forward(x, memories0, weights: dict, head_dim: int, params: Optional[S
     [D][hidden]) bf16, the rest fp32.  The operator runs on D_m = w_in.shape[0] channels
     as heads of ``head_dim`` with memories0, the outer query w_query [D_m][D_m], the skip
     [4][D_m] and dir_scale [4][D_m] as in scan_forward.  The workspace (uint8, at least
-    vh_block_workspace_size bytes) is allocated here when not given."""
+    vh_block_workspace_size bytes) is allocated here when not given.  f32_intermediates
+    selects the test mode that rounds no intermediate to bf16."""
     import torch
     _require_cuda("x", x, (torch.float32,))
     _require_cuda("memories0", memories0, (torch.float32,))
     B, H, W, D = x.shape
-    for k in CBlockWeights._fields_[3:]:
-        name = k[0]
+    for name in BLOCK_WEIGHT_NAMES:
         _require_cuda(name, weights[name],
                       (torch.bfloat16,) if name in BLOCK_GEMM_WEIGHTS else (torch.float32,))
     Dm = weights["w_in"].shape[0]
@@ -332,8 +335,8 @@ def block_forward(x, memories0, weights: dict, head_dim: int, params: Optional[S
     if out is None:
         out = torch.empty_like(x)
     _require_cuda("out", out, (torch.float32,))
-    cw = CBlockWeights(D, hidden, ln_eps, *[weights[k[0]].data_ptr()
-                                            for k in CBlockWeights._fields_[3:]])
+    cw = CBlockWeights(D, hidden, ln_eps, *[weights[n].data_ptr() for n in BLOCK_WEIGHT_NAMES],
+                       1 if f32_intermediates else 0)
     cp = make_cparams(B, Dm, head_dim, True, params,
                       dir_scale_ptr=dir_scale.data_ptr() if dir_scale is not None else 0,
                       stats_ptr=stats.data_ptr() if stats is not None else 0,
@@ -351,12 +354,14 @@ def block_forward(x, memories0, weights: dict, head_dim: int, params: Optional[S
     return out
 
 
-def block_workspace_size(x, weights: dict, head_dim: int, with_query: bool = True) -> int:
+def block_workspace_size(x, weights: dict, head_dim: int, with_query: bool = True,
+                         f32_intermediates: bool = False) -> int:
     """Bytes of workspace block_forward needs for x's shape and these weights."""
     B, H, W, D = x.shape
     cp = make_cparams(B, weights["w_in"].shape[0], head_dim, True, None,
                       w_query_ptr=1 if with_query else 0)
-    cw = CBlockWeights(D, weights["w_ff1"].shape[0], 1e-5)
+    cw = CBlockWeights(D, weights["w_ff1"].shape[0], 1e-5, *([None] * len(BLOCK_WEIGHT_NAMES)),
+                       1 if f32_intermediates else 0)
     return int(lib().vh_block_workspace_size(ctypes.byref(cp), ctypes.byref(cw), H, W))
 
 

@@ -20,13 +20,13 @@ cudaError_t launch_qproj(const void *x, bool bf16, int d, const float *wq, const
 cudaError_t launch_scan_bwd(const BwdArgs &ba, int d, bool bf16, cudaStream_t st);
 cudaError_t launch_cpe_ln(const float *x, const float *cw, const float *cb, const float *g,
                           const float *beta, float eps, float *x0, __nv_bfloat16 *a, int B, int H,
-                          int W, int D, cudaStream_t st);
+                          int W, int D, bool split, cudaStream_t st);
 cudaError_t launch_ln(const float *x, const float *g, const float *beta, float eps,
-                      __nv_bfloat16 *a, long npix, int D, cudaStream_t st);
-cudaError_t launch_dwgate(const float *u, const float *w, const float *b, __nv_bfloat16 *z,
-                          long npix, int C, int H, int W, cudaStream_t st);
-cudaError_t launch_posdw(const float *y, const __nv_bfloat16 *z, const float *w, const float *b,
-                         __nv_bfloat16 *yb, long npix, int C, int H, int W, cudaStream_t st);
+                      __nv_bfloat16 *a, long npix, int D, bool split, cudaStream_t st);
+cudaError_t launch_dwgate(const float *u, const float *w, const float *b, void *z, long npix, int C,
+                          int H, int W, bool f32, cudaStream_t st);
+cudaError_t launch_posdw(const float *y, const void *z, const float *w, const float *b, void *yb,
+                         long npix, int C, int H, int W, bool f32, cudaStream_t st);
 cudaError_t launch_gemm_tc(int M, int N, int K, const __nv_bfloat16 *w, const __nv_bfloat16 *act,
                            const float *bias, const float *res, void *out, int epi,
                            cudaStream_t st);
@@ -153,22 +153,25 @@ bool bwd_token_records(const vh_params *p, int H, int W, int chunk)
 
 // Byte offsets of the block's intermediates in its workspace (256-byte aligned regions).
 struct BlockLayout {
-    size_t x0, a, u, z, yb, h, qhat, total;
+    size_t x0, a, u, z, yb, h, qhat, w3, total;  // w3: the GEMM weights tripled along K (f32 mode)
 };
 
 BlockLayout block_layout(const vh_params *p, const vh_block_weights *w, int H, int W)
 {
     BlockLayout L{};
     const size_t N = (size_t)p->batch * H * W, D = w->dim, Dm = p->channels, Hd = w->hidden;
+    // fp32-intermediate test mode: GEMM activations as three bf16 pieces, fp32 Z
+    const size_t pc = w->f32_intermediates ? 3 : 1;
     size_t o = 0;
     auto take = [&](size_t bytes) { const size_t at = o; o += (bytes + 255) & ~(size_t)255; return at; };
     L.x0 = take(N * D * 4);
-    L.a = take(N * D * 2);
+    L.a = take(N * D * 2 * pc);
     L.u = take(N * Dm * 4);
-    L.z = take(N * Dm * 2);
-    L.yb = take(N * Dm * 2);
-    L.h = take(N * Hd * 2);
+    L.z = take(N * Dm * (w->f32_intermediates ? 4 : 2));
+    L.yb = take(N * Dm * 2 * pc);
+    L.h = take(N * Hd * 2 * pc);
     L.qhat = take(p->w_query ? 6 * N * Dm : 0);
+    L.w3 = take(w->f32_intermediates ? 3 * 2 * (Dm * D + D * Dm + Hd * D + D * Hd) : 0);
     L.total = o;
     return L;
 }
@@ -381,43 +384,64 @@ vh_status vh_block_forward(const float *x, const float *memories0, const vh_para
         overlaps(out, xb, p->workspace, L.total))
         return fail(VH_ERR_INVALID_ARG, "x, out and the workspace must not overlap");
     const float eps = w->ln_eps > 0.0f ? w->ln_eps : 1e-5f;
+    const bool f32 = w->f32_intermediates != 0;
+    const int pc = f32 ? 3 : 1;  // bf16 pieces per GEMM activation
     char *ws = static_cast<char *>(p->workspace);
     float *x0 = reinterpret_cast<float *>(ws + L.x0);
     __nv_bfloat16 *a = reinterpret_cast<__nv_bfloat16 *>(ws + L.a);
     float *u = reinterpret_cast<float *>(ws + L.u);  // U, then Y
-    __nv_bfloat16 *z = reinterpret_cast<__nv_bfloat16 *>(ws + L.z);
+    void *z = ws + L.z;
     __nv_bfloat16 *yb = reinterpret_cast<__nv_bfloat16 *>(ws + L.yb);
     __nv_bfloat16 *h = reinterpret_cast<__nv_bfloat16 *>(ws + L.h);
     auto bw = [](const void *q) { return static_cast<const __nv_bfloat16 *>(q); };
     cudaStream_t st = static_cast<cudaStream_t>(p->stream);
-    cudaError_t e;
+    cudaError_t e = cudaSuccess;
+    // the GEMM weights, tripled along K in f32 mode: [rows][3K] = [W | W | W], so that the
+    // product with the three pieces of an activation row is its fp32 product
+    const __nv_bfloat16 *w_in = bw(w->w_in), *w_out = bw(w->w_out), *w_ff1 = bw(w->w_ff1),
+                        *w_ff2 = bw(w->w_ff2);
+    if (f32) {
+        __nv_bfloat16 *w3 = reinterpret_cast<__nv_bfloat16 *>(ws + L.w3);
+        const struct { const __nv_bfloat16 *src; int rows, K; const __nv_bfloat16 **use; } mats[4] = {
+            {w_in, Dm, D, &w_in}, {w_out, D, Dm, &w_out}, {w_ff1, Hd, D, &w_ff1}, {w_ff2, D, Hd, &w_ff2}};
+        for (const auto &m : mats) {
+            for (int k = 0; k < 3 && e == cudaSuccess; ++k)
+                e = cudaMemcpy2DAsync(w3 + (size_t)k * m.K, (size_t)3 * m.K * 2, m.src, (size_t)m.K * 2,
+                                      (size_t)m.K * 2, m.rows, cudaMemcpyDeviceToDevice, st);
+            *m.use = w3;
+            w3 += (size_t)3 * m.K * m.rows;
+        }
+        if (e != cudaSuccess) return cuda_fail(e, "tripling the GEMM weights");
+    }
     // X0 = X + CPE(X), A = LN1(X0)
-    if ((e = vh::launch_cpe_ln(x, w->cpe_w, w->cpe_b, w->ln1_g, w->ln1_b, eps, x0, a, B, H, W, D, st)))
+    if ((e = vh::launch_cpe_ln(x, w->cpe_w, w->cpe_b, w->ln1_g, w->ln1_b, eps, x0, a, B, H, W, D, f32, st)))
         return cuda_fail(e, "CPE + LN1 launch");
     // U = A W_in^T + b_in
-    if ((e = vh::launch_gemm_tc((int)N, Dm, D, bw(w->w_in), a, w->b_in, nullptr, u, 0, st)))
+    if ((e = vh::launch_gemm_tc((int)N, Dm, pc * D, w_in, a, w->b_in, nullptr, u, 0, st)))
         return cuda_fail(e, "Proj_in GEMM launch");
     // Z = U + SiLU(DW(U))
-    if ((e = vh::launch_dwgate(u, w->dw_w, w->dw_b, z, N, Dm, H, W, st)))
+    if ((e = vh::launch_dwgate(u, w->dw_w, w->dw_b, z, N, Dm, H, W, f32, st)))
         return cuda_fail(e, "gated depthwise launch");
     // Y = F_VH(Z), into U's buffer
     vh_params q = *p;
     q.workspace = p->w_query ? ws + L.qhat : nullptr;
     q.workspace_bytes = p->w_query ? 6 * (size_t)N * Dm : 0;
+    if (f32) q.x_dtype = VH_DTYPE_F32;
     if ((s = vh_scan_forward(z, memories0, &q, H, W, VH_DIR_ALL, 0, u)) != VH_OK) return s;
-    // Y += DW_pos(Z), cast for Proj_out
-    if ((e = vh::launch_posdw(u, z, w->pos_w, w->pos_b, yb, N, Dm, H, W, st)))
+    // Y += DW_pos(Z), cast (f32 mode: split) for Proj_out
+    if ((e = vh::launch_posdw(u, z, w->pos_w, w->pos_b, yb, N, Dm, H, W, f32, st)))
         return cuda_fail(e, "positional depthwise launch");
     // X1 = X0 + Y W_out^T + b_out, into out
-    if ((e = vh::launch_gemm_tc((int)N, D, Dm, bw(w->w_out), yb, w->b_out, x0, out, 0, st)))
+    if ((e = vh::launch_gemm_tc((int)N, D, pc * Dm, w_out, yb, w->b_out, x0, out, 0, st)))
         return cuda_fail(e, "Proj_out GEMM launch");
     // out = X1 + W_ff2 GELU(W_ff1 LN2(X1) + b_ff1) + b_ff2
-    if ((e = vh::launch_ln(out, w->ln2_g, w->ln2_b, eps, a, N, D, st))) return cuda_fail(e, "LN2 launch");
-    // H = bf16(GELU(bf16(LN2(X1) W_ff1^T) + b_ff1)) (GELU in the GEMM's epilogue), then
-    // out = X1 + H W_ff2^T + b_ff2
-    if ((e = vh::launch_gemm_tc((int)N, Hd, D, bw(w->w_ff1), a, w->b_ff1, nullptr, h, 1, st)))
+    if ((e = vh::launch_ln(out, w->ln2_g, w->ln2_b, eps, a, N, D, f32, st)))
+        return cuda_fail(e, "LN2 launch");
+    // H = bf16(GELU(bf16(LN2(X1) W_ff1^T) + b_ff1)) (GELU in the GEMM's epilogue; f32 mode:
+    // GELU of the unrounded product, as three pieces), then out = X1 + H W_ff2^T + b_ff2
+    if ((e = vh::launch_gemm_tc((int)N, Hd, pc * D, w_ff1, a, w->b_ff1, nullptr, h, f32 ? 2 : 1, st)))
         return cuda_fail(e, "FFN1 GEMM launch");
-    if ((e = vh::launch_gemm_tc((int)N, D, Hd, bw(w->w_ff2), h, w->b_ff2, out, out, 0, st)))
+    if ((e = vh::launch_gemm_tc((int)N, D, pc * Hd, w_ff2, h, w->b_ff2, out, out, 0, st)))
         return cuda_fail(e, "FFN2 GEMM launch");
     return VH_OK;
 }

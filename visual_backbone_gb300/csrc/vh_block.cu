@@ -22,10 +22,24 @@ namespace vh {
 
 // ------------------------------------------------------------------ kernels
 
-// Per pixel (one warp): a = bf16(LN(x) * g + beta).  A lane holds channel pairs 2 lane +
-// 64 m (8-byte loads, bf16x2 stores); the scale and shift of its channels stay in
-// registers across the pixels it visits.  D even, x 8-byte aligned rows.
-template <int MAXP>
+// v = p1 + p2 + p3 with bf16 pieces, each the rounding of what the previous ones leave
+// (24 significant bits: the fp32-intermediate test mode's GEMM operands).
+__device__ __forceinline__ void split3_bf16x2(float v0, float v1, __nv_bfloat162 &p1, __nv_bfloat162 &p2,
+                                              __nv_bfloat162 &p3)
+{
+    p1 = __floats2bfloat162_rn(v0, v1);
+    const float2 f1 = __bfloat1622float2(p1);
+    const float r0 = v0 - f1.x, r1 = v1 - f1.y;
+    p2 = __floats2bfloat162_rn(r0, r1);
+    const float2 f2 = __bfloat1622float2(p2);
+    p3 = __floats2bfloat162_rn(r0 - f2.x, r1 - f2.y);
+}
+
+// Per pixel (one warp): a = bf16(LN(x) * g + beta), or with kSplit its three bf16 pieces
+// a[pix][c], a[pix][D + c], a[pix][2D + c] (fp32-intermediate test mode).  A lane holds
+// channel pairs 2 lane + 64 m (8-byte loads, bf16x2 stores); the scale and shift of its
+// channels stay in registers across the pixels it visits.  D even, x 8-byte aligned rows.
+template <int MAXP, bool kSplit>
 __global__ void __launch_bounds__(256) ln_kernel(const float *__restrict__ x,
                                                  const float *__restrict__ g,
                                                  const float *__restrict__ beta, float eps,
@@ -61,9 +75,19 @@ __global__ void __launch_bounds__(256) ln_kernel(const float *__restrict__ x,
 #pragma unroll
         for (int m = 0; m < MAXP; ++m) {
             const int c = 2 * lane + 64 * m;
-            if (c < D)
-                *reinterpret_cast<__nv_bfloat162 *>(a + pix * D + c) = __floats2bfloat162_rn(
-                    (v[m].x - mu) * rs * gv[m].x + bv[m].x, (v[m].y - mu) * rs * gv[m].y + bv[m].y);
+            if (c < D) {
+                const float o0 = (v[m].x - mu) * rs * gv[m].x + bv[m].x;
+                const float o1 = (v[m].y - mu) * rs * gv[m].y + bv[m].y;
+                if (kSplit) {
+                    __nv_bfloat162 p1, p2, p3;
+                    split3_bf16x2(o0, o1, p1, p2, p3);
+                    *reinterpret_cast<__nv_bfloat162 *>(a + pix * 3 * D + c) = p1;
+                    *reinterpret_cast<__nv_bfloat162 *>(a + pix * 3 * D + D + c) = p2;
+                    *reinterpret_cast<__nv_bfloat162 *>(a + pix * 3 * D + 2 * D + c) = p3;
+                } else {
+                    *reinterpret_cast<__nv_bfloat162 *>(a + pix * D + c) = __floats2bfloat162_rn(o0, o1);
+                }
+            }
         }
     }
 }
@@ -73,12 +97,14 @@ __global__ void __launch_bounds__(256) ln_kernel(const float *__restrict__ x,
 //   kCpe:  out_f32  = src + b + dw(src)             conditional positional encoding
 //   kGate: out_bf16 = src + SiLU(b + dw(src))       gated depthwise residual branch
 //   kPos:  out_bf16 = res + b + dw(src), src bf16   positional branch, cast for Proj_out
+// and, for the fp32-intermediate test mode, kGateF32 (the gated branch with fp32 out) and
+// kPosSplit (src fp32, out the three bf16 pieces of the positional sum, [pixel][3C]).
 // One CTA per image row.  A thread takes four consecutive channels (16-byte loads) of NP
 // neighbouring pixels: each tap loaded from shared memory serves all of them, and they
 // share the columns of their 3 x 3 windows (3 (NP + 2) 16-byte loads for NP outputs
 // instead of 9 NP).  The taps are summed in the order (di, dj) = (-1, -1), (-1, 0), ... (1, 1),
 // starting from the bias; taps outside the map are skipped.
-enum DwMode { kCpe = 0, kGate = 1, kPos = 2 };
+enum DwMode { kCpe = 0, kGate = 1, kPos = 2, kGateF32 = 3, kPosSplit = 4 };
 
 template <typename T> struct Vec4;
 template <> struct Vec4<float> {
@@ -104,12 +130,32 @@ __device__ __forceinline__ void fma4(float4 &acc, const float4 k, const float4 v
 
 template <int kMode, typename TIn>
 __device__ __forceinline__ void dw3_store(const TIn *__restrict__ src, const float *__restrict__ res,
-                                          void *__restrict__ out, size_t e, float4 acc)
+                                          void *__restrict__ out, size_t e, float4 acc, int C)
 {
     if (kMode == kCpe) {
         const float4 x = Vec4<TIn>::load(src + e);
         *reinterpret_cast<float4 *>(static_cast<float *>(out) + e) =
             make_float4(x.x + acc.x, x.y + acc.y, x.z + acc.z, x.w + acc.w);
+    } else if (kMode == kGateF32) {
+        const float4 u = Vec4<TIn>::load(src + e);
+        *reinterpret_cast<float4 *>(static_cast<float *>(out) + e) =
+            make_float4(u.x + acc.x / (1.0f + __expf(-acc.x)), u.y + acc.y / (1.0f + __expf(-acc.y)),
+                        u.z + acc.z / (1.0f + __expf(-acc.z)), u.w + acc.w / (1.0f + __expf(-acc.w)));
+    } else if (kMode == kPosSplit) {
+        // e = pix * C + c: the pieces go to [pix][c], [pix][C + c], [pix][2C + c]
+        const float4 y = *reinterpret_cast<const float4 *>(res + e);
+        const float4 r = make_float4(y.x + acc.x, y.y + acc.y, y.z + acc.z, y.w + acc.w);
+        const size_t pix = e / C, c = e - pix * C;
+        __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(out) + pix * 3 * C + c;
+        __nv_bfloat162 p1, p2, p3, q1, q2, q3;
+        split3_bf16x2(r.x, r.y, p1, p2, p3);
+        split3_bf16x2(r.z, r.w, q1, q2, q3);
+        reinterpret_cast<__nv_bfloat162 *>(o)[0] = p1;
+        reinterpret_cast<__nv_bfloat162 *>(o)[1] = q1;
+        reinterpret_cast<__nv_bfloat162 *>(o + C)[0] = p2;
+        reinterpret_cast<__nv_bfloat162 *>(o + C)[1] = q2;
+        reinterpret_cast<__nv_bfloat162 *>(o + 2 * C)[0] = p3;
+        reinterpret_cast<__nv_bfloat162 *>(o + 2 * C)[1] = q3;
     } else {
         float4 r;
         if (kMode == kGate) {
@@ -169,7 +215,7 @@ __global__ void __launch_bounds__(256) dw3_kernel(const TIn *__restrict__ src,
         const size_t e = ((size_t)row * W + j) * C + c;
 #pragma unroll
         for (int q = 0; q < NP; ++q)
-            if (j + q < W) dw3_store<kMode, TIn>(src, res, out, e + (size_t)q * C, acc[q]);
+            if (j + q < W) dw3_store<kMode, TIn>(src, res, out, e + (size_t)q * C, acc[q], C);
     }
 }
 
@@ -190,7 +236,7 @@ cudaError_t launch_dw3(const TIn *src, const float *res, const float *w, const f
 // ------------------------------------------------------------------ launches
 
 cudaError_t launch_ln(const float *x, const float *g, const float *beta, float eps,
-                      __nv_bfloat16 *a, long npix, int D, cudaStream_t st);
+                      __nv_bfloat16 *a, long npix, int D, bool split, cudaStream_t st);
 
 namespace {
 
@@ -206,34 +252,49 @@ unsigned grid_for(long threads)
 // CPE (x0 = x + dw(x) + b, fp32) then LN1 (bf16), two bandwidth-bound passes.
 cudaError_t launch_cpe_ln(const float *x, const float *cw, const float *cb, const float *g,
                           const float *beta, float eps, float *x0, __nv_bfloat16 *a, int B, int H,
-                          int W, int D, cudaStream_t st)
+                          int W, int D, bool split, cudaStream_t st)
 {
     cudaError_t e = launch_dw3<kCpe, float>(x, nullptr, cw, cb, x0, B * H, H, W, D, st);
     if (e != cudaSuccess) return e;
-    return launch_ln(x0, g, beta, eps, a, (long)B * H * W, D, st);
+    return launch_ln(x0, g, beta, eps, a, (long)B * H * W, D, split, st);
 }
 
+// LayerNorm of each pixel's D channels to bf16 (split: its three pieces, [pixel][3D]).
 cudaError_t launch_ln(const float *x, const float *g, const float *beta, float eps,
-                      __nv_bfloat16 *a, long npix, int D, cudaStream_t st)
+                      __nv_bfloat16 *a, long npix, int D, bool split, cudaStream_t st)
 {
     const unsigned grid = grid_for(npix * 32);
-    if (D <= 256)
-        ln_kernel<4><<<grid, 256, 0, st>>>(x, g, beta, eps, a, npix, D);
-    else
-        ln_kernel<16><<<grid, 256, 0, st>>>(x, g, beta, eps, a, npix, D);
+    if (D <= 256) {
+        if (split)
+            ln_kernel<4, true><<<grid, 256, 0, st>>>(x, g, beta, eps, a, npix, D);
+        else
+            ln_kernel<4, false><<<grid, 256, 0, st>>>(x, g, beta, eps, a, npix, D);
+    } else {
+        if (split)
+            ln_kernel<16, true><<<grid, 256, 0, st>>>(x, g, beta, eps, a, npix, D);
+        else
+            ln_kernel<16, false><<<grid, 256, 0, st>>>(x, g, beta, eps, a, npix, D);
+    }
     return cudaGetLastError();
 }
 
-cudaError_t launch_dwgate(const float *u, const float *w, const float *b, __nv_bfloat16 *z,
-                          long npix, int C, int H, int W, cudaStream_t st)
+// Z = U + SiLU(DW(U) + b): bf16 Z, or fp32 Z (f32).
+cudaError_t launch_dwgate(const float *u, const float *w, const float *b, void *z, long npix, int C,
+                          int H, int W, bool f32, cudaStream_t st)
 {
+    if (f32) return launch_dw3<kGateF32, float>(u, nullptr, w, b, z, (int)(npix / W), H, W, C, st);
     return launch_dw3<kGate, float>(u, nullptr, w, b, z, (int)(npix / W), H, W, C, st);
 }
 
-cudaError_t launch_posdw(const float *y, const __nv_bfloat16 *z, const float *w, const float *b,
-                         __nv_bfloat16 *yb, long npix, int C, int H, int W, cudaStream_t st)
+// Y + DW(Z) + b for Proj_out: bf16 from bf16 Z, or (f32) the three bf16 pieces from fp32 Z.
+cudaError_t launch_posdw(const float *y, const void *z, const float *w, const float *b, void *yb,
+                         long npix, int C, int H, int W, bool f32, cudaStream_t st)
 {
-    return launch_dw3<kPos, __nv_bfloat16>(z, y, w, b, yb, (int)(npix / W), H, W, C, st);
+    if (f32)
+        return launch_dw3<kPosSplit, float>(static_cast<const float *>(z), y, w, b, yb, (int)(npix / W),
+                                            H, W, C, st);
+    return launch_dw3<kPos, __nv_bfloat16>(static_cast<const __nv_bfloat16 *>(z), y, w, b, yb,
+                                           (int)(npix / W), H, W, C, st);
 }
 
 

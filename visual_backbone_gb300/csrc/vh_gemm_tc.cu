@@ -42,7 +42,7 @@ constexpr int SMEM_BYTES = OFF_BAR + 256;
 static_assert(SMEM_BYTES <= 227 * 1024, "one CTA per SM");
 static_assert(A_STAGE % 1024 == 0 && B_STAGE % 1024 == 0 && OFF_B % 1024 == 0, "swizzled tiles 1 KB aligned");
 
-enum { EPI_F32 = 0, EPI_GELU_BF16 = 1 };
+enum { EPI_F32 = 0, EPI_GELU_BF16 = 1, EPI_GELU_SPLIT3 = 2 };
 
 struct GemmArgs {
     const float *bias;  // [N] or nullptr
@@ -251,6 +251,23 @@ __global__ void __launch_bounds__(NT, 1)
                             out[(size_t)m * g.N + n] = (stg[rr * 33 + lane] + bn) + rv[rr];
                     }
                     __syncwarp();
+                } else if (g.epi == EPI_GELU_SPLIT3) {
+                    // fp32-intermediate test mode: GELU(acc + bias) unrounded, written as its
+                    // three bf16 pieces, out[m][n], out[m][N + n], out[m][2N + n]
+                    const int m = mbase + lane;
+                    __nv_bfloat16 *out = reinterpret_cast<__nv_bfloat16 *>(g.out) + (size_t)m * 3 * g.N;
+                    for (int e = 0; e < 32; ++e) {
+                        const int n = n0 + e;
+                        if (m < g.M && n < g.N) {
+                            const float y = gelu_exact(v[e] + __ldg(g.bias + n));
+                            const __nv_bfloat16 p1 = __float2bfloat16_rn(y);
+                            const float r1 = y - __bfloat162float(p1);
+                            const __nv_bfloat16 p2 = __float2bfloat16_rn(r1);
+                            out[n] = p1;
+                            out[g.N + n] = p2;
+                            out[2 * g.N + n] = __float2bfloat16_rn(r1 - __bfloat162float(p2));
+                        }
+                    }
                 } else {
                     uint32_t *stw = reinterpret_cast<uint32_t *>(stg);
 #pragma unroll
@@ -330,13 +347,15 @@ cudaError_t launch_gelu_debug(const float *a, __nv_bfloat16 *out, long long n, c
 }
 
 // out = act . w^T with the epilogue `epi` (0: + bias + res, fp32 out; 1: bf16 GELU of the
-// bf16-rounded product plus bias).  act [M][K], w [N][K] bf16 row-major; K a multiple of 8
+// bf16-rounded product plus bias; 2: GELU of the unrounded product plus bias as three bf16
+// pieces, out [M][3N]).  act [M][K], w [N][K] bf16 row-major; K a multiple of 8
 // (16-byte rows), 16-byte aligned pointers.  Returns a CUDA error code.
 cudaError_t launch_gemm_tc(int M, int N, int K, const __nv_bfloat16 *w, const __nv_bfloat16 *act,
                            const float *bias, const float *res, void *out, int epi,
                            cudaStream_t st)
 {
-    if (M < 1 || N < 1 || K < 8 || (K & 7) || (epi == gemm::EPI_GELU_BF16 && !bias))
+    if (M < 1 || N < 1 || K < 8 || (K & 7) || epi < gemm::EPI_F32 || epi > gemm::EPI_GELU_SPLIT3 ||
+        (epi != gemm::EPI_F32 && !bias))
         return cudaErrorInvalidValue;
     gemm::GemmArgs g{};
     g.bias = bias;
