@@ -122,6 +122,10 @@ __device__ __forceinline__ float gelu_exact(float a)
     return a * (a < 0.0f ? e : 1.0f - e);
 }
 
+// kSplit3: the fp32-intermediate test mode's epilogue alone (EPI_GELU_SPLIT3), in an
+// instantiation of its own so that its code does not shape the production epilogues'
+// register allocation; otherwise g.epi picks EPI_F32 or EPI_GELU_BF16 at run time.
+template <bool kSplit3>
 __global__ void __launch_bounds__(NT, 1)
     gemm_tc_kernel(const GemmArgs g, const __grid_constant__ CUtensorMap tm_a,
                    const __grid_constant__ CUtensorMap tm_b)
@@ -230,7 +234,7 @@ __global__ void __launch_bounds__(NT, 1)
                 if (n0 >= g.N) continue;
                 // the chunk (row per lane) goes through the warp's staging tile so that the
                 // global accesses run along rows: lane = column (fp32) or 32-bit word (bf16)
-                if (g.epi == EPI_F32) {
+                if (!kSplit3 && g.epi == EPI_F32) {
 #pragma unroll
                     for (int e = 0; e < 32; ++e) stg[lane * 33 + e] = v[e];
                     __syncwarp();
@@ -251,11 +255,12 @@ __global__ void __launch_bounds__(NT, 1)
                             out[(size_t)m * g.N + n] = (stg[rr * 33 + lane] + bn) + rv[rr];
                     }
                     __syncwarp();
-                } else if (g.epi == EPI_GELU_SPLIT3) {
+                } else if (kSplit3) {
                     // fp32-intermediate test mode: GELU(acc + bias) unrounded, written as its
                     // three bf16 pieces, out[m][n], out[m][N + n], out[m][2N + n]
                     const int m = mbase + lane;
                     __nv_bfloat16 *out = reinterpret_cast<__nv_bfloat16 *>(g.out) + (size_t)m * 3 * g.N;
+#pragma unroll
                     for (int e = 0; e < 32; ++e) {
                         const int n = n0 + e;
                         if (m < g.M && n < g.N) {
@@ -381,16 +386,20 @@ cudaError_t launch_gemm_tc(int M, int N, int K, const __nv_bfloat16 *w, const __
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!attr_set[dev]) {
-        e = cudaFuncSetAttribute(gemm::gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 gemm::SMEM_BYTES);
-        if (e != cudaSuccess) return e;
+        for (auto fn : {gemm::gemm_tc_kernel<false>, gemm::gemm_tc_kernel<true>}) {
+            e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, gemm::SMEM_BYTES);
+            if (e != cudaSuccess) return e;
+        }
         e = cudaDeviceGetAttribute(&nsm[dev], cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
         attr_set[dev] = 1;
     }
     const int ntiles = ((M + gemm::BM - 1) / gemm::BM) * g.ntn;
     const unsigned grid = (unsigned)(ntiles < nsm[dev] ? ntiles : nsm[dev]);
-    gemm::gemm_tc_kernel<<<grid, gemm::NT, gemm::SMEM_BYTES, st>>>(g, ma, mb);
+    if (epi == gemm::EPI_GELU_SPLIT3)
+        gemm::gemm_tc_kernel<true><<<grid, gemm::NT, gemm::SMEM_BYTES, st>>>(g, ma, mb);
+    else
+        gemm::gemm_tc_kernel<false><<<grid, gemm::NT, gemm::SMEM_BYTES, st>>>(g, ma, mb);
     return cudaGetLastError();
 }
 
