@@ -19,11 +19,15 @@ constexpr int QMAXC = 128;           // largest Cc handled here
 constexpr int QA_LBO = QM * 16;      // A: K-group stride (one 8-channel TMA box, 2 KB)
 constexpr int QA_SBO = 128;          // A: 8-row stride
 constexpr int QB_LBO = 128;          // B: K-group stride
+constexpr int QST_ROW = 80;          // staging row: one head's 32 bf16 values (64 B) + 16 B pad
+constexpr int QST_PIECE = QM * QST_ROW;
 // Shared memory, sized by Cc at launch: z tile (Cc/8 boxes) | 3 W_q pieces | Cc skip
-// coefficients | mbarriers, TMEM slot, flags.
+// coefficients | the epilogue's staging of one head's three pieces | mbarriers, TMEM slot,
+// flags.
 __host__ __device__ constexpr int qoff_b(int Cc) { return Cc * QA_LBO / 8; }
 __host__ __device__ constexpr int qoff_coef(int Cc) { return qoff_b(Cc) + 3 * Cc * Cc * 2; }
-__host__ __device__ constexpr int qoff_bar(int Cc) { return qoff_coef(Cc) + Cc * 4; }
+__host__ __device__ constexpr int qoff_st(int Cc) { return (qoff_coef(Cc) + Cc * 4 + 15) / 16 * 16; }
+__host__ __device__ constexpr int qoff_bar(int Cc) { return qoff_st(Cc) + 3 * QST_PIECE; }
 __host__ __device__ constexpr int qsmem(int Cc) { return qoff_bar(Cc) + 64; }
 
 __global__ void __launch_bounds__(128, 2)
@@ -112,8 +116,11 @@ __global__ void __launch_bounds__(128, 2)
         // the z tile has been consumed: fetch the next one while the epilogue runs
         if (issuer && !*abort_flag && t + gridDim.x < ntiles) issue_a(t + gridDim.x);
         const long pix = t * QM + tid;
+        const long tile0 = t * QM;                       // first pixel of the tile
+        const int tpix = (int)(npix - tile0 < QM ? npix - tile0 : QM);
         const uint32_t lrow = ((uint32_t)warp * 32u) << 16;
         const size_t plane = (size_t)npix * Cc;
+        unsigned char *stg = sm + qoff_st(Cc);
         for (int h0 = 0; h0 < Cc; h0 += 32) {
             float q[32];
             tmem_ld32(tbase + lrow + (uint32_t)h0, q);
@@ -121,8 +128,8 @@ __global__ void __launch_bounds__(128, 2)
                 const float rq = 1.0f / sqrtf(sumsq32(q) + knorm_eps);
 #pragma unroll
                 for (int e = 0; e < 32; ++e) q[e] *= rq;
-                // three pieces of the head's 32 values: 4 x 16 bytes per piece
-                __nv_bfloat16 *dst = qhat + (size_t)pix * Cc + h0;
+                // three pieces of the head's 32 values, staged by pixel row
+                unsigned char *row = stg + tid * QST_ROW;
 #pragma unroll
                 for (int g = 0; g < 4; ++g) {
                     uint4 w1, w2, w3;
@@ -135,30 +142,38 @@ __global__ void __launch_bounds__(128, 2)
                         b[i] = pack_bf16x2_rn(r0, r1);
                         c[i] = pack_bf16x2_rn(r0 - bf16_lo(b[i]), r1 - bf16_hi(b[i]));
                     }
-                    *reinterpret_cast<uint4 *>(dst + 8 * g) = w1;
-                    *reinterpret_cast<uint4 *>(dst + plane + 8 * g) = w2;
-                    *reinterpret_cast<uint4 *>(dst + 2 * plane + 8 * g) = w3;
+                    *reinterpret_cast<uint4 *>(row + 16 * g) = w1;
+                    *reinterpret_cast<uint4 *>(row + QST_PIECE + 16 * g) = w2;
+                    *reinterpret_cast<uint4 *>(row + 2 * QST_PIECE + 16 * g) = w3;
                 }
             }
+            __syncthreads();
+            // the tile's rows of this head, piece by piece: four 16-byte chunks a row, so a
+            // warp writes eight whole 64-byte row segments per store
+            for (int e = tid; e < 3 * 4 * tpix; e += 128) {
+                const int pcs = e / (4 * tpix), rem = e - pcs * 4 * tpix, r = rem >> 2, ch = rem & 3;
+                const uint4 v = *reinterpret_cast<const uint4 *>(stg + pcs * QST_PIECE + r * QST_ROW + 16 * ch);
+                *reinterpret_cast<uint4 *>(qhat + pcs * plane + (size_t)(tile0 + r) * Cc + h0 + 8 * ch) = v;
+            }
+            __syncthreads();
         }
-        if (skip && pix < npix) {
-            const __nv_bfloat16 *z = x + (size_t)pix * Cc;
-            float *o = out + (size_t)pix * Cc;
-            for (int c0 = 0; c0 < Cc; c0 += 8) {
-                const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(z + c0));
-                const uint32_t *zw = &raw.x;
-#pragma unroll
-                for (int hq = 0; hq < 2; ++hq) {
-                    const float4 c4 = *reinterpret_cast<const float4 *>(coef + c0 + 4 * hq);
-                    float4 v = make_float4(c4.x * bf16_lo(zw[2 * hq]), c4.y * bf16_hi(zw[2 * hq]),
-                                           c4.z * bf16_lo(zw[2 * hq + 1]), c4.w * bf16_hi(zw[2 * hq + 1]));
-                    float4 *dst = reinterpret_cast<float4 *>(o + c0 + 4 * hq);
-                    if (accumulate) {
-                        const float4 a4 = *dst;
-                        v.x += a4.x; v.y += a4.y; v.z += a4.z; v.w += a4.w;
-                    }
-                    *dst = v;
+        if (skip) {
+            // out over the tile's contiguous block of pixels x channels, four channels a
+            // thread per pass, coalesced
+            const size_t base = (size_t)tile0 * Cc;
+            const int n4 = tpix * Cc / 4;
+            for (int e = tid; e < n4; e += 128) {
+                const int c0 = (4 * e) % Cc;
+                const uint2 raw = __ldg(reinterpret_cast<const uint2 *>(x + base + 4 * (size_t)e));
+                const float4 c4 = *reinterpret_cast<const float4 *>(coef + c0);
+                float4 v = make_float4(c4.x * bf16_lo(raw.x), c4.y * bf16_hi(raw.x), c4.z * bf16_lo(raw.y),
+                                       c4.w * bf16_hi(raw.y));
+                float4 *dst = reinterpret_cast<float4 *>(out + base) + e;
+                if (accumulate) {
+                    const float4 a4 = *dst;
+                    v.x += a4.x; v.y += a4.y; v.z += a4.z; v.w += a4.w;
                 }
+                *dst = v;
             }
         }
         tc_before();
@@ -209,7 +224,7 @@ cudaError_t launch_qproj_tc(const void *x, bool bf16, int d, const float *wq, co
         attr_set[dev] = 1;
     }
     const long ntiles = (npix + QM - 1) / QM;
-    const int per_sm = qsmem(Cc) <= 110 * 1024 ? 2 : 1;  // two CTAs per SM when they fit
+    const int per_sm = qsmem(Cc) <= 112 * 1024 ? 2 : 1;  // two CTAs per SM when they fit
     const long slots = (long)per_sm * nsm;
     const unsigned grid = (unsigned)(ntiles < slots ? ntiles : slots);
     qproj_tc_kernel<<<grid, 128, qsmem(Cc), st>>>(tz, static_cast<const __nv_bfloat16 *>(x), wq, skip,
