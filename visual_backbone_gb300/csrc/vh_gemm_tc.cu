@@ -122,6 +122,74 @@ __device__ __forceinline__ float gelu_exact(float a)
     return a * (a < 0.0f ? e : 1.0f - e);
 }
 
+// Packed fp32 pairs (element 0 in the low word): each lane of an .f32x2 instruction is the
+// same correctly rounded fp32 operation as its scalar form.
+typedef unsigned long long f32x2;
+__device__ __forceinline__ f32x2 pk2(float lo, float hi)
+{
+    f32x2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void unpk2(f32x2 v, float &lo, float &hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c)
+{
+    f32x2 d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b)
+{
+    f32x2 d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b)
+{
+    f32x2 d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ f32x2 neg2(f32x2 a) { return a ^ 0x8000000080000000ull; }
+__device__ __forceinline__ f32x2 splat2(float v) { return pk2(v, v); }
+
+// gelu_exact on two values at once, the same operations in the same order on packed
+// pairs (bit for bit the scalar results): about half the instruction issues.
+__device__ __forceinline__ void gelu_exact2(float a0, float a1, float &g0, float &g1)
+{
+    const f32x2 ax = pk2(fminf(fabsf(a0), 13.5f), fminf(fabsf(a1), 13.5f));
+    float d0, d1;
+    unpk2(fma2(ax, splat2(0.353553391f), splat2(1.0f)), d0, d1);
+    const f32x2 t = pk2(rcp_approx(d0), rcp_approx(d1));
+    f32x2 S = splat2(-0.0300543532f);
+    S = fma2(S, t, splat2(0.144723058f));
+    S = fma2(S, t, splat2(-0.248414785f));
+    S = fma2(S, t, splat2(0.144257575f));
+    S = fma2(S, t, splat2(-0.0166995097f));
+    S = fma2(S, t, splat2(0.102680214f));
+    S = fma2(S, t, splat2(0.121239692f));
+    S = fma2(S, t, splat2(0.141226918f));
+    S = fma2(S, t, splat2(0.141041175f));
+    const f32x2 K = splat2(-0.721347520f), K_LO = splat2(-9.62981495e-09f);
+    const f32x2 a2 = mul2(ax, ax);
+    const f32x2 a2_lo = fma2(ax, ax, neg2(a2));
+    const f32x2 yh = mul2(a2, K);
+    const f32x2 yl = add2(fma2(a2, K, neg2(yh)), fma2(a2_lo, K, mul2(a2, K_LO)));
+    float y0, y1;
+    unpk2(yh, y0, y1);
+    const f32x2 p = pk2(ex2_approx(y0), ex2_approx(y1));
+    const f32x2 ex = fma2(p, mul2(yl, splat2(0.693147181f)), p);
+    const f32x2 e = mul2(mul2(t, S), ex);
+    const f32x2 ome = add2(splat2(1.0f), neg2(e));
+    float e0, e1, o0, o1;
+    unpk2(e, e0, e1);
+    unpk2(ome, o0, o1);
+    unpk2(mul2(pk2(a0, a1), pk2(a0 < 0.0f ? e0 : o0, a1 < 0.0f ? e1 : o1)), g0, g1);
+}
+
 // kSplit3: the fp32-intermediate test mode's epilogue alone (EPI_GELU_SPLIT3), in an
 // instantiation of its own so that its code does not shape the production epilogues'
 // register allocation; otherwise g.epi picks EPI_F32 or EPI_GELU_BF16 at run time.
@@ -282,7 +350,9 @@ __global__ void __launch_bounds__(NT, 1)
                         // the product rounded to bf16, then the bias and GELU, rounded again
                         const float p0 = __bfloat162float(__float2bfloat16_rn(v[e])) + b0;
                         const float p1 = __bfloat162float(__float2bfloat16_rn(v[e + 1])) + b1;
-                        stw[lane * 17 + e / 2] = pack_bf16x2_rn(gelu_exact(p0), gelu_exact(p1));
+                        float g0, g1;
+                        gelu_exact2(p0, p1, g0, g1);
+                        stw[lane * 17 + e / 2] = pack_bf16x2_rn(g0, g1);
                     }
                     __syncwarp();
                     // two rows of 16 words per pass
@@ -336,9 +406,18 @@ bool make_gemm_map(CUtensorMap *m, const void *p, int rows, int K, int box_rows)
 // The epilogue's GELU alone: out[i] = bf16(GELU(a[i])).
 __global__ void gelu_debug_kernel(const float *__restrict__ a, __nv_bfloat16 *__restrict__ out, long long n)
 {
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
-         i += (long long)gridDim.x * blockDim.x)
-        out[i] = __float2bfloat16_rn(gelu_exact(a[i]));
+    // pairs through the packed form the FFN1 epilogue uses, a last odd element alone
+    for (long long i = 2 * (blockIdx.x * (long long)blockDim.x + threadIdx.x); i < n;
+         i += 2 * (long long)gridDim.x * blockDim.x) {
+        if (i + 1 < n) {
+            float g0, g1;
+            gelu_exact2(a[i], a[i + 1], g0, g1);
+            out[i] = __float2bfloat16_rn(g0);
+            out[i + 1] = __float2bfloat16_rn(g1);
+        } else {
+            out[i] = __float2bfloat16_rn(gelu_exact(a[i]));
+        }
+    }
 }
 
 }  // namespace gemm
