@@ -202,3 +202,26 @@ def test_full_size_sampled(orc, vhlib, name, variant, impl):
         e_out = parity_err(g["out"][b:b + 1], o)
         e_mem = parity_err(g["mem"][b:b + 1], om)
         assert e_out < TOL and e_mem < TOL, (b, e_out, e_mem)
+
+
+@pytest.mark.parametrize("name", ["stage3"])
+@pytest.mark.parametrize("variant", ["plain", "longmem"])
+def test_full_size_sampled_d64_recurrence(orc, vhlib, name, variant):
+    """Stage-3 with the head_dim-64 tensor-core kernel's blocked recurrence forced (the
+    default there is the WY form): the whole batch, oracle on the first and last image."""
+    test_full_size_sampled(orc, vhlib, name, variant, "tc_recur")
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_kernels_agree_on_every_image(vhlib, name):
+    """The tensor-core kernel (as benchmarked) and the CUDA-core kernel, two independent
+    implementations, on the whole batch: every image, every element within the tolerance
+    (the oracle checks the first and last image above)."""
+    wl = synth.WORKLOADS[name].long_memory()
+    inp = synth.make_inputs(wl)
+    g = run_gpu(vhlib, inp, want_memories=True, impl="auto")
+    s = run_gpu(vhlib, inp, want_memories=True, impl="simt")
+    for b in range(wl.B):
+        e_out = parity_err(g["out"][b:b + 1], s["out"][b:b + 1])
+        e_mem = parity_err(g["mem"][b:b + 1], s["mem"][b:b + 1])
+        assert e_out < TOL and e_mem < TOL, (b, e_out, e_mem)
