@@ -162,6 +162,7 @@ __global__ void __launch_bounds__(128, 2)
             // thread per pass, coalesced
             const size_t base = (size_t)tile0 * Cc;
             const int n4 = tpix * Cc / 4;
+#pragma unroll 8
             for (int e = tid; e < n4; e += 128) {
                 const int c0 = (4 * e) % Cc;
                 const uint2 raw = __ldg(reinterpret_cast<const uint2 *>(x + base + 4 * (size_t)e));
