@@ -62,6 +62,7 @@ __global__ void __launch_bounds__(128, 2)
     }
     // W_q as the B operand: element (n = output, k = input) at
     // (n/8) * bsbo + (k/8) * 128 + (n%8) * 16 + (k%8) * 2 of each piece
+#pragma unroll 4
     for (int it = tid; it < Cc * (Cc / 8); it += 128) {
         const int n = it / (Cc / 8), kg = it % (Cc / 8);
         const float4 *w4 = reinterpret_cast<const float4 *>(wq + (size_t)n * Cc + 8 * kg);
@@ -150,6 +151,7 @@ __global__ void __launch_bounds__(128, 2)
             __syncthreads();
             // the tile's rows of this head, piece by piece: four 16-byte chunks a row, so a
             // warp writes eight whole 64-byte row segments per store
+#pragma unroll 4
             for (int e = tid; e < 3 * 4 * tpix; e += 128) {
                 const int pcs = e / (4 * tpix), rem = e - pcs * 4 * tpix, r = rem >> 2, ch = rem & 3;
                 const uint4 v = *reinterpret_cast<const uint4 *>(stg + pcs * QST_PIECE + r * QST_ROW + 16 * ch);
