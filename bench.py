@@ -915,10 +915,12 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="stage1")
     ap.add_argument("--variant", choices=["plain", "longmem"], default="plain")
-    ap.add_argument("--kernel", choices=["auto", "simt", "tc", "tc_wy", "tc_recur"], default="auto",
+    ap.add_argument("--kernel", choices=["auto", "simt", "tc", "tc_wy", "tc_recur", "tc_pipe"],
+                    default="auto",
                     help="scan kernel: auto / tc (tensor core, its faster gain form), tc_wy or "
                          "tc_recur (tensor core with the WY or the blocked-recurrence gain, the "
-                         "A/B pair at d = 32), simt (fp32 CUDA cores)")
+                         "A/B pair at d = 32), tc_pipe (the recurrence with a line's sub-tiles "
+                         "pipelined), simt (fp32 CUDA cores)")
     ap.add_argument("--chunk", type=int, default=-1,
                     help="chunk length for every route (the chunk-length ablation); default: "
                          "the workload's (rows / columns); a length that is not the row or "

@@ -97,8 +97,16 @@ enum {
                                   G = gamma_L I + W' K^T on the tensor core); the method as
                                   defined only, with H, W <= 64 at head_dim 32 and H, W <= 32
                                   at head_dim 64, else VH_ERR_UNSUPPORTED */
-    VH_IMPL_TC_RECUR = 4       /* tensor-core kernel, shared gain as the blocked per-token
-                                  recurrence of Eq. (46) */
+    VH_IMPL_TC_RECUR = 4,      /* tensor-core kernel, shared gain as the blocked per-token
+                                  recurrence of Eq. (46), one sub-tile after the other */
+    VH_IMPL_TC_PIPE = 5        /* head_dim 32 tensor-core kernel, the blocked recurrence with
+                                  the 64-token sub-tiles of a line pipelined: one warp pair
+                                  prepares and reads out sub-tile s + 1 while the other runs
+                                  the gain over sub-tile s (the same arithmetic as
+                                  VH_IMPL_TC_RECUR).  The method as defined only (no
+                                  control_flags, no w_query), else VH_ERR_UNSUPPORTED.
+                                  VH_IMPL_AUTO and VH_IMPL_TC take it where a line spans
+                                  several sub-tiles and the grid fits two CTAs per SM */
 };
 
 /* Indices of the optional device counters (params->stats, 8 x uint64). */

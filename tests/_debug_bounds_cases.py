@@ -17,6 +17,8 @@ CASES = [
     ("tc32-3x4", (1, 3, 4, 2, 32, 0, "bf16"), {"impl": "tc"}),
     ("tc32-70x5", (1, 70, 5, 1, 32, 0, "bf16"), {"impl": "tc"}),
     ("tc32-wy", (2, 9, 14, 2, 32, 0, "bf16"), {"impl": "tc_wy"}),
+    ("tc32-pipe", (1, 6, 131, 1, 32, 0, "bf16"), {"impl": "tc_pipe"}),
+    ("tc32-pipe-cols", (1, 70, 5, 1, 32, 0, "bf16"), {"impl": "tc_pipe"}),
     ("tc32-exact", (2, 7, 12, 2, 32, 0, "bf16"), {"impl": "tc", "exact": True}),
     ("tc64-14x14", (2, 14, 14, 1, 64, 0, "bf16"), {"impl": "tc"}),
     ("tc64-3x40", (1, 3, 40, 1, 64, 0, "bf16"), {"impl": "tc"}),

@@ -59,7 +59,7 @@ def test_expired_wait_reports_timeout_and_leaves_context_usable(vhlib, orc):
     inp = synth.make_inputs(wl)
     x = torch.from_numpy(inp.x_store.view(np.int16)).view(torch.bfloat16).cuda()
     m = torch.from_numpy(inp.mem0).cuda()
-    for impl in ("tc_recur", "tc_wy"):
+    for impl in ("tc_recur", "tc_wy", "tc_pipe"):
         st = torch.zeros(8, dtype=torch.int64, device="cuda")
         p = vhlib.ScanParams(alpha_init=wl.alpha_init, impl=impl, wait_limit=20000,
                              withhold_first_copy=True)
@@ -76,7 +76,8 @@ def test_expired_wait_reports_timeout_and_leaves_context_usable(vhlib, orc):
         assert parity_err(out.cpu().numpy(), o) < TOL
 
 
-@pytest.mark.parametrize("d,impl", [(32, "tc_recur"), (32, "tc_wy"), (64, "tc_wy"), (64, "tc_recur")])
+@pytest.mark.parametrize("d,impl", [(32, "tc_recur"), (32, "tc_wy"), (32, "tc_pipe"), (64, "tc_wy"),
+                                    (64, "tc_recur")])
 def test_wait_expiring_mid_scan_drains(vhlib, orc, d, impl):
     """A one-cycle wait limit makes the first wait that is not already complete give up
     while the CTA's own MMAs (and possibly a copy) are in flight.  The CTA lets them land

@@ -31,7 +31,7 @@ DTYPE_F32, DTYPE_BF16 = 0, 1
 GATE_GENERATED, GATE_FORCED_RAW, GATE_FORCED_EXEC = 0, 1, 2
 CTRL_NO_INJ_CAP, CTRL_NO_SPEC_CLAMP, CTRL_HARD_INJ, CTRL_SOFT_SPEC = 1, 2, 4, 8
 CTRL_NO_DGD, CTRL_FREEZE_KV, CTRL_FREEZE_DYN, CTRL_INTRA_READ = 16, 32, 64, 128
-IMPL = {"auto": 0, "simt": 1, "tc": 2, "tc_wy": 3, "tc_recur": 4}
+IMPL = {"auto": 0, "simt": 1, "tc": 2, "tc_wy": 3, "tc_recur": 4, "tc_pipe": 5}
 STAT_TOKENS, STAT_SPEC_ACTIVE, STAT_INJ_RATIO_GT1, STAT_NONFINITE = 0, 1, 2, 3
 STAT_TIMEOUT, STAT_BOUNDS, STAT_COUNT = 4, 5, 8
 

@@ -79,7 +79,7 @@ vh_status check_scan(const vh_params *p, unsigned dirs, int chunk)
     if (p->gate_mode < 0 || p->gate_mode > 2) return fail(VH_ERR_INVALID_ARG, "gate_mode %d", p->gate_mode);
     if (!(p->alpha_init > 0.0f && p->alpha_init < 1.0f))
         return fail(VH_ERR_INVALID_ARG, "alpha_init %g must lie in (0,1)", (double)p->alpha_init);
-    if (p->impl < VH_IMPL_AUTO || p->impl > VH_IMPL_TC_RECUR) return fail(VH_ERR_INVALID_ARG, "impl %d", p->impl);
+    if (p->impl < VH_IMPL_AUTO || p->impl > VH_IMPL_TC_PIPE) return fail(VH_ERR_INVALID_ARG, "impl %d", p->impl);
     if (p->control_flags & ~(unsigned)VH_CTRL_ALL)
         return fail(VH_ERR_INVALID_ARG, "control_flags 0x%x has unknown bits", p->control_flags);
     return VH_OK;
@@ -329,7 +329,8 @@ vh_status vh_scan_forward(const void *x, const float *memories0, const vh_params
             e = vh::launch_scan_tc(a, d, bf16, st, &handled, p->impl);
         if (e == cudaErrorNotSupported)
             return fail(VH_ERR_UNSUPPORTED, "the WY gain needs the method as defined (no control_flags, "
-                        "no w_query) and H, W <= 64 (head_dim 32) or <= 32 (head_dim 64)");
+                        "no w_query) and H, W <= 64 (head_dim 32) or <= 32 (head_dim 64); the "
+                        "pipelined form needs head_dim 32 and the method as defined");
         if (e != cudaSuccess) return cuda_fail(e, "tensor-core scan launch");
         if (!handled && p->impl != VH_IMPL_AUTO)
             return fail(VH_ERR_UNSUPPORTED, "no tensor-core kernel for d=%d dtype=%d chunk=%d",

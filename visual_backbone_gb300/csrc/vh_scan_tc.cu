@@ -85,6 +85,16 @@ constexpr int OFF_GT = OFF_SC + TT * 16;          // per block: k_a . k_b, a < b
 constexpr int OFF_BAR = OFF_GT + TT / NB * 8 * 4; // mbarriers, TMEM base, flags
 constexpr int SMEM_BYTES = OFF_BAR + 128;
 static_assert(SMEM_BYTES <= 75 * 1024, "three CTAs per SM");
+// Pipelined form for lines of several sub-tiles: a second set of the key, delta, scalar and
+// Gram tiles past the default layout, so the token pair prepares sub-tile s + 1 in one set
+// while the gain pair runs sub-tile s from the other.  Launched with this larger size (two
+// CTAs per SM).
+constexpr int OFF_KF2 = (SMEM_BYTES + 15) / 16 * 16;
+constexpr int OFF_DL2 = OFF_KF2 + TT * KS * 4;
+constexpr int OFF_SC2 = OFF_DL2 + TT * KS * 4;
+constexpr int OFF_GT2 = OFF_SC2 + TT * 16;
+constexpr int SMEM_PIPE = OFF_GT2 + TT / NB * 8 * 4;
+static_assert(SMEM_PIPE <= 113 * 1024, "two CTAs per SM");
 // Intra-chunk readout (ablation), past the default layout: fp32 normalised queries in
 // route order, and per block of NB tokens the cross entries k_a . q_b, a < b (6 of 8).
 // Launched with this larger size, the kernel runs two CTAs per SM.
@@ -278,7 +288,9 @@ __device__ __forceinline__ void wy_solve(const float *__restrict__ dl, const flo
 // (false for the method as defined, so its hot loops carry no test of them).
 // kWY: the shared gain in WY form (chunks of one sub-tile, the method as defined: kAbl
 // false, no outer queries); otherwise the blocked recurrence.
-template <bool kAbl, bool kWY>
+// kPipe: the blocked recurrence with the sub-tiles of a line pipelined across the two warp
+// pairs (the method as defined, no outer queries); the same arithmetic in the same order.
+template <bool kAbl, bool kWY, bool kPipe = false>
 __global__ void __launch_bounds__(NT, 3)
     scan_tc_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tm_row,
                    const __grid_constant__ CUtensorMap tm_col,
@@ -467,6 +479,623 @@ __global__ void __launch_bounds__(NT, 3)
     // 32(w - rw) + l, TMEM lane 32 rw + that row
     const int jq = 32 * (warp - rw) + lane;
 
+    // ---- the phases of one sub-tile, shared by the sequential and the pipelined loop.
+    // The per-token tiles (keys, deltas, scalars, Gram entries) are passed in, so the
+    // pipelined loop can alternate between two sets of them.
+    auto generate = [&](int c, int s) {
+        // ---- MMA 1: generation from the boundary state, Eq. (15):
+        //   [s_eta s_alpha 0.. | k_raw | v | q_raw] = x (s1 + s2 + s3)^T
+        // one M = 128, N = 112 MMA per piece and K step (x is exact in bf16).  The x
+        // tile is A rows 32 rw..32 rw+63; the other 64 A rows read the kilobyte next to
+        // the tile into TMEM lanes nobody reads.
+        if (issuer) {
+            tc_after();
+            if (wait_copy(mb_x, ph_x, nx_obs) && !*abort_flag) {
+                const uint64_t dq = sdesc(smem_u32(sX) - (rw >> 1) * LBO_X, LBO_X, SBO_X);
+                const uint64_t ds = sdesc(smem_u32(sS), LBO_K32, SBO_K32);
+#pragma unroll
+                for (int pc = 0; pc < 3; ++pc)
+#pragma unroll
+                    for (int ks = 0; ks < 2; ++ks)
+                        mma(tbase + COL_GEN, dadd(dq, ks * 2 * LBO_X),
+                            dadd(ds, pc * S_PIECE + ks * 2 * LBO_K32), idesc_bf16(128, 112),
+                            (pc | ks) != 0);
+                mma_commit(mb_gen);
+            }
+        }
+        ph_x ^= 1;
+        wt.wait(mb_gen, ph_gen);
+        ph_gen ^= 1;
+        tc_after();
+        // the x tile is free again: fetch the next sub-tile while this one is processed
+        if (issuer && !*abort_flag) {
+            const int ns = (s + 1 < nsub) ? s + 1 : 0;
+            const int nc = (s + 1 < nsub) ? c : c + 1;
+            if (nc < nlines) issue_x(nc, ns);
+        }
+    };
+    // per-token step, Eqs. (15), (19), (20), (53), on the token pair (lane = token):
+    // normalise k, form delta = k - v and their squared norms, publish the token's scalars
+    auto token_step = [&](float *KfT, float *DLT, float4 *SCT, bool valid, int jr, int c, int t0) {
+        float kr[32], vv[32];
+        float se, sa;
+        tmem_ld_kvs(tbase + lrow + COL_GEN, kr, vv, se, sa);
+        const float kkr = sumsq32(kr);
+        const float rk = __frsqrt_rn(kkr + a.knorm_eps);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+            kr[e] *= rk;            // k
+            vv[e] = kr[e] - vv[e];  // delta = k - v
+        }
+        const float kn2 = sumsq32(kr), dd2 = sumsq32(vv);
+        if (valid) {
+            float4 *kd = reinterpret_cast<float4 *>(KfT + jr * KS);
+            float4 *dd4 = reinterpret_cast<float4 *>(DLT + jr * KS);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                kd[e] = make_float4(kr[4 * e], kr[4 * e + 1], kr[4 * e + 2], kr[4 * e + 3]);
+                dd4[e] = make_float4(vv[4 * e], vv[4 * e + 1], vv[4 * e + 2], vv[4 * e + 3]);
+            }
+            SCT[jr] = make_float4(se, sa, kn2, dd2);
+            if (kAbl && a.rec && rec_ok) {  // token record scalars (backward support); the
+                                  // vectors follow while the gain runs
+                float4 *rd = reinterpret_cast<float4 *>(rec_at(a, c * Lline + t0 + jr));
+                rd[3 * D / 4] = make_float4(kkr, se, sa, kn2);
+                rd[3 * D / 4 + 1].x = dd2;
+            }
+        }
+        if (intra) {
+            // the normalised query for the gain pair, route order (fp32)
+            float qv[32];
+            if (!exact) {
+                tmem_ld32(tbase + lrow + COL_GEN + COL_QR, qv);
+                const float rq = __frsqrt_rn(sumsq32(qv) + a.knorm_eps);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) qv[e] *= rq;
+            } else {
+                // the outer query's three pieces from its TMA tile
+                wait_copy(mb_q, ph_q, nq_obs);  // (the drain reads the issuer's count)
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    const unsigned char *src = sQ + g * QX_LBO + jq * 16;
+                    const uint4 u1 = *reinterpret_cast<const uint4 *>(src);
+                    const uint4 u2 = *reinterpret_cast<const uint4 *>(src + QX_PIECE);
+                    const uint4 u3 = *reinterpret_cast<const uint4 *>(src + 2 * QX_PIECE);
+                    const uint32_t *w1 = &u1.x, *w2 = &u2.x, *w3 = &u3.x;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        qv[8 * g + 2 * i] = bf16_lo(w1[i]) + (bf16_lo(w2[i]) + bf16_lo(w3[i]));
+                        qv[8 * g + 2 * i + 1] = bf16_hi(w1[i]) + (bf16_hi(w2[i]) + bf16_hi(w3[i]));
+                    }
+                }
+            }
+            if (valid) {
+                float4 *qd = reinterpret_cast<float4 *>(Qf + jr * KS);
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    qd[e] = make_float4(qv[4 * e], qv[4 * e + 1], qv[4 * e + 2], qv[4 * e + 3]);
+            }
+        }
+    };
+    // gain pair (lane = route-ordered token): the gates and the step control
+    auto gate_step = [&](float4 *SCT, int Lt) {
+        // gates and step control of route-ordered token jg; the coefficients of the
+        // gain recurrence replace the scalars: (alpha, eta/alpha, 1/alpha, eta) for the
+        // scaled form, (alpha, 0, 0, eta) where alpha is too small to divide by
+        const int jg = tid & 63;
+        const bool tv = jg < Lt;
+        float alpha = 1.0f;
+        if (tv) {
+            const float4 sc = SCT[jg];
+            float eta, oma;
+            gates(a, sc.x, sc.y, eta, alpha, oma);
+            float eta_t;
+            if (a.gate_mode == VH_GATE_FORCED_EXEC) {
+                eta_t = a.forced_eta;
+            } else {
+                const StepOut so = step_control<kAbl>(a, eta, alpha, oma, sc.z, sc.w);
+                eta_t = so.eta_tilde;
+                n_spec += so.spec_active;
+                n_inj += so.inj_ratio_gt1;
+            }
+            const bool keep = alpha >= 1e-6f;
+            SCT[jg] = make_float4(alpha, keep ? __fdividef(eta_t, alpha) : 0.0f,
+                                 keep ? __frcp_rn(alpha) : 0.0f, eta_t);
+        }
+        // tokens whose retention could underflow the scaled gain within a few steps
+        const unsigned small = __ballot_sync(0xffffffffu, tv && !(alpha >= 0.01f));
+        if (lane == 0) vote[warp - 2 * gp] = small != 0u;
+    };
+    // token pair: the Gram entries of the gain recurrence's blocks
+    auto gram_step = [&](const float *KfT, float *GTT) {
+        // Gram entries k_a . k_b of each block of NB route-ordered tokens.  This
+        // warp's tokens are the 32 consecutive route rows from R0 (route order runs
+        // with the box rows forwards, against them backwards), eight whole blocks:
+        // pair i of block q goes to lane 6q + i (mod 32).
+        const int R0 = rev ? TT - 32 - 32 * (warp - rw) : 32 * (warp - rw);
+#pragma unroll
+        for (int pr = lane; pr < 48; pr += 32) {
+            const int q = pr / 6, pi = pr - 6 * q;
+            const int ia = pi < 3 ? 0 : (pi < 5 ? 1 : 2);
+            const int ib = pi < 3 ? pi + 1 : (pi < 5 ? pi - 1 : 3);
+            const float4 *ka = reinterpret_cast<const float4 *>(KfT + (R0 + NB * q + ia) * KS);
+            const float4 *kb = reinterpret_cast<const float4 *>(KfT + (R0 + NB * q + ib) * KS);
+            float g4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float4 fa = ka[e], fb = kb[e];
+                g4[0] = fmaf(fa.x, fb.x, g4[0]);
+                g4[1] = fmaf(fa.y, fb.y, g4[1]);
+                g4[2] = fmaf(fa.z, fb.z, g4[2]);
+                g4[3] = fmaf(fa.w, fb.w, g4[3]);
+            }
+            GTT[(R0 / NB + q) * 8 + pi] = (g4[0] + g4[1]) + (g4[2] + g4[3]);
+            if (intra) {  // and k_a . q_b for the intra-chunk readout
+                const float4 *qb = reinterpret_cast<const float4 *>(Qf + (R0 + NB * q + ib) * KS);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) g4[e] = 0.0f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float4 fa = ka[e], fb = qb[e];
+                    g4[0] = fmaf(fa.x, fb.x, g4[0]);
+                    g4[1] = fmaf(fa.y, fb.y, g4[1]);
+                    g4[2] = fmaf(fa.z, fb.z, g4[2]);
+                    g4[3] = fmaf(fa.w, fb.w, g4[3]);
+                }
+                CQ[(R0 / NB + q) * 8 + pi] = (g4[0] + g4[1]) + (g4[2] + g4[3]);
+            }
+        }
+    };
+    // gain pair: the shared gain over one sub-tile (first: the chunk's first; last: write G)
+    auto gain_step = [&](const float *KfT, float *DLT, const float4 *SCT, const float *GTT, int Lt,
+                         bool first, bool last) {
+        // ---- shared gain over this sub-tile's tokens, in route order, on the gain
+        // pair: its thread t owns row t/2 of G and columns 16(t%2)..16(t%2)+15 (one
+        // shuffle per token).  G = gam * ghat with
+        //   ghat <- ghat - (eta/alpha) (ghat k + delta / gam) k^T,  gam <- alpha gam,
+        // a pure scaling of G_j = alpha G_{j-1} - eta (G_{j-1} k + delta) k^T.  When
+        // every alpha of the sub-tile is >= 0.01 the scale is folded back every eight
+        // tokens (it cannot underflow sooner); otherwise every token is checked, and a
+        // token with alpha < 1e-6 is applied to G directly with the scale folded in.
+        const int grow = (tid & 63) >> 1, gq = tid & 1;
+        if (first) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) gh[e] = (16 * gq + e == grow) ? 1.0f : 0.0f;
+            gam = 1.0f;
+            inv_gam = 1.0f;
+        }
+        const bool careful = (vote[0] | vote[1]) != 0;
+        // operands of token j (key half, coefficients, delta entry); the next token's
+        // are loaded before the current one is applied, off the serial chain
+        struct Tok {
+            float k[16];
+            float4 c;
+            float d;
+        };
+        auto load = [&](int j, Tok &t) {
+#pragma unroll
+            for (int e = 0; e < 16; e += 4) {
+                const float4 f = *reinterpret_cast<const float4 *>(KfT + j * KS + 16 * gq + e);
+                t.k[e] = f.x; t.k[e + 1] = f.y; t.k[e + 2] = f.z; t.k[e + 3] = f.w;
+            }
+            t.c = SCT[j];
+            t.d = DLT[j * KS + grow];
+        };
+        auto fold = [&]() {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) gh[e] *= gam;
+            gam = 1.0f;
+            inv_gam = 1.0f;
+        };
+        // intra-chunk readout: u_j = gam (ghat . q_j) before token j's update, left
+        // in the token's delta slot (read by this row's two lanes only, both done)
+        auto read_u = [&](int j) {
+            const float4 *qp = reinterpret_cast<const float4 *>(Qf + j * KS + 16 * gq);
+            float p0 = 0.0f, p1 = 0.0f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float4 f = qp[e];
+                p0 = fmaf(gh[4 * e], f.x, p0);
+                p1 = fmaf(gh[4 * e + 1], f.y, p1);
+                p0 = fmaf(gh[4 * e + 2], f.z, p0);
+                p1 = fmaf(gh[4 * e + 3], f.w, p1);
+            }
+            float u = p0 + p1;
+            u += __shfl_xor_sync(0xffffffffu, u, 1);
+            __syncwarp();
+            if (gq == 0) DLT[j * KS + grow] = gam * u;
+        };
+        auto apply = [&](const Tok &t, bool chk, int j) {
+            if (intra) read_u(j);
+            float p4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) p4[e] = gh[e] * t.k[e];
+#pragma unroll
+            for (int e = 4; e < 16; ++e) p4[e & 3] = fmaf(gh[e], t.k[e], p4[e & 3]);
+            float dot = (p4[0] + p4[1]) + (p4[2] + p4[3]);
+            dot += __shfl_xor_sync(0xffffffffu, dot, 1);
+            if (no_dgd) dot = 0.0f;
+            if (!chk || t.c.z != 0.0f) {
+                const float sc = -t.c.y * fmaf(t.d, inv_gam, dot);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) gh[e] = fmaf(sc, t.k[e], gh[e]);
+                gam *= t.c.x;
+                inv_gam *= t.c.z;
+                if (chk && gam < 1e-20f) fold();
+            } else {  // G_j = alpha G_{j-1} - eta (G_{j-1} k + delta) k^T, unscaled
+                const float sc = -t.c.w * fmaf(gam, dot, t.d);
+                const float ag = t.c.x * gam;
+#pragma unroll
+                for (int e = 0; e < 16; ++e) gh[e] = fmaf(sc, t.k[e], ag * gh[e]);
+                gam = 1.0f;
+                inv_gam = 1.0f;
+            }
+        };
+        // rows Lt..TT-1 of the tiles hold stale values: a prefetch past the last token
+        // reads one and never applies it
+        if (careful) {
+            Tok ta, tb;
+            load(0, ta);
+            for (int j = 0; j < Lt; j += 2) {
+                load(min(j + 1, TT - 1), tb);
+                apply(ta, true, j);
+                if (j + 1 >= Lt) break;
+                load(min(j + 2, TT - 1), ta);
+                apply(tb, true, j + 1);
+            }
+        } else {
+            // blocks of NB tokens: with a = ghat_0 . k_j for the block's starting ghat,
+            //   ghat_{j-1} . k_j = a_j + sum_{i<j in block} sc_i (k_i . k_j),
+            // so the NB dot products are independent, the serial part is an NB-step
+            // scalar solve, and ghat takes one rank-NB update.
+            int j = 0;
+            for (; j + NB <= Lt; j += NB) {
+                float kb[NB][16];
+                float4 cb[NB];
+                float db[NB];
+#pragma unroll
+                for (int t = 0; t < NB; ++t) {
+#pragma unroll
+                    for (int e = 0; e < 16; e += 4) {
+                        const float4 f =
+                            *reinterpret_cast<const float4 *>(KfT + (j + t) * KS + 16 * gq + e);
+                        kb[t][e] = f.x; kb[t][e + 1] = f.y; kb[t][e + 2] = f.z; kb[t][e + 3] = f.w;
+                    }
+                    cb[t] = SCT[j + t];
+                    db[t] = DLT[(j + t) * KS + grow];
+                }
+                float4 g0 = *reinterpret_cast<const float4 *>(GTT + (j / NB) * 8);
+                float2 g1 = *reinterpret_cast<const float2 *>(GTT + (j / NB) * 8 + 4);
+                float av[NB];
+#pragma unroll
+                for (int t = 0; t < NB; ++t) {
+                    float p0 = gh[0] * kb[t][0], p1 = gh[1] * kb[t][1];
+#pragma unroll
+                    for (int e = 2; e < 16; e += 2) {
+                        p0 = fmaf(gh[e], kb[t][e], p0);
+                        p1 = fmaf(gh[e + 1], kb[t][e + 1], p1);
+                    }
+                    av[t] = p0 + p1;
+                }
+#pragma unroll
+                for (int t = 0; t < NB; ++t) av[t] += __shfl_xor_sync(0xffffffffu, av[t], 1);
+                // intra-chunk readout: ghat_0 . q_t for the block's tokens
+                float aq[NB];
+                if (intra) {
+#pragma unroll
+                    for (int t = 0; t < NB; ++t) {
+                        const float4 *qp = reinterpret_cast<const float4 *>(Qf + (j + t) * KS + 16 * gq);
+                        float p0 = 0.0f, p1 = 0.0f;
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float4 f = qp[e];
+                            p0 = fmaf(gh[4 * e], f.x, p0);
+                            p1 = fmaf(gh[4 * e + 1], f.y, p1);
+                            p0 = fmaf(gh[4 * e + 2], f.z, p0);
+                            p1 = fmaf(gh[4 * e + 3], f.w, p1);
+                        }
+                        aq[t] = p0 + p1;
+                    }
+#pragma unroll
+                    for (int t = 0; t < NB; ++t) aq[t] += __shfl_xor_sync(0xffffffffu, aq[t], 1);
+                }
+                if (no_dgd) {
+#pragma unroll
+                    for (int t = 0; t < NB; ++t) av[t] = 0.0f;
+                    g0 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                    g1 = make_float2(0.0f, 0.0f);
+                }
+                float iv = inv_gam;
+                const float s0 = -cb[0].y * fmaf(db[0], iv, av[0]);
+                iv *= cb[0].z;
+                const float s1 = -cb[1].y * (fmaf(db[1], iv, av[1]) + s0 * g0.x);
+                iv *= cb[1].z;
+                const float s2 = -cb[2].y * (fmaf(db[2], iv, av[2]) + fmaf(s1, g0.w, s0 * g0.y));
+                iv *= cb[2].z;
+                const float s3 =
+                    -cb[3].y * (fmaf(db[3], iv, av[3]) + fmaf(s2, g1.y, fmaf(s1, g1.x, s0 * g0.z)));
+                iv *= cb[3].z;
+                inv_gam = iv;
+                if (intra) {
+                    // ghat_{t-1} . q_t = ghat_0 . q_t + sum_{i<t} s_i (k_i . q_t), and
+                    // gam_{t-1} = gam_0 alpha_0 .. alpha_{t-1}
+                    const float4 c0 = *reinterpret_cast<const float4 *>(CQ + (j / NB) * 8);
+                    const float2 c1 = *reinterpret_cast<const float2 *>(CQ + (j / NB) * 8 + 4);
+                    float g = gam;
+                    const float u0 = g * aq[0];
+                    g *= cb[0].x;
+                    const float u1 = g * fmaf(s0, c0.x, aq[1]);
+                    g *= cb[1].x;
+                    const float u2 = g * fmaf(s1, c0.w, fmaf(s0, c0.y, aq[2]));
+                    g *= cb[2].x;
+                    const float u3 = g * fmaf(s2, c1.y, fmaf(s1, c1.x, fmaf(s0, c0.z, aq[3])));
+                    __syncwarp();
+                    if (gq == 0) {
+                        DLT[j * KS + grow] = u0;
+                        DLT[(j + 1) * KS + grow] = u1;
+                        DLT[(j + 2) * KS + grow] = u2;
+                        DLT[(j + 3) * KS + grow] = u3;
+                    }
+                }
+                gam *= (cb[0].x * cb[1].x) * (cb[2].x * cb[3].x);
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    gh[e] = fmaf(s3, kb[3][e],
+                                 fmaf(s2, kb[2][e], fmaf(s1, kb[1][e], fmaf(s0, kb[0][e], gh[e]))));
+                if (gam < 1e-20f) fold();
+            }
+            for (; j < Lt; ++j) {
+                Tok t;
+                load(j, t);
+                apply(t, false, j);
+            }
+            if (gam < 1e-20f) fold();
+        }
+        if (intra) {
+            __threadfence_block();
+            named_arrive(2, NT);  // u of every token of the sub-tile written
+        }
+        if (last) {
+            // G = gam * ghat: fp32 rows for the eta / alpha rows, and the update's B
+            // operand in three bf16 pieces (MN-major: this lane's 16 columns of its
+            // row are two 16-byte runs per piece).  When the chunk retains at least
+            // half of the state the operand is G - I: the MMA forms only the
+            // increment M_b (G - I), which the epilogue adds to M_b in fp32, so the
+            // tensor core's accumulation error is relative to the change.  Otherwise
+            // the state is mostly replaced and the MMA forms M_b G directly (no
+            // cancellation).
+            const bool use_delta = gam >= 0.5f;
+            float gv[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) gv[e] = gam * gh[e];
+            float4 *gd = reinterpret_cast<float4 *>(Gf + grow * GFS + 16 * gq);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                gd[e] = make_float4(gv[4 * e], gv[4 * e + 1], gv[4 * e + 2], gv[4 * e + 3]);
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                float v8[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    v8[i] = gv[8 * hh + i] - ((use_delta && 16 * gq + 8 * hh + i == grow) ? 1.0f : 0.0f);
+                store_split8(sG + (2 * gq + hh) * G_NSTR + (grow >> 3) * G_KSTR + (grow & 7) * 16,
+                             4 * G_NSTR, v8);
+            }
+            if ((tid & 63) == 0) *delta_form = use_delta ? 1 : 0;
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(mb_g);  // this warp's rows of G are written
+        }
+    };
+    // token pair, after the readout MMA: lambda_r y added at the token's pixel (Eq. (26))
+    auto add_readout = [&](int p, int Lidx, bool valid) {
+        float y[32];
+        tmem_ld32(tbase + lrow + COL_RO, y);
+        const int pix = rowr ? Lidx * W + p : p * W + Lidx;
+        if (valid && (!kAbl || ob) &&
+            VH_IN(a.stats, ((size_t)b * H * W + pix) * Cc + (size_t)h * D, D, map_elems(a))) {
+            float *dst = ob + (size_t)pix * Cc;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                float4 v4 = make_float4(y[4 * e], y[4 * e + 1], y[4 * e + 2], y[4 * e + 3]);
+                if (lam) {
+                    v4.x *= lam[4 * e]; v4.y *= lam[4 * e + 1];
+                    v4.z *= lam[4 * e + 2]; v4.w *= lam[4 * e + 3];
+                }
+                n_nf += !isfinite(v4.x) + !isfinite(v4.y) + !isfinite(v4.z) + !isfinite(v4.w);
+                red_add_v4(dst + 4 * e, v4);
+            }
+        }
+    };
+    // MMA 3 (chunk end, issuing thread): every d x d memory <- M_b G (Eq. (46)), issued as
+    // soon as the gain pair has written G's pieces.  The six cross terms go in as three MMAs
+    // per K step, one per piece of M_b against the pieces of G stacked along N:
+    //   cols [0,32): a1 b1 + a2 b1,  [32,64): a1 b2 + a2 b2,  [64,96): a1 b3 + a3 b1,
+    // summed by the epilogue.
+    auto issue_update = [&]() {
+        if (wt.wait(mb_g, ph_g) && !*abort_flag) {
+            tc_after();
+            const uint64_t da = sdesc(smem_u32(sS) + ROW_MEM / 8 * SBO_K32, LBO_K32, SBO_K32);
+            const uint64_t db = sdesc(smem_u32(sG), G_KSTR, G_NSTR);
+#pragma unroll
+            for (int ks = 0; ks < 2; ++ks) {
+                const uint32_t ka = ks * 2 * LBO_K32, kb = ks * 2 * G_KSTR;
+                mma(tbase + COL_UPD, dadd(da, ka), dadd(db, kb), idesc_bf16(128, 96, true),
+                    ks != 0);
+                mma(tbase + COL_UPD, dadd(da, S_PIECE + ka), dadd(db, kb),
+                    idesc_bf16(128, 64, true), 1);
+                mma(tbase + COL_UPD + 2 * D, dadd(da, 2 * S_PIECE + ka), dadd(db, kb),
+                    idesc_bf16(128, 32, true), 1);
+            }
+            mma_commit(mb_upd);
+        }
+    };
+    // chunk end, after the barrier that follows G: the eta / alpha rows and the new state
+    auto chunk_end = [&](int c) {
+        // the 1 x d eta and alpha rows on CUDA cores, in fp32 (lane = column); their
+        // operand rows are read by no pending MMA
+        if (warp == ew && !(kAbl && (a.control_flags & VH_CTRL_FREEZE_DYN))) {
+            float ne = 0.0f, na = 0.0f;
+#pragma unroll 8
+            for (int l = 0; l < D; ++l) {
+                const float gv = Gf[l * GFS + lane];
+                ne = fmaf(Sea[l], gv, ne);
+                na = fmaf(Sea[D + l], gv, na);
+            }
+            __syncwarp();
+            Sea[lane] = ne;
+            Sea[D + lane] = na;
+            if (kAbl && a.ckpt && ck_ok && c + 1 < nlines) {  // backward support
+                float *ck = a.ckpt + (size_t)blockIdx.x * a.ckpt_stride + (size_t)(c + 1) * SZ;
+                ck[4 * D * D + lane] = ne;
+                ck[4 * D * D + D + lane] = na;
+            }
+            __nv_bfloat16 p1, p2, p3;
+            const int g = lane >> 3, e = lane & 7;
+            split3(ne, p1, p2, p3);
+            unsigned char *d0 = sS + op_off(ROW_ETA, g) + 2 * e;
+            *reinterpret_cast<__nv_bfloat16 *>(d0) = p1;
+            *reinterpret_cast<__nv_bfloat16 *>(d0 + S_PIECE) = p2;
+            *reinterpret_cast<__nv_bfloat16 *>(d0 + 2 * S_PIECE) = p3;
+            split3(na, p1, p2, p3);
+            unsigned char *d1 = sS + op_off(ROW_ETA + 1, g) + 2 * e;
+            *reinterpret_cast<__nv_bfloat16 *>(d1) = p1;
+            *reinterpret_cast<__nv_bfloat16 *>(d1 + S_PIECE) = p2;
+            *reinterpret_cast<__nv_bfloat16 *>(d1 + 2 * S_PIECE) = p3;
+        }
+        wt.wait(mb_upd, ph_upd);
+        ph_upd ^= 1;
+        tc_after();
+        // new state rows: thread = memory row (TMEM lane), the three column blocks
+        // summed, re-split into the operand pieces.  In the increment form M_b is
+        // recovered exactly from its three pieces (their sum rounds back to the fp32
+        // value they were cut from) and added in fp32.
+        float v[32], w[32];
+        tmem_ld32(tbase + lrow + COL_UPD, v);
+        tmem_ld32(tbase + lrow + COL_UPD + D, w);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] += w[e];
+        tmem_ld32(tbase + lrow + COL_UPD + 2 * D, w);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] += w[e];
+        // a memory held fixed by an ablation switch keeps M_b (recovered from its
+        // pieces for memories_out) and its operand rows are not rewritten
+        const bool frz = frozen_row<kAbl>(a, tid, D);
+        if (frz) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = 0.0f;
+        }
+        const bool add_mb = frz || *delta_form != 0;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            unsigned char *src = sS + op_off(ROW_MEM + tid, g);
+            if (add_mb) {
+                const uint4 u1 = *reinterpret_cast<const uint4 *>(src);
+                const uint4 u2 = *reinterpret_cast<const uint4 *>(src + S_PIECE);
+                const uint4 u3 = *reinterpret_cast<const uint4 *>(src + 2 * S_PIECE);
+                const uint32_t *w1 = &u1.x, *w2 = &u2.x, *w3 = &u3.x;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    v[8 * g + 2 * i] += (bf16_lo(w1[i]) + bf16_lo(w2[i])) + bf16_lo(w3[i]);
+                    v[8 * g + 2 * i + 1] += (bf16_hi(w1[i]) + bf16_hi(w2[i])) + bf16_hi(w3[i]);
+                }
+            }
+            if (!frz) store_split8(src, S_PIECE, v + 8 * g);
+        }
+        if (kAbl && a.ckpt && ck_ok && c + 1 < nlines) {  // boundary state of the next chunk
+            float4 *d4 = reinterpret_cast<float4 *>(a.ckpt + (size_t)blockIdx.x * a.ckpt_stride +
+                                                    (size_t)(c + 1) * SZ + (size_t)tid * D);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                d4[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+        }
+        if (c == nlines - 1 && a.mem_out && mo_ok) {
+            float *mo = a.mem_out + (((size_t)b * 4 + r) * a.nh + h) * SZ;
+            float4 *d4 = reinterpret_cast<float4 *>(mo + (size_t)tid * D);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                d4[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+        }
+    };
+
+    if constexpr (kPipe) {
+    // ================= pipelined sub-tiles (lines longer than one sub-tile).  Step k of a
+    // chunk: the token pair reads out sub-tile k - 1 (its queries are still in TMEM), then
+    // generates sub-tile k and runs its per-token step and Gram entries into tile set k % 2;
+    // meanwhile the gain pair runs the gates and the shared gain of sub-tile k - 1 from set
+    // (k - 1) % 2.  One barrier per step; the chunk end follows step nsub.
+    static_assert(!kAbl && !kWY, "pipelined form: the method as defined, recurrence gain");
+    float *const Kf2 = reinterpret_cast<float *>(sm + OFF_KF2);
+    float *const DL2 = reinterpret_cast<float *>(sm + OFF_DL2);
+    float4 *const SC2 = reinterpret_cast<float4 *>(sm + OFF_SC2);
+    float *const GT2 = reinterpret_cast<float *>(sm + OFF_GT2);
+    for (int c = 0; c < nlines; ++c) {
+        const int Lidx = line_of(c);
+        for (int k = 0; k <= nsub; ++k) {
+            if (!gainw) {
+                if (k >= 1) {
+                    const int sr = k - 1;
+                    const int p = box_start(sr) + jq;
+                    const bool valid =
+                        p >= 0 && p < Lline && VH_IN(a.stats, (rev ? Lline - 1 - p : p) - sr * TT, 1, TT);
+                    // queries: q = normalize(M^q_b x), split into the readout's A operand
+                    float qr[32];
+                    tmem_ld32(tbase + lrow + COL_GEN + COL_QR, qr);
+                    const float rq = __frsqrt_rn(sumsq32(qr) + a.knorm_eps);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) qr[e] *= rq;
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) store_split8(sQ + op_off(jq, g), Q_PIECE, qr + 8 * g);
+                    fence_async_smem();
+                    tc_before();
+                    named_sync(1, 64);
+                    tc_after();
+                    // MMA 2: readout y = q M^m_b^T, Eq. (16)
+                    if (issuer && !*abort_flag) {
+                        mma_split6<Q_PIECE, S_PIECE>(tbase + COL_RO, smem_u32(sQ) - (rw >> 1) * 8 * SBO_K32,
+                                                     smem_u32(sS) + (ROW_MEM + 3 * D) / 8 * SBO_K32,
+                                                     idesc_bf16(128, 32));
+                        mma_commit(mb_ro);
+                    }
+                    wt.wait(mb_ro, ph_ro);
+                    ph_ro ^= 1;
+                    tc_after();
+                    add_readout(p, Lidx, valid);
+                    // the gain pair finishes the chunk's last sub-tile in this step
+                    if (k == nsub && issuer) issue_update();
+                }
+                if (k < nsub) {
+                    tc_before();
+                    named_sync(1, 64);  // both warps' TMEM reads above done
+                    tc_after();
+                    const int p = box_start(k) + jq;
+                    const int jr = (rev ? Lline - 1 - p : p) - k * TT;
+                    const bool valid = p >= 0 && p < Lline && VH_IN(a.stats, jr, 1, TT);
+                    const bool t2 = (k & 1) != 0;
+                    generate(c, k);
+                    token_step(t2 ? Kf2 : Kf, t2 ? DL2 : DLf, t2 ? SC2 : SC, valid, jr, c, k * TT);
+                    named_sync(1, 64);  // every token's key row written
+                    gram_step(t2 ? Kf2 : Kf, t2 ? GT2 : GT);
+                }
+            } else if (k >= 1) {
+                const int sg = k - 1;
+                const bool t2 = (sg & 1) != 0;
+                const int Lt = min(TT, Lline - sg * TT);
+                gate_step(t2 ? SC2 : SC, Lt);
+                named_sync(3, 64);  // both warps' coefficients and votes written
+                gain_step(t2 ? Kf2 : Kf, t2 ? DL2 : DLf, t2 ? SC2 : SC, t2 ? GT2 : GT, Lt, sg == 0, k == nsub);
+            }
+            tc_before();
+            __syncthreads();  // end of step k: tile set (k - 1) % 2 free again
+            tc_after();
+        }
+        ph_g ^= 1;
+        chunk_end(c);
+        fence_async_smem();
+        tc_before();
+        __syncthreads();  // end of chunk: operands rewritten, TMEM consumed
+    }
+    } else {
     for (int c = 0; c < nlines; ++c) {
         const int Lidx = line_of(c);
         for (int s = 0; s < nsub; ++s) {
@@ -476,36 +1105,7 @@ __global__ void __launch_bounds__(NT, 3)
             const int p = box_start(s) + jq;   // position along the line (token pair)
             const int jr = (rev ? Lline - 1 - p : p) - t0;  // route-ordered index in the sub-tile
             const bool valid = !gainw && p >= 0 && p < Lline && VH_IN(a.stats, jr, 1, TT);
-            // ---- MMA 1: generation from the boundary state, Eq. (15):
-            //   [s_eta s_alpha 0.. | k_raw | v | q_raw] = x (s1 + s2 + s3)^T
-            // one M = 128, N = 112 MMA per piece and K step (x is exact in bf16).  The x
-            // tile is A rows 32 rw..32 rw+63; the other 64 A rows read the kilobyte next to
-            // the tile into TMEM lanes nobody reads.
-            if (issuer) {
-                tc_after();
-                if (wait_copy(mb_x, ph_x, nx_obs) && !*abort_flag) {
-                    const uint64_t dq = sdesc(smem_u32(sX) - (rw >> 1) * LBO_X, LBO_X, SBO_X);
-                    const uint64_t ds = sdesc(smem_u32(sS), LBO_K32, SBO_K32);
-#pragma unroll
-                    for (int pc = 0; pc < 3; ++pc)
-#pragma unroll
-                        for (int ks = 0; ks < 2; ++ks)
-                            mma(tbase + COL_GEN, dadd(dq, ks * 2 * LBO_X),
-                                dadd(ds, pc * S_PIECE + ks * 2 * LBO_K32), idesc_bf16(128, 112),
-                                (pc | ks) != 0);
-                    mma_commit(mb_gen);
-                }
-            }
-            ph_x ^= 1;
-            wt.wait(mb_gen, ph_gen);
-            ph_gen ^= 1;
-            tc_after();
-            // the x tile is free again: fetch the next sub-tile while this one is processed
-            if (issuer && !*abort_flag) {
-                const int ns = (s + 1 < nsub) ? s + 1 : 0;
-                const int nc = (s + 1 < nsub) ? c : c + 1;
-                if (nc < nlines) issue_x(nc, ns);
-            }
+            generate(c, s);
             if constexpr (kWY) {
             // ================= WY form of the shared gain (one sub-tile per chunk) =========
             float *cpk = reinterpret_cast<float *>(sm + Lay<true>::CP);
@@ -800,375 +1400,17 @@ __global__ void __launch_bounds__(NT, 3)
             // normalises k, forms delta = k - v and their squared norms, and publishes the
             // token's scalars; then the gain pair (lane = route-ordered token) evaluates the
             // gates and the step control while the token pair forms the Gram entries.
-            if (!gainw) {
-                float kr[32], vv[32];
-                float se, sa;
-                tmem_ld_kvs(tbase + lrow + COL_GEN, kr, vv, se, sa);
-                const float kkr = sumsq32(kr);
-                const float rk = __frsqrt_rn(kkr + a.knorm_eps);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    kr[e] *= rk;            // k
-                    vv[e] = kr[e] - vv[e];  // delta = k - v
-                }
-                const float kn2 = sumsq32(kr), dd2 = sumsq32(vv);
-                if (valid) {
-                    float4 *kd = reinterpret_cast<float4 *>(Kf + jr * KS);
-                    float4 *dd4 = reinterpret_cast<float4 *>(DLf + jr * KS);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        kd[e] = make_float4(kr[4 * e], kr[4 * e + 1], kr[4 * e + 2], kr[4 * e + 3]);
-                        dd4[e] = make_float4(vv[4 * e], vv[4 * e + 1], vv[4 * e + 2], vv[4 * e + 3]);
-                    }
-                    SC[jr] = make_float4(se, sa, kn2, dd2);
-                    if (kAbl && a.rec && rec_ok) {  // token record scalars (backward support); the
-                                          // vectors follow while the gain runs
-                        float4 *rd = reinterpret_cast<float4 *>(rec_at(a, c * Lline + t0 + jr));
-                        rd[3 * D / 4] = make_float4(kkr, se, sa, kn2);
-                        rd[3 * D / 4 + 1].x = dd2;
-                    }
-                }
-                if (intra) {
-                    // the normalised query for the gain pair, route order (fp32)
-                    float qv[32];
-                    if (!exact) {
-                        tmem_ld32(tbase + lrow + COL_GEN + COL_QR, qv);
-                        const float rq = __frsqrt_rn(sumsq32(qv) + a.knorm_eps);
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) qv[e] *= rq;
-                    } else {
-                        // the outer query's three pieces from its TMA tile
-                        wait_copy(mb_q, ph_q, nq_obs);  // (the drain reads the issuer's count)
-#pragma unroll
-                        for (int g = 0; g < 4; ++g) {
-                            const unsigned char *src = sQ + g * QX_LBO + jq * 16;
-                            const uint4 u1 = *reinterpret_cast<const uint4 *>(src);
-                            const uint4 u2 = *reinterpret_cast<const uint4 *>(src + QX_PIECE);
-                            const uint4 u3 = *reinterpret_cast<const uint4 *>(src + 2 * QX_PIECE);
-                            const uint32_t *w1 = &u1.x, *w2 = &u2.x, *w3 = &u3.x;
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                qv[8 * g + 2 * i] = bf16_lo(w1[i]) + (bf16_lo(w2[i]) + bf16_lo(w3[i]));
-                                qv[8 * g + 2 * i + 1] = bf16_hi(w1[i]) + (bf16_hi(w2[i]) + bf16_hi(w3[i]));
-                            }
-                        }
-                    }
-                    if (valid) {
-                        float4 *qd = reinterpret_cast<float4 *>(Qf + jr * KS);
-#pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            qd[e] = make_float4(qv[4 * e], qv[4 * e + 1], qv[4 * e + 2], qv[4 * e + 3]);
-                    }
-                }
-            }
+            if (!gainw) token_step(Kf, DLf, SC, valid, jr, c, t0);
             __syncthreads();
-            if (gainw) {
-                // gates and step control of route-ordered token jg; the coefficients of the
-                // gain recurrence replace the scalars: (alpha, eta/alpha, 1/alpha, eta) for the
-                // scaled form, (alpha, 0, 0, eta) where alpha is too small to divide by
-                const int jg = tid & 63;
-                const bool tv = jg < Lt;
-                float alpha = 1.0f;
-                if (tv) {
-                    const float4 sc = SC[jg];
-                    float eta, oma;
-                    gates(a, sc.x, sc.y, eta, alpha, oma);
-                    float eta_t;
-                    if (a.gate_mode == VH_GATE_FORCED_EXEC) {
-                        eta_t = a.forced_eta;
-                    } else {
-                        const StepOut so = step_control<kAbl>(a, eta, alpha, oma, sc.z, sc.w);
-                        eta_t = so.eta_tilde;
-                        n_spec += so.spec_active;
-                        n_inj += so.inj_ratio_gt1;
-                    }
-                    const bool keep = alpha >= 1e-6f;
-                    SC[jg] = make_float4(alpha, keep ? __fdividef(eta_t, alpha) : 0.0f,
-                                         keep ? __frcp_rn(alpha) : 0.0f, eta_t);
-                }
-                // tokens whose retention could underflow the scaled gain within a few steps
-                const unsigned small = __ballot_sync(0xffffffffu, tv && !(alpha >= 0.01f));
-                if (lane == 0) vote[warp - 2 * gp] = small != 0u;
-            } else {
-                // Gram entries k_a . k_b of each block of NB route-ordered tokens.  This
-                // warp's tokens are the 32 consecutive route rows from R0 (route order runs
-                // with the box rows forwards, against them backwards), eight whole blocks:
-                // pair i of block q goes to lane 6q + i (mod 32).
-                const int R0 = rev ? TT - 32 - 32 * (warp - rw) : 32 * (warp - rw);
-#pragma unroll
-                for (int pr = lane; pr < 48; pr += 32) {
-                    const int q = pr / 6, pi = pr - 6 * q;
-                    const int ia = pi < 3 ? 0 : (pi < 5 ? 1 : 2);
-                    const int ib = pi < 3 ? pi + 1 : (pi < 5 ? pi - 1 : 3);
-                    const float4 *ka = reinterpret_cast<const float4 *>(Kf + (R0 + NB * q + ia) * KS);
-                    const float4 *kb = reinterpret_cast<const float4 *>(Kf + (R0 + NB * q + ib) * KS);
-                    float g4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const float4 fa = ka[e], fb = kb[e];
-                        g4[0] = fmaf(fa.x, fb.x, g4[0]);
-                        g4[1] = fmaf(fa.y, fb.y, g4[1]);
-                        g4[2] = fmaf(fa.z, fb.z, g4[2]);
-                        g4[3] = fmaf(fa.w, fb.w, g4[3]);
-                    }
-                    GT[(R0 / NB + q) * 8 + pi] = (g4[0] + g4[1]) + (g4[2] + g4[3]);
-                    if (intra) {  // and k_a . q_b for the intra-chunk readout
-                        const float4 *qb = reinterpret_cast<const float4 *>(Qf + (R0 + NB * q + ib) * KS);
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) g4[e] = 0.0f;
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const float4 fa = ka[e], fb = qb[e];
-                            g4[0] = fmaf(fa.x, fb.x, g4[0]);
-                            g4[1] = fmaf(fa.y, fb.y, g4[1]);
-                            g4[2] = fmaf(fa.z, fb.z, g4[2]);
-                            g4[3] = fmaf(fa.w, fb.w, g4[3]);
-                        }
-                        CQ[(R0 / NB + q) * 8 + pi] = (g4[0] + g4[1]) + (g4[2] + g4[3]);
-                    }
-                }
-            }
+            if (gainw)
+                gate_step(SC, Lt);
+            else
+                gram_step(Kf, GT);
             tc_before();
             __syncthreads();
             tc_after();
             if (gainw) {
-                // ---- shared gain over this sub-tile's tokens, in route order, on the gain
-                // pair: its thread t owns row t/2 of G and columns 16(t%2)..16(t%2)+15 (one
-                // shuffle per token).  G = gam * ghat with
-                //   ghat <- ghat - (eta/alpha) (ghat k + delta / gam) k^T,  gam <- alpha gam,
-                // a pure scaling of G_j = alpha G_{j-1} - eta (G_{j-1} k + delta) k^T.  When
-                // every alpha of the sub-tile is >= 0.01 the scale is folded back every eight
-                // tokens (it cannot underflow sooner); otherwise every token is checked, and a
-                // token with alpha < 1e-6 is applied to G directly with the scale folded in.
-                const int grow = (tid & 63) >> 1, gq = tid & 1;
-                if (s == 0) {
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) gh[e] = (16 * gq + e == grow) ? 1.0f : 0.0f;
-                    gam = 1.0f;
-                    inv_gam = 1.0f;
-                }
-                const bool careful = (vote[0] | vote[1]) != 0;
-                // operands of token j (key half, coefficients, delta entry); the next token's
-                // are loaded before the current one is applied, off the serial chain
-                struct Tok {
-                    float k[16];
-                    float4 c;
-                    float d;
-                };
-                auto load = [&](int j, Tok &t) {
-#pragma unroll
-                    for (int e = 0; e < 16; e += 4) {
-                        const float4 f = *reinterpret_cast<const float4 *>(Kf + j * KS + 16 * gq + e);
-                        t.k[e] = f.x; t.k[e + 1] = f.y; t.k[e + 2] = f.z; t.k[e + 3] = f.w;
-                    }
-                    t.c = SC[j];
-                    t.d = DLf[j * KS + grow];
-                };
-                auto fold = [&]() {
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) gh[e] *= gam;
-                    gam = 1.0f;
-                    inv_gam = 1.0f;
-                };
-                // intra-chunk readout: u_j = gam (ghat . q_j) before token j's update, left
-                // in the token's delta slot (read by this row's two lanes only, both done)
-                auto read_u = [&](int j) {
-                    const float4 *qp = reinterpret_cast<const float4 *>(Qf + j * KS + 16 * gq);
-                    float p0 = 0.0f, p1 = 0.0f;
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float4 f = qp[e];
-                        p0 = fmaf(gh[4 * e], f.x, p0);
-                        p1 = fmaf(gh[4 * e + 1], f.y, p1);
-                        p0 = fmaf(gh[4 * e + 2], f.z, p0);
-                        p1 = fmaf(gh[4 * e + 3], f.w, p1);
-                    }
-                    float u = p0 + p1;
-                    u += __shfl_xor_sync(0xffffffffu, u, 1);
-                    __syncwarp();
-                    if (gq == 0) DLf[j * KS + grow] = gam * u;
-                };
-                auto apply = [&](const Tok &t, bool chk, int j) {
-                    if (intra) read_u(j);
-                    float p4[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) p4[e] = gh[e] * t.k[e];
-#pragma unroll
-                    for (int e = 4; e < 16; ++e) p4[e & 3] = fmaf(gh[e], t.k[e], p4[e & 3]);
-                    float dot = (p4[0] + p4[1]) + (p4[2] + p4[3]);
-                    dot += __shfl_xor_sync(0xffffffffu, dot, 1);
-                    if (no_dgd) dot = 0.0f;
-                    if (!chk || t.c.z != 0.0f) {
-                        const float sc = -t.c.y * fmaf(t.d, inv_gam, dot);
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) gh[e] = fmaf(sc, t.k[e], gh[e]);
-                        gam *= t.c.x;
-                        inv_gam *= t.c.z;
-                        if (chk && gam < 1e-20f) fold();
-                    } else {  // G_j = alpha G_{j-1} - eta (G_{j-1} k + delta) k^T, unscaled
-                        const float sc = -t.c.w * fmaf(gam, dot, t.d);
-                        const float ag = t.c.x * gam;
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) gh[e] = fmaf(sc, t.k[e], ag * gh[e]);
-                        gam = 1.0f;
-                        inv_gam = 1.0f;
-                    }
-                };
-                // rows Lt..TT-1 of the tiles hold stale values: a prefetch past the last token
-                // reads one and never applies it
-                if (careful) {
-                    Tok ta, tb;
-                    load(0, ta);
-                    for (int j = 0; j < Lt; j += 2) {
-                        load(min(j + 1, TT - 1), tb);
-                        apply(ta, true, j);
-                        if (j + 1 >= Lt) break;
-                        load(min(j + 2, TT - 1), ta);
-                        apply(tb, true, j + 1);
-                    }
-                } else {
-                    // blocks of NB tokens: with a = ghat_0 . k_j for the block's starting ghat,
-                    //   ghat_{j-1} . k_j = a_j + sum_{i<j in block} sc_i (k_i . k_j),
-                    // so the NB dot products are independent, the serial part is an NB-step
-                    // scalar solve, and ghat takes one rank-NB update.
-                    int j = 0;
-                    for (; j + NB <= Lt; j += NB) {
-                        float kb[NB][16];
-                        float4 cb[NB];
-                        float db[NB];
-#pragma unroll
-                        for (int t = 0; t < NB; ++t) {
-#pragma unroll
-                            for (int e = 0; e < 16; e += 4) {
-                                const float4 f =
-                                    *reinterpret_cast<const float4 *>(Kf + (j + t) * KS + 16 * gq + e);
-                                kb[t][e] = f.x; kb[t][e + 1] = f.y; kb[t][e + 2] = f.z; kb[t][e + 3] = f.w;
-                            }
-                            cb[t] = SC[j + t];
-                            db[t] = DLf[(j + t) * KS + grow];
-                        }
-                        float4 g0 = *reinterpret_cast<const float4 *>(GT + (j / NB) * 8);
-                        float2 g1 = *reinterpret_cast<const float2 *>(GT + (j / NB) * 8 + 4);
-                        float av[NB];
-#pragma unroll
-                        for (int t = 0; t < NB; ++t) {
-                            float p0 = gh[0] * kb[t][0], p1 = gh[1] * kb[t][1];
-#pragma unroll
-                            for (int e = 2; e < 16; e += 2) {
-                                p0 = fmaf(gh[e], kb[t][e], p0);
-                                p1 = fmaf(gh[e + 1], kb[t][e + 1], p1);
-                            }
-                            av[t] = p0 + p1;
-                        }
-#pragma unroll
-                        for (int t = 0; t < NB; ++t) av[t] += __shfl_xor_sync(0xffffffffu, av[t], 1);
-                        // intra-chunk readout: ghat_0 . q_t for the block's tokens
-                        float aq[NB];
-                        if (intra) {
-#pragma unroll
-                            for (int t = 0; t < NB; ++t) {
-                                const float4 *qp = reinterpret_cast<const float4 *>(Qf + (j + t) * KS + 16 * gq);
-                                float p0 = 0.0f, p1 = 0.0f;
-#pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    const float4 f = qp[e];
-                                    p0 = fmaf(gh[4 * e], f.x, p0);
-                                    p1 = fmaf(gh[4 * e + 1], f.y, p1);
-                                    p0 = fmaf(gh[4 * e + 2], f.z, p0);
-                                    p1 = fmaf(gh[4 * e + 3], f.w, p1);
-                                }
-                                aq[t] = p0 + p1;
-                            }
-#pragma unroll
-                            for (int t = 0; t < NB; ++t) aq[t] += __shfl_xor_sync(0xffffffffu, aq[t], 1);
-                        }
-                        if (no_dgd) {
-#pragma unroll
-                            for (int t = 0; t < NB; ++t) av[t] = 0.0f;
-                            g0 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-                            g1 = make_float2(0.0f, 0.0f);
-                        }
-                        float iv = inv_gam;
-                        const float s0 = -cb[0].y * fmaf(db[0], iv, av[0]);
-                        iv *= cb[0].z;
-                        const float s1 = -cb[1].y * (fmaf(db[1], iv, av[1]) + s0 * g0.x);
-                        iv *= cb[1].z;
-                        const float s2 = -cb[2].y * (fmaf(db[2], iv, av[2]) + fmaf(s1, g0.w, s0 * g0.y));
-                        iv *= cb[2].z;
-                        const float s3 =
-                            -cb[3].y * (fmaf(db[3], iv, av[3]) + fmaf(s2, g1.y, fmaf(s1, g1.x, s0 * g0.z)));
-                        iv *= cb[3].z;
-                        inv_gam = iv;
-                        if (intra) {
-                            // ghat_{t-1} . q_t = ghat_0 . q_t + sum_{i<t} s_i (k_i . q_t), and
-                            // gam_{t-1} = gam_0 alpha_0 .. alpha_{t-1}
-                            const float4 c0 = *reinterpret_cast<const float4 *>(CQ + (j / NB) * 8);
-                            const float2 c1 = *reinterpret_cast<const float2 *>(CQ + (j / NB) * 8 + 4);
-                            float g = gam;
-                            const float u0 = g * aq[0];
-                            g *= cb[0].x;
-                            const float u1 = g * fmaf(s0, c0.x, aq[1]);
-                            g *= cb[1].x;
-                            const float u2 = g * fmaf(s1, c0.w, fmaf(s0, c0.y, aq[2]));
-                            g *= cb[2].x;
-                            const float u3 = g * fmaf(s2, c1.y, fmaf(s1, c1.x, fmaf(s0, c0.z, aq[3])));
-                            __syncwarp();
-                            if (gq == 0) {
-                                DLf[j * KS + grow] = u0;
-                                DLf[(j + 1) * KS + grow] = u1;
-                                DLf[(j + 2) * KS + grow] = u2;
-                                DLf[(j + 3) * KS + grow] = u3;
-                            }
-                        }
-                        gam *= (cb[0].x * cb[1].x) * (cb[2].x * cb[3].x);
-#pragma unroll
-                        for (int e = 0; e < 16; ++e)
-                            gh[e] = fmaf(s3, kb[3][e],
-                                         fmaf(s2, kb[2][e], fmaf(s1, kb[1][e], fmaf(s0, kb[0][e], gh[e]))));
-                        if (gam < 1e-20f) fold();
-                    }
-                    for (; j < Lt; ++j) {
-                        Tok t;
-                        load(j, t);
-                        apply(t, false, j);
-                    }
-                    if (gam < 1e-20f) fold();
-                }
-                if (intra) {
-                    __threadfence_block();
-                    named_arrive(2, NT);  // u of every token of the sub-tile written
-                }
-                if (last) {
-                    // G = gam * ghat: fp32 rows for the eta / alpha rows, and the update's B
-                    // operand in three bf16 pieces (MN-major: this lane's 16 columns of its
-                    // row are two 16-byte runs per piece).  When the chunk retains at least
-                    // half of the state the operand is G - I: the MMA forms only the
-                    // increment M_b (G - I), which the epilogue adds to M_b in fp32, so the
-                    // tensor core's accumulation error is relative to the change.  Otherwise
-                    // the state is mostly replaced and the MMA forms M_b G directly (no
-                    // cancellation).
-                    const bool use_delta = gam >= 0.5f;
-                    float gv[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) gv[e] = gam * gh[e];
-                    float4 *gd = reinterpret_cast<float4 *>(Gf + grow * GFS + 16 * gq);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        gd[e] = make_float4(gv[4 * e], gv[4 * e + 1], gv[4 * e + 2], gv[4 * e + 3]);
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        float v8[8];
-#pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            v8[i] = gv[8 * hh + i] - ((use_delta && 16 * gq + 8 * hh + i == grow) ? 1.0f : 0.0f);
-                        store_split8(sG + (2 * gq + hh) * G_NSTR + (grow >> 3) * G_KSTR + (grow & 7) * 16,
-                                     4 * G_NSTR, v8);
-                    }
-                    if ((tid & 63) == 0) *delta_form = use_delta ? 1 : 0;
-                    fence_async_smem();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(mb_g);  // this warp's rows of G are written
-                }
+                gain_step(Kf, DLf, SC, GT, Lt, s == 0, last);
             } else {
                 // ---- the token pair, while the gain runs: queries and the readout of this
                 // sub-tile.  For the intra-chunk readout it waits for the gain pair's u_t
@@ -1249,47 +1491,8 @@ __global__ void __launch_bounds__(NT, 3)
                     const int nc = (s + 1 < nsub) ? c : c + 1;
                     if (nc < nlines) issue_q(nc, ns);
                 }
-                // readout epilogue: lambda_r y added at the token's pixel (Eq. (26))
-                float y[32];
-                tmem_ld32(tbase + lrow + COL_RO, y);
-                const int pix = rowr ? Lidx * W + p : p * W + Lidx;
-                if (valid && (!kAbl || ob) &&
-                    VH_IN(a.stats, ((size_t)b * H * W + pix) * Cc + (size_t)h * D, D, map_elems(a))) {
-                    float *dst = ob + (size_t)pix * Cc;
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        float4 v4 = make_float4(y[4 * e], y[4 * e + 1], y[4 * e + 2], y[4 * e + 3]);
-                        if (lam) {
-                            v4.x *= lam[4 * e]; v4.y *= lam[4 * e + 1];
-                            v4.z *= lam[4 * e + 2]; v4.w *= lam[4 * e + 3];
-                        }
-                        n_nf += !isfinite(v4.x) + !isfinite(v4.y) + !isfinite(v4.z) + !isfinite(v4.w);
-                        red_add_v4(dst + 4 * e, v4);
-                    }
-                }
-                // ---- MMA 3 (chunk end): every d x d memory <- M_b G (Eq. (46)), issued as soon
-                // as the gain pair has written G's pieces.  The six cross terms go in as three
-                // MMAs per K step, one per piece of M_b against the pieces of G stacked along N:
-                //   cols [0,32): a1 b1 + a2 b1,  [32,64): a1 b2 + a2 b2,  [64,96): a1 b3 + a3 b1,
-                // summed by the epilogue.
-                if (last && issuer) {
-                    if (wt.wait(mb_g, ph_g) && !*abort_flag) {
-                        tc_after();
-                        const uint64_t da = sdesc(smem_u32(sS) + ROW_MEM / 8 * SBO_K32, LBO_K32, SBO_K32);
-                        const uint64_t db = sdesc(smem_u32(sG), G_KSTR, G_NSTR);
-#pragma unroll
-                        for (int ks = 0; ks < 2; ++ks) {
-                            const uint32_t ka = ks * 2 * LBO_K32, kb = ks * 2 * G_KSTR;
-                            mma(tbase + COL_UPD, dadd(da, ka), dadd(db, kb), idesc_bf16(128, 96, true),
-                                ks != 0);
-                            mma(tbase + COL_UPD, dadd(da, S_PIECE + ka), dadd(db, kb),
-                                idesc_bf16(128, 64, true), 1);
-                            mma(tbase + COL_UPD + 2 * D, dadd(da, 2 * S_PIECE + ka), dadd(db, kb),
-                                idesc_bf16(128, 32, true), 1);
-                        }
-                        mma_commit(mb_upd);
-                    }
-                }
+                add_readout(p, Lidx, valid);
+                if (last && issuer) issue_update();
             }
             }  // recurrence form
             ph_ro ^= 1;
@@ -1298,96 +1501,15 @@ __global__ void __launch_bounds__(NT, 3)
                 tc_before();
                 __syncthreads();  // G and its fp32 rows written, readout complete
                 tc_after();
-                // the 1 x d eta and alpha rows on CUDA cores, in fp32 (lane = column); their
-                // operand rows are read by no pending MMA
-                if (warp == ew && !(kAbl && (a.control_flags & VH_CTRL_FREEZE_DYN))) {
-                    float ne = 0.0f, na = 0.0f;
-#pragma unroll 8
-                    for (int l = 0; l < D; ++l) {
-                        const float gv = Gf[l * GFS + lane];
-                        ne = fmaf(Sea[l], gv, ne);
-                        na = fmaf(Sea[D + l], gv, na);
-                    }
-                    __syncwarp();
-                    Sea[lane] = ne;
-                    Sea[D + lane] = na;
-                    if (kAbl && a.ckpt && ck_ok && c + 1 < nlines) {  // backward support
-                        float *ck = a.ckpt + (size_t)blockIdx.x * a.ckpt_stride + (size_t)(c + 1) * SZ;
-                        ck[4 * D * D + lane] = ne;
-                        ck[4 * D * D + D + lane] = na;
-                    }
-                    __nv_bfloat16 p1, p2, p3;
-                    const int g = lane >> 3, e = lane & 7;
-                    split3(ne, p1, p2, p3);
-                    unsigned char *d0 = sS + op_off(ROW_ETA, g) + 2 * e;
-                    *reinterpret_cast<__nv_bfloat16 *>(d0) = p1;
-                    *reinterpret_cast<__nv_bfloat16 *>(d0 + S_PIECE) = p2;
-                    *reinterpret_cast<__nv_bfloat16 *>(d0 + 2 * S_PIECE) = p3;
-                    split3(na, p1, p2, p3);
-                    unsigned char *d1 = sS + op_off(ROW_ETA + 1, g) + 2 * e;
-                    *reinterpret_cast<__nv_bfloat16 *>(d1) = p1;
-                    *reinterpret_cast<__nv_bfloat16 *>(d1 + S_PIECE) = p2;
-                    *reinterpret_cast<__nv_bfloat16 *>(d1 + 2 * S_PIECE) = p3;
-                }
-                wt.wait(mb_upd, ph_upd);
-                ph_upd ^= 1;
-                tc_after();
-                // new state rows: thread = memory row (TMEM lane), the three column blocks
-                // summed, re-split into the operand pieces.  In the increment form M_b is
-                // recovered exactly from its three pieces (their sum rounds back to the fp32
-                // value they were cut from) and added in fp32.
-                float v[32], w[32];
-                tmem_ld32(tbase + lrow + COL_UPD, v);
-                tmem_ld32(tbase + lrow + COL_UPD + D, w);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) v[e] += w[e];
-                tmem_ld32(tbase + lrow + COL_UPD + 2 * D, w);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) v[e] += w[e];
-                // a memory held fixed by an ablation switch keeps M_b (recovered from its
-                // pieces for memories_out) and its operand rows are not rewritten
-                const bool frz = frozen_row<kAbl>(a, tid, D);
-                if (frz) {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) v[e] = 0.0f;
-                }
-                const bool add_mb = frz || *delta_form != 0;
-#pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    unsigned char *src = sS + op_off(ROW_MEM + tid, g);
-                    if (add_mb) {
-                        const uint4 u1 = *reinterpret_cast<const uint4 *>(src);
-                        const uint4 u2 = *reinterpret_cast<const uint4 *>(src + S_PIECE);
-                        const uint4 u3 = *reinterpret_cast<const uint4 *>(src + 2 * S_PIECE);
-                        const uint32_t *w1 = &u1.x, *w2 = &u2.x, *w3 = &u3.x;
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            v[8 * g + 2 * i] += (bf16_lo(w1[i]) + bf16_lo(w2[i])) + bf16_lo(w3[i]);
-                            v[8 * g + 2 * i + 1] += (bf16_hi(w1[i]) + bf16_hi(w2[i])) + bf16_hi(w3[i]);
-                        }
-                    }
-                    if (!frz) store_split8(src, S_PIECE, v + 8 * g);
-                }
-                if (kAbl && a.ckpt && ck_ok && c + 1 < nlines) {  // boundary state of the next chunk
-                    float4 *d4 = reinterpret_cast<float4 *>(a.ckpt + (size_t)blockIdx.x * a.ckpt_stride +
-                                                            (size_t)(c + 1) * SZ + (size_t)tid * D);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        d4[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
-                }
-                if (c == nlines - 1 && a.mem_out && mo_ok) {
-                    float *mo = a.mem_out + (((size_t)b * 4 + r) * a.nh + h) * SZ;
-                    float4 *d4 = reinterpret_cast<float4 *>(mo + (size_t)tid * D);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        d4[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
-                }
+                chunk_end(c);
             }
             fence_async_smem();
             tc_before();
             __syncthreads();  // end of sub-tile: operands rewritten, TMEM consumed
         }
     }
+
+    }  // pipelined or sequential sub-tiles
 
     if (a.mem_out && mo_ok && tid < 2 * D) {
         float *mo = a.mem_out + (((size_t)b * 4 + r) * a.nh + h) * SZ;
@@ -1496,6 +1618,10 @@ cudaError_t launch_scan_tc(const ScanArgs &a, int d, bool bf16, cudaStream_t st,
     const bool wy_ok = !abl && !a.qhat && a.H <= tc::TT && a.W <= tc::TT;
     if (gain == VH_IMPL_TC_WY && !wy_ok) return cudaErrorNotSupported;
     const bool wy = wy_ok && gain == VH_IMPL_TC_WY;
+    // the pipelined sub-tiles where a line spans several of them, as long as the grid fits
+    // the two CTAs per SM its shared memory allows (else the sequential form's three)
+    const bool pipe_ok = !abl && !a.qhat;
+    if (gain == VH_IMPL_TC_PIPE && !pipe_ok) return cudaErrorNotSupported;
     CUtensorMap mr, mc, qr, qc;
     if (!tc::make_map(&mr, a.x, a.B, a.H, a.W, a.Cc, true) ||
         !tc::make_map(&mc, a.x, a.B, a.H, a.W, a.Cc, false))
@@ -1522,14 +1648,26 @@ cudaError_t launch_scan_tc(const ScanArgs &a, int d, bool bf16, cudaStream_t st,
         e = cudaFuncSetAttribute(tc::scan_tc_kernel<false, true>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, tc::Lay<true>::BYTES);
         if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(tc::scan_tc_kernel<false, false, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, tc::SMEM_PIPE);
+        if (e != cudaSuccess) return e;
         attr_set[dev] = 1;
     }
     const unsigned grid = (unsigned)(a.B * a.ndirs * a.nh);
+    bool pipe = gain == VH_IMPL_TC_PIPE;
+    if (pipe_ok && (gain == VH_IMPL_AUTO || gain == VH_IMPL_TC) && (a.H > tc::TT || a.W > tc::TT)) {
+        int nsm = 0;
+        e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        pipe = grid <= 2u * (unsigned)nsm;
+    }
     if (abl) {
         const int smem = (a.control_flags & VH_CTRL_INTRA_READ) ? tc::SMEM_INTRA : tc::SMEM_BYTES;
         tc::scan_tc_kernel<true, false><<<grid, tc::NT, smem, st>>>(a, mr, mc, qr, qc);
     } else if (wy) {
         tc::scan_tc_kernel<false, true><<<grid, tc::NT, tc::Lay<true>::BYTES, st>>>(a, mr, mc, qr, qc);
+    } else if (pipe) {
+        tc::scan_tc_kernel<false, false, true><<<grid, tc::NT, tc::SMEM_PIPE, st>>>(a, mr, mc, qr, qc);
     } else {
         tc::scan_tc_kernel<false, false><<<grid, tc::NT, tc::SMEM_BYTES, st>>>(a, mr, mc, qr, qc);
     }

@@ -1057,7 +1057,7 @@ cudaError_t launch_scan_tc64(const ScanArgs &a, int d, bool bf16, cudaStream_t s
     const unsigned grid = (unsigned)(a.B * a.ndirs * a.nh);
     // the WY form where every chunk fits one sub-tile (both orientations), else the recurrence
     const bool wy_ok = a.H <= tc64::TT && a.W <= tc64::TT;
-    if (gain == VH_IMPL_TC_WY && !wy_ok) return cudaErrorNotSupported;
+    if ((gain == VH_IMPL_TC_WY && !wy_ok) || gain == VH_IMPL_TC_PIPE) return cudaErrorNotSupported;
     if (wy_ok && gain != VH_IMPL_TC_RECUR)
         tc64::scan_tc64_kernel<true><<<grid, tc64::NT, tc64::SMEM_BYTES, st>>>(a, mr, mc);
     else
