@@ -369,11 +369,10 @@ size_t vh_block_workspace_size(const vh_params *p, const vh_block_weights *w, in
  * loads the library holds it until the process exits), so B*H*W*channels may be at most
  * 2,796,202 (6 bytes per element); larger calls return VH_ERR_WORKSPACE.  p->workspace
  * and p->workspace_bytes are ignored; everything else is as in vh_scan_forward, whose
- * kernels run.  The first call on a device looks up the array's device address there
- * (make that first call before any stream capture) and keeps it for the life of the
- * process: cudaDeviceReset, or anything else that destroys and recreates the device's
- * primary context, can move the array, so do not call this entry point again on a device
- * after resetting it in the same process.  Every call uses the same array and
+ * kernels run.  Every call looks up the array's device address in the current context (so
+ * a device reset that moves the array is harmless); the first call on a device also loads
+ * the library's device code there, so make it before any stream capture.  Every call
+ * uses the same array and
  * rewrites it completely before reading it, so nothing needs clearing, but two calls
  * that overlap on the GPU (different streams, or another thread) race on it and corrupt
  * each other's queries: serialise them.  Without w_query it returns VH_ERR_INVALID_ARG

@@ -8,8 +8,6 @@
 // vh_scan_forward takes from the caller's workspace.  This entry point takes it from a
 // fixed array compiled into the library instead, and otherwise runs the same kernels
 // through vh_scan_forward.
-#include <mutex>
-
 #include "vh_common.cuh"
 
 namespace vh {
@@ -23,27 +21,12 @@ namespace {
 constexpr size_t kStaticScratchBytes = 16u << 20;
 static __device__ __align__(256) unsigned char g_qscratch[kStaticScratchBytes];
 
-std::mutex g_mu;
-void *g_scratch_ptr[64] = {};
-
-// The array's device address on the current device, looked up on the first call there and
-// kept for the process (a device reset that recreates the primary context can move the
-// array; the header tells callers not to use this entry point after one).
+// The array's device address in the current context, looked up on every call (a device
+// reset that recreates the primary context can move the array, so nothing is cached).
 cudaError_t scratch_address(void **ptr)
 {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lk(g_mu);
-    if (!g_scratch_ptr[dev]) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_qscratch);
-        if (e != cudaSuccess) return e;
-        g_scratch_ptr[dev] = p;
-    }
-    *ptr = g_scratch_ptr[dev];
-    return cudaSuccess;
+    *ptr = nullptr;
+    return cudaGetSymbolAddress(ptr, g_qscratch);
 }
 
 }  // namespace
