@@ -585,10 +585,14 @@ def run_ours(args, wl):
         flops, nbytes = algorithmic_cost(wl)
         if args.memories_out:
             nbytes += wl.B * 4 * wl.nh * (4 * wl.d * wl.d + 2 * wl.d) * 4
+        if args.readout == "outer":
+            nbytes += wl.tokens * wl.Cc * 6  # the scan reads the outer queries' three bf16 pieces
         peaks, src = load_peaks()
         achieved = flops / kern_avg_s / 1e12
         peak = float(peaks["bf16_tflops"])
-        traffic = recorded_traffic(wl.name, args.kernel, forward_sources(wl, args.kernel))
+        # (traffic.txt keys the outer-query readout's scan apart: it also reads the queries)
+        traffic = recorded_traffic(wl.name, args.kernel + ("+outer" if args.readout == "outer" else ""),
+                                   forward_sources(wl, args.kernel))
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": traffic,
                 "peak_source": f"bf16 dense burst, {'of measured' if src == 'measured' else 'of fallback'}",
