@@ -143,3 +143,33 @@ def test_pipe_rejects_other_methods(vhlib):
     wq = torch.randn(wl.Cc, wl.Cc).cuda()
     with pytest.raises(vhlib.VhError, match="pipelined"):
         vhlib.scan_forward(x, m, 32, w_query=wq, params=vhlib.ScanParams(impl="tc_pipe"))
+
+
+def test_pipe_accumulates_onto_out(vhlib):
+    """accumulate=True adds the readouts onto the caller's out, as the sequential form."""
+    import torch
+    from tests._helpers import to_device_x
+    wl = synth.Workload("pacc", 1, 6, 100, 1, 32, 0, "bf16", seed=45, alpha_init=0.999)
+    inp = synth.make_inputs(wl)
+    x = to_device_x(inp)
+    m = torch.from_numpy(inp.mem0).cuda()
+    base = torch.randn(1, wl.H, wl.W, wl.Cc, device="cuda")
+    p = vhlib.ScanParams(alpha_init=wl.alpha_init, impl="tc_pipe")
+    ref = vhlib.scan_forward(x, m, 32, dirs=3, params=p)
+    out = base.clone()
+    vhlib.scan_forward(x, m, 32, dirs=3, out=out, accumulate=True, params=p)
+    torch.cuda.synchronize()
+    torch.testing.assert_close(out, base + ref, rtol=1e-5, atol=1e-5)
+
+
+def test_pipe_square_map_with_explicit_chunk(orc, vhlib):
+    """A square map with chunk = H = W given explicitly (rows and columns of 96 tokens, two
+    sub-tiles each) runs the aligned pipelined form."""
+    wl = synth.Workload("psq", 1, 96, 96, 1, 32, 96, "bf16", seed=46, alpha_init=0.999)
+    inp = synth.make_inputs(wl)
+    p = vhlib.ScanParams(alpha_init=wl.alpha_init, impl="tc_pipe")
+    g = run_gpu(vhlib, inp, params=p, chunk=96, want_memories=True, want_stats=True, impl="tc_pipe")
+    assert g["stats"][4] == 0
+    o, om = orc.forward(inp.x64, inp.mem0, wl.H, wl.W, wl.nh, wl.d, chunk_len=96,
+                        params=oracle_params_like(orc, p), want_memories=True, nthreads=8)
+    assert parity_err(g["out"], o) < TOL and parity_err(g["mem"], om) < TOL
